@@ -1,0 +1,235 @@
+"""Pins for the CPU oracle's AsymSpec path, each against something other than the
+oracle itself: library routines (scipy logsumexp / softmax / entropy /
+jensenshannon, numpy argmax), closed forms derived by hand (tests/golden),
+the bounds and reductions stated in "AsymSpec: Context-Asymmetric Speculative
+Decoding for Agentic LLMs" (reading notes) sec. 4.1-4.2, and brute force over
+every draft id at small V in the probability domain."""
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special as sps
+from scipy.spatial.distance import jensenshannon
+from scipy.stats import entropy
+
+import gen
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(rng, n, V, dtype, scale=2.0):
+    x = rng.standard_normal((n, V)) * scale
+    return gen.store(x, dtype)
+
+
+def _w(x, dtype):
+    return gen.widen(x, dtype).astype(np.float64)
+
+
+@pytest.mark.parametrize("dtype", [gen.F32, gen.BF16])
+def test_lse_matches_scipy(dtype):
+    rng = np.random.default_rng(1)
+    for V in (1, 2, 7, 16, 1000, 32000):
+        x = _rows(rng, 1, V, dtype, 3.0)[0]
+        assert oracle.lse(x) == pytest.approx(sps.logsumexp(_w(x, dtype)), rel=1e-13, abs=1e-13)
+
+
+def test_lse_special_cases():
+    x = np.array([-np.inf, -np.inf], np.float32)
+    assert oracle.lse(x) == -np.inf
+    assert oracle.lse(np.array([3.25], np.float32)) == 3.25
+    # shift invariance with exactly representable shifts
+    rng = np.random.default_rng(2)
+    x = np.round(rng.standard_normal(257) * 64) / 64
+    x32 = x.astype(np.float32)
+    assert oracle.lse(x32 + np.float32(5.0)) == pytest.approx(oracle.lse(x32) + 5.0, abs=1e-12)
+    # temperature scale: lse(x / T)
+    assert oracle.lse(x32, 0.5) == pytest.approx(sps.logsumexp(x32.astype(np.float64) / 2.0), abs=1e-12)
+
+
+def _golden_jsd():
+    out = []
+    for line in open(os.path.join(GOLDEN, "jsd_closed_forms.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        name, a, b, v = [s.strip() for s in line.split("|")]
+        out.append((name, np.array([float(s) for s in a.split()], np.float32),
+                    np.array([float(s) for s in b.split()], np.float32), float(v)))
+    return out
+
+
+@pytest.mark.parametrize("case", _golden_jsd(), ids=lambda c: c[0])
+def test_jsd_closed_forms(case):
+    _, a, b, v = case
+    assert oracle.jsd(a, b) == pytest.approx(v, abs=1e-15)
+
+
+@pytest.mark.parametrize("dtype", [gen.F32, gen.BF16])
+def test_jsd_matches_library(dtype):
+    rng = np.random.default_rng(3)
+    for V in (2, 3, 16, 257, 5000):
+        a = _rows(rng, 1, V, dtype)[0]
+        b = _rows(rng, 1, V, dtype)[0]
+        p = sps.softmax(_w(a, dtype))
+        q = sps.softmax(_w(b, dtype))
+        ref = jensenshannon(p, q) ** 2            # natural log by default
+        ref2 = entropy(0.5 * (p + q)) - 0.5 * (entropy(p) + entropy(q))
+        D = oracle.jsd(a, b)
+        assert D == pytest.approx(ref, rel=1e-9, abs=1e-14)
+        assert D == pytest.approx(ref2, rel=1e-9, abs=1e-14)
+
+
+def test_jsd_bounds_identity_and_disjoint():
+    rng = np.random.default_rng(4)
+    for _ in range(50):
+        V = int(rng.integers(2, 64))
+        a = _rows(rng, 1, V, gen.F32, float(rng.uniform(0.1, 20)))[0]
+        b = _rows(rng, 1, V, gen.F32, float(rng.uniform(0.1, 20)))[0]
+        D = oracle.jsd(a, b)
+        assert -1e-15 <= D <= math.log(2) + 1e-15
+        assert oracle.jsd(a, a) == 0.0                       # a == b gives exactly 0
+    # one-hot spikes far apart approach ln 2
+    a = np.zeros(32, np.float32); a[3] = 60
+    b = np.zeros(32, np.float32); b[17] = 60
+    assert abs(oracle.jsd(a, b) - math.log(2)) < 1e-12
+    # symmetry
+    x, y = _rows(rng, 2, 100, gen.BF16)
+    assert oracle.jsd(x, y) == pytest.approx(oracle.jsd(y, x), rel=1e-14)
+
+
+@pytest.mark.parametrize("dtype", [gen.F32, gen.BF16])
+def test_fused_argmax_matches_numpy(dtype):
+    rng = np.random.default_rng(5)
+    for beta in (0.0, 1.0, 1.5, -0.75):
+        for V in (1, 2, 9, 16, 4097):
+            a, b, t = _rows(rng, 3, V, dtype)
+            af, bf, tf = (gen.widen(x, dtype) for x in (a, b, t))
+            d = (af - bf).astype(np.float32)                       # one rounding
+            s = (np.float64(np.float32(beta)) * d.astype(np.float64) + tf.astype(np.float64)).astype(np.float32)
+            assert oracle.fused_argmax(a, b, t, beta) == int(np.argmax(s))
+
+
+def test_fused_argmax_ties_and_nan():
+    t = np.array([1, 5, 5, 2, 5], np.float32)
+    z = np.zeros(5, np.float32)
+    assert oracle.fused_argmax(z, z, t, 1.0) == 1                  # lowest index among ties
+    t2 = np.array([np.nan, 1, 3, np.nan, 3], np.float32)
+    assert oracle.fused_argmax(z, z, t2, 0.0) == 2                 # NaN never wins
+    ninf = np.full(4, -np.inf, np.float32)
+    assert oracle.fused_argmax(z[:4], z[:4], ninf, 0.0) == 0       # all -inf: index 0
+    # beta = 0 reduces to argmax t
+    rng = np.random.default_rng(6)
+    a, b, t = _rows(rng, 3, 1000, gen.BF16)
+    assert oracle.fused_argmax(a, b, t, 0.0) == int(np.argmax(gen.widen(t, gen.BF16)))
+
+
+# ------------------------------------------------------------------ brute force
+
+def _brute_request(a, b, t, drafts, beta, gamma, dtype):
+    """Probability-domain restatement: accept iff p_t[d] > gamma * exp(-D) * p_b[d].
+    beta and gamma cross the boundary as fp32, so they are rounded the same way here."""
+    gamma = float(np.float32(gamma))
+    K = len(drafts)
+    n = K
+    margins = []
+    for i in range(K):
+        aw, bw, tw = _w(a[i], dtype), _w(b[i], dtype), _w(t[i], dtype)
+        pa, pb, pt = sps.softmax(aw), sps.softmax(bw), sps.softmax(tw)
+        D = jensenshannon(pa, pb) ** 2
+        lhs, rhs = pt[drafts[i]], gamma * math.exp(-D) * pb[drafts[i]]
+        margins.append(math.log(lhs) - math.log(rhs) if lhs > 0 and rhs > 0 else np.inf)
+        if not lhs > rhs:
+            n = i
+            break
+    af, bf, tf = (gen.widen(x[n], dtype) for x in (a, b, t))
+    s = (np.float64(np.float32(beta)) * (af - bf).astype(np.float32).astype(np.float64)
+         + tf.astype(np.float64)).astype(np.float32)
+    tokens = [int(x) for x in drafts[:n]] + [int(np.argmax(s))] + [-1] * (K - n)
+    return n, tokens, margins
+
+
+@pytest.mark.parametrize("dtype", [gen.F32, gen.BF16])
+def test_verify_brute_force_every_draft(dtype):
+    """Every draft id d in [0, V) at the first position, V <= 16, several (beta, gamma)."""
+    rng = np.random.default_rng(7)
+    checked = flagged = 0
+    for trial in range(12):
+        V = int(rng.integers(2, 17))
+        K = int(rng.integers(1, 4))
+        a = _rows(rng, K + 1, V, dtype, 1.5)
+        b = gen.store(_w(a, dtype) + rng.standard_normal(a.shape) * rng.uniform(0, 1.5), dtype)
+        t = gen.store(_w(b, dtype) + rng.standard_normal(a.shape), dtype)
+        beta, gamma = [(1.0, 0.5), (0.0, 1.0), (2.0, 0.4), (1.5, 0.7)][trial % 4]
+        for d0 in range(V):
+            drafts = rng.integers(0, V, size=K).astype(np.int32)
+            drafts[0] = d0
+            res = oracle.asymspec_verify(a[None], b[None], t[None], drafts[None], beta, gamma)
+            n, tokens, margins = _brute_request(a, b, t, drafts, beta, gamma, dtype)
+            if res.flags[0] & oracle.FLAG_NEAR_MARGIN:
+                flagged += 1
+                continue
+            checked += 1
+            assert res.accept_len[0] == n
+            assert list(res.tokens[0]) == tokens
+            for i, m in enumerate(margins):
+                if np.isfinite(m):
+                    assert res.margin[0, i] == pytest.approx(m, abs=1e-9)
+    assert checked > 100 and flagged < checked / 10
+
+
+def test_gamma_eff_bounds_and_degenerate_run():
+    """gamma_eff = gamma * exp(-D) lies in [gamma/2, gamma]; with beta = 0 the emitted
+    token is argmax t; with a == b, D = 0 and the gate is p_t(d) > gamma * p_b(d)."""
+    rng = np.random.default_rng(8)
+    batch = gen.make_asymspec_batch("spiky", 99, 24, 3, 600, gen.F32, identical_frac=0.3)
+    for beta, gamma in [(1.0, 0.5), (0.0, 1.0)]:
+        res = oracle.asymspec_verify(batch.a, batch.b, batch.t, batch.drafts, beta, gamma)
+        geff = gamma * np.exp(-res.D)
+        assert np.all(geff >= gamma / 2 - 1e-15) and np.all(geff <= gamma + 1e-15)
+        for r in range(batch.B):
+            n = res.accept_len[r]
+            tok = res.tokens[r, n]
+            if beta == 0.0 or batch.identical[r]:
+                assert tok == int(np.argmax(gen.widen(batch.t[r, n], gen.F32)))
+            if batch.identical[r]:
+                assert np.all(res.D[r] == 0.0)
+                for i in range(n + (1 if n < 3 else 0)):
+                    if i >= 3:
+                        break
+                    d = batch.drafts[r, i]
+                    lt = res.lse[r, i, 2]; lb = res.lse[r, i, 1]
+                    pt = math.exp(float(gen.widen(batch.t[r, i], gen.F32)[d]) - lt)
+                    pb = math.exp(float(gen.widen(batch.b[r, i], gen.F32)[d]) - lb)
+                    assert (pt > gamma * pb) == (i < n)
+    # the accept lengths differ between the two runs on at least one request
+    r1 = oracle.asymspec_verify(batch.a, batch.b, batch.t, batch.drafts, 1.0, 0.5)
+    r0 = oracle.asymspec_verify(batch.a, batch.b, batch.t, batch.drafts, 0.0, 1.0)
+    assert np.any(r1.accept_len != r0.accept_len) or np.any(r1.tokens != r0.tokens)
+
+
+def test_flags_nonfinite_and_bad_draft():
+    rng = np.random.default_rng(9)
+    a, b, t = (_rows(rng, 3, 20, gen.F32).reshape(1, 3, 20) for _ in range(3))
+    d = np.array([[1, 2]], np.int32)
+    a2 = a.copy(); a2[0, 1, 5] = np.nan
+    r = oracle.asymspec_verify(a2, b, t, d, 1.0, 0.5)
+    assert r.flags[0] & oracle.FLAG_NONFINITE and r.accept_len[0] == 0 and np.all(r.tokens == -1)
+    t2 = t.copy(); t2[0, 2, 0] = np.inf
+    assert oracle.asymspec_verify(a, b, t2, d, 1.0, 0.5).flags[0] & oracle.FLAG_NONFINITE
+    b2 = b.copy(); b2[0, 0, 3] = -np.inf                      # -inf is a legal logit
+    assert not oracle.asymspec_verify(a, b2, t, d, 1.0, 0.5).flags[0] & oracle.FLAG_NONFINITE
+    r = oracle.asymspec_verify(a, b, t, np.array([[1, 20]], np.int32), 1.0, 0.5)
+    assert r.flags[0] & oracle.FLAG_BAD_DRAFT and np.all(r.tokens == -1)
+
+
+def test_gate_is_strict():
+    """With t == b and gamma = 1 both sides of the printed inequality are equal
+    (D = 0 when a == b), so the strict test rejects the first draft."""
+    rng = np.random.default_rng(10)
+    a = _rows(rng, 3, 50, gen.BF16).reshape(1, 3, 50)
+    d = np.array([[4, 9]], np.int32)
+    r = oracle.asymspec_verify(a, a, a, d, 1.0, 1.0)
+    assert r.margin[0, 0] == 0.0 and r.accept_len[0] == 0
+    assert r.flags[0] & oracle.FLAG_NEAR_MARGIN
