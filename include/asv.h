@@ -1,0 +1,199 @@
+/*
+ * asv.h -- C ABI of the GB300 logit-space speculative verification library (libasv).
+ *
+ * One shared library with plain C entry points over caller-owned device
+ * buffers.  It covers the verification step of three speculative-decoding
+ * methods described on these pages:
+ *
+ *   [ASYM]  "AsymSpec: Context-Asymmetric Speculative Decoding for Agentic LLMs"
+ *           (reading notes), sec. 4.1 (contrastive delta-fusion) and sec. 4.2
+ *           (context-divergence-aware acceptance, the CDA gate).
+ *   [RAPID] "RAPID: Long-Context Inference with Retrieval-Augmented Speculative
+ *           Decoding" (paper notes), Key designs 2-4 (retrieval-augmented target,
+ *           tail protection, adjusted residual sampling).
+ *   [SCI]   "E2-SCI: Elastic Edge-Cloud Speculative Decoding via Credit Inertia"
+ *           (paper notes), Key design 3 (JSD test against an adaptive threshold
+ *           driven by an EWMA of the acceptance rate).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Logit tensors are row-major [B, K+1, V]: request b, position i (K draft
+ *    positions plus the bonus position K), vocabulary entry k; a row is V
+ *    contiguous elements, element type fp32 or bf16 (ASV_F32 / ASV_BF16).
+ *  - Every pointer argument is a DEVICE pointer owned by the caller unless the
+ *    name ends in _host.  The library never allocates, frees or retains memory.
+ *  - Calls are asynchronous on `stream`; nothing waits for the GPU.  The return
+ *    value reports argument validation and launch failures only.  Conditions
+ *    that depend on the data are written per request to out_req_status
+ *    (ASV_REQ_* bits); a flagged request gets accept length 0 and tokens -1.
+ *  - Output tokens per request: the accepted drafts, then one token chosen by the
+ *    verifier at the first rejection (or at the bonus position), then -1 padding.
+ *  - Rows are processed by thread-block clusters; rows whose base address is
+ *    16-byte aligned (V * element size a multiple of 16 and 16-byte aligned base
+ *    pointers) are staged with bulk copies, others with ordinary loads.
+ *  - `workspace` is device scratch of at least asv_workspace_bytes(...) bytes.
+ *    It must be zero-filled before its first use (asv_workspace_init does that);
+ *    every call leaves it zero-filled again.  Two calls that may run at the
+ *    same time must not share a workspace.
+ *  - Thread safety: the entry points keep no host state except the tuning
+ *    override and a per-device cache of launch attributes.
+ */
+#ifndef ASV_H_
+#define ASV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ASV_OK = 0,
+  ASV_ERR_NULL = 1,      /* a required pointer is NULL */
+  ASV_ERR_SHAPE = 2,     /* B < 0, K < 0 (K < 1 for SCI), V < 2, or V too large for one cluster */
+  ASV_ERR_ALIGN = 3,     /* a pointer is not aligned to its element size */
+  ASV_ERR_DTYPE = 4,     /* unknown element type, or a type the mode does not take */
+  ASV_ERR_PARAM = 5,     /* a scalar parameter is non-finite or out of range */
+  ASV_ERR_WORKSPACE = 6, /* workspace NULL or smaller than asv_workspace_bytes() */
+  ASV_ERR_CUDA = 7       /* a CUDA runtime call or the launch failed (see asv_last_cuda_error) */
+} asv_status;
+
+typedef enum { ASV_F32 = 0, ASV_BF16 = 1 } asv_dtype;
+
+typedef enum { ASV_MODE_ASYMSPEC = 0, ASV_MODE_RAPID = 1, ASV_MODE_SCI = 2 } asv_mode;
+
+/* Per-request status bits written by the kernels (never a trap). */
+#define ASV_REQ_NONFINITE 1u /* a row holds NaN or +inf, or is entirely -inf */
+#define ASV_REQ_BAD_DRAFT 2u /* a draft id lies outside [0, V) */
+#define ASV_REQ_TIMEOUT 4u   /* a bounded wait for staged data expired; outputs invalid */
+
+/* Human-readable name of a status code (static string). */
+const char* asv_status_string(asv_status s);
+
+/* cudaError_t value of the most recent ASV_ERR_CUDA on the calling thread (0 if none). */
+int asv_last_cuda_error(void);
+
+/* Bytes of device workspace one call of `mode` needs for a [B, K+1, V] batch. */
+size_t asv_workspace_bytes(int mode, int B, int K, int V, int dtype);
+
+/* Zero-fill `ws_bytes` bytes of workspace on `stream` (cudaMemsetAsync). */
+asv_status asv_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Tuning override for the launch plan: cluster size (CTAs per row, 1..16) and
+ * threads per CTA (128..1024, multiple of 32).  0 restores the automatic choice.
+ * Applies to later calls from any thread.
+ */
+asv_status asv_set_tuning(int cluster_ctas, int threads_per_cta);
+
+/* The plan the next call with these shapes would use (cluster size, threads, dynamic
+ * shared memory bytes, 1 if rows are staged with bulk copies).  Any output may be NULL. */
+asv_status asv_query_plan(int mode, int B, int K, int V, int dtype, int* cluster_ctas, int* threads_per_cta,
+                          int* smem_bytes, int* bulk_copy);
+
+/*
+ * asymspec_verify -- the AsymSpec verification step.  [ASYM] sec. 4.1-4.2.
+ *
+ * Inputs, each [B, K+1, V] of element type `dtype`:
+ *   a  drafter logits on the full context, b  drafter logits on the compressed
+ *   context, t  verifier logits on the compressed context.
+ *   draft_ids [B, K] int32: the drafted token at each of the K positions.
+ * Per row i:  D_i = JSD(softmax a_i || softmax b_i) (natural log, weights 1/2);
+ *   c_i = argmax_k (t_ik + beta * (a_ik - b_ik)), the fp32 score formed as one
+ *   rounded subtraction and one fused multiply-add, lowest index on ties.
+ * Draft i < K is accepted iff softmax(t_i)[d_i] > gamma * exp(-D_i) * softmax(b_i)[d_i]
+ * (strict; decided in double in the log domain).  The scan stops at the first
+ * rejection n (n = K if none); the request emits d_0..d_{n-1}, then c_n.
+ *
+ * beta: any finite value.  gamma: finite, > 0.
+ * Outputs: out_accept_len [B] int32; out_tokens [B, K+1] int32 (-1 padded);
+ *   out_D [B, K+1] float (clamped to [0, ln 2], may be NULL);
+ *   out_lse [B, K+1, 3] float, log-sum-exp of a, b, t (may be NULL);
+ *   out_req_status [B] uint32 ASV_REQ_* bits.
+ * B = 0 is a no-op that returns ASV_OK.
+ */
+asv_status asymspec_verify(const void* a, const void* b, const void* t, int dtype, const int32_t* draft_ids, int B,
+                           int K, int V, float beta, float gamma, int32_t* out_accept_len, int32_t* out_tokens,
+                           float* out_D, float* out_lse, uint32_t* out_req_status, void* workspace,
+                           size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * asymspec_verify_host -- asymspec_verify over HOST buffers, for callers whose
+ * logits live in host memory.  Copies a, b, t and draft_ids to the device arena,
+ * runs the verification, and copies accept lengths, tokens, D and request status
+ * back, all on `stream` (the call returns before the copies finish; synchronise
+ * the stream before reading the outputs).  Host buffers should be pinned.
+ * `arena` is caller-owned device memory of at least asv_host_arena_bytes(...)
+ * bytes, zero-filled before its first use; it holds the staged inputs, the
+ * outputs and the workspace.  out_D_host may be NULL.
+ */
+size_t asv_host_arena_bytes(int B, int K, int V, int dtype);
+asv_status asymspec_verify_host(const void* a_host, const void* b_host, const void* t_host, int dtype,
+                                const int32_t* draft_ids_host, int B, int K, int V, float beta, float gamma,
+                                int32_t* out_accept_len_host, int32_t* out_tokens_host, float* out_D_host,
+                                uint32_t* out_req_status_host, void* arena, size_t arena_bytes,
+                                cudaStream_t stream);
+
+/*
+ * rapid_verify -- RAPID verification with the retrieval-augmented target.
+ * [RAPID] Workflow; Key designs 2 (augmented target), 3 (tail protection),
+ * 4 (adjusted residual sampling).
+ *
+ * Inputs (fp32, [B, G+1, V]): z  target logits; q  drafter probabilities.
+ *   draft_ids [B, G] int32.
+ * Per row: p = softmax(z/T); zhat = z + eta*T*(q - p); phat = softmax(zhat/T);
+ *   tail = {k : phat_k < tail_frac * max phat};  protected target p' keeps p on
+ *   the tail and rescales phat on the rest so that p' sums to 1.
+ * Draft i is accepted iff u_i * q_i(d_i) < p'_i(d_i) with u_i a Philox4x32-10
+ * uniform; at the first rejection n the token is drawn from
+ * norm(max(p_n - p'_n, p_n - q_n, 0)) (from p_n if that is all zero); if all G
+ * drafts pass, the bonus token is drawn from p'_G.  Draws use an exponential
+ * race over Philox uniforms.
+ * Random numbers: key = (seed low 32 bits, seed high 32 bits); counter =
+ * (word / 4, position i, request b, stream + 4*offset); the uniform is
+ * ((word32 >> 9) + 0.5) * 2^-23 from word (word % 4) of the block; streams are
+ * 0 = accept test (word 0), 1 = residual draw (word k), 2 = bonus draw (word k).
+ * T > 0, eta >= 0, 0 <= tail_frac < 1, all finite.
+ * Outputs: out_accept_len [B], out_tokens [B, G+1], out_req_status [B].
+ */
+asv_status rapid_verify(const float* z, const float* q, const int32_t* draft_ids, int B, int G, int V, float T,
+                        float eta, float tail_frac, uint64_t seed, uint32_t offset, int32_t* out_accept_len,
+                        int32_t* out_tokens, uint32_t* out_req_status, void* workspace, size_t ws_bytes,
+                        cudaStream_t stream);
+
+/* E2-SCI threshold and credit parameters.  [SCI] Key design 3. */
+typedef struct {
+  double T_base;      /* base threshold */
+  double alpha_omega; /* alpha * omega, the credit gain */
+  double tau_credit;  /* neutral credit level */
+  double T_min;       /* lower clamp */
+  double T_max;       /* upper clamp */
+  double ewma_beta;   /* EWMA weight of the newest window (0.3) */
+} asv_sci_params;
+
+/*
+ * sci_verify -- one E2-SCI verification window per request.  [SCI] Key design 3.
+ *
+ * Inputs, [B, K+1, V] of `dtype`: draft logits and target logits; draft_ids [B, K].
+ * r_hat [B] double: the credit state, read and updated in place.
+ * Per request: T = clamp(T_base + alpha_omega*(r_hat - tau_credit), T_min, T_max);
+ *   J_i = JSD(softmax draft_i || softmax target_i); drafts are accepted while
+ *   J_i <= T; n = the accepted prefix; tokens = d_0..d_{n-1}, argmax(target_n);
+ *   r_hat <- (1 - ewma_beta)*r_hat + ewma_beta*(n/K).  A flagged request leaves
+ *   r_hat unchanged.  K >= 1.
+ * Outputs: out_accept_len [B], out_tokens [B, K+1], out_jsd [B, K+1] float (may be
+ *   NULL), out_T [B] float (may be NULL), out_req_status [B].
+ */
+asv_status sci_verify(const void* draft_logits, const void* target_logits, int dtype, const int32_t* draft_ids,
+                      int B, int K, int V, const asv_sci_params* params, double* r_hat, int32_t* out_accept_len,
+                      int32_t* out_tokens, float* out_jsd, float* out_T, uint32_t* out_req_status,
+                      void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ASV_H_ */

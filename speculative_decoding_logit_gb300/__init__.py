@@ -1,0 +1,45 @@
+"""GB300-native logit-space verification for speculative decoding.
+
+Thin Python binding over the C ABI in ``include/asv.h`` (``libasv.so``, built
+in-tree by :func:`build`).  Every step of the verification runs in the
+library's CUDA kernels; this module only checks tensor shapes, allocates the
+outputs with PyTorch and passes raw device pointers and the current CUDA
+stream.  There is no CPU fallback: on a machine without the library or
+without a CUDA device the calls raise.
+
+Entry points (same names as the C ABI):
+  asymspec_verify  AsymSpec CDA gate + delta-fusion ("AsymSpec: Context-Asymmetric
+                   Speculative Decoding for Agentic LLMs", sec. 4.1-4.2)
+  rapid_verify     RAPID retrieval-augmented target verification ("RAPID: Long-Context
+                   Inference with Retrieval-Augmented Speculative Decoding", Key designs 2-4)
+  sci_verify       E2-SCI JSD test against an adaptive threshold ("E2-SCI: Elastic
+                   Edge-Cloud Speculative Decoding via Credit Inertia", Key design 3)
+"""
+from __future__ import annotations
+
+from ._binding import (  # noqa: F401
+    ASV_BF16,
+    ASV_F32,
+    ASV_MODE_ASYMSPEC,
+    ASV_MODE_RAPID,
+    ASV_MODE_SCI,
+    REQ_BAD_DRAFT,
+    REQ_NONFINITE,
+    REQ_TIMEOUT,
+    AsvError,
+    AsymSpecOutput,
+    RapidOutput,
+    SciOutput,
+    SciParams,
+    asymspec_verify,
+    asymspec_verify_host,
+    host_arena_bytes,
+    library,
+    library_path,
+    query_plan,
+    rapid_verify,
+    sci_verify,
+    set_tuning,
+    workspace_bytes,
+)
+from .build import build  # noqa: F401

@@ -1,0 +1,399 @@
+// asv_api.cu -- the extern "C" entry points declared in include/asv.h: argument validation,
+// workspace layout, launch planning (cluster size, threads, shared memory) and dispatch.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "asv.h"
+#include "asv_internal.h"
+
+using asv::LaunchPlan;
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+std::atomic<int> g_tune_cluster{0};
+std::atomic<int> g_tune_threads{0};
+
+asv_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = int(e);
+  return ASV_ERR_CUDA;
+}
+
+struct DevInfo {
+  int sms = 0;
+  int smem_block_optin = 0;
+  int smem_sm = 0;
+};
+
+constexpr int kMaxDevices = 64;
+DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+cudaError_t dev_info(DevInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (d.sms == 0) {
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&d.smem_block_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+      return e;
+    if ((e = cudaDeviceGetAttribute(&d.smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess)
+      return e;
+  }
+  *out = d;
+  return cudaSuccess;
+}
+
+inline size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Workspace layout: [tickets: B x u32, padded to 256 B][records: R x record].
+size_t tickets_bytes(int B) { return round_up(size_t(B) * 4, 256); }
+
+size_t record_bytes(int mode) {
+  return mode == ASV_MODE_RAPID ? sizeof(asv::RapidRecord) : sizeof(asv::RowRecord);
+}
+
+// Launch plan.  Each CTA stages NT slices of n_slice entries.  Choose the smallest cluster
+// size whose staging lets two CTAs share an SM (so one CTA's copies overlap another's
+// arithmetic), then widen it while the batch has fewer CTAs than twice the SM count.
+cudaError_t plan_for(int kind, int dtype, int NT, int elem_bytes, int V, long long R, bool bulk, int static_smem,
+                     LaunchPlan* out) {
+  DevInfo di;
+  cudaError_t e = dev_info(&di);
+  if (e != cudaSuccess) return e;
+  const int vec = 16 / elem_bytes;
+  const int reserve = 1024;  // per-CTA shared memory the system keeps
+  auto stage_bytes = [&](int C) {
+    const int n = int(round_up(size_t(ceil_div(V, C)), size_t(vec)));
+    return std::pair<int, int>(n, int(NT * round_up(size_t(n) * elem_bytes, 128)));
+  };
+  int C = g_tune_cluster.load();
+  if (C <= 0) {
+    int c_fit = 0, c_two = 0;
+    for (int c = 1; c <= asv::kMaxCluster; ++c) {
+      const int sb = stage_bytes(c).second + static_smem;
+      if (sb <= di.smem_block_optin && !c_fit) c_fit = c;
+      if (2 * (sb + reserve) <= di.smem_sm && !c_two) c_two = c;
+    }
+    C = c_two ? c_two : c_fit;
+    if (C == 0) return cudaErrorInvalidValue;  // V too large for one cluster
+    const long long want = 2LL * di.sms;
+    if (R * C < want) {
+      int c_more = int((want + R - 1) / R);
+      c_more = std::min(c_more, asv::kMaxCluster);
+      c_more = std::min(c_more, std::max(1, V / 1024));
+      C = std::max(C, c_more);
+    }
+  }
+  const auto sb = stage_bytes(C);
+  if (sb.second + static_smem > di.smem_block_optin) return cudaErrorInvalidValue;
+  int threads = g_tune_threads.load();
+  if (threads <= 0) {
+    const int nvec = sb.first / vec;
+    threads = nvec >= 2048 ? 512 : (nvec >= 512 ? 256 : 128);
+  }
+  out->cluster = C;
+  out->threads = threads;
+  out->n_slice = sb.first;
+  out->smem = sb.second;
+  out->bulk = bulk ? 1 : 0;
+  (void)kind;
+  (void)dtype;
+  return cudaSuccess;
+}
+
+bool valid_dtype(int dt) { return dt == ASV_F32 || dt == ASV_BF16; }
+int elem_size(int dt) { return dt == ASV_F32 ? 4 : 2; }
+
+}  // namespace
+
+extern "C" {
+
+const char* asv_status_string(asv_status s) {
+  switch (s) {
+    case ASV_OK: return "ASV_OK";
+    case ASV_ERR_NULL: return "ASV_ERR_NULL: a required pointer is NULL";
+    case ASV_ERR_SHAPE: return "ASV_ERR_SHAPE: invalid B, K or V";
+    case ASV_ERR_ALIGN: return "ASV_ERR_ALIGN: misaligned pointer";
+    case ASV_ERR_DTYPE: return "ASV_ERR_DTYPE: unsupported element type";
+    case ASV_ERR_PARAM: return "ASV_ERR_PARAM: scalar parameter out of range";
+    case ASV_ERR_WORKSPACE: return "ASV_ERR_WORKSPACE: workspace missing or too small";
+    case ASV_ERR_CUDA: return "ASV_ERR_CUDA: CUDA runtime error";
+  }
+  return "unknown asv_status";
+}
+
+int asv_last_cuda_error(void) { return g_last_cuda_error; }
+
+size_t asv_workspace_bytes(int mode, int B, int K, int V, int dtype) {
+  (void)V;
+  (void)dtype;
+  if (B < 0 || K < 0) return 0;
+  return tickets_bytes(B) + size_t(B) * size_t(K + 1) * record_bytes(mode);
+}
+
+asv_status asv_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (!workspace) return ASV_ERR_NULL;
+  cudaError_t e = cudaMemsetAsync(workspace, 0, ws_bytes, stream);
+  return e == cudaSuccess ? ASV_OK : cuda_fail(e);
+}
+
+asv_status asv_set_tuning(int cluster_ctas, int threads_per_cta) {
+  if (cluster_ctas < 0 || cluster_ctas > asv::kMaxCluster) return ASV_ERR_PARAM;
+  if (threads_per_cta != 0 && (threads_per_cta < 128 || threads_per_cta > 512 || threads_per_cta % 32))
+    return ASV_ERR_PARAM;
+  g_tune_cluster.store(cluster_ctas);
+  g_tune_threads.store(threads_per_cta);
+  return ASV_OK;
+}
+
+asv_status asv_query_plan(int mode, int B, int K, int V, int dtype, int* cluster_ctas, int* threads_per_cta,
+                          int* smem_bytes, int* bulk_copy) {
+  if (B < 1 || K < 0 || V < 2) return ASV_ERR_SHAPE;
+  if (!valid_dtype(dtype)) return ASV_ERR_DTYPE;
+  if (mode == ASV_MODE_RAPID && dtype != ASV_F32) return ASV_ERR_DTYPE;
+  const int eb = elem_size(dtype);
+  const bool bulk = (size_t(V) * eb) % 16 == 0;
+  LaunchPlan pl;
+  const int NT = mode == ASV_MODE_ASYMSPEC ? 3 : 2;
+  const int st = mode == ASV_MODE_RAPID ? asv::rapid_static_smem_bytes() : asv::jsd_static_smem_bytes();
+  cudaError_t e = plan_for(mode, dtype, NT, eb, V, (long long)B * (K + 1), bulk, st, &pl);
+  if (e == cudaErrorInvalidValue) return ASV_ERR_SHAPE;
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (cluster_ctas) *cluster_ctas = pl.cluster;
+  if (threads_per_cta) *threads_per_cta = pl.threads;
+  if (smem_bytes) *smem_bytes = pl.smem;
+  if (bulk_copy) *bulk_copy = pl.bulk;
+  return ASV_OK;
+}
+
+static asv_status run_jsd(int mode, asv::JsdArgs& a, int dtype, void* workspace, size_t ws_bytes,
+                          cudaStream_t stream) {
+  const int amode = mode == asv::kModeAsym ? ASV_MODE_ASYMSPEC : ASV_MODE_SCI;
+  if (ws_bytes < asv_workspace_bytes(amode, a.B, a.K, a.V, dtype)) return ASV_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return ASV_ERR_ALIGN;
+  const int eb = elem_size(dtype);
+  const int NT = mode == asv::kModeAsym ? 3 : 2;
+  bool bulk = (size_t(a.V) * eb) % 16 == 0;
+  for (int j = 0; j < NT; ++j) bulk = bulk && aligned(a.x[j], 16);
+  LaunchPlan pl;
+  cudaError_t e = plan_for(amode, dtype, NT, eb, a.V, (long long)a.B * (a.K + 1), bulk, asv::jsd_static_smem_bytes(), &pl);
+  if (e == cudaErrorInvalidValue) return ASV_ERR_SHAPE;
+  if (e != cudaSuccess) return cuda_fail(e);
+  a.n_slice = pl.n_slice;
+  a.bulk = pl.bulk;
+  a.tickets = reinterpret_cast<uint32_t*>(workspace);
+  a.records = reinterpret_cast<asv::RowRecord*>(static_cast<char*>(workspace) + tickets_bytes(a.B));
+  e = asv::launch_jsd_family(mode, dtype, a, pl, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return ASV_OK;
+}
+
+asv_status asymspec_verify(const void* a, const void* b, const void* t, int dtype, const int32_t* draft_ids, int B,
+                           int K, int V, float beta, float gamma, int32_t* out_accept_len, int32_t* out_tokens,
+                           float* out_D, float* out_lse, uint32_t* out_req_status, void* workspace,
+                           size_t ws_bytes, cudaStream_t stream) {
+  if (B < 0 || K < 0 || V < 2) return ASV_ERR_SHAPE;
+  if ((long long)B * (K + 1) * asv::kMaxCluster > 0x7fffffffLL) return ASV_ERR_SHAPE;
+  if (!valid_dtype(dtype)) return ASV_ERR_DTYPE;
+  if (B == 0) return ASV_OK;
+  if (!a || !b || !t || (K > 0 && !draft_ids) || !out_accept_len || !out_tokens || !out_req_status) return ASV_ERR_NULL;
+  if (!workspace) return ASV_ERR_WORKSPACE;
+  const size_t eb = size_t(elem_size(dtype));
+  if (!aligned(a, eb) || !aligned(b, eb) || !aligned(t, eb) || !aligned(draft_ids, 4) || !aligned(out_accept_len, 4) ||
+      !aligned(out_tokens, 4) || !aligned(out_req_status, 4) || !aligned(out_D, 4) || !aligned(out_lse, 4))
+    return ASV_ERR_ALIGN;
+  if (!std::isfinite(beta) || !std::isfinite(gamma) || !(gamma > 0.0f)) return ASV_ERR_PARAM;
+  asv::JsdArgs args;
+  std::memset(&args, 0, sizeof(args));
+  args.x[0] = a;
+  args.x[1] = b;
+  args.x[2] = t;
+  args.draft_ids = draft_ids;
+  args.B = B;
+  args.K = K;
+  args.V = V;
+  args.beta = beta;
+  args.ln_gamma = std::log(double(gamma));
+  args.out_accept_len = out_accept_len;
+  args.out_tokens = out_tokens;
+  args.out_D = out_D;
+  args.out_lse = out_lse;
+  args.out_req_status = out_req_status;
+  return run_jsd(asv::kModeAsym, args, dtype, workspace, ws_bytes, stream);
+}
+
+asv_status sci_verify(const void* draft_logits, const void* target_logits, int dtype, const int32_t* draft_ids,
+                      int B, int K, int V, const asv_sci_params* params, double* r_hat, int32_t* out_accept_len,
+                      int32_t* out_tokens, float* out_jsd, float* out_T, uint32_t* out_req_status,
+                      void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (B < 0 || K < 1 || V < 2) return ASV_ERR_SHAPE;
+  if ((long long)B * (K + 1) * asv::kMaxCluster > 0x7fffffffLL) return ASV_ERR_SHAPE;
+  if (!valid_dtype(dtype)) return ASV_ERR_DTYPE;
+  if (B == 0) return ASV_OK;
+  if (!draft_logits || !target_logits || !draft_ids || !params || !r_hat || !out_accept_len || !out_tokens ||
+      !out_req_status)
+    return ASV_ERR_NULL;
+  if (!workspace) return ASV_ERR_WORKSPACE;
+  const size_t eb = size_t(elem_size(dtype));
+  if (!aligned(draft_logits, eb) || !aligned(target_logits, eb) || !aligned(draft_ids, 4) || !aligned(r_hat, 8) ||
+      !aligned(out_accept_len, 4) || !aligned(out_tokens, 4) || !aligned(out_jsd, 4) || !aligned(out_T, 4) ||
+      !aligned(out_req_status, 4))
+    return ASV_ERR_ALIGN;
+  const asv_sci_params& P = *params;
+  const double vals[6] = {P.T_base, P.alpha_omega, P.tau_credit, P.T_min, P.T_max, P.ewma_beta};
+  for (double v : vals)
+    if (!std::isfinite(v)) return ASV_ERR_PARAM;
+  if (P.T_min > P.T_max || P.ewma_beta < 0.0 || P.ewma_beta > 1.0) return ASV_ERR_PARAM;
+  asv::JsdArgs args;
+  std::memset(&args, 0, sizeof(args));
+  args.x[0] = draft_logits;
+  args.x[1] = target_logits;
+  args.draft_ids = draft_ids;
+  args.B = B;
+  args.K = K;
+  args.V = V;
+  args.T_base = P.T_base;
+  args.alpha_omega = P.alpha_omega;
+  args.tau_credit = P.tau_credit;
+  args.T_min = P.T_min;
+  args.T_max = P.T_max;
+  args.ewma_beta = P.ewma_beta;
+  args.r_hat = r_hat;
+  args.out_accept_len = out_accept_len;
+  args.out_tokens = out_tokens;
+  args.out_D = out_jsd;
+  args.out_T = out_T;
+  args.out_req_status = out_req_status;
+  return run_jsd(asv::kModeSci, args, dtype, workspace, ws_bytes, stream);
+}
+
+// Host-buffer variant: arena = [a | b | t | draft_ids | accept_len | tokens | D | status | workspace],
+// each part aligned to 256 bytes.
+static size_t host_arena_layout(int B, int K, int V, int dtype, size_t off[9]) {
+  const size_t R = size_t(B) * size_t(K + 1);
+  const size_t in_bytes = R * size_t(V) * size_t(elem_size(dtype));
+  const size_t sizes[9] = {in_bytes, in_bytes, in_bytes, size_t(B) * size_t(K) * 4, size_t(B) * 4, R * 4, R * 4,
+                           size_t(B) * 4, asv_workspace_bytes(ASV_MODE_ASYMSPEC, B, K, V, dtype)};
+  size_t o = 0;
+  for (int i = 0; i < 9; ++i) {
+    off[i] = o;
+    o = round_up(o + sizes[i], 256);
+  }
+  return o;
+}
+
+size_t asv_host_arena_bytes(int B, int K, int V, int dtype) {
+  if (B < 0 || K < 0 || V < 2 || !valid_dtype(dtype)) return 0;
+  size_t off[9];
+  return host_arena_layout(B, K, V, dtype, off);
+}
+
+asv_status asymspec_verify_host(const void* a_host, const void* b_host, const void* t_host, int dtype,
+                                const int32_t* draft_ids_host, int B, int K, int V, float beta, float gamma,
+                                int32_t* out_accept_len_host, int32_t* out_tokens_host, float* out_D_host,
+                                uint32_t* out_req_status_host, void* arena, size_t arena_bytes,
+                                cudaStream_t stream) {
+  if (B < 0 || K < 0 || V < 2) return ASV_ERR_SHAPE;
+  if (!valid_dtype(dtype)) return ASV_ERR_DTYPE;
+  if (B == 0) return ASV_OK;
+  if (!a_host || !b_host || !t_host || (K > 0 && !draft_ids_host) || !out_accept_len_host || !out_tokens_host ||
+      !out_req_status_host)
+    return ASV_ERR_NULL;
+  if (!arena) return ASV_ERR_WORKSPACE;
+  if (!aligned(arena, 256)) return ASV_ERR_ALIGN;
+  size_t off[9];
+  const size_t need = host_arena_layout(B, K, V, dtype, off);
+  if (arena_bytes < need) return ASV_ERR_WORKSPACE;
+  char* base = static_cast<char*>(arena);
+  const size_t R = size_t(B) * size_t(K + 1);
+  const size_t in_bytes = R * size_t(V) * size_t(elem_size(dtype));
+  const void* src[4] = {a_host, b_host, t_host, draft_ids_host};
+  const size_t nbytes[4] = {in_bytes, in_bytes, in_bytes, size_t(B) * size_t(K) * 4};
+  for (int i = 0; i < 4; ++i) {
+    if (nbytes[i] == 0) continue;
+    cudaError_t e = cudaMemcpyAsync(base + off[i], src[i], nbytes[i], cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  asv_status st = asymspec_verify(base + off[0], base + off[1], base + off[2], dtype,
+                                  reinterpret_cast<const int32_t*>(base + off[3]), B, K, V, beta, gamma,
+                                  reinterpret_cast<int32_t*>(base + off[4]), reinterpret_cast<int32_t*>(base + off[5]),
+                                  reinterpret_cast<float*>(base + off[6]), nullptr,
+                                  reinterpret_cast<uint32_t*>(base + off[7]), base + off[8],
+                                  need - off[8], stream);
+  if (st != ASV_OK) return st;
+  struct {
+    void* dst;
+    size_t o;
+    size_t n;
+  } outs[4] = {{out_accept_len_host, off[4], size_t(B) * 4},
+               {out_tokens_host, off[5], R * 4},
+               {out_D_host, off[6], R * 4},
+               {out_req_status_host, off[7], size_t(B) * 4}};
+  for (auto& o : outs) {
+    if (!o.dst) continue;
+    cudaError_t e = cudaMemcpyAsync(o.dst, base + o.o, o.n, cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return ASV_OK;
+}
+
+asv_status rapid_verify(const float* z, const float* q, const int32_t* draft_ids, int B, int G, int V, float T,
+                        float eta, float tail_frac, uint64_t seed, uint32_t offset, int32_t* out_accept_len,
+                        int32_t* out_tokens, uint32_t* out_req_status, void* workspace, size_t ws_bytes,
+                        cudaStream_t stream) {
+  if (B < 0 || G < 0 || V < 2) return ASV_ERR_SHAPE;
+  if ((long long)B * (G + 1) * asv::kMaxCluster > 0x7fffffffLL) return ASV_ERR_SHAPE;
+  if (B == 0) return ASV_OK;
+  if (!z || !q || (G > 0 && !draft_ids) || !out_accept_len || !out_tokens || !out_req_status) return ASV_ERR_NULL;
+  if (!workspace) return ASV_ERR_WORKSPACE;
+  if (!aligned(z, 4) || !aligned(q, 4) || !aligned(draft_ids, 4) || !aligned(out_accept_len, 4) ||
+      !aligned(out_tokens, 4) || !aligned(out_req_status, 4) || !aligned(workspace, 256))
+    return ASV_ERR_ALIGN;
+  if (!std::isfinite(T) || !(T > 0.0f) || !std::isfinite(eta) || eta < 0.0f || !std::isfinite(tail_frac) ||
+      tail_frac < 0.0f || tail_frac >= 1.0f)
+    return ASV_ERR_PARAM;
+  if (ws_bytes < asv_workspace_bytes(ASV_MODE_RAPID, B, G, V, ASV_F32)) return ASV_ERR_WORKSPACE;
+  bool bulk = (size_t(V) * 4) % 16 == 0 && aligned(z, 16) && aligned(q, 16);
+  LaunchPlan pl;
+  cudaError_t e = plan_for(ASV_MODE_RAPID, ASV_F32, 2, 4, V, (long long)B * (G + 1), bulk,
+                           asv::rapid_static_smem_bytes(), &pl);
+  if (e == cudaErrorInvalidValue) return ASV_ERR_SHAPE;
+  if (e != cudaSuccess) return cuda_fail(e);
+  asv::RapidArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.z = z;
+  a.q = q;
+  a.draft_ids = draft_ids;
+  a.B = B;
+  a.G = G;
+  a.V = V;
+  a.n_slice = pl.n_slice;
+  a.bulk = pl.bulk;
+  a.T = T;
+  a.inv_T = 1.0f / T;
+  a.eta = eta;
+  a.tail_frac = tail_frac;
+  a.ln_tail_frac = tail_frac > 0.0f ? std::log(tail_frac) : -INFINITY;
+  a.seed_lo = uint32_t(seed);
+  a.seed_hi = uint32_t(seed >> 32);
+  a.offset = offset;
+  a.out_accept_len = out_accept_len;
+  a.out_tokens = out_tokens;
+  a.out_req_status = out_req_status;
+  a.tickets = reinterpret_cast<uint32_t*>(workspace);
+  a.records = reinterpret_cast<asv::RapidRecord*>(static_cast<char*>(workspace) + tickets_bytes(B));
+  e = asv::launch_rapid(a, pl, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return ASV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,250 @@
+// asv_device.cuh -- device-side building blocks shared by the verification kernels:
+// inline-PTX wrappers for mbarriers, 1-D bulk copies (global -> shared), thread-block
+// cluster barriers and distributed shared memory, the special-function unit's
+// exp2/log2, bf16 unpacking, and warp-level reductions.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "asv_internal.h"
+
+namespace asv {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2f = 0.6931471805599453f;
+constexpr double kLn2 = 0.69314718055994530942;
+constexpr int kNumChunks = 4;          // bulk-copy chunks per staged slice (one mbarrier each)
+constexpr uint32_t kWaitPolls = 1u << 22;  // try_wait polls before a staged-data wait gives up
+
+// Row record bits (workspace).
+constexpr uint32_t kBitNonfinite = 1u;
+constexpr uint32_t kBitBadDraft = 2u;
+constexpr uint32_t kBitTimeout = 4u;
+constexpr uint32_t kBitAccept = 8u;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ------------------------------------------------------------------ mbarrier + bulk copy
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// 1-D bulk copy global -> this CTA's shared memory; completion is counted in bytes on `bar`.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Bounded wait for phase `parity` of `bar`.  Returns false if the poll budget ran out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t polls) {
+  for (uint32_t i = 0; i < polls; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+// ------------------------------------------------------------------ clusters / DSMEM
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  cluster_arrive();
+  cluster_wait();
+}
+
+// Address of the same shared-memory variable in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t local_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ double dsmem_ld_f64(uint32_t a) {
+  double v;
+  asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int32_t dsmem_ld_s32(uint32_t a) {
+  int32_t v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t dsmem_ld_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint16_t dsmem_ld_u16(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared::cluster.u16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
+  return v;
+}
+
+// ------------------------------------------------------------------ special-function unit
+
+// 2^x and log2(x) on the special-function unit (approximate, flush-to-zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ------------------------------------------------------------------ element types
+
+struct bf16_t {
+  uint16_t bits;
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+  using storage = float;
+  static constexpr int kVec = 4;  // elements per 16-byte vector
+  __device__ static __forceinline__ void load_vec(const float* s, int vi, float (&x)[4]) {
+    const float4 v = reinterpret_cast<const float4*>(s)[vi];
+    x[0] = v.x;
+    x[1] = v.y;
+    x[2] = v.z;
+    x[3] = v.w;
+  }
+  __device__ static __forceinline__ float to_float(float v) { return v; }
+  __device__ static __forceinline__ float neg_inf() { return __uint_as_float(0xff800000u); }
+  __device__ static __forceinline__ float from_smem_remote(uint32_t a) { return dsmem_ld_f32(a); }
+};
+
+template <>
+struct Elem<bf16_t> {
+  using storage = uint16_t;
+  static constexpr int kVec = 8;
+  __device__ static __forceinline__ void load_vec(const uint16_t* s, int vi, float (&x)[8]) {
+    const uint4 v = reinterpret_cast<const uint4*>(s)[vi];
+    x[0] = bf16_lo(v.x);
+    x[1] = bf16_hi(v.x);
+    x[2] = bf16_lo(v.y);
+    x[3] = bf16_hi(v.y);
+    x[4] = bf16_lo(v.z);
+    x[5] = bf16_hi(v.z);
+    x[6] = bf16_lo(v.w);
+    x[7] = bf16_hi(v.w);
+  }
+  __device__ static __forceinline__ float to_float(uint16_t v) { return __uint_as_float(uint32_t(v) << 16); }
+  __device__ static __forceinline__ uint16_t neg_inf() { return uint16_t(0xff80u); }
+  __device__ static __forceinline__ float from_smem_remote(uint32_t a) {
+    return __uint_as_float(uint32_t(dsmem_ld_u16(a)) << 16);
+  }
+};
+
+// ------------------------------------------------------------------ warp reductions
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_min(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// (value, index): larger value wins; equal values -> lower index.
+__device__ __forceinline__ void argmax_merge(float& v, int& i, float ov, int oi) {
+  if (ov > v || (ov == v && oi < i)) {
+    v = ov;
+    i = oi;
+  }
+}
+
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    argmax_merge(v, i, ov, oi);
+  }
+}
+
+// (value, index): smaller value wins; equal values -> lower index.
+__device__ __forceinline__ void argmin_merge(float& v, int& i, float ov, int oi) {
+  if (ov < v || (ov == v && oi < i)) {
+    v = ov;
+    i = oi;
+  }
+}
+
+__device__ __forceinline__ void warp_argmin(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    argmin_merge(v, i, ov, oi);
+  }
+}
+
+}  // namespace asv

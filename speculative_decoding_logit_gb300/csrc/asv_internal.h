@@ -1,0 +1,95 @@
+// asv_internal.h -- host-side declarations shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace asv {
+
+constexpr int kMaxCluster = 16;  // CTAs per row (16 needs the non-portable cluster attribute)
+
+// One row's result as the row's cluster leaves it in the workspace for the
+// request-level scan.  `value` is the row's divergence (SCI) or unused;
+// `token` the row's emitted-token candidate; `bits` the kBit* flags.
+struct __align__(16) RowRecord {
+  double value;
+  int32_t token;
+  uint32_t bits;
+};
+
+// RAPID row state kept for the request-level scan and the residual/bonus draw.
+struct __align__(32) RapidRecord {
+  double lse_z;   // log-sum-exp of z / T (natural log)
+  float zmax_hat; // max of zhat (over the row)
+  float head_scale; // (sum of p over the head) / (sum of exp((zhat - zmax_hat)/T) over the head)
+  float accept_ratio;
+  int32_t pad0;
+  uint32_t bits;
+  uint32_t pad1;
+};
+
+struct LaunchPlan {
+  int cluster;    // CTAs per row
+  int threads;    // threads per CTA
+  int n_slice;    // vocabulary entries per CTA (multiple of the 16-byte vector width)
+  int smem;       // dynamic shared memory bytes
+  int bulk;       // 1: rows staged with bulk copies
+};
+
+constexpr int kModeAsym = 0;
+constexpr int kModeSci = 1;
+
+struct JsdArgs {
+  const void* x[3];  // AsymSpec: a, b, t.  SCI: draft, target (x[2] unused)
+  const int32_t* draft_ids;
+  int B, K, V;
+  int n_slice;
+  int bulk;
+  float beta;
+  double ln_gamma;
+  // SCI
+  double T_base, alpha_omega, tau_credit, T_min, T_max, ewma_beta;
+  double* r_hat;
+  // outputs
+  int32_t* out_accept_len;
+  int32_t* out_tokens;
+  float* out_D;      // AsymSpec: JSD(a,b); SCI: JSD(draft,target)
+  float* out_lse;    // AsymSpec only, [R, 3]
+  float* out_T;      // SCI only
+  uint32_t* out_req_status;
+  // workspace
+  uint32_t* tickets;
+  RowRecord* records;
+};
+
+struct RapidArgs {
+  const float* z;
+  const float* q;
+  const int32_t* draft_ids;
+  int B, G, V;
+  int n_slice;
+  int bulk;
+  float T, inv_T, eta, tail_frac, ln_tail_frac;
+  uint32_t seed_lo, seed_hi, offset;
+  int32_t* out_accept_len;
+  int32_t* out_tokens;
+  uint32_t* out_req_status;
+  uint32_t* tickets;
+  RapidRecord* records;
+};
+
+// Kernel launchers (return the cudaError_t of the launch).
+cudaError_t launch_jsd_family(int mode, int dtype, const JsdArgs& args, const LaunchPlan& plan, cudaStream_t s);
+cudaError_t launch_rapid(const RapidArgs& args, const LaunchPlan& plan, cudaStream_t s);
+
+// Static shared memory the kernels use beside the dynamic staging area.
+int jsd_static_smem_bytes();
+int rapid_static_smem_bytes();
+
+// Occupancy query: clusters of `plan` that can be resident at once (0 = cannot launch).
+int jsd_max_active_clusters(int mode, int dtype, const LaunchPlan& plan);
+int rapid_max_active_clusters(const LaunchPlan& plan);
+
+}  // namespace asv

@@ -1,0 +1,80 @@
+"""GPU parity for the E2-SCI window: JSD within tolerance, accept lengths and tokens
+bit-exact (requests within 1e-6 of the threshold counted, not graded), credit state
+carried across windows identically."""
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+from parity_util import to_device, tol
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def asv():
+    import speculative_decoding_logit_gb300 as m
+    m.build()
+    return m
+
+
+def _window(asv, batch, r_hat, params=None):
+    p = params or asv.SciParams()
+    r = torch.from_numpy(np.array(r_hat, np.float64)).cuda()
+    out = asv.sci_verify(to_device(batch.a, batch.dtype), to_device(batch.t, batch.dtype),
+                         torch.from_numpy(batch.drafts).cuda(), r, p)
+    torch.cuda.synchronize()
+    op = oracle.SciParams(p.T_base, p.alpha_omega, p.tau_credit, p.T_min, p.T_max, p.ewma_beta)
+    ref = oracle.sci_verify(batch.a, batch.t, batch.drafts, r_hat, op)
+    return out, r.cpu().numpy(), ref
+
+
+def _compare(out, r_new, ref, dtype):
+    st = out.req_status.cpu().numpy().astype(np.uint32)
+    np.testing.assert_array_equal(st & 3, ref.flags & 3)
+    acc = out.accept_len.cpu().numpy()
+    tok = out.tokens.cpu().numpy()
+    graded = 0
+    for r in range(len(acc)):
+        if ref.flags[r] & oracle.FLAGS_UNGRADED:
+            continue
+        graded += 1
+        assert acc[r] == ref.accept_len[r]
+        np.testing.assert_array_equal(tok[r], ref.tokens[r])
+        assert r_new[r] == pytest.approx(ref.r_hat[r], abs=1e-15)
+    fin = (ref.flags & 1) == 0
+    np.testing.assert_allclose(out.jsd.cpu().numpy()[fin], ref.jsd[fin], atol=tol(dtype), rtol=0)
+    np.testing.assert_allclose(out.T.cpu().numpy(), ref.T, atol=1e-7)
+    return graded
+
+
+@pytest.mark.parametrize("dtype", [gen.F32, gen.BF16])
+@pytest.mark.parametrize("V", [33, 2048, 151936])
+def test_window_shapes(asv, dtype, V):
+    B = 16 if V < 100000 else 4
+    batch = gen.make_asymspec_batch("spiky", 900 + V, B, 8, V, dtype)
+    rng = np.random.default_rng(V)
+    out, r_new, ref = _window(asv, batch, rng.uniform(0, 1, B))
+    assert _compare(out, r_new, ref, dtype) >= B - 2
+
+
+def test_clamps_bind(asv):
+    batch = gen.make_asymspec_batch("spiky", 5, 8, 4, 1000, gen.BF16)
+    p = asv.SciParams(alpha_omega=2.0)
+    out, r_new, ref = _window(asv, batch, np.linspace(0, 1, 8), p)
+    T = out.T.cpu().numpy()
+    assert T.min() == pytest.approx(0.1) and T.max() == pytest.approx(0.6)
+    _compare(out, r_new, ref, gen.BF16)
+
+
+def test_five_windows_carry_state(asv):
+    """k = 5 windows with independently seeded tensors, credit state carried on the device."""
+    w = gen.WORKLOADS["sci_asymspec_b1024_k8_v151936_bf16"]
+    B = 32
+    r = np.full(B, w.params["r_hat0"])
+    for win in range(w.params["windows"]):
+        batch = gen.make_asymspec_batch(w.recipe, w.seed + win, B, w.K, w.V, w.dtype, processes=8)
+        out, r_gpu, ref = _window(asv, batch, r)
+        _compare(out, r_gpu, ref, w.dtype)
+        r = ref.r_hat
