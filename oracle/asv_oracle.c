@@ -65,12 +65,22 @@ static float widen_f(const void* base, int dtype, size_t i) {
 
 static double widen(const void* base, int dtype, size_t i) { return (double)widen_f(base, dtype, i); }
 
-/* NaN or +inf anywhere in the row (-inf is a legal logit: probability 0). */
+/* NaN or +inf anywhere in the row, or a row that is -inf everywhere (it has no
+ * softmax).  A single -inf is a legal logit: probability 0. */
 static int row_nonfinite(const void* x, int dtype, size_t off, int V) {
+  int all_ninf = 1;
   for (int k = 0; k < V; ++k) {
     double v = widen(x, dtype, off + (size_t)k);
     if (isnan(v) || (isinf(v) && v > 0)) return 1;
+    if (!(isinf(v) && v < 0)) all_ninf = 0;
   }
+  return all_ninf;
+}
+
+/* Any NaN or infinity (probabilities must be finite). */
+static int row_any_nonfinite(const float* x, size_t off, int V) {
+  for (int k = 0; k < V; ++k)
+    if (!isfinite(x[off + (size_t)k])) return 1;
   return 0;
 }
 
@@ -105,9 +115,9 @@ double oracle_jsd(const void* x, const void* y, int dtype, size_t offx, size_t o
 }
 
 /* Lowest index attaining the maximum of the fp32 score
- * s_k = fmaf(beta, a_k - b_k, t_k); entries whose score is NaN never win; a row
- * with no comparable score returns 0.  [ASYM] sec. 4.1: d' = argmax(t + beta*delta),
- * delta = a - b. */
+ * s_k = fmaf(beta, a_k - b_k, t_k).  An entry whose score is NaN or -inf (a token
+ * the fused scores make impossible) is never chosen; if no entry qualifies the
+ * result is 0.  [ASYM] sec. 4.1: d' = argmax(t + beta*delta), delta = a - b. */
 int oracle_fused_argmax(const void* a, const void* b, const void* t, int dtype, size_t off, int V,
                         float beta) {
   int best = -1;
@@ -118,7 +128,7 @@ int oracle_fused_argmax(const void* a, const void* b, const void* t, int dtype, 
     float tk = widen_f(t, dtype, off + (size_t)k);
     float d = ak - bk;
     float s = fmaf(beta, d, tk);
-    if (s > bv || (best < 0 && s == bv)) {
+    if (s > bv) {
       bv = s;
       best = k;
     }
@@ -135,7 +145,7 @@ int oracle_fused_argmax_f64(const void* a, const void* b, const void* t, int dty
   for (int k = 0; k < V; ++k) {
     double s = widen(t, dtype, off + (size_t)k) +
                beta * (widen(a, dtype, off + (size_t)k) - widen(b, dtype, off + (size_t)k));
-    if (s > bv || (best < 0 && s == bv)) {
+    if (s > bv) {
       bv = s;
       best = k;
     }
@@ -289,7 +299,7 @@ double oracle_rapid_uniform(uint64_t seed, uint32_t offset, uint32_t stream, uin
  *   prot_k = p_k on the tail; on the head phat_k * (1 - sum_tail p) / sum_head phat.
  * Arrays p, zhat, phat, prot are length V (any may be NULL).  Returns the
  * number of tail entries; *near is set when some phat_k lies within a relative
- * 1e-6 of the tail boundary.
+ * 1e-5 of the tail boundary (the library decides the mask in fp32).
  */
 int oracle_rapid_row(const float* z, const float* q, int V, double T, double eta, double tail_frac,
                      double* p_out, double* zhat_out, double* phat_out, double* prot_out, int* near) {
@@ -314,7 +324,7 @@ int oracle_rapid_row(const float* z, const float* q, int V, double T, double eta
   double tail_p = 0.0, head_ph = 0.0;
   int ntail = 0, nr = 0;
   for (int k = 0; k < V; ++k) {
-    if (fabs(ph[k] - thr) <= 1e-6 * thr) nr = 1;
+    if (fabs(ph[k] - thr) <= 1e-5 * thr) nr = 1;
     if (ph[k] < thr) {
       tail_p += p[k];
       ++ntail;
@@ -383,7 +393,7 @@ void oracle_rapid_verify(const float* z, const float* q, const int32_t* draft_id
     }
     for (int i = 0; i <= G; ++i) {
       size_t off = ((size_t)b * (G + 1) + i) * (size_t)V;
-      if (row_nonfinite(z, OR_F32, off, V) || row_nonfinite(q, OR_F32, off, V)) flags |= OR_NONFINITE;
+      if (row_nonfinite(z, OR_F32, off, V) || row_any_nonfinite(q, off, V)) flags |= OR_NONFINITE;
     }
     if (flags) {
       out_accept_len[b] = 0;
@@ -400,7 +410,7 @@ void oracle_rapid_verify(const float* z, const float* q, const int32_t* draft_id
       double u = oracle_rapid_uniform(seed, offset, 0u, (uint32_t)b, (uint32_t)i, 0u);
       double lhs = u * (double)q[off + (size_t)d];
       double rhs = prot[d];
-      if (fabs(lhs - rhs) <= 1e-6 * fabs(rhs)) flags |= OR_NEAR_MARGIN;
+      if (fabs(lhs - rhs) <= 1e-5 * fabs(rhs)) flags |= OR_NEAR_MARGIN;
       if (!(lhs < rhs)) {
         n = i;
         break;
@@ -498,7 +508,7 @@ void oracle_sci_verify(const void* draft, const void* target, int dtype, const i
     float bv = -INFINITY;
     for (int k = 0; k < V; ++k) {
       float v = widen_f(target, dtype, offn + (size_t)k);
-      if (v > bv || (c < 0 && v == bv)) {
+      if (v > bv) {
         bv = v;
         c = k;
       }

@@ -118,7 +118,9 @@ def test_fused_argmax_ties_and_nan():
     t2 = np.array([np.nan, 1, 3, np.nan, 3], np.float32)
     assert oracle.fused_argmax(z, z, t2, 0.0) == 2                 # NaN never wins
     ninf = np.full(4, -np.inf, np.float32)
-    assert oracle.fused_argmax(z[:4], z[:4], ninf, 0.0) == 0       # all -inf: index 0
+    assert oracle.fused_argmax(z[:4], z[:4], ninf, 0.0) == 0       # no finite score: index 0
+    t3 = np.array([-np.inf, -np.inf, -2.0, -np.inf], np.float32)
+    assert oracle.fused_argmax(z[:4], z[:4], t3, 0.0) == 2
     # beta = 0 reduces to argmax t
     rng = np.random.default_rng(6)
     a, b, t = _rows(rng, 3, 1000, gen.BF16)
@@ -220,6 +222,8 @@ def test_flags_nonfinite_and_bad_draft():
     assert oracle.asymspec_verify(a, b, t2, d, 1.0, 0.5).flags[0] & oracle.FLAG_NONFINITE
     b2 = b.copy(); b2[0, 0, 3] = -np.inf                      # -inf is a legal logit
     assert not oracle.asymspec_verify(a, b2, t, d, 1.0, 0.5).flags[0] & oracle.FLAG_NONFINITE
+    b3 = b.copy(); b3[0, 1, :] = -np.inf                      # ... but a row of -inf has no softmax
+    assert oracle.asymspec_verify(a, b3, t, d, 1.0, 0.5).flags[0] & oracle.FLAG_NONFINITE
     r = oracle.asymspec_verify(a, b, t, np.array([[1, 20]], np.int32), 1.0, 0.5)
     assert r.flags[0] & oracle.FLAG_BAD_DRAFT and np.all(r.tokens == -1)
 
