@@ -1,0 +1,318 @@
+"""Throughput benchmark of the fused AsymSpec verification step (CDA gate + delta-fusion).
+
+One step = one asymspec_verify call over the whole batch of the B=64, K=2, V=151936 bf16
+workload (64 requests x 3 rows of three logit tensors a, b, t = 175 MB), with inputs resident
+in HBM.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun, one rank per GPU; requests are independent, so every rank verifies
+its own batch (weak scaling, no collective on the data path).  `--impl reference` times the CPU
+oracle (the double-precision restatement of the pages) on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gen  # noqa: E402
+
+WORKLOAD = "asymspec_b64_k2_v151936_bf16"
+METRIC = "verified logit rows/s and HBM GB/s vs ~8 TB/s, fused CDA+δ verify, V=151936"
+BETA, GAMMA = 1.0, 0.5
+N_SETS = 4  # rotating input copies: 4 x 175 MB, larger than the 129 MB L2
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index, period_ms: int = 50):
+        self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    f"-lms={period_ms}", f"-i={gpu_index}"]
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=5)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_baseline_oracle(batch, budget_s: float = 20.0):
+    """The oracle, as it stands, on the host: whole requests until ~budget_s of CPU work."""
+    import oracle
+    oracle.lib()
+    rows = 0
+    t0 = time.perf_counter()
+    r = 0
+    while r < batch.B and (time.perf_counter() - t0) < budget_s:
+        oracle.asymspec_verify(batch.a[r:r + 1], batch.b[r:r + 1], batch.t[r:r + 1], batch.drafts[r:r + 1], BETA,
+                               GAMMA)
+        rows += batch.K + 1
+        r += 1
+    dt = time.perf_counter() - t0
+    return {"value": rows / dt, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": f"{r} of {batch.B} requests ({rows} rows of V={batch.V}), one pass, single-threaded C, float64"}
+
+
+def run_reference(args):
+    """CPU oracle timed as the reference arm: each step verifies one request whose rows are
+    cut to the first V' vocabulary entries (V' sized so the run ends within a few minutes);
+    throughput counts each step as 3 * V'/V rows."""
+    import oracle
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    w = gen.WORKLOADS[WORKLOAD]
+    batch = gen.make_asymspec_batch(w.recipe, w.seed, 2, w.K, w.V, w.dtype)
+    oracle.lib()
+    t0 = time.perf_counter()
+    oracle.asymspec_verify(batch.a[:1], batch.b[:1], batch.t[:1], batch.drafts[:1], BETA, GAMMA)
+    per_req = time.perf_counter() - t0
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    Vp = int(min(w.V, max(64, w.V * budget / per_req)))
+    Vp -= Vp % 8
+    cut = lambda x: np.ascontiguousarray(x[:1, :, :Vp])
+    a, b, t = cut(batch.a), cut(batch.b), cut(batch.t)
+    d = np.minimum(batch.drafts[:1], Vp - 1).astype(np.int32)
+    for _ in range(args.warmup):
+        oracle.asymspec_verify(a, b, t, d, BETA, GAMMA)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.asymspec_verify(a, b, t, d, BETA, GAMMA)
+    dt = time.perf_counter() - t0
+    rows = args.steps * (w.K + 1) * Vp / w.V
+    val = rows / dt
+    sample = f"per step: 1 request, rows cut to the first {Vp} of {w.V} entries (counted as {(w.K + 1) * Vp / w.V:.4f} rows)"
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "rows/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "B": w.B, "K": w.K, "V": w.V, "beta": BETA, "gamma": GAMMA},
+            "cpu_baseline": {"value": val, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import ctypes as C
+
+    import torch
+
+    import speculative_decoding_logit_gb300 as asv
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        dist = None
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    asv.build()
+    lib = asv.library()
+
+    w = gen.WORKLOADS[WORKLOAD]
+    batch = gen.make_asymspec_batch(w.recipe, w.seed, w.B, w.K, w.V, w.dtype, processes=8)
+    R = w.B * (w.K + 1)
+    in_bytes = 3 * R * w.V * 2
+
+    def todev(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    sets = [tuple(todev(x) for x in (batch.a, batch.b, batch.t)) for _ in range(N_SETS)]
+    d = torch.from_numpy(batch.drafts).to(dev)
+    out = asv.asymspec_verify(*sets[0], d, BETA, GAMMA)  # allocates outputs, loads the library
+    wsbuf = torch.zeros(asv.workspace_bytes(asv.ASV_MODE_ASYMSPEC, w.B, w.K, w.V, asv.ASV_BF16), dtype=torch.uint8,
+                        device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    # Pre-marshalled argument lists: the timed loop is one ctypes call per step.
+    calls = []
+    for (a, b, t) in sets:
+        calls.append((a.data_ptr(), b.data_ptr(), t.data_ptr(), asv.ASV_BF16, d.data_ptr(), w.B, w.K, w.V,
+                      BETA, GAMMA, out.accept_len.data_ptr(), out.tokens.data_ptr(), out.D.data_ptr(),
+                      out.lse.data_ptr(), out.req_status.data_ptr(), wsbuf.data_ptr(), wsbuf.numel(), sh))
+    fn = lib.asymspec_verify
+
+    def step(i):
+        st = fn(*calls[i % N_SETS])
+        if st != 0:
+            raise RuntimeError(f"asymspec_verify failed: {st}")
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(dev.index)
+    clocks = ClockSampler(gpu_id)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start
+    e0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step(i)
+        ev[i][1].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    elapsed_ms = e0.elapsed_time(e1)
+    launch_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    if dist:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    rows_total = R * args.steps * ws
+    value = rows_total / (elapsed_ms / 1e3)
+
+    # End to end through the C ABI with host (pinned) buffers: H2D of the step's inputs,
+    # the verification, D2H of the step's results, every step.
+    if True:
+        pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+        ha, hb, ht = (pin(x.view(np.int16)) for x in (batch.a, batch.b, batch.t))
+        hd = pin(batch.drafts)
+        o_acc = torch.empty(w.B, dtype=torch.int32).pin_memory()
+        o_tok = torch.empty(w.B, w.K + 1, dtype=torch.int32).pin_memory()
+        o_D = torch.empty(w.B, w.K + 1, dtype=torch.float32).pin_memory()
+        o_st = torch.empty(w.B, dtype=torch.int32).pin_memory()
+        arena = torch.zeros(asv.host_arena_bytes(w.B, w.K, w.V, asv.ASV_BF16), dtype=torch.uint8, device=dev)
+        hcall = (ha.data_ptr(), hb.data_ptr(), ht.data_ptr(), asv.ASV_BF16, hd.data_ptr(), w.B, w.K, w.V, BETA, GAMMA,
+                 o_acc.data_ptr(), o_tok.data_ptr(), o_D.data_ptr(), o_st.data_ptr(), arena.data_ptr(), arena.numel(),
+                 sh)
+        hfn = lib.asymspec_verify_host
+        for _ in range(3):
+            assert hfn(*hcall) == 0
+        torch.cuda.synchronize()
+        ne = max(10, min(200, args.steps // 50))
+        h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        h0.record(stream)
+        for _ in range(ne):
+            assert hfn(*hcall) == 0
+        h1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = h0.elapsed_time(h1)
+        assert np.array_equal(o_tok.numpy(), out.tokens.cpu().numpy())
+        h2d = 3 * R * w.V * 2 + w.B * w.K * 4
+        d2h = w.B * 4 + R * 4 + R * 4 + w.B * 4
+        e2e = {"value": R * ne * ws / (e_ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": ne, "ms_per_step": e_ms / ne}
+
+    peaks, peak_kind = _peaks()
+    achieved = in_bytes / (launch_ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": args.traffic, "peak_kind": peak_kind,
+            "frac_of_8tbs": achieved / 8000.0, "kernel_ms": launch_ms,
+            "algorithmic_bytes_per_launch": in_bytes}
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_oracle(batch)
+    plan = asv.query_plan(asv.ASV_MODE_ASYMSPEC, w.B, w.K, w.V, asv.ASV_BF16)
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "B": w.B, "K": w.K, "V": w.V, "beta": BETA, "gamma": GAMMA,
+                           "rows_per_step": R, "parallelism": f"replicas x{ws} (requests sharded, no collective)",
+                           "l2": f"{N_SETS} rotating input sets of {in_bytes / 1e6:.0f} MB (> 129 MB L2)",
+                           "plan": plan},
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps, "clocks": clk}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch from an ncu capture of the current kernel (else null)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -248,3 +248,52 @@ __device__ __forceinline__ void warp_argmin(float& v, int& i) {
 }
 
 }  // namespace asv
+
+namespace asv {
+
+__device__ __forceinline__ void dsmem_st_u32(uint32_t a, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+// ------------------------------------------------------------------ Philox4x32-10
+// Counter-based generator of Salmon, Moraes, Dror and Shaw ("Parallel random numbers: as easy
+// as 1, 2, 3", SC'11): ten rounds; a round multiplies words 0 and 2 by the two round
+// multipliers, XORs the high halves with words 1/3 and the key, and the key advances by the
+// two Weyl increments before every round but the first.
+struct Philox4 {
+  uint32_t v[4];
+};
+
+__device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
+                                                 uint32_t k1) {
+  constexpr uint32_t kMulA = 0xD2511F53u, kMulB = 0xCD9E8D57u;
+  constexpr uint32_t kWeylA = 0x9E3779B9u, kWeylB = 0xBB67AE85u;
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    if (round) {
+      k0 += kWeylA;
+      k1 += kWeylB;
+    }
+    const uint32_t hiA = __umulhi(kMulA, c0), loA = kMulA * c0;
+    const uint32_t hiB = __umulhi(kMulB, c2), loB = kMulB * c2;
+    const uint32_t n0 = hiB ^ c1 ^ k0;
+    const uint32_t n2 = hiA ^ c3 ^ k1;
+    c0 = n0;
+    c1 = loB;
+    c2 = n2;
+    c3 = loA;
+  }
+  Philox4 r;
+  r.v[0] = c0;
+  r.v[1] = c1;
+  r.v[2] = c2;
+  r.v[3] = c3;
+  return r;
+}
+
+// Uniform in (0, 1) from a 32-bit word: ((w >> 9) + 0.5) * 2^-23, exact in fp32.
+__device__ __forceinline__ float uniform_from_word(uint32_t w) {
+  return (float(w >> 9) + 0.5f) * 1.1920928955078125e-7f;
+}
+
+}  // namespace asv

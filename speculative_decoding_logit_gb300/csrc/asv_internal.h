@@ -19,15 +19,18 @@ struct __align__(16) RowRecord {
   uint32_t bits;
 };
 
-// RAPID row state kept for the request-level scan and the residual/bonus draw.
+// RAPID row state kept for the request-level scan and for the residual/bonus draw, which the
+// last row of a request to finish recomputes for the emitted position.  With zs = z / T:
+//   p_k = ex2(fma(zs_k, log2e, -zs_max*log2e)) * inv_sum, zhat_k = z_k + eta*T*(q_k - p_k),
+//   tail_k <=> zhat_k / T < zhat_max + ln(tail_frac),
+//   protected_k = p_k on the tail, ex2((zhat_k / T - zhat_max) * log2e) * head_scale on the head.
 struct __align__(32) RapidRecord {
-  double lse_z;   // log-sum-exp of z / T (natural log)
-  float zmax_hat; // max of zhat (over the row)
-  float head_scale; // (sum of p over the head) / (sum of exp((zhat - zmax_hat)/T) over the head)
-  float accept_ratio;
-  int32_t pad0;
+  float zs_max;
+  float inv_sum;
+  float zhat_max;   // max of zhat / T
+  float head_scale;
   uint32_t bits;
-  uint32_t pad1;
+  uint32_t pad[3];
 };
 
 struct LaunchPlan {

@@ -1,12 +1,473 @@
-// asv_rapid.cu -- RAPID verification kernel (retrieval-augmented target, tail protection,
-// adjusted residual sampling).  Placeholder until the kernel lands: the launcher reports
-// cudaErrorNotSupported, which the C ABI turns into ASV_ERR_CUDA.
+// asv_rapid.cu -- the RAPID verification kernel.
+//
+// Source: "RAPID: Long-Context Inference with Retrieval-Augmented Speculative Decoding" (paper
+// notes): Workflow (rejection sampling against the augmented target); Key design 2 (augmented
+// target zhat = z + eta*T*(q - p), p = softmax(z/T), phat = softmax(zhat/T)); Key design 3 (tokens
+// whose augmented probability is below 10% of the peak keep the original target probability);
+// Key design 4 (at a rejection the token is drawn from norm(max(p - phat, p - q, 0))).
+//
+// Decomposition as in the AsymSpec kernel: a cluster of C CTAs per row, each CTA staging its slice
+// of z and q in shared memory once.  Four sweeps over the staged slice, each followed by a cluster
+// exchange through distributed shared memory:
+//   1. max of z/T;  2. sum of exp(z/T - max) (and sum of q, for the finiteness check);
+//   3. max of zhat/T;  4. head sums: sum of p and of exp(zhat/T - max) over entries at or above
+//      the tail boundary zhat/T >= max + ln(tail_frac).
+// The protected target is then p on the tail and exp(zhat/T - max) * (head p-mass / head
+// exp-mass) on the head, which sums to 1 without a further normalisation pass.  CTA 0 of the row
+// decides the draft's accept test u*q(d) < protected(d) (u from Philox4x32-10) and files a row
+// record.  The last row of a request to finish runs the scan and, in the same cluster, draws the
+// emitted token at the stop position with an exponential race over that row (re-read from global
+// memory, normally still in L2): argmin_k E_k / w_k, E_k = -ln u_k, with w the residual
+// max(p - protected, p - q, 0) or, at the bonus position, the protected target.
+#include <climits>
+
+#include "asv_device.cuh"
 #include "asv_internal.h"
 
 namespace asv {
 
-int rapid_static_smem_bytes() { return 4096; }
-int rapid_max_active_clusters(const LaunchPlan&) { return 0; }
-cudaError_t launch_rapid(const RapidArgs&, const LaunchPlan&, cudaStream_t) { return cudaErrorNotSupported; }
+struct __align__(16) RapidXchg {
+  float zmax;
+  float zhmax;
+  uint32_t err;
+  uint32_t draw_active;  // set remotely by CTA 0 when this cluster draws for its request
+  double sum_e;
+  double sum_q;
+  double head_p;
+  double head_e;
+  float race_key;
+  int32_t race_idx;
+  int32_t draw_row;
+  float d_zs_max;  // the drawn row's record, broadcast by CTA 0
+  float d_inv_sum;
+  float d_zhat_max;
+  float d_head_scale;
+  uint32_t pad;
+};
+
+struct RowConsts {
+  float invT, etaT, ML, inv_sum, zhmax, thr, head_scale;
+};
+
+// p, zhat/T and the protected target of one entry, recomputed identically everywhere.
+__device__ __forceinline__ void rapid_entry(float z, float q, const RowConsts& c, float& p, float& zhs, float& prot) {
+  const float zs = z * c.invT;
+  p = ex2_approx(fmaf(zs, kLog2e, -c.ML)) * c.inv_sum;
+  const float zh = fmaf(c.etaT, q - p, z);
+  zhs = zh * c.invT;
+  prot = (zhs < c.thr) ? p : ex2_approx((zhs - c.zhmax) * kLog2e) * c.head_scale;
+}
+
+__global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
+  constexpr int VEC = 4;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  __shared__ RapidXchg xchg;
+  __shared__ float s_wf[32];
+  __shared__ int32_t s_wi[32];
+  __shared__ double s_wd[32][2];
+  __shared__ __align__(8) uint64_t s_bar[kNumChunks];
+  __shared__ uint32_t s_err;
+
+  const int tid = threadIdx.x;
+  const int nthr = blockDim.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int nwarps = nthr >> 5;
+  const uint32_t rank = cluster_rank();
+  const uint32_t C = cluster_size();
+  const int row = blockIdx.x / C;
+  const int G = p.G;
+  const int R1 = G + 1;
+  const int req = row / R1;
+  const int pos = row - req * R1;
+  const int V = p.V;
+  const int v0 = int(rank) * p.n_slice;
+  const int len = max(0, min(V - v0, p.n_slice));
+  const int nvec = (len + VEC - 1) / VEC;
+  const size_t row_base = size_t(row) * size_t(V);
+  const size_t stage_stride = (size_t(p.n_slice) * sizeof(float) + 127) & ~size_t(127);
+  float* zst = reinterpret_cast<float*>(smem_raw);
+  float* qst = reinterpret_cast<float*>(smem_raw + stage_stride);
+  const int chunk_vec = (nvec + kNumChunks - 1) / kNumChunks;
+
+  // ---------------------------------------------------------------- staging
+  if (tid == 0) {
+    s_err = 0;
+    xchg.draw_active = 0;
+#pragma unroll
+    for (int c = 0; c < kNumChunks; ++c) mbar_init(smem_addr(&s_bar[c]), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (p.bulk) {
+    if (tid == 0) {
+      for (int c = 0; c < kNumChunks; ++c) {
+        const int cv0 = c * chunk_vec;
+        const int cv1 = min(nvec, cv0 + chunk_vec);
+        if (cv1 <= cv0) break;
+        const uint32_t bytes = uint32_t(cv1 - cv0) * VEC * 4u;
+        const uint32_t bar = smem_addr(&s_bar[c]);
+        mbar_arrive_expect_tx(bar, 2 * bytes);
+        bulk_g2s(smem_addr(zst + cv0 * VEC), p.z + row_base + v0 + cv0 * VEC, bytes, bar);
+        bulk_g2s(smem_addr(qst + cv0 * VEC), p.q + row_base + v0 + cv0 * VEC, bytes, bar);
+      }
+    }
+  } else {
+    const int npad = nvec * VEC;
+    for (int k = tid; k < npad; k += nthr) {
+      zst[k] = (k < len) ? p.z[row_base + v0 + k] : -INFINITY;
+      qst[k] = (k < len) ? p.q[row_base + v0 + k] : 0.0f;
+    }
+    __syncthreads();
+  }
+
+  auto block_max = [&](float v) -> float {
+    v = warp_max(v);
+    if (lane == 0) s_wf[warp] = v;
+    __syncthreads();
+    float r = -INFINITY;
+    if (warp == 0) r = warp_max(lane < nwarps ? s_wf[lane] : -INFINITY);
+    __syncthreads();
+    return r;  // valid in warp 0
+  };
+  auto block_sum2 = [&](double a, double b, double& ra, double& rb) {
+    a = warp_sum(a);
+    b = warp_sum(b);
+    if (lane == 0) {
+      s_wd[warp][0] = a;
+      s_wd[warp][1] = b;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      ra = warp_sum(lane < nwarps ? s_wd[lane][0] : 0.0);
+      rb = warp_sum(lane < nwarps ? s_wd[lane][1] : 0.0);
+    }
+    __syncthreads();
+  };
+
+  const float invT = p.inv_T;
+  // ---------------------------------------------------------------- sweep 1: max of z/T
+  {
+    float m = -INFINITY;
+    for (int c = 0; c < kNumChunks; ++c) {
+      const int cv0 = c * chunk_vec;
+      const int cv1 = min(nvec, cv0 + chunk_vec);
+      if (cv1 <= cv0) break;
+      if (p.bulk && !mbar_wait(smem_addr(&s_bar[c]), 0, kWaitPolls)) atomicOr(&s_err, 1u);
+      for (int vi = cv0 + tid; vi < cv1; vi += nthr) {
+        const float4 z4 = reinterpret_cast<const float4*>(zst)[vi];
+        m = fmaxf(m, fmaxf(fmaxf(z4.x * invT, z4.y * invT), fmaxf(z4.z * invT, z4.w * invT)));
+      }
+    }
+    const float r = block_max(m);
+    if (tid == 0) {
+      xchg.zmax = r;
+      xchg.err = s_err;
+    }
+  }
+  cluster_sync();  // #1
+  float M = -INFINITY;
+  for (uint32_t q = 0; q < C; ++q) M = fmaxf(M, dsmem_ld_f32(dsmem_map(smem_addr(&xchg.zmax), q)));
+  RowConsts rc;
+  rc.invT = invT;
+  rc.etaT = p.eta * p.T;
+  rc.ML = isfinite(M) ? M * kLog2e : 0.0f;
+
+  // ---------------------------------------------------------------- sweep 2: sum of exp, sum of q
+  {
+    float e0 = 0.f, e1 = 0.f, q0 = 0.f, q1 = 0.f;
+    for (int vi = tid; vi < nvec; vi += nthr) {
+      const float4 z4 = reinterpret_cast<const float4*>(zst)[vi];
+      const float4 q4 = reinterpret_cast<const float4*>(qst)[vi];
+      e0 += ex2_approx(fmaf(z4.x * invT, kLog2e, -rc.ML)) + ex2_approx(fmaf(z4.z * invT, kLog2e, -rc.ML));
+      e1 += ex2_approx(fmaf(z4.y * invT, kLog2e, -rc.ML)) + ex2_approx(fmaf(z4.w * invT, kLog2e, -rc.ML));
+      q0 += q4.x + q4.z;
+      q1 += q4.y + q4.w;
+    }
+    double se = 0, sq = 0;
+    block_sum2(double(e0) + double(e1), double(q0) + double(q1), se, sq);
+    if (tid == 0) {
+      xchg.sum_e = se;
+      xchg.sum_q = sq;
+    }
+  }
+  cluster_sync();  // #2
+  double Se = 0.0, Sq = 0.0;
+  for (uint32_t q = 0; q < C; ++q) {
+    Se += dsmem_ld_f64(dsmem_map(smem_addr(&xchg.sum_e), q));
+    Sq += dsmem_ld_f64(dsmem_map(smem_addr(&xchg.sum_q), q));
+  }
+  const bool finite = isfinite(M) && isfinite(Se) && Se > 0.0 && isfinite(Sq);
+  rc.inv_sum = finite ? float(1.0 / Se) : 0.0f;
+  rc.zhmax = 0.f;
+  rc.thr = 0.f;
+  rc.head_scale = 0.f;
+
+  // ---------------------------------------------------------------- sweep 3: max of zhat/T
+  {
+    float m = -INFINITY;
+    if (finite) {
+      for (int vi = tid; vi < nvec; vi += nthr) {
+        const float4 z4 = reinterpret_cast<const float4*>(zst)[vi];
+        const float4 q4 = reinterpret_cast<const float4*>(qst)[vi];
+        const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
+        const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float pk = ex2_approx(fmaf(zz[e] * invT, kLog2e, -rc.ML)) * rc.inv_sum;
+          m = fmaxf(m, fmaf(rc.etaT, qq[e] - pk, zz[e]) * invT);
+        }
+      }
+    }
+    const float r = block_max(m);
+    if (tid == 0) xchg.zhmax = r;
+  }
+  cluster_sync();  // #3
+  {
+    float mh = -INFINITY;
+    for (uint32_t q = 0; q < C; ++q) mh = fmaxf(mh, dsmem_ld_f32(dsmem_map(smem_addr(&xchg.zhmax), q)));
+    rc.zhmax = mh;
+    rc.thr = mh + p.ln_tail_frac;
+  }
+
+  // ---------------------------------------------------------------- sweep 4: head sums
+  {
+    float hp0 = 0.f, he0 = 0.f;
+    if (finite) {
+      for (int vi = tid; vi < nvec; vi += nthr) {
+        const float4 z4 = reinterpret_cast<const float4*>(zst)[vi];
+        const float4 q4 = reinterpret_cast<const float4*>(qst)[vi];
+        const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
+        const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float pk = ex2_approx(fmaf(zz[e] * invT, kLog2e, -rc.ML)) * rc.inv_sum;
+          const float zhs = fmaf(rc.etaT, qq[e] - pk, zz[e]) * invT;
+          if (zhs >= rc.thr) {
+            hp0 += pk;
+            he0 += ex2_approx((zhs - rc.zhmax) * kLog2e);
+          }
+        }
+      }
+    }
+    double hp = 0, he = 0;
+    block_sum2(double(hp0), double(he0), hp, he);
+    if (tid == 0) {
+      xchg.head_p = hp;
+      xchg.head_e = he;
+      xchg.err = s_err;
+    }
+  }
+  cluster_sync();  // #4
+
+  // ---------------------------------------------------------------- row finalisation (CTA 0)
+  if (rank == 0 && tid == 0) {
+    double Hp = 0.0, He = 0.0;
+    uint32_t err = 0;
+    for (uint32_t q = 0; q < C; ++q) {
+      Hp += dsmem_ld_f64(dsmem_map(smem_addr(&xchg.head_p), q));
+      He += dsmem_ld_f64(dsmem_map(smem_addr(&xchg.head_e), q));
+      err |= dsmem_ld_u32(dsmem_map(smem_addr(&xchg.err), q));
+    }
+    rc.head_scale = (He > 0.0) ? float(Hp / He) : 0.0f;
+    uint32_t bits = 0;
+    if (!finite) bits |= kBitNonfinite;
+    if (err) bits |= kBitTimeout;
+    if (pos < G) {
+      const int d = p.draft_ids[size_t(req) * G + pos];
+      if (d < 0 || d >= V) {
+        bits |= kBitBadDraft;
+      } else if (finite) {
+        const uint32_t owner = uint32_t(d / p.n_slice);
+        const int off = d - int(owner) * p.n_slice;
+        const float zd = dsmem_ld_f32(dsmem_map(smem_addr(zst + off), owner));
+        const float qd = dsmem_ld_f32(dsmem_map(smem_addr(qst + off), owner));
+        float pd, zhsd, protd;
+        rapid_entry(zd, qd, rc, pd, zhsd, protd);
+        const Philox4 r4 = philox4x32_10(0u, uint32_t(pos), uint32_t(req), 0u + 4u * p.offset, p.seed_lo, p.seed_hi);
+        const float u = uniform_from_word(r4.v[0]);
+        if (u * qd < protd) bits |= kBitAccept;
+      }
+    }
+    RapidRecord rec;
+    rec.zs_max = M;
+    rec.inv_sum = rc.inv_sum;
+    rec.zhat_max = rc.zhmax;
+    rec.head_scale = rc.head_scale;
+    rec.bits = bits;
+    rec.pad[0] = rec.pad[1] = rec.pad[2] = 0;
+    p.records[row] = rec;
+    __threadfence();
+    const uint32_t ticket = atomicAdd(&p.tickets[req], 1u);
+    if (ticket == uint32_t(G)) {
+      __threadfence();
+      const volatile RapidRecord* recs = p.records + size_t(req) * R1;
+      uint32_t any = 0;
+      for (int i = 0; i < R1; ++i) any |= recs[i].bits;
+      const uint32_t status = ((any & kBitNonfinite) ? 1u : 0u) | ((any & kBitBadDraft) ? 2u : 0u) |
+                              ((any & kBitTimeout) ? 4u : 0u);
+      if (status) {
+        p.out_accept_len[req] = 0;
+        for (int i = 0; i < R1; ++i) p.out_tokens[size_t(req) * R1 + i] = -1;
+        p.out_req_status[req] = status;
+        p.tickets[req] = 0u;
+      } else {
+        int n = G;
+        for (int i = 0; i < G; ++i)
+          if (!(recs[i].bits & kBitAccept)) {
+            n = i;
+            break;
+          }
+        const float f0 = recs[n].zs_max, f1 = recs[n].inv_sum, f2 = recs[n].zhat_max, f3 = recs[n].head_scale;
+        for (uint32_t q = 0; q < C; ++q) {
+          dsmem_st_u32(dsmem_map(smem_addr(&xchg.draw_row), q), uint32_t(n));
+          dsmem_st_u32(dsmem_map(smem_addr(&xchg.d_zs_max), q), __float_as_uint(f0));
+          dsmem_st_u32(dsmem_map(smem_addr(&xchg.d_inv_sum), q), __float_as_uint(f1));
+          dsmem_st_u32(dsmem_map(smem_addr(&xchg.d_zhat_max), q), __float_as_uint(f2));
+          dsmem_st_u32(dsmem_map(smem_addr(&xchg.d_head_scale), q), __float_as_uint(f3));
+          dsmem_st_u32(dsmem_map(smem_addr(&xchg.draw_active), q), 1u);
+        }
+      }
+    }
+  }
+  cluster_sync();  // #5: the draw broadcast is visible
+
+  if (xchg.draw_active) {
+    // ---------------------------------------------------------------- residual / bonus draw
+    const int n = xchg.draw_row;
+    const uint32_t stream = (n < G) ? 1u : 2u;
+    RowConsts dc;
+    dc.invT = invT;
+    dc.etaT = p.eta * p.T;
+    dc.ML = isfinite(xchg.d_zs_max) ? xchg.d_zs_max * kLog2e : 0.0f;
+    dc.inv_sum = xchg.d_inv_sum;
+    dc.zhmax = xchg.d_zhat_max;
+    dc.thr = xchg.d_zhat_max + p.ln_tail_frac;
+    dc.head_scale = xchg.d_head_scale;
+    const size_t nbase = (size_t(req) * R1 + n) * size_t(V);
+    int winner = INT_MAX;
+    for (int pass = 0; pass < 2 && winner == INT_MAX; ++pass) {
+      // pass 0: residual (or protected target at the bonus position); pass 1: p, if the residual is all zero
+      float bk = INFINITY;
+      int bidx = INT_MAX;
+      for (int vi = tid; vi < nvec; vi += nthr) {
+        const int kb = v0 + vi * VEC;
+        const Philox4 r4 =
+            philox4x32_10(uint32_t(kb >> 2), uint32_t(n), uint32_t(req), stream + 4u * p.offset, p.seed_lo, p.seed_hi);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          const int k = kb + e;
+          if (k < v0 + len) {
+            const float z = p.z[nbase + k];
+            const float q = p.q[nbase + k];
+            float pk, zhs, prot;
+            rapid_entry(z, q, dc, pk, zhs, prot);
+            float w;
+            if (pass == 1) w = pk;
+            else if (n < G) w = fmaxf(fmaxf(pk - prot, pk - q), 0.0f);
+            else w = prot;
+            if (w > 0.0f) {
+              const float key = -logf(uniform_from_word(r4.v[e])) / w;
+              if (key < bk) {
+                bk = key;
+                bidx = k;
+              }
+            }
+          }
+        }
+      }
+      warp_argmin(bk, bidx);
+      if (lane == 0) {
+        s_wf[warp] = bk;
+        s_wi[warp] = bidx;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        float v = lane < nwarps ? s_wf[lane] : INFINITY;
+        int i = lane < nwarps ? s_wi[lane] : INT_MAX;
+        warp_argmin(v, i);
+        if (lane == 0) {
+          xchg.race_key = v;
+          xchg.race_idx = i;
+        }
+      }
+      cluster_sync();  // #6 (per pass)
+      float gv = INFINITY;
+      int gi = INT_MAX;
+      for (uint32_t q = 0; q < C; ++q)
+        argmin_merge(gv, gi, dsmem_ld_f32(dsmem_map(smem_addr(&xchg.race_key), q)),
+                     dsmem_ld_s32(dsmem_map(smem_addr(&xchg.race_idx), q)));
+      winner = gi;
+      cluster_sync();  // #7 (per pass): the exchange slots may be rewritten
+    }
+    if (rank == 0 && tid == 0) {
+      int32_t* toks = p.out_tokens + size_t(req) * R1;
+      const int32_t* dr = p.draft_ids + size_t(req) * G;
+      for (int i = 0; i < R1; ++i) toks[i] = (i < n) ? dr[i] : (i == n ? (winner == INT_MAX ? 0 : winner) : -1);
+      p.out_accept_len[req] = n;
+      p.out_req_status[req] = 0u;
+      p.tickets[req] = 0u;
+    }
+  }
+
+  if (p.bulk && tid == 0 && s_err) {
+    for (int c = 0; c < kNumChunks; ++c) {
+      const int cv0 = c * chunk_vec;
+      if (min(nvec, cv0 + chunk_vec) <= cv0) break;
+      mbar_wait(smem_addr(&s_bar[c]), 0, kWaitPolls);
+    }
+  }
+  cluster_sync();  // #8: shared memory stays alive until remote reads are done
+}
+
+int rapid_static_smem_bytes() { return int(sizeof(RapidXchg) + 32 * 4 + 32 * 4 + 32 * 2 * 8 + kNumChunks * 8 + 4); }
+
+cudaError_t launch_rapid(const RapidArgs& a, const LaunchPlan& plan, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(rapid_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem);
+  if (e != cudaSuccess) return e;
+  if (plan.cluster > 8) {
+    e = cudaFuncSetAttribute(rapid_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  const int R = a.B * (a.G + 1);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(R) * unsigned(plan.cluster), 1, 1);
+  cfg.blockDim = dim3(unsigned(plan.threads), 1, 1);
+  cfg.dynamicSmemBytes = size_t(plan.smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(plan.cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, rapid_kernel, a);
+}
+
+int rapid_max_active_clusters(const LaunchPlan& plan) {
+  if (cudaFuncSetAttribute(rapid_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem) != cudaSuccess)
+    return 0;
+  if (plan.cluster > 8 &&
+      cudaFuncSetAttribute(rapid_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(plan.cluster), 1, 1);
+  cfg.blockDim = dim3(unsigned(plan.threads), 1, 1);
+  cfg.dynamicSmemBytes = size_t(plan.smem);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(plan.cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, rapid_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
 
 }  // namespace asv

@@ -1,0 +1,107 @@
+"""GPU parity for RAPID: accept lengths and drawn tokens bit-exact against the oracle on the
+same Philox stream (requests the oracle flags within 1e-5 of the tail boundary, the accept
+test or a race tie are counted, not graded), plus the textbook eta = 0 distribution check on
+the library's own draws."""
+import numpy as np
+import pytest
+import scipy.special as sps
+import torch
+from scipy import stats
+
+import gen
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def asv():
+    import speculative_decoding_logit_gb300 as m
+    m.build()
+    return m
+
+
+def _run(asv, z, q, d, T, eta, tail, seed, offset=0):
+    out = asv.rapid_verify(torch.from_numpy(np.ascontiguousarray(z)).cuda(),
+                           torch.from_numpy(np.ascontiguousarray(q)).cuda(),
+                           torch.from_numpy(np.ascontiguousarray(d)).cuda(), T, eta, tail, seed, offset)
+    torch.cuda.synchronize()
+    return out
+
+
+def _compare(out, ref):
+    st = out.req_status.cpu().numpy().astype(np.uint32)
+    np.testing.assert_array_equal(st & 3, ref.flags & 3)
+    acc = out.accept_len.cpu().numpy()
+    tok = out.tokens.cpu().numpy()
+    graded = flagged = 0
+    for r in range(len(acc)):
+        if ref.flags[r] & oracle.FLAGS_UNGRADED:
+            flagged += 1
+            continue
+        graded += 1
+        assert acc[r] == ref.accept_len[r], f"request {r}"
+        np.testing.assert_array_equal(tok[r], ref.tokens[r], err_msg=f"request {r}")
+    return graded, flagged
+
+
+@pytest.mark.parametrize("V", [2, 17, 1000, 4096])
+@pytest.mark.parametrize("G", [0, 1, 10])
+def test_small_shapes(asv, V, G):
+    b = gen.make_rapid_batch(31 + V + G, 16, G, V)
+    for eta in (0.0, 5.0, 20.0):
+        out = _run(asv, b.z, b.q, b.drafts, 1.0, eta, 0.1, 1234)
+        ref = oracle.rapid_verify(b.z, b.q, b.drafts, 1.0, eta, 0.1, 1234)
+        g, f = _compare(out, ref)
+        assert g >= 14
+
+
+def test_temperature_and_offset(asv):
+    b = gen.make_rapid_batch(8, 24, 4, 3000)
+    for T, off in ((0.7, 0), (1.5, 3), (1.0, 17)):
+        out = _run(asv, b.z, b.q, b.drafts, T, 10.0, 0.1, 99, off)
+        ref = oracle.rapid_verify(b.z, b.q, b.drafts, T, 10.0, 0.1, 99, off)
+        _compare(out, ref)
+
+
+def test_rapid_b32_g10_v128256_full(asv):
+    w = gen.WORKLOADS["rapid_b32_g10_v128256_f32"]
+    b = gen.make_rapid_batch(w.seed, w.B, w.K, w.V)
+    tot = 0
+    for eta in w.params["etas"]:
+        out = _run(asv, b.z, b.q, b.drafts, w.params["T"], eta, w.params["tail_frac"], w.params["philox_seed"])
+        ref = oracle.rapid_verify(b.z, b.q, b.drafts, w.params["T"], eta, w.params["tail_frac"],
+                                  w.params["philox_seed"])
+        g, f = _compare(out, ref)
+        tot += g
+        assert f <= 2
+    assert tot >= 4 * 30
+
+
+def test_eta_zero_first_token_is_target_distributed(asv):
+    rng = np.random.default_rng(21)
+    V, B = 12, 20000
+    z = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    q = sps.softmax(z.astype(np.float64) + rng.standard_normal(V)).astype(np.float32)
+    qd = q.astype(np.float64) / q.astype(np.float64).sum()
+    zz = np.broadcast_to(z, (B, 2, V)).copy()
+    qq = np.broadcast_to(q, (B, 2, V)).copy()
+    d = rng.choice(V, size=(B, 1), p=qd).astype(np.int32)
+    out = _run(asv, zz, qq, d, 1.0, 0.0, 0.1, 4321)
+    first = out.tokens.cpu().numpy()[:, 0]
+    p = sps.softmax(z.astype(np.float64))
+    assert stats.chisquare(np.bincount(first, minlength=V), B * p).pvalue > 1e-4
+    ref = oracle.rapid_verify(zz, qq, d, 1.0, 0.0, 0.1, 4321)
+    _compare(out, ref)
+
+
+def test_nonfinite_and_bad_drafts(asv):
+    b = gen.make_rapid_batch(3, 4, 2, 256)
+    z, q, d = b.z.copy(), b.q.copy(), b.drafts.copy()
+    z[1, 1, 5] = np.nan
+    q[2, 0, 9] = np.inf
+    d[3, 0] = -1
+    out = _run(asv, z, q, d, 1.0, 5.0, 0.1, 7)
+    assert list(out.req_status.cpu().numpy()) == [0, 1, 1, 2]
+    ref = oracle.rapid_verify(z, q, d, 1.0, 5.0, 0.1, 7)
+    _compare(out, ref)
