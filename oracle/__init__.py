@@ -75,6 +75,11 @@ def _declare(L):
     L.oracle_asymspec_verify.argtypes = [_vp, _vp, _vp, C.c_int, _i32p, C.c_int, C.c_int, C.c_int, C.c_float,
                                          C.c_float, _i32p, _i32p, _f64p, _f64p, _f64p, _i32p, _u32p]
     L.oracle_asymspec_verify.restype = None
+    L.oracle_asymspec_verify_src.argtypes = [_vp, _vp, _vp, C.c_int, _i32p, C.c_int, C.c_int, C.c_int, C.c_float,
+                                             C.c_float, C.c_int, _i32p, _i32p, _f64p, _f64p, _f64p, _i32p, _u32p]
+    L.oracle_asymspec_verify_src.restype = None
+    L.oracle_fused_argmax_src.argtypes = [_vp, _vp, _vp, C.c_int, C.c_size_t, C.c_int, C.c_float, C.c_int]
+    L.oracle_fused_argmax_src.restype = C.c_int
     L.oracle_philox4x32_10.argtypes = [_u32p, _u32p, _u32p]
     L.oracle_philox4x32_10.restype = None
     L.oracle_uniform_from_word.argtypes = [C.c_uint32]
@@ -152,7 +157,18 @@ class AsymSpecResult:
     flags: np.ndarray        # [B] uint32
 
 
-def asymspec_verify(a, b, t, draft_ids, beta: float, gamma: float) -> AsymSpecResult:
+DELTA_A_MINUS_B = 0
+DELTA_A = 1
+DELTA_T_MINUS_B = 2
+
+
+def fused_argmax_src(a, b, t, beta: float, delta_source: int) -> int:
+    a, b, t = _c(a), _c(b), _c(t)
+    return lib().oracle_fused_argmax_src(a.ctypes.data, b.ctypes.data, t.ctypes.data, _elem_dtype(a), 0, a.size,
+                                         beta, delta_source)
+
+
+def asymspec_verify(a, b, t, draft_ids, beta: float, gamma: float, delta_source: int = 0) -> AsymSpecResult:
     a, b, t = _c(a), _c(b), _c(t)
     B, R, V = a.shape
     K = R - 1
@@ -160,8 +176,9 @@ def asymspec_verify(a, b, t, draft_ids, beta: float, gamma: float) -> AsymSpecRe
     out = AsymSpecResult(np.zeros(B, np.int32), np.zeros((B, R), np.int32), np.zeros((B, R)),
                          np.zeros((B, R, 3)), np.zeros((B, max(K, 0))), np.zeros((B, R), np.int32),
                          np.zeros(B, np.uint32))
-    lib().oracle_asymspec_verify(a.ctypes.data, b.ctypes.data, t.ctypes.data, _elem_dtype(a), _p(d, C.c_int32),
-                                 B, K, V, beta, gamma, _p(out.accept_len, C.c_int32), _p(out.tokens, C.c_int32),
+    lib().oracle_asymspec_verify_src(a.ctypes.data, b.ctypes.data, t.ctypes.data, _elem_dtype(a), _p(d, C.c_int32),
+                                 B, K, V, beta, gamma, delta_source, _p(out.accept_len, C.c_int32),
+                                 _p(out.tokens, C.c_int32),
                                  _p(out.D, C.c_double), _p(out.lse, C.c_double), _p(out.margin, C.c_double),
                                  _p(out.argmax, C.c_int32), _p(out.flags, C.c_uint32))
     return out

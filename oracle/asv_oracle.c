@@ -136,6 +136,28 @@ int oracle_fused_argmax(const void* a, const void* b, const void* t, int dtype, 
   return best < 0 ? 0 : best;
 }
 
+/* The same argmax with the context-gain signal chosen by `delta_source`
+ * ([ASYM] sec. 5, mechanism ablation): 0 -> delta = a - b (the method), 1 -> delta = a
+ * (raw enhanced logits), 2 -> delta = t - b (two-model difference).  The delta is one
+ * rounded fp32 operation (none for source 1), then one fused multiply-add. */
+int oracle_fused_argmax_src(const void* a, const void* b, const void* t, int dtype, size_t off, int V, float beta,
+                            int delta_source) {
+  int best = -1;
+  float bv = -INFINITY;
+  for (int k = 0; k < V; ++k) {
+    float ak = widen_f(a, dtype, off + (size_t)k);
+    float bk = widen_f(b, dtype, off + (size_t)k);
+    float tk = widen_f(t, dtype, off + (size_t)k);
+    float d = delta_source == 1 ? ak : (delta_source == 2 ? tk - bk : ak - bk);
+    float s = fmaf(beta, d, tk);
+    if (s > bv) {
+      bv = s;
+      best = k;
+    }
+  }
+  return best < 0 ? 0 : best;
+}
+
 /* Same score in double, for the informational count of rows where fp32 and
  * fp64 scores disagree on the winner. */
 int oracle_fused_argmax_f64(const void* a, const void* b, const void* t, int dtype, size_t off, int V,
@@ -169,10 +191,10 @@ int oracle_fused_argmax_f64(const void* a, const void* b, const void* t, int dty
  *   out_flags [B].  A request with a non-finite row or an out-of-range draft id
  *   gets accept_len 0 and tokens all -1.
  */
-void oracle_asymspec_verify(const void* a, const void* b, const void* t, int dtype,
-                            const int32_t* draft_ids, int B, int K, int V, float beta, float gamma,
-                            int32_t* out_accept_len, int32_t* out_tokens, double* out_D, double* out_lse,
-                            double* out_margin, int32_t* out_argmax, uint32_t* out_flags) {
+void oracle_asymspec_verify_src(const void* a, const void* b, const void* t, int dtype,
+                                const int32_t* draft_ids, int B, int K, int V, float beta, float gamma,
+                                int delta_source, int32_t* out_accept_len, int32_t* out_tokens, double* out_D,
+                                double* out_lse, double* out_margin, int32_t* out_argmax, uint32_t* out_flags) {
   const double ln_gamma = log((double)gamma);
   for (int r = 0; r < B; ++r) {
     uint32_t flags = 0;
@@ -191,7 +213,7 @@ void oracle_asymspec_verify(const void* a, const void* b, const void* t, int dty
       double Lb = oracle_lse(b, dtype, off, V, 1.0);
       double Lt = oracle_lse(t, dtype, off, V, 1.0);
       double D = oracle_jsd(a, b, dtype, off, off, V);
-      int c = oracle_fused_argmax(a, b, t, dtype, off, V, beta);
+      int c = oracle_fused_argmax_src(a, b, t, dtype, off, V, beta, delta_source);
       cbest[i] = c;
       size_t ri = (size_t)r * (K + 1) + i;
       if (out_D) out_D[ri] = D;
@@ -237,6 +259,14 @@ void oracle_asymspec_verify(const void* a, const void* b, const void* t, int dty
     free(margin);
     free(cbest);
   }
+}
+
+void oracle_asymspec_verify(const void* a, const void* b, const void* t, int dtype, const int32_t* draft_ids, int B,
+                            int K, int V, float beta, float gamma, int32_t* out_accept_len, int32_t* out_tokens,
+                            double* out_D, double* out_lse, double* out_margin, int32_t* out_argmax,
+                            uint32_t* out_flags) {
+  oracle_asymspec_verify_src(a, b, t, dtype, draft_ids, B, K, V, beta, gamma, 0, out_accept_len, out_tokens, out_D,
+                             out_lse, out_margin, out_argmax, out_flags);
 }
 
 /* ------------------------------------------------------------------ Philox */

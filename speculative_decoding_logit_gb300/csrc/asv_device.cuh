@@ -166,6 +166,12 @@ struct Elem<float> {
     x[2] = v.z;
     x[3] = v.w;
   }
+  static constexpr int kPairs = 2;
+  __device__ static __forceinline__ void load_pairs(const float* s, int vi, float2 (&x)[2]) {
+    const float4 v = reinterpret_cast<const float4*>(s)[vi];
+    x[0] = make_float2(v.x, v.y);
+    x[1] = make_float2(v.z, v.w);
+  }
   __device__ static __forceinline__ float to_float(float v) { return v; }
   __device__ static __forceinline__ float neg_inf() { return __uint_as_float(0xff800000u); }
   __device__ static __forceinline__ float from_smem_remote(uint32_t a) { return dsmem_ld_f32(a); }
@@ -185,6 +191,14 @@ struct Elem<bf16_t> {
     x[5] = bf16_hi(v.z);
     x[6] = bf16_lo(v.w);
     x[7] = bf16_hi(v.w);
+  }
+  static constexpr int kPairs = 4;
+  __device__ static __forceinline__ void load_pairs(const uint16_t* s, int vi, float2 (&x)[4]) {
+    const uint4 v = reinterpret_cast<const uint4*>(s)[vi];
+    x[0] = make_float2(bf16_lo(v.x), bf16_hi(v.x));
+    x[1] = make_float2(bf16_lo(v.y), bf16_hi(v.y));
+    x[2] = make_float2(bf16_lo(v.z), bf16_hi(v.z));
+    x[3] = make_float2(bf16_lo(v.w), bf16_hi(v.w));
   }
   __device__ static __forceinline__ float to_float(uint16_t v) { return __uint_as_float(uint32_t(v) << 16); }
   __device__ static __forceinline__ uint16_t neg_inf() { return uint16_t(0xff80u); }
@@ -294,6 +308,60 @@ __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint3
 // Uniform in (0, 1) from a 32-bit word: ((w >> 9) + 0.5) * 2^-23, exact in fp32.
 __device__ __forceinline__ float uniform_from_word(uint32_t w) {
   return (float(w >> 9) + 0.5f) * 1.1920928955078125e-7f;
+}
+
+}  // namespace asv
+
+namespace asv {
+
+// ------------------------------------------------------------------ packed arithmetic
+// Two fp32 lanes per instruction (sm_100+ f32x2 forms) and bf16x2 maxima on raw bit patterns.
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
+      " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// Lane-wise maximum of two bf16x2 words (exact; a NaN lane yields the other operand).
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+}  // namespace asv
+
+namespace asv {
+
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " sub.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
 }
 
 }  // namespace asv

@@ -34,6 +34,8 @@
 // give exactly 0.
 #include <cfloat>
 #include <climits>
+#include <cstdlib>
+#include <type_traits>
 
 #include "asv_device.cuh"
 #include "asv_internal.h"
@@ -48,6 +50,8 @@ struct __align__(16) JsdXchg {
   uint32_t err;      // staged-data wait expired in this CTA
   double sum[3];     // sums of ex2(fma(x, log2e, -M*log2e)) over the slice
   double jsd[2];     // divergence partial sums (p-form, q-form)
+  float argv2;       // lean variant: argmax partials exchanged after the second sweep
+  int32_t argi2;
 };
 
 template <int MODE>
@@ -80,7 +84,9 @@ __device__ __forceinline__ void jsd_entry(float xa, float xb, float dL, float Ma
   else acc_q += v;
 }
 
-template <typename T, int MODE>
+// Lean variant of the sweeps: maxima on raw data in sweep 1 (bf16x2 maxima), the argmax folded
+// into sweep 2 with one comparison per 16-byte vector, and packed two-lane fp32 arithmetic.
+template <typename T, int MODE, bool LEAN>
 __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
   using E = Elem<T>;
   using S = typename E::storage;
@@ -163,26 +169,63 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
   for (int j = 0; j < NT; ++j) mx[j] = -INFINITY;
   float bv = -INFINITY;
   int bi = INT_MAX;
-  for (int c = 0; c < kNumChunks; ++c) {
-    const int cv0 = c * chunk_vec;
-    const int cv1 = min(nvec, cv0 + chunk_vec);
-    if (cv1 <= cv0) break;
-    if (p.bulk && !mbar_wait(smem_addr(&s_bar[c]), 0, kWaitPolls)) atomicOr(&s_err, 1u);
-    for (int vi = cv0 + tid; vi < cv1; vi += nthr) {
-      float x[NT][VEC];
+  if constexpr (LEAN) {
+    if constexpr (std::is_same<T, bf16_t>::value) {
+      uint32_t m2[NT];
 #pragma unroll
-      for (int j = 0; j < NT; ++j) E::load_vec(stage[j], vi, x[j]);
-      const int k0 = v0 + vi * VEC;
+      for (int j = 0; j < NT; ++j) m2[j] = 0xff80ff80u;
+      for (int c = 0; c < kNumChunks; ++c) {
+        const int cv0 = c * chunk_vec;
+        const int cv1 = min(nvec, cv0 + chunk_vec);
+        if (cv1 <= cv0) break;
+        if (p.bulk && !mbar_wait(smem_addr(&s_bar[c]), 0, kWaitPolls)) atomicOr(&s_err, 1u);
+        for (int vi = cv0 + tid; vi < cv1; vi += nthr) {
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
+          for (int j = 0; j < NT; ++j) {
+            const uint4 w = reinterpret_cast<const uint4*>(stage[j])[vi];
+            m2[j] = bmax2(bmax2(m2[j], w.x), bmax2(w.y, bmax2(w.z, w.w)));
+          }
+        }
+      }
 #pragma unroll
-        for (int j = 0; j < NT; ++j) mx[j] = fmaxf(mx[j], x[j][e]);
-        float s;
-        if (MODE == kModeAsym) s = fmaf(p.beta, x[0][e] - x[1][e], x[2][e]);
-        else s = x[TGT][e];
-        if (s > bv) {
-          bv = s;
-          bi = k0 + e;
+      for (int j = 0; j < NT; ++j) mx[j] = fmaxf(bf16_lo(m2[j]), bf16_hi(m2[j]));
+    } else {
+      for (int c = 0; c < kNumChunks; ++c) {
+        const int cv0 = c * chunk_vec;
+        const int cv1 = min(nvec, cv0 + chunk_vec);
+        if (cv1 <= cv0) break;
+        if (p.bulk && !mbar_wait(smem_addr(&s_bar[c]), 0, kWaitPolls)) atomicOr(&s_err, 1u);
+        for (int vi = cv0 + tid; vi < cv1; vi += nthr) {
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            const float4 v = reinterpret_cast<const float4*>(stage[j])[vi];
+            mx[j] = fmaxf(fmaxf(mx[j], v.x), fmaxf(v.y, fmaxf(v.z, v.w)));
+          }
+        }
+      }
+    }
+  } else {
+    for (int c = 0; c < kNumChunks; ++c) {
+      const int cv0 = c * chunk_vec;
+      const int cv1 = min(nvec, cv0 + chunk_vec);
+      if (cv1 <= cv0) break;
+      if (p.bulk && !mbar_wait(smem_addr(&s_bar[c]), 0, kWaitPolls)) atomicOr(&s_err, 1u);
+      for (int vi = cv0 + tid; vi < cv1; vi += nthr) {
+        float x[NT][VEC];
+  #pragma unroll
+        for (int j = 0; j < NT; ++j) E::load_vec(stage[j], vi, x[j]);
+        const int k0 = v0 + vi * VEC;
+  #pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+  #pragma unroll
+          for (int j = 0; j < NT; ++j) mx[j] = fmaxf(mx[j], x[j][e]);
+          float s;
+          if (MODE == kModeAsym) s = fmaf(p.beta, x[0][e] - x[1][e], x[2][e]);
+          else s = x[TGT][e];
+          if (s > bv) {
+            bv = s;
+            bi = k0 + e;
+          }
         }
       }
     }
@@ -237,21 +280,80 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
   float ML[NT];
 #pragma unroll
   for (int j = 0; j < NT; ++j) ML[j] = isfinite(M[j]) ? M[j] * kLog2e : 0.0f;
+  float bv2 = -INFINITY;
+  int bi2 = INT_MAX;
   {
     float s0[NT], s1[NT];
 #pragma unroll
     for (int j = 0; j < NT; ++j) s0[j] = s1[j] = 0.0f;
-    for (int vi = tid; vi < nvec; vi += nthr) {
-      float x[NT][VEC];
+    if constexpr (LEAN) {
+      constexpr int NP = E::kPairs;
+      const float2 l2e2 = make_float2(kLog2e, kLog2e);
+      const float2 beta2 = make_float2(p.beta, p.beta);
+      float2 nml[NT], acc[NT];
 #pragma unroll
-      for (int j = 0; j < NT; ++j) E::load_vec(stage[j], vi, x[j]);
+      for (int j = 0; j < NT; ++j) {
+        nml[j] = make_float2(-ML[j], -ML[j]);
+        acc[j] = make_float2(0.0f, 0.0f);
+      }
+      for (int vi = tid; vi < nvec; vi += nthr) {
+        float2 x[NT][NP];
 #pragma unroll
-      for (int e = 0; e < VEC; e += 2) {
+        for (int j = 0; j < NT; ++j) E::load_pairs(stage[j], vi, x[j]);
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          s0[j] += ex2_approx(fmaf(x[j][e], kLog2e, -ML[j]));
-          s1[j] += ex2_approx(fmaf(x[j][e + 1], kLog2e, -ML[j]));
+        for (int q2 = 0; q2 < NP; ++q2) {
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            const float2 y = ffma2(x[j][q2], l2e2, nml[j]);
+            acc[j] = fadd2(acc[j], make_float2(ex2_approx(y.x), ex2_approx(y.y)));
+          }
         }
+        // verifier score of the vector's entries; one comparison per vector against the best so far
+        float2 sc[NP];
+#pragma unroll
+        for (int q2 = 0; q2 < NP; ++q2) {
+          if (MODE == kModeAsym) sc[q2] = ffma2(beta2, fsub2(x[0][q2], x[1][q2]), x[2][q2]);
+          else sc[q2] = x[TGT][q2];
+        }
+        float vm = fmaxf(sc[0].x, sc[0].y);
+#pragma unroll
+        for (int q2 = 1; q2 < NP; ++q2) vm = fmaxf(vm, fmaxf(sc[q2].x, sc[q2].y));
+        if (vm > bv2) {
+          int e_first = 2 * NP - 1;
+#pragma unroll
+          for (int q2 = NP - 1; q2 >= 0; --q2) {
+            if (sc[q2].y == vm) e_first = 2 * q2 + 1;
+            if (sc[q2].x == vm) e_first = 2 * q2;
+          }
+          bv2 = vm;
+          bi2 = v0 + vi * VEC + e_first;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        s0[j] = acc[j].x;
+        s1[j] = acc[j].y;
+      }
+    } else {
+      for (int vi = tid; vi < nvec; vi += nthr) {
+        float x[NT][VEC];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) E::load_vec(stage[j], vi, x[j]);
+#pragma unroll
+        for (int e = 0; e < VEC; e += 2) {
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            s0[j] += ex2_approx(fmaf(x[j][e], kLog2e, -ML[j]));
+            s1[j] += ex2_approx(fmaf(x[j][e + 1], kLog2e, -ML[j]));
+          }
+        }
+      }
+    }
+    if constexpr (LEAN) {
+      warp_argmax(bv2, bi2);
+      if (lane == 0) {
+        s_wf[warp][3] = bv2;
+        s_wi[warp] = bi2;
       }
     }
     double d[NT];
@@ -269,9 +371,24 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
         v = warp_sum(v);
         if (lane == 0) xchg.sum[j] = v;
       }
+      if constexpr (LEAN) {
+        float v2 = (lane < nwarps) ? s_wf[lane][3] : -INFINITY;
+        int i2 = (lane < nwarps) ? s_wi[lane] : INT_MAX;
+        warp_argmax(v2, i2);
+        if (lane == 0) {
+          xchg.argv2 = v2;
+          xchg.argi2 = i2;
+        }
+      }
     }
   }
   cluster_sync();  // #2
+  if constexpr (LEAN) {
+    const uint32_t base_v = smem_addr(&xchg.argv2);
+    const uint32_t base_i = smem_addr(&xchg.argi2);
+    for (uint32_t q = 0; q < C; ++q)
+      argmax_merge(rowv, rowi, dsmem_ld_f32(dsmem_map(base_v, q)), dsmem_ld_s32(dsmem_map(base_i, q)));
+  }
 
   double Ssum[NT];
 #pragma unroll
@@ -298,14 +415,41 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
     const float dL = finite ? float(lse[1] - lse[0]) : 0.0f;
     float ap0 = 0.0f, ap1 = 0.0f, aq0 = 0.0f, aq1 = 0.0f;
     if (finite) {
-      for (int vi = tid; vi < nvec; vi += nthr) {
-        float xa[VEC], xb[VEC];
-        E::load_vec(stage[0], vi, xa);
-        E::load_vec(stage[1], vi, xb);
+      if constexpr (LEAN && !JsdTraits<MODE>::kWide) {
+        constexpr int NP = E::kPairs;
+        const float2 l2e2 = make_float2(kLog2e, kLog2e);
+        const float2 dl2 = make_float2(dL, dL);
+        const float2 nmal = make_float2(-ML[0], -ML[0]);
+        float2 accp = make_float2(0.0f, 0.0f);
+        for (int vi = tid; vi < nvec; vi += nthr) {
+          float2 xa[NP], xb[NP];
+          E::load_pairs(stage[0], vi, xa);
+          E::load_pairs(stage[1], vi, xb);
 #pragma unroll
-        for (int e = 0; e < VEC; e += 2) {
-          jsd_entry<JsdTraits<MODE>::kWide>(xa[e], xb[e], dL, ML[0], ML[1], ap0, aq0);
-          jsd_entry<JsdTraits<MODE>::kWide>(xa[e + 1], xb[e + 1], dL, ML[0], ML[1], ap1, aq1);
+          for (int q2 = 0; q2 < NP; ++q2) {
+            const float2 u = fsub2(fsub2(xb[q2], xa[q2]), dl2);
+            if (fabsf(u.x) <= ASV_JSD_POLY_U0 && fabsf(u.y) <= ASV_JSD_POLY_U0) {
+              const float2 y = ffma2(xa[q2], l2e2, nmal);
+              const float2 ep = make_float2(ex2_approx(y.x), ex2_approx(y.y));
+              accp = ffma2(fmul2(ep, fmul2(u, u)), asv_jsd_poly2(u), accp);
+            } else {
+              jsd_entry<false>(xa[q2].x, xb[q2].x, dL, ML[0], ML[1], ap0, aq0);
+              jsd_entry<false>(xa[q2].y, xb[q2].y, dL, ML[0], ML[1], ap1, aq1);
+            }
+          }
+        }
+        ap0 += accp.x;
+        ap1 += accp.y;
+      } else {
+        for (int vi = tid; vi < nvec; vi += nthr) {
+          float xa[VEC], xb[VEC];
+          E::load_vec(stage[0], vi, xa);
+          E::load_vec(stage[1], vi, xb);
+#pragma unroll
+          for (int e = 0; e < VEC; e += 2) {
+            jsd_entry<JsdTraits<MODE>::kWide>(xa[e], xb[e], dL, ML[0], ML[1], ap0, aq0);
+            jsd_entry<JsdTraits<MODE>::kWide>(xa[e + 1], xb[e + 1], dL, ML[0], ML[1], ap1, aq1);
+          }
         }
       }
     }
@@ -438,9 +582,17 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
 
 int jsd_static_smem_bytes() { return int(sizeof(JsdXchg) + 32 * 4 * 4 + 32 * 4 + 32 * 3 * 8 + kNumChunks * 8 + 4); }
 
+static bool lean_variant() {
+  static const bool v = [] {
+    const char* e = std::getenv("ASV_JSD_VARIANT");
+    return !(e && e[0] == '0');
+  }();
+  return v;
+}
+
 template <typename T, int MODE>
 static cudaError_t launch_one(const JsdArgs& a, const LaunchPlan& plan, cudaStream_t s) {
-  auto kern = jsd_family_kernel<T, MODE>;
+  auto kern = lean_variant() ? jsd_family_kernel<T, MODE, true> : jsd_family_kernel<T, MODE, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem);
   if (e != cudaSuccess) return e;
   if (plan.cluster > 8) {
@@ -465,7 +617,7 @@ static cudaError_t launch_one(const JsdArgs& a, const LaunchPlan& plan, cudaStre
 
 template <typename T, int MODE>
 static int max_clusters_one(const LaunchPlan& plan) {
-  auto kern = jsd_family_kernel<T, MODE>;
+  auto kern = lean_variant() ? jsd_family_kernel<T, MODE, true> : jsd_family_kernel<T, MODE, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem) != cudaSuccess) return 0;
   if (plan.cluster > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
     return 0;

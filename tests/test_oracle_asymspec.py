@@ -237,3 +237,20 @@ def test_gate_is_strict():
     r = oracle.asymspec_verify(a, a, a, d, 1.0, 1.0)
     assert r.margin[0, 0] == 0.0 and r.accept_len[0] == 0
     assert r.flags[0] & oracle.FLAG_NEAR_MARGIN
+
+
+@pytest.mark.parametrize("src", [0, 1, 2])
+def test_delta_source_ablation_argmax(src):
+    """ASYM sec. 5 ablation: delta := a - b (method), a (raw), t - b (two-model difference);
+    checked against numpy argmax of the fp32 score."""
+    rng = np.random.default_rng(30 + src)
+    for dtype in (gen.F32, gen.BF16):
+        for beta in (0.0, 1.0, 2.0):
+            a, b, t = _rows(rng, 3, 3001, dtype)
+            af, bf, tf = (gen.widen(x, dtype) for x in (a, b, t))
+            d = {0: (af - bf), 1: af, 2: (tf - bf)}[src].astype(np.float32)
+            s = (np.float64(np.float32(beta)) * d.astype(np.float64) + tf.astype(np.float64)).astype(np.float32)
+            assert oracle.fused_argmax_src(a, b, t, beta, src) == int(np.argmax(s))
+    # the default source is the method's a - b
+    a, b, t = _rows(rng, 3, 500, gen.F32)
+    assert oracle.fused_argmax_src(a, b, t, 1.0, 0) == oracle.fused_argmax(a, b, t, 1.0)
