@@ -159,11 +159,10 @@ def run_reference(args):
 
 
 def run_ours(args):
-    import ctypes as C
-
     import torch
 
     import speculative_decoding_logit_gb300 as asv
+    from speculative_decoding_logit_gb300.shard import max_over_ranks
 
     ws, rank, local = _dist()
     if ws > 1:
@@ -233,16 +232,14 @@ def run_ours(args):
         dist.barrier()
     elapsed_ms = e0.elapsed_time(e1)
     launch_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
-    if dist:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(elapsed_ms)
     rows_total = R * args.steps * ws
     value = rows_total / (elapsed_ms / 1e3)
 
     # End to end through the C ABI with host (pinned) buffers: H2D of the step's inputs,
     # the verification, D2H of the step's results, every step.
-    if True:
+    e2e = None
+    if not args.no_e2e:
         pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
         ha, hb, ht = (pin(x.view(np.int16)) for x in (batch.a, batch.b, batch.t))
         hd = pin(batch.drafts)
@@ -265,7 +262,7 @@ def run_ours(args):
             assert hfn(*hcall) == 0
         h1.record(stream)
         torch.cuda.synchronize()
-        e_ms = h0.elapsed_time(h1)
+        e_ms = max_over_ranks(h0.elapsed_time(h1))
         assert np.array_equal(o_tok.numpy(), out.tokens.cpu().numpy())
         h2d = 3 * R * w.V * 2 + w.B * w.K * 4
         d2h = w.B * 4 + R * 4 + R * 4 + w.B * 4
@@ -306,6 +303,7 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch from an ncu capture of the current kernel (else null)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -84,7 +84,7 @@ asv_status asv_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t str
 
 /*
  * Tuning override for the launch plan: cluster size (CTAs per row, 1..16) and
- * threads per CTA (128..1024, multiple of 32).  0 restores the automatic choice.
+ * threads per CTA (128..512, multiple of 32).  0 restores the automatic choice.
  * Applies to later calls from any thread.
  */
 asv_status asv_set_tuning(int cluster_ctas, int threads_per_cta);
@@ -119,6 +119,28 @@ asv_status asymspec_verify(const void* a, const void* b, const void* t, int dtyp
                            int K, int V, float beta, float gamma, int32_t* out_accept_len, int32_t* out_tokens,
                            float* out_D, float* out_lse, uint32_t* out_req_status, void* workspace,
                            size_t ws_bytes, cudaStream_t stream);
+
+/* Context-gain signal used in the delta-fusion score ([ASYM] sec. 5, mechanism ablation). */
+typedef enum {
+  ASV_DELTA_A_MINUS_B = 0, /* delta = a - b: the method (same drafter, two context views) */
+  ASV_DELTA_A = 1,         /* delta = a: the raw full-context drafter logits */
+  ASV_DELTA_T_MINUS_B = 2  /* delta = t - b: a two-model difference on the compressed view */
+} asv_delta_source;
+
+typedef struct {
+  int delta_source; /* asv_delta_source; ASV_DELTA_A_MINUS_B in asymspec_verify */
+} asv_asym_options;
+
+/*
+ * asymspec_verify_ex -- asymspec_verify with options (NULL options = the defaults).  With
+ * delta_source != ASV_DELTA_A_MINUS_B the emitted token is argmax_k (t_k + beta * delta_k) for
+ * the chosen delta, formed the same way (one rounded fp32 operation, then one FMA); the gate,
+ * D and the log-sum-exps are unchanged.  Any other delta_source value is ASV_ERR_PARAM.
+ */
+asv_status asymspec_verify_ex(const void* a, const void* b, const void* t, int dtype, const int32_t* draft_ids,
+                              int B, int K, int V, float beta, float gamma, const asv_asym_options* options,
+                              int32_t* out_accept_len, int32_t* out_tokens, float* out_D, float* out_lse,
+                              uint32_t* out_req_status, void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * asymspec_verify_host -- asymspec_verify over HOST buffers, for callers whose

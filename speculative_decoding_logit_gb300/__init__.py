@@ -20,6 +20,9 @@ from __future__ import annotations
 from ._binding import (  # noqa: F401
     ASV_BF16,
     ASV_F32,
+    DELTA_A,
+    DELTA_A_MINUS_B,
+    DELTA_T_MINUS_B,
     ASV_MODE_ASYMSPEC,
     ASV_MODE_RAPID,
     ASV_MODE_SCI,

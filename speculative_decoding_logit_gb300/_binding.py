@@ -57,6 +57,15 @@ _sz = C.c_size_t
 _f = C.c_float
 
 
+class _AsymOptionsC(C.Structure):
+    _fields_ = [("delta_source", C.c_int)]
+
+
+DELTA_A_MINUS_B = 0
+DELTA_A = 1
+DELTA_T_MINUS_B = 2
+
+
 class _SciParamsC(C.Structure):
     _fields_ = [("T_base", C.c_double), ("alpha_omega", C.c_double), ("tau_credit", C.c_double),
                 ("T_min", C.c_double), ("T_max", C.c_double), ("ewma_beta", C.c_double)]
@@ -77,6 +86,9 @@ def _declare(L):
     L.asv_query_plan.restype = _i
     L.asymspec_verify.argtypes = [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _f, _f, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
     L.asymspec_verify.restype = _i
+    L.asymspec_verify_ex.argtypes = [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _f, _f, C.POINTER(_AsymOptionsC), _vp, _vp,
+                                     _vp, _vp, _vp, _vp, _sz, _vp]
+    L.asymspec_verify_ex.restype = _i
     L.asv_host_arena_bytes.argtypes = [_i, _i, _i, _i]
     L.asv_host_arena_bytes.restype = _sz
     L.asymspec_verify_host.argtypes = [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _f, _f, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
@@ -168,9 +180,11 @@ class AsymSpecOutput:
 
 
 def asymspec_verify(a: torch.Tensor, b: torch.Tensor, t: torch.Tensor, draft_ids: torch.Tensor,
-                    beta: float = 1.0, gamma: float = 0.5, *, out: Optional[AsymSpecOutput] = None,
-                    workspace: Optional[torch.Tensor] = None, stream=None) -> AsymSpecOutput:
-    """AsymSpec verification of a [B, K+1, V] batch (see include/asv.h)."""
+                    beta: float = 1.0, gamma: float = 0.5, *, delta_source: int = DELTA_A_MINUS_B,
+                    out: Optional[AsymSpecOutput] = None, workspace: Optional[torch.Tensor] = None,
+                    stream=None) -> AsymSpecOutput:
+    """AsymSpec verification of a [B, K+1, V] batch (see include/asv.h).  `delta_source`
+    selects the context-gain signal of the delta-fusion score (asymspec_verify_ex)."""
     _need_cuda(a, b, t, draft_ids)
     if a.dim() != 3 or a.shape != b.shape or a.shape != t.shape:
         raise AsvError(2, "a, b, t must share one [B, K+1, V] shape")
@@ -193,10 +207,19 @@ def asymspec_verify(a: torch.Tensor, b: torch.Tensor, t: torch.Tensor, draft_ids
     dt = _dtype_code(a)
     need = workspace_bytes(ASV_MODE_ASYMSPEC, B, K, V, dt)
     ws = workspace if workspace is not None else _workspace(dev, sh, need)
-    st = library().asymspec_verify(_ptr(a), _ptr(b), _ptr(t), dt, _ptr(draft_ids), B, K, V, float(beta),
-                                   float(gamma), _ptr(out.accept_len), _ptr(out.tokens), _ptr(out.D), _ptr(out.lse),
-                                   _ptr(out.req_status), _ptr(ws), ws.numel() * ws.element_size(), sh)
-    _check(st, "asymspec_verify")
+    if delta_source == DELTA_A_MINUS_B:
+        st = library().asymspec_verify(_ptr(a), _ptr(b), _ptr(t), dt, _ptr(draft_ids), B, K, V, float(beta),
+                                       float(gamma), _ptr(out.accept_len), _ptr(out.tokens), _ptr(out.D),
+                                       _ptr(out.lse), _ptr(out.req_status), _ptr(ws), ws.numel() * ws.element_size(),
+                                       sh)
+        _check(st, "asymspec_verify")
+    else:
+        opt = _AsymOptionsC(int(delta_source))
+        st = library().asymspec_verify_ex(_ptr(a), _ptr(b), _ptr(t), dt, _ptr(draft_ids), B, K, V, float(beta),
+                                          float(gamma), C.byref(opt), _ptr(out.accept_len), _ptr(out.tokens),
+                                          _ptr(out.D), _ptr(out.lse), _ptr(out.req_status), _ptr(ws),
+                                          ws.numel() * ws.element_size(), sh)
+        _check(st, "asymspec_verify_ex")
     return out
 
 

@@ -201,6 +201,16 @@ asv_status asymspec_verify(const void* a, const void* b, const void* t, int dtyp
                            int K, int V, float beta, float gamma, int32_t* out_accept_len, int32_t* out_tokens,
                            float* out_D, float* out_lse, uint32_t* out_req_status, void* workspace,
                            size_t ws_bytes, cudaStream_t stream) {
+  return asymspec_verify_ex(a, b, t, dtype, draft_ids, B, K, V, beta, gamma, nullptr, out_accept_len, out_tokens,
+                            out_D, out_lse, out_req_status, workspace, ws_bytes, stream);
+}
+
+asv_status asymspec_verify_ex(const void* a, const void* b, const void* t, int dtype, const int32_t* draft_ids,
+                              int B, int K, int V, float beta, float gamma, const asv_asym_options* options,
+                              int32_t* out_accept_len, int32_t* out_tokens, float* out_D, float* out_lse,
+                              uint32_t* out_req_status, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  const int dsrc = options ? options->delta_source : ASV_DELTA_A_MINUS_B;
+  if (dsrc < ASV_DELTA_A_MINUS_B || dsrc > ASV_DELTA_T_MINUS_B) return ASV_ERR_PARAM;
   if (B < 0 || K < 0 || V < 2) return ASV_ERR_SHAPE;
   if ((long long)B * (K + 1) * asv::kMaxCluster > 0x7fffffffLL) return ASV_ERR_SHAPE;
   if (!valid_dtype(dtype)) return ASV_ERR_DTYPE;
@@ -222,6 +232,7 @@ asv_status asymspec_verify(const void* a, const void* b, const void* t, int dtyp
   args.K = K;
   args.V = V;
   args.beta = beta;
+  args.delta_source = dsrc;
   args.ln_gamma = std::log(double(gamma));
   args.out_accept_len = out_accept_len;
   args.out_tokens = out_tokens;

@@ -51,6 +51,7 @@ struct JsdArgs {
   int n_slice;
   int bulk;
   float beta;
+  int delta_source;  // AsymSpec: 0 a - b, 1 a, 2 t - b
   double ln_gamma;
   // SCI
   double T_base, alpha_omega, tau_credit, T_min, T_max, ewma_beta;

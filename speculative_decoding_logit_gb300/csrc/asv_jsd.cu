@@ -4,29 +4,33 @@
 //   "AsymSpec: Context-Asymmetric Speculative Decoding for Agentic LLMs" (reading notes),
 //     sec. 4.1: context-gain signal delta = a - b and the delta-fusion token argmax(t + beta*delta);
 //     sec. 4.2: D = JSD(softmax a || softmax b), gamma_eff = gamma * exp(-D), accept while
-//     softmax(t)[d] > gamma_eff * softmax(b)[d], emit the delta-fusion token at the first rejection.
+//     softmax(t)[d] > gamma_eff * softmax(b)[d], emit the delta-fusion token at the first rejection;
+//     sec. 5: the delta-source ablation (delta := a, delta := t - b).
 //   "E2-SCI: Elastic Edge-Cloud Speculative Decoding via Credit Inertia" (paper notes), Key design 3:
 //     JSD(draft || target) against a threshold driven by an EWMA of the acceptance rate.
 //
 // Work decomposition.  One row (request r, position i) is V vocabulary entries of each input.  A
 // thread-block cluster of C CTAs owns one row; CTA q of the cluster owns entries
 // [q*n_slice, (q+1)*n_slice).  Each CTA stages its slice of every input in shared memory once (1-D
-// bulk copies in kNumChunks chunks, one mbarrier per chunk, so work starts on the first chunk while
-// the rest is in flight), and the three passes the divergence needs run out of shared memory:
-//   sweep 1: row maxima of every input and the argmax of the verifier score;
-//   sweep 2: sums of exp(x - max) (exponentials on the special-function unit);
+// bulk copies in kNumChunks chunks, one mbarrier each, so work starts on the first chunk while the
+// rest is in flight), and the three passes the divergence needs run out of shared memory:
+//   sweep 1: row maxima of every input (bf16: two-lane bf16 maxima on the raw words);
+//   sweep 2: sums of exp(x - max) on the special-function unit, and the argmax of the verifier
+//            score (one comparison per 16-byte vector against the best so far);
 //   sweep 3: the per-entry Jensen-Shannon terms.
-// Between sweeps the CTAs exchange partial results through distributed shared memory; every CTA
-// combines the partials in rank order, so all CTAs hold bit-identical row statistics.  HBM is read
-// exactly once per input byte.  CTA 0 finalises the row (gate, outputs, a 16-byte row record) and
-// takes a ticket on the request's counter; the last of the K+1 rows to finish runs the left-to-right
-// scan for its request and resets the counter, so the whole step is one launch with no spin-waits.
+// Arithmetic on entries is two-lane packed fp32 (fma/add/mul .f32x2) where it pairs up.  After each
+// sweep: warp shuffles in fp32, per-warp partials combined in fp64 by one thread, a cluster exchange
+// through distributed shared memory, and one warp that combines the C partials in rank order and
+// broadcasts the row constants, so every CTA holds bit-identical row statistics.  fp64 is used only
+// by single threads: this GPU's fp64 rate is a small fraction of its fp32 rate.  HBM is read exactly
+// once per input byte.  CTA 0 finalises the row (gate, outputs, a 16-byte row record) and takes a
+// ticket on the request's counter; the last of the K+1 rows to finish runs the left-to-right scan
+// and resets the counter, so the whole step is one launch with no spin-waits.
 //
 // Numerics.  Inputs are widened exactly to fp32.  exp(x - M) is formed as ex2(fma(x, log2e, -M*log2e)),
-// whose constant rounding error c is known exactly and removed from the log-sum-exp in double; the
-// divergence sums use the same form, so the factor cancels in their ratio with the row sums.
-// Per-thread partial sums are fp32 (two accumulators), combined across the CTA and cluster in fp64.
-// The gate is decided in double in the log domain.  The per-entry divergence term is evaluated from
+// whose constant rounding error c is known exactly and removed from the log-sum-exp; the divergence
+// sums use the same form, so the factor cancels in their ratio with the row sums.  The gate is
+// decided in double in the log domain.  The per-entry divergence term is evaluated from
 // u = (xb - xa) - (lse_b - lse_a):
 //   narrow form (|u| <= 2, AsymSpec's pair): p * u^2 * P(u), P a fitted polynomial;
 //   wide form (any u): max(p,q) * (A(r) - |u| r), r = exp(-|u|), A(r) = (1-r) B(r).
@@ -34,7 +38,6 @@
 // give exactly 0.
 #include <cfloat>
 #include <climits>
-#include <cstdlib>
 #include <type_traits>
 
 #include "asv_device.cuh"
@@ -44,14 +47,24 @@
 namespace asv {
 
 struct __align__(16) JsdXchg {
-  float mx[3];       // row-slice maxima of the inputs
-  float argv;        // best verifier score in the slice
-  int32_t argi;      // its vocabulary index
-  uint32_t err;      // staged-data wait expired in this CTA
-  double sum[3];     // sums of ex2(fma(x, log2e, -M*log2e)) over the slice
-  double jsd[2];     // divergence partial sums (p-form, q-form)
-  float argv2;       // lean variant: argmax partials exchanged after the second sweep
-  int32_t argi2;
+  float mx[3];     // slice maxima of the inputs
+  float argv;      // best verifier score in the slice
+  int32_t argi;    // its vocabulary index
+  uint32_t err;    // a staged-data wait expired in this CTA
+  double sum[3];   // slice sums of ex2(fma(x, log2e, -M*log2e))
+  double jsd[2];   // slice divergence sums (p-form, q-form)
+};
+
+// Row constants, computed by one thread after each cluster exchange and broadcast through shared memory.
+struct __align__(16) JsdRowConsts {
+  float M[3];
+  float ML[3];     // M * log2e, rounded
+  float dL;        // lse_b - lse_a (pair inputs 1 and 0), rounded
+  int32_t finite;
+  float rowv;
+  int32_t rowi;
+  double lse[3];
+  double S[3];
 };
 
 template <int MODE>
@@ -84,21 +97,49 @@ __device__ __forceinline__ void jsd_entry(float xa, float xb, float dL, float Ma
   else acc_q += v;
 }
 
-// Lean variant of the sweeps: maxima on raw data in sweep 1 (bf16x2 maxima), the argmax folded
-// into sweep 2 with one comparison per 16-byte vector, and packed two-lane fp32 arithmetic.
-template <typename T, int MODE, bool LEAN>
+// Natural log of a positive finite double without fp64 transcendental code: exponent from
+// the bits, the mantissa's log with log1pf (absolute error below 1e-7).
+__device__ __forceinline__ double ln_pos(double S) {
+  const long long bits = __double_as_longlong(S);
+  const int e = int((bits >> 52) & 0x7ff) - 1023;
+  const double m = __longlong_as_double((bits & 0x000fffffffffffffLL) | 0x3ff0000000000000LL);  // [1, 2)
+  return double(e) * kLn2 + double(log1pf(float(m - 1.0)));
+}
+
+// 1/x to double precision from an fp32 seed and one Newton step.
+__device__ __forceinline__ double rcp_pos(double x) {
+  const double r = double(1.0f / float(x));
+  return r * fma(-x, r, 2.0);
+}
+
+__device__ __forceinline__ float warp_sumf(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// The context-gain signal for the delta-fusion score: 0 -> a - b, 1 -> a, 2 -> t - b.
+template <int DSRC>
+__device__ __forceinline__ float2 delta2(float2 a, float2 b, float2 t) {
+  if constexpr (DSRC == 1) return a;
+  else if constexpr (DSRC == 2) return fsub2(t, b);
+  else return fsub2(a, b);
+}
+
+template <typename T, int MODE, int DSRC>
 __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
   using E = Elem<T>;
   using S = typename E::storage;
   constexpr int NT = JsdTraits<MODE>::NT;
   constexpr int TGT = JsdTraits<MODE>::TGT;
   constexpr int VEC = E::kVec;
+  constexpr int NP = E::kPairs;
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ JsdXchg xchg;
+  __shared__ JsdRowConsts rc;
   __shared__ float s_wf[32][4];
   __shared__ int32_t s_wi[32];
-  __shared__ double s_wd[32][3];
   __shared__ __align__(8) uint64_t s_bar[kNumChunks];
   __shared__ uint32_t s_err;
 
@@ -163,47 +204,29 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
     __syncthreads();
   }
 
-  // ---------------------------------------------------------------- sweep 1: maxima + argmax
+  // ---------------------------------------------------------------- sweep 1: maxima
   float mx[NT];
 #pragma unroll
   for (int j = 0; j < NT; ++j) mx[j] = -INFINITY;
-  float bv = -INFINITY;
-  int bi = INT_MAX;
-  if constexpr (LEAN) {
-    if constexpr (std::is_same<T, bf16_t>::value) {
-      uint32_t m2[NT];
+  if constexpr (std::is_same<T, bf16_t>::value) {
+    uint32_t m2[NT];
 #pragma unroll
-      for (int j = 0; j < NT; ++j) m2[j] = 0xff80ff80u;
-      for (int c = 0; c < kNumChunks; ++c) {
-        const int cv0 = c * chunk_vec;
-        const int cv1 = min(nvec, cv0 + chunk_vec);
-        if (cv1 <= cv0) break;
-        if (p.bulk && !mbar_wait(smem_addr(&s_bar[c]), 0, kWaitPolls)) atomicOr(&s_err, 1u);
-        for (int vi = cv0 + tid; vi < cv1; vi += nthr) {
+    for (int j = 0; j < NT; ++j) m2[j] = 0xff80ff80u;
+    for (int c = 0; c < kNumChunks; ++c) {
+      const int cv0 = c * chunk_vec;
+      const int cv1 = min(nvec, cv0 + chunk_vec);
+      if (cv1 <= cv0) break;
+      if (p.bulk && !mbar_wait(smem_addr(&s_bar[c]), 0, kWaitPolls)) atomicOr(&s_err, 1u);
+      for (int vi = cv0 + tid; vi < cv1; vi += nthr) {
 #pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            const uint4 w = reinterpret_cast<const uint4*>(stage[j])[vi];
-            m2[j] = bmax2(bmax2(m2[j], w.x), bmax2(w.y, bmax2(w.z, w.w)));
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < NT; ++j) mx[j] = fmaxf(bf16_lo(m2[j]), bf16_hi(m2[j]));
-    } else {
-      for (int c = 0; c < kNumChunks; ++c) {
-        const int cv0 = c * chunk_vec;
-        const int cv1 = min(nvec, cv0 + chunk_vec);
-        if (cv1 <= cv0) break;
-        if (p.bulk && !mbar_wait(smem_addr(&s_bar[c]), 0, kWaitPolls)) atomicOr(&s_err, 1u);
-        for (int vi = cv0 + tid; vi < cv1; vi += nthr) {
-#pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            const float4 v = reinterpret_cast<const float4*>(stage[j])[vi];
-            mx[j] = fmaxf(fmaxf(mx[j], v.x), fmaxf(v.y, fmaxf(v.z, v.w)));
-          }
+        for (int j = 0; j < NT; ++j) {
+          const uint4 w = reinterpret_cast<const uint4*>(stage[j])[vi];
+          m2[j] = bmax2(bmax2(m2[j], w.x), bmax2(w.y, bmax2(w.z, w.w)));
         }
       }
     }
+#pragma unroll
+    for (int j = 0; j < NT; ++j) mx[j] = fmaxf(bf16_lo(m2[j]), bf16_hi(m2[j]));
   } else {
     for (int c = 0; c < kNumChunks; ++c) {
       const int cv0 = c * chunk_vec;
@@ -211,212 +234,166 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
       if (cv1 <= cv0) break;
       if (p.bulk && !mbar_wait(smem_addr(&s_bar[c]), 0, kWaitPolls)) atomicOr(&s_err, 1u);
       for (int vi = cv0 + tid; vi < cv1; vi += nthr) {
-        float x[NT][VEC];
-  #pragma unroll
-        for (int j = 0; j < NT; ++j) E::load_vec(stage[j], vi, x[j]);
-        const int k0 = v0 + vi * VEC;
-  #pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-  #pragma unroll
-          for (int j = 0; j < NT; ++j) mx[j] = fmaxf(mx[j], x[j][e]);
-          float s;
-          if (MODE == kModeAsym) s = fmaf(p.beta, x[0][e] - x[1][e], x[2][e]);
-          else s = x[TGT][e];
-          if (s > bv) {
-            bv = s;
-            bi = k0 + e;
-          }
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const float4 v = reinterpret_cast<const float4*>(stage[j])[vi];
+          mx[j] = fmaxf(fmaxf(mx[j], v.x), fmaxf(v.y, fmaxf(v.z, v.w)));
         }
       }
     }
   }
 #pragma unroll
   for (int j = 0; j < NT; ++j) mx[j] = warp_max(mx[j]);
-  warp_argmax(bv, bi);
   if (lane == 0) {
 #pragma unroll
     for (int j = 0; j < NT; ++j) s_wf[warp][j] = mx[j];
-    s_wf[warp][3] = bv;
-    s_wi[warp] = bi;
   }
   __syncthreads();
   if (warp == 0) {
-    float m2[NT];
 #pragma unroll
-    for (int j = 0; j < NT; ++j) m2[j] = (lane < nwarps) ? s_wf[lane][j] : -INFINITY;
-    float v2 = (lane < nwarps) ? s_wf[lane][3] : -INFINITY;
-    int i2 = (lane < nwarps) ? s_wi[lane] : INT_MAX;
-#pragma unroll
-    for (int j = 0; j < NT; ++j) m2[j] = warp_max(m2[j]);
-    warp_argmax(v2, i2);
-    if (lane == 0) {
-#pragma unroll
-      for (int j = 0; j < NT; ++j) xchg.mx[j] = m2[j];
-      xchg.argv = v2;
-      xchg.argi = i2;
-      xchg.err = s_err;
+    for (int j = 0; j < NT; ++j) {
+      const float v = warp_max(lane < nwarps ? s_wf[lane][j] : -INFINITY);
+      if (lane == 0) xchg.mx[j] = v;
     }
   }
   cluster_sync();  // #1
-
-  // Row maxima and argmax: every CTA combines all ranks in the same order.
-  float M[NT];
+  if (warp == 0) {
+    // lane q < C reads CTA q's maxima; a warp max combines them.
 #pragma unroll
-  for (int j = 0; j < NT; ++j) M[j] = -INFINITY;
-  float rowv = -INFINITY;
-  int rowi = INT_MAX;
-  {
-    const uint32_t base_mx = smem_addr(&xchg.mx[0]);
-    const uint32_t base_v = smem_addr(&xchg.argv);
-    const uint32_t base_i = smem_addr(&xchg.argi);
-    for (uint32_t q = 0; q < C; ++q) {
-#pragma unroll
-      for (int j = 0; j < NT; ++j) M[j] = fmaxf(M[j], dsmem_ld_f32(dsmem_map(base_mx + 4 * j, q)));
-      argmax_merge(rowv, rowi, dsmem_ld_f32(dsmem_map(base_v, q)), dsmem_ld_s32(dsmem_map(base_i, q)));
+    for (int j = 0; j < NT; ++j) {
+      float v = -INFINITY;
+      if (lane < int(C)) v = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.mx[j]), uint32_t(lane)));
+      v = warp_max(v);
+      if (lane == 0) {
+        rc.M[j] = v;
+        rc.ML[j] = isfinite(v) ? v * kLog2e : 0.0f;
+      }
     }
   }
-
-  // ---------------------------------------------------------------- sweep 2: sums of exponentials
+  __syncthreads();
   float ML[NT];
 #pragma unroll
-  for (int j = 0; j < NT; ++j) ML[j] = isfinite(M[j]) ? M[j] * kLog2e : 0.0f;
-  float bv2 = -INFINITY;
-  int bi2 = INT_MAX;
+  for (int j = 0; j < NT; ++j) ML[j] = rc.ML[j];
+
+  // ---------------------------------------------------------------- sweep 2: exponential sums + argmax
   {
-    float s0[NT], s1[NT];
+    const float2 l2e2 = make_float2(kLog2e, kLog2e);
+    const float2 beta2 = make_float2(p.beta, p.beta);
+    float2 nml[NT], acc[NT];
 #pragma unroll
-    for (int j = 0; j < NT; ++j) s0[j] = s1[j] = 0.0f;
-    if constexpr (LEAN) {
-      constexpr int NP = E::kPairs;
-      const float2 l2e2 = make_float2(kLog2e, kLog2e);
-      const float2 beta2 = make_float2(p.beta, p.beta);
-      float2 nml[NT], acc[NT];
+    for (int j = 0; j < NT; ++j) {
+      nml[j] = make_float2(-ML[j], -ML[j]);
+      acc[j] = make_float2(0.0f, 0.0f);
+    }
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    for (int vi = tid; vi < nvec; vi += nthr) {
+      float2 x[NT][NP];
 #pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        nml[j] = make_float2(-ML[j], -ML[j]);
-        acc[j] = make_float2(0.0f, 0.0f);
-      }
-      for (int vi = tid; vi < nvec; vi += nthr) {
-        float2 x[NT][NP];
+      for (int j = 0; j < NT; ++j) E::load_pairs(stage[j], vi, x[j]);
 #pragma unroll
-        for (int j = 0; j < NT; ++j) E::load_pairs(stage[j], vi, x[j]);
+      for (int q2 = 0; q2 < NP; ++q2) {
 #pragma unroll
-        for (int q2 = 0; q2 < NP; ++q2) {
-#pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            const float2 y = ffma2(x[j][q2], l2e2, nml[j]);
-            acc[j] = fadd2(acc[j], make_float2(ex2_approx(y.x), ex2_approx(y.y)));
-          }
-        }
-        // verifier score of the vector's entries; one comparison per vector against the best so far
-        float2 sc[NP];
-#pragma unroll
-        for (int q2 = 0; q2 < NP; ++q2) {
-          if (MODE == kModeAsym) sc[q2] = ffma2(beta2, fsub2(x[0][q2], x[1][q2]), x[2][q2]);
-          else sc[q2] = x[TGT][q2];
-        }
-        float vm = fmaxf(sc[0].x, sc[0].y);
-#pragma unroll
-        for (int q2 = 1; q2 < NP; ++q2) vm = fmaxf(vm, fmaxf(sc[q2].x, sc[q2].y));
-        if (vm > bv2) {
-          int e_first = 2 * NP - 1;
-#pragma unroll
-          for (int q2 = NP - 1; q2 >= 0; --q2) {
-            if (sc[q2].y == vm) e_first = 2 * q2 + 1;
-            if (sc[q2].x == vm) e_first = 2 * q2;
-          }
-          bv2 = vm;
-          bi2 = v0 + vi * VEC + e_first;
+        for (int j = 0; j < NT; ++j) {
+          const float2 y = ffma2(x[j][q2], l2e2, nml[j]);
+          acc[j] = fadd2(acc[j], make_float2(ex2_approx(y.x), ex2_approx(y.y)));
         }
       }
+      // Verifier score of the vector's entries; one comparison per vector against the best so far.
+      float2 sc[NP];
 #pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        s0[j] = acc[j].x;
-        s1[j] = acc[j].y;
+      for (int q2 = 0; q2 < NP; ++q2) {
+        if constexpr (MODE == kModeAsym) sc[q2] = ffma2(beta2, delta2<DSRC>(x[0][q2], x[1][q2], x[2][q2]), x[2][q2]);
+        else sc[q2] = x[TGT][q2];
       }
-    } else {
-      for (int vi = tid; vi < nvec; vi += nthr) {
-        float x[NT][VEC];
+      float vm = fmaxf(sc[0].x, sc[0].y);
 #pragma unroll
-        for (int j = 0; j < NT; ++j) E::load_vec(stage[j], vi, x[j]);
+      for (int q2 = 1; q2 < NP; ++q2) vm = fmaxf(vm, fmaxf(sc[q2].x, sc[q2].y));
+      if (vm > bv) {
+        int e_first = 2 * NP - 1;
 #pragma unroll
-        for (int e = 0; e < VEC; e += 2) {
-#pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            s0[j] += ex2_approx(fmaf(x[j][e], kLog2e, -ML[j]));
-            s1[j] += ex2_approx(fmaf(x[j][e + 1], kLog2e, -ML[j]));
-          }
+        for (int q2 = NP - 1; q2 >= 0; --q2) {
+          if (sc[q2].y == vm) e_first = 2 * q2 + 1;
+          if (sc[q2].x == vm) e_first = 2 * q2;
         }
+        bv = vm;
+        bi = v0 + vi * VEC + e_first;
       }
     }
-    if constexpr (LEAN) {
-      warp_argmax(bv2, bi2);
-      if (lane == 0) {
-        s_wf[warp][3] = bv2;
-        s_wi[warp] = bi2;
-      }
-    }
-    double d[NT];
 #pragma unroll
-    for (int j = 0; j < NT; ++j) d[j] = warp_sum(double(s0[j]) + double(s1[j]));
+    for (int j = 0; j < NT; ++j) {
+      const float v = warp_sumf(acc[j].x + acc[j].y);
+      if (lane == 0) s_wf[warp][j] = v;
+    }
+    warp_argmax(bv, bi);
     if (lane == 0) {
-#pragma unroll
-      for (int j = 0; j < NT; ++j) s_wd[warp][j] = d[j];
+      s_wf[warp][3] = bv;
+      s_wi[warp] = bi;
     }
-    __syncthreads();
-    if (warp == 0) {
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float v2 = (lane < nwarps) ? s_wf[lane][3] : -INFINITY;
+    int i2 = (lane < nwarps) ? s_wi[lane] : INT_MAX;
+    warp_argmax(v2, i2);
+    if (lane == 0) {
+      xchg.argv = v2;
+      xchg.argi = i2;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
-        double v = (lane < nwarps) ? s_wd[lane][j] : 0.0;
-        v = warp_sum(v);
-        if (lane == 0) xchg.sum[j] = v;
+        double d = 0.0;
+        for (int w = 0; w < nwarps; ++w) d += double(s_wf[w][j]);
+        xchg.sum[j] = d;
       }
-      if constexpr (LEAN) {
-        float v2 = (lane < nwarps) ? s_wf[lane][3] : -INFINITY;
-        int i2 = (lane < nwarps) ? s_wi[lane] : INT_MAX;
-        warp_argmax(v2, i2);
-        if (lane == 0) {
-          xchg.argv2 = v2;
-          xchg.argi2 = i2;
-        }
-      }
+      xchg.err = s_err;
     }
   }
   cluster_sync();  // #2
-  if constexpr (LEAN) {
-    const uint32_t base_v = smem_addr(&xchg.argv2);
-    const uint32_t base_i = smem_addr(&xchg.argi2);
-    for (uint32_t q = 0; q < C; ++q)
-      argmax_merge(rowv, rowi, dsmem_ld_f32(dsmem_map(base_v, q)), dsmem_ld_s32(dsmem_map(base_i, q)));
-  }
-
-  double Ssum[NT];
+  if (warp == 0) {
+    float v2 = -INFINITY;
+    int i2 = INT_MAX;
+    if (lane < int(C)) {
+      v2 = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.argv), uint32_t(lane)));
+      i2 = dsmem_ld_s32(dsmem_map(smem_addr(&xchg.argi), uint32_t(lane)));
+    }
+    warp_argmax(v2, i2);
+    if (lane == 0) {
+      double sj[NT];
 #pragma unroll
-  for (int j = 0; j < NT; ++j) Ssum[j] = 0.0;
-  {
-    const uint32_t base = smem_addr(&xchg.sum[0]);
-    for (uint32_t q = 0; q < C; ++q) {
+      for (int j = 0; j < NT; ++j) sj[j] = 0.0;
+      for (uint32_t q = 0; q < C; ++q) {
 #pragma unroll
-      for (int j = 0; j < NT; ++j) Ssum[j] += dsmem_ld_f64(dsmem_map(base + 8 * j, q));
+        for (int j = 0; j < NT; ++j) sj[j] += dsmem_ld_f64(dsmem_map(smem_addr(&xchg.sum[j]), q));
+      }
+      // lse = M + ln(S') - c ln2 with c = fma(M, log2e, -ML) the exact rounding error of ML.
+      bool finite = true;
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        const float M = rc.M[j];
+        finite = finite && isfinite(M) && isfinite(sj[j]) && sj[j] > 0.0;
+      }
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        const float M = rc.M[j];
+        const float c = fmaf(M, kLog2e, -rc.ML[j]);
+        rc.S[j] = sj[j];
+        rc.lse[j] = finite ? double(M) + ln_pos(sj[j]) - double(c) * kLn2 : 0.0;
+      }
+      rc.finite = finite ? 1 : 0;
+      rc.dL = finite ? float(rc.lse[1] - rc.lse[0]) : 0.0f;
+      rc.rowv = v2;
+      rc.rowi = i2;
     }
   }
-  // lse = M + ln(S') - c ln2 with c = fma(M, log2e, -ML) the exact rounding error of ML.
-  double lse[NT];
-  bool finite = true;
-#pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    const float c = fmaf(M[j], kLog2e, -ML[j]);
-    lse[j] = double(M[j]) + log(Ssum[j]) - double(c) * kLn2;
-    finite = finite && isfinite(M[j]) && isfinite(Ssum[j]) && Ssum[j] > 0.0;
-  }
+  __syncthreads();
 
   // ---------------------------------------------------------------- sweep 3: divergence terms
   {
-    const float dL = finite ? float(lse[1] - lse[0]) : 0.0f;
+    const bool finite = rc.finite != 0;
+    const float dL = rc.dL;
     float ap0 = 0.0f, ap1 = 0.0f, aq0 = 0.0f, aq1 = 0.0f;
     if (finite) {
-      if constexpr (LEAN && !JsdTraits<MODE>::kWide) {
-        constexpr int NP = E::kPairs;
+      if constexpr (!JsdTraits<MODE>::kWide) {
         const float2 l2e2 = make_float2(kLog2e, kLog2e);
         const float2 dl2 = make_float2(dL, dL);
         const float2 nmal = make_float2(-ML[0], -ML[0]);
@@ -442,35 +419,34 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
         ap1 += accp.y;
       } else {
         for (int vi = tid; vi < nvec; vi += nthr) {
-          float xa[VEC], xb[VEC];
-          E::load_vec(stage[0], vi, xa);
-          E::load_vec(stage[1], vi, xb);
+          float2 xa[NP], xb[NP];
+          E::load_pairs(stage[0], vi, xa);
+          E::load_pairs(stage[1], vi, xb);
 #pragma unroll
-          for (int e = 0; e < VEC; e += 2) {
-            jsd_entry<JsdTraits<MODE>::kWide>(xa[e], xb[e], dL, ML[0], ML[1], ap0, aq0);
-            jsd_entry<JsdTraits<MODE>::kWide>(xa[e + 1], xb[e + 1], dL, ML[0], ML[1], ap1, aq1);
+          for (int q2 = 0; q2 < NP; ++q2) {
+            jsd_entry<true>(xa[q2].x, xb[q2].x, dL, ML[0], ML[1], ap0, aq0);
+            jsd_entry<true>(xa[q2].y, xb[q2].y, dL, ML[0], ML[1], ap1, aq1);
           }
         }
       }
     }
-    double dp = warp_sum(double(ap0) + double(ap1));
-    double dq = warp_sum(double(aq0) + double(aq1));
+    const float wp = warp_sumf(ap0 + ap1);
+    const float wq = warp_sumf(aq0 + aq1);
     if (lane == 0) {
-      s_wd[warp][0] = dp;
-      s_wd[warp][1] = dq;
+      s_wf[warp][0] = wp;
+      s_wf[warp][1] = wq;
     }
-    __syncthreads();
-    if (warp == 0) {
-      double vp = (lane < nwarps) ? s_wd[lane][0] : 0.0;
-      double vq = (lane < nwarps) ? s_wd[lane][1] : 0.0;
-      vp = warp_sum(vp);
-      vq = warp_sum(vq);
-      if (lane == 0) {
-        xchg.jsd[0] = vp;
-        xchg.jsd[1] = vq;
-        xchg.err = s_err;
-      }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    double dp = 0.0, dq = 0.0;
+    for (int w = 0; w < nwarps; ++w) {
+      dp += double(s_wf[w][0]);
+      dq += double(s_wf[w][1]);
     }
+    xchg.jsd[0] = dp;
+    xchg.jsd[1] = dq;
+    xchg.err = s_err;
   }
   cluster_sync();  // #3
 
@@ -478,43 +454,36 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
   if (rank == 0 && tid == 0) {
     double jp = 0.0, jq = 0.0;
     uint32_t err = 0;
-    {
-      const uint32_t bp = smem_addr(&xchg.jsd[0]);
-      const uint32_t be = smem_addr(&xchg.err);
-      for (uint32_t q = 0; q < C; ++q) {
-        jp += dsmem_ld_f64(dsmem_map(bp, q));
-        jq += dsmem_ld_f64(dsmem_map(bp + 8, q));
-        err |= dsmem_ld_u32(dsmem_map(be, q));
-      }
+    for (uint32_t q = 0; q < C; ++q) {
+      jp += dsmem_ld_f64(dsmem_map(smem_addr(&xchg.jsd[0]), q));
+      jq += dsmem_ld_f64(dsmem_map(smem_addr(&xchg.jsd[1]), q));
+      err |= dsmem_ld_u32(dsmem_map(smem_addr(&xchg.err), q));
     }
-    double D = 0.5 * (jp / Ssum[0] + jq / Ssum[1]);
+    const bool finite = rc.finite != 0;
+    double D = finite ? 0.5 * (jp * rcp_pos(rc.S[0]) + jq * rcp_pos(rc.S[1])) : 0.0;
     D = fmin(fmax(D, 0.0), kLn2);
     uint32_t bits = 0;
     if (!finite) bits |= kBitNonfinite;
     if (err) bits |= kBitTimeout;
-    const int token = (rowi == INT_MAX) ? 0 : rowi;
-    if (MODE == kModeAsym && pos < p.K) {
+    const int token = (rc.rowi == INT_MAX) ? 0 : rc.rowi;
+    if (pos < p.K) {
       const int d = p.draft_ids[size_t(req) * p.K + pos];
       if (d < 0 || d >= V) {
         bits |= kBitBadDraft;
-      } else if (finite) {
+      } else if (MODE == kModeAsym && finite) {
         // t_d and b_d from the slice of the CTA that staged entry d.
         const uint32_t owner = uint32_t(d / p.n_slice);
         const int off = d - int(owner) * p.n_slice;
-        const float td = E::from_smem_remote(dsmem_map(smem_addr(stage[2] + off), owner));
+        const float td = E::from_smem_remote(dsmem_map(smem_addr(stage[NT - 1] + off), owner));
         const float bd = E::from_smem_remote(dsmem_map(smem_addr(stage[1] + off), owner));
-        const double margin = (double(td) - lse[2]) - p.ln_gamma + D - (double(bd) - lse[1]);
+        const double margin = (double(td) - rc.lse[NT - 1]) - p.ln_gamma + D - (double(bd) - rc.lse[1]);
         if (margin > 0.0) bits |= kBitAccept;
       }
-    }
-    if (MODE == kModeSci && pos < p.K) {
-      const int d = p.draft_ids[size_t(req) * p.K + pos];
-      if (d < 0 || d >= V) bits |= kBitBadDraft;
     }
     if (p.out_D) p.out_D[row] = finite ? float(D) : __int_as_float(0x7fc00000);
     if (MODE == kModeAsym && p.out_lse) {
 #pragma unroll
-      for (int j = 0; j < 3; ++j) p.out_lse[size_t(row) * 3 + j] = float(lse[j]);
+      for (int j = 0; j < NT; ++j) p.out_lse[size_t(row) * 3 + j] = float(rc.lse[j]);
     }
     RowRecord rec;
     rec.value = D;
@@ -532,36 +501,31 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
       const uint32_t status = ((any & kBitNonfinite) ? 1u : 0u) | ((any & kBitBadDraft) ? 2u : 0u) |
                               ((any & kBitTimeout) ? 4u : 0u);
       int32_t* toks = p.out_tokens + size_t(req) * R1;
+      double thr = 0.0;
+      if (MODE == kModeSci) {
+        thr = p.T_base + p.alpha_omega * (p.r_hat[req] - p.tau_credit);
+        thr = fmax(p.T_min, fmin(thr, p.T_max));
+        if (p.out_T) p.out_T[req] = float(thr);
+      }
       if (status) {
         p.out_accept_len[req] = 0;
         for (int i = 0; i < R1; ++i) toks[i] = -1;
       } else {
         int n = p.K;
-        if (MODE == kModeAsym) {
-          for (int i = 0; i < p.K; ++i)
-            if (!(recs[i].bits & kBitAccept)) {
-              n = i;
-              break;
-            }
-        } else {
-          double thr = p.T_base + p.alpha_omega * (p.r_hat[req] - p.tau_credit);
-          thr = fmax(p.T_min, fmin(thr, p.T_max));
-          if (p.out_T) p.out_T[req] = float(thr);
-          for (int i = 0; i < p.K; ++i)
-            if (recs[i].value > thr) {
-              n = i;
-              break;
-            }
+        for (int i = 0; i < p.K; ++i) {
+          const bool ok = (MODE == kModeAsym) ? (recs[i].bits & kBitAccept) != 0 : !(recs[i].value > thr);
+          if (!ok) {
+            n = i;
+            break;
+          }
+        }
+        if (MODE == kModeSci) {
           const double pacc = double(n) / double(p.K);
           p.r_hat[req] = (1.0 - p.ewma_beta) * p.r_hat[req] + p.ewma_beta * pacc;
         }
         p.out_accept_len[req] = n;
         const int32_t* dr = p.draft_ids + size_t(req) * p.K;
         for (int i = 0; i < R1; ++i) toks[i] = (i < n) ? dr[i] : (i == n ? recs[n].token : -1);
-      }
-      if (MODE == kModeSci && status && p.out_T) {
-        const double thr = p.T_base + p.alpha_omega * (p.r_hat[req] - p.tau_credit);
-        p.out_T[req] = float(fmax(p.T_min, fmin(thr, p.T_max)));
       }
       p.out_req_status[req] = status;
       p.tickets[req] = 0u;
@@ -580,74 +544,67 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
   cluster_sync();  // #4
 }
 
-int jsd_static_smem_bytes() { return int(sizeof(JsdXchg) + 32 * 4 * 4 + 32 * 4 + 32 * 3 * 8 + kNumChunks * 8 + 4); }
-
-static bool lean_variant() {
-  static const bool v = [] {
-    const char* e = std::getenv("ASV_JSD_VARIANT");
-    return !(e && e[0] == '0');
-  }();
-  return v;
+int jsd_static_smem_bytes() {
+  return int(sizeof(JsdXchg) + sizeof(JsdRowConsts) + 32 * 4 * 4 + 32 * 4 + kNumChunks * 8 + 4 + 64);
 }
 
-template <typename T, int MODE>
-static cudaError_t launch_one(const JsdArgs& a, const LaunchPlan& plan, cudaStream_t s) {
-  auto kern = lean_variant() ? jsd_family_kernel<T, MODE, true> : jsd_family_kernel<T, MODE, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem);
-  if (e != cudaSuccess) return e;
-  if (plan.cluster > 8) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
+using JsdKernel = void (*)(const JsdArgs);
+
+static JsdKernel pick_kernel(int mode, int dtype, int dsrc) {
+  if (mode == kModeSci) return dtype == 0 ? jsd_family_kernel<float, kModeSci, 0> : jsd_family_kernel<bf16_t, kModeSci, 0>;
+  if (dtype == 0) {
+    if (dsrc == 1) return jsd_family_kernel<float, kModeAsym, 1>;
+    if (dsrc == 2) return jsd_family_kernel<float, kModeAsym, 2>;
+    return jsd_family_kernel<float, kModeAsym, 0>;
   }
-  const int R = a.B * (a.K + 1);
+  if (dsrc == 1) return jsd_family_kernel<bf16_t, kModeAsym, 1>;
+  if (dsrc == 2) return jsd_family_kernel<bf16_t, kModeAsym, 2>;
+  return jsd_family_kernel<bf16_t, kModeAsym, 0>;
+}
+
+static cudaLaunchConfig_t make_config(const LaunchPlan& plan, unsigned grid, cudaStream_t s, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(R) * unsigned(plan.cluster), 1, 1);
+  cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(unsigned(plan.threads), 1, 1);
   cfg.dynamicSmemBytes = size_t(plan.smem);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = unsigned(plan.cluster);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  return cfg;
+}
+
+static cudaError_t prepare(JsdKernel kern, const LaunchPlan& plan) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem);
+  if (e != cudaSuccess) return e;
+  if (plan.cluster > 8) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+cudaError_t launch_jsd_family(int mode, int dtype, const JsdArgs& a, const LaunchPlan& plan, cudaStream_t s) {
+  JsdKernel kern = pick_kernel(mode, dtype, a.delta_source);
+  cudaError_t e = prepare(kern, plan);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  const unsigned grid = unsigned(a.B) * unsigned(a.K + 1) * unsigned(plan.cluster);
+  cudaLaunchConfig_t cfg = make_config(plan, grid, s, attr);
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <typename T, int MODE>
-static int max_clusters_one(const LaunchPlan& plan) {
-  auto kern = lean_variant() ? jsd_family_kernel<T, MODE, true> : jsd_family_kernel<T, MODE, false>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem) != cudaSuccess) return 0;
-  if (plan.cluster > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-    return 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(plan.cluster), 1, 1);
-  cfg.blockDim = dim3(unsigned(plan.threads), 1, 1);
-  cfg.dynamicSmemBytes = size_t(plan.smem);
+int jsd_max_active_clusters(int mode, int dtype, const LaunchPlan& plan) {
+  JsdKernel kern = pick_kernel(mode, dtype, 0);
+  if (prepare(kern, plan) != cudaSuccess) return 0;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = unsigned(plan.cluster);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cudaLaunchConfig_t cfg = make_config(plan, unsigned(plan.cluster), 0, attr);
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   return n;
-}
-
-cudaError_t launch_jsd_family(int mode, int dtype, const JsdArgs& a, const LaunchPlan& plan, cudaStream_t s) {
-  if (mode == kModeAsym) return dtype == 0 ? launch_one<float, kModeAsym>(a, plan, s) : launch_one<bf16_t, kModeAsym>(a, plan, s);
-  return dtype == 0 ? launch_one<float, kModeSci>(a, plan, s) : launch_one<bf16_t, kModeSci>(a, plan, s);
-}
-
-int jsd_max_active_clusters(int mode, int dtype, const LaunchPlan& plan) {
-  if (mode == kModeAsym) return dtype == 0 ? max_clusters_one<float, kModeAsym>(plan) : max_clusters_one<bf16_t, kModeAsym>(plan);
-  return dtype == 0 ? max_clusters_one<float, kModeSci>(plan) : max_clusters_one<bf16_t, kModeSci>(plan);
 }
 
 }  // namespace asv

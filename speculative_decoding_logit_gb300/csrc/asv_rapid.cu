@@ -49,6 +49,20 @@ struct RowConsts {
   float invT, etaT, ML, inv_sum, zhmax, thr, head_scale;
 };
 
+// Row statistics broadcast by one thread after each cluster exchange.
+struct __align__(16) RapidShared {
+  float M;
+  float inv_sum;
+  float zhmax;
+  int32_t finite;
+};
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 // p, zhat/T and the protected target of one entry, recomputed identically everywhere.
 __device__ __forceinline__ void rapid_entry(float z, float q, const RowConsts& c, float& p, float& zhs, float& prot) {
   const float zs = z * c.invT;
@@ -62,9 +76,10 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
   constexpr int VEC = 4;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ RapidXchg xchg;
+  __shared__ RapidShared rs;
   __shared__ float s_wf[32];
   __shared__ int32_t s_wi[32];
-  __shared__ double s_wd[32][2];
+  __shared__ float s_w2[32][2];
   __shared__ __align__(8) uint64_t s_bar[kNumChunks];
   __shared__ uint32_t s_err;
 
@@ -130,17 +145,22 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
     __syncthreads();
     return r;  // valid in warp 0
   };
-  auto block_sum2 = [&](double a, double b, double& ra, double& rb) {
-    a = warp_sum(a);
-    b = warp_sum(b);
+  // fp32 warp sums; the per-warp partials are added in fp64 by thread 0 (valid there only).
+  auto block_sum2 = [&](float a, float b, double& ra, double& rb) {
+    a = warp_sum_f(a);
+    b = warp_sum_f(b);
     if (lane == 0) {
-      s_wd[warp][0] = a;
-      s_wd[warp][1] = b;
+      s_w2[warp][0] = a;
+      s_w2[warp][1] = b;
     }
     __syncthreads();
-    if (warp == 0) {
-      ra = warp_sum(lane < nwarps ? s_wd[lane][0] : 0.0);
-      rb = warp_sum(lane < nwarps ? s_wd[lane][1] : 0.0);
+    if (tid == 0) {
+      ra = 0.0;
+      rb = 0.0;
+      for (int w = 0; w < nwarps; ++w) {
+        ra += double(s_w2[w][0]);
+        rb += double(s_w2[w][1]);
+      }
     }
     __syncthreads();
   };
@@ -166,8 +186,14 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
     }
   }
   cluster_sync();  // #1
-  float M = -INFINITY;
-  for (uint32_t q = 0; q < C; ++q) M = fmaxf(M, dsmem_ld_f32(dsmem_map(smem_addr(&xchg.zmax), q)));
+  if (warp == 0) {
+    float v = -INFINITY;
+    if (lane < int(C)) v = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.zmax), uint32_t(lane)));
+    v = warp_max(v);
+    if (lane == 0) rs.M = v;
+  }
+  __syncthreads();
+  const float M = rs.M;
   RowConsts rc;
   rc.invT = invT;
   rc.etaT = p.eta * p.T;
@@ -185,20 +211,28 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
       q1 += q4.y + q4.w;
     }
     double se = 0, sq = 0;
-    block_sum2(double(e0) + double(e1), double(q0) + double(q1), se, sq);
+    block_sum2(e0 + e1, q0 + q1, se, sq);
     if (tid == 0) {
       xchg.sum_e = se;
       xchg.sum_q = sq;
     }
   }
   cluster_sync();  // #2
-  double Se = 0.0, Sq = 0.0;
-  for (uint32_t q = 0; q < C; ++q) {
-    Se += dsmem_ld_f64(dsmem_map(smem_addr(&xchg.sum_e), q));
-    Sq += dsmem_ld_f64(dsmem_map(smem_addr(&xchg.sum_q), q));
+  if (tid == 0) {
+    double Se = 0.0, Sq = 0.0;
+    for (uint32_t q = 0; q < C; ++q) {
+      Se += dsmem_ld_f64(dsmem_map(smem_addr(&xchg.sum_e), q));
+      Sq += dsmem_ld_f64(dsmem_map(smem_addr(&xchg.sum_q), q));
+    }
+    const bool fin = isfinite(M) && isfinite(Se) && Se > 0.0 && isfinite(Sq);
+    rs.finite = fin ? 1 : 0;
+    // 1/S from an fp32 seed and one Newton step, rounded to fp32
+    const double r0 = double(1.0f / float(Se));
+    rs.inv_sum = fin ? float(r0 * fma(-Se, r0, 2.0)) : 0.0f;
   }
-  const bool finite = isfinite(M) && isfinite(Se) && Se > 0.0 && isfinite(Sq);
-  rc.inv_sum = finite ? float(1.0 / Se) : 0.0f;
+  __syncthreads();
+  const bool finite = rs.finite != 0;
+  rc.inv_sum = rs.inv_sum;
   rc.zhmax = 0.f;
   rc.thr = 0.f;
   rc.head_scale = 0.f;
@@ -223,12 +257,15 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
     if (tid == 0) xchg.zhmax = r;
   }
   cluster_sync();  // #3
-  {
-    float mh = -INFINITY;
-    for (uint32_t q = 0; q < C; ++q) mh = fmaxf(mh, dsmem_ld_f32(dsmem_map(smem_addr(&xchg.zhmax), q)));
-    rc.zhmax = mh;
-    rc.thr = mh + p.ln_tail_frac;
+  if (warp == 0) {
+    float v = -INFINITY;
+    if (lane < int(C)) v = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.zhmax), uint32_t(lane)));
+    v = warp_max(v);
+    if (lane == 0) rs.zhmax = v;
   }
+  __syncthreads();
+  rc.zhmax = rs.zhmax;
+  rc.thr = rs.zhmax + p.ln_tail_frac;
 
   // ---------------------------------------------------------------- sweep 4: head sums
   {
@@ -251,7 +288,7 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
       }
     }
     double hp = 0, he = 0;
-    block_sum2(double(hp0), double(he0), hp, he);
+    block_sum2(hp0, he0, hp, he);
     if (tid == 0) {
       xchg.head_p = hp;
       xchg.head_e = he;
@@ -420,7 +457,9 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
   cluster_sync();  // #8: shared memory stays alive until remote reads are done
 }
 
-int rapid_static_smem_bytes() { return int(sizeof(RapidXchg) + 32 * 4 + 32 * 4 + 32 * 2 * 8 + kNumChunks * 8 + 4); }
+int rapid_static_smem_bytes() {
+  return int(sizeof(RapidXchg) + sizeof(RapidShared) + 32 * 4 + 32 * 4 + 32 * 2 * 4 + kNumChunks * 8 + 4 + 64);
+}
 
 cudaError_t launch_rapid(const RapidArgs& a, const LaunchPlan& plan, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(rapid_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem);

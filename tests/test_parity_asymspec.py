@@ -149,3 +149,18 @@ def test_sweep_b256_k4_v151936_f32_sampled(asv):
         for f in ("accept_len", "tokens", "D", "lse", "req_status"):
             setattr(s, f, getattr(out, f)[torch.from_numpy(sample).cuda()])
         compare_asymspec(s, ref, w.dtype)
+
+
+@pytest.mark.parametrize("src", [1, 2])
+@pytest.mark.parametrize("dtype", [gen.F32, gen.BF16])
+def test_delta_source_ablation(asv, src, dtype):
+    """The ablation's alternative context-gain signals (delta := a, delta := t - b)."""
+    batch = gen.make_asymspec_batch("spiky", 60 + src, 16, 3, 5000, dtype)
+    a, b, t = (to_device(x, dtype) for x in (batch.a, batch.b, batch.t))
+    d = torch.from_numpy(batch.drafts).cuda()
+    for beta in (1.0, 2.0):
+        out = asv.asymspec_verify(a, b, t, d, beta, 0.5, delta_source=src)
+        torch.cuda.synchronize()
+        ref = oracle.asymspec_verify(batch.a, batch.b, batch.t, batch.drafts, beta, 0.5, delta_source=src)
+        compare_asymspec(out, ref, dtype)
+        np.testing.assert_array_equal(out.tokens.cpu().numpy()[:, 0] >= 0, True)
