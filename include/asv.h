@@ -90,9 +90,10 @@ asv_status asv_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t str
 asv_status asv_set_tuning(int cluster_ctas, int threads_per_cta);
 
 /* The plan the next call with these shapes would use (cluster size, threads, dynamic
- * shared memory bytes, 1 if rows are staged with bulk copies).  Any output may be NULL. */
+ * shared memory bytes, 1 if rows are staged with bulk copies) and how many of its clusters
+ * the device can hold at once (cudaOccupancyMaxActiveClusters).  Any output may be NULL. */
 asv_status asv_query_plan(int mode, int B, int K, int V, int dtype, int* cluster_ctas, int* threads_per_cta,
-                          int* smem_bytes, int* bulk_copy);
+                          int* smem_bytes, int* bulk_copy, int* max_active_clusters);
 
 /*
  * asymspec_verify -- the AsymSpec verification step.  [ASYM] sec. 4.1-4.2.

@@ -82,7 +82,7 @@ def _declare(L):
     L.asv_workspace_init.restype = _i
     L.asv_set_tuning.argtypes = [_i, _i]
     L.asv_set_tuning.restype = _i
-    L.asv_query_plan.argtypes = [_i, _i, _i, _i, _i] + [C.POINTER(_i)] * 4
+    L.asv_query_plan.argtypes = [_i, _i, _i, _i, _i] + [C.POINTER(_i)] * 5
     L.asv_query_plan.restype = _i
     L.asymspec_verify.argtypes = [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _f, _f, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
     L.asymspec_verify.restype = _i
@@ -163,9 +163,10 @@ def set_tuning(cluster_ctas: int = 0, threads_per_cta: int = 0):
 
 
 def query_plan(mode: int, B: int, K: int, V: int, dtype: int) -> dict:
-    out = [C.c_int(0) for _ in range(4)]
+    out = [C.c_int(0) for _ in range(5)]
     _check(library().asv_query_plan(mode, B, K, V, dtype, *[C.byref(o) for o in out]), "asv_query_plan")
-    return {"cluster": out[0].value, "threads": out[1].value, "smem": out[2].value, "bulk": out[3].value}
+    return {"cluster": out[0].value, "threads": out[1].value, "smem": out[2].value, "bulk": out[3].value,
+            "max_active_clusters": out[4].value}
 
 
 # ------------------------------------------------------------------ AsymSpec

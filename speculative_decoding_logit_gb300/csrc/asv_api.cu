@@ -156,7 +156,7 @@ asv_status asv_set_tuning(int cluster_ctas, int threads_per_cta) {
 }
 
 asv_status asv_query_plan(int mode, int B, int K, int V, int dtype, int* cluster_ctas, int* threads_per_cta,
-                          int* smem_bytes, int* bulk_copy) {
+                          int* smem_bytes, int* bulk_copy, int* max_active_clusters) {
   if (B < 1 || K < 0 || V < 2) return ASV_ERR_SHAPE;
   if (!valid_dtype(dtype)) return ASV_ERR_DTYPE;
   if (mode == ASV_MODE_RAPID && dtype != ASV_F32) return ASV_ERR_DTYPE;
@@ -172,6 +172,12 @@ asv_status asv_query_plan(int mode, int B, int K, int V, int dtype, int* cluster
   if (threads_per_cta) *threads_per_cta = pl.threads;
   if (smem_bytes) *smem_bytes = pl.smem;
   if (bulk_copy) *bulk_copy = pl.bulk;
+  if (max_active_clusters) {
+    *max_active_clusters = mode == ASV_MODE_RAPID
+                               ? asv::rapid_max_active_clusters(pl)
+                               : asv::jsd_max_active_clusters(mode == ASV_MODE_SCI ? asv::kModeSci : asv::kModeAsym,
+                                                              dtype, pl);
+  }
   return ASV_OK;
 }
 
