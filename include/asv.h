@@ -161,6 +161,30 @@ asv_status asymspec_verify_host(const void* a_host, const void* b_host, const vo
                                 cudaStream_t stream);
 
 /*
+ * asymspec_verify_static -- asymspec_verify without a caller workspace, for callers that cannot
+ * allocate device memory: code handed only its input and output buffers (for instance a plugin
+ * inside a serving framework whose memory pool it does not own), or code that must not allocate
+ * once it is running.  The paper has no counterpart; this is a packaging variant.
+ *
+ * The scratch lives in a file-scope device array of ASV_STATIC_SCRATCH_BYTES bytes (1 MiB),
+ * reserved on every GPU that loads the library's device code and held until the process exits.
+ * The call allocates nothing (no cudaMalloc, no cudaFree, no allocating library routine).
+ * - Batches whose workspace (asv_workspace_bytes) exceeds ASV_STATIC_SCRATCH_BYTES are rejected
+ *   with ASV_ERR_WORKSPACE (at K = 8 that is a little over 7,000 requests).
+ * - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ *   that device current and caches it; make that first call before any stream capture.
+ * - Every call shares the one array.  Each call clears the part that must start at zero (one
+ *   cudaMemsetAsync on `stream`) before its kernel; calls that may overlap on the GPU (other
+ *   streams, other host threads) race on the array and must not be issued.
+ * Everything else is as asymspec_verify.
+ */
+#define ASV_STATIC_SCRATCH_BYTES (1u << 20)
+asv_status asymspec_verify_static(const void* a, const void* b, const void* t, int dtype, const int32_t* draft_ids,
+                                  int B, int K, int V, float beta, float gamma, int32_t* out_accept_len,
+                                  int32_t* out_tokens, float* out_D, float* out_lse, uint32_t* out_req_status,
+                                  cudaStream_t stream);
+
+/*
  * rapid_verify -- RAPID verification with the retrieval-augmented target.
  * [RAPID] Workflow; Key designs 2 (augmented target), 3 (tail protection),
  * 4 (adjusted residual sampling).

@@ -1,0 +1,70 @@
+// asv_static_scratch.cu -- asymspec_verify_static: the AsymSpec verification for callers that
+// cannot allocate device memory themselves.
+//
+// Some callers are handed only their input and output buffers: a plugin running inside a
+// serving framework whose memory pool it does not own, or code that must not allocate once it
+// is running (an allocation can block, fragment a pool or fail under memory pressure).  They
+// cannot provide the few kilobytes of workspace that asymspec_verify takes (the per-request
+// tickets and per-row records of the last-arriver scan).  This entry point keeps that scratch in
+// a file-scope device array instead, reserved when the library's device code is loaded on a GPU
+// and held by that GPU until the process exits.  It calls no cudaMalloc/cudaFree and no
+// allocating library routine.
+#include <cstddef>
+#include <cstdint>
+#include <mutex>
+
+#include "asv.h"
+#include "asv_internal.h"
+
+namespace {
+
+// The scratch: tickets (one per request, padded to 256 bytes) then one 16-byte record per row.
+static __device__ __align__(256) unsigned char g_static_scratch[ASV_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+void* g_scratch_addr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+// Device address of g_static_scratch on the current device.  In host code the array's name is
+// only a host-side stand-in, so the address is looked up once per device (with that device
+// current) and cached.
+cudaError_t scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" asv_status asymspec_verify_static(const void* a, const void* b, const void* t, int dtype,
+                                             const int32_t* draft_ids, int B, int K, int V, float beta, float gamma,
+                                             int32_t* out_accept_len, int32_t* out_tokens, float* out_D,
+                                             float* out_lse, uint32_t* out_req_status, cudaStream_t stream) {
+  if (B < 0 || K < 0 || V < 2) return ASV_ERR_SHAPE;
+  const size_t need = asv_workspace_bytes(ASV_MODE_ASYMSPEC, B, K, V, dtype);
+  if (need > size_t(ASV_STATIC_SCRATCH_BYTES)) return ASV_ERR_WORKSPACE;  // batch too large for the static scratch
+  if (B == 0) return ASV_OK;
+  void* ws = nullptr;
+  cudaError_t e = scratch_address(&ws);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return ASV_ERR_CUDA;
+  }
+  // The scan's tickets must start at zero.  A finished call leaves them zero, but the array is
+  // shared by every call, so clear them on the stream rather than trust what the last call left.
+  const size_t tickets = (size_t(B) * 4 + 255) / 256 * 256;
+  e = cudaMemsetAsync(ws, 0, tickets, stream);
+  if (e != cudaSuccess) return ASV_ERR_CUDA;
+  return asymspec_verify(a, b, t, dtype, draft_ids, B, K, V, beta, gamma, out_accept_len, out_tokens, out_D, out_lse,
+                         out_req_status, ws, size_t(ASV_STATIC_SCRATCH_BYTES), stream);
+}

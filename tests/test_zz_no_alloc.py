@@ -1,0 +1,74 @@
+"""asymspec_verify_static, the entry point for callers that cannot allocate device memory
+(for instance a plugin handed only its input and output buffers by a serving framework, or
+code that must not allocate once running): it keeps its scratch in a library-owned static
+device array.  Checked through the C ABI against asymspec_verify (caller workspace) on two
+calls in a row, and for the size limit.  This file is collected last on purpose."""
+import ctypes as C
+
+import numpy as np
+import pytest
+import torch
+
+import gen
+
+pytestmark = pytest.mark.gpu
+
+STATIC_SCRATCH_BYTES = 1 << 20
+
+
+def _to_dev(x, dtype):
+    if dtype == gen.F32:
+        return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def _static_call(lib, a, b, t, d, dtype, B, K, V, beta, gamma):
+    f = lib.asymspec_verify_static
+    vp = C.c_void_p
+    f.argtypes = [vp, vp, vp, C.c_int, vp, C.c_int, C.c_int, C.c_int, C.c_float, C.c_float, vp, vp, vp, vp, vp, vp]
+    f.restype = C.c_int
+    acc = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    tok = torch.full((B, K + 1), -7, dtype=torch.int32, device="cuda")
+    D = torch.full((B, K + 1), -1.0, dtype=torch.float32, device="cuda")
+    lse = torch.full((B, K + 1, 3), -1.0, dtype=torch.float32, device="cuda")
+    st = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    rc = f(a.data_ptr(), b.data_ptr(), t.data_ptr(), dtype, d.data_ptr(), B, K, V, beta, gamma, acc.data_ptr(),
+           tok.data_ptr(), D.data_ptr(), lse.data_ptr(), st.data_ptr(), stream)
+    torch.cuda.synchronize()
+    return rc, acc, tok, D, lse, st
+
+
+def test_static_scratch_matches_workspace_entry_point():
+    import speculative_decoding_logit_gb300 as asv
+    asv.build()
+    lib = asv.library()
+    cases = [(gen.BF16, "gumbel_zipf", 12, 3, 6000, 1.0, 0.5, 401),
+             (gen.F32, "spiky", 9, 2, 4099, 0.0, 1.0, 402)]   # second call: other shape, unaligned rows
+    for dtype, recipe, B, K, V, beta, gamma, seed in cases:
+        batch = gen.make_asymspec_batch(recipe, seed, B, K, V, dtype)
+        a, b, t = (_to_dev(x, dtype) for x in (batch.a, batch.b, batch.t))
+        d = torch.from_numpy(batch.drafts).cuda()
+        ref = asv.asymspec_verify(a, b, t, d, beta, gamma)
+        torch.cuda.synchronize()
+        rc, acc, tok, D, lse, st = _static_call(lib, a, b, t, d, dtype, B, K, V, beta, gamma)
+        assert rc == 0
+        assert torch.equal(acc, ref.accept_len) and torch.equal(tok, ref.tokens)
+        assert torch.equal(st, ref.req_status)
+        tol = 1e-5 if dtype == gen.F32 else 2e-3
+        assert torch.allclose(D, ref.D, atol=tol, rtol=0) and torch.allclose(lse, ref.lse, atol=tol, rtol=0)
+
+
+def test_static_scratch_rejects_batches_beyond_its_size():
+    import speculative_decoding_logit_gb300 as asv
+    asv.build()
+    lib = asv.library()
+    K = 8
+    B = 8000   # 256-byte-padded tickets + 16 bytes per row exceed 1 MiB
+    assert lib.asv_workspace_bytes(0, B, K, 1000, 1) > STATIC_SCRATCH_BYTES
+    f = lib.asymspec_verify_static
+    vp = C.c_void_p
+    f.argtypes = [vp, vp, vp, C.c_int, vp, C.c_int, C.c_int, C.c_int, C.c_float, C.c_float, vp, vp, vp, vp, vp, vp]
+    f.restype = C.c_int
+    P = 1 << 20
+    assert f(P, P, P, 1, P, B, K, 1000, 1.0, 0.5, P, P, P, P, P, None) == 6   # ASV_ERR_WORKSPACE, nothing launched
