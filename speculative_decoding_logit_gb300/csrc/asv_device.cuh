@@ -365,3 +365,49 @@ __device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
 }
 
 }  // namespace asv
+
+namespace asv {
+
+// ------------------------------------------------------------------ compensated fp32 sums
+// A value carried as an unevaluated sum hi + lo of two floats (Knuth's TwoSum keeps the
+// rounding error of each addition), so partial sums cross warps and CTAs without fp64.
+struct DF {
+  float hi, lo;
+};
+
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  const float s = a.hi + b.hi;
+  const float bb = s - a.hi;
+  const float e = (a.hi - (s - bb)) + (b.hi - bb) + (a.lo + b.lo);
+  const float hi = s + e;
+  return DF{hi, e - (hi - s)};
+}
+
+__device__ __forceinline__ DF warp_sum_df(DF v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    DF w;
+    w.hi = __shfl_xor_sync(0xffffffffu, v.hi, o);
+    w.lo = __shfl_xor_sync(0xffffffffu, v.lo, o);
+    v = df_add(v, w);
+  }
+  return v;
+}
+
+__device__ __forceinline__ void dsmem_st_f32(uint32_t a, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+
+// ln(x) for a positive finite float: x = 2^e * m with m in [0.75, 1.5), ln x = e ln2 + log1p(m - 1);
+// m - 1 is exact and |log1p(m - 1)| < 0.41, so the absolute error stays near 6e-8.
+__device__ __forceinline__ float ln_split(float x) {
+  int e = int((__float_as_uint(x) >> 23) & 0xff) - 127;
+  float m = __uint_as_float((__float_as_uint(x) & 0x007fffffu) | 0x3f800000u);  // [1, 2)
+  if (m >= 1.5f) {
+    m *= 0.5f;
+    e += 1;
+  }
+  return fmaf(float(e), 0.693147182464599609375f, fmaf(float(e), -1.904654323148236e-09f, log1pf(m - 1.0f)));
+}
+
+}  // namespace asv

@@ -19,13 +19,16 @@
 //            score (one comparison per 16-byte vector against the best so far);
 //   sweep 3: the per-entry Jensen-Shannon terms.
 // Arithmetic on entries is two-lane packed fp32 (fma/add/mul .f32x2) where it pairs up.  After each
-// sweep: warp shuffles in fp32, per-warp partials combined in fp64 by one thread, a cluster exchange
-// through distributed shared memory, and one warp that combines the C partials in rank order and
-// broadcasts the row constants, so every CTA holds bit-identical row statistics.  fp64 is used only
-// by single threads: this GPU's fp64 rate is a small fraction of its fp32 rate.  HBM is read exactly
-// once per input byte.  CTA 0 finalises the row (gate, outputs, a 16-byte row record) and takes a
-// ticket on the request's counter; the last of the K+1 rows to finish runs the left-to-right scan
-// and resets the counter, so the whole step is one launch with no spin-waits.
+// sweep: warp shuffles, per-warp partials combined by one warp, a cluster exchange through
+// distributed shared memory, and one warp that combines the C partials in rank order and
+// broadcasts the row constants, so every CTA holds bit-identical row statistics.  Sums that cross
+// warps and CTAs are carried as compensated fp32 pairs: this GPU's fp64 rate is a small fraction of
+// its fp32 rate, so fp64 appears only in CTA 0's few finalisation steps.  HBM is read exactly once
+// per input byte.  Before the last exchange every CTA pushes its final partials (and the CTA holding
+// the draft's entry pushes t_d and b_d) into CTA 0, so the other CTAs leave right after it.  CTA 0
+// finalises the row (gate, outputs, a 16-byte row record) and takes a ticket on the request's
+// counter; the last of the K+1 rows to finish runs the left-to-right scan and resets the counter,
+// so the whole step is one launch with no spin-waits.
 //
 // Numerics.  Inputs are widened exactly to fp32.  exp(x - M) is formed as ex2(fma(x, log2e, -M*log2e)),
 // whose constant rounding error c is known exactly and removed from the log-sum-exp; the divergence
@@ -47,24 +50,28 @@
 namespace asv {
 
 struct __align__(16) JsdXchg {
-  float mx[3];     // slice maxima of the inputs
-  float argv;      // best verifier score in the slice
-  int32_t argi;    // its vocabulary index
-  uint32_t err;    // a staged-data wait expired in this CTA
-  double sum[3];   // slice sums of ex2(fma(x, log2e, -M*log2e))
-  double jsd[2];   // slice divergence sums (p-form, q-form)
+  float mx[3];        // slice maxima of the inputs
+  float argv;         // best verifier score in the slice
+  int32_t argi;       // its vocabulary index
+  float sum_hi[3];    // slice sums of ex2(fma(x, log2e, -M*log2e)) as hi + lo
+  float sum_lo[3];
+  // Pushed into CTA 0 by every CTA before the third exchange, so that CTA 0 alone reads
+  // them afterwards and the other CTAs can leave:
+  float jsd_from[kMaxCluster][4];  // slice divergence sums: p-form hi, lo, q-form hi, lo
+  uint32_t err_from[kMaxCluster];  // a staged-data wait expired in that CTA
+  float td, bd;                    // t_d and b_d, from the CTA that staged entry d
 };
 
 // Row constants, computed by one thread after each cluster exchange and broadcast through shared memory.
 struct __align__(16) JsdRowConsts {
   float M[3];
   float ML[3];     // M * log2e, rounded
-  float dL;        // lse_b - lse_a (pair inputs 1 and 0), rounded
+  float S_hi[3];   // row sums of ex2(fma(x, log2e, -ML)) as hi + lo
+  float S_lo[3];
+  float dL;        // lse_b - lse_a (pair inputs 1 and 0)
   int32_t finite;
   float rowv;
   int32_t rowi;
-  double lse[3];
-  double S[3];
 };
 
 template <int MODE>
@@ -104,12 +111,6 @@ __device__ __forceinline__ double ln_pos(double S) {
   const int e = int((bits >> 52) & 0x7ff) - 1023;
   const double m = __longlong_as_double((bits & 0x000fffffffffffffLL) | 0x3ff0000000000000LL);  // [1, 2)
   return double(e) * kLn2 + double(log1pf(float(m - 1.0)));
-}
-
-// 1/x to double precision from an fp32 seed and one Newton step.
-__device__ __forceinline__ double rcp_pos(double x) {
-  const double r = double(1.0f / float(x));
-  return r * fma(-x, r, 2.0);
 }
 
 __device__ __forceinline__ float warp_sumf(float v) {
@@ -336,16 +337,17 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
     float v2 = (lane < nwarps) ? s_wf[lane][3] : -INFINITY;
     int i2 = (lane < nwarps) ? s_wi[lane] : INT_MAX;
     warp_argmax(v2, i2);
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const DF d = warp_sum_df(DF{lane < nwarps ? s_wf[lane][j] : 0.0f, 0.0f});
+      if (lane == 0) {
+        xchg.sum_hi[j] = d.hi;
+        xchg.sum_lo[j] = d.lo;
+      }
+    }
     if (lane == 0) {
       xchg.argv = v2;
       xchg.argi = i2;
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        double d = 0.0;
-        for (int w = 0; w < nwarps; ++w) d += double(s_wf[w][j]);
-        xchg.sum[j] = d;
-      }
-      xchg.err = s_err;
     }
   }
   cluster_sync();  // #2
@@ -357,30 +359,35 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
       i2 = dsmem_ld_s32(dsmem_map(smem_addr(&xchg.argi), uint32_t(lane)));
     }
     warp_argmax(v2, i2);
-    if (lane == 0) {
-      double sj[NT];
+    DF Sj[NT];
 #pragma unroll
-      for (int j = 0; j < NT; ++j) sj[j] = 0.0;
-      for (uint32_t q = 0; q < C; ++q) {
-#pragma unroll
-        for (int j = 0; j < NT; ++j) sj[j] += dsmem_ld_f64(dsmem_map(smem_addr(&xchg.sum[j]), q));
+    for (int j = 0; j < NT; ++j) {
+      DF d{0.0f, 0.0f};
+      if (lane < int(C)) {
+        d.hi = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.sum_hi[j]), uint32_t(lane)));
+        d.lo = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.sum_lo[j]), uint32_t(lane)));
       }
-      // lse = M + ln(S') - c ln2 with c = fma(M, log2e, -ML) the exact rounding error of ML.
+      Sj[j] = warp_sum_df(d);
+    }
+    if (lane == 0) {
       bool finite = true;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
-        const float M = rc.M[j];
-        finite = finite && isfinite(M) && isfinite(sj[j]) && sj[j] > 0.0;
+        finite = finite && isfinite(rc.M[j]) && isfinite(Sj[j].hi) && Sj[j].hi > 0.0f;
+        rc.S_hi[j] = Sj[j].hi;
+        rc.S_lo[j] = Sj[j].lo;
       }
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        const float M = rc.M[j];
-        const float c = fmaf(M, kLog2e, -rc.ML[j]);
-        rc.S[j] = sj[j];
-        rc.lse[j] = finite ? double(M) + ln_pos(sj[j]) - double(c) * kLn2 : 0.0;
+      // lse_b - lse_a = (Mb - Ma) + ln(Sb / Sa) - (cb - ca) ln2, c = fma(M, log2e, -ML) the exact
+      // rounding error of ML (the sums carry a factor 2^c).
+      float dL = 0.0f;
+      if (finite) {
+        const float ca = fmaf(rc.M[0], kLog2e, -rc.ML[0]);
+        const float cb = fmaf(rc.M[1], kLog2e, -rc.ML[1]);
+        const float ratio = (Sj[1].hi + Sj[1].lo) / (Sj[0].hi + Sj[0].lo);
+        dL = (rc.M[1] - rc.M[0]) + (ln_split(ratio) - (cb - ca) * kLn2f);
       }
       rc.finite = finite ? 1 : 0;
-      rc.dL = finite ? float(rc.lse[1] - rc.lse[0]) : 0.0f;
+      rc.dL = dL;
       rc.rowv = v2;
       rc.rowi = i2;
     }
@@ -438,99 +445,27 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
     }
   }
   __syncthreads();
-  if (tid == 0) {
-    double dp = 0.0, dq = 0.0;
-    for (int w = 0; w < nwarps; ++w) {
-      dp += double(s_wf[w][0]);
-      dq += double(s_wf[w][1]);
-    }
-    xchg.jsd[0] = dp;
-    xchg.jsd[1] = dq;
-    xchg.err = s_err;
-  }
-  cluster_sync();  // #3
-
-  // ---------------------------------------------------------------- row finalisation (CTA 0)
-  if (rank == 0 && tid == 0) {
-    double jp = 0.0, jq = 0.0;
-    uint32_t err = 0;
-    for (uint32_t q = 0; q < C; ++q) {
-      jp += dsmem_ld_f64(dsmem_map(smem_addr(&xchg.jsd[0]), q));
-      jq += dsmem_ld_f64(dsmem_map(smem_addr(&xchg.jsd[1]), q));
-      err |= dsmem_ld_u32(dsmem_map(smem_addr(&xchg.err), q));
-    }
-    const bool finite = rc.finite != 0;
-    double D = finite ? 0.5 * (jp * rcp_pos(rc.S[0]) + jq * rcp_pos(rc.S[1])) : 0.0;
-    D = fmin(fmax(D, 0.0), kLn2);
-    uint32_t bits = 0;
-    if (!finite) bits |= kBitNonfinite;
-    if (err) bits |= kBitTimeout;
-    const int token = (rc.rowi == INT_MAX) ? 0 : rc.rowi;
-    if (pos < p.K) {
-      const int d = p.draft_ids[size_t(req) * p.K + pos];
-      if (d < 0 || d >= V) {
-        bits |= kBitBadDraft;
-      } else if (MODE == kModeAsym && finite) {
-        // t_d and b_d from the slice of the CTA that staged entry d.
-        const uint32_t owner = uint32_t(d / p.n_slice);
-        const int off = d - int(owner) * p.n_slice;
-        const float td = E::from_smem_remote(dsmem_map(smem_addr(stage[NT - 1] + off), owner));
-        const float bd = E::from_smem_remote(dsmem_map(smem_addr(stage[1] + off), owner));
-        const double margin = (double(td) - rc.lse[NT - 1]) - p.ln_gamma + D - (double(bd) - rc.lse[1]);
-        if (margin > 0.0) bits |= kBitAccept;
+  const int dpos = (pos < p.K) ? p.draft_ids[size_t(req) * p.K + pos] : -1;
+  if (warp == 0) {
+    const DF dp = warp_sum_df(DF{lane < nwarps ? s_wf[lane][0] : 0.0f, 0.0f});
+    const DF dq = warp_sum_df(DF{lane < nwarps ? s_wf[lane][1] : 0.0f, 0.0f});
+    if (lane == 0) {
+      // Push this CTA's partials into CTA 0.
+      const uint32_t base = smem_addr(&xchg.jsd_from[rank][0]);
+      dsmem_st_f32(dsmem_map(base + 0, 0), dp.hi);
+      dsmem_st_f32(dsmem_map(base + 4, 0), dp.lo);
+      dsmem_st_f32(dsmem_map(base + 8, 0), dq.hi);
+      dsmem_st_f32(dsmem_map(base + 12, 0), dq.lo);
+      dsmem_st_u32(dsmem_map(smem_addr(&xchg.err_from[rank]), 0), s_err);
+      // The CTA that staged the draft's entry pushes t_d and b_d.
+      if (MODE == kModeAsym && dpos >= v0 && dpos < v0 + len) {
+        const int off = dpos - v0;
+        dsmem_st_f32(dsmem_map(smem_addr(&xchg.td), 0), E::to_float(stage[NT - 1][off]));
+        dsmem_st_f32(dsmem_map(smem_addr(&xchg.bd), 0), E::to_float(stage[1][off]));
       }
-    }
-    if (p.out_D) p.out_D[row] = finite ? float(D) : __int_as_float(0x7fc00000);
-    if (MODE == kModeAsym && p.out_lse) {
-#pragma unroll
-      for (int j = 0; j < NT; ++j) p.out_lse[size_t(row) * 3 + j] = float(rc.lse[j]);
-    }
-    RowRecord rec;
-    rec.value = D;
-    rec.token = token;
-    rec.bits = bits;
-    p.records[row] = rec;
-    __threadfence();
-    const uint32_t ticket = atomicAdd(&p.tickets[req], 1u);
-    if (ticket == uint32_t(p.K)) {
-      // Last row of this request: the left-to-right scan.
-      __threadfence();
-      const volatile RowRecord* recs = p.records + size_t(req) * R1;
-      uint32_t any = 0;
-      for (int i = 0; i < R1; ++i) any |= recs[i].bits;
-      const uint32_t status = ((any & kBitNonfinite) ? 1u : 0u) | ((any & kBitBadDraft) ? 2u : 0u) |
-                              ((any & kBitTimeout) ? 4u : 0u);
-      int32_t* toks = p.out_tokens + size_t(req) * R1;
-      double thr = 0.0;
-      if (MODE == kModeSci) {
-        thr = p.T_base + p.alpha_omega * (p.r_hat[req] - p.tau_credit);
-        thr = fmax(p.T_min, fmin(thr, p.T_max));
-        if (p.out_T) p.out_T[req] = float(thr);
-      }
-      if (status) {
-        p.out_accept_len[req] = 0;
-        for (int i = 0; i < R1; ++i) toks[i] = -1;
-      } else {
-        int n = p.K;
-        for (int i = 0; i < p.K; ++i) {
-          const bool ok = (MODE == kModeAsym) ? (recs[i].bits & kBitAccept) != 0 : !(recs[i].value > thr);
-          if (!ok) {
-            n = i;
-            break;
-          }
-        }
-        if (MODE == kModeSci) {
-          const double pacc = double(n) / double(p.K);
-          p.r_hat[req] = (1.0 - p.ewma_beta) * p.r_hat[req] + p.ewma_beta * pacc;
-        }
-        p.out_accept_len[req] = n;
-        const int32_t* dr = p.draft_ids + size_t(req) * p.K;
-        for (int i = 0; i < R1; ++i) toks[i] = (i < n) ? dr[i] : (i == n ? recs[n].token : -1);
-      }
-      p.out_req_status[req] = status;
-      p.tickets[req] = 0u;
     }
   }
+  cluster_sync();  // #3: after this only CTA 0 touches shared memory, and only its own
 
   // A CTA whose staged-data wait expired waits (bounded) for its copies before leaving.
   if (p.bulk && tid == 0 && s_err) {
@@ -540,8 +475,91 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
       mbar_wait(smem_addr(&s_bar[c]), 0, kWaitPolls);
     }
   }
-  // Keep this CTA's shared memory alive until CTA 0 has finished its remote reads.
-  cluster_sync();  // #4
+  if (rank != 0 || tid != 0) return;
+
+  // ---------------------------------------------------------------- row finalisation (CTA 0)
+  DF jp{0.0f, 0.0f}, jq{0.0f, 0.0f};
+  uint32_t err = 0;
+  for (uint32_t q = 0; q < C; ++q) {
+    jp = df_add(jp, DF{xchg.jsd_from[q][0], xchg.jsd_from[q][1]});
+    jq = df_add(jq, DF{xchg.jsd_from[q][2], xchg.jsd_from[q][3]});
+    err |= xchg.err_from[q];
+  }
+  const bool finite = rc.finite != 0;
+  float D = 0.0f;
+  if (finite) {
+    D = 0.5f * ((jp.hi + jp.lo) / (rc.S_hi[0] + rc.S_lo[0]) + (jq.hi + jq.lo) / (rc.S_hi[1] + rc.S_lo[1]));
+    D = fminf(fmaxf(D, 0.0f), kLn2f);
+  }
+  // Log-sum-exps (double, this thread only): lse = M + ln(S) - c ln2.
+  double lse[NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const float c = fmaf(rc.M[j], kLog2e, -rc.ML[j]);
+    lse[j] = finite ? double(rc.M[j]) + ln_pos(double(rc.S_hi[j]) + double(rc.S_lo[j])) - double(c) * kLn2 : 0.0;
+  }
+  uint32_t bits = 0;
+  if (!finite) bits |= kBitNonfinite;
+  if (err) bits |= kBitTimeout;
+  const int token = (rc.rowi == INT_MAX) ? 0 : rc.rowi;
+  if (pos < p.K) {
+    if (dpos < 0 || dpos >= V) {
+      bits |= kBitBadDraft;
+    } else if (MODE == kModeAsym && finite) {
+      const double margin = (double(xchg.td) - lse[NT - 1]) - p.ln_gamma + double(D) - (double(xchg.bd) - lse[1]);
+      if (margin > 0.0) bits |= kBitAccept;
+    }
+  }
+  if (p.out_D) p.out_D[row] = finite ? D : __int_as_float(0x7fc00000);
+  if (MODE == kModeAsym && p.out_lse) {
+#pragma unroll
+    for (int j = 0; j < NT; ++j) p.out_lse[size_t(row) * 3 + j] = float(lse[j]);
+  }
+  RowRecord rec;
+  rec.value = double(D);
+  rec.token = token;
+  rec.bits = bits;
+  p.records[row] = rec;
+  __threadfence();
+  const uint32_t ticket = atomicAdd(&p.tickets[req], 1u);
+  if (ticket == uint32_t(p.K)) {
+    // Last row of this request: the left-to-right scan.
+    __threadfence();
+    const volatile RowRecord* recs = p.records + size_t(req) * R1;
+    uint32_t any = 0;
+    for (int i = 0; i < R1; ++i) any |= recs[i].bits;
+    const uint32_t status = ((any & kBitNonfinite) ? 1u : 0u) | ((any & kBitBadDraft) ? 2u : 0u) |
+                            ((any & kBitTimeout) ? 4u : 0u);
+    int32_t* toks = p.out_tokens + size_t(req) * R1;
+    double thr = 0.0;
+    if (MODE == kModeSci) {
+      thr = p.T_base + p.alpha_omega * (p.r_hat[req] - p.tau_credit);
+      thr = fmax(p.T_min, fmin(thr, p.T_max));
+      if (p.out_T) p.out_T[req] = float(thr);
+    }
+    if (status) {
+      p.out_accept_len[req] = 0;
+      for (int i = 0; i < R1; ++i) toks[i] = -1;
+    } else {
+      int n = p.K;
+      for (int i = 0; i < p.K; ++i) {
+        const bool ok = (MODE == kModeAsym) ? (recs[i].bits & kBitAccept) != 0 : !(recs[i].value > thr);
+        if (!ok) {
+          n = i;
+          break;
+        }
+      }
+      if (MODE == kModeSci) {
+        const double pacc = double(n) / double(p.K);
+        p.r_hat[req] = (1.0 - p.ewma_beta) * p.r_hat[req] + p.ewma_beta * pacc;
+      }
+      p.out_accept_len[req] = n;
+      const int32_t* dr = p.draft_ids + size_t(req) * p.K;
+      for (int i = 0; i < R1; ++i) toks[i] = (i < n) ? dr[i] : (i == n ? recs[n].token : -1);
+    }
+    p.out_req_status[req] = status;
+    p.tickets[req] = 0u;
+  }
 }
 
 int jsd_static_smem_bytes() {

@@ -31,10 +31,10 @@ struct __align__(16) RapidXchg {
   float zhmax;
   uint32_t err;
   uint32_t draw_active;  // set remotely by CTA 0 when this cluster draws for its request
-  double sum_e;
-  double sum_q;
-  double head_p;
-  double head_e;
+  float sum_e[2];   // hi, lo
+  float sum_q[2];
+  float head_p[2];
+  float head_e[2];
   float race_key;
   int32_t race_idx;
   int32_t draw_row;
@@ -145,8 +145,9 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
     __syncthreads();
     return r;  // valid in warp 0
   };
-  // fp32 warp sums; the per-warp partials are added in fp64 by thread 0 (valid there only).
-  auto block_sum2 = [&](float a, float b, double& ra, double& rb) {
+  // fp32 warp sums; the per-warp partials are combined by warp 0 as compensated pairs and
+  // written to dst_a / dst_b (hi, lo) in this CTA's exchange slot.
+  auto block_sum2 = [&](float a, float b, float* dst_a, float* dst_b) {
     a = warp_sum_f(a);
     b = warp_sum_f(b);
     if (lane == 0) {
@@ -154,15 +155,26 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
       s_w2[warp][1] = b;
     }
     __syncthreads();
-    if (tid == 0) {
-      ra = 0.0;
-      rb = 0.0;
-      for (int w = 0; w < nwarps; ++w) {
-        ra += double(s_w2[w][0]);
-        rb += double(s_w2[w][1]);
+    if (warp == 0) {
+      const DF ra = warp_sum_df(DF{lane < nwarps ? s_w2[lane][0] : 0.0f, 0.0f});
+      const DF rb = warp_sum_df(DF{lane < nwarps ? s_w2[lane][1] : 0.0f, 0.0f});
+      if (lane == 0) {
+        dst_a[0] = ra.hi;
+        dst_a[1] = ra.lo;
+        dst_b[0] = rb.hi;
+        dst_b[1] = rb.lo;
       }
     }
     __syncthreads();
+  };
+  // Sum over the cluster of a (hi, lo) slot, in warp 0 (result valid in lane 0).
+  auto cluster_sum = [&](const float* slot) -> DF {
+    DF d{0.0f, 0.0f};
+    if (lane < int(C)) {
+      d.hi = dsmem_ld_f32(dsmem_map(smem_addr(&slot[0]), uint32_t(lane)));
+      d.lo = dsmem_ld_f32(dsmem_map(smem_addr(&slot[1]), uint32_t(lane)));
+    }
+    return warp_sum_df(d);
   };
 
   const float invT = p.inv_T;
@@ -210,25 +222,17 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
       q0 += q4.x + q4.z;
       q1 += q4.y + q4.w;
     }
-    double se = 0, sq = 0;
-    block_sum2(e0 + e1, q0 + q1, se, sq);
-    if (tid == 0) {
-      xchg.sum_e = se;
-      xchg.sum_q = sq;
-    }
+    block_sum2(e0 + e1, q0 + q1, xchg.sum_e, xchg.sum_q);
   }
   cluster_sync();  // #2
-  if (tid == 0) {
-    double Se = 0.0, Sq = 0.0;
-    for (uint32_t q = 0; q < C; ++q) {
-      Se += dsmem_ld_f64(dsmem_map(smem_addr(&xchg.sum_e), q));
-      Sq += dsmem_ld_f64(dsmem_map(smem_addr(&xchg.sum_q), q));
+  if (warp == 0) {
+    const DF Se = cluster_sum(xchg.sum_e);
+    const DF Sq = cluster_sum(xchg.sum_q);
+    if (lane == 0) {
+      const bool fin = isfinite(M) && isfinite(Se.hi) && Se.hi > 0.0f && isfinite(Sq.hi);
+      rs.finite = fin ? 1 : 0;
+      rs.inv_sum = fin ? 1.0f / (Se.hi + Se.lo) : 0.0f;
     }
-    const bool fin = isfinite(M) && isfinite(Se) && Se > 0.0 && isfinite(Sq);
-    rs.finite = fin ? 1 : 0;
-    // 1/S from an fp32 seed and one Newton step, rounded to fp32
-    const double r0 = double(1.0f / float(Se));
-    rs.inv_sum = fin ? float(r0 * fma(-Se, r0, 2.0)) : 0.0f;
   }
   __syncthreads();
   const bool finite = rs.finite != 0;
@@ -287,26 +291,25 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
         }
       }
     }
-    double hp = 0, he = 0;
-    block_sum2(hp0, he0, hp, he);
-    if (tid == 0) {
-      xchg.head_p = hp;
-      xchg.head_e = he;
-      xchg.err = s_err;
-    }
+    block_sum2(hp0, he0, xchg.head_p, xchg.head_e);
+    if (tid == 0) xchg.err = s_err;
   }
   cluster_sync();  // #4
 
   // ---------------------------------------------------------------- row finalisation (CTA 0)
+  DF Hp{0.0f, 0.0f}, He{0.0f, 0.0f};
+  uint32_t err = 0;
+  if (rank == 0 && warp == 0) {
+    Hp = cluster_sum(xchg.head_p);
+    He = cluster_sum(xchg.head_e);
+    uint32_t e = (lane < int(C)) ? dsmem_ld_u32(dsmem_map(smem_addr(&xchg.err), uint32_t(lane))) : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) e |= __shfl_xor_sync(0xffffffffu, e, o);
+    err = e;
+  }
   if (rank == 0 && tid == 0) {
-    double Hp = 0.0, He = 0.0;
-    uint32_t err = 0;
-    for (uint32_t q = 0; q < C; ++q) {
-      Hp += dsmem_ld_f64(dsmem_map(smem_addr(&xchg.head_p), q));
-      He += dsmem_ld_f64(dsmem_map(smem_addr(&xchg.head_e), q));
-      err |= dsmem_ld_u32(dsmem_map(smem_addr(&xchg.err), q));
-    }
-    rc.head_scale = (He > 0.0) ? float(Hp / He) : 0.0f;
+    const float he = He.hi + He.lo;
+    rc.head_scale = (he > 0.0f) ? (Hp.hi + Hp.lo) / he : 0.0f;
     uint32_t bits = 0;
     if (!finite) bits |= kBitNonfinite;
     if (err) bits |= kBitTimeout;
