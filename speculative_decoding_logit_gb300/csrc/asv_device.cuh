@@ -15,7 +15,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2f = 0.6931471805599453f;
 constexpr double kLn2 = 0.69314718055994530942;
 constexpr int kNumChunks = 4;          // bulk-copy chunks per staged slice (one mbarrier each)
-constexpr uint32_t kWaitPolls = 1u << 22;  // try_wait polls before a staged-data wait gives up
+constexpr uint32_t kWaitPolls = 1u << 16;     // try_wait attempts before a staged-data wait gives up
+constexpr uint32_t kWaitSuspendNs = 100000u;  // each attempt may sleep up to 100 us (woken by completion)
 
 // Row record bits (workspace).
 constexpr uint32_t kBitNonfinite = 1u;
@@ -50,14 +51,16 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
-// Bounded wait for phase `parity` of `bar`.  Returns false if the poll budget ran out.
+// Bounded wait for phase `parity` of `bar`: each attempt sleeps until the phase completes or the
+// suspend-time hint elapses, so waiting warps do not spin on the issue slots.  Returns false if
+// `polls` attempts all expired (at most polls * kWaitSuspendNs).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t polls) {
   for (uint32_t i = 0; i < polls; ++i) {
     uint32_t done;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(done)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kWaitSuspendNs)
         : "memory");
     if (done) return true;
   }
@@ -88,6 +91,18 @@ __device__ __forceinline__ void cluster_wait() {
 
 __device__ __forceinline__ void cluster_sync() {
   cluster_arrive();
+  cluster_wait();
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+// Cluster barrier where only warp 0 has written data other CTAs read: warp 0 arrives with
+// release semantics, the other warps relaxed; everyone waits with acquire semantics.
+__device__ __forceinline__ void cluster_sync_w0(int warp) {
+  if (warp == 0) cluster_arrive();
+  else cluster_arrive_relaxed();
   cluster_wait();
 }
 
@@ -317,6 +332,14 @@ namespace asv {
 // ------------------------------------------------------------------ packed arithmetic
 // Two fp32 lanes per instruction (sm_100+ f32x2 forms) and bf16x2 maxima on raw bit patterns.
 
+#ifdef ASV_SCALAR_PAIRS
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  return make_float2(fmaf(a.x, b.x, c.x), fmaf(a.y, b.y, c.y));
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return make_float2(a.x * b.x, a.y * b.y); }
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) { return make_float2(a.x - b.x, a.y - b.y); }
+#else
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   float2 d;
   asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
@@ -343,6 +366,7 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return d;
 }
+#endif
 
 // Lane-wise maximum of two bf16x2 words (exact; a NaN lane yields the other operand).
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
@@ -355,6 +379,7 @@ __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
 
 namespace asv {
 
+#ifndef ASV_SCALAR_PAIRS
 __device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
   float2 d;
   asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
@@ -363,6 +388,7 @@ __device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return d;
 }
+#endif
 
 }  // namespace asv
 

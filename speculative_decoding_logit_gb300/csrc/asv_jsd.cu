@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
       if (lane == 0) xchg.mx[j] = v;
     }
   }
-  cluster_sync();  // #1
+  cluster_sync_w0(warp);  // #1
   if (warp == 0) {
     // lane q < C reads CTA q's maxima; a warp max combines them.
 #pragma unroll
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
       xchg.argi = i2;
     }
   }
-  cluster_sync();  // #2
+  cluster_sync_w0(warp);  // #2
   if (warp == 0) {
     float v2 = -INFINITY;
     int i2 = INT_MAX;
@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
       }
     }
   }
-  cluster_sync();  // #3: after this only CTA 0 touches shared memory, and only its own
+  cluster_sync_w0(warp);  // #3: after this only CTA 0 touches shared memory, and only its own
 
   // A CTA whose staged-data wait expired waits (bounded) for its copies before leaving.
   if (p.bulk && tid == 0 && s_err) {
