@@ -45,4 +45,4 @@ from ._binding import (  # noqa: F401
     set_tuning,
     workspace_bytes,
 )
-from .build import build  # noqa: F401
+from .nvcc_build import build  # noqa: F401

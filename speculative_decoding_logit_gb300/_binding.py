@@ -9,7 +9,7 @@ from typing import Optional
 
 import torch
 
-from . import build as _build
+from . import nvcc_build as _build
 
 ASV_F32 = 0
 ASV_BF16 = 1

@@ -14,7 +14,10 @@ namespace asv {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2f = 0.6931471805599453f;
 constexpr double kLn2 = 0.69314718055994530942;
-constexpr int kNumChunks = 4;          // bulk-copy chunks per staged slice (one mbarrier each)
+#ifndef ASV_NUM_CHUNKS
+#define ASV_NUM_CHUNKS 4
+#endif
+constexpr int kNumChunks = ASV_NUM_CHUNKS;  // bulk-copy chunks per staged slice (one mbarrier each)
 constexpr uint32_t kWaitPolls = 1u << 16;     // try_wait attempts before a staged-data wait gives up
 constexpr uint32_t kWaitSuspendNs = 100000u;  // each attempt may sleep up to 100 us (woken by completion)
 
