@@ -47,6 +47,12 @@
 #include "asv_internal.h"
 #include "jsd_poly.inc"
 
+// Polynomial evaluation in the narrow divergence form: 0 packed with coefficient immediates,
+// 1 packed with the coefficient pairs held in registers, 2 scalar with immediates.
+#ifndef ASV_POLY_MODE
+#define ASV_POLY_MODE 1
+#endif
+
 namespace asv {
 
 struct __align__(16) JsdXchg {
@@ -404,6 +410,9 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
         const float2 l2e2 = make_float2(kLog2e, kLog2e);
         const float2 dl2 = make_float2(dL, dL);
         const float2 nmal = make_float2(-ML[0], -ML[0]);
+#if ASV_POLY_MODE == 1
+        const asv_jsd_poly2h_coeffs pk = asv_jsd_poly2h_load();
+#endif
         float2 accp = make_float2(0.0f, 0.0f);
         for (int vi = tid; vi < nvec; vi += nthr) {
           float2 xa[NP], xb[NP];
@@ -415,7 +424,13 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
             if (fabsf(u.x) <= ASV_JSD_POLY_U0 && fabsf(u.y) <= ASV_JSD_POLY_U0) {
               const float2 y = ffma2(xa[q2], l2e2, nmal);
               const float2 ep = make_float2(ex2_approx(y.x), ex2_approx(y.y));
+#if ASV_POLY_MODE == 1
+              accp = ffma2(fmul2(ep, fmul2(u, u)), asv_jsd_poly2h(u, pk), accp);
+#elif ASV_POLY_MODE == 2
+              accp = ffma2(fmul2(ep, fmul2(u, u)), make_float2(asv_jsd_poly(u.x), asv_jsd_poly(u.y)), accp);
+#else
               accp = ffma2(fmul2(ep, fmul2(u, u)), asv_jsd_poly2(u), accp);
+#endif
             } else {
               jsd_entry<false>(xa[q2].x, xb[q2].x, dL, ML[0], ML[1], ap0, aq0);
               jsd_entry<false>(xa[q2].y, xb[q2].y, dL, ML[0], ML[1], ap1, aq1);

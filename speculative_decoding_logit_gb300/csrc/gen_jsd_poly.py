@@ -116,6 +116,25 @@ def emit2(fh, name, var, coef):
     fh.write("  return acc;\n}\n")
 
 
+def emit2h(fh, name, var, coef):
+    """Packed form with the coefficient pairs held in registers: a struct filled once (outside
+    the loop) and a Horner evaluation that reads it."""
+    deg = len(coef) - 1
+    fh.write(f"struct {name}_coeffs {{\n  float2 c[{deg + 1}];\n}};\n")
+    fh.write(f"static __device__ __forceinline__ {name}_coeffs {name}_load() {{\n  {name}_coeffs k;\n")
+    for d in range(deg + 1):
+        c = float(coef[d]).hex()
+        fh.write(f"  k.c[{d}] = make_float2({c}f, {c}f);\n")
+        # opaque to the compiler, so the pair stays in registers instead of being rebuilt per use
+        fh.write(f"  asm volatile(\"\" : \"+f\"(k.c[{d}].x), \"+f\"(k.c[{d}].y));\n")
+    fh.write("  return k;\n}\n")
+    fh.write(f"static __device__ __forceinline__ float2 {name}(float2 {var}, const {name}_coeffs& k) {{\n")
+    fh.write(f"  float2 acc = k.c[{deg}];\n")
+    for d in range(deg - 1, -1, -1):
+        fh.write(f"  acc = asv::ffma2(acc, {var}, k.c[{d}]);\n")
+    fh.write("  return acc;\n}\n")
+
+
 def main():
     coef = fit_rounded(P, DEG, -U0, U0)
     bcoef = fit_rounded(Bfun, R_DEG, 0.0, 1.0)
@@ -143,6 +162,7 @@ def main():
         emit(fh, "asv_jsd_wide_b", "r", bcoef)
         emit2(fh, "asv_jsd_poly2", "u", coef)
         emit2(fh, "asv_jsd_wide_b2", "r", bcoef)
+        emit2h(fh, "asv_jsd_poly2h", "u", coef)
     print(f"wrote {out}: P rel err {err:.3e} exact, {err32:.3e} fp32; B rel err {berr:.3e} exact, {berr32:.3e} fp32")
 
 
