@@ -110,6 +110,33 @@ cudaError_t plan_for(int kind, int dtype, int NT, int elem_bytes, int V, long lo
   return cudaSuccess;
 }
 
+// Plan for the streaming AsymSpec / SCI kernel.  It stages nothing, so a CTA needs only
+// registers; pass B re-reads the divergence pair from L2, so the slices of the CTAs resident at
+// once (about four per SM) must fit comfortably in L2: C is the smallest cluster size that keeps
+// them under kL2Budget, raised while the batch has fewer than four CTAs per SM.
+cudaError_t plan_jsd(int elem_bytes, int V, long long R, bool aligned, LaunchPlan* out) {
+  DevInfo di;
+  cudaError_t e = dev_info(&di);
+  if (e != cudaSuccess) return e;
+  const int vec = 16 / elem_bytes;
+  int C = g_tune_cluster.load();
+  if (C <= 0) {
+    constexpr double kL2Budget = 48.0 * 1024 * 1024;
+    const double resident = 4.0 * di.sms;
+    C = int(std::ceil(resident * 2.0 * double(V) * elem_bytes / kL2Budget));
+    const long long want = 4LL * di.sms;
+    if (R * C < want) C = int((want + R - 1) / R);
+    C = std::min(C, std::max(1, V / 1024));
+    C = std::max(1, std::min(C, asv::kMaxCluster));
+  }
+  out->cluster = C;
+  out->threads = asv::jsd_threads();
+  out->n_slice = int(round_up(size_t(ceil_div(V, C)), size_t(vec)));
+  out->smem = 0;
+  out->bulk = aligned ? 1 : 0;
+  return cudaSuccess;
+}
+
 bool valid_dtype(int dt) { return dt == ASV_F32 || dt == ASV_BF16; }
 int elem_size(int dt) { return dt == ASV_F32 ? 4 : 2; }
 
@@ -163,9 +190,9 @@ asv_status asv_query_plan(int mode, int B, int K, int V, int dtype, int* cluster
   const int eb = elem_size(dtype);
   const bool bulk = (size_t(V) * eb) % 16 == 0;
   LaunchPlan pl;
-  const int NT = mode == ASV_MODE_ASYMSPEC ? 3 : 2;
-  const int st = mode == ASV_MODE_RAPID ? asv::rapid_static_smem_bytes() : asv::jsd_static_smem_bytes();
-  cudaError_t e = plan_for(mode, dtype, NT, eb, V, (long long)B * (K + 1), bulk, st, &pl);
+  cudaError_t e = mode == ASV_MODE_RAPID
+                      ? plan_for(mode, dtype, 2, eb, V, (long long)B * (K + 1), bulk, asv::rapid_static_smem_bytes(), &pl)
+                      : plan_jsd(eb, V, (long long)B * (K + 1), bulk, &pl);
   if (e == cudaErrorInvalidValue) return ASV_ERR_SHAPE;
   if (e != cudaSuccess) return cuda_fail(e);
   if (cluster_ctas) *cluster_ctas = pl.cluster;
@@ -191,7 +218,7 @@ static asv_status run_jsd(int mode, asv::JsdArgs& a, int dtype, void* workspace,
   bool bulk = (size_t(a.V) * eb) % 16 == 0;
   for (int j = 0; j < NT; ++j) bulk = bulk && aligned(a.x[j], 16);
   LaunchPlan pl;
-  cudaError_t e = plan_for(amode, dtype, NT, eb, a.V, (long long)a.B * (a.K + 1), bulk, asv::jsd_static_smem_bytes(), &pl);
+  cudaError_t e = plan_jsd(eb, a.V, (long long)a.B * (a.K + 1), bulk, &pl);
   if (e == cudaErrorInvalidValue) return ASV_ERR_SHAPE;
   if (e != cudaSuccess) return cuda_fail(e);
   a.n_slice = pl.n_slice;

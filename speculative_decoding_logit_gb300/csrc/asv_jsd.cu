@@ -10,31 +10,34 @@
 //     JSD(draft || target) against a threshold driven by an EWMA of the acceptance rate.
 //
 // Work decomposition.  One row (request r, position i) is V vocabulary entries of each input.  A
-// thread-block cluster of C CTAs owns one row; CTA q of the cluster owns entries
-// [q*n_slice, (q+1)*n_slice).  Each CTA stages its slice of every input in shared memory once (1-D
-// bulk copies in kNumChunks chunks, one mbarrier each, so work starts on the first chunk while the
-// rest is in flight), and the three passes the divergence needs run out of shared memory:
-//   sweep 1: row maxima of every input (bf16: two-lane bf16 maxima on the raw words);
-//   sweep 2: sums of exp(x - max) on the special-function unit, and the argmax of the verifier
-//            score (one comparison per 16-byte vector against the best so far);
-//   sweep 3: the per-entry Jensen-Shannon terms.
-// Arithmetic on entries is two-lane packed fp32 (fma/add/mul .f32x2) where it pairs up.  After each
-// sweep: warp shuffles, per-warp partials combined by one warp, a cluster exchange through
-// distributed shared memory, and one warp that combines the C partials in rank order and
-// broadcasts the row constants, so every CTA holds bit-identical row statistics.  Sums that cross
-// warps and CTAs are carried as compensated fp32 pairs: this GPU's fp64 rate is a small fraction of
-// its fp32 rate, so fp64 appears only in CTA 0's few finalisation steps.  HBM is read exactly once
-// per input byte.  Before the last exchange every CTA pushes its final partials (and the CTA holding
-// the draft's entry pushes t_d and b_d) into CTA 0, so the other CTAs leave right after it.  CTA 0
-// finalises the row (gate, outputs, a 16-byte row record) and takes a ticket on the request's
-// counter; the last of the K+1 rows to finish runs the left-to-right scan and resets the counter,
-// so the whole step is one launch with no spin-waits.
+// thread-block cluster of C CTAs owns one row; CTA q owns entries [q*n_slice, (q+1)*n_slice).  The
+// kernel streams; it stages nothing in shared memory:
+//   pass A  reads the slice of every input from HBM once (16-byte loads that bypass L1, one vector
+//           prefetched ahead) and keeps per thread a running maximum and a sum of exp(x - max)
+//           (rescaled on the rare occasions the maximum grows) for each input, plus the argmax of
+//           the verifier score;
+//   exchange the CTA's statistics go to every CTA of the cluster through distributed shared
+//           memory; one warp combines the C partials in rank order, so every CTA holds bit-identical
+//           row statistics (log-sum-exps, the lse difference used below, the argmax);
+//   pass B  re-reads the slice of the divergence pair (a and b; SCI: draft and target), which the
+//           L2 cache still holds from pass A (the resident CTAs' slices are a few tens of MB), and
+//           sums the per-entry Jensen-Shannon terms;
+//   finish  every CTA pushes its pass-B sums into CTA 0 and leaves; CTA 0 finalises the row (gate,
+//           outputs, a 16-byte row record) and takes a ticket on the request's counter.  The last of
+//           the K+1 rows to finish runs the left-to-right scan and resets the counter, so the whole
+//           step is one launch with no spin-waits.
+// Without shared-memory staging a CTA needs only registers, so several CTAs share an SM and hide
+// each other's exchanges.  Arithmetic on entries is two-lane packed fp32 (fma/add/mul/sub .f32x2)
+// where it pairs up.  Sums that cross warps and CTAs are carried as compensated fp32 pairs: this
+// GPU's fp64 rate is a small fraction of its fp32 rate, so fp64 appears only in CTA 0's few
+// finalisation steps.
 //
-// Numerics.  Inputs are widened exactly to fp32.  exp(x - M) is formed as ex2(fma(x, log2e, -M*log2e)),
-// whose constant rounding error c is known exactly and removed from the log-sum-exp; the divergence
-// sums use the same form, so the factor cancels in their ratio with the row sums.  The gate is
-// decided in double in the log domain.  The per-entry divergence term is evaluated from
-// u = (xb - xa) - (lse_b - lse_a):
+// Numerics.  Inputs are widened exactly to fp32.  exp(x - M) is formed as ex2(fma(x, log2e, -M*log2e))
+// against the current reference maximum; partial sums move between references with exp2f of the
+// difference of the (rounded) references, and the row sums end up against ML = M*log2e rounded, the
+// reference pass B uses, so the divergence sums and the row sums share one scale.  The constant
+// rounding error of ML is removed from the log-sum-exps.  The gate is decided in double in the log
+// domain.  The per-entry divergence term is evaluated from u = (xb - xa) - (lse_b - lse_a):
 //   narrow form (|u| <= 2, AsymSpec's pair): p * u^2 * P(u), P a fitted polynomial;
 //   wide form (any u): max(p,q) * (A(r) - |u| r), r = exp(-|u|), A(r) = (1-r) B(r).
 // Both are sums of non-negative terms (no cancellation between large entropies), and identical rows
@@ -47,32 +50,25 @@
 #include "asv_internal.h"
 #include "jsd_poly.inc"
 
-// Polynomial evaluation in the narrow divergence form: 0 packed with coefficient immediates,
-// 1 packed with the coefficient pairs held in registers, 2 scalar with immediates.
-#ifndef ASV_POLY_MODE
-#define ASV_POLY_MODE 1
-#endif
-
 namespace asv {
 
+constexpr int kJsdThreads = 256;  // threads per CTA the kernel is compiled for (launch bounds)
+
 struct __align__(16) JsdXchg {
-  float mx[3];        // slice maxima of the inputs
-  float argv;         // best verifier score in the slice
-  int32_t argi;       // its vocabulary index
-  float sum_hi[3];    // slice sums of ex2(fma(x, log2e, -M*log2e)) as hi + lo
+  float mx[3];        // CTA maxima of the inputs
+  float sum_hi[3];    // CTA sums of exp2(x log2e - mL_cta), mL_cta = mx * log2e rounded, as hi + lo
   float sum_lo[3];
-  // Pushed into CTA 0 by every CTA before the third exchange, so that CTA 0 alone reads
-  // them afterwards and the other CTAs can leave:
-  float jsd_from[kMaxCluster][4];  // slice divergence sums: p-form hi, lo, q-form hi, lo
-  uint32_t err_from[kMaxCluster];  // a staged-data wait expired in that CTA
-  float td, bd;                    // t_d and b_d, from the CTA that staged entry d
+  float argv;         // best verifier score in the CTA's slice
+  int32_t argi;       // its vocabulary index
+  // Pushed into CTA 0 by every CTA before the second exchange; only CTA 0 reads them afterwards.
+  float jsd_from[kMaxCluster][4];  // pass-B sums: p-form hi, lo, q-form hi, lo
 };
 
-// Row constants, computed by one thread after each cluster exchange and broadcast through shared memory.
+// Row constants, computed by one thread after the exchange and broadcast through shared memory.
 struct __align__(16) JsdRowConsts {
   float M[3];
   float ML[3];     // M * log2e, rounded
-  float S_hi[3];   // row sums of ex2(fma(x, log2e, -ML)) as hi + lo
+  float S_hi[3];   // row sums of exp2(x log2e - ML) as hi + lo
   float S_lo[3];
   float dL;        // lse_b - lse_a (pair inputs 1 and 0)
   int32_t finite;
@@ -82,13 +78,117 @@ struct __align__(16) JsdRowConsts {
 
 template <int MODE>
 struct JsdTraits {
-  static constexpr int NT = (MODE == kModeAsym) ? 3 : 2;  // staged inputs
+  static constexpr int NT = (MODE == kModeAsym) ? 3 : 2;  // streamed inputs
   static constexpr int TGT = NT - 1;                       // index of the verifier/target input
   static constexpr bool kWide = (MODE == kModeSci);        // divergence term form
 };
 
-// Per-entry Jensen-Shannon contribution, accumulated un-normalised:
-// acc_p += exp(xa - Ma) * f(u) for entries in p-form, acc_q += exp(xb - Mb) * f(-u) in q-form.
+// ------------------------------------------------------------------ global vector access
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+// A 16-byte vector of one input: 8 bf16 or 4 fp32 entries, as raw words.
+template <typename T>
+struct GVec;
+
+template <>
+struct GVec<bf16_t> {
+  static constexpr int kVec = 8;
+  static constexpr int kPairs = 4;
+  static constexpr int kBytes = 2;
+  __device__ static __forceinline__ uint4 pad() {
+    return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+  }
+  // Entries [k, k+8) of a row slice; `aligned` slices use one 16-byte load, others ordinary loads
+  // with -inf at and beyond `lim`.
+  __device__ static __forceinline__ uint4 load(const void* base, int k, int lim, bool aligned) {
+    const uint16_t* r = static_cast<const uint16_t*>(base);
+    if (aligned) return ldg_stream(r + k);
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = (k + 2 * i < lim) ? uint32_t(__ldg(r + k + 2 * i)) : 0xff80u;
+      const uint32_t hi = (k + 2 * i + 1 < lim) ? uint32_t(__ldg(r + k + 2 * i + 1)) : 0xff80u;
+      w[i] = lo | (hi << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  __device__ static __forceinline__ void pairs(const uint4& v, float2 (&x)[4]) {
+    x[0] = make_float2(bf16_lo(v.x), bf16_hi(v.x));
+    x[1] = make_float2(bf16_lo(v.y), bf16_hi(v.y));
+    x[2] = make_float2(bf16_lo(v.z), bf16_hi(v.z));
+    x[3] = make_float2(bf16_lo(v.w), bf16_hi(v.w));
+  }
+  __device__ static __forceinline__ float at(const void* base, size_t k) {
+    return __uint_as_float(uint32_t(__ldg(static_cast<const uint16_t*>(base) + k)) << 16);
+  }
+};
+
+template <>
+struct GVec<float> {
+  static constexpr int kVec = 4;
+  static constexpr int kPairs = 2;
+  static constexpr int kBytes = 4;
+  __device__ static __forceinline__ uint4 pad() {
+    return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+  }
+  __device__ static __forceinline__ uint4 load(const void* base, int k, int lim, bool aligned) {
+    const float* r = static_cast<const float*>(base);
+    if (aligned) return ldg_stream(r + k);
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = (k + i < lim) ? __float_as_uint(__ldg(r + k + i)) : 0xff800000u;
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  __device__ static __forceinline__ void pairs(const uint4& v, float2 (&x)[2]) {
+    x[0] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+    x[1] = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+  }
+  __device__ static __forceinline__ float at(const void* base, size_t k) {
+    return __ldg(static_cast<const float*>(base) + k);
+  }
+};
+
+// Running maximum of one input over the vectors a thread has seen.  bf16 keeps it as two-lane
+// bf16x2 maxima of the raw words (exact; a change is one integer comparison), fp32 as a float.
+template <typename T>
+struct RunMax;
+
+template <>
+struct RunMax<bf16_t> {
+  uint32_t m2 = 0xff80ff80u;
+  __device__ __forceinline__ bool update(const uint4& v) {
+    const uint32_t n = bmax2(m2, bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w)));
+    const bool changed = (n != m2);
+    m2 = n;
+    return changed;
+  }
+  __device__ __forceinline__ float value() const { return fmaxf(bf16_lo(m2), bf16_hi(m2)); }
+};
+
+template <>
+struct RunMax<float> {
+  float m = -INFINITY;
+  __device__ __forceinline__ bool update(const uint4& v) {
+    const float n = fmaxf(fmaxf(m, fmaxf(__uint_as_float(v.x), __uint_as_float(v.y))),
+                          fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+    const bool changed = (n > m);
+    m = n;
+    return changed;
+  }
+  __device__ __forceinline__ float value() const { return m; }
+};
+
+// ------------------------------------------------------------------ per-entry divergence term
+
+// Accumulated un-normalised: acc_p += exp(xa - Ma) * f(u) in p-form, acc_q += exp(xb - Mb) * f(-u)
+// in q-form (wide form only).
 template <bool WIDE>
 __device__ __forceinline__ void jsd_entry(float xa, float xb, float dL, float MaL, float MbL, float& acc_p,
                                           float& acc_q) {
@@ -125,6 +225,10 @@ __device__ __forceinline__ float warp_sumf(float v) {
   return v;
 }
 
+// Reference for exponentials against a maximum M: M * log2e, or 0 while M is -inf (then every
+// exponential is exp2(-inf) = 0 and a finite stand-in avoids inf - inf).
+__device__ __forceinline__ float ref_of(float M) { return isfinite(M) ? M * kLog2e : 0.0f; }
+
 // The context-gain signal for the delta-fusion score: 0 -> a - b, 1 -> a, 2 -> t - b.
 template <int DSRC>
 __device__ __forceinline__ float2 delta2(float2 a, float2 b, float2 t) {
@@ -134,27 +238,23 @@ __device__ __forceinline__ float2 delta2(float2 a, float2 b, float2 t) {
 }
 
 template <typename T, int MODE, int DSRC>
-__global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
-  using E = Elem<T>;
-  using S = typename E::storage;
+__global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArgs p) {
+  using G = GVec<T>;
   constexpr int NT = JsdTraits<MODE>::NT;
   constexpr int TGT = JsdTraits<MODE>::TGT;
-  constexpr int VEC = E::kVec;
-  constexpr int NP = E::kPairs;
+  constexpr int VEC = G::kVec;
+  constexpr int NP = G::kPairs;
+  constexpr int kWarps = kJsdThreads / 32;
 
-  extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ JsdXchg xchg;
   __shared__ JsdRowConsts rc;
-  __shared__ float s_wf[32][4];
-  __shared__ int32_t s_wi[32];
-  __shared__ __align__(8) uint64_t s_bar[kNumChunks];
-  __shared__ uint32_t s_err;
+  __shared__ float s_wf[kWarps][4];
+  __shared__ int32_t s_wi[kWarps];
+  __shared__ float s_wm[kWarps][3];
 
   const int tid = threadIdx.x;
-  const int nthr = blockDim.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int nwarps = nthr >> 5;
   const uint32_t rank = cluster_rank();
   const uint32_t C = cluster_size();
   const int row = blockIdx.x / C;
@@ -165,148 +265,62 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
   const int v0 = int(rank) * p.n_slice;
   const int len = max(0, min(V - v0, p.n_slice));
   const int nvec = (len + VEC - 1) / VEC;
+  const bool aligned = p.bulk != 0;
   const size_t row_base = size_t(row) * size_t(V);
-  const size_t stage_stride = (size_t(p.n_slice) * sizeof(S) + 127) & ~size_t(127);
 
-  S* stage[NT];
+  const void* slice[NT];
 #pragma unroll
-  for (int j = 0; j < NT; ++j) stage[j] = reinterpret_cast<S*>(smem_raw + j * stage_stride);
+  for (int j = 0; j < NT; ++j) slice[j] = static_cast<const char*>(p.x[j]) + (row_base + size_t(v0)) * G::kBytes;
 
-  const int chunk_vec = (nvec + kNumChunks - 1) / kNumChunks;
-
-  // ---------------------------------------------------------------- staging
-  if (tid == 0) {
-    s_err = 0;
+  // ---------------------------------------------------------------- pass A: maxima, exp sums, argmax
+  RunMax<T> rmax[NT];
+  float mL[NT];
+  float2 acc[NT];
 #pragma unroll
-    for (int c = 0; c < kNumChunks; ++c) mbar_init(smem_addr(&s_bar[c]), 1);
-    fence_mbar_init();
+  for (int j = 0; j < NT; ++j) {
+    mL[j] = 0.0f;
+    acc[j] = make_float2(0.0f, 0.0f);
   }
-  __syncthreads();
-  if (p.bulk) {
-    if (tid == 0) {
-      for (int c = 0; c < kNumChunks; ++c) {
-        const int cv0 = c * chunk_vec;
-        const int cv1 = min(nvec, cv0 + chunk_vec);
-        if (cv1 <= cv0) break;
-        const uint32_t bytes = uint32_t(cv1 - cv0) * VEC * sizeof(S);
-        const uint32_t bar = smem_addr(&s_bar[c]);
-        mbar_arrive_expect_tx(bar, bytes * NT);
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          const S* src = reinterpret_cast<const S*>(p.x[j]) + row_base + v0 + size_t(cv0) * VEC;
-          bulk_g2s(smem_addr(stage[j] + size_t(cv0) * VEC), src, bytes, bar);
-        }
-      }
-    }
-  } else {
-    // Unaligned rows: ordinary loads, the slice padded to the vector width with -inf.
-    const int npad = nvec * VEC;
-    for (int k = tid; k < npad; k += nthr) {
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        const S* src = reinterpret_cast<const S*>(p.x[j]);
-        stage[j][k] = (k < len) ? src[row_base + v0 + k] : E::neg_inf();
-      }
-    }
-    __syncthreads();
-  }
-
-  // ---------------------------------------------------------------- sweep 1: maxima
-  float mx[NT];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) mx[j] = -INFINITY;
-  if constexpr (std::is_same<T, bf16_t>::value) {
-    uint32_t m2[NT];
-#pragma unroll
-    for (int j = 0; j < NT; ++j) m2[j] = 0xff80ff80u;
-    for (int c = 0; c < kNumChunks; ++c) {
-      const int cv0 = c * chunk_vec;
-      const int cv1 = min(nvec, cv0 + chunk_vec);
-      if (cv1 <= cv0) break;
-      if (p.bulk && !mbar_wait(smem_addr(&s_bar[c]), 0, kWaitPolls)) atomicOr(&s_err, 1u);
-      for (int vi = cv0 + tid; vi < cv1; vi += nthr) {
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          const uint4 w = reinterpret_cast<const uint4*>(stage[j])[vi];
-          m2[j] = bmax2(bmax2(m2[j], w.x), bmax2(w.y, bmax2(w.z, w.w)));
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < NT; ++j) mx[j] = fmaxf(bf16_lo(m2[j]), bf16_hi(m2[j]));
-  } else {
-    for (int c = 0; c < kNumChunks; ++c) {
-      const int cv0 = c * chunk_vec;
-      const int cv1 = min(nvec, cv0 + chunk_vec);
-      if (cv1 <= cv0) break;
-      if (p.bulk && !mbar_wait(smem_addr(&s_bar[c]), 0, kWaitPolls)) atomicOr(&s_err, 1u);
-      for (int vi = cv0 + tid; vi < cv1; vi += nthr) {
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          const float4 v = reinterpret_cast<const float4*>(stage[j])[vi];
-          mx[j] = fmaxf(fmaxf(mx[j], v.x), fmaxf(v.y, fmaxf(v.z, v.w)));
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < NT; ++j) mx[j] = warp_max(mx[j]);
-  if (lane == 0) {
-#pragma unroll
-    for (int j = 0; j < NT; ++j) s_wf[warp][j] = mx[j];
-  }
-  __syncthreads();
-  if (warp == 0) {
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      const float v = warp_max(lane < nwarps ? s_wf[lane][j] : -INFINITY);
-      if (lane == 0) xchg.mx[j] = v;
-    }
-  }
-  cluster_sync_w0(warp);  // #1
-  if (warp == 0) {
-    // lane q < C reads CTA q's maxima; a warp max combines them.
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      float v = -INFINITY;
-      if (lane < int(C)) v = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.mx[j]), uint32_t(lane)));
-      v = warp_max(v);
-      if (lane == 0) {
-        rc.M[j] = v;
-        rc.ML[j] = isfinite(v) ? v * kLog2e : 0.0f;
-      }
-    }
-  }
-  __syncthreads();
-  float ML[NT];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) ML[j] = rc.ML[j];
-
-  // ---------------------------------------------------------------- sweep 2: exponential sums + argmax
+  float bv = -INFINITY;
+  int bi = INT_MAX;
   {
     const float2 l2e2 = make_float2(kLog2e, kLog2e);
     const float2 beta2 = make_float2(p.beta, p.beta);
-    float2 nml[NT], acc[NT];
+    uint4 cur[NT], nxt[NT];
+    int vi = tid;
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      nml[j] = make_float2(-ML[j], -ML[j]);
-      acc[j] = make_float2(0.0f, 0.0f);
-    }
-    float bv = -INFINITY;
-    int bi = INT_MAX;
-    for (int vi = tid; vi < nvec; vi += nthr) {
+    for (int j = 0; j < NT; ++j) cur[j] = (vi < nvec) ? G::load(slice[j], vi * VEC, len, aligned) : G::pad();
+    for (; vi < nvec; vi += kJsdThreads) {
+      const int vn = vi + kJsdThreads;
+#pragma unroll
+      for (int j = 0; j < NT; ++j) nxt[j] = (vn < nvec) ? G::load(slice[j], vn * VEC, len, aligned) : G::pad();
+      // Running maxima; on the rare growth move the partial sum to the new reference.
+      bool grew = false;
+#pragma unroll
+      for (int j = 0; j < NT; ++j) grew |= rmax[j].update(cur[j]);
+      if (grew) {
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const float nL = ref_of(rmax[j].value());
+          if (nL != mL[j]) {
+            const float f = (acc[j].x != 0.0f || acc[j].y != 0.0f) ? exp2f(mL[j] - nL) : 0.0f;
+            acc[j] = fmul2(acc[j], make_float2(f, f));
+            mL[j] = nL;
+          }
+        }
+      }
       float2 x[NT][NP];
 #pragma unroll
-      for (int j = 0; j < NT; ++j) E::load_pairs(stage[j], vi, x[j]);
+      for (int j = 0; j < NT; ++j) G::pairs(cur[j], x[j]);
 #pragma unroll
       for (int q2 = 0; q2 < NP; ++q2) {
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-          const float2 y = ffma2(x[j][q2], l2e2, nml[j]);
+          const float2 y = ffma2(x[j][q2], l2e2, make_float2(-mL[j], -mL[j]));
           acc[j] = fadd2(acc[j], make_float2(ex2_approx(y.x), ex2_approx(y.y)));
         }
       }
-      // Verifier score of the vector's entries; one comparison per vector against the best so far.
+      // Verifier score; one comparison per vector against the best so far.
       float2 sc[NP];
 #pragma unroll
       for (int q2 = 0; q2 < NP; ++q2) {
@@ -326,27 +340,45 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
         bv = vm;
         bi = v0 + vi * VEC + e_first;
       }
-    }
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      const float v = warp_sumf(acc[j].x + acc[j].y);
-      if (lane == 0) s_wf[warp][j] = v;
+      for (int j = 0; j < NT; ++j) cur[j] = nxt[j];
     }
-    warp_argmax(bv, bi);
-    if (lane == 0) {
-      s_wf[warp][3] = bv;
-      s_wi[warp] = bi;
-    }
+  }
+
+  // CTA maxima, then every thread moves its sum to the CTA reference and the sums are added.
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const float w = warp_max(rmax[j].value());
+    if (lane == 0) s_wm[warp][j] = w;
+  }
+  warp_argmax(bv, bi);
+  if (lane == 0) {
+    s_wf[warp][3] = bv;
+    s_wi[warp] = bi;
+  }
+  __syncthreads();
+  float Mc[NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    float m = s_wm[0][j];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) m = fmaxf(m, s_wm[w][j]);
+    Mc[j] = m;
+    const float s = acc[j].x + acc[j].y;
+    const float moved = (s != 0.0f) ? s * exp2f(mL[j] - ref_of(m)) : 0.0f;
+    const float ws = warp_sumf(moved);
+    if (lane == 0) s_wf[warp][j] = ws;
   }
   __syncthreads();
   if (warp == 0) {
-    float v2 = (lane < nwarps) ? s_wf[lane][3] : -INFINITY;
-    int i2 = (lane < nwarps) ? s_wi[lane] : INT_MAX;
+    float v2 = (lane < kWarps) ? s_wf[lane][3] : -INFINITY;
+    int i2 = (lane < kWarps) ? s_wi[lane] : INT_MAX;
     warp_argmax(v2, i2);
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      const DF d = warp_sum_df(DF{lane < nwarps ? s_wf[lane][j] : 0.0f, 0.0f});
+      const DF d = warp_sum_df(DF{lane < kWarps ? s_wf[lane][j] : 0.0f, 0.0f});
       if (lane == 0) {
+        xchg.mx[j] = Mc[j];
         xchg.sum_hi[j] = d.hi;
         xchg.sum_lo[j] = d.lo;
       }
@@ -356,41 +388,59 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
       xchg.argi = i2;
     }
   }
-  cluster_sync_w0(warp);  // #2
+  cluster_sync_w0(warp);  // #1
+
+  // ---------------------------------------------------------------- row statistics (warp 0)
   if (warp == 0) {
+    // lane q < C holds CTA q's partials; move every CTA's sums to the row reference, then add.
+    float mq[NT];
+    DF sq[NT];
     float v2 = -INFINITY;
     int i2 = INT_MAX;
-    if (lane < int(C)) {
-      v2 = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.argv), uint32_t(lane)));
-      i2 = dsmem_ld_s32(dsmem_map(smem_addr(&xchg.argi), uint32_t(lane)));
-    }
-    warp_argmax(v2, i2);
-    DF Sj[NT];
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      DF d{0.0f, 0.0f};
-      if (lane < int(C)) {
-        d.hi = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.sum_hi[j]), uint32_t(lane)));
-        d.lo = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.sum_lo[j]), uint32_t(lane)));
+      mq[j] = -INFINITY;
+      sq[j] = DF{0.0f, 0.0f};
+    }
+    if (lane < int(C)) {
+      const uint32_t q = uint32_t(lane);
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        mq[j] = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.mx[j]), q));
+        sq[j].hi = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.sum_hi[j]), q));
+        sq[j].lo = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.sum_lo[j]), q));
       }
-      Sj[j] = warp_sum_df(d);
+      v2 = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.argv), q));
+      i2 = dsmem_ld_s32(dsmem_map(smem_addr(&xchg.argi), q));
+    }
+    warp_argmax(v2, i2);
+    DF S[NT];
+    float M[NT], MLr[NT];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      M[j] = warp_max(mq[j]);
+      MLr[j] = ref_of(M[j]);
+      const float f = (sq[j].hi != 0.0f) ? exp2f(ref_of(mq[j]) - MLr[j]) : 0.0f;
+      S[j] = warp_sum_df(DF{sq[j].hi * f, sq[j].lo * f});
     }
     if (lane == 0) {
       bool finite = true;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
-        finite = finite && isfinite(rc.M[j]) && isfinite(Sj[j].hi) && Sj[j].hi > 0.0f;
-        rc.S_hi[j] = Sj[j].hi;
-        rc.S_lo[j] = Sj[j].lo;
+        finite = finite && isfinite(M[j]) && isfinite(S[j].hi) && S[j].hi > 0.0f;
+        rc.M[j] = M[j];
+        rc.ML[j] = MLr[j];
+        rc.S_hi[j] = S[j].hi;
+        rc.S_lo[j] = S[j].lo;
       }
       // lse_b - lse_a = (Mb - Ma) + ln(Sb / Sa) - (cb - ca) ln2, c = fma(M, log2e, -ML) the exact
-      // rounding error of ML (the sums carry a factor 2^c).
+      // rounding error of ML (the sums are against ML).
       float dL = 0.0f;
       if (finite) {
-        const float ca = fmaf(rc.M[0], kLog2e, -rc.ML[0]);
-        const float cb = fmaf(rc.M[1], kLog2e, -rc.ML[1]);
-        const float ratio = (Sj[1].hi + Sj[1].lo) / (Sj[0].hi + Sj[0].lo);
-        dL = (rc.M[1] - rc.M[0]) + (ln_split(ratio) - (cb - ca) * kLn2f);
+        const float ca = fmaf(M[0], kLog2e, -MLr[0]);
+        const float cb = fmaf(M[1], kLog2e, -MLr[1]);
+        const float ratio = (S[1].hi + S[1].lo) / (S[0].hi + S[0].lo);
+        dL = (M[1] - M[0]) + (ln_split(ratio) - (cb - ca) * kLn2f);
       }
       rc.finite = finite ? 1 : 0;
       rc.dL = dL;
@@ -400,55 +450,60 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
   }
   __syncthreads();
 
-  // ---------------------------------------------------------------- sweep 3: divergence terms
+  // ---------------------------------------------------------------- pass B: divergence terms
   {
     const bool finite = rc.finite != 0;
     const float dL = rc.dL;
+    const float ML0 = rc.ML[0], ML1 = rc.ML[1];
     float ap0 = 0.0f, ap1 = 0.0f, aq0 = 0.0f, aq1 = 0.0f;
     if (finite) {
+      int vi = tid;
+      uint4 ca = (vi < nvec) ? G::load(slice[0], vi * VEC, len, aligned) : G::pad();
+      uint4 cb = (vi < nvec) ? G::load(slice[1], vi * VEC, len, aligned) : G::pad();
       if constexpr (!JsdTraits<MODE>::kWide) {
         const float2 l2e2 = make_float2(kLog2e, kLog2e);
         const float2 dl2 = make_float2(dL, dL);
-        const float2 nmal = make_float2(-ML[0], -ML[0]);
-#if ASV_POLY_MODE == 1
-        const asv_jsd_poly2h_coeffs pk = asv_jsd_poly2h_load();
-#endif
+        const float2 nmal = make_float2(-ML0, -ML0);
         float2 accp = make_float2(0.0f, 0.0f);
-        for (int vi = tid; vi < nvec; vi += nthr) {
+        for (; vi < nvec; vi += kJsdThreads) {
+          const int vn = vi + kJsdThreads;
+          const uint4 na = (vn < nvec) ? G::load(slice[0], vn * VEC, len, aligned) : G::pad();
+          const uint4 nb = (vn < nvec) ? G::load(slice[1], vn * VEC, len, aligned) : G::pad();
           float2 xa[NP], xb[NP];
-          E::load_pairs(stage[0], vi, xa);
-          E::load_pairs(stage[1], vi, xb);
+          G::pairs(ca, xa);
+          G::pairs(cb, xb);
 #pragma unroll
           for (int q2 = 0; q2 < NP; ++q2) {
             const float2 u = fsub2(fsub2(xb[q2], xa[q2]), dl2);
             if (fabsf(u.x) <= ASV_JSD_POLY_U0 && fabsf(u.y) <= ASV_JSD_POLY_U0) {
               const float2 y = ffma2(xa[q2], l2e2, nmal);
               const float2 ep = make_float2(ex2_approx(y.x), ex2_approx(y.y));
-#if ASV_POLY_MODE == 1
-              accp = ffma2(fmul2(ep, fmul2(u, u)), asv_jsd_poly2h(u, pk), accp);
-#elif ASV_POLY_MODE == 2
-              accp = ffma2(fmul2(ep, fmul2(u, u)), make_float2(asv_jsd_poly(u.x), asv_jsd_poly(u.y)), accp);
-#else
               accp = ffma2(fmul2(ep, fmul2(u, u)), asv_jsd_poly2(u), accp);
-#endif
             } else {
-              jsd_entry<false>(xa[q2].x, xb[q2].x, dL, ML[0], ML[1], ap0, aq0);
-              jsd_entry<false>(xa[q2].y, xb[q2].y, dL, ML[0], ML[1], ap1, aq1);
+              jsd_entry<false>(xa[q2].x, xb[q2].x, dL, ML0, ML1, ap0, aq0);
+              jsd_entry<false>(xa[q2].y, xb[q2].y, dL, ML0, ML1, ap1, aq1);
             }
           }
+          ca = na;
+          cb = nb;
         }
         ap0 += accp.x;
         ap1 += accp.y;
       } else {
-        for (int vi = tid; vi < nvec; vi += nthr) {
+        for (; vi < nvec; vi += kJsdThreads) {
+          const int vn = vi + kJsdThreads;
+          const uint4 na = (vn < nvec) ? G::load(slice[0], vn * VEC, len, aligned) : G::pad();
+          const uint4 nb = (vn < nvec) ? G::load(slice[1], vn * VEC, len, aligned) : G::pad();
           float2 xa[NP], xb[NP];
-          E::load_pairs(stage[0], vi, xa);
-          E::load_pairs(stage[1], vi, xb);
+          G::pairs(ca, xa);
+          G::pairs(cb, xb);
 #pragma unroll
           for (int q2 = 0; q2 < NP; ++q2) {
-            jsd_entry<true>(xa[q2].x, xb[q2].x, dL, ML[0], ML[1], ap0, aq0);
-            jsd_entry<true>(xa[q2].y, xb[q2].y, dL, ML[0], ML[1], ap1, aq1);
+            jsd_entry<true>(xa[q2].x, xb[q2].x, dL, ML0, ML1, ap0, aq0);
+            jsd_entry<true>(xa[q2].y, xb[q2].y, dL, ML0, ML1, ap1, aq1);
           }
+          ca = na;
+          cb = nb;
         }
       }
     }
@@ -460,45 +515,26 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
     }
   }
   __syncthreads();
-  const int dpos = (pos < p.K) ? p.draft_ids[size_t(req) * p.K + pos] : -1;
   if (warp == 0) {
-    const DF dp = warp_sum_df(DF{lane < nwarps ? s_wf[lane][0] : 0.0f, 0.0f});
-    const DF dq = warp_sum_df(DF{lane < nwarps ? s_wf[lane][1] : 0.0f, 0.0f});
+    const DF dp = warp_sum_df(DF{lane < kWarps ? s_wf[lane][0] : 0.0f, 0.0f});
+    const DF dq = warp_sum_df(DF{lane < kWarps ? s_wf[lane][1] : 0.0f, 0.0f});
     if (lane == 0) {
-      // Push this CTA's partials into CTA 0.
+      // Push this CTA's pass-B sums into CTA 0.
       const uint32_t base = smem_addr(&xchg.jsd_from[rank][0]);
       dsmem_st_f32(dsmem_map(base + 0, 0), dp.hi);
       dsmem_st_f32(dsmem_map(base + 4, 0), dp.lo);
       dsmem_st_f32(dsmem_map(base + 8, 0), dq.hi);
       dsmem_st_f32(dsmem_map(base + 12, 0), dq.lo);
-      dsmem_st_u32(dsmem_map(smem_addr(&xchg.err_from[rank]), 0), s_err);
-      // The CTA that staged the draft's entry pushes t_d and b_d.
-      if (MODE == kModeAsym && dpos >= v0 && dpos < v0 + len) {
-        const int off = dpos - v0;
-        dsmem_st_f32(dsmem_map(smem_addr(&xchg.td), 0), E::to_float(stage[NT - 1][off]));
-        dsmem_st_f32(dsmem_map(smem_addr(&xchg.bd), 0), E::to_float(stage[1][off]));
-      }
     }
   }
-  cluster_sync_w0(warp);  // #3: after this only CTA 0 touches shared memory, and only its own
-
-  // A CTA whose staged-data wait expired waits (bounded) for its copies before leaving.
-  if (p.bulk && tid == 0 && s_err) {
-    for (int c = 0; c < kNumChunks; ++c) {
-      const int cv0 = c * chunk_vec;
-      if (min(nvec, cv0 + chunk_vec) <= cv0) break;
-      mbar_wait(smem_addr(&s_bar[c]), 0, kWaitPolls);
-    }
-  }
+  cluster_sync_w0(warp);  // #2: after this only CTA 0 touches shared memory, and only its own
   if (rank != 0 || tid != 0) return;
 
   // ---------------------------------------------------------------- row finalisation (CTA 0)
   DF jp{0.0f, 0.0f}, jq{0.0f, 0.0f};
-  uint32_t err = 0;
   for (uint32_t q = 0; q < C; ++q) {
     jp = df_add(jp, DF{xchg.jsd_from[q][0], xchg.jsd_from[q][1]});
     jq = df_add(jq, DF{xchg.jsd_from[q][2], xchg.jsd_from[q][3]});
-    err |= xchg.err_from[q];
   }
   const bool finite = rc.finite != 0;
   float D = 0.0f;
@@ -515,13 +551,15 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
   }
   uint32_t bits = 0;
   if (!finite) bits |= kBitNonfinite;
-  if (err) bits |= kBitTimeout;
   const int token = (rc.rowi == INT_MAX) ? 0 : rc.rowi;
   if (pos < p.K) {
-    if (dpos < 0 || dpos >= V) {
+    const int d = p.draft_ids[size_t(req) * p.K + pos];
+    if (d < 0 || d >= V) {
       bits |= kBitBadDraft;
     } else if (MODE == kModeAsym && finite) {
-      const double margin = (double(xchg.td) - lse[NT - 1]) - p.ln_gamma + double(D) - (double(xchg.bd) - lse[1]);
+      const float td = G::at(p.x[NT - 1], row_base + size_t(d));
+      const float bd = G::at(p.x[1], row_base + size_t(d));
+      const double margin = (double(td) - lse[NT - 1]) - p.ln_gamma + double(D) - (double(bd) - lse[1]);
       if (margin > 0.0) bits |= kBitAccept;
     }
   }
@@ -543,8 +581,7 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
     const volatile RowRecord* recs = p.records + size_t(req) * R1;
     uint32_t any = 0;
     for (int i = 0; i < R1; ++i) any |= recs[i].bits;
-    const uint32_t status = ((any & kBitNonfinite) ? 1u : 0u) | ((any & kBitBadDraft) ? 2u : 0u) |
-                            ((any & kBitTimeout) ? 4u : 0u);
+    const uint32_t status = ((any & kBitNonfinite) ? 1u : 0u) | ((any & kBitBadDraft) ? 2u : 0u);
     int32_t* toks = p.out_tokens + size_t(req) * R1;
     double thr = 0.0;
     if (MODE == kModeSci) {
@@ -577,9 +614,8 @@ __global__ void __launch_bounds__(512) jsd_family_kernel(const JsdArgs p) {
   }
 }
 
-int jsd_static_smem_bytes() {
-  return int(sizeof(JsdXchg) + sizeof(JsdRowConsts) + 32 * 4 * 4 + 32 * 4 + kNumChunks * 8 + 4 + 64);
-}
+int jsd_static_smem_bytes() { return 0; }
+int jsd_threads() { return kJsdThreads; }
 
 using JsdKernel = void (*)(const JsdArgs);
 
@@ -598,8 +634,8 @@ static JsdKernel pick_kernel(int mode, int dtype, int dsrc) {
 static cudaLaunchConfig_t make_config(const LaunchPlan& plan, unsigned grid, cudaStream_t s, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(unsigned(plan.threads), 1, 1);
-  cfg.dynamicSmemBytes = size_t(plan.smem);
+  cfg.blockDim = dim3(unsigned(kJsdThreads), 1, 1);
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = unsigned(plan.cluster);
@@ -611,10 +647,8 @@ static cudaLaunchConfig_t make_config(const LaunchPlan& plan, unsigned grid, cud
 }
 
 static cudaError_t prepare(JsdKernel kern, const LaunchPlan& plan) {
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem);
-  if (e != cudaSuccess) return e;
-  if (plan.cluster > 8) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  return e;
+  if (plan.cluster > 8) return cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return cudaSuccess;
 }
 
 cudaError_t launch_jsd_family(int mode, int dtype, const JsdArgs& a, const LaunchPlan& plan, cudaStream_t s) {
