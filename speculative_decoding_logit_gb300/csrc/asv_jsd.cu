@@ -237,7 +237,7 @@ __device__ __forceinline__ float2 delta2(float2 a, float2 b, float2 t) {
   else return fsub2(a, b);
 }
 
-template <typename T, int MODE, int DSRC>
+template <typename T, int MODE, int DSRC, bool ALIGNED>
 __global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArgs p) {
   using G = GVec<T>;
   constexpr int NT = JsdTraits<MODE>::NT;
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArg
   const int v0 = int(rank) * p.n_slice;
   const int len = max(0, min(V - v0, p.n_slice));
   const int nvec = (len + VEC - 1) / VEC;
-  const bool aligned = p.bulk != 0;
+  constexpr bool aligned = ALIGNED;
   const size_t row_base = size_t(row) * size_t(V);
 
   const void* slice[NT];
@@ -288,12 +288,17 @@ __global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArg
     const float2 beta2 = make_float2(p.beta, p.beta);
     uint4 cur[NT], nxt[NT];
     int vi = tid;
+    if (vi < nvec) {
 #pragma unroll
-    for (int j = 0; j < NT; ++j) cur[j] = (vi < nvec) ? G::load(slice[j], vi * VEC, len, aligned) : G::pad();
+      for (int j = 0; j < NT; ++j) cur[j] = G::load(slice[j], vi * VEC, len, aligned);
+    }
     for (; vi < nvec; vi += kJsdThreads) {
       const int vn = vi + kJsdThreads;
+      // Prefetch the next vector (consumed only while it is in range).
+      if (vn < nvec) {
 #pragma unroll
-      for (int j = 0; j < NT; ++j) nxt[j] = (vn < nvec) ? G::load(slice[j], vn * VEC, len, aligned) : G::pad();
+        for (int j = 0; j < NT; ++j) nxt[j] = G::load(slice[j], vn * VEC, len, aligned);
+      }
       // Running maxima; on the rare growth move the partial sum to the new reference.
       bool grew = false;
 #pragma unroll
@@ -458,8 +463,11 @@ __global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArg
     float ap0 = 0.0f, ap1 = 0.0f, aq0 = 0.0f, aq1 = 0.0f;
     if (finite) {
       int vi = tid;
-      uint4 ca = (vi < nvec) ? G::load(slice[0], vi * VEC, len, aligned) : G::pad();
-      uint4 cb = (vi < nvec) ? G::load(slice[1], vi * VEC, len, aligned) : G::pad();
+      uint4 ca, cb, na, nb;
+      if (vi < nvec) {
+        ca = G::load(slice[0], vi * VEC, len, aligned);
+        cb = G::load(slice[1], vi * VEC, len, aligned);
+      }
       if constexpr (!JsdTraits<MODE>::kWide) {
         const float2 l2e2 = make_float2(kLog2e, kLog2e);
         const float2 dl2 = make_float2(dL, dL);
@@ -467,8 +475,10 @@ __global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArg
         float2 accp = make_float2(0.0f, 0.0f);
         for (; vi < nvec; vi += kJsdThreads) {
           const int vn = vi + kJsdThreads;
-          const uint4 na = (vn < nvec) ? G::load(slice[0], vn * VEC, len, aligned) : G::pad();
-          const uint4 nb = (vn < nvec) ? G::load(slice[1], vn * VEC, len, aligned) : G::pad();
+          if (vn < nvec) {
+            na = G::load(slice[0], vn * VEC, len, aligned);
+            nb = G::load(slice[1], vn * VEC, len, aligned);
+          }
           float2 xa[NP], xb[NP];
           G::pairs(ca, xa);
           G::pairs(cb, xb);
@@ -492,8 +502,10 @@ __global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArg
       } else {
         for (; vi < nvec; vi += kJsdThreads) {
           const int vn = vi + kJsdThreads;
-          const uint4 na = (vn < nvec) ? G::load(slice[0], vn * VEC, len, aligned) : G::pad();
-          const uint4 nb = (vn < nvec) ? G::load(slice[1], vn * VEC, len, aligned) : G::pad();
+          if (vn < nvec) {
+            na = G::load(slice[0], vn * VEC, len, aligned);
+            nb = G::load(slice[1], vn * VEC, len, aligned);
+          }
           float2 xa[NP], xb[NP];
           G::pairs(ca, xa);
           G::pairs(cb, xb);
@@ -619,16 +631,22 @@ int jsd_threads() { return kJsdThreads; }
 
 using JsdKernel = void (*)(const JsdArgs);
 
-static JsdKernel pick_kernel(int mode, int dtype, int dsrc) {
-  if (mode == kModeSci) return dtype == 0 ? jsd_family_kernel<float, kModeSci, 0> : jsd_family_kernel<bf16_t, kModeSci, 0>;
+template <bool AL>
+static JsdKernel pick_aligned(int mode, int dtype, int dsrc) {
+  if (mode == kModeSci)
+    return dtype == 0 ? jsd_family_kernel<float, kModeSci, 0, AL> : jsd_family_kernel<bf16_t, kModeSci, 0, AL>;
   if (dtype == 0) {
-    if (dsrc == 1) return jsd_family_kernel<float, kModeAsym, 1>;
-    if (dsrc == 2) return jsd_family_kernel<float, kModeAsym, 2>;
-    return jsd_family_kernel<float, kModeAsym, 0>;
+    if (dsrc == 1) return jsd_family_kernel<float, kModeAsym, 1, AL>;
+    if (dsrc == 2) return jsd_family_kernel<float, kModeAsym, 2, AL>;
+    return jsd_family_kernel<float, kModeAsym, 0, AL>;
   }
-  if (dsrc == 1) return jsd_family_kernel<bf16_t, kModeAsym, 1>;
-  if (dsrc == 2) return jsd_family_kernel<bf16_t, kModeAsym, 2>;
-  return jsd_family_kernel<bf16_t, kModeAsym, 0>;
+  if (dsrc == 1) return jsd_family_kernel<bf16_t, kModeAsym, 1, AL>;
+  if (dsrc == 2) return jsd_family_kernel<bf16_t, kModeAsym, 2, AL>;
+  return jsd_family_kernel<bf16_t, kModeAsym, 0, AL>;
+}
+
+static JsdKernel pick_kernel(int mode, int dtype, int dsrc, bool aligned) {
+  return aligned ? pick_aligned<true>(mode, dtype, dsrc) : pick_aligned<false>(mode, dtype, dsrc);
 }
 
 static cudaLaunchConfig_t make_config(const LaunchPlan& plan, unsigned grid, cudaStream_t s, cudaLaunchAttribute* attr) {
@@ -652,7 +670,7 @@ static cudaError_t prepare(JsdKernel kern, const LaunchPlan& plan) {
 }
 
 cudaError_t launch_jsd_family(int mode, int dtype, const JsdArgs& a, const LaunchPlan& plan, cudaStream_t s) {
-  JsdKernel kern = pick_kernel(mode, dtype, a.delta_source);
+  JsdKernel kern = pick_kernel(mode, dtype, a.delta_source, a.bulk != 0);
   cudaError_t e = prepare(kern, plan);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
@@ -662,7 +680,7 @@ cudaError_t launch_jsd_family(int mode, int dtype, const JsdArgs& a, const Launc
 }
 
 int jsd_max_active_clusters(int mode, int dtype, const LaunchPlan& plan) {
-  JsdKernel kern = pick_kernel(mode, dtype, 0);
+  JsdKernel kern = pick_kernel(mode, dtype, 0, plan.bulk != 0);
   if (prepare(kern, plan) != cudaSuccess) return 0;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_config(plan, unsigned(plan.cluster), 0, attr);
