@@ -50,6 +50,11 @@
 #include "asv_internal.h"
 #include "jsd_poly.inc"
 
+// Running maxima taken from the unpacked fp32 values (1) or from bf16x2 maxima of the raw words (0).
+#ifndef ASV_MAX_FROM_FLOATS
+#define ASV_MAX_FROM_FLOATS 1
+#endif
+
 namespace asv {
 
 constexpr int kJsdThreads = 256;  // threads per CTA the kernel is compiled for (launch bounds)
@@ -274,10 +279,12 @@ __global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArg
 
   // ---------------------------------------------------------------- pass A: maxima, exp sums, argmax
   RunMax<T> rmax[NT];
+  float runm[NT];
   float mL[NT];
   float2 acc[NT];
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
+    runm[j] = -INFINITY;
     mL[j] = 0.0f;
     acc[j] = make_float2(0.0f, 0.0f);
   }
@@ -299,14 +306,32 @@ __global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArg
 #pragma unroll
         for (int j = 0; j < NT; ++j) nxt[j] = G::load(slice[j], vn * VEC, len, aligned);
       }
+      float2 x[NT][NP];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) G::pairs(cur[j], x[j]);
       // Running maxima; on the rare growth move the partial sum to the new reference.
       bool grew = false;
+#if ASV_MAX_FROM_FLOATS
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        float vmx = fmaxf(x[j][0].x, x[j][0].y);
+#pragma unroll
+        for (int q2 = 1; q2 < NP; ++q2) vmx = fmaxf(vmx, fmaxf(x[j][q2].x, x[j][q2].y));
+        grew |= (vmx > runm[j]);
+        runm[j] = fmaxf(runm[j], vmx);
+      }
+#else
 #pragma unroll
       for (int j = 0; j < NT; ++j) grew |= rmax[j].update(cur[j]);
+#endif
       if (grew) {
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
+#if ASV_MAX_FROM_FLOATS
+          const float nL = ref_of(runm[j]);
+#else
           const float nL = ref_of(rmax[j].value());
+#endif
           if (nL != mL[j]) {
             const float f = (acc[j].x != 0.0f || acc[j].y != 0.0f) ? exp2f(mL[j] - nL) : 0.0f;
             acc[j] = fmul2(acc[j], make_float2(f, f));
@@ -314,9 +339,6 @@ __global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArg
           }
         }
       }
-      float2 x[NT][NP];
-#pragma unroll
-      for (int j = 0; j < NT; ++j) G::pairs(cur[j], x[j]);
 #pragma unroll
       for (int q2 = 0; q2 < NP; ++q2) {
 #pragma unroll
@@ -353,7 +375,11 @@ __global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArg
   // CTA maxima, then every thread moves its sum to the CTA reference and the sums are added.
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
+#if ASV_MAX_FROM_FLOATS
+    const float w = warp_max(runm[j]);
+#else
     const float w = warp_max(rmax[j].value());
+#endif
     if (lane == 0) s_wm[warp][j] = w;
   }
   warp_argmax(bv, bi);
