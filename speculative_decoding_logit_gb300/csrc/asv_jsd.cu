@@ -50,11 +50,6 @@
 #include "asv_internal.h"
 #include "jsd_poly.inc"
 
-// Running maxima taken from the unpacked fp32 values (1) or from bf16x2 maxima of the raw words (0).
-#ifndef ASV_MAX_FROM_FLOATS
-#define ASV_MAX_FROM_FLOATS 1
-#endif
-
 namespace asv {
 
 constexpr int kJsdThreads = 256;  // threads per CTA the kernel is compiled for (launch bounds)
@@ -160,34 +155,51 @@ struct GVec<float> {
   }
 };
 
-// Running maximum of one input over the vectors a thread has seen.  bf16 keeps it as two-lane
-// bf16x2 maxima of the raw words (exact; a change is one integer comparison), fp32 as a float.
+// Running maximum of one input over the vectors a thread has seen, and the reference the
+// thread's exponentials are taken against.  The reference moves only when a value exceeds it by
+// more than kRefSlack (in log2 units): terms then stay below 2^kRefSlack, far from fp32 overflow,
+// and the rescale of the partial sum is needed about once per thread (on its first finite value)
+// instead of on every growth of the maximum.  bf16 compares raw bf16x2 words (exact), fp32 floats.
+constexpr float kRefSlack = 64.0f;
+
 template <typename T>
 struct RunMax;
 
 template <>
 struct RunMax<bf16_t> {
-  uint32_t m2 = 0xff80ff80u;
+  uint32_t m2 = 0xff80ff80u;   // two-lane running maximum
+  uint32_t thr2 = 0xff80ff80u; // two-lane bf16 threshold (rounded down): a larger value moves the reference
+  // Returns true when a value of the vector exceeds the threshold.
   __device__ __forceinline__ bool update(const uint4& v) {
-    const uint32_t n = bmax2(m2, bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w)));
-    const bool changed = (n != m2);
-    m2 = n;
-    return changed;
+    const uint32_t vm = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
+    m2 = bmax2(m2, vm);
+    return bmax2(vm, thr2) != thr2;
   }
   __device__ __forceinline__ float value() const { return fmaxf(bf16_lo(m2), bf16_hi(m2)); }
+  __device__ __forceinline__ bool started() const { return thr2 != 0xff80ff80u; }
+  // New threshold for reference L (log2 units): the largest bf16 not above (L + slack) / log2e.
+  __device__ __forceinline__ void set_threshold(float L) {
+    const float t = (L + kRefSlack) * 0.693147180559945f;
+    uint32_t b = __float_as_uint(t) >> 16;              // truncate toward zero
+    if (t > 0.0f && __uint_as_float(b << 16) > t) b -= 1;  // (truncation of a positive value is not above it)
+    if (t < 0.0f && __uint_as_float(b << 16) > t) b += 1;  // negative: move away from zero
+    thr2 = b | (b << 16);
+  }
 };
 
 template <>
 struct RunMax<float> {
   float m = -INFINITY;
+  float thr = -INFINITY;
   __device__ __forceinline__ bool update(const uint4& v) {
-    const float n = fmaxf(fmaxf(m, fmaxf(__uint_as_float(v.x), __uint_as_float(v.y))),
-                          fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
-    const bool changed = (n > m);
-    m = n;
-    return changed;
+    const float vm = fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                           fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+    m = fmaxf(m, vm);
+    return vm > thr;
   }
   __device__ __forceinline__ float value() const { return m; }
+  __device__ __forceinline__ bool started() const { return thr != -INFINITY; }
+  __device__ __forceinline__ void set_threshold(float L) { thr = (L + kRefSlack) * 0.693147180559945f; }
 };
 
 // ------------------------------------------------------------------ per-entry divergence term
@@ -279,12 +291,10 @@ __global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArg
 
   // ---------------------------------------------------------------- pass A: maxima, exp sums, argmax
   RunMax<T> rmax[NT];
-  float runm[NT];
   float mL[NT];
   float2 acc[NT];
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
-    runm[j] = -INFINITY;
     mL[j] = 0.0f;
     acc[j] = make_float2(0.0f, 0.0f);
   }
@@ -306,39 +316,30 @@ __global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArg
 #pragma unroll
         for (int j = 0; j < NT; ++j) nxt[j] = G::load(slice[j], vn * VEC, len, aligned);
       }
-      float2 x[NT][NP];
+      // Running maxima; when a value passes the reference's slack, move the partial sum to a new
+      // reference at the current maximum.
+      bool far = false;
 #pragma unroll
-      for (int j = 0; j < NT; ++j) G::pairs(cur[j], x[j]);
-      // Running maxima; on the rare growth move the partial sum to the new reference.
-      bool grew = false;
-#if ASV_MAX_FROM_FLOATS
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        float vmx = fmaxf(x[j][0].x, x[j][0].y);
-#pragma unroll
-        for (int q2 = 1; q2 < NP; ++q2) vmx = fmaxf(vmx, fmaxf(x[j][q2].x, x[j][q2].y));
-        grew |= (vmx > runm[j]);
-        runm[j] = fmaxf(runm[j], vmx);
-      }
-#else
-#pragma unroll
-      for (int j = 0; j < NT; ++j) grew |= rmax[j].update(cur[j]);
-#endif
-      if (grew) {
+      for (int j = 0; j < NT; ++j) far |= rmax[j].update(cur[j]);
+      if (far) {
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-#if ASV_MAX_FROM_FLOATS
-          const float nL = ref_of(runm[j]);
-#else
-          const float nL = ref_of(rmax[j].value());
-#endif
-          if (nL != mL[j]) {
-            const float f = (acc[j].x != 0.0f || acc[j].y != 0.0f) ? exp2f(mL[j] - nL) : 0.0f;
-            acc[j] = fmul2(acc[j], make_float2(f, f));
-            mL[j] = nL;
+          const float M = rmax[j].value();
+          // Nothing finite seen yet (-inf), or a +inf/NaN row (flagged later): keep waiting.
+          if (isfinite(M)) {
+            const float nL = M * kLog2e;
+            if (!rmax[j].started() || nL > mL[j] + kRefSlack) {
+              const float f = (acc[j].x != 0.0f || acc[j].y != 0.0f) ? exp2f(mL[j] - nL) : 0.0f;
+              acc[j] = fmul2(acc[j], make_float2(f, f));
+              mL[j] = nL;
+              rmax[j].set_threshold(nL);
+            }
           }
         }
       }
+      float2 x[NT][NP];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) G::pairs(cur[j], x[j]);
 #pragma unroll
       for (int q2 = 0; q2 < NP; ++q2) {
 #pragma unroll
@@ -375,11 +376,7 @@ __global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArg
   // CTA maxima, then every thread moves its sum to the CTA reference and the sums are added.
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
-#if ASV_MAX_FROM_FLOATS
-    const float w = warp_max(runm[j]);
-#else
     const float w = warp_max(rmax[j].value());
-#endif
     if (lane == 0) s_wm[warp][j] = w;
   }
   warp_argmax(bv, bi);
