@@ -15,6 +15,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import re
 import subprocess
 import sys
 import threading
@@ -31,6 +32,7 @@ WORKLOAD = "asymspec_b64_k2_v151936_bf16"
 METRIC = "verified logit rows/s and HBM GB/s vs ~8 TB/s, fused CDA+δ verify, V=151936"
 BETA, GAMMA = 1.0, 0.5
 N_SETS = 4  # rotating input copies: 4 x 175 MB, larger than the 129 MB L2
+KERNEL_SOURCE = "asv_jsd.cu"  # the timed kernel; its ncu summary under profiles/ records a hash of it
 
 
 def _peaks():
@@ -39,6 +41,24 @@ def _peaks():
             return json.load(f), "measured"
     except OSError:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def _profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary of the timed kernel, or None when the
+    kernel source has changed since that capture (the summary records a hash of the source)."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", f"jsd_family_{WORKLOAD}.md")
+    src = os.path.join(ROOT, "speculative_decoding_logit_gb300", "csrc", KERNEL_SOURCE)
+    try:
+        text = open(prof).read()
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    if not (m_sha and m_tr) or m_sha.group(1) != h:
+        return None
+    return float(m_tr.group(1))
 
 
 class ClockSampler:
@@ -270,9 +290,10 @@ def run_ours(args):
                "d2h_bytes_per_step": d2h, "steps": ne, "ms_per_step": e_ms / ne}
 
     peaks, peak_kind = _peaks()
+    traffic = args.traffic if args.traffic is not None else _profiled_traffic()
     achieved = in_bytes / (launch_ms / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / peaks["hbm_gbs"], "traffic": args.traffic, "peak_kind": peak_kind,
+            "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "peak_kind": peak_kind,
             "frac_of_8tbs": achieved / 8000.0, "kernel_ms": launch_ms,
             "algorithmic_bytes_per_launch": in_bytes}
     cpu = None
