@@ -38,10 +38,11 @@
 // reference pass B uses, so the divergence sums and the row sums share one scale.  The constant
 // rounding error of ML is removed from the log-sum-exps.  The gate is decided in double in the log
 // domain.  The per-entry divergence term is evaluated from u = (xb - xa) - (lse_b - lse_a):
-//   narrow form (|u| <= 2, AsymSpec's pair): p * u^2 * P(u), P a fitted polynomial;
-//   wide form (any u): max(p,q) * (A(r) - |u| r), r = exp(-|u|), A(r) = (1-r) B(r).
+//   narrow form (|u| <= 2): sqrt(p q) u^2 R(u^2), R an even-symmetric fitted polynomial;
+//   wide form (any u):      max(p,q) (A(r) - |u| r), r = exp(-|u|), A(r) = (1 - r) B(r).
 // Both are sums of non-negative terms (no cancellation between large entropies), and identical rows
-// give exactly 0.
+// give exactly 0.  Loads of data read for the last time (the verifier input in pass A, the pair in
+// pass B) mark their L2 lines for early eviction.
 #include <cfloat>
 #include <climits>
 #include <type_traits>
@@ -61,7 +62,7 @@ struct __align__(16) JsdXchg {
   float argv;         // best verifier score in the CTA's slice
   int32_t argi;       // its vocabulary index
   // Pushed into CTA 0 by every CTA before the second exchange; only CTA 0 reads them afterwards.
-  float jsd_from[kMaxCluster][4];  // pass-B sums: p-form hi, lo, q-form hi, lo
+  float jsd_from[kMaxCluster][6];  // pass-B sums (hi, lo): narrow form, wide p-form, wide q-form
 };
 
 // Row constants, computed by one thread after the exchange and broadcast through shared memory.
@@ -71,6 +72,7 @@ struct __align__(16) JsdRowConsts {
   float S_hi[3];   // row sums of exp2(x log2e - ML) as hi + lo
   float S_lo[3];
   float dL;        // lse_b - lse_a (pair inputs 1 and 0)
+  float hML;       // fl(ML[0]/2 + ML[1]/2), the narrow form's reference
   int32_t finite;
   float rowv;
   int32_t rowi;
@@ -80,7 +82,6 @@ template <int MODE>
 struct JsdTraits {
   static constexpr int NT = (MODE == kModeAsym) ? 3 : 2;  // streamed inputs
   static constexpr int TGT = NT - 1;                       // index of the verifier/target input
-  static constexpr bool kWide = (MODE == kModeSci);        // divergence term form
 };
 
 // ------------------------------------------------------------------ global vector access
@@ -90,6 +91,14 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
       : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint4 ldg_stream_last(const void* p, uint64_t pol) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p), "l"(pol));
   return v;
 }
 
@@ -107,9 +116,11 @@ struct GVec<bf16_t> {
   }
   // Entries [k, k+8) of a row slice; `aligned` slices use one 16-byte load, others ordinary loads
   // with -inf at and beyond `lim`.
-  __device__ static __forceinline__ uint4 load(const void* base, int k, int lim, bool aligned) {
+  // `last`: the data is read for the last time (its L2 lines are marked for early eviction).
+  __device__ static __forceinline__ uint4 load(const void* base, int k, int lim, bool aligned, bool last = false,
+                                               uint64_t pol = 0) {
     const uint16_t* r = static_cast<const uint16_t*>(base);
-    if (aligned) return ldg_stream(r + k);
+    if (aligned) return last ? ldg_stream_last(r + k, pol) : ldg_stream(r + k);
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -138,9 +149,10 @@ struct GVec<float> {
   __device__ static __forceinline__ uint4 pad() {
     return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
   }
-  __device__ static __forceinline__ uint4 load(const void* base, int k, int lim, bool aligned) {
+  __device__ static __forceinline__ uint4 load(const void* base, int k, int lim, bool aligned, bool last = false,
+                                               uint64_t pol = 0) {
     const float* r = static_cast<const float*>(base);
-    if (aligned) return ldg_stream(r + k);
+    if (aligned) return last ? ldg_stream_last(r + k, pol) : ldg_stream(r + k);
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) w[i] = (k + i < lim) ? __float_as_uint(__ldg(r + k + i)) : 0xff800000u;
@@ -204,27 +216,42 @@ struct RunMax<float> {
 
 // ------------------------------------------------------------------ per-entry divergence term
 
-// Accumulated un-normalised: acc_p += exp(xa - Ma) * f(u) in p-form, acc_q += exp(xb - Mb) * f(-u)
-// in q-form (wide form only).
-template <bool WIDE>
-__device__ __forceinline__ void jsd_entry(float xa, float xb, float dL, float MaL, float MbL, float& acc_p,
+// Row constants pass B needs.
+struct RowB {
+  float dL;   // lse_b - lse_a
+  float MaL;  // references of the pair (M log2e, rounded)
+  float MbL;
+  float hML;  // fl((MaL + MbL) / 2), the narrow form's reference
+};
+
+// One entry, either form.  acc_n: narrow terms sqrt(ea eb) u^2 R(u^2), with ea = exp2(xa log2e -
+// MaL) and eb likewise; acc_p / acc_q: wide terms in p-form (ea h) / q-form (eb h).
+__device__ __forceinline__ void jsd_entry(float xa, float xb, const RowB& rb, float& acc_n, float& acc_p,
                                           float& acc_q) {
-  const float u = (xb - xa) - dL;
-  if (!WIDE && fabsf(u) <= ASV_JSD_POLY_U0) {
-    const float ep = ex2_approx(fmaf(xa, kLog2e, -MaL));
-    acc_p = fmaf(ep * (u * u), asv_jsd_poly(u), acc_p);
+  const float u = (xb - xa) - rb.dL;
+  const float s2 = u * u;
+  if (s2 <= ASV_JSD_EVEN_S0) {
+    const float e = ex2_approx(fmaf(xa + xb, 0.5f * kLog2e, -rb.hML));
+    acc_n = fmaf(e * s2, asv_jsd_even(s2), acc_n);
     return;
   }
   // Wide form.  u <= 0: p >= q, term = p * h(|u|); u > 0 (or NaN): term = q * h(|u|).
   const bool pform = (u <= 0.0f);
   const float s = fabsf(u);
-  const float em = ex2_approx(pform ? fmaf(xa, kLog2e, -MaL) : fmaf(xb, kLog2e, -MbL));
+  const float em = ex2_approx(pform ? fmaf(xa, kLog2e, -rb.MaL) : fmaf(xb, kLog2e, -rb.MbL));
   const float r = ex2_approx(-s * kLog2e);
   const float sr = (r > 0.0f) ? s * r : 0.0f;
   const float h = fmaf(1.0f - r, asv_jsd_wide_b(r), -sr);
   const float v = (em > 0.0f) ? em * h : 0.0f;
   if (pform) acc_p += v;
   else acc_q += v;
+}
+
+// Maximum that propagates NaN (fmaxf drops it), so a NaN entry fails the narrow-form test.
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
 }
 
 // Natural log of a positive finite double without fp64 transcendental code: exponent from
@@ -289,6 +316,8 @@ __global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArg
 #pragma unroll
   for (int j = 0; j < NT; ++j) slice[j] = static_cast<const char*>(p.x[j]) + (row_base + size_t(v0)) * G::kBytes;
 
+  const uint64_t pol_last = policy_evict_first();
+
   // ---------------------------------------------------------------- pass A: maxima, exp sums, argmax
   RunMax<T> rmax[NT];
   float mL[NT];
@@ -307,14 +336,14 @@ __global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArg
     int vi = tid;
     if (vi < nvec) {
 #pragma unroll
-      for (int j = 0; j < NT; ++j) cur[j] = G::load(slice[j], vi * VEC, len, aligned);
+      for (int j = 0; j < NT; ++j) cur[j] = G::load(slice[j], vi * VEC, len, aligned, j == 2, pol_last);
     }
     for (; vi < nvec; vi += kJsdThreads) {
       const int vn = vi + kJsdThreads;
       // Prefetch the next vector (consumed only while it is in range).
       if (vn < nvec) {
 #pragma unroll
-        for (int j = 0; j < NT; ++j) nxt[j] = G::load(slice[j], vn * VEC, len, aligned);
+        for (int j = 0; j < NT; ++j) nxt[j] = G::load(slice[j], vn * VEC, len, aligned, j == 2, pol_last);
       }
       // Running maxima; when a value passes the reference's slack, move the partial sum to a new
       // reference at the current maximum.
@@ -472,6 +501,8 @@ __global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArg
       }
       rc.finite = finite ? 1 : 0;
       rc.dL = dL;
+      // hML = fl(ML[0]/2 + ML[1]/2); its rounding error is removed from the narrow sum at the end.
+      rc.hML = 0.5f * MLr[0] + 0.5f * MLr[1];
       rc.rowv = v2;
       rc.rowi = i2;
     }
@@ -481,169 +512,198 @@ __global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArg
   // ---------------------------------------------------------------- pass B: divergence terms
   {
     const bool finite = rc.finite != 0;
-    const float dL = rc.dL;
-    const float ML0 = rc.ML[0], ML1 = rc.ML[1];
-    float ap0 = 0.0f, ap1 = 0.0f, aq0 = 0.0f, aq1 = 0.0f;
+    RowB rb;
+    rb.dL = rc.dL;
+    rb.MaL = rc.ML[0];
+    rb.MbL = rc.ML[1];
+    rb.hML = rc.hML;
+    float2 accn = make_float2(0.0f, 0.0f);
+    float an = 0.0f, ap = 0.0f, aq = 0.0f;
     if (finite) {
+      const float2 dl2 = make_float2(rb.dL, rb.dL);
+      const float2 hl2e2 = make_float2(0.5f * kLog2e, 0.5f * kLog2e);
+      const float2 nhml2 = make_float2(-rb.hML, -rb.hML);
       int vi = tid;
       uint4 ca, cb, na, nb;
       if (vi < nvec) {
-        ca = G::load(slice[0], vi * VEC, len, aligned);
-        cb = G::load(slice[1], vi * VEC, len, aligned);
+        ca = G::load(slice[0], vi * VEC, len, aligned, true, pol_last);
+        cb = G::load(slice[1], vi * VEC, len, aligned, true, pol_last);
       }
-      if constexpr (!JsdTraits<MODE>::kWide) {
-        const float2 l2e2 = make_float2(kLog2e, kLog2e);
-        const float2 dl2 = make_float2(dL, dL);
-        const float2 nmal = make_float2(-ML0, -ML0);
-        float2 accp = make_float2(0.0f, 0.0f);
-        for (; vi < nvec; vi += kJsdThreads) {
-          const int vn = vi + kJsdThreads;
-          if (vn < nvec) {
-            na = G::load(slice[0], vn * VEC, len, aligned);
-            nb = G::load(slice[1], vn * VEC, len, aligned);
-          }
-          float2 xa[NP], xb[NP];
-          G::pairs(ca, xa);
-          G::pairs(cb, xb);
+      for (; vi < nvec; vi += kJsdThreads) {
+        const int vn = vi + kJsdThreads;
+        if (vn < nvec) {
+          na = G::load(slice[0], vn * VEC, len, aligned, true, pol_last);
+          nb = G::load(slice[1], vn * VEC, len, aligned, true, pol_last);
+        }
+        float2 xa[NP], xb[NP], uu[NP], s2[NP];
+        G::pairs(ca, xa);
+        G::pairs(cb, xb);
+#pragma unroll
+        for (int q2 = 0; q2 < NP; ++q2) {
+          uu[q2] = fsub2(fsub2(xb[q2], xa[q2]), dl2);
+          s2[q2] = fmul2(uu[q2], uu[q2]);
+        }
+        // Narrow form for the whole vector unless one entry is outside it (or NaN: -inf pairs).
+        float smax = fmax_nan(s2[0].x, s2[0].y);
+#pragma unroll
+        for (int q2 = 1; q2 < NP; ++q2) smax = fmax_nan(smax, fmax_nan(s2[q2].x, s2[q2].y));
+        if (smax <= ASV_JSD_EVEN_S0) {
 #pragma unroll
           for (int q2 = 0; q2 < NP; ++q2) {
-            const float2 u = fsub2(fsub2(xb[q2], xa[q2]), dl2);
-            if (fabsf(u.x) <= ASV_JSD_POLY_U0 && fabsf(u.y) <= ASV_JSD_POLY_U0) {
-              const float2 y = ffma2(xa[q2], l2e2, nmal);
-              const float2 ep = make_float2(ex2_approx(y.x), ex2_approx(y.y));
-              accp = ffma2(fmul2(ep, fmul2(u, u)), asv_jsd_poly2(u), accp);
-            } else {
-              jsd_entry<false>(xa[q2].x, xb[q2].x, dL, ML0, ML1, ap0, aq0);
-              jsd_entry<false>(xa[q2].y, xb[q2].y, dL, ML0, ML1, ap1, aq1);
-            }
+            const float2 y = ffma2(fadd2(xa[q2], xb[q2]), hl2e2, nhml2);
+            const float2 e = make_float2(ex2_approx(y.x), ex2_approx(y.y));
+            accn = ffma2(fmul2(e, s2[q2]), asv_jsd_even2(s2[q2]), accn);
           }
-          ca = na;
-          cb = nb;
-        }
-        ap0 += accp.x;
-        ap1 += accp.y;
-      } else {
-        for (; vi < nvec; vi += kJsdThreads) {
-          const int vn = vi + kJsdThreads;
-          if (vn < nvec) {
-            na = G::load(slice[0], vn * VEC, len, aligned);
-            nb = G::load(slice[1], vn * VEC, len, aligned);
-          }
-          float2 xa[NP], xb[NP];
-          G::pairs(ca, xa);
-          G::pairs(cb, xb);
+        } else {
 #pragma unroll
           for (int q2 = 0; q2 < NP; ++q2) {
-            jsd_entry<true>(xa[q2].x, xb[q2].x, dL, ML0, ML1, ap0, aq0);
-            jsd_entry<true>(xa[q2].y, xb[q2].y, dL, ML0, ML1, ap1, aq1);
+            jsd_entry(xa[q2].x, xb[q2].x, rb, an, ap, aq);
+            jsd_entry(xa[q2].y, xb[q2].y, rb, an, ap, aq);
           }
-          ca = na;
-          cb = nb;
         }
+        ca = na;
+        cb = nb;
       }
     }
-    const float wp = warp_sumf(ap0 + ap1);
-    const float wq = warp_sumf(aq0 + aq1);
+    const float wn = warp_sumf((accn.x + accn.y) + an);
+    const float wp = warp_sumf(ap);
+    const float wq = warp_sumf(aq);
     if (lane == 0) {
-      s_wf[warp][0] = wp;
-      s_wf[warp][1] = wq;
+      s_wf[warp][0] = wn;
+      s_wf[warp][1] = wp;
+      s_wf[warp][2] = wq;
     }
   }
   __syncthreads();
   if (warp == 0) {
-    const DF dp = warp_sum_df(DF{lane < kWarps ? s_wf[lane][0] : 0.0f, 0.0f});
-    const DF dq = warp_sum_df(DF{lane < kWarps ? s_wf[lane][1] : 0.0f, 0.0f});
+    const DF dn = warp_sum_df(DF{lane < kWarps ? s_wf[lane][0] : 0.0f, 0.0f});
+    const DF dp = warp_sum_df(DF{lane < kWarps ? s_wf[lane][1] : 0.0f, 0.0f});
+    const DF dq = warp_sum_df(DF{lane < kWarps ? s_wf[lane][2] : 0.0f, 0.0f});
     if (lane == 0) {
       // Push this CTA's pass-B sums into CTA 0.
       const uint32_t base = smem_addr(&xchg.jsd_from[rank][0]);
-      dsmem_st_f32(dsmem_map(base + 0, 0), dp.hi);
-      dsmem_st_f32(dsmem_map(base + 4, 0), dp.lo);
-      dsmem_st_f32(dsmem_map(base + 8, 0), dq.hi);
-      dsmem_st_f32(dsmem_map(base + 12, 0), dq.lo);
+      dsmem_st_f32(dsmem_map(base + 0, 0), dn.hi);
+      dsmem_st_f32(dsmem_map(base + 4, 0), dn.lo);
+      dsmem_st_f32(dsmem_map(base + 8, 0), dp.hi);
+      dsmem_st_f32(dsmem_map(base + 12, 0), dp.lo);
+      dsmem_st_f32(dsmem_map(base + 16, 0), dq.hi);
+      dsmem_st_f32(dsmem_map(base + 20, 0), dq.lo);
     }
   }
   cluster_sync_w0(warp);  // #2: after this only CTA 0 touches shared memory, and only its own
-  if (rank != 0 || tid != 0) return;
+  if (rank != 0 || warp != 0) return;
 
-  // ---------------------------------------------------------------- row finalisation (CTA 0)
-  DF jp{0.0f, 0.0f}, jq{0.0f, 0.0f};
-  for (uint32_t q = 0; q < C; ++q) {
-    jp = df_add(jp, DF{xchg.jsd_from[q][0], xchg.jsd_from[q][1]});
-    jq = df_add(jq, DF{xchg.jsd_from[q][2], xchg.jsd_from[q][3]});
-  }
+  // ---------------------------------------------------------------- row finalisation (CTA 0, warp 0)
+  const unsigned kAll = 0xffffffffu;
+  const int K = p.K;
   const bool finite = rc.finite != 0;
+  // The draft token's verifier and compressed-drafter logits (lanes 1, 2), loaded early.
+  const int d = (pos < K) ? p.draft_ids[size_t(req) * K + pos] : -1;
+  const bool d_ok = d >= 0 && d < V;
+  float xd = 0.0f;
+  if (MODE == kModeAsym && finite && d_ok && (lane == 1 || lane == 2))
+    xd = G::at(p.x[lane == 1 ? NT - 1 : 1], row_base + size_t(d));
+  // Pass-B sums of the cluster's CTAs, in rank order (lane q holds CTA q's).
+  DF jn{0.0f, 0.0f}, jp{0.0f, 0.0f}, jq{0.0f, 0.0f};
+  if (lane < int(C)) {
+    jn = DF{xchg.jsd_from[lane][0], xchg.jsd_from[lane][1]};
+    jp = DF{xchg.jsd_from[lane][2], xchg.jsd_from[lane][3]};
+    jq = DF{xchg.jsd_from[lane][4], xchg.jsd_from[lane][5]};
+  }
+  jn = warp_sum_df(jn);
+  jp = warp_sum_df(jp);
+  jq = warp_sum_df(jq);
   float D = 0.0f;
   if (finite) {
-    D = 0.5f * ((jp.hi + jp.lo) / (rc.S_hi[0] + rc.S_lo[0]) + (jq.hi + jq.lo) / (rc.S_hi[1] + rc.S_lo[1]));
-    D = fminf(fmaxf(D, 0.0f), kLn2f);
+    // Narrow terms are against sqrt(ea eb) 2^(MaL/2 + MbL/2 - hML); the row sums Sa, Sb against
+    // MaL, MbL.  delta = hML - (MaL/2 + MbL/2) exactly (TwoSum of the two halves).
+    const float ha = 0.5f * rc.ML[0], hb = 0.5f * rc.ML[1];
+    const float bb = rc.hML - ha;
+    const float delta = -((ha - (rc.hML - bb)) + (hb - bb));
+    const float Sa = rc.S_hi[0] + rc.S_lo[0];
+    const float Sb = rc.S_hi[1] + rc.S_lo[1];
+    const float narrow = __fdiv_rn((jn.hi + jn.lo) * exp2f(delta), __fsqrt_rn(Sa) * __fsqrt_rn(Sb));
+    const float wide = __fdiv_rn(jp.hi + jp.lo, Sa) + __fdiv_rn(jq.hi + jq.lo, Sb);
+    D = fminf(fmaxf(0.5f * (narrow + wide), 0.0f), kLn2f);
   }
-  // Log-sum-exps (double, this thread only): lse = M + ln(S) - c ln2.
-  double lse[NT];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    const float c = fmaf(rc.M[j], kLog2e, -rc.ML[j]);
-    lse[j] = finite ? double(rc.M[j]) + ln_pos(double(rc.S_hi[j]) + double(rc.S_lo[j])) - double(c) * kLn2 : 0.0;
+  // Log-sum-exps, one input per lane (double): lse = M + ln(S) - c ln2.
+  double my_lse = 0.0;
+  if (lane < NT && finite) {
+    const float c = fmaf(rc.M[lane], kLog2e, -rc.ML[lane]);
+    my_lse = double(rc.M[lane]) + ln_pos(double(rc.S_hi[lane]) + double(rc.S_lo[lane])) - double(c) * kLn2;
   }
+  const double lse_b = __shfl_sync(kAll, my_lse, 1);
+  const double lse_v = __shfl_sync(kAll, my_lse, NT - 1);
+  const float td = __shfl_sync(kAll, xd, 1);
+  const float bd = __shfl_sync(kAll, xd, 2);
   uint32_t bits = 0;
   if (!finite) bits |= kBitNonfinite;
-  const int token = (rc.rowi == INT_MAX) ? 0 : rc.rowi;
-  if (pos < p.K) {
-    const int d = p.draft_ids[size_t(req) * p.K + pos];
-    if (d < 0 || d >= V) {
+  if (pos < K) {
+    if (!d_ok) {
       bits |= kBitBadDraft;
     } else if (MODE == kModeAsym && finite) {
-      const float td = G::at(p.x[NT - 1], row_base + size_t(d));
-      const float bd = G::at(p.x[1], row_base + size_t(d));
-      const double margin = (double(td) - lse[NT - 1]) - p.ln_gamma + double(D) - (double(bd) - lse[1]);
+      const double margin = (double(td) - lse_v) - p.ln_gamma + double(D) - (double(bd) - lse_b);
       if (margin > 0.0) bits |= kBitAccept;
     }
   }
-  if (p.out_D) p.out_D[row] = finite ? D : __int_as_float(0x7fc00000);
-  if (MODE == kModeAsym && p.out_lse) {
-#pragma unroll
-    for (int j = 0; j < NT; ++j) p.out_lse[size_t(row) * 3 + j] = float(lse[j]);
+  if (lane == 0 && p.out_D) p.out_D[row] = finite ? D : __int_as_float(0x7fc00000);
+  if (MODE == kModeAsym && p.out_lse && lane < NT) p.out_lse[size_t(row) * 3 + lane] = float(my_lse);
+  uint32_t ticket = 0;
+  if (lane == 0) {
+    RowRecord rec;
+    rec.value = double(D);
+    rec.token = (rc.rowi == INT_MAX) ? 0 : rc.rowi;
+    rec.bits = bits;
+    p.records[row] = rec;
+    ticket = atom_add_acq_rel_gpu(&p.tickets[req], 1u);
   }
-  RowRecord rec;
-  rec.value = double(D);
-  rec.token = token;
-  rec.bits = bits;
-  p.records[row] = rec;
-  __threadfence();
-  const uint32_t ticket = atomicAdd(&p.tickets[req], 1u);
-  if (ticket == uint32_t(p.K)) {
-    // Last row of this request: the left-to-right scan.
-    __threadfence();
-    const volatile RowRecord* recs = p.records + size_t(req) * R1;
-    uint32_t any = 0;
-    for (int i = 0; i < R1; ++i) any |= recs[i].bits;
-    const uint32_t status = ((any & kBitNonfinite) ? 1u : 0u) | ((any & kBitBadDraft) ? 2u : 0u);
-    int32_t* toks = p.out_tokens + size_t(req) * R1;
-    double thr = 0.0;
+  ticket = __shfl_sync(kAll, ticket, 0);
+  if (ticket != uint32_t(K)) return;
+
+  // Last row of this request: the left-to-right scan, 32 records per step.
+  (void)ld_acquire_gpu(&p.tickets[req]);  // every lane acquires the other rows' records
+  RowRecord* recs = p.records + size_t(req) * R1;
+  double thr = 0.0;
+  if (MODE == kModeSci) {
+    thr = p.T_base + p.alpha_omega * (p.r_hat[req] - p.tau_credit);
+    thr = fmax(p.T_min, fmin(thr, p.T_max));
+  }
+  uint32_t any = 0;
+  int n = K;      // accepted prefix
+  int tok_n = 0;  // token of row n
+  for (int base = 0; base < R1; base += 32) {
+    const int i = base + lane;
+    uint32_t b = 0;
+    double v = 0.0;
+    int tk = 0;
+    if (i < R1) {
+      const float4 w = ld_cg_f4(recs + i);
+      v = __hiloint2double(__float_as_int(w.y), __float_as_int(w.x));
+      tk = __float_as_int(w.z);
+      b = __float_as_uint(w.w);
+    }
+    any |= __reduce_or_sync(kAll, b);
+    const bool ok = (MODE == kModeAsym) ? (b & kBitAccept) != 0 : !(v > thr);
+    const unsigned rej = __ballot_sync(kAll, i < K && !ok);
+    if (n == K && rej != 0u) n = base + __ffs(rej) - 1;
+    const int src = (n >= base && n < base + 32) ? n - base : 0;
+    const int tk_src = __shfl_sync(kAll, tk, src);
+    if (n >= base && n < base + 32) tok_n = tk_src;
+  }
+  const uint32_t status = ((any & kBitNonfinite) ? 1u : 0u) | ((any & kBitBadDraft) ? 2u : 0u) |
+                          ((any & kBitTimeout) ? 4u : 0u);
+  int32_t* toks = p.out_tokens + size_t(req) * R1;
+  const int32_t* dr = p.draft_ids + size_t(req) * K;
+  for (int i = lane; i < R1; i += 32) {
+    toks[i] = status ? -1 : ((i < n) ? dr[i] : (i == n ? tok_n : -1));
+    recs[i] = RowRecord{};  // consumed: a call leaves the workspace zeroed
+  }
+  if (lane == 0) {
     if (MODE == kModeSci) {
-      thr = p.T_base + p.alpha_omega * (p.r_hat[req] - p.tau_credit);
-      thr = fmax(p.T_min, fmin(thr, p.T_max));
       if (p.out_T) p.out_T[req] = float(thr);
+      if (!status) p.r_hat[req] = (1.0 - p.ewma_beta) * p.r_hat[req] + p.ewma_beta * (double(n) / double(K));
     }
-    if (status) {
-      p.out_accept_len[req] = 0;
-      for (int i = 0; i < R1; ++i) toks[i] = -1;
-    } else {
-      int n = p.K;
-      for (int i = 0; i < p.K; ++i) {
-        const bool ok = (MODE == kModeAsym) ? (recs[i].bits & kBitAccept) != 0 : !(recs[i].value > thr);
-        if (!ok) {
-          n = i;
-          break;
-        }
-      }
-      if (MODE == kModeSci) {
-        const double pacc = double(n) / double(p.K);
-        p.r_hat[req] = (1.0 - p.ewma_beta) * p.r_hat[req] + p.ewma_beta * pacc;
-      }
-      p.out_accept_len[req] = n;
-      const int32_t* dr = p.draft_ids + size_t(req) * p.K;
-      for (int i = 0; i < R1; ++i) toks[i] = (i < n) ? dr[i] : (i == n ? recs[n].token : -1);
-    }
+    p.out_accept_len[req] = status ? 0 : n;
     p.out_req_status[req] = status;
     p.tickets[req] = 0u;
   }

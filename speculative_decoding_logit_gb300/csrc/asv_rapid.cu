@@ -350,6 +350,8 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
         p.out_accept_len[req] = 0;
         for (int i = 0; i < R1; ++i) p.out_tokens[size_t(req) * R1 + i] = -1;
         p.out_req_status[req] = status;
+        // The request's records are consumed: clear them (a call leaves the workspace zeroed).
+        for (int i = 0; i < R1; ++i) p.records[size_t(req) * R1 + i] = RapidRecord{};
         p.tickets[req] = 0u;
       } else {
         int n = G;
@@ -359,6 +361,7 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
             break;
           }
         const float f0 = recs[n].zs_max, f1 = recs[n].inv_sum, f2 = recs[n].zhat_max, f3 = recs[n].head_scale;
+        for (int i = 0; i < R1; ++i) p.records[size_t(req) * R1 + i] = RapidRecord{};
         for (uint32_t q = 0; q < C; ++q) {
           dsmem_st_u32(dsmem_map(smem_addr(&xchg.draw_row), q), uint32_t(n));
           dsmem_st_u32(dsmem_map(smem_addr(&xchg.d_zs_max), q), __float_as_uint(f0));

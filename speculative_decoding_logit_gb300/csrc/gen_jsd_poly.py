@@ -1,19 +1,23 @@
-"""Build step: fit the polynomial the kernels use for the per-entry
-Jensen-Shannon term on |u| <= U0, and write jsd_poly.inc.
+"""Build step: fit the polynomials the kernels use for the per-entry
+Jensen-Shannon term, and write jsd_poly.inc.
 
 For one vocabulary entry with probabilities p (first distribution) and
 q = p * e^u (second), the entry's share of
     2 * JSD = sum_k [ p_k ln(2 p_k / (p_k + q_k)) + q_k ln(2 q_k / (p_k + q_k)) ]
 is p * f(u) with
     f(u) = (1 + e^u) ln(2 / (1 + e^u)) + u e^u      (f >= 0, f(0) = 0, f ~ u^2/4).
-Narrow form (|u| <= U0): f(u) = u^2 * P(u).  Writing f this way keeps f(0)
-exactly 0, so identical rows give a divergence of exactly 0.
+The share is symmetric in p and q, so p f(u) = q f(-u), i.e. f(u) = e^u f(-u).
+
+Narrow form (|u| <= U0): p f(u) = sqrt(p q) * u^2 * R(u^2).  R(u^2) = e^(-u/2) f(u) / u^2
+is even in u (the symmetry above), so it is a polynomial in s = u^2 of low degree.
+Writing the share this way keeps it exactly 0 at u = 0, so identical rows give a
+divergence of exactly 0, and sqrt(p q) = exp((ln p + ln q) / 2) costs one exponential.
 
 Wide form (any u): with m = max(p, q), s = |u| and r = e^-s = min(p,q)/max(p,q),
 the entry's share is m * (A(r) - s*r) with A(r) = (1 + r) ln(2 / (1 + r)), and
 A(r) = (1 - r) * B(r) with B smooth on [0, 1] (B(0) = ln 2, B(1) = 1).
 
-Both P and B are fitted here in 50-digit arithmetic by least squares in
+Both R and B are fitted here in 50-digit arithmetic by least squares in
 relative error on Chebyshev nodes; coefficients are rounded to fp32 one at a
 time from the highest degree down, each rounding followed by a refit of the
 remaining lower coefficients.
@@ -28,7 +32,7 @@ import numpy as np
 
 mp.mp.dps = 50
 U0 = 2.0
-DEG = 11
+DEG = 6  # degree of R in s = u^2
 
 
 def f(u):
@@ -42,6 +46,15 @@ def P(u):
     if abs(u) < mp.mpf("1e-12"):
         return mp.mpf(1) / 4
     return f(u) / (u * u)
+
+
+def Rfun(s):
+    """R(s) = e^(-u/2) f(u) / u^2 at u = sqrt(s) (the same value at u = -sqrt(s))."""
+    s = mp.mpf(s)
+    if s < mp.mpf("1e-24"):
+        return mp.mpf(1) / 4
+    u = mp.sqrt(s)
+    return P(u) * mp.e ** (-u / 2)
 
 
 R_DEG = 11
@@ -117,33 +130,34 @@ def emit2(fh, name, var, coef):
 
 
 def main():
-    coef = fit_rounded(P, DEG, -U0, U0)
+    S0 = U0 * U0
+    coef = fit_rounded(Rfun, DEG, 0.0, S0)
     bcoef = fit_rounded(Bfun, R_DEG, 0.0, 1.0)
     rs = np.linspace(0, 1, 2001)
     berr = float(max(abs(sum(mp.mpf(bcoef[d]) * mp.mpf(x) ** d for d in range(R_DEG + 1)) / Bfun(x) - 1) for x in rs))
     rs32 = rs.astype(np.float32)
     bacc = horner32(bcoef, rs32)
     berr32 = float(max(abs(float(bacc[i]) / float(Bfun(float(rs32[i]))) - 1) for i in range(len(rs))))
-    # exact-arithmetic relative error of u^2 P(u) with the fp32 coefficients
-    xs = np.linspace(-U0, U0, 4001)
-    err = float(max(abs(sum(mp.mpf(coef[d]) * mp.mpf(x) ** d for d in range(DEG + 1)) / P(x) - 1) for x in xs))
+    # exact-arithmetic relative error of R with the fp32 coefficients
+    xs = np.linspace(0.0, S0, 4001)
+    err = float(max(abs(sum(mp.mpf(coef[d]) * mp.mpf(x) ** d for d in range(DEG + 1)) / Rfun(x) - 1) for x in xs))
     # fp32 Horner evaluation, as the kernel does it
     xs32 = xs.astype(np.float32)
     acc = horner32(coef, xs32)
-    err32 = float(max(abs(float(acc[i]) / float(P(float(xs32[i]))) - 1) for i in range(len(xs))))
+    err32 = float(max(abs(float(acc[i]) / float(Rfun(float(xs32[i]))) - 1) for i in range(len(xs))))
     out = os.path.join(os.path.dirname(os.path.abspath(__file__)), "jsd_poly.inc")
     with open(out, "w") as fh:
         fh.write("// Generated by gen_jsd_poly.py -- do not edit.\n")
-        fh.write(f"// Narrow form: f(u) = u^2 * P(u) on |u| <= {U0}, P of degree {DEG}.\n")
-        fh.write(f"//   max relative error of P: {err:.3e} (exact arithmetic), {err32:.3e} (fp32 Horner).\n")
+        fh.write(f"// Narrow form: p f(u) = sqrt(p q) u^2 R(u^2) on |u| <= {U0}, R of degree {DEG} in u^2.\n")
+        fh.write(f"//   max relative error of R: {err:.3e} (exact arithmetic), {err32:.3e} (fp32 Horner).\n")
         fh.write(f"// Wide form: A(r) = (1 - r) * B(r) on [0, 1], B of degree {R_DEG}.\n")
         fh.write(f"//   max relative error of B: {berr:.3e} (exact arithmetic), {berr32:.3e} (fp32 Horner).\n")
-        fh.write(f"#define ASV_JSD_POLY_U0 {U0:.1f}f\n")
-        emit(fh, "asv_jsd_poly", "u", coef)
+        fh.write(f"#define ASV_JSD_EVEN_S0 {S0:.1f}f\n")
+        emit(fh, "asv_jsd_even", "s", coef)
         emit(fh, "asv_jsd_wide_b", "r", bcoef)
-        emit2(fh, "asv_jsd_poly2", "u", coef)
+        emit2(fh, "asv_jsd_even2", "s", coef)
         emit2(fh, "asv_jsd_wide_b2", "r", bcoef)
-    print(f"wrote {out}: P rel err {err:.3e} exact, {err32:.3e} fp32; B rel err {berr:.3e} exact, {berr32:.3e} fp32")
+    print(f"wrote {out}: R rel err {err:.3e} exact, {err32:.3e} fp32; B rel err {berr:.3e} exact, {berr32:.3e} fp32")
 
 
 if __name__ == "__main__":

@@ -27,6 +27,7 @@ def compare_asymspec(gpu, ref: "oracle.AsymSpecResult", dtype, rows=None):
     lse = gpu.lse.cpu().numpy().astype(np.float64)
     st = gpu.req_status.cpu().numpy().astype(np.uint32)
     np.testing.assert_array_equal(st & 3, ref.flags & 3)
+    assert not (st & 4).any(), "a bounded wait expired (ASV_REQ_TIMEOUT)"
     graded = flagged = 0
     for r in range(len(acc)):
         if ref.flags[r] & oracle.FLAGS_UNGRADED:

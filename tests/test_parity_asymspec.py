@@ -53,6 +53,22 @@ def test_draft_counts(asv, K):
     compare_asymspec(out, ref, gen.BF16)
 
 
+def test_workspace_left_zeroed(asv):
+    # Calls of growing size share one workspace; each must leave all of it zero, because a later
+    # call lays its request tickets over the bytes an earlier one used for row records.
+    shapes = [(9, 0, 3000), (9, 1, 3000), (12, 3, 8192), (3, 7, 32000), (20, 2, 1000)]
+    need = max(asv.workspace_bytes(asv.ASV_MODE_ASYMSPEC, B, K, V, asv.ASV_BF16) for B, K, V in shapes)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    for B, K, V in shapes:
+        batch = gen.make_asymspec_batch("gumbel_zipf", 90 + B + K, B, K, V, gen.BF16)
+        a, b, t = (to_device(x, batch.dtype) for x in (batch.a, batch.b, batch.t))
+        out = asv.asymspec_verify(a, b, t, torch.from_numpy(batch.drafts).cuda(), 1.0, 0.5, workspace=ws)
+        torch.cuda.synchronize()
+        ref = oracle.asymspec_verify(batch.a, batch.b, batch.t, batch.drafts, 1.0, 0.5)
+        compare_asymspec(out, ref, gen.BF16)
+        assert int(torch.count_nonzero(ws)) == 0, f"workspace not cleared after B={B} K={K} V={V}"
+
+
 def test_empty_batch(asv):
     z = torch.zeros(0, 3, 100, device="cuda")
     d = torch.zeros(0, 2, dtype=torch.int32, device="cuda")

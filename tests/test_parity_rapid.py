@@ -32,6 +32,7 @@ def _run(asv, z, q, d, T, eta, tail, seed, offset=0):
 def _compare(out, ref):
     st = out.req_status.cpu().numpy().astype(np.uint32)
     np.testing.assert_array_equal(st & 3, ref.flags & 3)
+    assert not (st & 4).any(), "a bounded wait expired (ASV_REQ_TIMEOUT)"
     acc = out.accept_len.cpu().numpy()
     tok = out.tokens.cpu().numpy()
     graded = flagged = 0
@@ -93,6 +94,21 @@ def test_eta_zero_first_token_is_target_distributed(asv):
     assert stats.chisquare(np.bincount(first, minlength=V), B * p).pvalue > 1e-4
     ref = oracle.rapid_verify(zz, qq, d, 1.0, 0.0, 0.1, 4321)
     _compare(out, ref)
+
+
+def test_workspace_left_zeroed(asv):
+    # Growing batches share one workspace; every call must leave all of it zero (a later call lays
+    # its tickets over the bytes an earlier one used for row records).
+    shapes = [(3, 2, 256), (40, 4, 1000), (7, 1, 4096), (300, 2, 64)]
+    need = max(asv.workspace_bytes(asv.ASV_MODE_RAPID, B, G, V, asv.ASV_F32) for B, G, V in shapes)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    for i, (B, G, V) in enumerate(shapes):
+        b = gen.make_rapid_batch(600 + i, B, G, V)
+        out = asv.rapid_verify(torch.from_numpy(b.z).cuda(), torch.from_numpy(b.q).cuda(),
+                               torch.from_numpy(b.drafts).cuda(), 1.0, 5.0, 0.1, 99, workspace=ws)
+        torch.cuda.synchronize()
+        _compare(out, oracle.rapid_verify(b.z, b.q, b.drafts, 1.0, 5.0, 0.1, 99))
+        assert int(torch.count_nonzero(ws)) == 0, f"workspace not cleared after B={B} G={G} V={V}"
 
 
 def test_nonfinite_and_bad_drafts(asv):

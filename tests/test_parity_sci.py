@@ -33,6 +33,7 @@ def _window(asv, batch, r_hat, params=None):
 def _compare(out, r_new, ref, dtype):
     st = out.req_status.cpu().numpy().astype(np.uint32)
     np.testing.assert_array_equal(st & 3, ref.flags & 3)
+    assert not (st & 4).any(), "a bounded wait expired (ASV_REQ_TIMEOUT)"
     acc = out.accept_len.cpu().numpy()
     tok = out.tokens.cpu().numpy()
     graded = 0

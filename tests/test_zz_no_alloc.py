@@ -4,6 +4,8 @@ code that must not allocate once running): it keeps its scratch in a library-own
 device array.  Checked through the C ABI against asymspec_verify (caller workspace) on two
 calls in a row, and for the size limit.  This file is collected last on purpose."""
 import ctypes as C
+import os
+import re
 
 import numpy as np
 import pytest
@@ -13,7 +15,14 @@ import gen
 
 pytestmark = pytest.mark.gpu
 
-STATIC_SCRATCH_BYTES = 1 << 20
+
+def _static_scratch_bytes():
+    """ASV_STATIC_SCRATCH_BYTES as include/asv.h defines it (read from the header, so the limit a
+    test relies on cannot drift from the library's)."""
+    hdr = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "asv.h")
+    m = re.search(r"#define\s+ASV_STATIC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", open(hdr).read())
+    assert m, "ASV_STATIC_SCRATCH_BYTES not found in asv.h"
+    return int(m.group(1)) << int(m.group(2))
 
 
 def _to_dev(x, dtype):
@@ -63,12 +72,16 @@ def test_static_scratch_rejects_batches_beyond_its_size():
     import speculative_decoding_logit_gb300 as asv
     asv.build()
     lib = asv.library()
-    K = 8
-    B = 8000   # 256-byte-padded tickets + 16 bytes per row exceed 1 MiB
-    assert lib.asv_workspace_bytes(0, B, K, 1000, 1) > STATIC_SCRATCH_BYTES
+    K, V = 8, 1000
+    B = 200000   # about 2 million rows: a workspace far beyond the static scratch
+    need = lib.asv_workspace_bytes(0, B, K, V, 1)
+    limit = _static_scratch_bytes()
+    # The call below passes placeholder addresses: it must be rejected before any launch, so the
+    # batch has to be far beyond the limit (checked here, not assumed).
+    assert need > 8 * limit, (need, limit)
     f = lib.asymspec_verify_static
     vp = C.c_void_p
     f.argtypes = [vp, vp, vp, C.c_int, vp, C.c_int, C.c_int, C.c_int, C.c_float, C.c_float, vp, vp, vp, vp, vp, vp]
     f.restype = C.c_int
     P = 1 << 20
-    assert f(P, P, P, 1, P, B, K, 1000, 1.0, 0.5, P, P, P, P, P, None) == 6   # ASV_ERR_WORKSPACE, nothing launched
+    assert f(P, P, P, 1, P, B, K, V, 1.0, 0.5, P, P, P, P, P, None) == 6   # ASV_ERR_WORKSPACE, nothing launched
