@@ -111,9 +111,11 @@ cudaError_t plan_for(int kind, int dtype, int NT, int elem_bytes, int V, long lo
 }
 
 // Plan for the streaming AsymSpec / SCI kernel.  It stages nothing, so a CTA needs only
-// registers; pass B re-reads the divergence pair from L2, so the slices of the CTAs resident at
-// once (about four per SM) must fit comfortably in L2: C is the smallest cluster size that keeps
-// them under kL2Budget, raised while the batch has fewer than four CTAs per SM.
+// registers and jsd_ctas_per_sm() CTAs share an SM (its launch bounds); pass B re-reads the
+// divergence pair from L2.  Cluster size: the smallest C whose R*C CTAs fill at least 90% of one wave of resident CTAs
+// and whose last wave is at least 85% full -- fewer CTAs per row mean fewer cluster exchanges,
+// while a partly empty last wave leaves SMs idle.  A batch too small to fill a wave even at C = 16
+// takes the largest C (at least 1024 entries per CTA).
 cudaError_t plan_jsd(int elem_bytes, int V, long long R, bool aligned, LaunchPlan* out) {
   DevInfo di;
   cudaError_t e = dev_info(&di);
@@ -121,13 +123,17 @@ cudaError_t plan_jsd(int elem_bytes, int V, long long R, bool aligned, LaunchPla
   const int vec = 16 / elem_bytes;
   int C = g_tune_cluster.load();
   if (C <= 0) {
-    constexpr double kL2Budget = 48.0 * 1024 * 1024;
-    const double resident = 4.0 * di.sms;
-    C = int(std::ceil(resident * 2.0 * double(V) * elem_bytes / kL2Budget));
-    const long long want = 4LL * di.sms;
-    if (R * C < want) C = int((want + R - 1) / R);
-    C = std::min(C, std::max(1, V / 1024));
-    C = std::max(1, std::min(C, asv::kMaxCluster));
+    const int c_max = std::max(1, std::min(asv::kMaxCluster, V / 1024));
+    const double resident = double(asv::jsd_ctas_per_sm()) * di.sms;
+    C = c_max;
+    for (int c = 1; c <= c_max; ++c) {
+      const double waves = double(R) * c / resident;
+      if (waves < 0.9) continue;
+      if (waves / std::ceil(waves) >= 0.85) {
+        C = c;
+        break;
+      }
+    }
   }
   out->cluster = C;
   out->threads = asv::jsd_threads();

@@ -63,6 +63,13 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return pol;
 }
 
+// L2 policy that keeps lines cached in preference to others (data read again soon).
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // bulk_g2s with an L2 cache policy.
 __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
                                               uint64_t pol) {

@@ -90,7 +90,8 @@ cudaError_t launch_rapid(const RapidArgs& args, const LaunchPlan& plan, cudaStre
 
 // Static shared memory the kernels use beside the dynamic staging area.
 int jsd_static_smem_bytes();
-int jsd_threads();  // threads per CTA of the AsymSpec / SCI kernel
+int jsd_threads();      // threads per CTA of the AsymSpec / SCI kernel
+int jsd_ctas_per_sm();  // CTAs of it that share an SM (its launch bounds)
 int rapid_static_smem_bytes();
 
 // Occupancy query: clusters of `plan` that can be resident at once (0 = cannot launch).

@@ -41,8 +41,8 @@
 //   narrow form (|u| <= 2): sqrt(p q) u^2 R(u^2), R an even-symmetric fitted polynomial;
 //   wide form (any u):      max(p,q) (A(r) - |u| r), r = exp(-|u|), A(r) = (1 - r) B(r).
 // Both are sums of non-negative terms (no cancellation between large entropies), and identical rows
-// give exactly 0.  Loads of data read for the last time (the verifier input in pass A, the pair in
-// pass B) mark their L2 lines for early eviction.
+// give exactly 0.  Loads carry L2 cache policies: the divergence pair is marked evict-last in pass A
+// (pass B reads it again) and evict-first in pass B, the verifier input evict-first.
 #include <cfloat>
 #include <climits>
 #include <type_traits>
@@ -54,6 +54,7 @@
 namespace asv {
 
 constexpr int kJsdThreads = 256;  // threads per CTA the kernel is compiled for (launch bounds)
+constexpr int kJsdCtasPerSm = 4;  // CTAs per SM the kernel is compiled for (launch bounds)
 
 struct __align__(16) JsdXchg {
   float mx[3];        // CTA maxima of the inputs
@@ -94,7 +95,9 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   return v;
 }
 
-__device__ __forceinline__ uint4 ldg_stream_last(const void* p, uint64_t pol) {
+// 16-byte load with an L2 cache policy (evict-first for data read for the last time, evict-last
+// for the divergence pair, which pass B reads again).
+__device__ __forceinline__ uint4 ldg_stream_pol(const void* p, uint64_t pol) {
   uint4 v;
   asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
@@ -116,11 +119,11 @@ struct GVec<bf16_t> {
   }
   // Entries [k, k+8) of a row slice; `aligned` slices use one 16-byte load, others ordinary loads
   // with -inf at and beyond `lim`.
-  // `last`: the data is read for the last time (its L2 lines are marked for early eviction).
-  __device__ static __forceinline__ uint4 load(const void* base, int k, int lim, bool aligned, bool last = false,
+  // With a policy (`hint`), the load carries that L2 cache policy.
+  __device__ static __forceinline__ uint4 load(const void* base, int k, int lim, bool aligned, bool hint = false,
                                                uint64_t pol = 0) {
     const uint16_t* r = static_cast<const uint16_t*>(base);
-    if (aligned) return last ? ldg_stream_last(r + k, pol) : ldg_stream(r + k);
+    if (aligned) return hint ? ldg_stream_pol(r + k, pol) : ldg_stream(r + k);
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -149,10 +152,10 @@ struct GVec<float> {
   __device__ static __forceinline__ uint4 pad() {
     return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
   }
-  __device__ static __forceinline__ uint4 load(const void* base, int k, int lim, bool aligned, bool last = false,
+  __device__ static __forceinline__ uint4 load(const void* base, int k, int lim, bool aligned, bool hint = false,
                                                uint64_t pol = 0) {
     const float* r = static_cast<const float*>(base);
-    if (aligned) return last ? ldg_stream_last(r + k, pol) : ldg_stream(r + k);
+    if (aligned) return hint ? ldg_stream_pol(r + k, pol) : ldg_stream(r + k);
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) w[i] = (k + i < lim) ? __float_as_uint(__ldg(r + k + i)) : 0xff800000u;
@@ -282,7 +285,7 @@ __device__ __forceinline__ float2 delta2(float2 a, float2 b, float2 t) {
 }
 
 template <typename T, int MODE, int DSRC, bool ALIGNED>
-__global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArgs p) {
+__global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(const JsdArgs p) {
   using G = GVec<T>;
   constexpr int NT = JsdTraits<MODE>::NT;
   constexpr int TGT = JsdTraits<MODE>::TGT;
@@ -316,7 +319,10 @@ __global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArg
 #pragma unroll
   for (int j = 0; j < NT; ++j) slice[j] = static_cast<const char*>(p.x[j]) + (row_base + size_t(v0)) * G::kBytes;
 
+  // L2 policies: the verifier input is read once (evict first); the divergence pair is read again
+  // by pass B (evict last until then, evict first on that last read).
   const uint64_t pol_last = policy_evict_first();
+  const uint64_t pol_keep = policy_evict_last();
 
   // ---------------------------------------------------------------- pass A: maxima, exp sums, argmax
   RunMax<T> rmax[NT];
@@ -336,14 +342,14 @@ __global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArg
     int vi = tid;
     if (vi < nvec) {
 #pragma unroll
-      for (int j = 0; j < NT; ++j) cur[j] = G::load(slice[j], vi * VEC, len, aligned, j == 2, pol_last);
+      for (int j = 0; j < NT; ++j) cur[j] = G::load(slice[j], vi * VEC, len, aligned, true, j == 2 ? pol_last : pol_keep);
     }
     for (; vi < nvec; vi += kJsdThreads) {
       const int vn = vi + kJsdThreads;
       // Prefetch the next vector (consumed only while it is in range).
       if (vn < nvec) {
 #pragma unroll
-        for (int j = 0; j < NT; ++j) nxt[j] = G::load(slice[j], vn * VEC, len, aligned, j == 2, pol_last);
+        for (int j = 0; j < NT; ++j) nxt[j] = G::load(slice[j], vn * VEC, len, aligned, true, j == 2 ? pol_last : pol_keep);
       }
       // Running maxima; when a value passes the reference's slack, move the partial sum to a new
       // reference at the current maximum.
@@ -711,6 +717,7 @@ __global__ void __launch_bounds__(kJsdThreads, 4) jsd_family_kernel(const JsdArg
 
 int jsd_static_smem_bytes() { return 0; }
 int jsd_threads() { return kJsdThreads; }
+int jsd_ctas_per_sm() { return kJsdCtasPerSm; }
 
 using JsdKernel = void (*)(const JsdArgs);
 
