@@ -102,6 +102,13 @@ def _declare(L):
     L.oracle_sci_verify.argtypes = [_vp, _vp, C.c_int, _i32p, C.c_int, C.c_int, C.c_int] + [C.c_double] * 6 + \
         [_f64p, _i32p, _i32p, _f64p, _f64p, _u32p]
     L.oracle_sci_verify.restype = None
+    L.oracle_sci_stab_threshold.argtypes = [C.POINTER(SciStateC), C.c_double, C.c_double, C.c_int, C.c_double,
+                                            C.POINTER(C.c_int32)]
+    L.oracle_sci_stab_threshold.restype = C.c_double
+    L.oracle_sci_verify_stab.argtypes = [_vp, _vp, C.c_int, _i32p, C.c_int, C.c_int, C.c_int] + \
+        [C.c_double] * 7 + [C.c_int, C.c_double, C.c_double, C.POINTER(SciStateC), _f64p, _i32p, _i32p, _f64p,
+                            _f64p, _u32p]
+    L.oracle_sci_verify_stab.restype = None
 
 
 def _p(a, ct):
@@ -252,6 +259,34 @@ def rapid_verify(z, q, draft_ids, T: float, eta: float, tail_frac: float, seed: 
 
 # ------------------------------------------------------------------ E2-SCI
 
+class SciStateC(C.Structure):
+    """Per-request stabiliser state (T_applied, age, flags: 1 set, 2 fallback pending)."""
+    _fields_ = [("T_applied", C.c_double), ("age", C.c_int32), ("flags", C.c_uint32)]
+
+
+@dataclass(frozen=True)
+class SciStabilisers:
+    """E2-SCI stabilisers: hysteresis band, minimum refresh interval (windows), and the fallback to
+    a conservative threshold after a window whose acceptance rate is below fallback_acc."""
+    hysteresis: float = 0.0
+    min_refresh: int = 1
+    fallback_acc: float = 0.0
+    fallback_T: float = 0.1
+
+
+def sci_state(B: int):
+    """A zero-filled stabiliser state array for B requests (before the first window)."""
+    return (SciStateC * B)()
+
+
+def sci_stab_threshold(state: "SciStateC", T_cand: float, s: SciStabilisers):
+    """One window's threshold from the candidate and the state; returns (T_used, new_age)."""
+    age = C.c_int32(0)
+    T = lib().oracle_sci_stab_threshold(C.byref(state), T_cand, s.hysteresis, s.min_refresh, s.fallback_T,
+                                        C.byref(age))
+    return T, age.value
+
+
 @dataclass(frozen=True)
 class SciParams:
     T_base: float = 0.3
@@ -280,7 +315,9 @@ class SciResult:
     flags: np.ndarray
 
 
-def sci_verify(draft, target, draft_ids, r_hat, p: SciParams = SciParams()) -> SciResult:
+def sci_verify(draft, target, draft_ids, r_hat, p: SciParams = SciParams(), stab: "SciStabilisers" = None,
+               state=None) -> SciResult:
+    """One window per request; with `stab`, `state` (from sci_state) is read and updated in place."""
     draft, target = _c(draft), _c(target)
     B, R, V = draft.shape
     K = R - 1
@@ -288,8 +325,17 @@ def sci_verify(draft, target, draft_ids, r_hat, p: SciParams = SciParams()) -> S
     rh = np.array(r_hat, np.float64, copy=True).reshape(B)
     out = SciResult(np.zeros(B, np.int32), np.zeros((B, R), np.int32), np.zeros((B, R)), np.zeros(B), rh,
                     np.zeros(B, np.uint32))
-    lib().oracle_sci_verify(draft.ctypes.data, target.ctypes.data, _elem_dtype(draft), _p(d, C.c_int32), B, K, V,
-                            p.T_base, p.alpha_omega, p.tau_credit, p.T_min, p.T_max, p.ewma_beta,
-                            _p(rh, C.c_double), _p(out.accept_len, C.c_int32), _p(out.tokens, C.c_int32),
-                            _p(out.jsd, C.c_double), _p(out.T, C.c_double), _p(out.flags, C.c_uint32))
+    if stab is None:
+        lib().oracle_sci_verify(draft.ctypes.data, target.ctypes.data, _elem_dtype(draft), _p(d, C.c_int32), B, K,
+                                V, p.T_base, p.alpha_omega, p.tau_credit, p.T_min, p.T_max, p.ewma_beta,
+                                _p(rh, C.c_double), _p(out.accept_len, C.c_int32), _p(out.tokens, C.c_int32),
+                                _p(out.jsd, C.c_double), _p(out.T, C.c_double), _p(out.flags, C.c_uint32))
+        return out
+    if state is None or len(state) != B:
+        raise ValueError("stabilisers need a state array of B entries (sci_state(B))")
+    lib().oracle_sci_verify_stab(draft.ctypes.data, target.ctypes.data, _elem_dtype(draft), _p(d, C.c_int32), B, K, V,
+                                 p.T_base, p.alpha_omega, p.tau_credit, p.T_min, p.T_max, p.ewma_beta,
+                                 stab.hysteresis, int(stab.min_refresh), stab.fallback_acc, stab.fallback_T, state,
+                                 _p(rh, C.c_double), _p(out.accept_len, C.c_int32), _p(out.tokens, C.c_int32),
+                                 _p(out.jsd, C.c_double), _p(out.T, C.c_double), _p(out.flags, C.c_uint32))
     return out

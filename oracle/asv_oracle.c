@@ -492,22 +492,64 @@ double oracle_sci_threshold(double r_hat, double T_base, double alpha_omega, dou
 double oracle_sci_ewma(double r_hat, double p_acc, double beta) { return (1.0 - beta) * r_hat + beta * p_acc; }
 
 /*
+ * E2-SCI stabilisers ([SCI] Key design 3 names hysteresis, a minimum refresh interval and a
+ * fallback to a conservative threshold when the accuracy under the predicted threshold drops
+ * below delta; it gives no constants).  One window's threshold from the candidate T_cand and the
+ * request's state (T_applied, age = windows since the applied threshold last changed, set,
+ * fallback pending):
+ *   first window (not set)            -> T_cand
+ *   fallback pending                  -> fallback_T
+ *   age >= min_refresh and |T_cand - T_applied| > hysteresis -> T_cand
+ *   otherwise                         -> T_applied (age grows by one)
+ * A change sets age to 1.  After the window, fallback is pending for the next one iff the
+ * window's acceptance rate n / K is below fallback_acc.  With hysteresis 0, min_refresh 1 and
+ * fallback_acc 0 every window uses T_cand.
+ */
+typedef struct {
+  double T_applied;
+  int32_t age;
+  uint32_t flags; /* 1: a threshold has been applied; 2: fallback pending */
+} oracle_sci_state;
+
+double oracle_sci_stab_threshold(const oracle_sci_state* st, double T_cand, double hysteresis, int min_refresh,
+                                 double fallback_T, int32_t* new_age) {
+  if (!(st->flags & 1u)) {
+    *new_age = 1;
+    return T_cand;
+  }
+  if (st->flags & 2u) {
+    *new_age = 1;
+    return fallback_T;
+  }
+  if (st->age >= min_refresh && fabs(T_cand - st->T_applied) > hysteresis) {
+    *new_age = 1;
+    return T_cand;
+  }
+  *new_age = st->age + 1;
+  return st->T_applied;
+}
+
+/*
  * One E2-SCI verification window per request over [B, K+1, V] draft and
  * target logits.  [SCI] Key design 3.
- *   T = threshold(r_hat[r]);  J_i = JSD(softmax draft_i || softmax target_i);
+ *   T = threshold(r_hat[r]) (through the stabilisers when `state` is given);
+ *   J_i = JSD(softmax draft_i || softmax target_i);
  *   draft i is accepted while J_i <= T (rejected when J_i > T); n = accepted prefix;
  *   tokens = d_0..d_{n-1}, argmax(target_n) (lowest index);
- *   p_acc = n / K;  r_hat[r] <- ewma(r_hat[r], p_acc)   (in place).
- * out_jsd [B,K+1] and out_T [B] are optional.
+ *   p_acc = n / K;  r_hat[r] <- ewma(r_hat[r], p_acc)   (in place; state updated likewise).
+ * out_jsd [B,K+1] and out_T [B] are optional.  A flagged request keeps its r_hat and state.
  */
-void oracle_sci_verify(const void* draft, const void* target, int dtype, const int32_t* draft_ids, int B, int K,
-                       int V, double T_base, double alpha_omega, double tau_credit, double T_min, double T_max,
-                       double ewma_beta, double* r_hat, int32_t* out_accept_len, int32_t* out_tokens,
-                       double* out_jsd, double* out_T, uint32_t* out_flags) {
+void oracle_sci_verify_stab(const void* draft, const void* target, int dtype, const int32_t* draft_ids, int B,
+                            int K, int V, double T_base, double alpha_omega, double tau_credit, double T_min,
+                            double T_max, double ewma_beta, double hysteresis, int min_refresh, double fallback_acc,
+                            double fallback_T, oracle_sci_state* state, double* r_hat, int32_t* out_accept_len,
+                            int32_t* out_tokens, double* out_jsd, double* out_T, uint32_t* out_flags) {
   double* J = (double*)malloc(sizeof(double) * (size_t)(K + 1));
   for (int r = 0; r < B; ++r) {
     uint32_t flags = 0;
     double T = oracle_sci_threshold(r_hat[r], T_base, alpha_omega, tau_credit, T_min, T_max);
+    int32_t age = 0;
+    if (state) T = oracle_sci_stab_threshold(&state[r], T, hysteresis, min_refresh, fallback_T, &age);
     if (out_T) out_T[r] = T;
     for (int i = 0; i < K; ++i) {
       int d = draft_ids[(size_t)r * K + i];
@@ -551,8 +593,23 @@ void oracle_sci_verify(const void* draft, const void* target, int dtype, const i
       else if (i == n) v = c;
       out_tokens[(size_t)r * (K + 1) + i] = v;
     }
-    r_hat[r] = oracle_sci_ewma(r_hat[r], K > 0 ? (double)n / (double)K : 0.0, ewma_beta);
+    const double p_acc = K > 0 ? (double)n / (double)K : 0.0;
+    r_hat[r] = oracle_sci_ewma(r_hat[r], p_acc, ewma_beta);
+    if (state) {
+      state[r].T_applied = T;
+      state[r].age = age;
+      state[r].flags = 1u | (p_acc < fallback_acc ? 2u : 0u);
+    }
     if (out_flags) out_flags[r] = flags;
   }
   free(J);
+}
+
+void oracle_sci_verify(const void* draft, const void* target, int dtype, const int32_t* draft_ids, int B, int K,
+                       int V, double T_base, double alpha_omega, double tau_credit, double T_min, double T_max,
+                       double ewma_beta, double* r_hat, int32_t* out_accept_len, int32_t* out_tokens,
+                       double* out_jsd, double* out_T, uint32_t* out_flags) {
+  oracle_sci_verify_stab(draft, target, dtype, draft_ids, B, K, V, T_base, alpha_omega, tau_credit, T_min, T_max,
+                         ewma_beta, 0.0, 1, 0.0, 0.0, NULL, r_hat, out_accept_len, out_tokens, out_jsd, out_T,
+                         out_flags);
 }

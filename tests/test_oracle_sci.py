@@ -95,3 +95,74 @@ def test_five_windows_state_carry_and_resume():
     for w in wins[2:]:
         r3 = oracle.sci_verify(w.a, w.t, w.drafts, r3).r_hat
     np.testing.assert_array_equal(r, r3)
+
+
+# ------------------------------------------------------------------ stabilisers
+
+def _stab_golden():
+    rows = []
+    with open(os.path.join(GOLDEN, "sci_stabilisers.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                w, n, T, r = line.split()
+                rows.append((int(w), int(n), float(T), float(r)))
+    return rows
+
+
+def _scripted_window(rng, n, K, V):
+    """Rows before n: draft == target (J = 0, accepted at any T >= 0); row n (if n < K): disjoint
+    spikes (J close to ln 2, rejected at any T <= 0.6)."""
+    draft = rng.standard_normal((1, K + 1, V)).astype(np.float32)
+    target = draft.copy()
+    if n < K:
+        draft[0, n, :] = -50.0
+        target[0, n, :] = -50.0
+        draft[0, n, 0] = 50.0
+        target[0, n, 1] = 50.0
+    return draft, target, np.zeros((1, K), np.int32)
+
+
+def test_stabiliser_golden_sequence():
+    rng = np.random.default_rng(5)
+    stab = oracle.SciStabilisers(hysteresis=0.02, min_refresh=2, fallback_acc=0.3, fallback_T=0.12)
+    state = oracle.sci_state(1)
+    r_hat = np.array([0.6])
+    for w, n, T_exp, r_exp in _stab_golden():
+        draft, target, d = _scripted_window(rng, n, 4, 16)
+        out = oracle.sci_verify(draft, target, d, r_hat, stab=stab, state=state)
+        assert out.accept_len[0] == n, w
+        assert out.T[0] == pytest.approx(T_exp, abs=1e-12), w
+        assert out.r_hat[0] == pytest.approx(r_exp, abs=1e-12), w
+        r_hat = out.r_hat
+
+
+def test_stabiliser_rule_cases():
+    s = oracle.SciStabilisers(hysteresis=0.05, min_refresh=3, fallback_acc=0.5, fallback_T=0.11)
+    st = oracle.sci_state(1)[0]
+    assert oracle.sci_stab_threshold(st, 0.33, s) == (0.33, 1)          # first window takes the candidate
+    st.flags, st.T_applied, st.age = 1, 0.30, 2
+    assert oracle.sci_stab_threshold(st, 0.40, s) == (0.30, 3)          # refresh interval not reached
+    st.age = 3
+    assert oracle.sci_stab_threshold(st, 0.34, s) == (0.30, 4)          # inside the hysteresis band
+    assert oracle.sci_stab_threshold(st, 0.36, s) == (0.36, 1)          # outside it: change
+    assert oracle.sci_stab_threshold(st, 0.24, s) == (0.24, 1)          # the band works both ways
+    st.flags = 3
+    assert oracle.sci_stab_threshold(st, 0.50, s) == (0.11, 1)          # fallback pending wins
+
+
+def test_stabilisers_off_equal_plain_windows():
+    rng = np.random.default_rng(8)
+    B, K, V = 6, 4, 300
+    off = oracle.SciStabilisers(hysteresis=0.0, min_refresh=1, fallback_acc=0.0, fallback_T=0.1)
+    state = oracle.sci_state(B)
+    r_a = np.full(B, 0.6)
+    r_b = r_a.copy()
+    for w in range(4):
+        draft, target, d = _straddling_window(rng, B, K, V, gen.F32)
+        a = oracle.sci_verify(draft, target, d, r_a)
+        b = oracle.sci_verify(draft, target, d, r_b, stab=off, state=state)
+        np.testing.assert_array_equal(a.accept_len, b.accept_len)
+        np.testing.assert_array_equal(a.tokens, b.tokens)
+        np.testing.assert_array_equal(a.T, b.T)
+        np.testing.assert_array_equal(a.r_hat, b.r_hat)
+        r_a, r_b = a.r_hat, b.r_hat
