@@ -102,6 +102,12 @@ def _declare(L):
     L.oracle_sci_verify.argtypes = [_vp, _vp, C.c_int, _i32p, C.c_int, C.c_int, C.c_int] + [C.c_double] * 6 + \
         [_f64p, _i32p, _i32p, _f64p, _f64p, _u32p]
     L.oracle_sci_verify.restype = None
+    L.oracle_rapid_row_mode.argtypes = [_f32p, _f32p, C.c_int, C.c_double, C.c_double, C.c_double, C.c_int, _f64p,
+                                        _f64p, _f64p, _f64p, C.POINTER(C.c_int)]
+    L.oracle_rapid_row_mode.restype = C.c_int
+    L.oracle_rapid_verify_mode.argtypes = [_f32p, _f32p, _i32p, C.c_int, C.c_int, C.c_int, C.c_double, C.c_double,
+                                           C.c_double, C.c_int, C.c_uint64, C.c_uint32, _i32p, _i32p, _u32p]
+    L.oracle_rapid_verify_mode.restype = None
     L.oracle_sci_stab_threshold.argtypes = [C.POINTER(SciStateC), C.c_double, C.c_double, C.c_int, C.c_double,
                                             C.POINTER(C.c_int32)]
     L.oracle_sci_stab_threshold.restype = C.c_double
@@ -219,14 +225,15 @@ class RapidRow:
     near: bool
 
 
-def rapid_row(z, q, T: float, eta: float, tail_frac: float = 0.1) -> RapidRow:
+def rapid_row(z, q, T: float, eta: float, tail_frac: float = 0.1, tail_mode: int = 0) -> RapidRow:
     z = _c(np.asarray(z, np.float32))
     q = _c(np.asarray(q, np.float32))
     V = z.size
     p, zh, ph, pr = (np.zeros(V) for _ in range(4))
     near = C.c_int(0)
-    n = lib().oracle_rapid_row(_p(z, C.c_float), _p(q, C.c_float), V, T, eta, tail_frac, _p(p, C.c_double),
-                               _p(zh, C.c_double), _p(ph, C.c_double), _p(pr, C.c_double), C.byref(near))
+    n = lib().oracle_rapid_row_mode(_p(z, C.c_float), _p(q, C.c_float), V, T, eta, tail_frac, tail_mode,
+                                    _p(p, C.c_double), _p(zh, C.c_double), _p(ph, C.c_double), _p(pr, C.c_double),
+                                    C.byref(near))
     return RapidRow(p, zh, ph, pr, n, bool(near.value))
 
 
@@ -244,16 +251,17 @@ class RapidResult:
     flags: np.ndarray
 
 
-def rapid_verify(z, q, draft_ids, T: float, eta: float, tail_frac: float, seed: int, offset: int = 0) -> RapidResult:
+def rapid_verify(z, q, draft_ids, T: float, eta: float, tail_frac: float, seed: int, offset: int = 0,
+                 tail_mode: int = 0) -> RapidResult:
     z = _c(np.asarray(z, np.float32))
     q = _c(np.asarray(q, np.float32))
     B, R, V = z.shape
     G = R - 1
     d = _c(np.asarray(draft_ids, np.int32).reshape(B, G))
     out = RapidResult(np.zeros(B, np.int32), np.zeros((B, R), np.int32), np.zeros(B, np.uint32))
-    lib().oracle_rapid_verify(_p(z, C.c_float), _p(q, C.c_float), _p(d, C.c_int32), B, G, V, T, eta, tail_frac,
-                              seed, offset, _p(out.accept_len, C.c_int32), _p(out.tokens, C.c_int32),
-                              _p(out.flags, C.c_uint32))
+    lib().oracle_rapid_verify_mode(_p(z, C.c_float), _p(q, C.c_float), _p(d, C.c_int32), B, G, V, T, eta,
+                                   tail_frac, tail_mode, seed, offset, _p(out.accept_len, C.c_int32),
+                                   _p(out.tokens, C.c_int32), _p(out.flags, C.c_uint32))
     return out
 
 

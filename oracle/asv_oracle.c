@@ -326,13 +326,16 @@ double oracle_rapid_uniform(uint64_t seed, uint32_t offset, uint32_t stream, uin
  *   zhat = z + eta * T * (q - p)
  *   phat = softmax(zhat / T)
  *   tail = { k : phat_k < tail_frac * max_j phat_j }
- *   prot_k = p_k on the tail; on the head phat_k * (1 - sum_tail p) / sum_head phat.
+ *   tail_mode 0: prot_k = p_k on the tail; on the head phat_k * (1 - sum_tail p) / sum_head phat.
+ *   tail_mode 1 (the other reading: substitute p on the tail, then renormalise every entry):
+ *     w_k = p_k on the tail, phat_k on the head; prot_k = w_k / sum_j w_j.
  * Arrays p, zhat, phat, prot are length V (any may be NULL).  Returns the
  * number of tail entries; *near is set when some phat_k lies within a relative
  * 1e-5 of the tail boundary (the library decides the mask in fp32).
  */
-int oracle_rapid_row(const float* z, const float* q, int V, double T, double eta, double tail_frac,
-                     double* p_out, double* zhat_out, double* phat_out, double* prot_out, int* near) {
+int oracle_rapid_row_mode(const float* z, const float* q, int V, double T, double eta, double tail_frac,
+                          int tail_mode, double* p_out, double* zhat_out, double* phat_out, double* prot_out,
+                          int* near) {
   double* p = (double*)malloc(sizeof(double) * (size_t)V);
   double* zh = (double*)malloc(sizeof(double) * (size_t)V);
   double* ph = (double*)malloc(sizeof(double) * (size_t)V);
@@ -363,17 +366,27 @@ int oracle_rapid_row(const float* z, const float* q, int V, double T, double eta
     }
   }
   double scale = (1.0 - tail_p) / head_ph;
+  double wsum = 0.0;  /* tail_mode 1: the sum of the substituted weights */
+  for (int k = 0; k < V; ++k) wsum += (ph[k] < thr) ? p[k] : ph[k];
   for (int k = 0; k < V; ++k) {
     if (p_out) p_out[k] = p[k];
     if (zhat_out) zhat_out[k] = zh[k];
     if (phat_out) phat_out[k] = ph[k];
-    if (prot_out) prot_out[k] = (ph[k] < thr) ? p[k] : ph[k] * scale;
+    if (prot_out) {
+      if (tail_mode == 0) prot_out[k] = (ph[k] < thr) ? p[k] : ph[k] * scale;
+      else prot_out[k] = ((ph[k] < thr) ? p[k] : ph[k]) / wsum;
+    }
   }
   if (near) *near = nr;
   free(p);
   free(zh);
   free(ph);
   return ntail;
+}
+
+int oracle_rapid_row(const float* z, const float* q, int V, double T, double eta, double tail_frac, double* p_out,
+                     double* zhat_out, double* phat_out, double* prot_out, int* near) {
+  return oracle_rapid_row_mode(z, q, V, T, eta, tail_frac, 0, p_out, zhat_out, phat_out, prot_out, near);
 }
 
 /* Exponential race: argmin_k E_k / w_k over w_k > 0, E_k = -ln u_k with u_k the
@@ -409,9 +422,9 @@ int oracle_race(const double* w, int V, uint64_t seed, uint32_t offset, uint32_t
  *             from p_n if that residual is all zero);
  *   else:     token G ~ prot_G (stream 2).
  */
-void oracle_rapid_verify(const float* z, const float* q, const int32_t* draft_ids, int B, int G, int V, double T,
-                         double eta, double tail_frac, uint64_t seed, uint32_t offset, int32_t* out_accept_len,
-                         int32_t* out_tokens, uint32_t* out_flags) {
+void oracle_rapid_verify_mode(const float* z, const float* q, const int32_t* draft_ids, int B, int G, int V,
+                              double T, double eta, double tail_frac, int tail_mode, uint64_t seed, uint32_t offset,
+                              int32_t* out_accept_len, int32_t* out_tokens, uint32_t* out_flags) {
   double* p = (double*)malloc(sizeof(double) * (size_t)V);
   double* prot = (double*)malloc(sizeof(double) * (size_t)V);
   double* r = (double*)malloc(sizeof(double) * (size_t)V);
@@ -434,7 +447,7 @@ void oracle_rapid_verify(const float* z, const float* q, const int32_t* draft_id
     int n = G, near = 0;
     for (int i = 0; i < G; ++i) {
       size_t off = ((size_t)b * (G + 1) + i) * (size_t)V;
-      oracle_rapid_row(z + off, q + off, V, T, eta, tail_frac, NULL, NULL, NULL, prot, &near);
+      oracle_rapid_row_mode(z + off, q + off, V, T, eta, tail_frac, tail_mode, NULL, NULL, NULL, prot, &near);
       if (near) flags |= OR_NEAR_TAIL;
       int d = draft_ids[(size_t)b * G + i];
       double u = oracle_rapid_uniform(seed, offset, 0u, (uint32_t)b, (uint32_t)i, 0u);
@@ -447,7 +460,7 @@ void oracle_rapid_verify(const float* z, const float* q, const int32_t* draft_id
       }
     }
     size_t off = ((size_t)b * (G + 1) + n) * (size_t)V;
-    oracle_rapid_row(z + off, q + off, V, T, eta, tail_frac, p, NULL, NULL, prot, &near);
+    oracle_rapid_row_mode(z + off, q + off, V, T, eta, tail_frac, tail_mode, p, NULL, NULL, prot, &near);
     if (near) flags |= OR_NEAR_TAIL;
     int tok, rn = 0;
     if (n < G) {
@@ -475,6 +488,13 @@ void oracle_rapid_verify(const float* z, const float* q, const int32_t* draft_id
   free(p);
   free(prot);
   free(r);
+}
+
+void oracle_rapid_verify(const float* z, const float* q, const int32_t* draft_ids, int B, int G, int V, double T,
+                         double eta, double tail_frac, uint64_t seed, uint32_t offset, int32_t* out_accept_len,
+                         int32_t* out_tokens, uint32_t* out_flags) {
+  oracle_rapid_verify_mode(z, q, draft_ids, B, G, V, T, eta, tail_frac, 0, seed, offset, out_accept_len, out_tokens,
+                           out_flags);
 }
 
 /* ------------------------------------------------------------------ E2-SCI */

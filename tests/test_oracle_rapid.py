@@ -124,3 +124,38 @@ def test_verify_scan_structure():
                 u = oracle.rapid_uniform(1234, 0, 0, r, i, 0)
                 dd = b.drafts[r, i]
                 assert (u * float(b.q[r, i, dd]) < row.prot[dd]) == (i < n)
+
+
+# ------------------------------------------------------------------ the other tail-protection reading
+
+def _tail_case(seed, V=200, eta=10.0):
+    rng = np.random.default_rng(seed)
+    z = (2.0 * rng.standard_normal(V) - 1.1 * np.log(rng.permutation(V) + 1.0)).astype(np.float32)
+    q = sps.softmax(z.astype(np.float64) + rng.standard_normal(V)).astype(np.float32)
+    return z, q, eta
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_renormalised_tail_reading(seed):
+    """tail_mode 1: p substitutes phat on the tail, then every entry is renormalised, so the
+    protected target is w / sum(w) with w = p on the tail and phat on the head."""
+    z, q, eta = _tail_case(seed)
+    r0 = oracle.rapid_row(z, q, 1.0, eta, 0.1, tail_mode=0)
+    r1 = oracle.rapid_row(z, q, 1.0, eta, 0.1, tail_mode=1)
+    np.testing.assert_array_equal(r0.p, r1.p)
+    np.testing.assert_array_equal(r0.phat, r1.phat)
+    tail = r1.phat < 0.1 * r1.phat.max()
+    assert 0 < tail.sum() < len(z)
+    assert r1.prot.sum() == pytest.approx(1.0, abs=1e-12)
+    # one common factor 1/Z on both sides of the boundary
+    ratios = np.concatenate([r1.prot[tail] / r1.p[tail], r1.prot[~tail] / r1.phat[~tail]])
+    np.testing.assert_allclose(ratios, ratios[0], rtol=1e-12)
+    # unlike the default reading, the tail is scaled too (Z != 1 here)
+    assert abs(ratios[0] - 1.0) > 1e-6
+    np.testing.assert_allclose(r0.prot[tail], r0.p[tail], rtol=0, atol=0)
+
+
+def test_renormalised_tail_reading_eta_zero_is_p():
+    z, q, _ = _tail_case(7)
+    r1 = oracle.rapid_row(z, q, 1.0, 0.0, 0.1, tail_mode=1)
+    np.testing.assert_allclose(r1.prot, r1.p, rtol=1e-12, atol=0)
