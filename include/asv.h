@@ -211,6 +211,20 @@ asv_status rapid_verify(const float* z, const float* q, const int32_t* draft_ids
                         int32_t* out_tokens, uint32_t* out_req_status, void* workspace, size_t ws_bytes,
                         cudaStream_t stream);
 
+/* RAPID options ([RAPID] Key design 3 leaves the renormalisation of the protected target open). */
+typedef struct {
+  int tail_mode; /* 0: tail entries keep p exactly and the head is rescaled so the protected target
+                    sums to 1 (the reading rapid_verify uses); 1: p substitutes phat on the tail and
+                    every entry is renormalised (tail p/Z, head phat/Z, Z = tail p-mass + head
+                    phat-mass) */
+} asv_rapid_options;
+
+/* rapid_verify with options (NULL = the defaults).  An unknown tail_mode is ASV_ERR_PARAM. */
+asv_status rapid_verify_ex(const float* z, const float* q, const int32_t* draft_ids, int B, int G, int V, float T,
+                           float eta, float tail_frac, uint64_t seed, uint32_t offset, const asv_rapid_options* options,
+                           int32_t* out_accept_len, int32_t* out_tokens, uint32_t* out_req_status, void* workspace,
+                           size_t ws_bytes, cudaStream_t stream);
+
 /* E2-SCI threshold and credit parameters.  [SCI] Key design 3. */
 typedef struct {
   double T_base;      /* base threshold */
@@ -238,6 +252,47 @@ asv_status sci_verify(const void* draft_logits, const void* target_logits, int d
                       int B, int K, int V, const asv_sci_params* params, double* r_hat, int32_t* out_accept_len,
                       int32_t* out_tokens, float* out_jsd, float* out_T, uint32_t* out_req_status,
                       void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * E2-SCI stabilisers.  [SCI] Key design 3 adds hysteresis, a minimum refresh interval and a
+ * fallback to a conservative threshold when accuracy under the predicted threshold drops below a
+ * bound, and gives no constants; these are the parameters.  One window's threshold, from the
+ * candidate T_cand = clamp(T_base + alpha_omega*(r_hat - tau_credit), T_min, T_max) and the
+ * request's state:
+ *   first window (state not set)                               -> T_cand
+ *   fallback pending                                           -> fallback_T
+ *   age >= min_refresh and |T_cand - T_applied| > hysteresis   -> T_cand
+ *   otherwise                                                  -> T_applied
+ * A change sets age to 1, keeping T_applied adds one.  After the window, a fallback is pending
+ * for the next window iff n / K < fallback_acc.  hysteresis = 0, min_refresh = 1 and
+ * fallback_acc = 0 reproduce sci_verify.
+ */
+typedef struct {
+  double hysteresis;   /* >= 0 */
+  int32_t min_refresh; /* >= 1 windows */
+  int32_t reserved;    /* 0 */
+  double fallback_acc; /* acceptance rate below which the next window falls back */
+  double fallback_T;   /* the conservative threshold */
+} asv_sci_stabilisers;
+
+/* Per-request stabiliser state, device memory, zero-filled before a request's first window. */
+typedef struct {
+  double T_applied; /* threshold used by the last window */
+  int32_t age;      /* windows since T_applied last changed */
+  uint32_t flags;   /* 1: a threshold has been applied; 2: fallback pending */
+} asv_sci_state;
+
+/*
+ * sci_verify_ex -- sci_verify with stabilisers.  `stab` NULL is sci_verify; otherwise `state`
+ * [B] (16-byte aligned) is read and updated in place with r_hat (a flagged request leaves both
+ * unchanged) and out_T reports the threshold the window used.  Invalid stabiliser values are
+ * ASV_ERR_PARAM.
+ */
+asv_status sci_verify_ex(const void* draft_logits, const void* target_logits, int dtype, const int32_t* draft_ids,
+                         int B, int K, int V, const asv_sci_params* params, const asv_sci_stabilisers* stab,
+                         double* r_hat, asv_sci_state* state, int32_t* out_accept_len, int32_t* out_tokens,
+                         float* out_jsd, float* out_T, uint32_t* out_req_status, void* workspace, size_t ws_bytes,
+                         cudaStream_t stream);
 
 #ifdef __cplusplus
 }

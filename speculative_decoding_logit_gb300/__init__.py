@@ -34,6 +34,9 @@ from ._binding import (  # noqa: F401
     RapidOutput,
     SciOutput,
     SciParams,
+    SciStabilisers,
+    TAIL_KEEP_P,
+    TAIL_RENORMALISE_ALL,
     asymspec_verify,
     asymspec_verify_host,
     host_arena_bytes,
@@ -41,6 +44,8 @@ from ._binding import (  # noqa: F401
     library_path,
     query_plan,
     rapid_verify,
+    sci_state_decode,
+    sci_state_new,
     sci_verify,
     set_tuning,
     workspace_bytes,

@@ -66,6 +66,15 @@ DELTA_A = 1
 DELTA_T_MINUS_B = 2
 
 
+class _RapidOptionsC(C.Structure):
+    _fields_ = [("tail_mode", C.c_int)]
+
+
+class _SciStabC(C.Structure):
+    _fields_ = [("hysteresis", C.c_double), ("min_refresh", C.c_int32), ("reserved", C.c_int32),
+                ("fallback_acc", C.c_double), ("fallback_T", C.c_double)]
+
+
 class _SciParamsC(C.Structure):
     _fields_ = [("T_base", C.c_double), ("alpha_omega", C.c_double), ("tau_credit", C.c_double),
                 ("T_min", C.c_double), ("T_max", C.c_double), ("ewma_beta", C.c_double)]
@@ -99,6 +108,12 @@ def _declare(L):
     L.sci_verify.argtypes = [_vp, _vp, _i, _vp, _i, _i, _i, C.POINTER(_SciParamsC), _vp, _vp, _vp, _vp, _vp, _vp,
                              _vp, _sz, _vp]
     L.sci_verify.restype = _i
+    L.rapid_verify_ex.argtypes = [_vp, _vp, _vp, _i, _i, _i, _f, _f, _f, C.c_uint64, C.c_uint32,
+                                  C.POINTER(_RapidOptionsC), _vp, _vp, _vp, _vp, _sz, _vp]
+    L.rapid_verify_ex.restype = _i
+    L.sci_verify_ex.argtypes = [_vp, _vp, _i, _vp, _i, _i, _i, C.POINTER(_SciParamsC), C.POINTER(_SciStabC), _vp,
+                                _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+    L.sci_verify_ex.restype = _i
 
 
 def _check(status: int, what: str):
@@ -250,10 +265,16 @@ class RapidOutput:
     req_status: torch.Tensor
 
 
+TAIL_KEEP_P = 0          # tail entries keep p, the head is rescaled (rapid_verify's reading)
+TAIL_RENORMALISE_ALL = 1  # p substitutes phat on the tail, then every entry is renormalised
+
+
 def rapid_verify(z: torch.Tensor, q: torch.Tensor, draft_ids: torch.Tensor, T: float = 1.0, eta: float = 10.0,
-                 tail_frac: float = 0.1, seed: int = 1234, offset: int = 0, *, out: Optional[RapidOutput] = None,
-                 workspace: Optional[torch.Tensor] = None, stream=None) -> RapidOutput:
-    """RAPID verification of fp32 target logits z and drafter probabilities q, [B, G+1, V]."""
+                 tail_frac: float = 0.1, seed: int = 1234, offset: int = 0, *, tail_mode: int = TAIL_KEEP_P,
+                 out: Optional[RapidOutput] = None, workspace: Optional[torch.Tensor] = None,
+                 stream=None) -> RapidOutput:
+    """RAPID verification of fp32 target logits z and drafter probabilities q, [B, G+1, V]
+    (`tail_mode` selects the reading of the tail protection, see rapid_verify_ex)."""
     _need_cuda(z, q, draft_ids)
     if z.dim() != 3 or z.shape != q.shape:
         raise AsvError(2, "z and q must share one [B, G+1, V] shape")
@@ -273,10 +294,12 @@ def rapid_verify(z: torch.Tensor, q: torch.Tensor, draft_ids: torch.Tensor, T: f
                           torch.empty(B, dtype=torch.int32, device=dev))
     need = workspace_bytes(ASV_MODE_RAPID, B, G, V, ASV_F32)
     ws = workspace if workspace is not None else _workspace(dev, sh, need)
-    st = library().rapid_verify(_ptr(z), _ptr(q), _ptr(draft_ids), B, G, V, float(T), float(eta), float(tail_frac),
-                                int(seed) & 0xFFFFFFFFFFFFFFFF, int(offset) & 0xFFFFFFFF, _ptr(out.accept_len),
-                                _ptr(out.tokens), _ptr(out.req_status), _ptr(ws), ws.numel(), sh)
-    _check(st, "rapid_verify")
+    opt = _RapidOptionsC(int(tail_mode))
+    st = library().rapid_verify_ex(_ptr(z), _ptr(q), _ptr(draft_ids), B, G, V, float(T), float(eta),
+                                   float(tail_frac), int(seed) & 0xFFFFFFFFFFFFFFFF, int(offset) & 0xFFFFFFFF,
+                                   C.byref(opt), _ptr(out.accept_len), _ptr(out.tokens), _ptr(out.req_status),
+                                   _ptr(ws), ws.numel(), sh)
+    _check(st, "rapid_verify_ex")
     return out
 
 
@@ -301,10 +324,33 @@ class SciOutput:
     req_status: torch.Tensor
 
 
+@dataclass(frozen=True)
+class SciStabilisers:
+    """E2-SCI stabilisers (see sci_verify_ex in include/asv.h)."""
+    hysteresis: float = 0.0
+    min_refresh: int = 1
+    fallback_acc: float = 0.0
+    fallback_T: float = 0.1
+
+
+def sci_state_new(B: int, device="cuda") -> torch.Tensor:
+    """Zero-filled stabiliser state for B requests: [B, 4] int32 (16 bytes per request: T_applied
+    as float64, then age and flags)."""
+    return torch.zeros(B, 4, dtype=torch.int32, device=device)
+
+
+def sci_state_decode(state: torch.Tensor):
+    """(T_applied float64 [B], age int32 [B], flags int32 [B]) of a state tensor (copied to host)."""
+    h = state.cpu().contiguous()
+    return h[:, :2].contiguous().view(torch.float64).reshape(-1), h[:, 2].clone(), h[:, 3].clone()
+
+
 def sci_verify(draft: torch.Tensor, target: torch.Tensor, draft_ids: torch.Tensor, r_hat: torch.Tensor,
-               params: SciParams = SciParams(), *, out: Optional[SciOutput] = None,
+               params: SciParams = SciParams(), *, stabilisers: Optional[SciStabilisers] = None,
+               state: Optional[torch.Tensor] = None, out: Optional[SciOutput] = None,
                workspace: Optional[torch.Tensor] = None, stream=None) -> SciOutput:
-    """One E2-SCI window; r_hat (float64 [B], device) is updated in place."""
+    """One E2-SCI window; r_hat (float64 [B], device) is updated in place, and with `stabilisers`
+    so is `state` (from sci_state_new)."""
     _need_cuda(draft, target, draft_ids, r_hat)
     if draft.dim() != 3 or draft.shape != target.shape or draft.dtype != target.dtype:
         raise AsvError(2, "draft and target must share one [B, K+1, V] shape and dtype")
@@ -316,6 +362,10 @@ def sci_verify(draft: torch.Tensor, target: torch.Tensor, draft_ids: torch.Tenso
         raise AsvError(2, "r_hat must be float64 [B]")
     for n, x in (("draft", draft), ("target", target), ("draft_ids", draft_ids), ("r_hat", r_hat)):
         _contig(x, n)
+    if stabilisers is not None:
+        if state is None or state.dtype != torch.int32 or tuple(state.shape) != (B, 4) or not state.is_cuda:
+            raise AsvError(2, "state must be an int32 [B, 4] CUDA tensor (sci_state_new)")
+        _contig(state, "state")
     dev = draft.device
     sh = _stream_handle(dev, stream)
     if out is None:
@@ -329,8 +379,16 @@ def sci_verify(draft: torch.Tensor, target: torch.Tensor, draft_ids: torch.Tenso
     ws = workspace if workspace is not None else _workspace(dev, sh, need)
     pc = _SciParamsC(params.T_base, params.alpha_omega, params.tau_credit, params.T_min, params.T_max,
                      params.ewma_beta)
-    st = library().sci_verify(_ptr(draft), _ptr(target), dt, _ptr(draft_ids), B, K, V, C.byref(pc), _ptr(r_hat),
-                              _ptr(out.accept_len), _ptr(out.tokens), _ptr(out.jsd), _ptr(out.T),
-                              _ptr(out.req_status), _ptr(ws), ws.numel(), sh)
-    _check(st, "sci_verify")
+    if stabilisers is None:
+        st = library().sci_verify(_ptr(draft), _ptr(target), dt, _ptr(draft_ids), B, K, V, C.byref(pc), _ptr(r_hat),
+                                  _ptr(out.accept_len), _ptr(out.tokens), _ptr(out.jsd), _ptr(out.T),
+                                  _ptr(out.req_status), _ptr(ws), ws.numel(), sh)
+        _check(st, "sci_verify")
+        return out
+    sc = _SciStabC(float(stabilisers.hysteresis), int(stabilisers.min_refresh), 0, float(stabilisers.fallback_acc),
+                   float(stabilisers.fallback_T))
+    st = library().sci_verify_ex(_ptr(draft), _ptr(target), dt, _ptr(draft_ids), B, K, V, C.byref(pc), C.byref(sc),
+                                 _ptr(r_hat), _ptr(state), _ptr(out.accept_len), _ptr(out.tokens), _ptr(out.jsd),
+                                 _ptr(out.T), _ptr(out.req_status), _ptr(ws), ws.numel(), sh)
+    _check(st, "sci_verify_ex")
     return out

@@ -8,6 +8,8 @@
 #include "asv.h"
 #include "asv_internal.h"
 
+static_assert(sizeof(asv_sci_state) == sizeof(asv::SciState), "asv_sci_state layout");
+
 using asv::LaunchPlan;
 
 namespace {
@@ -285,6 +287,15 @@ asv_status sci_verify(const void* draft_logits, const void* target_logits, int d
                       int B, int K, int V, const asv_sci_params* params, double* r_hat, int32_t* out_accept_len,
                       int32_t* out_tokens, float* out_jsd, float* out_T, uint32_t* out_req_status,
                       void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  return sci_verify_ex(draft_logits, target_logits, dtype, draft_ids, B, K, V, params, nullptr, r_hat, nullptr,
+                       out_accept_len, out_tokens, out_jsd, out_T, out_req_status, workspace, ws_bytes, stream);
+}
+
+asv_status sci_verify_ex(const void* draft_logits, const void* target_logits, int dtype, const int32_t* draft_ids,
+                         int B, int K, int V, const asv_sci_params* params, const asv_sci_stabilisers* stab,
+                         double* r_hat, asv_sci_state* state, int32_t* out_accept_len, int32_t* out_tokens,
+                         float* out_jsd, float* out_T, uint32_t* out_req_status, void* workspace, size_t ws_bytes,
+                         cudaStream_t stream) {
   if (B < 0 || K < 1 || V < 2) return ASV_ERR_SHAPE;
   if ((long long)B * (K + 1) * asv::kMaxCluster > 0x7fffffffLL) return ASV_ERR_SHAPE;
   if (!valid_dtype(dtype)) return ASV_ERR_DTYPE;
@@ -303,6 +314,13 @@ asv_status sci_verify(const void* draft_logits, const void* target_logits, int d
   for (double v : vals)
     if (!std::isfinite(v)) return ASV_ERR_PARAM;
   if (P.T_min > P.T_max || P.ewma_beta < 0.0 || P.ewma_beta > 1.0) return ASV_ERR_PARAM;
+  if (stab) {
+    if (!state) return ASV_ERR_NULL;
+    if (!aligned(state, 16)) return ASV_ERR_ALIGN;
+    if (!std::isfinite(stab->hysteresis) || stab->hysteresis < 0.0 || stab->min_refresh < 1 ||
+        !std::isfinite(stab->fallback_acc) || !std::isfinite(stab->fallback_T))
+      return ASV_ERR_PARAM;
+  }
   asv::JsdArgs args;
   std::memset(&args, 0, sizeof(args));
   args.x[0] = draft_logits;
@@ -318,6 +336,13 @@ asv_status sci_verify(const void* draft_logits, const void* target_logits, int d
   args.T_max = P.T_max;
   args.ewma_beta = P.ewma_beta;
   args.r_hat = r_hat;
+  if (stab) {
+    args.sci_state = reinterpret_cast<asv::SciState*>(state);
+    args.hyst = stab->hysteresis;
+    args.min_refresh = stab->min_refresh;
+    args.fb_acc = stab->fallback_acc;
+    args.fb_T = stab->fallback_T;
+  }
   args.out_accept_len = out_accept_len;
   args.out_tokens = out_tokens;
   args.out_D = out_jsd;
@@ -400,6 +425,16 @@ asv_status rapid_verify(const float* z, const float* q, const int32_t* draft_ids
                         float eta, float tail_frac, uint64_t seed, uint32_t offset, int32_t* out_accept_len,
                         int32_t* out_tokens, uint32_t* out_req_status, void* workspace, size_t ws_bytes,
                         cudaStream_t stream) {
+  return rapid_verify_ex(z, q, draft_ids, B, G, V, T, eta, tail_frac, seed, offset, nullptr, out_accept_len,
+                         out_tokens, out_req_status, workspace, ws_bytes, stream);
+}
+
+asv_status rapid_verify_ex(const float* z, const float* q, const int32_t* draft_ids, int B, int G, int V, float T,
+                           float eta, float tail_frac, uint64_t seed, uint32_t offset, const asv_rapid_options* options,
+                           int32_t* out_accept_len, int32_t* out_tokens, uint32_t* out_req_status, void* workspace,
+                           size_t ws_bytes, cudaStream_t stream) {
+  const int tail_mode = options ? options->tail_mode : 0;
+  if (tail_mode != 0 && tail_mode != 1) return ASV_ERR_PARAM;
   if (B < 0 || G < 0 || V < 2) return ASV_ERR_SHAPE;
   if ((long long)B * (G + 1) * asv::kMaxCluster > 0x7fffffffLL) return ASV_ERR_SHAPE;
   if (B == 0) return ASV_OK;
@@ -433,6 +468,7 @@ asv_status rapid_verify(const float* z, const float* q, const int32_t* draft_ids
   a.eta = eta;
   a.tail_frac = tail_frac;
   a.ln_tail_frac = tail_frac > 0.0f ? std::log(tail_frac) : -INFINITY;
+  a.tail_mode = tail_mode;
   a.seed_lo = uint32_t(seed);
   a.seed_hi = uint32_t(seed >> 32);
   a.offset = offset;

@@ -23,14 +23,23 @@ struct __align__(16) RowRecord {
 // last row of a request to finish recomputes for the emitted position.  With zs = z / T:
 //   p_k = ex2(fma(zs_k, log2e, -zs_max*log2e)) * inv_sum, zhat_k = z_k + eta*T*(q_k - p_k),
 //   tail_k <=> zhat_k / T < zhat_max + ln(tail_frac),
-//   protected_k = p_k on the tail, ex2((zhat_k / T - zhat_max) * log2e) * head_scale on the head.
+//   protected_k = p_k * tail_scale on the tail, ex2((zhat_k / T - zhat_max) * log2e) * head_scale on
+//   the head.
 struct __align__(32) RapidRecord {
   float zs_max;
   float inv_sum;
   float zhat_max;   // max of zhat / T
   float head_scale;
   uint32_t bits;
-  uint32_t pad[3];
+  float tail_scale;  // 1, or 1/Z under the alternative tail reading
+  uint32_t pad[2];
+};
+
+// Per-request E2-SCI stabiliser state (layout of asv_sci_state).
+struct __align__(16) SciState {
+  double T_applied;
+  int32_t age;
+  uint32_t flags;  // 1: a threshold has been applied; 2: fallback pending
 };
 
 struct LaunchPlan {
@@ -56,6 +65,10 @@ struct JsdArgs {
   // SCI
   double T_base, alpha_omega, tau_credit, T_min, T_max, ewma_beta;
   double* r_hat;
+  // SCI stabilisers (state == nullptr: off)
+  SciState* sci_state;
+  double hyst, fb_acc, fb_T;
+  int min_refresh;
   // outputs
   int32_t* out_accept_len;
   int32_t* out_tokens;
@@ -76,6 +89,7 @@ struct RapidArgs {
   int n_slice;
   int bulk;
   float T, inv_T, eta, tail_frac, ln_tail_frac;
+  int tail_mode;  // 0: tail keeps p, head rescaled; 1: substitute p on the tail, renormalise all
   uint32_t seed_lo, seed_hi, offset;
   int32_t* out_accept_len;
   int32_t* out_tokens;

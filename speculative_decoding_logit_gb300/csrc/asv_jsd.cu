@@ -669,10 +669,26 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
   // Last row of this request: the left-to-right scan, 32 records per step.
   (void)ld_acquire_gpu(&p.tickets[req]);  // every lane acquires the other rows' records
   RowRecord* recs = p.records + size_t(req) * R1;
+  // SCI threshold (double, each operation rounded once as written), then the stabilisers.
   double thr = 0.0;
+  int32_t new_age = 0;
   if (MODE == kModeSci) {
-    thr = p.T_base + p.alpha_omega * (p.r_hat[req] - p.tau_credit);
+    thr = __dadd_rn(p.T_base, __dmul_rn(p.alpha_omega, __dsub_rn(p.r_hat[req], p.tau_credit)));
     thr = fmax(p.T_min, fmin(thr, p.T_max));
+    if (p.sci_state) {
+      const SciState st = p.sci_state[req];
+      if (!(st.flags & 1u)) {
+        new_age = 1;
+      } else if (st.flags & 2u) {
+        thr = p.fb_T;
+        new_age = 1;
+      } else if (st.age >= p.min_refresh && fabs(__dsub_rn(thr, st.T_applied)) > p.hyst) {
+        new_age = 1;
+      } else {
+        thr = st.T_applied;
+        new_age = st.age + 1;
+      }
+    }
   }
   uint32_t any = 0;
   int n = K;      // accepted prefix
@@ -707,7 +723,17 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
   if (lane == 0) {
     if (MODE == kModeSci) {
       if (p.out_T) p.out_T[req] = float(thr);
-      if (!status) p.r_hat[req] = (1.0 - p.ewma_beta) * p.r_hat[req] + p.ewma_beta * (double(n) / double(K));
+      if (!status) {
+        const double pacc = __ddiv_rn(double(n), double(K));
+        p.r_hat[req] = __dadd_rn(__dmul_rn(__dsub_rn(1.0, p.ewma_beta), p.r_hat[req]), __dmul_rn(p.ewma_beta, pacc));
+        if (p.sci_state) {
+          SciState st;
+          st.T_applied = thr;
+          st.age = new_age;
+          st.flags = 1u | (pacc < p.fb_acc ? 2u : 0u);
+          p.sci_state[req] = st;
+        }
+      }
     }
     p.out_accept_len[req] = status ? 0 : n;
     p.out_req_status[req] = status;

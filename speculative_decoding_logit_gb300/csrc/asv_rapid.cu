@@ -13,7 +13,10 @@
 //   3. max of zhat/T;  4. head sums: sum of p and of exp(zhat/T - max) over entries at or above
 //      the tail boundary zhat/T >= max + ln(tail_frac).
 // The protected target is then p on the tail and exp(zhat/T - max) * (head p-mass / head
-// exp-mass) on the head, which sums to 1 without a further normalisation pass.  CTA 0 of the row
+// exp-mass) on the head, which sums to 1 without a further normalisation pass.  The alternative
+// reading of the protection (tail_mode 1: substitute p for phat on the tail, then renormalise
+// every entry) also sums p over the tail and exp(zhat/T - max) over every entry in sweep 4; then
+// the tail is p / Z and the head phat / Z with Z = (tail p-mass) + (head phat-mass).  CTA 0 of the row
 // decides the draft's accept test u*q(d) < protected(d) (u from Philox4x32-10) and files a row
 // record.  The last row of a request to finish runs the scan and, in the same cluster, draws the
 // emitted token at the stop position with an exponential race over that row (re-read from global
@@ -42,11 +45,13 @@ struct __align__(16) RapidXchg {
   float d_inv_sum;
   float d_zhat_max;
   float d_head_scale;
-  uint32_t pad;
+  float d_tail_scale;
+  float tail_p[2];  // tail_mode 1: sum of p over the tail
+  float all_e[2];   // tail_mode 1: sum of exp(zhat/T - max) over every entry
 };
 
 struct RowConsts {
-  float invT, etaT, ML, inv_sum, zhmax, thr, head_scale;
+  float invT, etaT, ML, inv_sum, zhmax, thr, head_scale, tail_scale;
 };
 
 // Row statistics broadcast by one thread after each cluster exchange.
@@ -69,7 +74,7 @@ __device__ __forceinline__ void rapid_entry(float z, float q, const RowConsts& c
   p = ex2_approx(fmaf(zs, kLog2e, -c.ML)) * c.inv_sum;
   const float zh = fmaf(c.etaT, q - p, z);
   zhs = zh * c.invT;
-  prot = (zhs < c.thr) ? p : ex2_approx((zhs - c.zhmax) * kLog2e) * c.head_scale;
+  prot = (zhs < c.thr) ? p * c.tail_scale : ex2_approx((zhs - c.zhmax) * kLog2e) * c.head_scale;
 }
 
 __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
@@ -240,6 +245,7 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
   rc.zhmax = 0.f;
   rc.thr = 0.f;
   rc.head_scale = 0.f;
+  rc.tail_scale = 1.0f;
 
   // ---------------------------------------------------------------- sweep 3: max of zhat/T
   {
@@ -273,7 +279,7 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
 
   // ---------------------------------------------------------------- sweep 4: head sums
   {
-    float hp0 = 0.f, he0 = 0.f;
+    float hp0 = 0.f, he0 = 0.f, tp0 = 0.f, ae0 = 0.f;
     if (finite) {
       for (int vi = tid; vi < nvec; vi += nthr) {
         const float4 z4 = reinterpret_cast<const float4*>(zst)[vi];
@@ -284,24 +290,40 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
         for (int e = 0; e < 4; ++e) {
           const float pk = ex2_approx(fmaf(zz[e] * invT, kLog2e, -rc.ML)) * rc.inv_sum;
           const float zhs = fmaf(rc.etaT, qq[e] - pk, zz[e]) * invT;
-          if (zhs >= rc.thr) {
-            hp0 += pk;
-            he0 += ex2_approx((zhs - rc.zhmax) * kLog2e);
+          if (p.tail_mode == 0) {
+            if (zhs >= rc.thr) {
+              hp0 += pk;
+              he0 += ex2_approx((zhs - rc.zhmax) * kLog2e);
+            }
+          } else {
+            const float ek = ex2_approx((zhs - rc.zhmax) * kLog2e);
+            ae0 += ek;
+            if (zhs >= rc.thr) {
+              hp0 += pk;
+              he0 += ek;
+            } else {
+              tp0 += pk;
+            }
           }
         }
       }
     }
     block_sum2(hp0, he0, xchg.head_p, xchg.head_e);
+    if (p.tail_mode != 0) block_sum2(tp0, ae0, xchg.tail_p, xchg.all_e);
     if (tid == 0) xchg.err = s_err;
   }
   cluster_sync();  // #4
 
   // ---------------------------------------------------------------- row finalisation (CTA 0)
-  DF Hp{0.0f, 0.0f}, He{0.0f, 0.0f};
+  DF Hp{0.0f, 0.0f}, He{0.0f, 0.0f}, Tp{0.0f, 0.0f}, Ae{0.0f, 0.0f};
   uint32_t err = 0;
   if (rank == 0 && warp == 0) {
     Hp = cluster_sum(xchg.head_p);
     He = cluster_sum(xchg.head_e);
+    if (p.tail_mode != 0) {
+      Tp = cluster_sum(xchg.tail_p);
+      Ae = cluster_sum(xchg.all_e);
+    }
     uint32_t e = (lane < int(C)) ? dsmem_ld_u32(dsmem_map(smem_addr(&xchg.err), uint32_t(lane))) : 0u;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) e |= __shfl_xor_sync(0xffffffffu, e, o);
@@ -309,7 +331,18 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
   }
   if (rank == 0 && tid == 0) {
     const float he = He.hi + He.lo;
-    rc.head_scale = (he > 0.0f) ? (Hp.hi + Hp.lo) / he : 0.0f;
+    if (p.tail_mode == 0) {
+      rc.head_scale = (he > 0.0f) ? (Hp.hi + Hp.lo) / he : 0.0f;
+      rc.tail_scale = 1.0f;
+    } else {
+      // Z = tail p-mass + head phat-mass, phat = exp(zhat/T - max) / Ae:
+      // tail p / Z, head exp(zhat/T - max) / (Ae Z) = exp(..) / (Ae Tp + He).
+      const float tp = Tp.hi + Tp.lo, ae = Ae.hi + Ae.lo;
+      const float z = tp + (ae > 0.0f ? he / ae : 0.0f);
+      rc.tail_scale = (z > 0.0f) ? 1.0f / z : 0.0f;
+      const float den = fmaf(ae, tp, he);
+      rc.head_scale = (den > 0.0f) ? 1.0f / den : 0.0f;
+    }
     uint32_t bits = 0;
     if (!finite) bits |= kBitNonfinite;
     if (err) bits |= kBitTimeout;
@@ -334,8 +367,9 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
     rec.inv_sum = rc.inv_sum;
     rec.zhat_max = rc.zhmax;
     rec.head_scale = rc.head_scale;
+    rec.tail_scale = rc.tail_scale;
     rec.bits = bits;
-    rec.pad[0] = rec.pad[1] = rec.pad[2] = 0;
+    rec.pad[0] = rec.pad[1] = 0;
     p.records[row] = rec;
     __threadfence();
     const uint32_t ticket = atomicAdd(&p.tickets[req], 1u);
@@ -361,6 +395,7 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
             break;
           }
         const float f0 = recs[n].zs_max, f1 = recs[n].inv_sum, f2 = recs[n].zhat_max, f3 = recs[n].head_scale;
+        const float f4 = recs[n].tail_scale;
         for (int i = 0; i < R1; ++i) p.records[size_t(req) * R1 + i] = RapidRecord{};
         for (uint32_t q = 0; q < C; ++q) {
           dsmem_st_u32(dsmem_map(smem_addr(&xchg.draw_row), q), uint32_t(n));
@@ -368,6 +403,7 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
           dsmem_st_u32(dsmem_map(smem_addr(&xchg.d_inv_sum), q), __float_as_uint(f1));
           dsmem_st_u32(dsmem_map(smem_addr(&xchg.d_zhat_max), q), __float_as_uint(f2));
           dsmem_st_u32(dsmem_map(smem_addr(&xchg.d_head_scale), q), __float_as_uint(f3));
+          dsmem_st_u32(dsmem_map(smem_addr(&xchg.d_tail_scale), q), __float_as_uint(f4));
           dsmem_st_u32(dsmem_map(smem_addr(&xchg.draw_active), q), 1u);
         }
       }
@@ -387,6 +423,7 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
     dc.zhmax = xchg.d_zhat_max;
     dc.thr = xchg.d_zhat_max + p.ln_tail_frac;
     dc.head_scale = xchg.d_head_scale;
+    dc.tail_scale = xchg.d_tail_scale;
     const size_t nbase = (size_t(req) * R1 + n) * size_t(V);
     int winner = INT_MAX;
     for (int pass = 0; pass < 2 && winner == INT_MAX; ++pass) {

@@ -21,10 +21,11 @@ def asv():
     return m
 
 
-def _run(asv, z, q, d, T, eta, tail, seed, offset=0):
+def _run(asv, z, q, d, T, eta, tail, seed, offset=0, tail_mode=0):
     out = asv.rapid_verify(torch.from_numpy(np.ascontiguousarray(z)).cuda(),
                            torch.from_numpy(np.ascontiguousarray(q)).cuda(),
-                           torch.from_numpy(np.ascontiguousarray(d)).cuda(), T, eta, tail, seed, offset)
+                           torch.from_numpy(np.ascontiguousarray(d)).cuda(), T, eta, tail, seed, offset,
+                           tail_mode=tail_mode)
     torch.cuda.synchronize()
     return out
 
@@ -77,6 +78,33 @@ def test_rapid_b32_g10_v128256_full(asv):
         tot += g
         assert f <= 2
     assert tot >= 4 * 30
+
+
+@pytest.mark.parametrize("eta", [40.0, 50.0])
+def test_upward_speculation_eta(asv, eta):
+    """The page's upward-speculation setting (a larger drafter guiding a smaller target): eta 40, 50."""
+    w = gen.WORKLOADS["rapid_b32_g10_v128256_f32"]
+    b = gen.make_rapid_batch(w.seed + int(eta), 16, w.K, w.V)
+    out = _run(asv, b.z, b.q, b.drafts, 1.0, eta, 0.1, w.params["philox_seed"])
+    ref = oracle.rapid_verify(b.z, b.q, b.drafts, 1.0, eta, 0.1, w.params["philox_seed"])
+    g, f = _compare(out, ref)
+    assert g >= 12
+
+
+@pytest.mark.parametrize("V,G", [(17, 2), (1000, 4), (4096, 10)])
+def test_renormalised_tail_reading(asv, V, G):
+    """tail_mode 1 (p substitutes phat on the tail, then every entry is renormalised) against the
+    oracle's reading of the same; at eta > 0 it differs from the default reading."""
+    b = gen.make_rapid_batch(500 + V, 24, G, V)
+    differs = 0
+    for eta in (0.0, 10.0, 40.0):
+        out = _run(asv, b.z, b.q, b.drafts, 1.0, eta, 0.1, 4321, tail_mode=asv.TAIL_RENORMALISE_ALL)
+        ref = oracle.rapid_verify(b.z, b.q, b.drafts, 1.0, eta, 0.1, 4321, tail_mode=1)
+        g, f = _compare(out, ref)
+        assert g >= 20
+        ref0 = oracle.rapid_verify(b.z, b.q, b.drafts, 1.0, eta, 0.1, 4321, tail_mode=0)
+        differs += int((ref.tokens != ref0.tokens).any())
+    assert differs >= 1
 
 
 def test_eta_zero_first_token_is_target_distributed(asv):

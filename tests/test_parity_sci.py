@@ -79,3 +79,34 @@ def test_five_windows_carry_state(asv):
         out, r_gpu, ref = _window(asv, batch, r)
         _compare(out, r_gpu, ref, w.dtype)
         r = ref.r_hat
+
+
+def test_stabilised_windows(asv):
+    """Six windows with hysteresis, a refresh interval of 2 and a fallback, state on the device."""
+    B, K, V = 24, 4, 4096
+    stab = asv.SciStabilisers(hysteresis=0.01, min_refresh=2, fallback_acc=0.5, fallback_T=0.12)
+    ostab = oracle.SciStabilisers(0.01, 2, 0.5, 0.12)
+    p = asv.SciParams(alpha_omega=0.5)
+    op = oracle.SciParams(p.T_base, p.alpha_omega, p.tau_credit, p.T_min, p.T_max, p.ewma_beta)
+    state = asv.sci_state_new(B)
+    ostate = oracle.sci_state(B)
+    rng = np.random.default_rng(31)
+    r_ref = rng.uniform(0.2, 1.0, B)
+    r_gpu = torch.from_numpy(r_ref.copy()).cuda()
+    applied_fallback = 0
+    for win in range(6):
+        batch = gen.make_asymspec_batch("spiky", 4000 + win, B, K, V, gen.F32)
+        out = asv.sci_verify(to_device(batch.a, batch.dtype), to_device(batch.t, batch.dtype),
+                             torch.from_numpy(batch.drafts).cuda(), r_gpu, p, stabilisers=stab, state=state)
+        torch.cuda.synchronize()
+        ref = oracle.sci_verify(batch.a, batch.t, batch.drafts, r_ref, op, stab=ostab, state=ostate)
+        _compare(out, r_gpu.cpu().numpy(), ref, gen.F32)
+        T_app, age, flags = asv.sci_state_decode(state)
+        for r in range(B):
+            if ref.flags[r] & oracle.FLAGS_UNGRADED:
+                continue
+            assert T_app[r].item() == pytest.approx(ostate[r].T_applied, abs=1e-15)
+            assert age[r].item() == ostate[r].age and flags[r].item() == ostate[r].flags
+        applied_fallback += int(np.isclose(ref.T, 0.12).sum())
+        r_ref = ref.r_hat
+    assert applied_fallback > 0  # the fallback path ran
