@@ -63,7 +63,13 @@ typedef enum {
 
 typedef enum { ASV_F32 = 0, ASV_BF16 = 1 } asv_dtype;
 
-typedef enum { ASV_MODE_ASYMSPEC = 0, ASV_MODE_RAPID = 1, ASV_MODE_SCI = 2 } asv_mode;
+typedef enum {
+  ASV_MODE_ASYMSPEC = 0,
+  ASV_MODE_RAPID = 1,
+  ASV_MODE_SCI = 2,
+  ASV_MODE_SWEEP = 3,        /* asymspec_verify_sweep */
+  ASV_MODE_ASYMSPEC_SCI = 4  /* asymspec_sci_verify */
+} asv_mode;
 
 /* Per-request status bits written by the kernels (never a trap). */
 #define ASV_REQ_NONFINITE 1u /* a row holds NaN or +inf, or is entirely -inf */
@@ -142,6 +148,26 @@ asv_status asymspec_verify_ex(const void* a, const void* b, const void* t, int d
                               int B, int K, int V, float beta, float gamma, const asv_asym_options* options,
                               int32_t* out_accept_len, int32_t* out_tokens, float* out_D, float* out_lse,
                               uint32_t* out_req_status, void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * asymspec_verify_sweep -- AsymSpec for every (beta, gamma) of a grid from one read of a, b, t.
+ * [ASYM] sec. 5 sweeps beta and gamma over a flat region; D and the log-sum-exps do not depend on
+ * them, the emitted token depends on beta only and the gate on gamma only, so one pass over the
+ * inputs serves the whole grid.  betas [n_beta] (1..ASV_SWEEP_MAX_BETA, finite) and gammas
+ * [n_gamma] (1..ASV_SWEEP_MAX_GAMMA, > 0) are HOST arrays.  For grid point (beta_i, gamma_j) the
+ * results equal asymspec_verify(..., beta_i, gamma_j, ...):
+ *   out_accept_len [n_gamma, B]        (the accepted prefix depends on gamma only)
+ *   out_tokens     [n_beta, n_gamma, B, K+1]
+ *   out_D [B, K+1], out_lse [B, K+1, 3] (may be NULL), out_req_status [B].
+ * The workspace is asv_workspace_bytes(ASV_MODE_SWEEP, ...).
+ */
+#define ASV_SWEEP_MAX_BETA 4
+#define ASV_SWEEP_MAX_GAMMA 8
+asv_status asymspec_verify_sweep(const void* a, const void* b, const void* t, int dtype, const int32_t* draft_ids,
+                                 int B, int K, int V, const float* betas, int n_beta, const float* gammas,
+                                 int n_gamma, int32_t* out_accept_len, int32_t* out_tokens, float* out_D,
+                                 float* out_lse, uint32_t* out_req_status, void* workspace, size_t ws_bytes,
+                                 cudaStream_t stream);
 
 /*
  * asymspec_verify_host -- asymspec_verify over HOST buffers, for callers whose
@@ -293,6 +319,23 @@ asv_status sci_verify_ex(const void* draft_logits, const void* target_logits, in
                          double* r_hat, asv_sci_state* state, int32_t* out_accept_len, int32_t* out_tokens,
                          float* out_jsd, float* out_T, uint32_t* out_req_status, void* workspace, size_t ws_bytes,
                          cudaStream_t stream);
+
+/*
+ * asymspec_sci_verify -- AsymSpec and one E2-SCI window on the same tensors from one read.
+ * E2-SCI takes draft = a and target = t; its divergence JSD(a || t) is summed in the same pass
+ * as D = JSD(a || b).  The AsymSpec outputs equal asymspec_verify(a, b, t, ..., beta, gamma);
+ * the SCI outputs equal sci_verify(a, t, ..., params, r_hat) (r_hat updated in place):
+ * out_sci_accept_len [B], out_sci_tokens [B, K+1], out_jsd [B, K+1] (may be NULL), out_T [B]
+ * (may be NULL).  out_req_status [B] is shared (a flagged request gets accept length 0 and
+ * tokens -1 in both modes and keeps its r_hat).  K >= 1.  The workspace is
+ * asv_workspace_bytes(ASV_MODE_ASYMSPEC_SCI, ...).
+ */
+asv_status asymspec_sci_verify(const void* a, const void* b, const void* t, int dtype, const int32_t* draft_ids,
+                               int B, int K, int V, float beta, float gamma, const asv_sci_params* params,
+                               double* r_hat, int32_t* out_accept_len, int32_t* out_tokens, float* out_D,
+                               float* out_lse, int32_t* out_sci_accept_len, int32_t* out_sci_tokens, float* out_jsd,
+                               float* out_T, uint32_t* out_req_status, void* workspace, size_t ws_bytes,
+                               cudaStream_t stream);
 
 #ifdef __cplusplus
 }

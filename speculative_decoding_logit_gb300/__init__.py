@@ -26,6 +26,12 @@ from ._binding import (  # noqa: F401
     ASV_MODE_ASYMSPEC,
     ASV_MODE_RAPID,
     ASV_MODE_SCI,
+    ASV_MODE_SWEEP,
+    ASV_MODE_ASYMSPEC_SCI,
+    AsymSciOutput,
+    SweepOutput,
+    asymspec_sci_verify,
+    asymspec_verify_sweep,
     REQ_BAD_DRAFT,
     REQ_NONFINITE,
     REQ_TIMEOUT,

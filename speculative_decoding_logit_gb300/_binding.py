@@ -108,6 +108,12 @@ def _declare(L):
     L.sci_verify.argtypes = [_vp, _vp, _i, _vp, _i, _i, _i, C.POINTER(_SciParamsC), _vp, _vp, _vp, _vp, _vp, _vp,
                              _vp, _sz, _vp]
     L.sci_verify.restype = _i
+    L.asymspec_verify_sweep.argtypes = [_vp, _vp, _vp, _i, _vp, _i, _i, _i, C.POINTER(_f), _i, C.POINTER(_f), _i,
+                                        _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+    L.asymspec_verify_sweep.restype = _i
+    L.asymspec_sci_verify.argtypes = [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _f, _f, C.POINTER(_SciParamsC), _vp, _vp,
+                                      _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+    L.asymspec_sci_verify.restype = _i
     L.rapid_verify_ex.argtypes = [_vp, _vp, _vp, _i, _i, _i, _f, _f, _f, C.c_uint64, C.c_uint32,
                                   C.POINTER(_RapidOptionsC), _vp, _vp, _vp, _vp, _sz, _vp]
     L.rapid_verify_ex.restype = _i
@@ -241,6 +247,99 @@ def asymspec_verify(a: torch.Tensor, b: torch.Tensor, t: torch.Tensor, draft_ids
 
 def host_arena_bytes(B: int, K: int, V: int, dtype: int) -> int:
     return int(library().asv_host_arena_bytes(B, K, V, dtype))
+
+
+ASV_MODE_SWEEP = 3
+ASV_MODE_ASYMSPEC_SCI = 4
+
+
+@dataclass
+class SweepOutput:
+    accept_len: torch.Tensor  # [n_gamma, B] int32
+    tokens: torch.Tensor      # [n_beta, n_gamma, B, K+1] int32
+    D: torch.Tensor           # [B, K+1] float32
+    lse: torch.Tensor         # [B, K+1, 3] float32
+    req_status: torch.Tensor  # [B] int32
+
+
+def _check_asym_inputs(a, b, t, draft_ids):
+    _need_cuda(a, b, t, draft_ids)
+    if a.dim() != 3 or a.shape != b.shape or a.shape != t.shape:
+        raise AsvError(2, "a, b, t must share one [B, K+1, V] shape")
+    if a.dtype != b.dtype or a.dtype != t.dtype:
+        raise AsvError(4, "a, b, t must share one dtype")
+    B, R1, V = a.shape
+    if draft_ids.dtype != torch.int32 or tuple(draft_ids.shape) != (B, R1 - 1):
+        raise AsvError(2, "draft_ids must be int32 [B, K]")
+    for n, x in (("a", a), ("b", b), ("t", t), ("draft_ids", draft_ids)):
+        _contig(x, n)
+    return B, R1 - 1, V
+
+
+def asymspec_verify_sweep(a: torch.Tensor, b: torch.Tensor, t: torch.Tensor, draft_ids: torch.Tensor, betas,
+                          gammas, *, workspace: Optional[torch.Tensor] = None, stream=None) -> SweepOutput:
+    """AsymSpec for every (beta, gamma) of a grid from one read of a, b, t (asymspec_verify_sweep)."""
+    B, K, V = _check_asym_inputs(a, b, t, draft_ids)
+    betas = [float(x) for x in betas]
+    gammas = [float(x) for x in gammas]
+    nb, ng = len(betas), len(gammas)
+    dev = a.device
+    sh = _stream_handle(dev, stream)
+    out = SweepOutput(torch.empty(ng, B, dtype=torch.int32, device=dev),
+                      torch.empty(nb, ng, B, K + 1, dtype=torch.int32, device=dev),
+                      torch.empty(B, K + 1, dtype=torch.float32, device=dev),
+                      torch.empty(B, K + 1, 3, dtype=torch.float32, device=dev),
+                      torch.empty(B, dtype=torch.int32, device=dev))
+    dt = _dtype_code(a)
+    ws = workspace if workspace is not None else _workspace(dev, sh, workspace_bytes(ASV_MODE_SWEEP, B, K, V, dt))
+    bb = (_f * max(nb, 1))(*betas)
+    gg = (_f * max(ng, 1))(*gammas)
+    st = library().asymspec_verify_sweep(_ptr(a), _ptr(b), _ptr(t), dt, _ptr(draft_ids), B, K, V, bb, nb, gg, ng,
+                                         _ptr(out.accept_len), _ptr(out.tokens), _ptr(out.D), _ptr(out.lse),
+                                         _ptr(out.req_status), _ptr(ws), ws.numel(), sh)
+    _check(st, "asymspec_verify_sweep")
+    return out
+
+
+@dataclass
+class AsymSciOutput:
+    accept_len: torch.Tensor      # AsymSpec [B]
+    tokens: torch.Tensor          # AsymSpec [B, K+1]
+    D: torch.Tensor               # JSD(a || b) [B, K+1]
+    lse: torch.Tensor             # [B, K+1, 3]
+    sci_accept_len: torch.Tensor  # E2-SCI [B]
+    sci_tokens: torch.Tensor      # E2-SCI [B, K+1]
+    jsd: torch.Tensor             # JSD(a || t) [B, K+1]
+    T: torch.Tensor               # E2-SCI threshold [B]
+    req_status: torch.Tensor      # [B]
+
+
+def asymspec_sci_verify(a: torch.Tensor, b: torch.Tensor, t: torch.Tensor, draft_ids: torch.Tensor, beta: float,
+                        gamma: float, r_hat: torch.Tensor, params: "SciParams" = None, *,
+                        workspace: Optional[torch.Tensor] = None, stream=None) -> AsymSciOutput:
+    """AsymSpec and one E2-SCI window (draft = a, target = t) from one read (asymspec_sci_verify);
+    r_hat (float64 [B], device) is updated in place."""
+    B, K, V = _check_asym_inputs(a, b, t, draft_ids)
+    if r_hat.dtype != torch.float64 or tuple(r_hat.shape) != (B,) or not r_hat.is_cuda:
+        raise AsvError(2, "r_hat must be a float64 [B] CUDA tensor")
+    params = params or SciParams()
+    dev = a.device
+    sh = _stream_handle(dev, stream)
+    i32 = lambda *sh_: torch.empty(*sh_, dtype=torch.int32, device=dev)
+    f32 = lambda *sh_: torch.empty(*sh_, dtype=torch.float32, device=dev)
+    out = AsymSciOutput(i32(B), i32(B, K + 1), f32(B, K + 1), f32(B, K + 1, 3), i32(B), i32(B, K + 1),
+                        f32(B, K + 1), f32(B), i32(B))
+    dt = _dtype_code(a)
+    ws = workspace if workspace is not None else _workspace(dev, sh,
+                                                            workspace_bytes(ASV_MODE_ASYMSPEC_SCI, B, K, V, dt))
+    pc = _SciParamsC(params.T_base, params.alpha_omega, params.tau_credit, params.T_min, params.T_max,
+                     params.ewma_beta)
+    st = library().asymspec_sci_verify(_ptr(a), _ptr(b), _ptr(t), dt, _ptr(draft_ids), B, K, V, float(beta),
+                                       float(gamma), C.byref(pc), _ptr(r_hat), _ptr(out.accept_len), _ptr(out.tokens),
+                                       _ptr(out.D), _ptr(out.lse), _ptr(out.sci_accept_len), _ptr(out.sci_tokens),
+                                       _ptr(out.jsd), _ptr(out.T), _ptr(out.req_status), _ptr(ws), ws.numel(), sh)
+    _check(st, "asymspec_sci_verify")
+    return out
 
 
 def asymspec_verify_host(a, b, t, draft_ids, beta, gamma, arena: torch.Tensor, out_accept_len, out_tokens, out_D,

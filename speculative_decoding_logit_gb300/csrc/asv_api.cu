@@ -60,7 +60,9 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 size_t tickets_bytes(int B) { return round_up(size_t(B) * 4, 256); }
 
 size_t record_bytes(int mode) {
-  return mode == ASV_MODE_RAPID ? sizeof(asv::RapidRecord) : sizeof(asv::RowRecord);
+  if (mode == ASV_MODE_RAPID) return sizeof(asv::RapidRecord);
+  if (mode == ASV_MODE_SWEEP || mode == ASV_MODE_ASYMSPEC_SCI) return sizeof(asv::MultiRecord);
+  return sizeof(asv::RowRecord);
 }
 
 // Launch plan.  Each CTA stages NT slices of n_slice entries.  Choose the smallest cluster
@@ -218,7 +220,9 @@ asv_status asv_query_plan(int mode, int B, int K, int V, int dtype, int* cluster
 
 static asv_status run_jsd(int mode, asv::JsdArgs& a, int dtype, void* workspace, size_t ws_bytes,
                           cudaStream_t stream) {
-  const int amode = mode == asv::kModeAsym ? ASV_MODE_ASYMSPEC : ASV_MODE_SCI;
+  int amode = mode == asv::kModeAsym ? ASV_MODE_ASYMSPEC : ASV_MODE_SCI;
+  if (a.variant == 1) amode = ASV_MODE_SWEEP;
+  if (a.variant == 2) amode = ASV_MODE_ASYMSPEC_SCI;
   if (ws_bytes < asv_workspace_bytes(amode, a.B, a.K, a.V, dtype)) return ASV_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return ASV_ERR_ALIGN;
   const int eb = elem_size(dtype);
@@ -233,6 +237,7 @@ static asv_status run_jsd(int mode, asv::JsdArgs& a, int dtype, void* workspace,
   a.bulk = pl.bulk;
   a.tickets = reinterpret_cast<uint32_t*>(workspace);
   a.records = reinterpret_cast<asv::RowRecord*>(static_cast<char*>(workspace) + tickets_bytes(a.B));
+  a.mrecords = reinterpret_cast<asv::MultiRecord*>(static_cast<char*>(workspace) + tickets_bytes(a.B));
   e = asv::launch_jsd_family(mode, dtype, a, pl, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   return ASV_OK;
@@ -272,7 +277,8 @@ asv_status asymspec_verify_ex(const void* a, const void* b, const void* t, int d
   args.B = B;
   args.K = K;
   args.V = V;
-  args.beta = beta;
+  args.betas[0] = beta;
+  args.n_beta = 1;
   args.delta_source = dsrc;
   args.ln_gamma = std::log(double(gamma));
   args.out_accept_len = out_accept_len;
@@ -349,6 +355,118 @@ asv_status sci_verify_ex(const void* draft_logits, const void* target_logits, in
   args.out_T = out_T;
   args.out_req_status = out_req_status;
   return run_jsd(asv::kModeSci, args, dtype, workspace, ws_bytes, stream);
+}
+
+// Shared checks of the AsymSpec-family entry points over three [B, K+1, V] inputs.
+static asv_status check_asym_inputs(const void* a, const void* b, const void* t, int dtype, const int32_t* draft_ids,
+                                    int B, int K, int V) {
+  if (B < 0 || K < 0 || V < 2) return ASV_ERR_SHAPE;
+  if ((long long)B * (K + 1) * asv::kMaxCluster > 0x7fffffffLL) return ASV_ERR_SHAPE;
+  if (!valid_dtype(dtype)) return ASV_ERR_DTYPE;
+  if (B == 0) return ASV_OK;
+  if (!a || !b || !t || (K > 0 && !draft_ids)) return ASV_ERR_NULL;
+  const size_t eb = size_t(elem_size(dtype));
+  if (!aligned(a, eb) || !aligned(b, eb) || !aligned(t, eb) || !aligned(draft_ids, 4)) return ASV_ERR_ALIGN;
+  return ASV_OK;
+}
+
+asv_status asymspec_verify_sweep(const void* a, const void* b, const void* t, int dtype, const int32_t* draft_ids,
+                                 int B, int K, int V, const float* betas, int n_beta, const float* gammas,
+                                 int n_gamma, int32_t* out_accept_len, int32_t* out_tokens, float* out_D,
+                                 float* out_lse, uint32_t* out_req_status, void* workspace, size_t ws_bytes,
+                                 cudaStream_t stream) {
+  asv_status st = check_asym_inputs(a, b, t, dtype, draft_ids, B, K, V);
+  if (st != ASV_OK || B == 0) return st;
+  if (!betas || !gammas || !out_accept_len || !out_tokens || !out_req_status) return ASV_ERR_NULL;
+  if (!workspace) return ASV_ERR_WORKSPACE;
+  if (n_beta < 1 || n_beta > ASV_SWEEP_MAX_BETA || n_gamma < 1 || n_gamma > ASV_SWEEP_MAX_GAMMA) return ASV_ERR_PARAM;
+  if (!aligned(out_accept_len, 4) || !aligned(out_tokens, 4) || !aligned(out_req_status, 4) || !aligned(out_D, 4) ||
+      !aligned(out_lse, 4))
+    return ASV_ERR_ALIGN;
+  asv::JsdArgs args;
+  std::memset(&args, 0, sizeof(args));
+  for (int i = 0; i < 4; ++i) {
+    const float be = betas[i < n_beta ? i : 0];
+    if (!std::isfinite(be)) return ASV_ERR_PARAM;
+    args.betas[i] = be;
+  }
+  for (int g = 0; g < n_gamma; ++g) {
+    if (!std::isfinite(gammas[g]) || !(gammas[g] > 0.0f)) return ASV_ERR_PARAM;
+    args.ln_gammas[g] = std::log(double(gammas[g]));
+  }
+  args.variant = 1;
+  args.n_beta = n_beta;
+  args.n_gamma = n_gamma;
+  args.x[0] = a;
+  args.x[1] = b;
+  args.x[2] = t;
+  args.draft_ids = draft_ids;
+  args.B = B;
+  args.K = K;
+  args.V = V;
+  args.out_accept_len = out_accept_len;
+  args.out_tokens = out_tokens;
+  args.out_D = out_D;
+  args.out_lse = out_lse;
+  args.out_req_status = out_req_status;
+  return run_jsd(asv::kModeAsym, args, dtype, workspace, ws_bytes, stream);
+}
+
+asv_status asymspec_sci_verify(const void* a, const void* b, const void* t, int dtype, const int32_t* draft_ids,
+                               int B, int K, int V, float beta, float gamma, const asv_sci_params* params,
+                               double* r_hat, int32_t* out_accept_len, int32_t* out_tokens, float* out_D,
+                               float* out_lse, int32_t* out_sci_accept_len, int32_t* out_sci_tokens, float* out_jsd,
+                               float* out_T, uint32_t* out_req_status, void* workspace, size_t ws_bytes,
+                               cudaStream_t stream) {
+  if (K < 1 && B > 0) return ASV_ERR_SHAPE;
+  asv_status st = check_asym_inputs(a, b, t, dtype, draft_ids, B, K, V);
+  if (st != ASV_OK || B == 0) return st;
+  if (!params || !r_hat || !out_accept_len || !out_tokens || !out_sci_accept_len || !out_sci_tokens ||
+      !out_req_status)
+    return ASV_ERR_NULL;
+  if (!workspace) return ASV_ERR_WORKSPACE;
+  if (!aligned(r_hat, 8) || !aligned(out_accept_len, 4) || !aligned(out_tokens, 4) || !aligned(out_D, 4) ||
+      !aligned(out_lse, 4) || !aligned(out_sci_accept_len, 4) || !aligned(out_sci_tokens, 4) ||
+      !aligned(out_jsd, 4) || !aligned(out_T, 4) || !aligned(out_req_status, 4))
+    return ASV_ERR_ALIGN;
+  if (!std::isfinite(beta) || !std::isfinite(gamma) || !(gamma > 0.0f)) return ASV_ERR_PARAM;
+  const asv_sci_params& P = *params;
+  const double vals[6] = {P.T_base, P.alpha_omega, P.tau_credit, P.T_min, P.T_max, P.ewma_beta};
+  for (double v : vals)
+    if (!std::isfinite(v)) return ASV_ERR_PARAM;
+  if (P.T_min > P.T_max || P.ewma_beta < 0.0 || P.ewma_beta > 1.0) return ASV_ERR_PARAM;
+  asv::JsdArgs args;
+  std::memset(&args, 0, sizeof(args));
+  args.variant = 2;
+  args.betas[0] = args.betas[1] = args.betas[2] = args.betas[3] = beta;
+  args.n_beta = 1;
+  args.ln_gamma = std::log(double(gamma));
+  args.ln_gammas[0] = args.ln_gamma;
+  args.n_gamma = 1;
+  args.x[0] = a;
+  args.x[1] = b;
+  args.x[2] = t;
+  args.draft_ids = draft_ids;
+  args.B = B;
+  args.K = K;
+  args.V = V;
+  args.T_base = P.T_base;
+  args.alpha_omega = P.alpha_omega;
+  args.tau_credit = P.tau_credit;
+  args.T_min = P.T_min;
+  args.T_max = P.T_max;
+  args.ewma_beta = P.ewma_beta;
+  args.r_hat = r_hat;
+  args.out_accept_len = out_accept_len;
+  args.out_tokens = out_tokens;
+  args.out_D = out_D;
+  args.out_lse = out_lse;
+  args.out_J = out_jsd;
+  args.out_sci_accept_len = out_sci_accept_len;
+  args.out_sci_tokens = out_sci_tokens;
+  args.out_T = out_T;
+  args.out_req_status = out_req_status;
+  return run_jsd(asv::kModeAsym, args, dtype, workspace, ws_bytes, stream);
 }
 
 // Host-buffer variant: arena = [a | b | t | draft_ids | accept_len | tokens | D | status | workspace],

@@ -25,6 +25,16 @@ struct __align__(16) RowRecord {
 //   tail_k <=> zhat_k / T < zhat_max + ln(tail_frac),
 //   protected_k = p_k * tail_scale on the tail, ex2((zhat_k / T - zhat_max) * log2e) * head_scale on
 //   the head.
+// One row's result in the multi-outcome kernels (the all-(beta, gamma) sweep; AsymSpec fused with
+// E2-SCI): JSD(a || t) (fused), the emitted-token candidates of the argmax slots, one gate bit per
+// gamma, and the kBit* problem flags.
+struct __align__(16) MultiRecord {
+  double J;
+  int32_t tok[4];
+  uint32_t gate_bits;
+  uint32_t flags;
+};
+
 struct __align__(32) RapidRecord {
   float zs_max;
   float inv_sum;
@@ -59,9 +69,13 @@ struct JsdArgs {
   int B, K, V;
   int n_slice;
   int bulk;
-  float beta;
+  int variant;       // 0 single outcome; 1 all-(beta, gamma) sweep; 2 AsymSpec fused with E2-SCI
+  float betas[4];    // betas[0] is the AsymSpec beta; the sweep uses n_beta of them
+  int n_beta;
   int delta_source;  // AsymSpec: 0 a - b, 1 a, 2 t - b
   double ln_gamma;
+  double ln_gammas[8];  // sweep: n_gamma values of ln(gamma); fused: ln_gammas[0] = ln_gamma
+  int n_gamma;
   // SCI
   double T_base, alpha_omega, tau_credit, T_min, T_max, ewma_beta;
   double* r_hat;
@@ -75,10 +89,14 @@ struct JsdArgs {
   float* out_D;      // AsymSpec: JSD(a,b); SCI: JSD(draft,target)
   float* out_lse;    // AsymSpec only, [R, 3]
   float* out_T;      // SCI only
+  float* out_J;               // fused: JSD(a || t) [R]
+  int32_t* out_sci_accept_len;  // fused: E2-SCI accept lengths [B]
+  int32_t* out_sci_tokens;      // fused: E2-SCI tokens [B, K+1]
   uint32_t* out_req_status;
   // workspace
   uint32_t* tickets;
   RowRecord* records;
+  MultiRecord* mrecords;  // multi-outcome variants (the same workspace bytes as `records`)
 };
 
 struct RapidArgs {

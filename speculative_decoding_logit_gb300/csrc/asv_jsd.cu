@@ -56,14 +56,18 @@ namespace asv {
 constexpr int kJsdThreads = 256;  // threads per CTA the kernel is compiled for (launch bounds)
 constexpr int kJsdCtasPerSm = 4;  // CTAs per SM the kernel is compiled for (launch bounds)
 
+constexpr int kMaxArg = 4;  // argmax slots: fused scores for up to 4 betas, or 1 beta and the plain target
+constexpr int kMaxGamma = 8;  // gammas of one sweep
+
 struct __align__(16) JsdXchg {
   float mx[3];        // CTA maxima of the inputs
   float sum_hi[3];    // CTA sums of exp2(x log2e - mL_cta), mL_cta = mx * log2e rounded, as hi + lo
   float sum_lo[3];
-  float argv;         // best verifier score in the CTA's slice
-  int32_t argi;       // its vocabulary index
+  float argv[kMaxArg];    // best scores in the CTA's slice
+  int32_t argi[kMaxArg];  // their vocabulary indices
   // Pushed into CTA 0 by every CTA before the second exchange; only CTA 0 reads them afterwards.
-  float jsd_from[kMaxCluster][6];  // pass-B sums (hi, lo): narrow form, wide p-form, wide q-form
+  // Pass-B sums (hi, lo): narrow form, wide p-form, wide q-form; then the second pair's (fused).
+  float jsd_from[kMaxCluster][12];
 };
 
 // Row constants, computed by one thread after the exchange and broadcast through shared memory.
@@ -74,9 +78,10 @@ struct __align__(16) JsdRowConsts {
   float S_lo[3];
   float dL;        // lse_b - lse_a (pair inputs 1 and 0)
   float hML;       // fl(ML[0]/2 + ML[1]/2), the narrow form's reference
+  float dL2;       // fused: lse_t - lse_a (pair inputs 2 and 0)
+  float hML2;      // fused: fl(ML[0]/2 + ML[2]/2)
   int32_t finite;
-  float rowv;
-  int32_t rowi;
+  int32_t rowi[kMaxArg];
 };
 
 template <int MODE>
@@ -284,7 +289,10 @@ __device__ __forceinline__ float2 delta2(float2 a, float2 b, float2 t) {
   else return fsub2(a, b);
 }
 
-template <typename T, int MODE, int DSRC, bool ALIGNED>
+// NB: fused scores t + beta_b * delta for NB betas (AsymSpec; the all-(beta, gamma) sweep takes 4).
+// FUSE: AsymSpec and E2-SCI in one read -- pass B also sums JSD(a || t), and an extra argmax slot
+// holds the plain target argmax.
+template <typename T, int MODE, int DSRC, bool ALIGNED, int NB, bool FUSE>
 __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(const JsdArgs p) {
   using G = GVec<T>;
   constexpr int NT = JsdTraits<MODE>::NT;
@@ -292,11 +300,16 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
   constexpr int VEC = G::kVec;
   constexpr int NP = G::kPairs;
   constexpr int kWarps = kJsdThreads / 32;
+  constexpr int NA = NB + (FUSE ? 1 : 0);  // argmax slots
+  constexpr bool kMulti = (NB > 1) || FUSE;
+  static_assert(NA <= kMaxArg, "argmax slots");
+  static_assert(!FUSE || (MODE == kModeAsym && NB == 1), "fused mode pairs one AsymSpec beta with E2-SCI");
 
   __shared__ JsdXchg xchg;
   __shared__ JsdRowConsts rc;
-  __shared__ float s_wf[kWarps][4];
-  __shared__ int32_t s_wi[kWarps];
+  __shared__ float s_wf[kWarps][6];
+  __shared__ float s_av[kWarps][kMaxArg];
+  __shared__ int32_t s_ai[kWarps][kMaxArg];
   __shared__ float s_wm[kWarps][3];
 
   const int tid = threadIdx.x;
@@ -319,10 +332,11 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
 #pragma unroll
   for (int j = 0; j < NT; ++j) slice[j] = static_cast<const char*>(p.x[j]) + (row_base + size_t(v0)) * G::kBytes;
 
-  // L2 policies: the verifier input is read once (evict first); the divergence pair is read again
-  // by pass B (evict last until then, evict first on that last read).
+  // L2 policies: the verifier input is read once (evict first; fused: pass B reads it again); the
+  // divergence pair is read again by pass B (evict last until then, evict first on that last read).
   const uint64_t pol_last = policy_evict_first();
   const uint64_t pol_keep = policy_evict_last();
+  const uint64_t pol_t = FUSE ? pol_keep : pol_last;
 
   // ---------------------------------------------------------------- pass A: maxima, exp sums, argmax
   RunMax<T> rmax[NT];
@@ -333,23 +347,30 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
     mL[j] = 0.0f;
     acc[j] = make_float2(0.0f, 0.0f);
   }
-  float bv = -INFINITY;
-  int bi = INT_MAX;
+  float bv[NA];
+  int bi[NA];
+#pragma unroll
+  for (int s = 0; s < NA; ++s) {
+    bv[s] = -INFINITY;
+    bi[s] = INT_MAX;
+  }
   {
     const float2 l2e2 = make_float2(kLog2e, kLog2e);
-    const float2 beta2 = make_float2(p.beta, p.beta);
+    float2 beta2[NB];
+#pragma unroll
+    for (int s = 0; s < NB; ++s) beta2[s] = make_float2(p.betas[s], p.betas[s]);
     uint4 cur[NT], nxt[NT];
     int vi = tid;
     if (vi < nvec) {
 #pragma unroll
-      for (int j = 0; j < NT; ++j) cur[j] = G::load(slice[j], vi * VEC, len, aligned, true, j == 2 ? pol_last : pol_keep);
+      for (int j = 0; j < NT; ++j) cur[j] = G::load(slice[j], vi * VEC, len, aligned, true, j == 2 ? pol_t : pol_keep);
     }
     for (; vi < nvec; vi += kJsdThreads) {
       const int vn = vi + kJsdThreads;
       // Prefetch the next vector (consumed only while it is in range).
       if (vn < nvec) {
 #pragma unroll
-        for (int j = 0; j < NT; ++j) nxt[j] = G::load(slice[j], vn * VEC, len, aligned, true, j == 2 ? pol_last : pol_keep);
+        for (int j = 0; j < NT; ++j) nxt[j] = G::load(slice[j], vn * VEC, len, aligned, true, j == 2 ? pol_t : pol_keep);
       }
       // Running maxima; when a value passes the reference's slack, move the partial sum to a new
       // reference at the current maximum.
@@ -383,25 +404,32 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
           acc[j] = fadd2(acc[j], make_float2(ex2_approx(y.x), ex2_approx(y.y)));
         }
       }
-      // Verifier score; one comparison per vector against the best so far.
-      float2 sc[NP];
+      // Verifier scores; one comparison per vector and score against the best so far.
 #pragma unroll
-      for (int q2 = 0; q2 < NP; ++q2) {
-        if constexpr (MODE == kModeAsym) sc[q2] = ffma2(beta2, delta2<DSRC>(x[0][q2], x[1][q2], x[2][q2]), x[2][q2]);
-        else sc[q2] = x[TGT][q2];
-      }
-      float vm = fmaxf(sc[0].x, sc[0].y);
+      for (int sl = 0; sl < NA; ++sl) {
+        float2 sc[NP];
 #pragma unroll
-      for (int q2 = 1; q2 < NP; ++q2) vm = fmaxf(vm, fmaxf(sc[q2].x, sc[q2].y));
-      if (vm > bv) {
-        int e_first = 2 * NP - 1;
-#pragma unroll
-        for (int q2 = NP - 1; q2 >= 0; --q2) {
-          if (sc[q2].y == vm) e_first = 2 * q2 + 1;
-          if (sc[q2].x == vm) e_first = 2 * q2;
+        for (int q2 = 0; q2 < NP; ++q2) {
+          if constexpr (MODE == kModeAsym) {
+            if (FUSE && sl == NB) sc[q2] = x[2][q2];  // the plain target argmax (E2-SCI's emitted token)
+            else sc[q2] = ffma2(beta2[sl < NB ? sl : 0], delta2<DSRC>(x[0][q2], x[1][q2], x[2][q2]), x[2][q2]);
+          } else {
+            sc[q2] = x[TGT][q2];
+          }
         }
-        bv = vm;
-        bi = v0 + vi * VEC + e_first;
+        float vm = fmaxf(sc[0].x, sc[0].y);
+#pragma unroll
+        for (int q2 = 1; q2 < NP; ++q2) vm = fmaxf(vm, fmaxf(sc[q2].x, sc[q2].y));
+        if (vm > bv[sl]) {
+          int e_first = 2 * NP - 1;
+#pragma unroll
+          for (int q2 = NP - 1; q2 >= 0; --q2) {
+            if (sc[q2].y == vm) e_first = 2 * q2 + 1;
+            if (sc[q2].x == vm) e_first = 2 * q2;
+          }
+          bv[sl] = vm;
+          bi[sl] = v0 + vi * VEC + e_first;
+        }
       }
 #pragma unroll
       for (int j = 0; j < NT; ++j) cur[j] = nxt[j];
@@ -414,10 +442,13 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
     const float w = warp_max(rmax[j].value());
     if (lane == 0) s_wm[warp][j] = w;
   }
-  warp_argmax(bv, bi);
-  if (lane == 0) {
-    s_wf[warp][3] = bv;
-    s_wi[warp] = bi;
+#pragma unroll
+  for (int sl = 0; sl < NA; ++sl) {
+    warp_argmax(bv[sl], bi[sl]);
+    if (lane == 0) {
+      s_av[warp][sl] = bv[sl];
+      s_ai[warp][sl] = bi[sl];
+    }
   }
   __syncthreads();
   float Mc[NT];
@@ -434,9 +465,16 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
   }
   __syncthreads();
   if (warp == 0) {
-    float v2 = (lane < kWarps) ? s_wf[lane][3] : -INFINITY;
-    int i2 = (lane < kWarps) ? s_wi[lane] : INT_MAX;
-    warp_argmax(v2, i2);
+#pragma unroll
+    for (int sl = 0; sl < NA; ++sl) {
+      float v2 = (lane < kWarps) ? s_av[lane][sl] : -INFINITY;
+      int i2 = (lane < kWarps) ? s_ai[lane][sl] : INT_MAX;
+      warp_argmax(v2, i2);
+      if (lane == 0) {
+        xchg.argv[sl] = v2;
+        xchg.argi[sl] = i2;
+      }
+    }
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       const DF d = warp_sum_df(DF{lane < kWarps ? s_wf[lane][j] : 0.0f, 0.0f});
@@ -446,10 +484,6 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
         xchg.sum_lo[j] = d.lo;
       }
     }
-    if (lane == 0) {
-      xchg.argv = v2;
-      xchg.argi = i2;
-    }
   }
   cluster_sync_w0(warp);  // #1
 
@@ -458,8 +492,13 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
     // lane q < C holds CTA q's partials; move every CTA's sums to the row reference, then add.
     float mq[NT];
     DF sq[NT];
-    float v2 = -INFINITY;
-    int i2 = INT_MAX;
+    float v2[NA];
+    int i2[NA];
+#pragma unroll
+    for (int sl = 0; sl < NA; ++sl) {
+      v2[sl] = -INFINITY;
+      i2[sl] = INT_MAX;
+    }
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       mq[j] = -INFINITY;
@@ -473,10 +512,14 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
         sq[j].hi = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.sum_hi[j]), q));
         sq[j].lo = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.sum_lo[j]), q));
       }
-      v2 = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.argv), q));
-      i2 = dsmem_ld_s32(dsmem_map(smem_addr(&xchg.argi), q));
+#pragma unroll
+      for (int sl = 0; sl < NA; ++sl) {
+        v2[sl] = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.argv[sl]), q));
+        i2[sl] = dsmem_ld_s32(dsmem_map(smem_addr(&xchg.argi[sl]), q));
+      }
     }
-    warp_argmax(v2, i2);
+#pragma unroll
+    for (int sl = 0; sl < NA; ++sl) warp_argmax(v2[sl], i2[sl]);
     DF S[NT];
     float M[NT], MLr[NT];
 #pragma unroll
@@ -509,8 +552,19 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
       rc.dL = dL;
       // hML = fl(ML[0]/2 + ML[1]/2); its rounding error is removed from the narrow sum at the end.
       rc.hML = 0.5f * MLr[0] + 0.5f * MLr[1];
-      rc.rowv = v2;
-      rc.rowi = i2;
+      if constexpr (FUSE) {
+        float dL2 = 0.0f;
+        if (finite) {
+          const float ca = fmaf(M[0], kLog2e, -MLr[0]);
+          const float ct = fmaf(M[2], kLog2e, -MLr[2]);
+          const float ratio = (S[2].hi + S[2].lo) / (S[0].hi + S[0].lo);
+          dL2 = (M[2] - M[0]) + (ln_split(ratio) - (ct - ca) * kLn2f);
+        }
+        rc.dL2 = dL2;
+        rc.hML2 = 0.5f * MLr[0] + 0.5f * MLr[2];
+      }
+#pragma unroll
+      for (int sl = 0; sl < NA; ++sl) rc.rowi[sl] = i2[sl];
     }
   }
   __syncthreads();
@@ -518,54 +572,75 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
   // ---------------------------------------------------------------- pass B: divergence terms
   {
     const bool finite = rc.finite != 0;
-    RowB rb;
+    RowB rb, rb2;
     rb.dL = rc.dL;
     rb.MaL = rc.ML[0];
     rb.MbL = rc.ML[1];
     rb.hML = rc.hML;
-    float2 accn = make_float2(0.0f, 0.0f);
-    float an = 0.0f, ap = 0.0f, aq = 0.0f;
-    if (finite) {
-      const float2 dl2 = make_float2(rb.dL, rb.dL);
+    if constexpr (FUSE) {
+      rb2.dL = rc.dL2;
+      rb2.MaL = rc.ML[0];
+      rb2.MbL = rc.ML[2];
+      rb2.hML = rc.hML2;
+    }
+    // Accumulators per pair: narrow (packed), narrow/wide p-form/wide q-form (scalar).
+    float2 accn = make_float2(0.0f, 0.0f), accn2 = make_float2(0.0f, 0.0f);
+    float an = 0.0f, ap = 0.0f, aq = 0.0f, an2 = 0.0f, ap2 = 0.0f, aq2 = 0.0f;
+    // One vector of the pair (xa, xb) against row constants rb.
+    auto pair_terms = [&](const float2 (&xa)[NP], const float2 (&xb)[NP], const RowB& r, float2& acn, float& sn,
+                          float& sp, float& sq) {
+      const float2 dl2 = make_float2(r.dL, r.dL);
       const float2 hl2e2 = make_float2(0.5f * kLog2e, 0.5f * kLog2e);
-      const float2 nhml2 = make_float2(-rb.hML, -rb.hML);
+      const float2 nhml2 = make_float2(-r.hML, -r.hML);
+      float2 s2[NP];
+#pragma unroll
+      for (int q2 = 0; q2 < NP; ++q2) {
+        const float2 uu = fsub2(fsub2(xb[q2], xa[q2]), dl2);
+        s2[q2] = fmul2(uu, uu);
+      }
+      // Narrow form for the whole vector unless one entry is outside it (or NaN: -inf pairs).
+      float smax = fmax_nan(s2[0].x, s2[0].y);
+#pragma unroll
+      for (int q2 = 1; q2 < NP; ++q2) smax = fmax_nan(smax, fmax_nan(s2[q2].x, s2[q2].y));
+      if (smax <= ASV_JSD_EVEN_S0) {
+#pragma unroll
+        for (int q2 = 0; q2 < NP; ++q2) {
+          const float2 y = ffma2(fadd2(xa[q2], xb[q2]), hl2e2, nhml2);
+          const float2 e = make_float2(ex2_approx(y.x), ex2_approx(y.y));
+          acn = ffma2(fmul2(e, s2[q2]), asv_jsd_even2(s2[q2]), acn);
+        }
+      } else {
+#pragma unroll
+        for (int q2 = 0; q2 < NP; ++q2) {
+          jsd_entry(xa[q2].x, xb[q2].x, r, sn, sp, sq);
+          jsd_entry(xa[q2].y, xb[q2].y, r, sn, sp, sq);
+        }
+      }
+    };
+    if (finite) {
       int vi = tid;
-      uint4 ca, cb, na, nb;
+      uint4 ca, cb, ct, na, nb, nt;
       if (vi < nvec) {
         ca = G::load(slice[0], vi * VEC, len, aligned, true, pol_last);
         cb = G::load(slice[1], vi * VEC, len, aligned, true, pol_last);
+        if constexpr (FUSE) ct = G::load(slice[NT - 1], vi * VEC, len, aligned, true, pol_last);
       }
       for (; vi < nvec; vi += kJsdThreads) {
         const int vn = vi + kJsdThreads;
         if (vn < nvec) {
           na = G::load(slice[0], vn * VEC, len, aligned, true, pol_last);
           nb = G::load(slice[1], vn * VEC, len, aligned, true, pol_last);
+          if constexpr (FUSE) nt = G::load(slice[NT - 1], vn * VEC, len, aligned, true, pol_last);
         }
-        float2 xa[NP], xb[NP], uu[NP], s2[NP];
+        float2 xa[NP], xb[NP];
         G::pairs(ca, xa);
         G::pairs(cb, xb);
-#pragma unroll
-        for (int q2 = 0; q2 < NP; ++q2) {
-          uu[q2] = fsub2(fsub2(xb[q2], xa[q2]), dl2);
-          s2[q2] = fmul2(uu[q2], uu[q2]);
-        }
-        // Narrow form for the whole vector unless one entry is outside it (or NaN: -inf pairs).
-        float smax = fmax_nan(s2[0].x, s2[0].y);
-#pragma unroll
-        for (int q2 = 1; q2 < NP; ++q2) smax = fmax_nan(smax, fmax_nan(s2[q2].x, s2[q2].y));
-        if (smax <= ASV_JSD_EVEN_S0) {
-#pragma unroll
-          for (int q2 = 0; q2 < NP; ++q2) {
-            const float2 y = ffma2(fadd2(xa[q2], xb[q2]), hl2e2, nhml2);
-            const float2 e = make_float2(ex2_approx(y.x), ex2_approx(y.y));
-            accn = ffma2(fmul2(e, s2[q2]), asv_jsd_even2(s2[q2]), accn);
-          }
-        } else {
-#pragma unroll
-          for (int q2 = 0; q2 < NP; ++q2) {
-            jsd_entry(xa[q2].x, xb[q2].x, rb, an, ap, aq);
-            jsd_entry(xa[q2].y, xb[q2].y, rb, an, ap, aq);
-          }
+        pair_terms(xa, xb, rb, accn, an, ap, aq);
+        if constexpr (FUSE) {
+          float2 xt[NP];
+          G::pairs(ct, xt);
+          pair_terms(xa, xt, rb2, accn2, an2, ap2, aq2);
+          ct = nt;
         }
         ca = na;
         cb = nb;
@@ -579,21 +654,29 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
       s_wf[warp][1] = wp;
       s_wf[warp][2] = wq;
     }
+    if constexpr (FUSE) {
+      const float wn2 = warp_sumf((accn2.x + accn2.y) + an2);
+      const float wp2 = warp_sumf(ap2);
+      const float wq2 = warp_sumf(aq2);
+      if (lane == 0) {
+        s_wf[warp][3] = wn2;
+        s_wf[warp][4] = wp2;
+        s_wf[warp][5] = wq2;
+      }
+    }
   }
   __syncthreads();
   if (warp == 0) {
-    const DF dn = warp_sum_df(DF{lane < kWarps ? s_wf[lane][0] : 0.0f, 0.0f});
-    const DF dp = warp_sum_df(DF{lane < kWarps ? s_wf[lane][1] : 0.0f, 0.0f});
-    const DF dq = warp_sum_df(DF{lane < kWarps ? s_wf[lane][2] : 0.0f, 0.0f});
-    if (lane == 0) {
-      // Push this CTA's pass-B sums into CTA 0.
-      const uint32_t base = smem_addr(&xchg.jsd_from[rank][0]);
-      dsmem_st_f32(dsmem_map(base + 0, 0), dn.hi);
-      dsmem_st_f32(dsmem_map(base + 4, 0), dn.lo);
-      dsmem_st_f32(dsmem_map(base + 8, 0), dp.hi);
-      dsmem_st_f32(dsmem_map(base + 12, 0), dp.lo);
-      dsmem_st_f32(dsmem_map(base + 16, 0), dq.hi);
-      dsmem_st_f32(dsmem_map(base + 20, 0), dq.lo);
+    constexpr int NS = FUSE ? 6 : 3;
+#pragma unroll
+    for (int m = 0; m < NS; ++m) {
+      const DF dm = warp_sum_df(DF{lane < kWarps ? s_wf[lane][m] : 0.0f, 0.0f});
+      if (lane == 0) {
+        // Push this CTA's pass-B sums into CTA 0.
+        const uint32_t base = smem_addr(&xchg.jsd_from[rank][2 * m]);
+        dsmem_st_f32(dsmem_map(base + 0, 0), dm.hi);
+        dsmem_st_f32(dsmem_map(base + 4, 0), dm.lo);
+      }
     }
   }
   cluster_sync_w0(warp);  // #2: after this only CTA 0 touches shared memory, and only its own
@@ -632,6 +715,29 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
     const float wide = __fdiv_rn(jp.hi + jp.lo, Sa) + __fdiv_rn(jq.hi + jq.lo, Sb);
     D = fminf(fmaxf(0.5f * (narrow + wide), 0.0f), kLn2f);
   }
+  // Fused: J = JSD(a || t) from the second pair's sums, the same way.
+  float J = 0.0f;
+  if constexpr (FUSE) {
+    DF kn{0.0f, 0.0f}, kp{0.0f, 0.0f}, kq{0.0f, 0.0f};
+    if (lane < int(C)) {
+      kn = DF{xchg.jsd_from[lane][6], xchg.jsd_from[lane][7]};
+      kp = DF{xchg.jsd_from[lane][8], xchg.jsd_from[lane][9]};
+      kq = DF{xchg.jsd_from[lane][10], xchg.jsd_from[lane][11]};
+    }
+    kn = warp_sum_df(kn);
+    kp = warp_sum_df(kp);
+    kq = warp_sum_df(kq);
+    if (finite) {
+      const float ha = 0.5f * rc.ML[0], ht = 0.5f * rc.ML[2];
+      const float bb = rc.hML2 - ha;
+      const float delta = -((ha - (rc.hML2 - bb)) + (ht - bb));
+      const float Sa = rc.S_hi[0] + rc.S_lo[0];
+      const float St = rc.S_hi[2] + rc.S_lo[2];
+      const float narrow = __fdiv_rn((kn.hi + kn.lo) * exp2f(delta), __fsqrt_rn(Sa) * __fsqrt_rn(St));
+      const float wide = __fdiv_rn(kp.hi + kp.lo, Sa) + __fdiv_rn(kq.hi + kq.lo, St);
+      J = fminf(fmaxf(0.5f * (narrow + wide), 0.0f), kLn2f);
+    }
+  }
   // Log-sum-exps, one input per lane (double): lse = M + ln(S) - c ln2.
   double my_lse = 0.0;
   if (lane < NT && finite) {
@@ -642,6 +748,7 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
   const double lse_v = __shfl_sync(kAll, my_lse, NT - 1);
   const float td = __shfl_sync(kAll, xd, 1);
   const float bd = __shfl_sync(kAll, xd, 2);
+  if constexpr (!kMulti) {
   uint32_t bits = 0;
   if (!finite) bits |= kBitNonfinite;
   if (pos < K) {
@@ -658,7 +765,7 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
   if (lane == 0) {
     RowRecord rec;
     rec.value = double(D);
-    rec.token = (rc.rowi == INT_MAX) ? 0 : rc.rowi;
+    rec.token = (rc.rowi[0] == INT_MAX) ? 0 : rc.rowi[0];
     rec.bits = bits;
     p.records[row] = rec;
     ticket = atom_add_acq_rel_gpu(&p.tickets[req], 1u);
@@ -739,6 +846,107 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
     p.out_req_status[req] = status;
     p.tickets[req] = 0u;
   }
+  } else {
+    // ---------------------------------------------------------------- multi-outcome row (sweep / fused)
+    uint32_t flags = finite ? 0u : kBitNonfinite;
+    uint32_t gate_bits = 0;
+    if (pos < K) {
+      if (!d_ok) {
+        flags |= kBitBadDraft;
+      } else if (finite) {
+        // margin without ln(gamma); the gate for gamma_g is margin0 - ln(gamma_g) > 0.
+        const double margin0 = (double(td) - lse_v) + double(D) - (double(bd) - lse_b);
+        for (int g = 0; g < p.n_gamma; ++g)
+          if (margin0 - p.ln_gammas[g] > 0.0) gate_bits |= 1u << g;
+      }
+    }
+    if (lane == 0) {
+      if (p.out_D) p.out_D[row] = finite ? D : __int_as_float(0x7fc00000);
+      if (FUSE && p.out_J) p.out_J[row] = finite ? J : __int_as_float(0x7fc00000);
+    }
+    if (p.out_lse && lane < NT) p.out_lse[size_t(row) * 3 + lane] = float(my_lse);
+    uint32_t ticket = 0;
+    if (lane == 0) {
+      MultiRecord rec;
+      rec.J = double(J);
+#pragma unroll
+      for (int sl = 0; sl < kMaxArg; ++sl) rec.tok[sl] = (sl < NA && rc.rowi[sl] != INT_MAX) ? rc.rowi[sl] : 0;
+      rec.gate_bits = gate_bits;
+      rec.flags = flags;
+      p.mrecords[row] = rec;
+      ticket = atom_add_acq_rel_gpu(&p.tickets[req], 1u);
+    }
+    ticket = __shfl_sync(kAll, ticket, 0);
+    if (ticket != uint32_t(K)) return;
+
+    // Last row of this request: one scan per gamma (and, fused, the E2-SCI scan), 32 records a step.
+    (void)ld_acquire_gpu(&p.tickets[req]);
+    MultiRecord* recs = p.mrecords + size_t(req) * R1;
+    double thr = 0.0;
+    if (FUSE) {
+      thr = __dadd_rn(p.T_base, __dmul_rn(p.alpha_omega, __dsub_rn(p.r_hat[req], p.tau_credit)));
+      thr = fmax(p.T_min, fmin(thr, p.T_max));
+    }
+    uint32_t any = 0;
+    int n_g[kMaxGamma];
+#pragma unroll
+    for (int g = 0; g < kMaxGamma; ++g) n_g[g] = K;
+    int n_sci = K;
+    for (int base = 0; base < R1; base += 32) {
+      const int i = base + lane;
+      uint32_t gb = 0, fl = 0;
+      double jv = 0.0;
+      if (i < R1) {
+        const float4 w0 = ld_cg_f4(recs + i);
+        const float4 w1 = ld_cg_f4(reinterpret_cast<const char*>(recs + i) + 16);
+        jv = __hiloint2double(__float_as_int(w0.y), __float_as_int(w0.x));
+        gb = __float_as_uint(w1.z);
+        fl = __float_as_uint(w1.w);
+      }
+      any |= __reduce_or_sync(kAll, fl);
+#pragma unroll
+      for (int g = 0; g < kMaxGamma; ++g) {
+        const unsigned rej = __ballot_sync(kAll, i < K && !((gb >> g) & 1u));
+        if (n_g[g] == K && rej != 0u) n_g[g] = base + __ffs(rej) - 1;
+      }
+      if (FUSE) {
+        const unsigned rej = __ballot_sync(kAll, i < K && jv > thr);
+        if (n_sci == K && rej != 0u) n_sci = base + __ffs(rej) - 1;
+      }
+    }
+    const uint32_t status = ((any & kBitNonfinite) ? 1u : 0u) | ((any & kBitBadDraft) ? 2u : 0u) |
+                            ((any & kBitTimeout) ? 4u : 0u);
+    const int32_t* dr = p.draft_ids + size_t(req) * K;
+    const int B = p.B;
+    for (int g = 0; g < p.n_gamma; ++g) {
+      const int n = n_g[g];
+      if (lane == 0) p.out_accept_len[size_t(g) * B + req] = status ? 0 : n;
+      for (int b2 = 0; b2 < NB && b2 < p.n_beta; ++b2) {
+        const int tok_n = __ldcg(&recs[n].tok[b2]);  // (L2: another SM wrote it)
+        int32_t* toks = p.out_tokens + ((size_t(b2) * p.n_gamma + g) * B + req) * R1;
+        for (int i = lane; i < R1; i += 32) toks[i] = status ? -1 : ((i < n) ? dr[i] : (i == n ? tok_n : -1));
+      }
+    }
+    if constexpr (FUSE) {
+      const int tok_n = __ldcg(&recs[n_sci].tok[NB]);
+      int32_t* toks = p.out_sci_tokens + size_t(req) * R1;
+      for (int i = lane; i < R1; i += 32) toks[i] = status ? -1 : ((i < n_sci) ? dr[i] : (i == n_sci ? tok_n : -1));
+      if (lane == 0) {
+        if (p.out_T) p.out_T[req] = float(thr);
+        p.out_sci_accept_len[req] = status ? 0 : n_sci;
+        if (!status) {
+          const double pacc = __ddiv_rn(double(n_sci), double(K));
+          p.r_hat[req] = __dadd_rn(__dmul_rn(__dsub_rn(1.0, p.ewma_beta), p.r_hat[req]), __dmul_rn(p.ewma_beta, pacc));
+        }
+      }
+    }
+    __syncwarp();
+    for (int i = lane; i < R1; i += 32) recs[i] = MultiRecord{};  // consumed: the workspace is left zeroed
+    if (lane == 0) {
+      p.out_req_status[req] = status;
+      p.tickets[req] = 0u;
+    }
+  }
 }
 
 int jsd_static_smem_bytes() { return 0; }
@@ -747,22 +955,31 @@ int jsd_ctas_per_sm() { return kJsdCtasPerSm; }
 
 using JsdKernel = void (*)(const JsdArgs);
 
+// variant 0: the single-outcome kernels; 1: the all-(beta, gamma) sweep (4 betas); 2: AsymSpec and
+// E2-SCI fused (AsymSpec mode, delta = a - b).
 template <bool AL>
-static JsdKernel pick_aligned(int mode, int dtype, int dsrc) {
+static JsdKernel pick_aligned(int mode, int dtype, int dsrc, int variant) {
+  if (variant == 1)
+    return dtype == 0 ? jsd_family_kernel<float, kModeAsym, 0, AL, 4, false>
+                      : jsd_family_kernel<bf16_t, kModeAsym, 0, AL, 4, false>;
+  if (variant == 2)
+    return dtype == 0 ? jsd_family_kernel<float, kModeAsym, 0, AL, 1, true>
+                      : jsd_family_kernel<bf16_t, kModeAsym, 0, AL, 1, true>;
   if (mode == kModeSci)
-    return dtype == 0 ? jsd_family_kernel<float, kModeSci, 0, AL> : jsd_family_kernel<bf16_t, kModeSci, 0, AL>;
+    return dtype == 0 ? jsd_family_kernel<float, kModeSci, 0, AL, 1, false>
+                      : jsd_family_kernel<bf16_t, kModeSci, 0, AL, 1, false>;
   if (dtype == 0) {
-    if (dsrc == 1) return jsd_family_kernel<float, kModeAsym, 1, AL>;
-    if (dsrc == 2) return jsd_family_kernel<float, kModeAsym, 2, AL>;
-    return jsd_family_kernel<float, kModeAsym, 0, AL>;
+    if (dsrc == 1) return jsd_family_kernel<float, kModeAsym, 1, AL, 1, false>;
+    if (dsrc == 2) return jsd_family_kernel<float, kModeAsym, 2, AL, 1, false>;
+    return jsd_family_kernel<float, kModeAsym, 0, AL, 1, false>;
   }
-  if (dsrc == 1) return jsd_family_kernel<bf16_t, kModeAsym, 1, AL>;
-  if (dsrc == 2) return jsd_family_kernel<bf16_t, kModeAsym, 2, AL>;
-  return jsd_family_kernel<bf16_t, kModeAsym, 0, AL>;
+  if (dsrc == 1) return jsd_family_kernel<bf16_t, kModeAsym, 1, AL, 1, false>;
+  if (dsrc == 2) return jsd_family_kernel<bf16_t, kModeAsym, 2, AL, 1, false>;
+  return jsd_family_kernel<bf16_t, kModeAsym, 0, AL, 1, false>;
 }
 
-static JsdKernel pick_kernel(int mode, int dtype, int dsrc, bool aligned) {
-  return aligned ? pick_aligned<true>(mode, dtype, dsrc) : pick_aligned<false>(mode, dtype, dsrc);
+static JsdKernel pick_kernel(int mode, int dtype, int dsrc, bool aligned, int variant) {
+  return aligned ? pick_aligned<true>(mode, dtype, dsrc, variant) : pick_aligned<false>(mode, dtype, dsrc, variant);
 }
 
 static cudaLaunchConfig_t make_config(const LaunchPlan& plan, unsigned grid, cudaStream_t s, cudaLaunchAttribute* attr) {
@@ -786,7 +1003,7 @@ static cudaError_t prepare(JsdKernel kern, const LaunchPlan& plan) {
 }
 
 cudaError_t launch_jsd_family(int mode, int dtype, const JsdArgs& a, const LaunchPlan& plan, cudaStream_t s) {
-  JsdKernel kern = pick_kernel(mode, dtype, a.delta_source, a.bulk != 0);
+  JsdKernel kern = pick_kernel(mode, dtype, a.delta_source, a.bulk != 0, a.variant);
   cudaError_t e = prepare(kern, plan);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
@@ -796,7 +1013,7 @@ cudaError_t launch_jsd_family(int mode, int dtype, const JsdArgs& a, const Launc
 }
 
 int jsd_max_active_clusters(int mode, int dtype, const LaunchPlan& plan) {
-  JsdKernel kern = pick_kernel(mode, dtype, 0, plan.bulk != 0);
+  JsdKernel kern = pick_kernel(mode, dtype, 0, plan.bulk != 0, 0);
   if (prepare(kern, plan) != cudaSuccess) return 0;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_config(plan, unsigned(plan.cluster), 0, attr);
