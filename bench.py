@@ -315,6 +315,100 @@ def run_ours(args):
     return 0
 
 
+def run_workload(args):
+    """Device-timed throughput of one of the other workloads (one launch per step, inputs resident
+    in HBM, timed with CUDA events on the launching stream; inputs larger than L2, or rotating
+    copies that together are).  Prints the same JSON line shape (no e2e or CPU leg)."""
+    import torch
+
+    import speculative_decoding_logit_gb300 as asv
+
+    w = gen.WORKLOADS[args.workload]
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    asv.build()
+    todev = lambda x, dt: (torch.from_numpy(np.ascontiguousarray(x)).to(dev) if dt == gen.F32 else
+                           torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev))
+    R = w.B * (w.K + 1)
+    extra = {}
+    if w.mode == "rapid":
+        b = gen.make_rapid_batch(w.seed, w.B, w.K, w.V)
+        sets = [(todev(b.z, gen.F32), todev(b.q, gen.F32)) for _ in range(3)]
+        d = torch.from_numpy(b.drafts).to(dev)
+        eta = 10.0
+        step_bytes = 2 * R * w.V * 4
+        call = lambda i: asv.rapid_verify(*sets[i % 3], d, w.params["T"], eta, w.params["tail_frac"],
+                                          w.params["philox_seed"])
+        dtype, kernel = "f32", "rapid_kernel"
+        extra = {"eta": eta, "sets": 3}
+    else:
+        # Generated requests tiled along the batch when the workload is large (the kernel's work per
+        # row does not depend on which request the row belongs to, and the rows are far apart).
+        gen_B = min(w.B, 64)
+        batch = gen.make_asymspec_batch(w.recipe, w.seed, gen_B, w.K, w.V, w.dtype,
+                                        identical_frac=w.params.get("identical_frac", 0.0), processes=8)
+        tile = (w.B + gen_B - 1) // gen_B
+        rep = lambda x: np.concatenate([x] * tile, axis=0)[:w.B]
+        a, b_, t = (todev(rep(x), w.dtype) for x in (batch.a, batch.b, batch.t))
+        d = torch.from_numpy(rep(batch.drafts)).to(dev)
+        s_el = 4 if w.dtype == gen.F32 else 2
+        step_bytes = 3 * R * w.V * s_el
+        nsets = max(1, min(4, int(np.ceil(4 * 129e6 / step_bytes))))
+        sets = [(a, b_, t)] + [tuple(x.clone() for x in (a, b_, t)) for _ in range(nsets - 1)]
+        dtype = "f32" if w.dtype == gen.F32 else "bf16"
+        extra = {"requests_generated": gen_B, "tiled": tile, "sets": nsets}
+        if args.workload == "asymspec_sweep_b256_k4_v151936_f32":
+            betas, gammas = [0.0, 1.0, 1.5, 2.0], [0.4, 0.5, 0.7, 1.0]
+            call = lambda i: asv.asymspec_verify_sweep(*sets[i % nsets], d, betas, gammas)
+            kernel = "jsd_family_kernel (sweep: 4 betas x 4 gammas)"
+            extra["grid_points"] = 16
+        elif args.workload == "sci_asymspec_b1024_k8_v151936_bf16":
+            r_hat = torch.full((w.B,), w.params["r_hat0"], dtype=torch.float64, device=dev)
+            call = lambda i: asv.asymspec_sci_verify(*sets[i % nsets], d, 1.0, 0.5, r_hat)
+            kernel = "jsd_family_kernel (AsymSpec fused with E2-SCI)"
+        else:
+            call = lambda i: asv.asymspec_verify(*sets[i % nsets], d, 1.0, 0.5)
+            kernel = "jsd_family_kernel"
+    for i in range(max(3, args.warmup)):
+        call(i)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = "0"
+    clocks = ClockSampler(gpu_id)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    e0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        call(i)
+        ev[i][1].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    elapsed_ms = e0.elapsed_time(e1)
+    launch_ms = float(np.mean([x.elapsed_time(y) for x, y in ev]))
+    peaks, peak_kind = _peaks()
+    achieved = step_bytes / (launch_ms / 1e3) / 1e9
+    line = {"metric": f"verified logit rows/s ({args.workload})", "value": R * args.steps / (elapsed_ms / 1e3),
+            "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+            "config": dict({"workload": args.workload, "B": w.B, "K": w.K, "V": w.V, "rows_per_step": R,
+                            "kernel": kernel}, **extra),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_kind": peak_kind,
+                         "kernel_ms": launch_ms, "algorithmic_bytes_per_launch": step_bytes},
+            "gpu_launches": args.steps, "clocks": clk}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -325,11 +419,15 @@ def main():
                     help="DRAM bytes per launch from an ncu capture of the current kernel (else null)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(gen.WORKLOADS),
+                    help="another workload (device-timed line only; the default is the headline workload)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload != WORKLOAD:
+        return run_workload(args)
     return run_ours(args)
 
 
