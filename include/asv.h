@@ -280,6 +280,21 @@ asv_status sci_verify(const void* draft_logits, const void* target_logits, int d
                       void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * sci_verify_prehit -- sci_verify with the first-token pre-hit of [SCI] Key design 4 (PLC): the
+ * first draft of every window is verified first, and a window whose first draft fails the
+ * threshold is dropped without reading its later rows (accept length 0, the target's argmax at
+ * position 0, r_hat updated with acceptance 0).  Two launches on `stream`: row 0 of every request,
+ * then rows 1..K of the windows kept.  For finite inputs the outputs equal sci_verify's, except
+ * that out_jsd holds only row 0 of a dropped window (its later entries are not written); a
+ * dropped window never sees non-finite values past its first row, so such a request is flagged
+ * by sci_verify but not here.  Draft ids are all checked.  K >= 1.
+ */
+asv_status sci_verify_prehit(const void* draft_logits, const void* target_logits, int dtype, const int32_t* draft_ids,
+                             int B, int K, int V, const asv_sci_params* params, double* r_hat, int32_t* out_accept_len,
+                             int32_t* out_tokens, float* out_jsd, float* out_T, uint32_t* out_req_status,
+                             void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * E2-SCI stabilisers.  [SCI] Key design 3 adds hysteresis, a minimum refresh interval and a
  * fallback to a conservative threshold when accuracy under the predicted threshold drops below a
  * bound, and gives no constants; these are the parameters.  One window's threshold, from the

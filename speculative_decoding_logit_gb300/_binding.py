@@ -114,6 +114,9 @@ def _declare(L):
     L.asymspec_sci_verify.argtypes = [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _f, _f, C.POINTER(_SciParamsC), _vp, _vp,
                                       _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
     L.asymspec_sci_verify.restype = _i
+    L.sci_verify_prehit.argtypes = [_vp, _vp, _i, _vp, _i, _i, _i, C.POINTER(_SciParamsC), _vp, _vp, _vp, _vp, _vp,
+                                    _vp, _vp, _sz, _vp]
+    L.sci_verify_prehit.restype = _i
     L.rapid_verify_ex.argtypes = [_vp, _vp, _vp, _i, _i, _i, _f, _f, _f, C.c_uint64, C.c_uint32,
                                   C.POINTER(_RapidOptionsC), _vp, _vp, _vp, _vp, _sz, _vp]
     L.rapid_verify_ex.restype = _i
@@ -446,10 +449,11 @@ def sci_state_decode(state: torch.Tensor):
 
 def sci_verify(draft: torch.Tensor, target: torch.Tensor, draft_ids: torch.Tensor, r_hat: torch.Tensor,
                params: SciParams = SciParams(), *, stabilisers: Optional[SciStabilisers] = None,
-               state: Optional[torch.Tensor] = None, out: Optional[SciOutput] = None,
+               state: Optional[torch.Tensor] = None, prehit: bool = False, out: Optional[SciOutput] = None,
                workspace: Optional[torch.Tensor] = None, stream=None) -> SciOutput:
     """One E2-SCI window; r_hat (float64 [B], device) is updated in place, and with `stabilisers`
-    so is `state` (from sci_state_new)."""
+    so is `state` (from sci_state_new).  `prehit` verifies every window's first draft first and
+    drops windows whose first draft fails (sci_verify_prehit; no stabilisers)."""
     _need_cuda(draft, target, draft_ids, r_hat)
     if draft.dim() != 3 or draft.shape != target.shape or draft.dtype != target.dtype:
         raise AsvError(2, "draft and target must share one [B, K+1, V] shape and dtype")
@@ -478,6 +482,14 @@ def sci_verify(draft: torch.Tensor, target: torch.Tensor, draft_ids: torch.Tenso
     ws = workspace if workspace is not None else _workspace(dev, sh, need)
     pc = _SciParamsC(params.T_base, params.alpha_omega, params.tau_credit, params.T_min, params.T_max,
                      params.ewma_beta)
+    if prehit:
+        if stabilisers is not None:
+            raise AsvError(5, "the pre-hit path takes no stabilisers")
+        st = library().sci_verify_prehit(_ptr(draft), _ptr(target), dt, _ptr(draft_ids), B, K, V, C.byref(pc),
+                                         _ptr(r_hat), _ptr(out.accept_len), _ptr(out.tokens), _ptr(out.jsd),
+                                         _ptr(out.T), _ptr(out.req_status), _ptr(ws), ws.numel(), sh)
+        _check(st, "sci_verify_prehit")
+        return out
     if stabilisers is None:
         st = library().sci_verify(_ptr(draft), _ptr(target), dt, _ptr(draft_ids), B, K, V, C.byref(pc), _ptr(r_hat),
                                   _ptr(out.accept_len), _ptr(out.tokens), _ptr(out.jsd), _ptr(out.T),

@@ -170,10 +170,17 @@ const char* asv_status_string(asv_status s) {
 
 int asv_last_cuda_error(void) { return g_last_cuda_error; }
 
+// Workspace: [tickets: B x u32, padded to 256 B][records: R x record]; E2-SCI adds the pre-hit
+// drop flags [B x u32] after the records (256-byte aligned).
+static size_t records_end(int mode, int B, int K) {
+  return round_up(tickets_bytes(B) + size_t(B) * size_t(K + 1) * record_bytes(mode), 256);
+}
+
 size_t asv_workspace_bytes(int mode, int B, int K, int V, int dtype) {
   (void)V;
   (void)dtype;
   if (B < 0 || K < 0) return 0;
+  if (mode == ASV_MODE_SCI) return records_end(mode, B, K) + size_t(B) * 4;
   return tickets_bytes(B) + size_t(B) * size_t(K + 1) * record_bytes(mode);
 }
 
@@ -238,6 +245,20 @@ static asv_status run_jsd(int mode, asv::JsdArgs& a, int dtype, void* workspace,
   a.tickets = reinterpret_cast<uint32_t*>(workspace);
   a.records = reinterpret_cast<asv::RowRecord*>(static_cast<char*>(workspace) + tickets_bytes(a.B));
   a.mrecords = reinterpret_cast<asv::MultiRecord*>(static_cast<char*>(workspace) + tickets_bytes(a.B));
+  if (mode == asv::kModeSci && a.prehit_phase != 0) {
+    // E2-SCI pre-hit: phase 1 over row 0 of every request, phase 2 over rows 1..K of the requests
+    // phase 1 kept, then the drop flags are cleared (the workspace is left zeroed).
+    a.dropped = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + records_end(ASV_MODE_SCI, a.B, a.K));
+    a.prehit_phase = 1;
+    e = asv::launch_jsd_family(mode, dtype, a, pl, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    a.prehit_phase = 2;
+    e = asv::launch_jsd_family(mode, dtype, a, pl, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaMemsetAsync(a.dropped, 0, size_t(a.B) * 4, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return ASV_OK;
+  }
   e = asv::launch_jsd_family(mode, dtype, a, pl, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   return ASV_OK;
@@ -297,11 +318,34 @@ asv_status sci_verify(const void* draft_logits, const void* target_logits, int d
                        out_accept_len, out_tokens, out_jsd, out_T, out_req_status, workspace, ws_bytes, stream);
 }
 
+static asv_status sci_run(const void* draft_logits, const void* target_logits, int dtype, const int32_t* draft_ids,
+                          int B, int K, int V, const asv_sci_params* params, const asv_sci_stabilisers* stab,
+                          double* r_hat, asv_sci_state* state, int prehit, int32_t* out_accept_len,
+                          int32_t* out_tokens, float* out_jsd, float* out_T, uint32_t* out_req_status,
+                          void* workspace, size_t ws_bytes, cudaStream_t stream);
+
 asv_status sci_verify_ex(const void* draft_logits, const void* target_logits, int dtype, const int32_t* draft_ids,
                          int B, int K, int V, const asv_sci_params* params, const asv_sci_stabilisers* stab,
                          double* r_hat, asv_sci_state* state, int32_t* out_accept_len, int32_t* out_tokens,
                          float* out_jsd, float* out_T, uint32_t* out_req_status, void* workspace, size_t ws_bytes,
                          cudaStream_t stream) {
+  return sci_run(draft_logits, target_logits, dtype, draft_ids, B, K, V, params, stab, r_hat, state, 0,
+                 out_accept_len, out_tokens, out_jsd, out_T, out_req_status, workspace, ws_bytes, stream);
+}
+
+asv_status sci_verify_prehit(const void* draft_logits, const void* target_logits, int dtype, const int32_t* draft_ids,
+                             int B, int K, int V, const asv_sci_params* params, double* r_hat, int32_t* out_accept_len,
+                             int32_t* out_tokens, float* out_jsd, float* out_T, uint32_t* out_req_status,
+                             void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  return sci_run(draft_logits, target_logits, dtype, draft_ids, B, K, V, params, nullptr, r_hat, nullptr, 1,
+                 out_accept_len, out_tokens, out_jsd, out_T, out_req_status, workspace, ws_bytes, stream);
+}
+
+static asv_status sci_run(const void* draft_logits, const void* target_logits, int dtype, const int32_t* draft_ids,
+                          int B, int K, int V, const asv_sci_params* params, const asv_sci_stabilisers* stab,
+                          double* r_hat, asv_sci_state* state, int prehit, int32_t* out_accept_len,
+                          int32_t* out_tokens, float* out_jsd, float* out_T, uint32_t* out_req_status,
+                          void* workspace, size_t ws_bytes, cudaStream_t stream) {
   if (B < 0 || K < 1 || V < 2) return ASV_ERR_SHAPE;
   if ((long long)B * (K + 1) * asv::kMaxCluster > 0x7fffffffLL) return ASV_ERR_SHAPE;
   if (!valid_dtype(dtype)) return ASV_ERR_DTYPE;
@@ -342,6 +386,7 @@ asv_status sci_verify_ex(const void* draft_logits, const void* target_logits, in
   args.T_max = P.T_max;
   args.ewma_beta = P.ewma_beta;
   args.r_hat = r_hat;
+  args.prehit_phase = prehit;
   if (stab) {
     args.sci_state = reinterpret_cast<asv::SciState*>(state);
     args.hyst = stab->hysteresis;

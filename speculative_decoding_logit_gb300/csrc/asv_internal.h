@@ -79,6 +79,9 @@ struct JsdArgs {
   // SCI
   double T_base, alpha_omega, tau_credit, T_min, T_max, ewma_beta;
   double* r_hat;
+  // E2-SCI pre-hit: 0 off; 1 row 0 of every request; 2 rows 1..K of requests not dropped
+  int prehit_phase;
+  uint32_t* dropped;  // [B] 1 when phase 1 dropped the request's window
   // SCI stabilisers (state == nullptr: off)
   SciState* sci_state;
   double hyst, fb_acc, fb_T;

@@ -317,8 +317,17 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
   const int warp = tid >> 5;
   const uint32_t rank = cluster_rank();
   const uint32_t C = cluster_size();
-  const int row = blockIdx.x / C;
   const int R1 = p.K + 1;
+  // Rows: one per cluster.  E2-SCI pre-hit: phase 1 takes row 0 of every request, phase 2 rows
+  // 1..K of every request, skipping requests that phase 1 dropped (the whole cluster returns).
+  int row = blockIdx.x / C;
+  if (MODE == kModeSci && p.prehit_phase == 1) {
+    row *= R1;
+  } else if (MODE == kModeSci && p.prehit_phase == 2) {
+    const int rq = row / p.K;
+    if (*reinterpret_cast<const volatile uint32_t*>(p.dropped + rq)) return;
+    row = rq * R1 + 1 + (row - rq * p.K);
+  }
   const int req = row / R1;
   const int pos = row - req * R1;
   const int V = p.V;
@@ -761,6 +770,34 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
   }
   if (lane == 0 && p.out_D) p.out_D[row] = finite ? D : __int_as_float(0x7fc00000);
   if (MODE == kModeAsym && p.out_lse && lane < NT) p.out_lse[size_t(row) * 3 + lane] = float(my_lse);
+  if (MODE == kModeSci && p.prehit_phase == 1) {
+    // Pre-hit: the window is dropped when its first draft fails the threshold (or row 0 is not
+    // finite, or a draft id is out of range); the request then finishes here with n = 0.
+    double thr = __dadd_rn(p.T_base, __dmul_rn(p.alpha_omega, __dsub_rn(p.r_hat[req], p.tau_credit)));
+    thr = fmax(p.T_min, fmin(thr, p.T_max));
+    const int32_t* dr = p.draft_ids + size_t(req) * K;
+    bool bad = false;
+    for (int i = lane; i < K; i += 32) bad = bad || dr[i] < 0 || dr[i] >= V;
+    bad = __any_sync(kAll, bad);
+    const bool drop = !finite || bad || double(D) > thr;
+    if (drop) {
+      const uint32_t status = (finite ? 0u : 1u) | (bad ? 2u : 0u);
+      int32_t* toks = p.out_tokens + size_t(req) * R1;
+      const int tok0 = (rc.rowi[0] == INT_MAX) ? 0 : rc.rowi[0];
+      for (int i = lane; i < R1; i += 32) toks[i] = status ? -1 : (i == 0 ? tok0 : -1);
+      if (lane == 0) {
+        if (p.out_T) p.out_T[req] = float(thr);
+        if (!status) {
+          const double pacc = 0.0;
+          p.r_hat[req] = __dadd_rn(__dmul_rn(__dsub_rn(1.0, p.ewma_beta), p.r_hat[req]), __dmul_rn(p.ewma_beta, pacc));
+        }
+        p.out_accept_len[req] = 0;
+        p.out_req_status[req] = status;
+        p.dropped[req] = 1u;
+      }
+      return;
+    }
+  }
   uint32_t ticket = 0;
   if (lane == 0) {
     RowRecord rec;
@@ -1007,7 +1044,11 @@ cudaError_t launch_jsd_family(int mode, int dtype, const JsdArgs& a, const Launc
   cudaError_t e = prepare(kern, plan);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
-  const unsigned grid = unsigned(a.B) * unsigned(a.K + 1) * unsigned(plan.cluster);
+  // Rows launched: every row, or (E2-SCI pre-hit) row 0 of each request, then rows 1..K.
+  const unsigned rows = a.prehit_phase == 1 ? unsigned(a.B)
+                        : a.prehit_phase == 2 ? unsigned(a.B) * unsigned(a.K)
+                                              : unsigned(a.B) * unsigned(a.K + 1);
+  const unsigned grid = rows * unsigned(plan.cluster);
   cudaLaunchConfig_t cfg = make_config(plan, grid, s, attr);
   return cudaLaunchKernelEx(&cfg, kern, a);
 }

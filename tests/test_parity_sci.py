@@ -110,3 +110,42 @@ def test_stabilised_windows(asv):
         applied_fallback += int(np.isclose(ref.T, 0.12).sum())
         r_ref = ref.r_hat
     assert applied_fallback > 0  # the fallback path ran
+
+
+@pytest.mark.parametrize("dtype,V", [(gen.F32, 2048), (gen.BF16, 8192), (gen.F32, 1001)])
+def test_prehit_equals_full_window(asv, dtype, V):
+    """First-token pre-hit: a window whose first draft fails is dropped without reading its later
+    rows; for finite inputs the decisions, tokens, thresholds and credit equal the full window's."""
+    B, K = 32, 6
+    rng = np.random.default_rng(V)
+    batch = gen.make_asymspec_batch("spiky", 1200 + V, B, K, V, dtype)
+    r0 = rng.uniform(0.0, 1.0, B)
+    p = asv.SciParams(alpha_omega=1.0)   # thresholds spread over [0.1, 0.6]
+    op = oracle.SciParams(p.T_base, p.alpha_omega, p.tau_credit, p.T_min, p.T_max, p.ewma_beta)
+    r_gpu = torch.from_numpy(r0.copy()).cuda()
+    out = asv.sci_verify(to_device(batch.a, batch.dtype), to_device(batch.t, batch.dtype),
+                         torch.from_numpy(batch.drafts).cuda(), r_gpu, p, prehit=True)
+    torch.cuda.synchronize()
+    ref = oracle.sci_verify(batch.a, batch.t, batch.drafts, r0, op)
+    st = out.req_status.cpu().numpy().astype(np.uint32)
+    np.testing.assert_array_equal(st & 3, ref.flags & 3)
+    acc = out.accept_len.cpu().numpy()
+    tok = out.tokens.cpu().numpy()
+    jsd = out.jsd.cpu().numpy()
+    r_new = r_gpu.cpu().numpy()
+    dropped = graded = 0
+    for r in range(B):
+        if ref.flags[r] & oracle.FLAGS_UNGRADED:
+            continue
+        graded += 1
+        assert acc[r] == ref.accept_len[r]
+        np.testing.assert_array_equal(tok[r], ref.tokens[r])
+        assert r_new[r] == pytest.approx(ref.r_hat[r], abs=1e-15)
+        cols = 1 if ref.accept_len[r] == 0 else K + 1   # a dropped window has only row 0's J
+        dropped += int(ref.accept_len[r] == 0)
+        np.testing.assert_allclose(jsd[r, :cols], ref.jsd[r, :cols], atol=tol(dtype), rtol=0)
+    np.testing.assert_allclose(out.T.cpu().numpy(), ref.T, atol=1e-7)
+    assert graded >= B - 4 and dropped >= 3
+    # the workspace is left zeroed (the drop flags are cleared)
+    for buf in asv._binding._ws_cache.values():
+        assert int(torch.count_nonzero(buf)) == 0
