@@ -331,6 +331,7 @@ def run_workload(args):
                            torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev))
     R = w.B * (w.K + 1)
     extra = {}
+    per_step = 2 if w.mode == "rapid" else 1  # RAPID: verification launch + draw launch
     if w.mode == "rapid":
         b = gen.make_rapid_batch(w.seed, w.B, w.K, w.V)
         sets = [(todev(b.z, gen.F32), todev(b.q, gen.F32)) for _ in range(3)]
@@ -339,7 +340,7 @@ def run_workload(args):
         step_bytes = 2 * R * w.V * 4
         call = lambda i: asv.rapid_verify(*sets[i % 3], d, w.params["T"], eta, w.params["tail_frac"],
                                           w.params["philox_seed"])
-        dtype, kernel = "f32", "rapid_kernel"
+        dtype, kernel = "f32", "rapid_kernel + rapid_draw_kernel"
         extra = {"eta": eta, "sets": 3}
     else:
         # Generated requests tiled along the batch when the workload is large (the kernel's work per
@@ -404,7 +405,7 @@ def run_workload(args):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_kind": peak_kind,
                          "kernel_ms": launch_ms, "algorithmic_bytes_per_launch": step_bytes},
-            "gpu_launches": args.steps, "clocks": clk}
+            "gpu_launches": per_step * args.steps, "clocks": clk}
     print(json.dumps(line), flush=True)
     return 0
 

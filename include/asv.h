@@ -28,9 +28,10 @@
  *    (ASV_REQ_* bits); a flagged request gets accept length 0 and tokens -1.
  *  - Output tokens per request: the accepted drafts, then one token chosen by the
  *    verifier at the first rejection (or at the bonus position), then -1 padding.
- *  - Rows are processed by thread-block clusters; rows whose base address is
- *    16-byte aligned (V * element size a multiple of 16 and 16-byte aligned base
- *    pointers) are staged with bulk copies, others with ordinary loads.
+ *  - Rows are processed by thread-block clusters that stream them; rows whose
+ *    base address is 16-byte aligned (V * element size a multiple of 16 and
+ *    16-byte aligned base pointers) are read with 16-byte vector loads, others
+ *    with element loads.
  *  - `workspace` is device scratch of at least asv_workspace_bytes(...) bytes.
  *    It must be zero-filled before its first use (asv_workspace_init does that);
  *    every call leaves it zero-filled again.  Two calls that may run at the
@@ -74,7 +75,7 @@ typedef enum {
 /* Per-request status bits written by the kernels (never a trap). */
 #define ASV_REQ_NONFINITE 1u /* a row holds NaN or +inf, or is entirely -inf */
 #define ASV_REQ_BAD_DRAFT 2u /* a draft id lies outside [0, V) */
-#define ASV_REQ_TIMEOUT 4u   /* a bounded wait for staged data expired; outputs invalid */
+#define ASV_REQ_TIMEOUT 4u   /* reserved: a bounded wait expired (no current kernel waits on data) */
 
 /* Human-readable name of a status code (static string). */
 const char* asv_status_string(asv_status s);
@@ -89,14 +90,15 @@ size_t asv_workspace_bytes(int mode, int B, int K, int V, int dtype);
 asv_status asv_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
- * Tuning override for the launch plan: cluster size (CTAs per row, 1..16) and
- * threads per CTA (128..512, multiple of 32).  0 restores the automatic choice.
- * Applies to later calls from any thread.
+ * Tuning override for the launch plan: cluster size (CTAs per row, 1..16; 0
+ * restores the automatic choice).  threads_per_cta must be 0 or 256, the size
+ * the kernels are compiled for (anything else is ASV_ERR_PARAM).  Applies to
+ * later calls from any thread.
  */
 asv_status asv_set_tuning(int cluster_ctas, int threads_per_cta);
 
 /* The plan the next call with these shapes would use (cluster size, threads, dynamic
- * shared memory bytes, 1 if rows are staged with bulk copies) and how many of its clusters
+ * shared memory bytes, 1 if rows take 16-byte vector loads) and how many of its clusters
  * the device can hold at once (cudaOccupancyMaxActiveClusters).  Any output may be NULL. */
 asv_status asv_query_plan(int mode, int B, int K, int V, int dtype, int* cluster_ctas, int* threads_per_cta,
                           int* smem_bytes, int* bulk_copy, int* max_active_clusters);

@@ -1,5 +1,6 @@
 // asv_api.cu -- the extern "C" entry points declared in include/asv.h: argument validation,
 // workspace layout, launch planning (cluster size, threads, shared memory) and dispatch.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -16,7 +17,6 @@ namespace {
 
 thread_local int g_last_cuda_error = 0;
 std::atomic<int> g_tune_cluster{0};
-std::atomic<int> g_tune_threads{0};
 
 asv_status cuda_fail(cudaError_t e) {
   g_last_cuda_error = int(e);
@@ -25,8 +25,6 @@ asv_status cuda_fail(cudaError_t e) {
 
 struct DevInfo {
   int sms = 0;
-  int smem_block_optin = 0;
-  int smem_sm = 0;
 };
 
 constexpr int kMaxDevices = 64;
@@ -42,10 +40,6 @@ cudaError_t dev_info(DevInfo* out) {
   DevInfo& d = g_dev[dev];
   if (d.sms == 0) {
     if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&d.smem_block_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
-      return e;
-    if ((e = cudaDeviceGetAttribute(&d.smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess)
-      return e;
   }
   *out = d;
   return cudaSuccess;
@@ -65,86 +59,62 @@ size_t record_bytes(int mode) {
   return sizeof(asv::RowRecord);
 }
 
-// Launch plan.  Each CTA stages NT slices of n_slice entries.  Choose the smallest cluster
-// size whose staging lets two CTAs share an SM (so one CTA's copies overlap another's
-// arithmetic), then widen it while the batch has fewer CTAs than twice the SM count.
-cudaError_t plan_for(int kind, int dtype, int NT, int elem_bytes, int V, long long R, bool bulk, int static_smem,
-                     LaunchPlan* out) {
-  DevInfo di;
-  cudaError_t e = dev_info(&di);
-  if (e != cudaSuccess) return e;
-  const int vec = 16 / elem_bytes;
-  const int reserve = 1024;  // per-CTA shared memory the system keeps
-  auto stage_bytes = [&](int C) {
-    const int n = int(round_up(size_t(ceil_div(V, C)), size_t(vec)));
-    return std::pair<int, int>(n, int(NT * round_up(size_t(n) * elem_bytes, 128)));
-  };
+// Cluster size for the streaming kernels, which stage nothing, so `ctas_per_sm` CTAs (their
+// launch bounds) share an SM and each pass re-reads its slice from L2.  The smallest C whose R*C
+// CTAs fill at least 90% of one wave of resident CTAs and whose last wave is at least 85% full --
+// fewer CTAs per row mean fewer cluster exchanges, while a partly empty last wave leaves SMs idle.
+// A batch too small to fill a wave even at C = 16 takes the largest C (at least 1024 entries per
+// CTA).  A tuning override replaces the choice.
+int wave_fill_cluster(int V, long long R, int ctas_per_sm, int sms) {
   int C = g_tune_cluster.load();
-  if (C <= 0) {
-    int c_fit = 0, c_two = 0;
-    for (int c = 1; c <= asv::kMaxCluster; ++c) {
-      const int sb = stage_bytes(c).second + static_smem;
-      if (sb <= di.smem_block_optin && !c_fit) c_fit = c;
-      if (2 * (sb + reserve) <= di.smem_sm && !c_two) c_two = c;
-    }
-    C = c_two ? c_two : c_fit;
-    if (C == 0) return cudaErrorInvalidValue;  // V too large for one cluster
-    const long long want = 2LL * di.sms;
-    if (R * C < want) {
-      int c_more = int((want + R - 1) / R);
-      c_more = std::min(c_more, asv::kMaxCluster);
-      c_more = std::min(c_more, std::max(1, V / 1024));
-      C = std::max(C, c_more);
-    }
+  if (C > 0) return C;
+  const int c_max = std::max(1, std::min(asv::kMaxCluster, V / 1024));
+  const double resident = double(ctas_per_sm) * sms;
+  for (int c = 1; c <= c_max; ++c) {
+    const double waves = double(R) * c / resident;
+    if (waves < 0.9) continue;
+    if (waves / std::ceil(waves) >= 0.85) return c;
   }
-  const auto sb = stage_bytes(C);
-  if (sb.second + static_smem > di.smem_block_optin) return cudaErrorInvalidValue;
-  int threads = g_tune_threads.load();
-  if (threads <= 0) {
-    const int nvec = sb.first / vec;
-    threads = nvec >= 2048 ? 512 : (nvec >= 512 ? 256 : 128);
-  }
-  out->cluster = C;
-  out->threads = threads;
-  out->n_slice = sb.first;
-  out->smem = sb.second;
-  out->bulk = bulk ? 1 : 0;
-  (void)kind;
-  (void)dtype;
-  return cudaSuccess;
+  return c_max;
 }
 
-// Plan for the streaming AsymSpec / SCI kernel.  It stages nothing, so a CTA needs only
-// registers and jsd_ctas_per_sm() CTAs share an SM (its launch bounds); pass B re-reads the
-// divergence pair from L2.  Cluster size: the smallest C whose R*C CTAs fill at least 90% of one wave of resident CTAs
-// and whose last wave is at least 85% full -- fewer CTAs per row mean fewer cluster exchanges,
-// while a partly empty last wave leaves SMs idle.  A batch too small to fill a wave even at C = 16
-// takes the largest C (at least 1024 entries per CTA).
+// Plan for the AsymSpec / SCI kernel.
 cudaError_t plan_jsd(int elem_bytes, int V, long long R, bool aligned, LaunchPlan* out) {
   DevInfo di;
   cudaError_t e = dev_info(&di);
   if (e != cudaSuccess) return e;
   const int vec = 16 / elem_bytes;
-  int C = g_tune_cluster.load();
-  if (C <= 0) {
-    const int c_max = std::max(1, std::min(asv::kMaxCluster, V / 1024));
-    const double resident = double(asv::jsd_ctas_per_sm()) * di.sms;
-    C = c_max;
-    for (int c = 1; c <= c_max; ++c) {
-      const double waves = double(R) * c / resident;
-      if (waves < 0.9) continue;
-      if (waves / std::ceil(waves) >= 0.85) {
-        C = c;
-        break;
-      }
-    }
-  }
+  const int C = wave_fill_cluster(V, R, asv::jsd_ctas_per_sm(), di.sms);
   out->cluster = C;
   out->threads = asv::jsd_threads();
   out->n_slice = int(round_up(size_t(ceil_div(V, C)), size_t(vec)));
   out->smem = 0;
   out->bulk = aligned ? 1 : 0;
   return cudaSuccess;
+}
+
+// Plan for the RAPID kernel (fp32 rows, four entries per 16-byte vector).
+cudaError_t plan_rapid(int V, long long R, bool aligned, LaunchPlan* out) {
+  DevInfo di;
+  cudaError_t e = dev_info(&di);
+  if (e != cudaSuccess) return e;
+  const int C = wave_fill_cluster(V, R, asv::rapid_ctas_per_sm(), di.sms);
+  out->cluster = C;
+  out->threads = asv::rapid_threads();
+  out->n_slice = int(round_up(size_t(ceil_div(V, C)), 4));
+  out->smem = 0;
+  out->bulk = aligned ? 1 : 0;
+  return cudaSuccess;
+}
+
+// CTAs per request of the RAPID draw launch: about four waves of resident CTAs over the batch's
+// requests (the draw is arithmetic-bound: Philox, a logarithm and a division per entry), at least
+// 1024 entries per CTA.
+int rapid_draw_ctas(int V, int B) {
+  DevInfo di;
+  const int sms = dev_info(&di) == cudaSuccess ? di.sms : 1;
+  const long long want = (4LL * asv::rapid_ctas_per_sm() * sms + B - 1) / std::max(B, 1);
+  return int(std::max(1LL, std::min<long long>(want, std::max(1, V / 1024))));
 }
 
 bool valid_dtype(int dt) { return dt == ASV_F32 || dt == ASV_BF16; }
@@ -181,6 +151,7 @@ size_t asv_workspace_bytes(int mode, int B, int K, int V, int dtype) {
   (void)dtype;
   if (B < 0 || K < 0) return 0;
   if (mode == ASV_MODE_SCI) return records_end(mode, B, K) + size_t(B) * 4;
+  if (mode == ASV_MODE_RAPID) return records_end(mode, B, K) + size_t(B) * sizeof(asv::RapidJob);
   return tickets_bytes(B) + size_t(B) * size_t(K + 1) * record_bytes(mode);
 }
 
@@ -192,10 +163,8 @@ asv_status asv_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t str
 
 asv_status asv_set_tuning(int cluster_ctas, int threads_per_cta) {
   if (cluster_ctas < 0 || cluster_ctas > asv::kMaxCluster) return ASV_ERR_PARAM;
-  if (threads_per_cta != 0 && (threads_per_cta < 128 || threads_per_cta > 512 || threads_per_cta % 32))
-    return ASV_ERR_PARAM;
+  if (threads_per_cta != 0 && threads_per_cta != asv::jsd_threads()) return ASV_ERR_PARAM;
   g_tune_cluster.store(cluster_ctas);
-  g_tune_threads.store(threads_per_cta);
   return ASV_OK;
 }
 
@@ -208,7 +177,7 @@ asv_status asv_query_plan(int mode, int B, int K, int V, int dtype, int* cluster
   const bool bulk = (size_t(V) * eb) % 16 == 0;
   LaunchPlan pl;
   cudaError_t e = mode == ASV_MODE_RAPID
-                      ? plan_for(mode, dtype, 2, eb, V, (long long)B * (K + 1), bulk, asv::rapid_static_smem_bytes(), &pl)
+                      ? plan_rapid(V, (long long)B * (K + 1), bulk, &pl)
                       : plan_jsd(eb, V, (long long)B * (K + 1), bulk, &pl);
   if (e == cudaErrorInvalidValue) return ASV_ERR_SHAPE;
   if (e != cudaSuccess) return cuda_fail(e);
@@ -612,8 +581,7 @@ asv_status rapid_verify_ex(const float* z, const float* q, const int32_t* draft_
   if (ws_bytes < asv_workspace_bytes(ASV_MODE_RAPID, B, G, V, ASV_F32)) return ASV_ERR_WORKSPACE;
   bool bulk = (size_t(V) * 4) % 16 == 0 && aligned(z, 16) && aligned(q, 16);
   LaunchPlan pl;
-  cudaError_t e = plan_for(ASV_MODE_RAPID, ASV_F32, 2, 4, V, (long long)B * (G + 1), bulk,
-                           asv::rapid_static_smem_bytes(), &pl);
+  cudaError_t e = plan_rapid(V, (long long)B * (G + 1), bulk, &pl);
   if (e == cudaErrorInvalidValue) return ASV_ERR_SHAPE;
   if (e != cudaSuccess) return cuda_fail(e);
   asv::RapidArgs a;
@@ -640,6 +608,8 @@ asv_status rapid_verify_ex(const float* z, const float* q, const int32_t* draft_
   a.out_req_status = out_req_status;
   a.tickets = reinterpret_cast<uint32_t*>(workspace);
   a.records = reinterpret_cast<asv::RapidRecord*>(static_cast<char*>(workspace) + tickets_bytes(B));
+  a.jobs = reinterpret_cast<asv::RapidJob*>(static_cast<char*>(workspace) + records_end(ASV_MODE_RAPID, B, G));
+  a.draw_ctas = rapid_draw_ctas(V, B);
   e = asv::launch_rapid(a, pl, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   return ASV_OK;

@@ -1,7 +1,7 @@
 // asv_device.cuh -- device-side building blocks shared by the verification kernels:
-// inline-PTX wrappers for mbarriers, 1-D bulk copies (global -> shared), thread-block
-// cluster barriers and distributed shared memory, the special-function unit's
-// exp2/log2, bf16 unpacking, and warp-level reductions.
+// inline-PTX wrappers for L2 cache policies, GPU-scope release/acquire, thread-block
+// cluster barriers and distributed shared memory, the special-function unit's exp2/log2,
+// bf16 unpacking, packed fp32 arithmetic, compensated sums, Philox and warp reductions.
 #pragma once
 
 #include <cstdint>
@@ -14,9 +14,6 @@ namespace asv {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2f = 0.6931471805599453f;
 constexpr double kLn2 = 0.69314718055994530942;
-constexpr int kNumChunks = 4;                 // RAPID: bulk-copy chunks per staged slice (one mbarrier each)
-constexpr uint32_t kWaitPolls = 1u << 16;     // try_wait attempts before a staged-data wait gives up
-constexpr uint32_t kWaitSuspendNs = 100000u;  // each attempt may sleep up to 100 us (woken by completion)
 
 // Row record bits (workspace).
 constexpr uint32_t kBitNonfinite = 1u;
@@ -28,33 +25,7 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// ------------------------------------------------------------------ mbarrier + bulk copy
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-// Arrival without a transaction count (completes the phase of a count-1 barrier).
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-// 1-D bulk copy global -> this CTA's shared memory; completion is counted in bytes on `bar`.
-// dst, src and bytes must be multiples of 16.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
+// ------------------------------------------------------------------ L2 cache policies
 
 // L2 policy that marks lines for early eviction (data read for the last time).
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -68,32 +39,6 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   return pol;
-}
-
-// bulk_g2s with an L2 cache policy.
-__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
-                                              uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
-      : "memory");
-}
-
-// Bounded wait for phase `parity` of `bar`: each attempt sleeps until the phase completes or the
-// suspend-time hint elapses, so waiting warps do not spin on the issue slots.  Returns false if
-// `polls` attempts all expired (at most polls * kWaitSuspendNs).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t polls) {
-  for (uint32_t i = 0; i < polls; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(bar), "r"(parity), "r"(kWaitSuspendNs)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
 }
 
 // ------------------------------------------------------------------ GPU-scope synchronisation
@@ -229,61 +174,6 @@ struct bf16_t {
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-template <typename T>
-struct Elem;
-
-template <>
-struct Elem<float> {
-  using storage = float;
-  static constexpr int kVec = 4;  // elements per 16-byte vector
-  __device__ static __forceinline__ void load_vec(const float* s, int vi, float (&x)[4]) {
-    const float4 v = reinterpret_cast<const float4*>(s)[vi];
-    x[0] = v.x;
-    x[1] = v.y;
-    x[2] = v.z;
-    x[3] = v.w;
-  }
-  static constexpr int kPairs = 2;
-  __device__ static __forceinline__ void load_pairs(const float* s, int vi, float2 (&x)[2]) {
-    const float4 v = reinterpret_cast<const float4*>(s)[vi];
-    x[0] = make_float2(v.x, v.y);
-    x[1] = make_float2(v.z, v.w);
-  }
-  __device__ static __forceinline__ float to_float(float v) { return v; }
-  __device__ static __forceinline__ float neg_inf() { return __uint_as_float(0xff800000u); }
-  __device__ static __forceinline__ float from_smem_remote(uint32_t a) { return dsmem_ld_f32(a); }
-};
-
-template <>
-struct Elem<bf16_t> {
-  using storage = uint16_t;
-  static constexpr int kVec = 8;
-  __device__ static __forceinline__ void load_vec(const uint16_t* s, int vi, float (&x)[8]) {
-    const uint4 v = reinterpret_cast<const uint4*>(s)[vi];
-    x[0] = bf16_lo(v.x);
-    x[1] = bf16_hi(v.x);
-    x[2] = bf16_lo(v.y);
-    x[3] = bf16_hi(v.y);
-    x[4] = bf16_lo(v.z);
-    x[5] = bf16_hi(v.z);
-    x[6] = bf16_lo(v.w);
-    x[7] = bf16_hi(v.w);
-  }
-  static constexpr int kPairs = 4;
-  __device__ static __forceinline__ void load_pairs(const uint16_t* s, int vi, float2 (&x)[4]) {
-    const uint4 v = reinterpret_cast<const uint4*>(s)[vi];
-    x[0] = make_float2(bf16_lo(v.x), bf16_hi(v.x));
-    x[1] = make_float2(bf16_lo(v.y), bf16_hi(v.y));
-    x[2] = make_float2(bf16_lo(v.z), bf16_hi(v.z));
-    x[3] = make_float2(bf16_lo(v.w), bf16_hi(v.w));
-  }
-  __device__ static __forceinline__ float to_float(uint16_t v) { return __uint_as_float(uint32_t(v) << 16); }
-  __device__ static __forceinline__ uint16_t neg_inf() { return uint16_t(0xff80u); }
-  __device__ static __forceinline__ float from_smem_remote(uint32_t a) {
-    return __uint_as_float(uint32_t(dsmem_ld_u16(a)) << 16);
-  }
-};
 
 // ------------------------------------------------------------------ warp reductions
 

@@ -45,6 +45,23 @@ struct __align__(32) RapidRecord {
   uint32_t pad[2];
 };
 
+// RAPID: the draw the verification's scan leaves for the draw launch (one per request): the stop
+// row and its record's row constants, then the draw launch's own race slots and counter.
+struct __align__(64) RapidJob {
+  float zs_max;
+  float inv_sum;
+  float zhat_max;
+  float head_scale;
+  float tail_scale;
+  int32_t row;      // stop position n (residual draw if n < G, bonus draw if n == G)
+  uint32_t active;  // 1 while the draw is pending
+  uint32_t ticket;  // CTAs of the draw launch done with this request
+  // Race winners as ~((key bits << 32) | index), combined with atomic max (zero = none yet):
+  // [0] the residual (bonus position: the protected target), [1] p, used if [0] has no entry.
+  unsigned long long slot[2];
+  uint32_t pad[4];
+};
+
 // Per-request E2-SCI stabiliser state (layout of asv_sci_state).
 struct __align__(16) SciState {
   double T_applied;
@@ -117,17 +134,18 @@ struct RapidArgs {
   uint32_t* out_req_status;
   uint32_t* tickets;
   RapidRecord* records;
+  RapidJob* jobs;
+  int draw_ctas;  // CTAs per request of the draw launch
 };
 
 // Kernel launchers (return the cudaError_t of the launch).
 cudaError_t launch_jsd_family(int mode, int dtype, const JsdArgs& args, const LaunchPlan& plan, cudaStream_t s);
 cudaError_t launch_rapid(const RapidArgs& args, const LaunchPlan& plan, cudaStream_t s);
 
-// Static shared memory the kernels use beside the dynamic staging area.
-int jsd_static_smem_bytes();
 int jsd_threads();      // threads per CTA of the AsymSpec / SCI kernel
 int jsd_ctas_per_sm();  // CTAs of it that share an SM (its launch bounds)
-int rapid_static_smem_bytes();
+int rapid_threads();      // threads per CTA of the RAPID kernel
+int rapid_ctas_per_sm();  // CTAs of it that share an SM (its launch bounds)
 
 // Occupancy query: clusters of `plan` that can be resident at once (0 = cannot launch).
 int jsd_max_active_clusters(int mode, int dtype, const LaunchPlan& plan);

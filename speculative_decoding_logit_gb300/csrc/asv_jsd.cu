@@ -986,7 +986,6 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
   }
 }
 
-int jsd_static_smem_bytes() { return 0; }
 int jsd_threads() { return kJsdThreads; }
 int jsd_ctas_per_sm() { return kJsdCtasPerSm; }
 

@@ -6,22 +6,41 @@
 // whose augmented probability is below 10% of the peak keep the original target probability);
 // Key design 4 (at a rejection the token is drawn from norm(max(p - phat, p - q, 0))).
 //
-// Decomposition as in the AsymSpec kernel: a cluster of C CTAs per row, each CTA staging its slice
-// of z and q in shared memory once.  Four sweeps over the staged slice, each followed by a cluster
-// exchange through distributed shared memory:
-//   1. max of z/T;  2. sum of exp(z/T - max) (and sum of q, for the finiteness check);
-//   3. max of zhat/T;  4. head sums: sum of p and of exp(zhat/T - max) over entries at or above
-//      the tail boundary zhat/T >= max + ln(tail_frac).
-// The protected target is then p on the tail and exp(zhat/T - max) * (head p-mass / head
-// exp-mass) on the head, which sums to 1 without a further normalisation pass.  The alternative
-// reading of the protection (tail_mode 1: substitute p for phat on the tail, then renormalise
-// every entry) also sums p over the tail and exp(zhat/T - max) over every entry in sweep 4; then
-// the tail is p / Z and the head phat / Z with Z = (tail p-mass) + (head phat-mass).  CTA 0 of the row
-// decides the draft's accept test u*q(d) < protected(d) (u from Philox4x32-10) and files a row
-// record.  The last row of a request to finish runs the scan and, in the same cluster, draws the
-// emitted token at the stop position with an exponential race over that row (re-read from global
-// memory, normally still in L2): argmin_k E_k / w_k, E_k = -ln u_k, with w the residual
-// max(p - protected, p - q, 0) or, at the bonus position, the protected target.
+// Decomposition as in the AsymSpec kernel: a cluster of C CTAs per row, CTA q owning entries
+// [q*n_slice, (q+1)*n_slice) of z and q.  The kernel streams; it stages nothing in shared memory:
+//   pass A  reads z and q from HBM once (16-byte loads that bypass L1, one vector prefetched):
+//           running maximum of z/T and a sum of exp(z/T - ref) against a lazily moved reference,
+//           the sum of q (finiteness), and the entries where z/T and q peak;
+//   exch 1  row maximum M and S = sum exp(z/T - M), so p = exp(z/T - M) / S from here on; a lower
+//           bound L0 on max zhat/T: zhat/T at the two peak entries;
+//   pass B  re-reads z and q (the L2 cache still holds them: evict-last in pass A) and forms p and
+//           zhat/T of every entry; running maximum of zhat/T.  An entry at or above (bound so far) +
+//           ln(tail_frac), the bound being L0 or the thread's own maximum, may lie in the head
+//           {zhat/T >= max + ln(tail_frac)}; a thread keeps up to two such candidates in registers
+//           (dropping those the rising bound excludes); a third marks its CTA.  Under the second
+//           tail reading (and for tail_frac = 0) pass B also sums p and exp(zhat/T - ref) over
+//           every entry;
+//   exch 2  row maximum Mh of zhat/T and the head boundary Mh + ln(tail_frac);
+//   head    head sums (p-mass, exp(zhat/T - Mh)-mass) over the candidates -- every head entry is a
+//           candidate, because the bound never exceeds Mh -- or, in a marked CTA, over a third read
+//           of the slice (pass C, from L2);
+//   exch 3  every CTA pushes its head sums into CTA 0 and leaves.
+// The protected target is then p on the tail and exp(zhat/T - Mh) * (head p-mass / head exp-mass)
+// on the head, which sums to 1 without a further normalisation pass.  The alternative reading of
+// the protection (tail_mode 1: substitute p for phat on the tail, then renormalise every entry)
+// makes the tail p / Z and the head phat / Z with Z = (tail p-mass) + (head phat-mass), the tail
+// p-mass being (all p-mass) - (head p-mass).  CTA 0 of the row decides the draft's accept test
+// u*q(d) < protected(d) (u from Philox4x32-10) and files a row record; the last row of a request
+// to finish runs the scan, writes the outputs and leaves a draw job (the stop row and its
+// constants).  A second launch, one cluster per request, draws the emitted token at the stop
+// position with an exponential race over that row (re-read from global memory, normally still in
+// L2): argmin_k E_k / w_k, E_k = -ln u_k, with w the residual max(p - protected, p - q, 0) or, at
+// the bonus position, the protected target.  No CTA waits on another cluster, and no CTA of the
+// verification waits for its row's finalisation.
+//
+// Every quantity of an entry (p, zhat/T, the protected value) is formed by the same sequence of
+// correctly rounded operations wherever it is needed -- pass B (two lanes per instruction), pass C,
+// the accept test and the draw (one lane) -- so the head test gives the same answer everywhere.
 #include <climits>
 
 #include "asv_device.cuh"
@@ -29,36 +48,39 @@
 
 namespace asv {
 
+constexpr int kRapidThreads = 256;    // threads per CTA (launch bounds)
+constexpr int kRapidCtasPerSm = 4;    // CTAs per SM the kernel is compiled for (launch bounds)
+constexpr float kRapidSlack = 64.0f;  // reference slack (log2 units), as in the AsymSpec kernel
+
 struct __align__(16) RapidXchg {
-  float zmax;
-  float zhmax;
-  uint32_t err;
-  uint32_t draw_active;  // set remotely by CTA 0 when this cluster draws for its request
-  float sum_e[2];   // hi, lo
-  float sum_q[2];
-  float head_p[2];
-  float head_e[2];
-  float race_key;
-  int32_t race_idx;
-  int32_t draw_row;
-  float d_zs_max;  // the drawn row's record, broadcast by CTA 0
-  float d_inv_sum;
-  float d_zhat_max;
-  float d_head_scale;
-  float d_tail_scale;
-  float tail_p[2];  // tail_mode 1: sum of p over the tail
-  float all_e[2];   // tail_mode 1: sum of exp(zhat/T - max) over every entry
+  // Exchange 1 (read by every CTA of the cluster).
+  float zmax;  // CTA maximum of z/T
+  float se[2];  // CTA sum of exp2(z/T log2e - ref(zmax)), hi + lo
+  float sq[2];  // CTA sum of q, hi + lo
+  float pk_v[2];    // peaks of z/T and of q in the CTA's slice: value,
+  int32_t pk_i[2];  // index,
+  float pk_z[2];    // z there,
+  float pk_q[2];    // q there
+  // Exchange 2.
+  float zhmax;  // CTA maximum of zhat/T (at least L0)
+  float ae[2];  // sum of exp2(zhat/T log2e - ref(zhmax)) over the slice (AE)
+  float pa[2];  // sum of p over the slice (AE)
+  // Exchange 3: pushed into CTA 0 by every CTA.  Head p-mass (hi, lo), head exp-mass (hi, lo).
+  float head[kMaxCluster][4];
 };
 
 struct RowConsts {
   float invT, etaT, ML, inv_sum, zhmax, thr, head_scale, tail_scale;
 };
 
-// Row statistics broadcast by one thread after each cluster exchange.
+// Row statistics, computed identically by warp 0 of every CTA and broadcast through shared memory.
 struct __align__(16) RapidShared {
-  float M;
-  float inv_sum;
-  float zhmax;
+  float M;        // max z/T
+  float inv_sum;  // 1 / sum exp2(z/T log2e - ML)
+  float L0;       // lower bound of max zhat/T
+  float zhmax;    // max zhat/T
+  float ae_hi, ae_lo;  // row sum of exp2(zhat/T log2e - ref(zhmax)) (AE)
+  float pa_hi, pa_lo;  // row sum of p (AE)
   int32_t finite;
 };
 
@@ -68,31 +90,84 @@ __device__ __forceinline__ float warp_sum_f(float v) {
   return v;
 }
 
-// p, zhat/T and the protected target of one entry, recomputed identically everywhere.
-__device__ __forceinline__ void rapid_entry(float z, float q, const RowConsts& c, float& p, float& zhs, float& prot) {
-  const float zs = z * c.invT;
-  p = ex2_approx(fmaf(zs, kLog2e, -c.ML)) * c.inv_sum;
-  const float zh = fmaf(c.etaT, q - p, z);
-  zhs = zh * c.invT;
-  prot = (zhs < c.thr) ? p * c.tail_scale : ex2_approx((zhs - c.zhmax) * kLog2e) * c.head_scale;
+__device__ __forceinline__ float ref_of(float M) { return isfinite(M) ? M * kLog2e : 0.0f; }
+
+// Argmax over a warp carrying two payload values with the winner (larger value; ties: lower index).
+__device__ __forceinline__ void warp_argmax_pl(float& v, int& i, float& a, float& b) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    const float oa = __shfl_xor_sync(0xffffffffu, a, o);
+    const float ob = __shfl_xor_sync(0xffffffffu, b, o);
+    if (ov > v || (ov == v && oi < i)) {
+      v = ov;
+      i = oi;
+      a = oa;
+      b = ob;
+    }
+  }
 }
 
-__global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
+// p and zhat/T of one entry.  Explicitly rounded operations (no contraction), matching the
+// two-lane forms of pass B bit for bit.
+__device__ __forceinline__ void rapid_p_zhs(float z, float q, const RowConsts& c, float& p, float& zhs) {
+  const float zs = __fmul_rn(z, c.invT);
+  p = __fmul_rn(ex2_approx(__fmaf_rn(zs, kLog2e, -c.ML)), c.inv_sum);
+  zhs = __fmul_rn(__fmaf_rn(c.etaT, __fsub_rn(q, p), z), c.invT);
+}
+
+// exp(zhat/T - Mh): the head weight.
+__device__ __forceinline__ float head_exp(float zhs, float zhmax) {
+  return ex2_approx(__fmul_rn(__fsub_rn(zhs, zhmax), kLog2e));
+}
+
+// p, zhat/T and the protected target of one entry.
+__device__ __forceinline__ void rapid_entry(float z, float q, const RowConsts& c, float& p, float& zhs, float& prot) {
+  rapid_p_zhs(z, q, c, p, zhs);
+  prot = (zhs < c.thr) ? __fmul_rn(p, c.tail_scale) : __fmul_rn(head_exp(zhs, c.zhmax), c.head_scale);
+}
+
+// Four entries [k, k+4) of a row slice: one 16-byte load with an L2 policy when the slice is
+// aligned, else element loads with `pad` at and beyond `lim`.
+__device__ __forceinline__ float4 ld4(const float* base, int k, int lim, bool aligned, uint64_t pol, float pad) {
+  float4 v;
+  if (aligned) {
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "l"(base + k), "l"(pol));
+    return v;
+  }
+  v.x = (k + 0 < lim) ? __ldg(base + k + 0) : pad;
+  v.y = (k + 1 < lim) ? __ldg(base + k + 1) : pad;
+  v.z = (k + 2 < lim) ? __ldg(base + k + 2) : pad;
+  v.w = (k + 3 < lim) ? __ldg(base + k + 3) : pad;
+  return v;
+}
+
+// Two-lane p and zhat/T of the pairs (z, q) -- the operations of rapid_p_zhs, lane by lane.
+__device__ __forceinline__ void pzhs2(float2 z, float2 q, float2 invT2, float2 nML2, float2 inv2, float2 etaT2,
+                                      float2& pk, float2& zh) {
+  const float2 zs = fmul2(z, invT2);
+  const float2 y = ffma2(zs, make_float2(kLog2e, kLog2e), nML2);
+  pk = fmul2(make_float2(ex2_approx(y.x), ex2_approx(y.y)), inv2);
+  zh = fmul2(ffma2(etaT2, fsub2(q, pk), z), invT2);
+}
+
+// AE: the second tail reading (or tail_frac = 0) needs the all-entry sums of p and exp(zhat/T).
+template <bool ALIGNED, bool AE>
+__global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(const RapidArgs p) {
   constexpr int VEC = 4;
-  extern __shared__ __align__(128) unsigned char smem_raw[];
+  constexpr int kWarps = kRapidThreads / 32;
   __shared__ RapidXchg xchg;
   __shared__ RapidShared rs;
-  __shared__ float s_wf[32];
-  __shared__ int32_t s_wi[32];
-  __shared__ float s_w2[32][2];
-  __shared__ __align__(8) uint64_t s_bar[kNumChunks];
-  __shared__ uint32_t s_err;
+  __shared__ float s_w[kWarps][4];
+  __shared__ float s_pv[kWarps][2], s_pz[kWarps][2], s_pq[kWarps][2];
+  __shared__ int32_t s_pi[kWarps][2];
 
   const int tid = threadIdx.x;
-  const int nthr = blockDim.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int nwarps = nthr >> 5;
   const uint32_t rank = cluster_rank();
   const uint32_t C = cluster_size();
   const int row = blockIdx.x / C;
@@ -105,438 +180,693 @@ __global__ void __launch_bounds__(512) rapid_kernel(const RapidArgs p) {
   const int len = max(0, min(V - v0, p.n_slice));
   const int nvec = (len + VEC - 1) / VEC;
   const size_t row_base = size_t(row) * size_t(V);
-  const size_t stage_stride = (size_t(p.n_slice) * sizeof(float) + 127) & ~size_t(127);
-  float* zst = reinterpret_cast<float*>(smem_raw);
-  float* qst = reinterpret_cast<float*>(smem_raw + stage_stride);
-  const int chunk_vec = (nvec + kNumChunks - 1) / kNumChunks;
+  const float* zsl = p.z + row_base + v0;
+  const float* qsl = p.q + row_base + v0;
+  const uint64_t pol_keep = policy_evict_last();
+  const uint64_t pol_last = policy_evict_first();
+  const float invT = p.inv_T;
+  const float etaT = p.eta * p.T;
+  const float ln_tf = p.ln_tail_frac;
+  const bool cand_on = ln_tf > -INFINITY;  // tail_frac = 0 puts every entry in the head
+  const float2 invT2 = make_float2(invT, invT);
+  const float2 etaT2 = make_float2(etaT, etaT);
 
-  // ---------------------------------------------------------------- staging
-  if (tid == 0) {
-    s_err = 0;
-    xchg.draw_active = 0;
-#pragma unroll
-    for (int c = 0; c < kNumChunks; ++c) mbar_init(smem_addr(&s_bar[c]), 1);
-    fence_mbar_init();
+  // The draft token's z and q for the accept test in CTA 0 (loaded now, used at the end).
+  int d = -1;
+  float zd = 0.0f, qd = 0.0f;
+  if (rank == 0 && tid == 0 && pos < G) {
+    d = p.draft_ids[size_t(req) * G + pos];
+    if (d >= 0 && d < V) {
+      zd = __ldg(p.z + row_base + d);
+      qd = __ldg(p.q + row_base + d);
+    }
   }
-  __syncthreads();
-  if (p.bulk) {
-    if (tid == 0) {
-      for (int c = 0; c < kNumChunks; ++c) {
-        const int cv0 = c * chunk_vec;
-        const int cv1 = min(nvec, cv0 + chunk_vec);
-        if (cv1 <= cv0) break;
-        const uint32_t bytes = uint32_t(cv1 - cv0) * VEC * 4u;
-        const uint32_t bar = smem_addr(&s_bar[c]);
-        mbar_arrive_expect_tx(bar, 2 * bytes);
-        bulk_g2s(smem_addr(zst + cv0 * VEC), p.z + row_base + v0 + cv0 * VEC, bytes, bar);
-        bulk_g2s(smem_addr(qst + cv0 * VEC), p.q + row_base + v0 + cv0 * VEC, bytes, bar);
+
+  // ---------------------------------------------------------------- pass A (HBM)
+  float m = -INFINITY, thr = -INFINITY, mL = 0.0f;
+  float2 acc = make_float2(0.0f, 0.0f), qacc = make_float2(0.0f, 0.0f);
+  // Peaks: [0] of z/T (payload z, q), [1] of q (payload z, q).
+  float pv[2] = {-INFINITY, -INFINITY}, pz[2] = {0.0f, 0.0f}, pq[2] = {0.0f, 0.0f};
+  int pi[2] = {INT_MAX, INT_MAX};
+  {
+    const float2 l2e2 = make_float2(kLog2e, kLog2e);
+    int vi = tid;
+    float4 cz, cq, nz, nq;
+    if (vi < nvec) {
+      cz = ld4(zsl, vi * VEC, len, ALIGNED, pol_keep, -INFINITY);
+      cq = ld4(qsl, vi * VEC, len, ALIGNED, pol_keep, 0.0f);
+    }
+    for (; vi < nvec; vi += kRapidThreads) {
+      const int vn = vi + kRapidThreads;
+      if (vn < nvec) {
+        nz = ld4(zsl, vn * VEC, len, ALIGNED, pol_keep, -INFINITY);
+        nq = ld4(qsl, vn * VEC, len, ALIGNED, pol_keep, 0.0f);
+      }
+      const float2 s0 = fmul2(make_float2(cz.x, cz.y), invT2);
+      const float2 s1 = fmul2(make_float2(cz.z, cz.w), invT2);
+      const float vm = fmaxf(fmaxf(s0.x, s0.y), fmaxf(s1.x, s1.y));
+      const float vq = fmaxf(fmaxf(cq.x, cq.y), fmaxf(cq.z, cq.w));
+      m = fmaxf(m, vm);
+      if (vm > thr || vm > pv[0] || vq > pv[1]) {
+        if (vm > thr && isfinite(m)) {
+          // Move the partial sum to a reference at the current maximum (about once per thread).
+          const float nL = m * kLog2e;
+          if (thr == -INFINITY || nL > mL + kRapidSlack) {
+            const float f = (acc.x != 0.0f || acc.y != 0.0f) ? exp2f(mL - nL) : 0.0f;
+            acc = fmul2(acc, make_float2(f, f));
+            mL = nL;
+            thr = (nL + kRapidSlack) * 0.693147180559945f;
+          }
+        }
+        const float sv[4] = {s0.x, s0.y, s1.x, s1.y};
+        const float zv[4] = {cz.x, cz.y, cz.z, cz.w};
+        const float qv[4] = {cq.x, cq.y, cq.z, cq.w};
+        const int kb = v0 + vi * VEC;
+        // The first entry holding the vector's peak, and its payload (unrolled selects).
+        if (vm > pv[0]) {
+          int e = 3;
+          float a = zv[3], b = qv[3];
+#pragma unroll
+          for (int j = 2; j >= 0; --j)
+            if (sv[j] == vm) {
+              e = j;
+              a = zv[j];
+              b = qv[j];
+            }
+          pv[0] = vm;
+          pi[0] = kb + e;
+          pz[0] = a;
+          pq[0] = b;
+        }
+        if (vq > pv[1]) {
+          int e = 3;
+          float a = zv[3], b = qv[3];
+#pragma unroll
+          for (int j = 2; j >= 0; --j)
+            if (qv[j] == vq) {
+              e = j;
+              a = zv[j];
+              b = qv[j];
+            }
+          pv[1] = vq;
+          pi[1] = kb + e;
+          pz[1] = a;
+          pq[1] = b;
+        }
+      }
+      const float2 y0 = ffma2(s0, l2e2, make_float2(-mL, -mL));
+      const float2 y1 = ffma2(s1, l2e2, make_float2(-mL, -mL));
+      acc = fadd2(acc, make_float2(ex2_approx(y0.x), ex2_approx(y0.y)));
+      acc = fadd2(acc, make_float2(ex2_approx(y1.x), ex2_approx(y1.y)));
+      qacc = fadd2(qacc, make_float2(cq.x, cq.y));
+      qacc = fadd2(qacc, make_float2(cq.z, cq.w));
+      cz = nz;
+      cq = nq;
+    }
+  }
+
+  // CTA statistics: maximum; sums moved to the CTA reference; peaks.
+  {
+    const float w = warp_max(m);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      warp_argmax_pl(pv[k], pi[k], pz[k], pq[k]);
+      if (lane == 0) {
+        s_pv[warp][k] = pv[k];
+        s_pi[warp][k] = pi[k];
+        s_pz[warp][k] = pz[k];
+        s_pq[warp][k] = pq[k];
       }
     }
-  } else {
-    const int npad = nvec * VEC;
-    for (int k = tid; k < npad; k += nthr) {
-      zst[k] = (k < len) ? p.z[row_base + v0 + k] : -INFINITY;
-      qst[k] = (k < len) ? p.q[row_base + v0 + k] : 0.0f;
-    }
+    if (lane == 0) s_w[warp][3] = w;
     __syncthreads();
-  }
-
-  auto block_max = [&](float v) -> float {
-    v = warp_max(v);
-    if (lane == 0) s_wf[warp] = v;
-    __syncthreads();
-    float r = -INFINITY;
-    if (warp == 0) r = warp_max(lane < nwarps ? s_wf[lane] : -INFINITY);
-    __syncthreads();
-    return r;  // valid in warp 0
-  };
-  // fp32 warp sums; the per-warp partials are combined by warp 0 as compensated pairs and
-  // written to dst_a / dst_b (hi, lo) in this CTA's exchange slot.
-  auto block_sum2 = [&](float a, float b, float* dst_a, float* dst_b) {
-    a = warp_sum_f(a);
-    b = warp_sum_f(b);
+    float Mc = s_w[0][3];
+#pragma unroll
+    for (int k = 1; k < kWarps; ++k) Mc = fmaxf(Mc, s_w[k][3]);
+    const float s = acc.x + acc.y;
+    const float moved = (s != 0.0f) ? s * exp2f(mL - ref_of(Mc)) : 0.0f;
+    const float ws = warp_sum_f(moved);
+    const float wq = warp_sum_f(qacc.x + qacc.y);
     if (lane == 0) {
-      s_w2[warp][0] = a;
-      s_w2[warp][1] = b;
+      s_w[warp][0] = ws;
+      s_w[warp][1] = wq;
     }
     __syncthreads();
     if (warp == 0) {
-      const DF ra = warp_sum_df(DF{lane < nwarps ? s_w2[lane][0] : 0.0f, 0.0f});
-      const DF rb = warp_sum_df(DF{lane < nwarps ? s_w2[lane][1] : 0.0f, 0.0f});
+      const DF se = warp_sum_df(DF{lane < kWarps ? s_w[lane][0] : 0.0f, 0.0f});
+      const DF sq = warp_sum_df(DF{lane < kWarps ? s_w[lane][1] : 0.0f, 0.0f});
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        float v = lane < kWarps ? s_pv[lane][k] : -INFINITY;
+        int i = lane < kWarps ? s_pi[lane][k] : INT_MAX;
+        float a = lane < kWarps ? s_pz[lane][k] : 0.0f;
+        float b = lane < kWarps ? s_pq[lane][k] : 0.0f;
+        warp_argmax_pl(v, i, a, b);
+        if (lane == 0) {
+          xchg.pk_v[k] = v;
+          xchg.pk_i[k] = i;
+          xchg.pk_z[k] = a;
+          xchg.pk_q[k] = b;
+        }
+      }
       if (lane == 0) {
-        dst_a[0] = ra.hi;
-        dst_a[1] = ra.lo;
-        dst_b[0] = rb.hi;
-        dst_b[1] = rb.lo;
+        xchg.zmax = Mc;
+        xchg.se[0] = se.hi;
+        xchg.se[1] = se.lo;
+        xchg.sq[0] = sq.hi;
+        xchg.sq[1] = sq.lo;
       }
     }
-    __syncthreads();
-  };
-  // Sum over the cluster of a (hi, lo) slot, in warp 0 (result valid in lane 0).
-  auto cluster_sum = [&](const float* slot) -> DF {
-    DF d{0.0f, 0.0f};
+  }
+  cluster_sync_w0(warp);  // #1
+
+  // ---------------------------------------------------------------- row statistics (warp 0)
+  if (warp == 0) {
+    float mq = -INFINITY;
+    DF se{0.0f, 0.0f}, sq{0.0f, 0.0f};
+    float v[2] = {-INFINITY, -INFINITY}, a[2] = {0.0f, 0.0f}, b[2] = {0.0f, 0.0f};
+    int i[2] = {INT_MAX, INT_MAX};
     if (lane < int(C)) {
-      d.hi = dsmem_ld_f32(dsmem_map(smem_addr(&slot[0]), uint32_t(lane)));
-      d.lo = dsmem_ld_f32(dsmem_map(smem_addr(&slot[1]), uint32_t(lane)));
-    }
-    return warp_sum_df(d);
-  };
-
-  const float invT = p.inv_T;
-  // ---------------------------------------------------------------- sweep 1: max of z/T
-  {
-    float m = -INFINITY;
-    for (int c = 0; c < kNumChunks; ++c) {
-      const int cv0 = c * chunk_vec;
-      const int cv1 = min(nvec, cv0 + chunk_vec);
-      if (cv1 <= cv0) break;
-      if (p.bulk && !mbar_wait(smem_addr(&s_bar[c]), 0, kWaitPolls)) atomicOr(&s_err, 1u);
-      for (int vi = cv0 + tid; vi < cv1; vi += nthr) {
-        const float4 z4 = reinterpret_cast<const float4*>(zst)[vi];
-        m = fmaxf(m, fmaxf(fmaxf(z4.x * invT, z4.y * invT), fmaxf(z4.z * invT, z4.w * invT)));
+      const uint32_t q = uint32_t(lane);
+      mq = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.zmax), q));
+      se.hi = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.se[0]), q));
+      se.lo = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.se[1]), q));
+      sq.hi = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.sq[0]), q));
+      sq.lo = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.sq[1]), q));
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        v[k] = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.pk_v[k]), q));
+        i[k] = dsmem_ld_s32(dsmem_map(smem_addr(&xchg.pk_i[k]), q));
+        a[k] = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.pk_z[k]), q));
+        b[k] = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.pk_q[k]), q));
       }
     }
-    const float r = block_max(m);
-    if (tid == 0) {
-      xchg.zmax = r;
-      xchg.err = s_err;
-    }
-  }
-  cluster_sync();  // #1
-  if (warp == 0) {
-    float v = -INFINITY;
-    if (lane < int(C)) v = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.zmax), uint32_t(lane)));
-    v = warp_max(v);
-    if (lane == 0) rs.M = v;
-  }
-  __syncthreads();
-  const float M = rs.M;
-  RowConsts rc;
-  rc.invT = invT;
-  rc.etaT = p.eta * p.T;
-  rc.ML = isfinite(M) ? M * kLog2e : 0.0f;
-
-  // ---------------------------------------------------------------- sweep 2: sum of exp, sum of q
-  {
-    float e0 = 0.f, e1 = 0.f, q0 = 0.f, q1 = 0.f;
-    for (int vi = tid; vi < nvec; vi += nthr) {
-      const float4 z4 = reinterpret_cast<const float4*>(zst)[vi];
-      const float4 q4 = reinterpret_cast<const float4*>(qst)[vi];
-      e0 += ex2_approx(fmaf(z4.x * invT, kLog2e, -rc.ML)) + ex2_approx(fmaf(z4.z * invT, kLog2e, -rc.ML));
-      e1 += ex2_approx(fmaf(z4.y * invT, kLog2e, -rc.ML)) + ex2_approx(fmaf(z4.w * invT, kLog2e, -rc.ML));
-      q0 += q4.x + q4.z;
-      q1 += q4.y + q4.w;
-    }
-    block_sum2(e0 + e1, q0 + q1, xchg.sum_e, xchg.sum_q);
-  }
-  cluster_sync();  // #2
-  if (warp == 0) {
-    const DF Se = cluster_sum(xchg.sum_e);
-    const DF Sq = cluster_sum(xchg.sum_q);
+    const float M = warp_max(mq);
+    const float ML = ref_of(M);
+    const float f = (se.hi != 0.0f) ? exp2f(ref_of(mq) - ML) : 0.0f;
+    const DF S = warp_sum_df(DF{se.hi * f, se.lo * f});
+    const DF Q = warp_sum_df(sq);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) warp_argmax_pl(v[k], i[k], a[k], b[k]);
     if (lane == 0) {
-      const bool fin = isfinite(M) && isfinite(Se.hi) && Se.hi > 0.0f && isfinite(Sq.hi);
+      const bool fin = isfinite(M) && isfinite(S.hi) && S.hi > 0.0f && isfinite(Q.hi);
+      rs.M = M;
       rs.finite = fin ? 1 : 0;
-      rs.inv_sum = fin ? 1.0f / (Se.hi + Se.lo) : 0.0f;
+      rs.inv_sum = fin ? 1.0f / (S.hi + S.lo) : 0.0f;
+      // L0: zhat/T at the peaks of z/T and of q (entries of this row, so L0 <= max zhat/T).
+      float L0 = -INFINITY;
+      if (fin) {
+        RowConsts c;
+        c.invT = invT;
+        c.etaT = etaT;
+        c.ML = ML;
+        c.inv_sum = rs.inv_sum;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          if (i[k] != INT_MAX) {
+            float pk, zh;
+            rapid_p_zhs(a[k], b[k], c, pk, zh);
+            L0 = fmaxf(L0, zh);
+          }
+        }
+      }
+      rs.L0 = L0;
     }
   }
   __syncthreads();
   const bool finite = rs.finite != 0;
+  RowConsts rc;
+  rc.invT = invT;
+  rc.etaT = etaT;
+  rc.ML = ref_of(rs.M);
   rc.inv_sum = rs.inv_sum;
-  rc.zhmax = 0.f;
-  rc.thr = 0.f;
-  rc.head_scale = 0.f;
+  rc.zhmax = 0.0f;
+  rc.thr = 0.0f;
+  rc.head_scale = 0.0f;
   rc.tail_scale = 1.0f;
 
-  // ---------------------------------------------------------------- sweep 3: max of zhat/T
-  {
-    float m = -INFINITY;
-    if (finite) {
-      for (int vi = tid; vi < nvec; vi += nthr) {
-        const float4 z4 = reinterpret_cast<const float4*>(zst)[vi];
-        const float4 q4 = reinterpret_cast<const float4*>(qst)[vi];
-        const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
-        const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float pk = ex2_approx(fmaf(zz[e] * invT, kLog2e, -rc.ML)) * rc.inv_sum;
-          m = fmaxf(m, fmaf(rc.etaT, qq[e] - pk, zz[e]) * invT);
-        }
-      }
+  // ---------------------------------------------------------------- pass B (L2)
+  float L = rs.L0;  // bound: L0, raised by this thread's own entries; ends as its max of zhat/T
+  float c0z = 0.0f, c0p = 0.0f, c1z = 0.0f, c1p = 0.0f;  // head candidates (zhat/T, p)
+  int nc = 0;
+  bool ovf = false;
+  float2 aacc = make_float2(0.0f, 0.0f), pall = make_float2(0.0f, 0.0f);
+  float aL = ref_of(L), athr = isfinite(L) ? (aL + kRapidSlack) * 0.693147180559945f : -INFINITY;
+  if (finite) {
+    const float2 nML2 = make_float2(-rc.ML, -rc.ML);
+    const float2 inv2 = make_float2(rc.inv_sum, rc.inv_sum);
+    float cthr = cand_on ? L + ln_tf : INFINITY;
+    int vi = tid;
+    float4 cz, cq, nz, nq;
+    if (vi < nvec) {
+      cz = ld4(zsl, vi * VEC, len, ALIGNED, pol_last, -INFINITY);
+      cq = ld4(qsl, vi * VEC, len, ALIGNED, pol_last, 0.0f);
     }
-    const float r = block_max(m);
-    if (tid == 0) xchg.zhmax = r;
-  }
-  cluster_sync();  // #3
-  if (warp == 0) {
-    float v = -INFINITY;
-    if (lane < int(C)) v = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.zhmax), uint32_t(lane)));
-    v = warp_max(v);
-    if (lane == 0) rs.zhmax = v;
-  }
-  __syncthreads();
-  rc.zhmax = rs.zhmax;
-  rc.thr = rs.zhmax + p.ln_tail_frac;
-
-  // ---------------------------------------------------------------- sweep 4: head sums
-  {
-    float hp0 = 0.f, he0 = 0.f, tp0 = 0.f, ae0 = 0.f;
-    if (finite) {
-      for (int vi = tid; vi < nvec; vi += nthr) {
-        const float4 z4 = reinterpret_cast<const float4*>(zst)[vi];
-        const float4 q4 = reinterpret_cast<const float4*>(qst)[vi];
-        const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
-        const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float pk = ex2_approx(fmaf(zz[e] * invT, kLog2e, -rc.ML)) * rc.inv_sum;
-          const float zhs = fmaf(rc.etaT, qq[e] - pk, zz[e]) * invT;
-          if (p.tail_mode == 0) {
-            if (zhs >= rc.thr) {
-              hp0 += pk;
-              he0 += ex2_approx((zhs - rc.zhmax) * kLog2e);
-            }
-          } else {
-            const float ek = ex2_approx((zhs - rc.zhmax) * kLog2e);
-            ae0 += ek;
-            if (zhs >= rc.thr) {
-              hp0 += pk;
-              he0 += ek;
-            } else {
-              tp0 += pk;
+    for (; vi < nvec; vi += kRapidThreads) {
+      const int vn = vi + kRapidThreads;
+      if (vn < nvec) {
+        nz = ld4(zsl, vn * VEC, len, ALIGNED, pol_last, -INFINITY);
+        nq = ld4(qsl, vn * VEC, len, ALIGNED, pol_last, 0.0f);
+      }
+      float2 p0, p1, h0, h1;
+      pzhs2(make_float2(cz.x, cz.y), make_float2(cq.x, cq.y), invT2, nML2, inv2, etaT2, p0, h0);
+      pzhs2(make_float2(cz.z, cz.w), make_float2(cq.z, cq.w), invT2, nML2, inv2, etaT2, p1, h1);
+      const float vm = fmaxf(fmaxf(h0.x, h0.y), fmaxf(h1.x, h1.y));
+      const float Ln = fmaxf(L, vm);
+      if (vm >= cthr || (AE && vm > athr)) {
+        if (cand_on) {
+          if (Ln > L) {
+            // The bound rose: drop candidates below the new boundary (they cannot be head entries).
+            cthr = Ln + ln_tf;
+            if (nc == 2 && c1z < cthr) nc = 1;
+            if (nc >= 1 && c0z < cthr) {
+              c0z = c1z;
+              c0p = c1p;
+              nc -= 1;
             }
           }
-        }
-      }
-    }
-    block_sum2(hp0, he0, xchg.head_p, xchg.head_e);
-    if (p.tail_mode != 0) block_sum2(tp0, ae0, xchg.tail_p, xchg.all_e);
-    if (tid == 0) xchg.err = s_err;
-  }
-  cluster_sync();  // #4
-
-  // ---------------------------------------------------------------- row finalisation (CTA 0)
-  DF Hp{0.0f, 0.0f}, He{0.0f, 0.0f}, Tp{0.0f, 0.0f}, Ae{0.0f, 0.0f};
-  uint32_t err = 0;
-  if (rank == 0 && warp == 0) {
-    Hp = cluster_sum(xchg.head_p);
-    He = cluster_sum(xchg.head_e);
-    if (p.tail_mode != 0) {
-      Tp = cluster_sum(xchg.tail_p);
-      Ae = cluster_sum(xchg.all_e);
-    }
-    uint32_t e = (lane < int(C)) ? dsmem_ld_u32(dsmem_map(smem_addr(&xchg.err), uint32_t(lane))) : 0u;
+          const float hv[4] = {h0.x, h0.y, h1.x, h1.y};
+          const float pv4[4] = {p0.x, p0.y, p1.x, p1.y};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) e |= __shfl_xor_sync(0xffffffffu, e, o);
-    err = e;
-  }
-  if (rank == 0 && tid == 0) {
-    const float he = He.hi + He.lo;
-    if (p.tail_mode == 0) {
-      rc.head_scale = (he > 0.0f) ? (Hp.hi + Hp.lo) / he : 0.0f;
-      rc.tail_scale = 1.0f;
-    } else {
-      // Z = tail p-mass + head phat-mass, phat = exp(zhat/T - max) / Ae:
-      // tail p / Z, head exp(zhat/T - max) / (Ae Z) = exp(..) / (Ae Tp + He).
-      const float tp = Tp.hi + Tp.lo, ae = Ae.hi + Ae.lo;
-      const float z = tp + (ae > 0.0f ? he / ae : 0.0f);
-      rc.tail_scale = (z > 0.0f) ? 1.0f / z : 0.0f;
-      const float den = fmaf(ae, tp, he);
-      rc.head_scale = (den > 0.0f) ? 1.0f / den : 0.0f;
-    }
-    uint32_t bits = 0;
-    if (!finite) bits |= kBitNonfinite;
-    if (err) bits |= kBitTimeout;
-    if (pos < G) {
-      const int d = p.draft_ids[size_t(req) * G + pos];
-      if (d < 0 || d >= V) {
-        bits |= kBitBadDraft;
-      } else if (finite) {
-        const uint32_t owner = uint32_t(d / p.n_slice);
-        const int off = d - int(owner) * p.n_slice;
-        const float zd = dsmem_ld_f32(dsmem_map(smem_addr(zst + off), owner));
-        const float qd = dsmem_ld_f32(dsmem_map(smem_addr(qst + off), owner));
-        float pd, zhsd, protd;
-        rapid_entry(zd, qd, rc, pd, zhsd, protd);
-        const Philox4 r4 = philox4x32_10(0u, uint32_t(pos), uint32_t(req), 0u + 4u * p.offset, p.seed_lo, p.seed_hi);
-        const float u = uniform_from_word(r4.v[0]);
-        if (u * qd < protd) bits |= kBitAccept;
-      }
-    }
-    RapidRecord rec;
-    rec.zs_max = M;
-    rec.inv_sum = rc.inv_sum;
-    rec.zhat_max = rc.zhmax;
-    rec.head_scale = rc.head_scale;
-    rec.tail_scale = rc.tail_scale;
-    rec.bits = bits;
-    rec.pad[0] = rec.pad[1] = 0;
-    p.records[row] = rec;
-    __threadfence();
-    const uint32_t ticket = atomicAdd(&p.tickets[req], 1u);
-    if (ticket == uint32_t(G)) {
-      __threadfence();
-      const volatile RapidRecord* recs = p.records + size_t(req) * R1;
-      uint32_t any = 0;
-      for (int i = 0; i < R1; ++i) any |= recs[i].bits;
-      const uint32_t status = ((any & kBitNonfinite) ? 1u : 0u) | ((any & kBitBadDraft) ? 2u : 0u) |
-                              ((any & kBitTimeout) ? 4u : 0u);
-      if (status) {
-        p.out_accept_len[req] = 0;
-        for (int i = 0; i < R1; ++i) p.out_tokens[size_t(req) * R1 + i] = -1;
-        p.out_req_status[req] = status;
-        // The request's records are consumed: clear them (a call leaves the workspace zeroed).
-        for (int i = 0; i < R1; ++i) p.records[size_t(req) * R1 + i] = RapidRecord{};
-        p.tickets[req] = 0u;
-      } else {
-        int n = G;
-        for (int i = 0; i < G; ++i)
-          if (!(recs[i].bits & kBitAccept)) {
-            n = i;
-            break;
-          }
-        const float f0 = recs[n].zs_max, f1 = recs[n].inv_sum, f2 = recs[n].zhat_max, f3 = recs[n].head_scale;
-        const float f4 = recs[n].tail_scale;
-        for (int i = 0; i < R1; ++i) p.records[size_t(req) * R1 + i] = RapidRecord{};
-        for (uint32_t q = 0; q < C; ++q) {
-          dsmem_st_u32(dsmem_map(smem_addr(&xchg.draw_row), q), uint32_t(n));
-          dsmem_st_u32(dsmem_map(smem_addr(&xchg.d_zs_max), q), __float_as_uint(f0));
-          dsmem_st_u32(dsmem_map(smem_addr(&xchg.d_inv_sum), q), __float_as_uint(f1));
-          dsmem_st_u32(dsmem_map(smem_addr(&xchg.d_zhat_max), q), __float_as_uint(f2));
-          dsmem_st_u32(dsmem_map(smem_addr(&xchg.d_head_scale), q), __float_as_uint(f3));
-          dsmem_st_u32(dsmem_map(smem_addr(&xchg.d_tail_scale), q), __float_as_uint(f4));
-          dsmem_st_u32(dsmem_map(smem_addr(&xchg.draw_active), q), 1u);
-        }
-      }
-    }
-  }
-  cluster_sync();  // #5: the draw broadcast is visible
-
-  if (xchg.draw_active) {
-    // ---------------------------------------------------------------- residual / bonus draw
-    const int n = xchg.draw_row;
-    const uint32_t stream = (n < G) ? 1u : 2u;
-    RowConsts dc;
-    dc.invT = invT;
-    dc.etaT = p.eta * p.T;
-    dc.ML = isfinite(xchg.d_zs_max) ? xchg.d_zs_max * kLog2e : 0.0f;
-    dc.inv_sum = xchg.d_inv_sum;
-    dc.zhmax = xchg.d_zhat_max;
-    dc.thr = xchg.d_zhat_max + p.ln_tail_frac;
-    dc.head_scale = xchg.d_head_scale;
-    dc.tail_scale = xchg.d_tail_scale;
-    const size_t nbase = (size_t(req) * R1 + n) * size_t(V);
-    int winner = INT_MAX;
-    for (int pass = 0; pass < 2 && winner == INT_MAX; ++pass) {
-      // pass 0: residual (or protected target at the bonus position); pass 1: p, if the residual is all zero
-      float bk = INFINITY;
-      int bidx = INT_MAX;
-      for (int vi = tid; vi < nvec; vi += nthr) {
-        const int kb = v0 + vi * VEC;
-        const Philox4 r4 =
-            philox4x32_10(uint32_t(kb >> 2), uint32_t(n), uint32_t(req), stream + 4u * p.offset, p.seed_lo, p.seed_hi);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          const int k = kb + e;
-          if (k < v0 + len) {
-            const float z = p.z[nbase + k];
-            const float q = p.q[nbase + k];
-            float pk, zhs, prot;
-            rapid_entry(z, q, dc, pk, zhs, prot);
-            float w;
-            if (pass == 1) w = pk;
-            else if (n < G) w = fmaxf(fmaxf(pk - prot, pk - q), 0.0f);
-            else w = prot;
-            if (w > 0.0f) {
-              const float key = -logf(uniform_from_word(r4.v[e])) / w;
-              if (key < bk) {
-                bk = key;
-                bidx = k;
+          for (int e = 0; e < 4; ++e) {
+            if (hv[e] >= cthr) {
+              if (nc == 0) {
+                c0z = hv[e];
+                c0p = pv4[e];
+                nc = 1;
+              } else if (nc == 1) {
+                c1z = hv[e];
+                c1p = pv4[e];
+                nc = 2;
+              } else {
+                ovf = true;
               }
             }
           }
         }
-      }
-      warp_argmin(bk, bidx);
-      if (lane == 0) {
-        s_wf[warp] = bk;
-        s_wi[warp] = bidx;
-      }
-      __syncthreads();
-      if (warp == 0) {
-        float v = lane < nwarps ? s_wf[lane] : INFINITY;
-        int i = lane < nwarps ? s_wi[lane] : INT_MAX;
-        warp_argmin(v, i);
-        if (lane == 0) {
-          xchg.race_key = v;
-          xchg.race_idx = i;
+        if (AE && vm > athr && isfinite(Ln)) {
+          const float nL = Ln * kLog2e;
+          if (athr == -INFINITY || nL > aL + kRapidSlack) {
+            const float f = (aacc.x != 0.0f || aacc.y != 0.0f) ? exp2f(aL - nL) : 0.0f;
+            aacc = fmul2(aacc, make_float2(f, f));
+            aL = nL;
+            athr = (nL + kRapidSlack) * 0.693147180559945f;
+          }
         }
       }
-      cluster_sync();  // #6 (per pass)
-      float gv = INFINITY;
-      int gi = INT_MAX;
-      for (uint32_t q = 0; q < C; ++q)
-        argmin_merge(gv, gi, dsmem_ld_f32(dsmem_map(smem_addr(&xchg.race_key), q)),
-                     dsmem_ld_s32(dsmem_map(smem_addr(&xchg.race_idx), q)));
-      winner = gi;
-      cluster_sync();  // #7 (per pass): the exchange slots may be rewritten
-    }
-    if (rank == 0 && tid == 0) {
-      int32_t* toks = p.out_tokens + size_t(req) * R1;
-      const int32_t* dr = p.draft_ids + size_t(req) * G;
-      for (int i = 0; i < R1; ++i) toks[i] = (i < n) ? dr[i] : (i == n ? (winner == INT_MAX ? 0 : winner) : -1);
-      p.out_accept_len[req] = n;
-      p.out_req_status[req] = 0u;
-      p.tickets[req] = 0u;
+      L = Ln;
+      if constexpr (AE) {
+        const float2 l2e2 = make_float2(kLog2e, kLog2e);
+        const float2 y0 = ffma2(h0, l2e2, make_float2(-aL, -aL));
+        const float2 y1 = ffma2(h1, l2e2, make_float2(-aL, -aL));
+        aacc = fadd2(aacc, make_float2(ex2_approx(y0.x), ex2_approx(y0.y)));
+        aacc = fadd2(aacc, make_float2(ex2_approx(y1.x), ex2_approx(y1.y)));
+        pall = fadd2(pall, p0);
+        pall = fadd2(pall, p1);
+      }
+      cz = nz;
+      cq = nq;
     }
   }
+  {
+    const float w = warp_max(L);
+    if (lane == 0) s_w[warp][3] = w;
+    __syncthreads();
+    float Mc = s_w[0][3];
+#pragma unroll
+    for (int k = 1; k < kWarps; ++k) Mc = fmaxf(Mc, s_w[k][3]);
+    float wa = 0.0f, wp = 0.0f;
+    if constexpr (AE) {
+      const float s = aacc.x + aacc.y;
+      wa = warp_sum_f((s != 0.0f) ? s * exp2f(aL - ref_of(Mc)) : 0.0f);
+      wp = warp_sum_f(pall.x + pall.y);
+    }
+    if (lane == 0) {
+      s_w[warp][0] = wa;
+      s_w[warp][1] = wp;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const DF sa = warp_sum_df(DF{lane < kWarps ? s_w[lane][0] : 0.0f, 0.0f});
+      const DF sp = warp_sum_df(DF{lane < kWarps ? s_w[lane][1] : 0.0f, 0.0f});
+      if (lane == 0) {
+        xchg.zhmax = Mc;
+        xchg.ae[0] = sa.hi;
+        xchg.ae[1] = sa.lo;
+        xchg.pa[0] = sp.hi;
+        xchg.pa[1] = sp.lo;
+      }
+    }
+  }
+  const bool cta_ovf = __syncthreads_or(ovf ? 1 : 0) != 0;
+  cluster_sync_w0(warp);  // #2
 
-  if (p.bulk && tid == 0 && s_err) {
-    for (int c = 0; c < kNumChunks; ++c) {
-      const int cv0 = c * chunk_vec;
-      if (min(nvec, cv0 + chunk_vec) <= cv0) break;
-      mbar_wait(smem_addr(&s_bar[c]), 0, kWaitPolls);
+  if (warp == 0) {
+    float mq = -INFINITY;
+    DF sa{0.0f, 0.0f}, sp{0.0f, 0.0f};
+    if (lane < int(C)) {
+      const uint32_t q = uint32_t(lane);
+      mq = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.zhmax), q));
+      if constexpr (AE) {
+        sa.hi = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.ae[0]), q));
+        sa.lo = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.ae[1]), q));
+        sp.hi = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.pa[0]), q));
+        sp.lo = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.pa[1]), q));
+      }
+    }
+    const float Mh = warp_max(mq);
+    if constexpr (AE) {
+      const float f = (sa.hi != 0.0f) ? exp2f(ref_of(mq) - ref_of(Mh)) : 0.0f;
+      sa = warp_sum_df(DF{sa.hi * f, sa.lo * f});
+      sp = warp_sum_df(sp);
+    }
+    if (lane == 0) {
+      rs.zhmax = Mh;
+      rs.ae_hi = sa.hi;
+      rs.ae_lo = sa.lo;
+      rs.pa_hi = sp.hi;
+      rs.pa_lo = sp.lo;
     }
   }
-  cluster_sync();  // #8: shared memory stays alive until remote reads are done
+  __syncthreads();
+  rc.zhmax = rs.zhmax;
+  rc.thr = rs.zhmax + ln_tf;
+
+  // ---------------------------------------------------------------- head sums
+  {
+    float hp = 0.0f, he = 0.0f;
+    if (finite && cand_on) {
+      if (!cta_ovf) {
+        if (nc >= 1 && c0z >= rc.thr) {
+          hp += c0p;
+          he += head_exp(c0z, rc.zhmax);
+        }
+        if (nc >= 2 && c1z >= rc.thr) {
+          hp += c1p;
+          he += head_exp(c1z, rc.zhmax);
+        }
+      } else {
+        // Pass C: a thread ran out of candidate slots; test every entry of the slice.
+        for (int vi = tid; vi < nvec; vi += kRapidThreads) {
+          const float4 z4 = ld4(zsl, vi * VEC, len, ALIGNED, pol_last, -INFINITY);
+          const float4 q4 = ld4(qsl, vi * VEC, len, ALIGNED, pol_last, 0.0f);
+          const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
+          const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float pk, zh;
+            rapid_p_zhs(zz[e], qq[e], rc, pk, zh);
+            if (zh >= rc.thr) {
+              hp += pk;
+              he += head_exp(zh, rc.zhmax);
+            }
+          }
+        }
+      }
+    }
+    const float wh = warp_sum_f(hp);
+    const float we = warp_sum_f(he);
+    if (lane == 0) {
+      s_w[warp][0] = wh;
+      s_w[warp][1] = we;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const DF dh = warp_sum_df(DF{lane < kWarps ? s_w[lane][0] : 0.0f, 0.0f});
+      const DF de = warp_sum_df(DF{lane < kWarps ? s_w[lane][1] : 0.0f, 0.0f});
+      if (lane == 0) {
+        const uint32_t base = smem_addr(&xchg.head[rank][0]);
+        dsmem_st_f32(dsmem_map(base + 0, 0), dh.hi);
+        dsmem_st_f32(dsmem_map(base + 4, 0), dh.lo);
+        dsmem_st_f32(dsmem_map(base + 8, 0), de.hi);
+        dsmem_st_f32(dsmem_map(base + 12, 0), de.lo);
+      }
+    }
+  }
+  cluster_sync_w0(warp);  // #3: after this only CTA 0 touches shared memory, and only its own
+  if (rank != 0 || warp != 0) return;
+
+  // ---------------------------------------------------------------- row finalisation (CTA 0, warp 0)
+  DF Hp{0.0f, 0.0f}, He{0.0f, 0.0f};
+  if (lane < int(C)) {
+    Hp = DF{xchg.head[lane][0], xchg.head[lane][1]};
+    He = DF{xchg.head[lane][2], xchg.head[lane][3]};
+  }
+  Hp = warp_sum_df(Hp);
+  He = warp_sum_df(He);
+  if (lane != 0) return;
+  {
+    float hp = Hp.hi + Hp.lo, he = He.hi + He.lo;
+    const float ae = rs.ae_hi + rs.ae_lo, pa = rs.pa_hi + rs.pa_lo;
+    if (!cand_on) {  // tail_frac = 0: the head is the whole row
+      hp = pa;
+      he = ae;
+    }
+    if (p.tail_mode == 0) {
+      rc.head_scale = (he > 0.0f) ? hp / he : 0.0f;
+      rc.tail_scale = 1.0f;
+    } else {
+      // Z = tail p-mass + head phat-mass, phat = exp(zhat/T - max) / ae:
+      // tail p / Z, head exp(zhat/T - max) / (ae Z) = exp(..) / (ae tp + he).
+      const float tp = pa - hp;
+      const float zz = tp + (ae > 0.0f ? he / ae : 0.0f);
+      rc.tail_scale = (zz > 0.0f) ? 1.0f / zz : 0.0f;
+      const float den = fmaf(ae, tp, he);
+      rc.head_scale = (den > 0.0f) ? 1.0f / den : 0.0f;
+    }
+  }
+  uint32_t bits = 0;
+  if (!finite) bits |= kBitNonfinite;
+  if (pos < G) {
+    if (d < 0 || d >= V) {
+      bits |= kBitBadDraft;
+    } else if (finite) {
+      float pd, zhsd, protd;
+      rapid_entry(zd, qd, rc, pd, zhsd, protd);
+      const Philox4 r4 = philox4x32_10(0u, uint32_t(pos), uint32_t(req), 0u + 4u * p.offset, p.seed_lo, p.seed_hi);
+      const float u = uniform_from_word(r4.v[0]);
+      if (u * qd < protd) bits |= kBitAccept;
+    }
+  }
+  RapidRecord rec;
+  rec.zs_max = rs.M;
+  rec.inv_sum = rc.inv_sum;
+  rec.zhat_max = rc.zhmax;
+  rec.head_scale = rc.head_scale;
+  rec.tail_scale = rc.tail_scale;
+  rec.bits = bits;
+  rec.pad[0] = rec.pad[1] = 0;
+  p.records[row] = rec;
+  __threadfence();
+  const uint32_t ticket = atomicAdd(&p.tickets[req], 1u);
+  if (ticket != uint32_t(G)) return;
+  // The last row of the request: scan the records, write the outputs and leave the draw job.
+  __threadfence();
+  const volatile RapidRecord* recs = p.records + size_t(req) * R1;
+  uint32_t any = 0;
+  for (int i = 0; i < R1; ++i) any |= recs[i].bits;
+  const uint32_t status = ((any & kBitNonfinite) ? 1u : 0u) | ((any & kBitBadDraft) ? 2u : 0u);
+  int32_t* toks = p.out_tokens + size_t(req) * R1;
+  if (status) {
+    p.out_accept_len[req] = 0;
+    for (int i = 0; i < R1; ++i) toks[i] = -1;
+    p.out_req_status[req] = status;
+  } else {
+    int n = G;
+    for (int i = 0; i < G; ++i)
+      if (!(recs[i].bits & kBitAccept)) {
+        n = i;
+        break;
+      }
+    RapidJob job = {};
+    job.zs_max = recs[n].zs_max;
+    job.inv_sum = recs[n].inv_sum;
+    job.zhat_max = recs[n].zhat_max;
+    job.head_scale = recs[n].head_scale;
+    job.tail_scale = recs[n].tail_scale;
+    job.row = n;
+    job.active = 1u;
+    p.jobs[req] = job;
+    const int32_t* dr = p.draft_ids + size_t(req) * G;
+    for (int i = 0; i < R1; ++i) toks[i] = (i < n) ? dr[i] : -1;  // toks[n]: the draw launch
+    p.out_accept_len[req] = n;
+    p.out_req_status[req] = 0u;
+  }
+  // The request's records and counter are consumed: clear them (a call leaves the workspace zeroed).
+  for (int i = 0; i < R1; ++i) p.records[size_t(req) * R1 + i] = RapidRecord{};
+  p.tickets[req] = 0u;
 }
 
-int rapid_static_smem_bytes() {
-  return int(sizeof(RapidXchg) + sizeof(RapidShared) + 32 * 4 + 32 * 4 + 32 * 2 * 4 + kNumChunks * 8 + 4 + 64);
+// The residual / bonus draw of every request whose verification left a job.  draw_ctas CTAs per
+// request (no cluster), each over its slice of the stop row, race all entries once for both
+// weightings (exponential race, argmin_k E_k / w_k, E_k = -ln u_k with the same uniform): the
+// residual max(p - protected, p - q, 0) (at the bonus position the protected target), and p, which
+// decides only if every residual weight is zero.  A CTA's winners go into the job's slots with one
+// 64-bit atomic max each (key bits above the index, inverted, so the smaller key and then the lower
+// index win); the last CTA of the request writes the token and clears the job.
+__global__ void __launch_bounds__(kRapidThreads) rapid_draw_kernel(const RapidArgs p) {
+  constexpr int VEC = 4;
+  constexpr int kWarps = kRapidThreads / 32;
+  __shared__ unsigned long long s_best[kWarps][2];
+  __shared__ uint32_t s_last;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int parts = p.draw_ctas;
+  const int req = blockIdx.x / parts;
+  const int part = blockIdx.x - req * parts;
+  RapidJob* job = p.jobs + req;
+  if (!job->active) return;  // uniform over the CTA
+  const int G = p.G;
+  const int R1 = G + 1;
+  const int V = p.V;
+  const int n = job->row;
+  const int v0 = part * p.n_slice;
+  const int len = max(0, min(V - v0, p.n_slice));
+  const int nvec = (len + VEC - 1) / VEC;
+  const uint32_t stream = (n < G) ? 1u : 2u;
+  RowConsts dc;
+  dc.invT = p.inv_T;
+  dc.etaT = p.eta * p.T;
+  dc.ML = ref_of(job->zs_max);
+  dc.inv_sum = job->inv_sum;
+  dc.zhmax = job->zhat_max;
+  dc.thr = job->zhat_max + p.ln_tail_frac;
+  dc.head_scale = job->head_scale;
+  dc.tail_scale = job->tail_scale;
+  const size_t nbase = (size_t(req) * R1 + n) * size_t(V) + size_t(v0);
+  const float* zr = p.z + nbase;
+  const float* qr = p.q + nbase;
+  const bool al = p.bulk != 0;
+  const uint64_t pol = policy_evict_first();
+  // Packed, inverted: larger is better; 0 = nothing yet.
+  unsigned long long best[2] = {0ull, 0ull};
+  for (int vi = tid; vi < nvec; vi += kRapidThreads) {
+    const int kl = vi * VEC;
+    const int kb = v0 + kl;
+    const float4 z4 = ld4(zr, kl, len, al, pol, -INFINITY);
+    const float4 q4 = ld4(qr, kl, len, al, pol, 0.0f);
+    const Philox4 r4 =
+        philox4x32_10(uint32_t(kb >> 2), uint32_t(n), uint32_t(req), stream + 4u * p.offset, p.seed_lo, p.seed_hi);
+    const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
+    const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+      if (kl + e < len) {
+        float pk, zhs, prot;
+        rapid_entry(zz[e], qq[e], dc, pk, zhs, prot);
+        const float w0 = (n < G) ? fmaxf(fmaxf(pk - prot, pk - qq[e]), 0.0f) : prot;
+        if (w0 > 0.0f || pk > 0.0f) {
+          const float E = -logf(uniform_from_word(r4.v[e]));
+          const unsigned long long idx = uint32_t(kb + e);
+          if (w0 > 0.0f) {
+            const unsigned long long c = ~((static_cast<unsigned long long>(__float_as_uint(E / w0)) << 32) | idx);
+            best[0] = c > best[0] ? c : best[0];
+          }
+          if (pk > 0.0f) {
+            const unsigned long long c = ~((static_cast<unsigned long long>(__float_as_uint(E / pk)) << 32) | idx);
+            best[1] = c > best[1] ? c : best[1];
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xffffffffu, best[k], o);
+      best[k] = other > best[k] ? other : best[k];
+    }
+    if (lane == 0) s_best[warp][k] = best[k];
+  }
+  __syncthreads();
+  if (tid == 0) {
+    unsigned long long b0 = 0ull, b1 = 0ull;
+    for (int w = 0; w < kWarps; ++w) {
+      b0 = s_best[w][0] > b0 ? s_best[w][0] : b0;
+      b1 = s_best[w][1] > b1 ? s_best[w][1] : b1;
+    }
+    if (b0) atomicMax(&job->slot[0], b0);
+    if (b1) atomicMax(&job->slot[1], b1);
+    __threadfence();
+    s_last = (atomicAdd(&job->ticket, 1u) == uint32_t(parts - 1)) ? 1u : 0u;
+    if (s_last) {
+      __threadfence();
+      const unsigned long long w0 = atomicAdd(&job->slot[0], 0ull);
+      const unsigned long long w1 = atomicAdd(&job->slot[1], 0ull);
+      const unsigned long long w = w0 ? w0 : w1;
+      const int tok = w ? int(uint32_t(~w)) : 0;
+      p.out_tokens[size_t(req) * R1 + n] = tok;
+      *job = RapidJob{};  // the job is consumed (a call leaves the workspace zeroed)
+    }
+  }
 }
 
-cudaError_t launch_rapid(const RapidArgs& a, const LaunchPlan& plan, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(rapid_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem);
-  if (e != cudaSuccess) return e;
-  if (plan.cluster > 8) {
-    e = cudaFuncSetAttribute(rapid_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-  }
-  const int R = a.B * (a.G + 1);
+int rapid_threads() { return kRapidThreads; }
+int rapid_ctas_per_sm() { return kRapidCtasPerSm; }
+
+namespace {
+
+cudaLaunchConfig_t cluster_config(unsigned ctas, unsigned cluster, cudaLaunchAttribute* attr, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(R) * unsigned(plan.cluster), 1, 1);
-  cfg.blockDim = dim3(unsigned(plan.threads), 1, 1);
-  cfg.dynamicSmemBytes = size_t(plan.smem);
+  cfg.gridDim = dim3(ctas, 1, 1);
+  cfg.blockDim = dim3(unsigned(kRapidThreads), 1, 1);
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = unsigned(plan.cluster);
+  attr[0].val.clusterDim.x = cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, rapid_kernel, a);
+  return cfg;
+}
+
+template <typename K>
+cudaError_t allow_cluster(K kern, int cluster) {
+  if (cluster <= 8) return cudaSuccess;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
+
+template <bool AL, bool AE>
+cudaError_t launch_verify(const RapidArgs& a, const LaunchPlan& plan, cudaStream_t s) {
+  auto kern = rapid_kernel<AL, AE>;
+  cudaError_t e = allow_cluster(kern, plan.cluster);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg =
+      cluster_config(unsigned(a.B * (a.G + 1)) * unsigned(plan.cluster), unsigned(plan.cluster), attr, s);
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+}  // namespace
+
+static bool rapid_needs_all_sums(const RapidArgs& a) { return a.tail_mode != 0 || !(a.ln_tail_frac > -INFINITY); }
+
+// Two launches on the stream: the verification (every row), then the draws (draw_ctas CTAs per
+// request, with slices of their own: n_slice is recomputed for them).
+cudaError_t launch_rapid(const RapidArgs& a, const LaunchPlan& plan, cudaStream_t s) {
+  const bool ae = rapid_needs_all_sums(a);
+  cudaError_t e;
+  if (plan.bulk) e = ae ? launch_verify<true, true>(a, plan, s) : launch_verify<true, false>(a, plan, s);
+  else e = ae ? launch_verify<false, true>(a, plan, s) : launch_verify<false, false>(a, plan, s);
+  if (e != cudaSuccess) return e;
+  RapidArgs b = a;
+  const int parts = a.draw_ctas;
+  b.n_slice = ((a.V + parts - 1) / parts + 3) / 4 * 4;
+  rapid_draw_kernel<<<unsigned(a.B) * unsigned(parts), kRapidThreads, 0, s>>>(b);
+  return cudaGetLastError();
 }
 
 int rapid_max_active_clusters(const LaunchPlan& plan) {
-  if (cudaFuncSetAttribute(rapid_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem) != cudaSuccess)
-    return 0;
-  if (plan.cluster > 8 &&
-      cudaFuncSetAttribute(rapid_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+  auto kern = rapid_kernel<true, false>;
+  if (plan.cluster > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(plan.cluster), 1, 1);
-  cfg.blockDim = dim3(unsigned(plan.threads), 1, 1);
-  cfg.dynamicSmemBytes = size_t(plan.smem);
+  cfg.blockDim = dim3(unsigned(kRapidThreads), 1, 1);
+  cfg.dynamicSmemBytes = 0;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = unsigned(plan.cluster);
@@ -545,7 +875,7 @@ int rapid_max_active_clusters(const LaunchPlan& plan) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, rapid_kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }

@@ -38,7 +38,8 @@ def test_status_strings_and_workspace_sizes(lib):
         assert lib.asv_status_string(s).startswith(b"ASV_")
     # tickets padded to 256 B + 16-byte row records (AsymSpec/SCI) or 32-byte (RAPID)
     assert lib.asv_workspace_bytes(0, 64, 2, 151936, 1) == 256 + 64 * 3 * 16
-    assert lib.asv_workspace_bytes(1, 32, 10, 128256, 0) == 256 + 32 * 11 * 32
+    # RAPID: tickets, row records (to a 256-byte boundary), one draw job per request
+    assert lib.asv_workspace_bytes(1, 32, 10, 128256, 0) == 256 + 32 * 11 * 32 + 32 * 64
     assert lib.asv_workspace_bytes(0, -1, 2, 10, 0) == 0
 
 

@@ -149,3 +149,63 @@ def test_nonfinite_and_bad_drafts(asv):
     assert list(out.req_status.cpu().numpy()) == [0, 1, 1, 2]
     ref = oracle.rapid_verify(z, q, d, 1.0, 5.0, 0.1, 7)
     _compare(out, ref)
+
+
+def _plateau_batch(seed, B, G, V, n_top):
+    """Rows where n_top entries share the top logit (their zhat/T lie within ln(tail_frac) of the
+    maximum): more head candidates than a thread keeps, so the slices holding them take the
+    exact third read.  Drafts drawn from q, as in the workload generator."""
+    rng = np.random.default_rng(seed)
+    z = (rng.standard_normal((B, G + 1, V)) - 3.0).astype(np.float32)
+    for b in range(B):
+        for i in range(G + 1):
+            top = rng.choice(V, size=min(n_top, V), replace=False)
+            z[b, i, top] = 5.0
+    q = sps.softmax(z.astype(np.float64) + 0.3 * rng.standard_normal(z.shape), axis=-1).astype(np.float32)
+    d = np.zeros((B, G), dtype=np.int32)
+    for b in range(B):
+        for i in range(G):
+            pq = q[b, i].astype(np.float64)
+            d[b, i] = rng.choice(V, p=pq / pq.sum())
+    return z, q, d
+
+
+@pytest.mark.parametrize("V,n_top", [(4096, 64), (32000, 600), (128256, 3000), (1000, 1000)])
+def test_head_plateaus(asv, V, n_top):
+    """Wide heads: the candidate slots overflow and those CTAs sum the head from a third read."""
+    z, q, d = _plateau_batch(70 + V, 12, 3, V, n_top)
+    for eta, mode in ((0.0, 0), (10.0, 0), (10.0, 1)):
+        out = _run(asv, z, q, d, 1.0, eta, 0.1, 555, tail_mode=mode)
+        ref = oracle.rapid_verify(z, q, d, 1.0, eta, 0.1, 555, tail_mode=mode)
+        g, f = _compare(out, ref)
+        assert g >= 9
+
+
+@pytest.mark.parametrize("tail", [0.0, 1e-6, 0.5])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_tail_fraction_extremes(asv, tail, mode):
+    """tail_frac = 0 (every entry in the head), a tiny fraction (a head reaching ~14 nats below the
+    maximum) and a large one, under both tail readings."""
+    b = gen.make_rapid_batch(900, 32, 4, 32000)
+    out = _run(asv, b.z, b.q, b.drafts, 1.0, 10.0, tail, 2024, tail_mode=mode)
+    ref = oracle.rapid_verify(b.z, b.q, b.drafts, 1.0, 10.0, tail, 2024, tail_mode=mode)
+    g, f = _compare(out, ref)
+    # A boundary 14 nats below the peak crosses dense logits: the oracle leaves about a quarter of
+    # the requests ungraded (an entry within 1e-5 of the boundary); the rest must match exactly.
+    assert g >= 20
+
+
+@pytest.mark.parametrize("cluster", [1, 2, 3, 8, 16])
+def test_cluster_sizes(asv, cluster):
+    """Every cluster size, including 16 CTAs (non-portable) and slices left empty for small V."""
+    try:
+        asv.set_tuning(cluster, 0)
+        for V in (17, 5000, 128256):
+            b = gen.make_rapid_batch(40 + V + cluster, 8, 3, V)
+            for mode in (0, 1):
+                out = _run(asv, b.z, b.q, b.drafts, 1.0, 10.0, 0.1, 77, tail_mode=mode)
+                ref = oracle.rapid_verify(b.z, b.q, b.drafts, 1.0, 10.0, 0.1, 77, tail_mode=mode)
+                g, f = _compare(out, ref)
+                assert g >= 6
+    finally:
+        asv.set_tuning(0, 0)
