@@ -93,27 +93,34 @@ cudaError_t plan_jsd(int elem_bytes, int V, long long R, bool aligned, LaunchPla
   return cudaSuccess;
 }
 
-// Plan for the RAPID kernel (fp32 rows, four entries per 16-byte vector).
-cudaError_t plan_rapid(int V, long long R, bool aligned, LaunchPlan* out) {
+// Plan for the RAPID kernel (fp32 rows, four entries per 16-byte vector).  Without the all-entry
+// sums a CTA keeps a 2-byte bound per vector of its slice in shared memory: at least as many CTAs
+// per row as keep that within 48 KB, so four CTAs still share an SM.
+cudaError_t plan_rapid(int V, long long R, bool aligned, bool all_sums, LaunchPlan* out) {
   DevInfo di;
   cudaError_t e = dev_info(&di);
   if (e != cudaSuccess) return e;
-  const int C = wave_fill_cluster(V, R, asv::rapid_ctas_per_sm(), di.sms);
+  int C = wave_fill_cluster(V, R, asv::rapid_ctas_per_sm(), di.sms);
+  auto n_slice = [&](int c) { return int(round_up(size_t(ceil_div(V, c)), 4)); };
+  if (g_tune_cluster.load() <= 0)
+    while (C < asv::kMaxCluster && asv::rapid_smem_bytes(all_sums, n_slice(C)) > 48 * 1024) ++C;
+  if (asv::rapid_smem_bytes(all_sums, n_slice(C)) > 200 * 1024) return cudaErrorInvalidValue;  // V too large
   out->cluster = C;
   out->threads = asv::rapid_threads();
-  out->n_slice = int(round_up(size_t(ceil_div(V, C)), 4));
-  out->smem = 0;
+  out->n_slice = n_slice(C);
+  out->smem = asv::rapid_smem_bytes(all_sums, out->n_slice);
   out->bulk = aligned ? 1 : 0;
   return cudaSuccess;
 }
 
-// CTAs per request of the RAPID draw launch: about four waves of resident CTAs over the batch's
-// requests (the draw is arithmetic-bound: Philox, a logarithm and a division per entry), at least
-// 1024 entries per CTA.
+// CTAs per request of the RAPID draw launch: at least one wave of resident CTAs over the batch's
+// requests, and slices of at most 6144 entries (the staged copy of a slice, 8 bytes per entry,
+// stays within 48 KB of shared memory), at least 1024 entries per CTA.
 int rapid_draw_ctas(int V, int B) {
   DevInfo di;
   const int sms = dev_info(&di) == cudaSuccess ? di.sms : 1;
-  const long long want = (4LL * asv::rapid_ctas_per_sm() * sms + B - 1) / std::max(B, 1);
+  const long long wave = (1LL * asv::rapid_ctas_per_sm() * sms + B - 1) / std::max(B, 1);
+  const long long want = std::max<long long>(wave, (V + 6143) / 6144);
   return int(std::max(1LL, std::min<long long>(want, std::max(1, V / 1024))));
 }
 
@@ -177,7 +184,7 @@ asv_status asv_query_plan(int mode, int B, int K, int V, int dtype, int* cluster
   const bool bulk = (size_t(V) * eb) % 16 == 0;
   LaunchPlan pl;
   cudaError_t e = mode == ASV_MODE_RAPID
-                      ? plan_rapid(V, (long long)B * (K + 1), bulk, &pl)
+                      ? plan_rapid(V, (long long)B * (K + 1), bulk, false, &pl)
                       : plan_jsd(eb, V, (long long)B * (K + 1), bulk, &pl);
   if (e == cudaErrorInvalidValue) return ASV_ERR_SHAPE;
   if (e != cudaSuccess) return cuda_fail(e);
@@ -581,7 +588,8 @@ asv_status rapid_verify_ex(const float* z, const float* q, const int32_t* draft_
   if (ws_bytes < asv_workspace_bytes(ASV_MODE_RAPID, B, G, V, ASV_F32)) return ASV_ERR_WORKSPACE;
   bool bulk = (size_t(V) * 4) % 16 == 0 && aligned(z, 16) && aligned(q, 16);
   LaunchPlan pl;
-  cudaError_t e = plan_rapid(V, (long long)B * (G + 1), bulk, &pl);
+  const float ln_tf = tail_frac > 0.0f ? std::log(tail_frac) : -INFINITY;
+  cudaError_t e = plan_rapid(V, (long long)B * (G + 1), bulk, asv::rapid_needs_all_sums(tail_mode, ln_tf), &pl);
   if (e == cudaErrorInvalidValue) return ASV_ERR_SHAPE;
   if (e != cudaSuccess) return cuda_fail(e);
   asv::RapidArgs a;
@@ -598,7 +606,7 @@ asv_status rapid_verify_ex(const float* z, const float* q, const int32_t* draft_
   a.inv_T = 1.0f / T;
   a.eta = eta;
   a.tail_frac = tail_frac;
-  a.ln_tail_frac = tail_frac > 0.0f ? std::log(tail_frac) : -INFINITY;
+  a.ln_tail_frac = ln_tf;
   a.tail_mode = tail_mode;
   a.seed_lo = uint32_t(seed);
   a.seed_hi = uint32_t(seed >> 32);

@@ -41,6 +41,15 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return pol;
 }
 
+// 16-byte asynchronous copy global -> shared (cp.async, L2 cache policy); completes for the
+// issuing thread at cp_async_wait_all.  Both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(pol)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ------------------------------------------------------------------ GPU-scope synchronisation
 // Release/acquire operations at GPU scope for flags that CTAs of one launch exchange through
 // global memory.

@@ -51,6 +51,8 @@ namespace asv {
 constexpr int kRapidThreads = 256;    // threads per CTA (launch bounds)
 constexpr int kRapidCtasPerSm = 4;    // CTAs per SM the kernel is compiled for (launch bounds)
 constexpr float kRapidSlack = 64.0f;  // reference slack (log2 units), as in the AsymSpec kernel
+constexpr int kDrawThreads = 256;     // threads per CTA of the draw launch
+constexpr int kGroup = 4;             // vectors of a thread per stored bound of U (a power of 2)
 
 struct __align__(16) RapidXchg {
   // Exchange 1 (read by every CTA of the cluster).
@@ -145,6 +147,17 @@ __device__ __forceinline__ float4 ld4(const float* base, int k, int lim, bool al
   return v;
 }
 
+// Four entries for a sparse re-read: an L1-allocating load (the same vector is read again soon).
+__device__ __forceinline__ float4 ld4c(const float* base, int k, int lim, bool aligned, float pad) {
+  if (aligned) return __ldg(reinterpret_cast<const float4*>(base + k));
+  float4 v;
+  v.x = (k + 0 < lim) ? __ldg(base + k + 0) : pad;
+  v.y = (k + 1 < lim) ? __ldg(base + k + 1) : pad;
+  v.z = (k + 2 < lim) ? __ldg(base + k + 2) : pad;
+  v.w = (k + 3 < lim) ? __ldg(base + k + 3) : pad;
+  return v;
+}
+
 // Two-lane p and zhat/T of the pairs (z, q) -- the operations of rapid_p_zhs, lane by lane.
 __device__ __forceinline__ void pzhs2(float2 z, float2 q, float2 invT2, float2 nML2, float2 inv2, float2 etaT2,
                                       float2& pk, float2& zh) {
@@ -164,6 +177,10 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
   __shared__ float s_w[kWarps][4];
   __shared__ float s_pv[kWarps][2], s_pz[kWarps][2], s_pq[kWarps][2];
   __shared__ int32_t s_pi[kWarps][2];
+  // !AE: for each thread and each group of kGroup of its vectors (vi = tid + j T, j = g kGroup ...
+  // g kGroup + kGroup - 1), the maximum of U = fl(fl(fma(eta T, q, z)) / T) over their entries;
+  // entry [g][tid].
+  extern __shared__ __align__(16) float s_umax[];
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -203,47 +220,62 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
   }
 
   // ---------------------------------------------------------------- pass A (HBM)
-  float m = -INFINITY, thr = -INFINITY, mL = 0.0f;
+  float thr = -INFINITY, mL = 0.0f;
   float2 acc = make_float2(0.0f, 0.0f), qacc = make_float2(0.0f, 0.0f);
-  // Peaks: [0] of z/T (payload z, q), [1] of q (payload z, q).
+  float ub_t = -INFINITY;  // !AE: the largest bound this thread stored
+  // Peaks: [0] of z/T (its value is the thread's running maximum; payload z, q), [1] of the second
+  // key below (payload z, q).
   float pv[2] = {-INFINITY, -INFINITY}, pz[2] = {0.0f, 0.0f}, pq[2] = {0.0f, 0.0f};
   int pi[2] = {INT_MAX, INT_MAX};
   {
     const float2 l2e2 = make_float2(kLog2e, kLog2e);
+    // AE: pass B re-reads the whole slice (keep it in L2); else only a few vectors.
+    const uint64_t polA = AE ? pol_keep : pol_last;
+    float gmax = -INFINITY;
+    int it = 0;
     int vi = tid;
     float4 cz, cq, nz, nq;
     if (vi < nvec) {
-      cz = ld4(zsl, vi * VEC, len, ALIGNED, pol_keep, -INFINITY);
-      cq = ld4(qsl, vi * VEC, len, ALIGNED, pol_keep, 0.0f);
+      cz = ld4(zsl, vi * VEC, len, ALIGNED, polA, -INFINITY);
+      cq = ld4(qsl, vi * VEC, len, ALIGNED, polA, 0.0f);
     }
     for (; vi < nvec; vi += kRapidThreads) {
       const int vn = vi + kRapidThreads;
       if (vn < nvec) {
-        nz = ld4(zsl, vn * VEC, len, ALIGNED, pol_keep, -INFINITY);
-        nq = ld4(qsl, vn * VEC, len, ALIGNED, pol_keep, 0.0f);
+        nz = ld4(zsl, vn * VEC, len, ALIGNED, polA, -INFINITY);
+        nq = ld4(qsl, vn * VEC, len, ALIGNED, polA, 0.0f);
       }
       const float2 s0 = fmul2(make_float2(cz.x, cz.y), invT2);
       const float2 s1 = fmul2(make_float2(cz.z, cz.w), invT2);
       const float vm = fmaxf(fmaxf(s0.x, s0.y), fmaxf(s1.x, s1.y));
-      const float vq = fmaxf(fmaxf(cq.x, cq.y), fmaxf(cq.z, cq.w));
-      m = fmaxf(m, vm);
-      if (vm > thr || vm > pv[0] || vq > pv[1]) {
-        if (vm > thr && isfinite(m)) {
-          // Move the partial sum to a reference at the current maximum (about once per thread).
-          const float nL = m * kLog2e;
-          if (thr == -INFINITY || nL > mL + kRapidSlack) {
-            const float f = (acc.x != 0.0f || acc.y != 0.0f) ? exp2f(mL - nL) : 0.0f;
-            acc = fmul2(acc, make_float2(f, f));
-            mL = nL;
-            thr = (nL + kRapidSlack) * 0.693147180559945f;
-          }
+      // The second peak's key: !AE, U = fl(fl(fma(eta T, q, z)) / T), which bounds zhat/T entry by
+      // entry (p >= 0, every operation monotone and correctly rounded); AE, q.
+      float2 k0, k1;
+      if constexpr (!AE) {
+        k0 = fmul2(ffma2(etaT2, make_float2(cq.x, cq.y), make_float2(cz.x, cz.y)), invT2);
+        k1 = fmul2(ffma2(etaT2, make_float2(cq.z, cq.w), make_float2(cz.z, cz.w)), invT2);
+      } else {
+        k0 = make_float2(cq.x, cq.y);
+        k1 = make_float2(cq.z, cq.w);
+      }
+      const float vk = fmaxf(fmaxf(k0.x, k0.y), fmaxf(k1.x, k1.y));
+      if constexpr (!AE) {
+        // One bound per kGroup consecutive vectors of this thread.
+        gmax = fmaxf(gmax, vk);
+        if ((it & (kGroup - 1)) == kGroup - 1 || vn >= nvec) {
+          s_umax[(it / kGroup) * kRapidThreads + tid] = gmax;
+          ub_t = fmaxf(ub_t, gmax);
+          gmax = -INFINITY;
         }
-        const float sv[4] = {s0.x, s0.y, s1.x, s1.y};
+        ++it;
+      }
+      if (vm > pv[0] || vk > pv[1]) {
         const float zv[4] = {cz.x, cz.y, cz.z, cz.w};
         const float qv[4] = {cq.x, cq.y, cq.z, cq.w};
         const int kb = v0 + vi * VEC;
         // The first entry holding the vector's peak, and its payload (unrolled selects).
         if (vm > pv[0]) {
+          const float sv[4] = {s0.x, s0.y, s1.x, s1.y};
           int e = 3;
           float a = zv[3], b = qv[3];
 #pragma unroll
@@ -257,18 +289,29 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
           pi[0] = kb + e;
           pz[0] = a;
           pq[0] = b;
+          if (vm > thr && isfinite(vm)) {
+            // Move the partial sum to a reference at the new maximum (about once per thread).
+            const float nL = vm * kLog2e;
+            if (thr == -INFINITY || nL > mL + kRapidSlack) {
+              const float f = (acc.x != 0.0f || acc.y != 0.0f) ? exp2f(mL - nL) : 0.0f;
+              acc = fmul2(acc, make_float2(f, f));
+              mL = nL;
+              thr = (nL + kRapidSlack) * 0.693147180559945f;
+            }
+          }
         }
-        if (vq > pv[1]) {
+        if (vk > pv[1]) {
+          const float kv[4] = {k0.x, k0.y, k1.x, k1.y};
           int e = 3;
           float a = zv[3], b = qv[3];
 #pragma unroll
           for (int j = 2; j >= 0; --j)
-            if (qv[j] == vq) {
+            if (kv[j] == vk) {
               e = j;
               a = zv[j];
               b = qv[j];
             }
-          pv[1] = vq;
+          pv[1] = vk;
           pi[1] = kb + e;
           pz[1] = a;
           pq[1] = b;
@@ -287,7 +330,7 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
 
   // CTA statistics: maximum; sums moved to the CTA reference; peaks.
   {
-    const float w = warp_max(m);
+    const float w = warp_max(pv[0]);
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       warp_argmax_pl(pv[k], pi[k], pz[k], pq[k]);
@@ -405,14 +448,17 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
   rc.head_scale = 0.0f;
   rc.tail_scale = 1.0f;
 
-  // ---------------------------------------------------------------- pass B (L2)
+  // ---------------------------------------------------------------- pass B
+  // AE: every entry (L2), with head candidates and the all-entry sums.  Otherwise only the vectors
+  // whose bound max U reaches L0 + ln(tail_frac): the maximum of zhat/T (>= L0) and every head entry
+  // (>= Mh + ln(tail_frac) >= L0 + ln(tail_frac)) lie there, since zhat/T <= U.
   float L = rs.L0;  // bound: L0, raised by this thread's own entries; ends as its max of zhat/T
   float c0z = 0.0f, c0p = 0.0f, c1z = 0.0f, c1p = 0.0f;  // head candidates (zhat/T, p)
   int nc = 0;
   bool ovf = false;
   float2 aacc = make_float2(0.0f, 0.0f), pall = make_float2(0.0f, 0.0f);
   float aL = ref_of(L), athr = isfinite(L) ? (aL + kRapidSlack) * 0.693147180559945f : -INFINITY;
-  if (finite) {
+  if (AE && finite) {
     const float2 nML2 = make_float2(-rc.ML, -rc.ML);
     const float2 inv2 = make_float2(rc.inv_sum, rc.inv_sum);
     float cthr = cand_on ? L + ln_tf : INFINITY;
@@ -488,6 +534,27 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
       cq = nq;
     }
   }
+  if (!AE && finite && ub_t >= L + ln_tf) {
+    const float2 nML2 = make_float2(-rc.ML, -rc.ML);
+    const float2 inv2 = make_float2(rc.inv_sum, rc.inv_sum);
+    const float thrU = L + ln_tf;
+    for (int g = 0; g * kGroup * kRapidThreads + tid < nvec; ++g) {
+      if (s_umax[g * kRapidThreads + tid] >= thrU) {
+#pragma unroll
+        for (int r = 0; r < kGroup; ++r) {
+          const int vi = (g * kGroup + r) * kRapidThreads + tid;
+          if (vi < nvec) {
+            const float4 z4 = ld4c(zsl, vi * VEC, len, ALIGNED, -INFINITY);
+            const float4 q4 = ld4c(qsl, vi * VEC, len, ALIGNED, 0.0f);
+            float2 p0, p1, h0, h1;
+            pzhs2(make_float2(z4.x, z4.y), make_float2(q4.x, q4.y), invT2, nML2, inv2, etaT2, p0, h0);
+            pzhs2(make_float2(z4.z, z4.w), make_float2(q4.z, q4.w), invT2, nML2, inv2, etaT2, p1, h1);
+            L = fmaxf(L, fmaxf(fmaxf(h0.x, h0.y), fmaxf(h1.x, h1.y)));
+          }
+        }
+      }
+    }
+  }
   {
     const float w = warp_max(L);
     if (lane == 0) s_w[warp][3] = w;
@@ -555,7 +622,31 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
   // ---------------------------------------------------------------- head sums
   {
     float hp = 0.0f, he = 0.0f;
-    if (finite && cand_on) {
+    if (!AE && finite && ub_t >= rc.thr) {
+      // The head lies in the vectors whose bound reaches the boundary (re-read, normally from L1).
+      for (int g = 0; g * kGroup * kRapidThreads + tid < nvec; ++g) {
+        if (s_umax[g * kRapidThreads + tid] >= rc.thr) {
+          for (int r = 0; r < kGroup; ++r) {
+            const int vi = (g * kGroup + r) * kRapidThreads + tid;
+            if (vi >= nvec) break;
+            const float4 z4 = ld4c(zsl, vi * VEC, len, ALIGNED, -INFINITY);
+            const float4 q4 = ld4c(qsl, vi * VEC, len, ALIGNED, 0.0f);
+            const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
+            const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float pk, zh;
+              rapid_p_zhs(zz[e], qq[e], rc, pk, zh);
+              if (zh >= rc.thr) {
+                hp += pk;
+                he += head_exp(zh, rc.zhmax);
+              }
+            }
+          }
+        }
+      }
+    }
+    if (AE && finite && cand_on) {
       if (!cta_ovf) {
         if (nc >= 1 && c0z >= rc.thr) {
           hp += c0p;
@@ -701,12 +792,18 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
 // request (no cluster), each over its slice of the stop row, race all entries once for both
 // weightings (exponential race, argmin_k E_k / w_k, E_k = -ln u_k with the same uniform): the
 // residual max(p - protected, p - q, 0) (at the bonus position the protected target), and p, which
-// decides only if every residual weight is zero.  A CTA's winners go into the job's slots with one
-// 64-bit atomic max each (key bits above the index, inverted, so the smaller key and then the lower
-// index win); the last CTA of the request writes the token and clears the job.
-__global__ void __launch_bounds__(kRapidThreads) rapid_draw_kernel(const RapidArgs p) {
+// decides only if every residual weight is zero.  Pruning keeps the result exact: E_k > 1 - u_k
+// (1 - u_k exact, at least 2^-24), so an entry with (1 - u_k) >= w_k K (1 + 2^-20), K the best key
+// its warp has seen, has a key (as computed: logf, one division) above K and cannot win; the
+// logarithm and the division are skipped for it, and Philox for a vector where even 1 - u = 2^-24
+// cannot win.  A CTA's winners go into the job's slots with one 64-bit atomic max each (key bits
+// above the index, inverted, so the smaller key and then the lower index win); the last CTA of the
+// request writes the token and clears the job.
+__global__ void __launch_bounds__(kDrawThreads) rapid_draw_kernel(const RapidArgs p) {
   constexpr int VEC = 4;
-  constexpr int kWarps = kRapidThreads / 32;
+  constexpr int kWarps = kDrawThreads / 32;
+  constexpr float kMargin = 1.0f + 0x1p-20f;
+  constexpr float kMinOneMinusU = 0x1p-24f;
   __shared__ unsigned long long s_best[kWarps][2];
   __shared__ uint32_t s_last;
   const int tid = threadIdx.x;
@@ -739,38 +836,80 @@ __global__ void __launch_bounds__(kRapidThreads) rapid_draw_kernel(const RapidAr
   const float* qr = p.q + nbase;
   const bool al = p.bulk != 0;
   const uint64_t pol = policy_evict_first();
-  // Packed, inverted: larger is better; 0 = nothing yet.
-  unsigned long long best[2] = {0ull, 0ull};
-  for (int vi = tid; vi < nvec; vi += kRapidThreads) {
-    const int kl = vi * VEC;
-    const int kb = v0 + kl;
-    const float4 z4 = ld4(zr, kl, len, al, pol, -INFINITY);
-    const float4 q4 = ld4(qr, kl, len, al, pol, 0.0f);
-    const Philox4 r4 =
-        philox4x32_10(uint32_t(kb >> 2), uint32_t(n), uint32_t(req), stream + 4u * p.offset, p.seed_lo, p.seed_hi);
-    const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
-    const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+  const int iters = (nvec + kDrawThreads - 1) / kDrawThreads;  // uniform over the CTA
+  // Aligned rows: every vector of the thread is copied to shared memory at once (one round trip
+  // to memory instead of one per vector); each thread reads back only its own copies.
+  extern __shared__ float4 s_stage[];  // [iters][z, q][kDrawThreads]
+  if (al) {
+    for (int it = 0; it < iters; ++it) {
+      const int vi = it * kDrawThreads + tid;
+      if (vi < nvec) {
+        cp_async16(smem_addr(&s_stage[(2 * it + 0) * kDrawThreads + tid]), zr + vi * VEC, pol);
+        cp_async16(smem_addr(&s_stage[(2 * it + 1) * kDrawThreads + tid]), qr + vi * VEC, pol);
+      }
+    }
+    cp_async_wait_all();
+  }
+  float key[2] = {INFINITY, INFINITY};  // this thread's best keys and their indices
+  int idx[2] = {INT_MAX, INT_MAX};
+  float bound[2] = {INFINITY, INFINITY};  // the best keys its warp has seen (pruning bound)
+  for (int it = 0; it < iters; ++it) {
+    const int vi = it * kDrawThreads + tid;
+    if (vi < nvec) {
+      const int kl = vi * VEC;
+      const int kb = v0 + kl;
+      const float4 z4 = al ? s_stage[(2 * it + 0) * kDrawThreads + tid] : ld4(zr, kl, len, false, pol, -INFINITY);
+      const float4 q4 = al ? s_stage[(2 * it + 1) * kDrawThreads + tid] : ld4(qr, kl, len, false, pol, 0.0f);
+      const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
+      const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+      float w[2][4];
+      bool any = false;
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-      if (kl + e < len) {
+      for (int e = 0; e < VEC; ++e) {
         float pk, zhs, prot;
         rapid_entry(zz[e], qq[e], dc, pk, zhs, prot);
-        const float w0 = (n < G) ? fmaxf(fmaxf(pk - prot, pk - qq[e]), 0.0f) : prot;
-        if (w0 > 0.0f || pk > 0.0f) {
-          const float E = -logf(uniform_from_word(r4.v[e]));
-          const unsigned long long idx = uint32_t(kb + e);
-          if (w0 > 0.0f) {
-            const unsigned long long c = ~((static_cast<unsigned long long>(__float_as_uint(E / w0)) << 32) | idx);
-            best[0] = c > best[0] ? c : best[0];
-          }
-          if (pk > 0.0f) {
-            const unsigned long long c = ~((static_cast<unsigned long long>(__float_as_uint(E / pk)) << 32) | idx);
-            best[1] = c > best[1] ? c : best[1];
+        const bool in = kl + e < len;
+        w[0][e] = in ? ((n < G) ? fmaxf(fmaxf(pk - prot, pk - qq[e]), 0.0f) : prot) : 0.0f;
+        w[1][e] = in ? pk : 0.0f;
+#pragma unroll
+        for (int s = 0; s < 2; ++s) any |= w[s][e] > 0.0f && !(kMinOneMinusU >= w[s][e] * bound[s] * kMargin);
+      }
+      if (any) {
+        const Philox4 r4 =
+            philox4x32_10(uint32_t(kb >> 2), uint32_t(n), uint32_t(req), stream + 4u * p.offset, p.seed_lo, p.seed_hi);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          const float u = uniform_from_word(r4.v[e]);
+          const float lo = 1.0f - u;  // exact
+          bool cand[2];
+#pragma unroll
+          for (int s = 0; s < 2; ++s) cand[s] = w[s][e] > 0.0f && !(lo >= w[s][e] * bound[s] * kMargin);
+          if (cand[0] || cand[1]) {
+            const float E = -logf(u);
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+              if (cand[s]) {
+                const float k = E / w[s][e];
+                if (k < key[s]) {  // entries arrive in increasing index: ties keep the earlier one
+                  key[s] = k;
+                  idx[s] = kb + e;
+                }
+              }
+            }
           }
         }
       }
     }
+    // Share the bound across the warp (non-negative floats order like their bit patterns).
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+      bound[s] = __uint_as_float(__reduce_min_sync(0xffffffffu, __float_as_uint(fminf(bound[s], key[s]))));
   }
+  unsigned long long best[2];
+#pragma unroll
+  for (int s = 0; s < 2; ++s)
+    best[s] = (idx[s] == INT_MAX) ? 0ull
+                                  : ~((static_cast<unsigned long long>(__float_as_uint(key[s])) << 32) | uint32_t(idx[s]));
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
 #pragma unroll
@@ -808,11 +947,12 @@ int rapid_ctas_per_sm() { return kRapidCtasPerSm; }
 
 namespace {
 
-cudaLaunchConfig_t cluster_config(unsigned ctas, unsigned cluster, cudaLaunchAttribute* attr, cudaStream_t s) {
+cudaLaunchConfig_t cluster_config(unsigned ctas, unsigned cluster, size_t smem, cudaLaunchAttribute* attr,
+                                  cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas, 1, 1);
   cfg.blockDim = dim3(unsigned(kRapidThreads), 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cluster;
@@ -829,25 +969,42 @@ cudaError_t allow_cluster(K kern, int cluster) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
+template <typename K>
+cudaError_t prepare(K kern, const LaunchPlan& plan) {
+  cudaError_t e = allow_cluster(kern, plan.cluster);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem);
+}
+
 template <bool AL, bool AE>
 cudaError_t launch_verify(const RapidArgs& a, const LaunchPlan& plan, cudaStream_t s) {
   auto kern = rapid_kernel<AL, AE>;
-  cudaError_t e = allow_cluster(kern, plan.cluster);
+  cudaError_t e = prepare(kern, plan);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
-  const cudaLaunchConfig_t cfg =
-      cluster_config(unsigned(a.B * (a.G + 1)) * unsigned(plan.cluster), unsigned(plan.cluster), attr, s);
+  const cudaLaunchConfig_t cfg = cluster_config(unsigned(a.B * (a.G + 1)) * unsigned(plan.cluster),
+                                                unsigned(plan.cluster), size_t(plan.smem), attr, s);
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace
 
-static bool rapid_needs_all_sums(const RapidArgs& a) { return a.tail_mode != 0 || !(a.ln_tail_frac > -INFINITY); }
+bool rapid_needs_all_sums(int tail_mode, float ln_tail_frac) { return tail_mode != 0 || !(ln_tail_frac > -INFINITY); }
+
+int rapid_draw_smem_bytes(int n_slice, bool aligned) {
+  const int iters = (n_slice / 4 + kDrawThreads - 1) / kDrawThreads;
+  return aligned ? iters * 2 * kDrawThreads * 16 : 0;
+}
+
+int rapid_smem_bytes(bool all_sums, int n_slice) {
+  const int iters = (n_slice / 4 + kRapidThreads - 1) / kRapidThreads;
+  return all_sums ? 0 : (iters + kGroup - 1) / kGroup * kRapidThreads * 4;
+}
 
 // Two launches on the stream: the verification (every row), then the draws (draw_ctas CTAs per
 // request, with slices of their own: n_slice is recomputed for them).
 cudaError_t launch_rapid(const RapidArgs& a, const LaunchPlan& plan, cudaStream_t s) {
-  const bool ae = rapid_needs_all_sums(a);
+  const bool ae = rapid_needs_all_sums(a.tail_mode, a.ln_tail_frac);
   cudaError_t e;
   if (plan.bulk) e = ae ? launch_verify<true, true>(a, plan, s) : launch_verify<true, false>(a, plan, s);
   else e = ae ? launch_verify<false, true>(a, plan, s) : launch_verify<false, false>(a, plan, s);
@@ -855,25 +1012,22 @@ cudaError_t launch_rapid(const RapidArgs& a, const LaunchPlan& plan, cudaStream_
   RapidArgs b = a;
   const int parts = a.draw_ctas;
   b.n_slice = ((a.V + parts - 1) / parts + 3) / 4 * 4;
-  rapid_draw_kernel<<<unsigned(a.B) * unsigned(parts), kRapidThreads, 0, s>>>(b);
+  const int smem = rapid_draw_smem_bytes(b.n_slice, a.bulk != 0);
+  e = cudaFuncSetAttribute(rapid_draw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  rapid_draw_kernel<<<unsigned(a.B) * unsigned(parts), kDrawThreads, size_t(smem), s>>>(b);
   return cudaGetLastError();
 }
 
 int rapid_max_active_clusters(const LaunchPlan& plan) {
   auto kern = rapid_kernel<true, false>;
-  if (plan.cluster > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+  if (prepare(kern, plan) != cudaSuccess) {
+    cudaGetLastError();
     return 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(plan.cluster), 1, 1);
-  cfg.blockDim = dim3(unsigned(kRapidThreads), 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  }
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = unsigned(plan.cluster);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  const cudaLaunchConfig_t cfg = cluster_config(unsigned(plan.cluster), unsigned(plan.cluster), size_t(plan.smem),
+                                                attr, nullptr);
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
     cudaGetLastError();
