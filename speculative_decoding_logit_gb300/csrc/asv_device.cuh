@@ -50,6 +50,14 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Wait until at most N of this thread's committed copy groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ------------------------------------------------------------------ GPU-scope synchronisation
 // Release/acquire operations at GPU scope for flags that CTAs of one launch exchange through
 // global memory.

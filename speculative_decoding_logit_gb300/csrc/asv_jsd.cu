@@ -38,7 +38,7 @@
 // reference pass B uses, so the divergence sums and the row sums share one scale.  The constant
 // rounding error of ML is removed from the log-sum-exps.  The gate is decided in double in the log
 // domain.  The per-entry divergence term is evaluated from u = (xb - xa) - (lse_b - lse_a):
-//   narrow form (|u| <= 2): sqrt(p q) u^2 R(u^2), R an even-symmetric fitted polynomial;
+//   narrow form (|u| <= 4): sqrt(p q) u^2 R(u^2), R an even-symmetric fitted polynomial;
 //   wide form (any u):      max(p,q) (A(r) - |u| r), r = exp(-|u|), A(r) = (1 - r) B(r).
 // Both are sums of non-negative terms (no cancellation between large entropies), and identical rows
 // give exactly 0.  Loads carry L2 cache policies: the divergence pair is marked evict-last in pass A
@@ -55,6 +55,8 @@ namespace asv {
 
 constexpr int kJsdThreads = 256;  // threads per CTA the kernel is compiled for (launch bounds)
 constexpr int kJsdCtasPerSm = 4;  // CTAs per SM the kernel is compiled for (launch bounds)
+
+constexpr int kRing = 4;  // pass-B vectors in flight per input per thread (a power of 2)
 
 constexpr int kMaxArg = 4;  // argmax slots: fused scores for up to 4 betas, or 1 beta and the plain target
 constexpr int kMaxGamma = 8;  // gammas of one sweep
@@ -307,6 +309,9 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
 
   __shared__ JsdXchg xchg;
   __shared__ JsdRowConsts rc;
+  // Pass B ring (aligned slices): [kRing][NPB][kJsdThreads] 16-byte vectors.
+  constexpr int NPB = FUSE ? 3 : 2;
+  extern __shared__ __align__(16) uint4 s_ring[];
   __shared__ float s_wf[kWarps][6];
   __shared__ float s_av[kWarps][kMaxArg];
   __shared__ int32_t s_ai[kWarps][kMaxArg];
@@ -626,7 +631,40 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
         }
       }
     };
-    if (finite) {
+    if (finite && ALIGNED) {
+      // Aligned slices: a ring of kRing vectors per input per thread, filled by 16-byte cp.async
+      // copies from L2 (no registers held by copies in flight).  Each thread reads only its own
+      // slots, and refills a slot only after the arithmetic has consumed it.
+      const char* src[3] = {static_cast<const char*>(slice[0]), static_cast<const char*>(slice[1]),
+                            static_cast<const char*>(slice[NT - 1])};
+      auto issue = [&](int j) {
+        const int vi = tid + j * kJsdThreads;
+        if (vi < nvec) {
+#pragma unroll
+          for (int m = 0; m < NPB; ++m)
+            cp_async16(smem_addr(&s_ring[((j & (kRing - 1)) * NPB + m) * kJsdThreads + tid]),
+                       src[m] + size_t(vi) * 16u, pol_last);
+        }
+        cp_async_commit();
+      };
+#pragma unroll
+      for (int j = 0; j < kRing; ++j) issue(j);
+      for (int j = 0; tid + j * kJsdThreads < nvec; ++j) {
+        cp_async_wait_group<kRing - 1>();  // the copies of vector j have landed
+        const int slot = (j & (kRing - 1)) * NPB;
+        float2 xa[NP], xb[NP];
+        G::pairs(s_ring[(slot + 0) * kJsdThreads + tid], xa);
+        G::pairs(s_ring[(slot + 1) * kJsdThreads + tid], xb);
+        pair_terms(xa, xb, rb, accn, an, ap, aq);
+        if constexpr (FUSE) {
+          float2 xt[NP];
+          G::pairs(s_ring[(slot + 2) * kJsdThreads + tid], xt);
+          pair_terms(xa, xt, rb2, accn2, an2, ap2, aq2);
+        }
+        issue(j + kRing);
+      }
+      cp_async_wait_all();
+    } else if (finite) {
       int vi = tid;
       uint4 ca, cb, ct, na, nb, nt;
       if (vi < nvec) {
@@ -1018,11 +1056,17 @@ static JsdKernel pick_kernel(int mode, int dtype, int dsrc, bool aligned, int va
   return aligned ? pick_aligned<true>(mode, dtype, dsrc, variant) : pick_aligned<false>(mode, dtype, dsrc, variant);
 }
 
-static cudaLaunchConfig_t make_config(const LaunchPlan& plan, unsigned grid, cudaStream_t s, cudaLaunchAttribute* attr) {
+// Dynamic shared memory: the pass-B ring of the aligned instantiations.
+static int ring_bytes(bool aligned, int variant) {
+  return aligned ? kRing * (variant == 2 ? 3 : 2) * kJsdThreads * 16 : 0;
+}
+
+static cudaLaunchConfig_t make_config(const LaunchPlan& plan, unsigned grid, int smem, cudaStream_t s,
+                                      cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(unsigned(kJsdThreads), 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = size_t(smem);
   cfg.stream = s;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = unsigned(plan.cluster);
@@ -1033,14 +1077,18 @@ static cudaLaunchConfig_t make_config(const LaunchPlan& plan, unsigned grid, cud
   return cfg;
 }
 
-static cudaError_t prepare(JsdKernel kern, const LaunchPlan& plan) {
-  if (plan.cluster > 8) return cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  return cudaSuccess;
+static cudaError_t prepare(JsdKernel kern, const LaunchPlan& plan, int smem) {
+  if (plan.cluster > 8) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
 cudaError_t launch_jsd_family(int mode, int dtype, const JsdArgs& a, const LaunchPlan& plan, cudaStream_t s) {
   JsdKernel kern = pick_kernel(mode, dtype, a.delta_source, a.bulk != 0, a.variant);
-  cudaError_t e = prepare(kern, plan);
+  const int smem = ring_bytes(a.bulk != 0, a.variant);
+  cudaError_t e = prepare(kern, plan, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   // Rows launched: every row, or (E2-SCI pre-hit) row 0 of each request, then rows 1..K.
@@ -1048,15 +1096,19 @@ cudaError_t launch_jsd_family(int mode, int dtype, const JsdArgs& a, const Launc
                         : a.prehit_phase == 2 ? unsigned(a.B) * unsigned(a.K)
                                               : unsigned(a.B) * unsigned(a.K + 1);
   const unsigned grid = rows * unsigned(plan.cluster);
-  cudaLaunchConfig_t cfg = make_config(plan, grid, s, attr);
+  cudaLaunchConfig_t cfg = make_config(plan, grid, smem, s, attr);
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 int jsd_max_active_clusters(int mode, int dtype, const LaunchPlan& plan) {
   JsdKernel kern = pick_kernel(mode, dtype, 0, plan.bulk != 0, 0);
-  if (prepare(kern, plan) != cudaSuccess) return 0;
+  const int smem = ring_bytes(plan.bulk != 0, 0);
+  if (prepare(kern, plan, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = make_config(plan, unsigned(plan.cluster), 0, attr);
+  cudaLaunchConfig_t cfg = make_config(plan, unsigned(plan.cluster), smem, 0, attr);
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
     cudaGetLastError();

@@ -31,8 +31,8 @@ import mpmath as mp
 import numpy as np
 
 mp.mp.dps = 50
-U0 = 2.0
-DEG = 6  # degree of R in s = u^2
+U0 = 4.0
+DEG = 10  # degree of R in s = u^2
 
 
 def f(u):
