@@ -346,6 +346,14 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
 #pragma unroll
   for (int j = 0; j < NT; ++j) slice[j] = static_cast<const char*>(p.x[j]) + (row_base + size_t(v0)) * G::kBytes;
 
+  // The finalising warp (warp 0 of CTA 0) needs the row's draft token and, for the gate, its
+  // verifier and compressed-drafter logits: lanes 1 and 2 load the token now and the logits after
+  // pass A, so the loads' latency is not on the row's critical path (single-outcome kernels; the
+  // multi-outcome ones, short of registers, load them when they finalise).
+  const bool fin_lane = !kMulti && rank == 0 && warp == 0 && (lane == 1 || lane == 2);
+  int d_pre = -1;
+  if (fin_lane && pos < p.K) d_pre = __ldg(p.draft_ids + size_t(req) * p.K + pos);
+
   // L2 policies: the verifier input is read once (evict first; fused: pass B reads it again); the
   // divergence pair is read again by pass B (evict last until then, evict first on that last read).
   const uint64_t pol_last = policy_evict_first();
@@ -449,6 +457,10 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
       for (int j = 0; j < NT; ++j) cur[j] = nxt[j];
     }
   }
+
+  float xd_pre = 0.0f;
+  if (MODE == kModeAsym && fin_lane && d_pre >= 0 && d_pre < V)
+    xd_pre = G::at(p.x[lane == 1 ? NT - 1 : 1], row_base + size_t(d_pre));
 
   // CTA maxima, then every thread moves its sum to the CTA reference and the sums are added.
 #pragma unroll
@@ -601,8 +613,11 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
     float2 accn = make_float2(0.0f, 0.0f), accn2 = make_float2(0.0f, 0.0f);
     float an = 0.0f, ap = 0.0f, aq = 0.0f, an2 = 0.0f, ap2 = 0.0f, aq2 = 0.0f;
     // One vector of the pair (xa, xb) against row constants rb.
+    // sh: the short narrow form (|u| <= 3, fewer terms), for the AsymSpec pair, whose u stays small;
+    // the E2-SCI pair (draft, target) spreads wider and takes the |u| <= 4 form.
     auto pair_terms = [&](const float2 (&xa)[NP], const float2 (&xb)[NP], const RowB& r, float2& acn, float& sn,
-                          float& sp, float& sq) {
+                          float& sp, float& sq, const bool sh) {
+      const float kS0 = sh ? ASV_JSD_SHORT_S0 : ASV_JSD_EVEN_S0;
       const float2 dl2 = make_float2(r.dL, r.dL);
       const float2 hl2e2 = make_float2(0.5f * kLog2e, 0.5f * kLog2e);
       const float2 nhml2 = make_float2(-r.hML, -r.hML);
@@ -612,16 +627,25 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
         const float2 uu = fsub2(fsub2(xb[q2], xa[q2]), dl2);
         s2[q2] = fmul2(uu, uu);
       }
-      // Narrow form for the whole vector unless one entry is outside it (or NaN: -inf pairs).
-      float smax = fmax_nan(s2[0].x, s2[0].y);
+      // Narrow form for the whole vector unless one entry is outside it (or NaN: -inf pairs).  The
+      // terms are non-negative, so a sum within the domain puts every entry in it (a NaN fails the
+      // test); only when the sum is outside are the entries checked one by one.
+      float2 ss = s2[0];
 #pragma unroll
-      for (int q2 = 1; q2 < NP; ++q2) smax = fmax_nan(smax, fmax_nan(s2[q2].x, s2[q2].y));
-      if (smax <= ASV_JSD_EVEN_S0) {
+      for (int q2 = 1; q2 < NP; ++q2) ss = fadd2(ss, s2[q2]);
+      bool narrow = (ss.x + ss.y) <= kS0;
+      if (!narrow) {
+        float smax = fmax_nan(s2[0].x, s2[0].y);
+#pragma unroll
+        for (int q2 = 1; q2 < NP; ++q2) smax = fmax_nan(smax, fmax_nan(s2[q2].x, s2[q2].y));
+        narrow = smax <= kS0;
+      }
+      if (narrow) {
 #pragma unroll
         for (int q2 = 0; q2 < NP; ++q2) {
           const float2 y = ffma2(fadd2(xa[q2], xb[q2]), hl2e2, nhml2);
           const float2 e = make_float2(ex2_approx(y.x), ex2_approx(y.y));
-          acn = ffma2(fmul2(e, s2[q2]), asv_jsd_even2(s2[q2]), acn);
+          acn = ffma2(fmul2(e, s2[q2]), sh ? asv_jsd_short2(s2[q2]) : asv_jsd_even2(s2[q2]), acn);
         }
       } else {
 #pragma unroll
@@ -631,6 +655,7 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
         }
       }
     };
+    constexpr bool kPairShort = MODE == kModeAsym;
     if (finite && ALIGNED) {
       // Aligned slices: a ring of kRing vectors per input per thread, filled by 16-byte cp.async
       // copies from L2 (no registers held by copies in flight).  Each thread reads only its own
@@ -655,11 +680,11 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
         float2 xa[NP], xb[NP];
         G::pairs(s_ring[(slot + 0) * kJsdThreads + tid], xa);
         G::pairs(s_ring[(slot + 1) * kJsdThreads + tid], xb);
-        pair_terms(xa, xb, rb, accn, an, ap, aq);
+        pair_terms(xa, xb, rb, accn, an, ap, aq, kPairShort);
         if constexpr (FUSE) {
           float2 xt[NP];
           G::pairs(s_ring[(slot + 2) * kJsdThreads + tid], xt);
-          pair_terms(xa, xt, rb2, accn2, an2, ap2, aq2);
+          pair_terms(xa, xt, rb2, accn2, an2, ap2, aq2, false);
         }
         issue(j + kRing);
       }
@@ -682,11 +707,11 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
         float2 xa[NP], xb[NP];
         G::pairs(ca, xa);
         G::pairs(cb, xb);
-        pair_terms(xa, xb, rb, accn, an, ap, aq);
+        pair_terms(xa, xb, rb, accn, an, ap, aq, kPairShort);
         if constexpr (FUSE) {
           float2 xt[NP];
           G::pairs(ct, xt);
-          pair_terms(xa, xt, rb2, accn2, an2, ap2, aq2);
+          pair_terms(xa, xt, rb2, accn2, an2, ap2, aq2, false);
           ct = nt;
         }
         ca = na;
@@ -733,11 +758,11 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
   const unsigned kAll = 0xffffffffu;
   const int K = p.K;
   const bool finite = rc.finite != 0;
-  // The draft token's verifier and compressed-drafter logits (lanes 1, 2), loaded early.
-  const int d = (pos < K) ? p.draft_ids[size_t(req) * K + pos] : -1;
+  // The draft token and its verifier / compressed-drafter logits (lanes 1, 2), loaded early.
+  const int d = (pos < K) ? (kMulti ? p.draft_ids[size_t(req) * K + pos] : __shfl_sync(kAll, d_pre, 1)) : -1;
   const bool d_ok = d >= 0 && d < V;
-  float xd = 0.0f;
-  if (MODE == kModeAsym && finite && d_ok && (lane == 1 || lane == 2))
+  float xd = xd_pre;
+  if (kMulti && MODE == kModeAsym && finite && d_ok && (lane == 1 || lane == 2))
     xd = G::at(p.x[lane == 1 ? NT - 1 : 1], row_base + size_t(d));
   // Pass-B sums of the cluster's CTAs, in rank order (lane q holds CTA q's).
   DF jn{0.0f, 0.0f}, jp{0.0f, 0.0f}, jq{0.0f, 0.0f};

@@ -17,6 +17,10 @@ Wide form (any u): with m = max(p, q), s = |u| and r = e^-s = min(p,q)/max(p,q),
 the entry's share is m * (A(r) - s*r) with A(r) = (1 + r) ln(2 / (1 + r)), and
 A(r) = (1 - r) * B(r) with B smooth on [0, 1] (B(0) = ln 2, B(1) = 1).
 
+A second, shorter narrow form (|u| <= U1 = 3, R of degree DEG1 = 7) serves pairs whose u stays
+small (the AsymSpec pair a, b): it is as accurate as the wide-domain one in fp32 and three
+multiply-adds shorter.
+
 Both R and B are fitted here in 50-digit arithmetic by least squares in
 relative error on Chebyshev nodes; coefficients are rounded to fp32 one at a
 time from the highest degree down, each rounding followed by a refit of the
@@ -33,6 +37,8 @@ import numpy as np
 mp.mp.dps = 50
 U0 = 4.0
 DEG = 10  # degree of R in s = u^2
+U1 = 3.0
+DEG1 = 7  # degree of the short form's R
 
 
 def f(u):
@@ -145,6 +151,13 @@ def main():
     xs32 = xs.astype(np.float32)
     acc = horner32(coef, xs32)
     err32 = float(max(abs(float(acc[i]) / float(Rfun(float(xs32[i]))) - 1) for i in range(len(xs))))
+    S1 = U1 * U1
+    coef1 = fit_rounded(Rfun, DEG1, 0.0, S1)
+    xs1 = np.linspace(0.0, S1, 4001)
+    err1 = float(max(abs(sum(mp.mpf(coef1[d]) * mp.mpf(x) ** d for d in range(DEG1 + 1)) / Rfun(x) - 1) for x in xs1))
+    xs1_32 = xs1.astype(np.float32)
+    acc1 = horner32(coef1, xs1_32)
+    err1_32 = float(max(abs(float(acc1[i]) / float(Rfun(float(xs1_32[i]))) - 1) for i in range(len(xs1))))
     out = os.path.join(os.path.dirname(os.path.abspath(__file__)), "jsd_poly.inc")
     with open(out, "w") as fh:
         fh.write("// Generated by gen_jsd_poly.py -- do not edit.\n")
@@ -152,12 +165,17 @@ def main():
         fh.write(f"//   max relative error of R: {err:.3e} (exact arithmetic), {err32:.3e} (fp32 Horner).\n")
         fh.write(f"// Wide form: A(r) = (1 - r) * B(r) on [0, 1], B of degree {R_DEG}.\n")
         fh.write(f"//   max relative error of B: {berr:.3e} (exact arithmetic), {berr32:.3e} (fp32 Horner).\n")
+        fh.write(f"// Short narrow form: |u| <= {U1}, R of degree {DEG1} in u^2.\n")
+        fh.write(f"//   max relative error of R: {err1:.3e} (exact arithmetic), {err1_32:.3e} (fp32 Horner).\n")
         fh.write(f"#define ASV_JSD_EVEN_S0 {S0:.1f}f\n")
+        fh.write(f"#define ASV_JSD_SHORT_S0 {S1:.1f}f\n")
         emit(fh, "asv_jsd_even", "s", coef)
         emit(fh, "asv_jsd_wide_b", "r", bcoef)
         emit2(fh, "asv_jsd_even2", "s", coef)
         emit2(fh, "asv_jsd_wide_b2", "r", bcoef)
-    print(f"wrote {out}: R rel err {err:.3e} exact, {err32:.3e} fp32; B rel err {berr:.3e} exact, {berr32:.3e} fp32")
+        emit2(fh, "asv_jsd_short2", "s", coef1)
+    print(f"wrote {out}: R rel err {err:.3e} exact, {err32:.3e} fp32; B rel err {berr:.3e} exact, {berr32:.3e} fp32; "
+          f"short R rel err {err1:.3e} exact, {err1_32:.3e} fp32")
 
 
 if __name__ == "__main__":
