@@ -381,19 +381,8 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
     float2 beta2[NB];
 #pragma unroll
     for (int s = 0; s < NB; ++s) beta2[s] = make_float2(p.betas[s], p.betas[s]);
-    uint4 cur[NT], nxt[NT];
-    int vi = tid;
-    if (vi < nvec) {
-#pragma unroll
-      for (int j = 0; j < NT; ++j) cur[j] = G::load(slice[j], vi * VEC, len, aligned, true, j == 2 ? pol_t : pol_keep);
-    }
-    for (; vi < nvec; vi += kJsdThreads) {
-      const int vn = vi + kJsdThreads;
-      // Prefetch the next vector (consumed only while it is in range).
-      if (vn < nvec) {
-#pragma unroll
-        for (int j = 0; j < NT; ++j) nxt[j] = G::load(slice[j], vn * VEC, len, aligned, true, j == 2 ? pol_t : pol_keep);
-      }
+    // One vector (entries [vi*VEC, vi*VEC + VEC) of the slice) of every input into the pass-A state.
+    auto a_body = [&](const uint4 (&cur)[NT], const int vi) {
       // Running maxima; when a value passes the reference's slack, move the partial sum to a new
       // reference at the current maximum.
       bool far = false;
@@ -453,8 +442,44 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
           bi[sl] = v0 + vi * VEC + e_first;
         }
       }
+    };
+    uint4 cur[NT], nxt[NT];
+    int vi = tid;
+    if (vi < nvec) {
 #pragma unroll
-      for (int j = 0; j < NT; ++j) cur[j] = nxt[j];
+      for (int j = 0; j < NT; ++j) cur[j] = G::load(slice[j], vi * VEC, len, aligned, true, j == 2 ? pol_t : pol_keep);
+    }
+    if constexpr (!kMulti && ALIGNED) {
+      // Two vectors per trip, the prefetch alternating between cur and nxt (no register copies);
+      // a prefetched vector is consumed only while it is in range.
+      for (; vi < nvec; vi += 2 * kJsdThreads) {
+        if (vi + kJsdThreads < nvec) {
+#pragma unroll
+          for (int j = 0; j < NT; ++j)
+            nxt[j] = G::load(slice[j], (vi + kJsdThreads) * VEC, len, aligned, true, j == 2 ? pol_t : pol_keep);
+        }
+        a_body(cur, vi);
+        if (vi + kJsdThreads >= nvec) break;
+        if (vi + 2 * kJsdThreads < nvec) {
+#pragma unroll
+          for (int j = 0; j < NT; ++j)
+            cur[j] = G::load(slice[j], (vi + 2 * kJsdThreads) * VEC, len, aligned, true, j == 2 ? pol_t : pol_keep);
+        }
+        a_body(nxt, vi + kJsdThreads);
+      }
+    } else {
+      // Multi-outcome kernels (more state, short of registers) and element-wise loads of unaligned
+      // rows: one vector per trip.
+      for (; vi < nvec; vi += kJsdThreads) {
+        if (vi + kJsdThreads < nvec) {
+#pragma unroll
+          for (int j = 0; j < NT; ++j)
+            nxt[j] = G::load(slice[j], (vi + kJsdThreads) * VEC, len, aligned, true, j == 2 ? pol_t : pol_keep);
+        }
+        a_body(cur, vi);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) cur[j] = nxt[j];
+      }
     }
   }
 

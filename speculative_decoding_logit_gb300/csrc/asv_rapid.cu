@@ -234,17 +234,9 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
     float gmax = -INFINITY;
     int it = 0;
     int vi = tid;
-    float4 cz, cq, nz, nq;
-    if (vi < nvec) {
-      cz = ld4(zsl, vi * VEC, len, ALIGNED, polA, -INFINITY);
-      cq = ld4(qsl, vi * VEC, len, ALIGNED, polA, 0.0f);
-    }
-    for (; vi < nvec; vi += kRapidThreads) {
+    // One vector (entries [vi*VEC, vi*VEC + VEC) of the slice) of z and q into the pass-A state.
+    auto a_body = [&](const float4& cz, const float4& cq, const int vi) {
       const int vn = vi + kRapidThreads;
-      if (vn < nvec) {
-        nz = ld4(zsl, vn * VEC, len, ALIGNED, polA, -INFINITY);
-        nq = ld4(qsl, vn * VEC, len, ALIGNED, polA, 0.0f);
-      }
       const float2 s0 = fmul2(make_float2(cz.x, cz.y), invT2);
       const float2 s1 = fmul2(make_float2(cz.z, cz.w), invT2);
       const float vm = fmaxf(fmaxf(s0.x, s0.y), fmaxf(s1.x, s1.y));
@@ -323,8 +315,26 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
       acc = fadd2(acc, make_float2(ex2_approx(y1.x), ex2_approx(y1.y)));
       qacc = fadd2(qacc, make_float2(cq.x, cq.y));
       qacc = fadd2(qacc, make_float2(cq.z, cq.w));
-      cz = nz;
-      cq = nq;
+    };
+    float4 cz, cq, nz, nq;
+    if (vi < nvec) {
+      cz = ld4(zsl, vi * VEC, len, ALIGNED, polA, -INFINITY);
+      cq = ld4(qsl, vi * VEC, len, ALIGNED, polA, 0.0f);
+    }
+    // Two vectors per trip, the prefetch alternating between (cz, cq) and (nz, nq) (no register
+    // copies); a prefetched vector is consumed only while it is in range.
+    for (; vi < nvec; vi += 2 * kRapidThreads) {
+      if (vi + kRapidThreads < nvec) {
+        nz = ld4(zsl, (vi + kRapidThreads) * VEC, len, ALIGNED, polA, -INFINITY);
+        nq = ld4(qsl, (vi + kRapidThreads) * VEC, len, ALIGNED, polA, 0.0f);
+      }
+      a_body(cz, cq, vi);
+      if (vi + kRapidThreads >= nvec) break;
+      if (vi + 2 * kRapidThreads < nvec) {
+        cz = ld4(zsl, (vi + 2 * kRapidThreads) * VEC, len, ALIGNED, polA, -INFINITY);
+        cq = ld4(qsl, (vi + 2 * kRapidThreads) * VEC, len, ALIGNED, polA, 0.0f);
+      }
+      a_body(nz, nq, vi + kRapidThreads);
     }
   }
 
