@@ -449,7 +449,8 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
 #pragma unroll
       for (int j = 0; j < NT; ++j) cur[j] = G::load(slice[j], vi * VEC, len, aligned, true, j == 2 ? pol_t : pol_keep);
     }
-    if constexpr (!kMulti && ALIGNED) {
+    // (bf16 multi-outcome kernels, short of registers, keep one vector per trip.)
+    if constexpr (ALIGNED && (!kMulti || std::is_same<T, float>::value)) {
       // Two vectors per trip, the prefetch alternating between cur and nxt (no register copies);
       // a prefetched vector is consumed only while it is in range.
       for (; vi < nvec; vi += 2 * kJsdThreads) {
@@ -468,8 +469,7 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
         a_body(nxt, vi + kJsdThreads);
       }
     } else {
-      // Multi-outcome kernels (more state, short of registers) and element-wise loads of unaligned
-      // rows: one vector per trip.
+      // bf16 multi-outcome kernels and element-wise loads of unaligned rows: one vector per trip.
       for (; vi < nvec; vi += kJsdThreads) {
         if (vi + kJsdThreads < nvec) {
 #pragma unroll

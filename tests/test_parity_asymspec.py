@@ -180,3 +180,29 @@ def test_delta_source_ablation(asv, src, dtype):
         ref = oracle.asymspec_verify(batch.a, batch.b, batch.t, batch.drafts, beta, 0.5, delta_source=src)
         compare_asymspec(out, ref, dtype)
         np.testing.assert_array_equal(out.tokens.cpu().numpy()[:, 0] >= 0, True)
+
+
+@pytest.mark.parametrize("dtype", [gen.F32, gen.BF16])
+def test_divergence_forms_across_their_domains(asv, dtype):
+    """Rows whose per-entry log-ratio u spreads over [-7, 7]: every 16-byte vector mixes entries of
+    the short narrow form (|u| <= 3), the |u| <= 4 narrow form (taken entry by entry) and the wide
+    form, and some vectors fail the packed-sum test while every entry is in the domain.  D agrees
+    with the oracle far inside the tolerance (the fitted forms are good to ~1e-7 relative)."""
+    B, K, V = 6, 2, 12288
+    rng = np.random.default_rng(20261202 + dtype)
+    a = rng.normal(0.0, 1.5, size=(B, K + 1, V))
+    shift = rng.uniform(-7.0, 7.0, size=(B, K + 1, V)) * (rng.random((B, K + 1, V)) < 0.4)
+    # request 4: u of every entry inside the short domain but most packed sums outside it
+    shift[4] = rng.uniform(-2.9, 2.9, size=(K + 1, V)) * (rng.random((K + 1, V)) < 0.9)
+    b = a + shift
+    t = b + rng.normal(0.0, 1.0, size=(B, K + 1, V))
+    a_s, b_s, t_s = (gen.store(x, dtype) for x in (a, b, t))
+    drafts = np.argmax(gen.widen(a_s, dtype)[:, :K], axis=-1).astype(np.int32)
+    out = asv.asymspec_verify(to_device(a_s, dtype), to_device(b_s, dtype), to_device(t_s, dtype),
+                              torch.from_numpy(drafts).cuda(), 1.0, 0.5)
+    torch.cuda.synchronize()
+    ref = oracle.asymspec_verify(a_s, b_s, t_s, drafts, 1.0, 0.5)
+    compare_asymspec(out, ref, dtype)
+    D = out.D.cpu().numpy().astype(np.float64)
+    assert np.all(ref.D > 0.05)  # the rows are far from identical
+    np.testing.assert_allclose(D, ref.D, rtol=2e-6, atol=0)
