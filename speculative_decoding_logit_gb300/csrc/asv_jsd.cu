@@ -44,6 +44,7 @@
 // give exactly 0.  Loads carry L2 cache policies: the divergence pair is marked evict-last in pass A
 // (pass B reads it again) and evict-first in pass B, the verifier input evict-first.
 #include <cfloat>
+#include <cstddef>
 #include <climits>
 #include <type_traits>
 
@@ -61,12 +62,19 @@ constexpr int kRing = 4;  // pass-B vectors in flight per input per thread (a po
 constexpr int kMaxArg = 4;  // argmax slots: fused scores for up to 4 betas, or 1 beta and the plain target
 constexpr int kMaxGamma = 8;  // gammas of one sweep
 
-struct __align__(16) JsdXchg {
+// One CTA's pass-A partials.
+struct __align__(16) JsdPart {
   float mx[3];        // CTA maxima of the inputs
   float sum_hi[3];    // CTA sums of exp2(x log2e - mL_cta), mL_cta = mx * log2e rounded, as hi + lo
   float sum_lo[3];
   float argv[kMaxArg];    // best scores in the CTA's slice
   int32_t argi[kMaxArg];  // their vocabulary indices
+};
+
+struct __align__(16) JsdXchg {
+  // Every CTA pushes its pass-A partials into from[its rank] of every CTA of the cluster before the
+  // first exchange, so each CTA combines them from its own shared memory afterwards.
+  JsdPart from[kMaxCluster];
   // Pushed into CTA 0 by every CTA before the second exchange; only CTA 0 reads them afterwards.
   // Pass-B sums (hi, lo): narrow form, wide p-form, wide q-form; then the second pair's (fused).
   float jsd_from[kMaxCluster][12];
@@ -333,6 +341,9 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
     if (*reinterpret_cast<const volatile uint32_t*>(p.dropped + rq)) return;
     row = rq * R1 + 1 + (row - rq * p.K);
   }
+  // Split cluster barrier: every thread arrives now and waits after pass A, before the first write
+  // into another CTA's shared memory, so every CTA of the cluster has started by then.
+  cluster_arrive_relaxed();
   const int req = row / R1;
   const int pos = row - req * R1;
   const int V = p.V;
@@ -515,24 +526,27 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
     if (lane == 0) s_wf[warp][j] = ws;
   }
   __syncthreads();
+  cluster_wait();
   if (warp == 0) {
+    // Every lane holds the CTA's reduced partials; lane q < C pushes them into CTA q.
+    const uint32_t dst = smem_addr(&xchg.from[rank]);
 #pragma unroll
     for (int sl = 0; sl < NA; ++sl) {
       float v2 = (lane < kWarps) ? s_av[lane][sl] : -INFINITY;
       int i2 = (lane < kWarps) ? s_ai[lane][sl] : INT_MAX;
       warp_argmax(v2, i2);
-      if (lane == 0) {
-        xchg.argv[sl] = v2;
-        xchg.argi[sl] = i2;
+      if (lane < int(C)) {
+        dsmem_st_f32(dsmem_map(dst + offsetof(JsdPart, argv) + 4u * sl, uint32_t(lane)), v2);
+        dsmem_st_u32(dsmem_map(dst + offsetof(JsdPart, argi) + 4u * sl, uint32_t(lane)), uint32_t(i2));
       }
     }
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       const DF d = warp_sum_df(DF{lane < kWarps ? s_wf[lane][j] : 0.0f, 0.0f});
-      if (lane == 0) {
-        xchg.mx[j] = Mc[j];
-        xchg.sum_hi[j] = d.hi;
-        xchg.sum_lo[j] = d.lo;
+      if (lane < int(C)) {
+        dsmem_st_f32(dsmem_map(dst + offsetof(JsdPart, mx) + 4u * j, uint32_t(lane)), Mc[j]);
+        dsmem_st_f32(dsmem_map(dst + offsetof(JsdPart, sum_hi) + 4u * j, uint32_t(lane)), d.hi);
+        dsmem_st_f32(dsmem_map(dst + offsetof(JsdPart, sum_lo) + 4u * j, uint32_t(lane)), d.lo);
       }
     }
   }
@@ -556,17 +570,17 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
       sq[j] = DF{0.0f, 0.0f};
     }
     if (lane < int(C)) {
-      const uint32_t q = uint32_t(lane);
+      const JsdPart& f = xchg.from[lane];
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
-        mq[j] = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.mx[j]), q));
-        sq[j].hi = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.sum_hi[j]), q));
-        sq[j].lo = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.sum_lo[j]), q));
+        mq[j] = f.mx[j];
+        sq[j].hi = f.sum_hi[j];
+        sq[j].lo = f.sum_lo[j];
       }
 #pragma unroll
       for (int sl = 0; sl < NA; ++sl) {
-        v2[sl] = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.argv[sl]), q));
-        i2[sl] = dsmem_ld_s32(dsmem_map(smem_addr(&xchg.argi[sl]), q));
+        v2[sl] = f.argv[sl];
+        i2[sl] = f.argi[sl];
       }
     }
 #pragma unroll
