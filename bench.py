@@ -363,6 +363,10 @@ def run_workload(args):
     import speculative_decoding_logit_gb300 as asv
 
     w = gen.WORKLOADS[args.workload]
+    if args.requests:
+        # A smaller batch of the same workload (profiling captures must stay within a few GB).
+        import dataclasses
+        w = dataclasses.replace(w, B=min(w.B, args.requests))
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     asv.build()
@@ -459,6 +463,8 @@ def main():
                     help="DRAM bytes per launch from an ncu capture of the current kernel (else null)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
+    ap.add_argument("--requests", type=int, default=0,
+                    help="with --workload: verify only this many requests (small cases for ncu captures)")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(gen.WORKLOADS),
                     help="another workload (device-timed line only; the default is the headline workload)")
     args = ap.parse_args()
