@@ -32,7 +32,9 @@ WORKLOAD = "asymspec_b64_k2_v151936_bf16"
 METRIC = "verified logit rows/s and HBM GB/s vs ~8 TB/s, fused CDA+δ verify, V=151936"
 BETA, GAMMA = 1.0, 0.5
 N_SETS = 4  # rotating input copies: 4 x 175 MB, larger than the 129 MB L2
-KERNEL_SOURCE = "asv_jsd.cu"  # the timed kernel; its ncu summary under profiles/ records a hash of it
+# The timed kernel's sources; its ncu summary under profiles/ records a hash of them (SHA-256 of the
+# files' bytes concatenated in this order, first 16 hex digits).
+KERNEL_SOURCES = ("asv_jsd.cu", "asv_jsd_common.cuh", "asv_device.cuh", "jsd_poly.inc", "asv_internal.h")
 
 
 def _peaks():
@@ -43,15 +45,23 @@ def _peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
+def kernel_source_hash() -> str:
+    import hashlib
+    csrc = os.path.join(ROOT, "speculative_decoding_logit_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def _profiled_traffic():
     """DRAM bytes per launch from the committed ncu summary of the timed kernel, or None when the
-    kernel source has changed since that capture (the summary records a hash of the source)."""
-    import hashlib
+    kernel source has changed since that capture (the summary records a hash of the sources)."""
     prof = os.path.join(ROOT, "profiles", f"jsd_family_{WORKLOAD}.md")
-    src = os.path.join(ROOT, "speculative_decoding_logit_gb300", "csrc", KERNEL_SOURCE)
     try:
         text = open(prof).read()
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        h = kernel_source_hash()
     except OSError:
         return None
     m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)

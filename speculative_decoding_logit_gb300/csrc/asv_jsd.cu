@@ -260,55 +260,89 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
   if (MODE == kModeAsym && fin_lane && d_pre >= 0 && d_pre < V)
     xd_pre = G::at(p.x[lane == 1 ? NT - 1 : 1], row_base + size_t(d_pre));
 
-  // CTA maxima, then every thread moves its sum to the CTA reference and the sums are added.
+  // Pass B of aligned slices streams the divergence pair (fused: and the verifier input) from L2
+  // through a ring of kRing vectors per input per thread in shared memory, filled by 16-byte
+  // cp.async copies (no registers held by copies in flight); each thread reads only its own slots
+  // and refills a slot only after the arithmetic has consumed it.  The first kRing slots are filled
+  // now, so that their reads overlap the row's exchange.
+  auto ring_issue = [&](int j) {
+    const int vi = tid + j * kJsdThreads;
+    if (vi < nvec) {
+#pragma unroll
+      for (int m = 0; m < NPB; ++m)
+        cp_async16(smem_addr(&s_ring[((j & (kRing - 1)) * NPB + m) * kJsdThreads + tid]),
+                   static_cast<const char*>(slice[m < 2 ? m : NT - 1]) + size_t(vi) * 16u, pol_last);
+    }
+    cp_async_commit();
+  };
+  if constexpr (ALIGNED) {
+#pragma unroll
+    for (int j = 0; j < kRing; ++j) ring_issue(j);
+  }
+
+  // CTA partials.  Each warp reduces its maxima and argmax slots, then its sums against its own
+  // maximum; warp 0 combines the warps' results -- lane j < NT input j, lane NT + s argmax slot s,
+  // each reading its values of every warp (reads issued together) and adding them in registers in
+  // warp order -- and pushes them into every CTA of the cluster.  The serial sections of the row
+  // keep dependent shuffle and shared-memory round trips few: while other CTAs on the SM stream
+  // their loads, each such round trip waits behind those loads (a few hundred cycles).
+  float wmax[NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) wmax[j] = warp_max(rmax[j].value());
+#pragma unroll
+  for (int sl = 0; sl < NA; ++sl) warp_argmax(bv[sl], bi[sl]);
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
-    const float w = warp_max(rmax[j].value());
-    if (lane == 0) s_wm[warp][j] = w;
-  }
-#pragma unroll
-  for (int sl = 0; sl < NA; ++sl) {
-    warp_argmax(bv[sl], bi[sl]);
+    const float s = acc[j].x + acc[j].y;
+    const float moved = (s != 0.0f) ? s * exp2f(mL[j] - ref_of(wmax[j])) : 0.0f;
+    const float ws = warp_sumf(moved);
     if (lane == 0) {
+      s_wm[warp][j] = wmax[j];
+      s_wf[warp][j] = ws;
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int sl = 0; sl < NA; ++sl) {
       s_av[warp][sl] = bv[sl];
       s_ai[warp][sl] = bi[sl];
     }
   }
   __syncthreads();
-  float Mc[NT];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    float m = s_wm[0][j];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) m = fmaxf(m, s_wm[w][j]);
-    Mc[j] = m;
-    const float s = acc[j].x + acc[j].y;
-    const float moved = (s != 0.0f) ? s * exp2f(mL[j] - ref_of(m)) : 0.0f;
-    const float ws = warp_sumf(moved);
-    if (lane == 0) s_wf[warp][j] = ws;
-  }
-  __syncthreads();
   cluster_wait();
-  if (warp == 0) {
-    // Every lane holds the CTA's reduced partials; lane q < C pushes them into CTA q.
+  if (warp == 0 && lane < NT + NA) {
     const uint32_t dst = smem_addr(&xchg.from[rank]);
+    if (lane < NT) {
+      const int j = lane;
+      float m[kWarps], sw[kWarps];
 #pragma unroll
-    for (int sl = 0; sl < NA; ++sl) {
-      float v2 = (lane < kWarps) ? s_av[lane][sl] : -INFINITY;
-      int i2 = (lane < kWarps) ? s_ai[lane][sl] : INT_MAX;
-      warp_argmax(v2, i2);
-      if (lane < int(C)) {
-        dsmem_st_f32(dsmem_map(dst + offsetof(JsdPart, argv) + 4u * sl, uint32_t(lane)), v2);
-        dsmem_st_u32(dsmem_map(dst + offsetof(JsdPart, argi) + 4u * sl, uint32_t(lane)), uint32_t(i2));
+      for (int w = 0; w < kWarps; ++w) {
+        m[w] = s_wm[w][j];
+        sw[w] = s_wf[w][j];
       }
-    }
+      float Mc = m[0];
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      const DF d = warp_sum_df(DF{lane < kWarps ? s_wf[lane][j] : 0.0f, 0.0f});
-      if (lane < int(C)) {
-        dsmem_st_f32(dsmem_map(dst + offsetof(JsdPart, mx) + 4u * j, uint32_t(lane)), Mc[j]);
-        dsmem_st_f32(dsmem_map(dst + offsetof(JsdPart, sum_hi) + 4u * j, uint32_t(lane)), d.hi);
-        dsmem_st_f32(dsmem_map(dst + offsetof(JsdPart, sum_lo) + 4u * j, uint32_t(lane)), d.lo);
+      for (int w = 1; w < kWarps; ++w) Mc = fmaxf(Mc, m[w]);
+      const float Rc = ref_of(Mc);
+      DF d{0.0f, 0.0f};
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        if (sw[w] != 0.0f) d = df_add(d, DF{sw[w] * exp2f(ref_of(m[w]) - Rc), 0.0f});
+      }
+      for (uint32_t q = 0; q < C; ++q) {
+        dsmem_st_f32(dsmem_map(dst + offsetof(JsdPart, mx) + 4u * j, q), Mc);
+        dsmem_st_f32(dsmem_map(dst + offsetof(JsdPart, sum_hi) + 4u * j, q), d.hi);
+        dsmem_st_f32(dsmem_map(dst + offsetof(JsdPart, sum_lo) + 4u * j, q), d.lo);
+      }
+    } else {
+      const int sl = lane - NT;
+      float v = s_av[0][sl];
+      int i = s_ai[0][sl];
+#pragma unroll
+      for (int w = 1; w < kWarps; ++w) argmax_merge(v, i, s_av[w][sl], s_ai[w][sl]);
+      for (uint32_t q = 0; q < C; ++q) {
+        dsmem_st_f32(dsmem_map(dst + offsetof(JsdPart, argv) + 4u * sl, q), v);
+        dsmem_st_u32(dsmem_map(dst + offsetof(JsdPart, argi) + 4u * sl, q), uint32_t(i));
       }
     }
   }
@@ -316,46 +350,60 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
 
   // ---------------------------------------------------------------- row statistics (warp 0)
   if (warp == 0) {
-    // lane q < C holds CTA q's partials; move every CTA's sums to the row reference, then add.
-    float mq[NT];
-    DF sq[NT];
-    float v2[NA];
-    int i2[NA];
+    // Lane j < NT combines input j's maxima and sums over the cluster's CTAs, lane NT + s argmax
+    // slot s: each lane reads its values of four CTAs at a time (reads issued together) and combines
+    // them in registers in rank order; one batch of independent shuffles brings them to lane 0.
+    const int j = lane < NT ? lane : 0;
+    const int sl = (lane >= NT && lane < NT + NA) ? lane - NT : 0;
+    float Mj = -INFINITY;
+    DF Sj{0.0f, 0.0f};  // against ref_of(Mj)
+    float av = -INFINITY;
+    int ai = INT_MAX;
+    for (uint32_t q0 = 0; q0 < C; q0 += 4) {
+      float mx4[4], hi4[4], lo4[4], av4[4];
+      int ai4[4];
 #pragma unroll
-    for (int sl = 0; sl < NA; ++sl) {
-      v2[sl] = -INFINITY;
-      i2[sl] = INT_MAX;
-    }
+      for (int u = 0; u < 4; ++u) {
+        const bool ok = q0 + u < C;
+        const JsdPart& f = xchg.from[ok ? q0 + u : 0];
+        mx4[u] = ok ? f.mx[j] : -INFINITY;
+        hi4[u] = ok ? f.sum_hi[j] : 0.0f;
+        lo4[u] = ok ? f.sum_lo[j] : 0.0f;
+        av4[u] = ok ? f.argv[sl] : -INFINITY;
+        ai4[u] = ok ? f.argi[sl] : INT_MAX;
+      }
+      float Mn = Mj;
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      mq[j] = -INFINITY;
-      sq[j] = DF{0.0f, 0.0f};
-    }
-    if (lane < int(C)) {
-      const JsdPart& f = xchg.from[lane];
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        mq[j] = f.mx[j];
-        sq[j].hi = f.sum_hi[j];
-        sq[j].lo = f.sum_lo[j];
+      for (int u = 0; u < 4; ++u) {
+        Mn = fmaxf(Mn, mx4[u]);
+        argmax_merge(av, ai, av4[u], ai4[u]);
+      }
+      const float Rn = ref_of(Mn);
+      if (Sj.hi != 0.0f) {  // (more than four CTAs) move the running sum to the new reference
+        const float g = exp2f(ref_of(Mj) - Rn);
+        Sj = DF{Sj.hi * g, Sj.lo * g};
       }
 #pragma unroll
-      for (int sl = 0; sl < NA; ++sl) {
-        v2[sl] = f.argv[sl];
-        i2[sl] = f.argi[sl];
+      for (int u = 0; u < 4; ++u) {
+        if (hi4[u] != 0.0f) {
+          const float g = exp2f(ref_of(mx4[u]) - Rn);
+          Sj = df_add(Sj, DF{hi4[u] * g, lo4[u] * g});
+        }
       }
+      Mj = Mn;
     }
-#pragma unroll
-    for (int sl = 0; sl < NA; ++sl) warp_argmax(v2[sl], i2[sl]);
     DF S[NT];
     float M[NT], MLr[NT];
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      M[j] = warp_max(mq[j]);
-      MLr[j] = ref_of(M[j]);
-      const float f = (sq[j].hi != 0.0f) ? exp2f(ref_of(mq[j]) - MLr[j]) : 0.0f;
-      S[j] = warp_sum_df(DF{sq[j].hi * f, sq[j].lo * f});
+    for (int jj = 0; jj < NT; ++jj) {
+      M[jj] = __shfl_sync(0xffffffffu, Mj, jj);
+      S[jj].hi = __shfl_sync(0xffffffffu, Sj.hi, jj);
+      S[jj].lo = __shfl_sync(0xffffffffu, Sj.lo, jj);
+      MLr[jj] = ref_of(M[jj]);
     }
+    int i2[NA];
+#pragma unroll
+    for (int s2 = 0; s2 < NA; ++s2) i2[s2] = __shfl_sync(0xffffffffu, ai, NT + s2);
     if (lane == 0) {
       bool finite = true;
 #pragma unroll
@@ -458,23 +506,7 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
     };
     constexpr bool kPairShort = MODE == kModeAsym;
     if (finite && ALIGNED) {
-      // Aligned slices: a ring of kRing vectors per input per thread, filled by 16-byte cp.async
-      // copies from L2 (no registers held by copies in flight).  Each thread reads only its own
-      // slots, and refills a slot only after the arithmetic has consumed it.
-      const char* src[3] = {static_cast<const char*>(slice[0]), static_cast<const char*>(slice[1]),
-                            static_cast<const char*>(slice[NT - 1])};
-      auto issue = [&](int j) {
-        const int vi = tid + j * kJsdThreads;
-        if (vi < nvec) {
-#pragma unroll
-          for (int m = 0; m < NPB; ++m)
-            cp_async16(smem_addr(&s_ring[((j & (kRing - 1)) * NPB + m) * kJsdThreads + tid]),
-                       src[m] + size_t(vi) * 16u, pol_last);
-        }
-        cp_async_commit();
-      };
-#pragma unroll
-      for (int j = 0; j < kRing; ++j) issue(j);
+      // (the ring's first kRing slots were filled before the exchange)
       for (int j = 0; tid + j * kJsdThreads < nvec; ++j) {
         cp_async_wait_group<kRing - 1>();  // the copies of vector j have landed
         const int slot = (j & (kRing - 1)) * NPB;
@@ -487,7 +519,7 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
           G::pairs(s_ring[(slot + 2) * kJsdThreads + tid], xt);
           pair_terms(xa, xt, rb2, accn2, an2, ap2, aq2, false);
         }
-        issue(j + kRing);
+        ring_issue(j + kRing);
       }
       cp_async_wait_all();
     } else if (finite) {
@@ -519,6 +551,7 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
         cb = nb;
       }
     }
+    if (ALIGNED && !finite) cp_async_wait_all();  // the ring's first copies, unused
     const float wn = warp_sumf((accn.x + accn.y) + an);
     const float wp = warp_sumf(ap);
     const float wq = warp_sumf(aq);
@@ -539,18 +572,19 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
     }
   }
   __syncthreads();
-  if (warp == 0) {
-    constexpr int NS = FUSE ? 6 : 3;
+  constexpr int NS = FUSE ? 6 : 3;
+  if (warp == 0 && lane < NS) {
+    // Lane m adds sum m of the CTA's warps in warp order (reads issued together) and pushes it into
+    // CTA 0.
+    float v[kWarps];
 #pragma unroll
-    for (int m = 0; m < NS; ++m) {
-      const DF dm = warp_sum_df(DF{lane < kWarps ? s_wf[lane][m] : 0.0f, 0.0f});
-      if (lane == 0) {
-        // Push this CTA's pass-B sums into CTA 0.
-        const uint32_t base = smem_addr(&xchg.jsd_from[rank][2 * m]);
-        dsmem_st_f32(dsmem_map(base + 0, 0), dm.hi);
-        dsmem_st_f32(dsmem_map(base + 4, 0), dm.lo);
-      }
-    }
+    for (int w = 0; w < kWarps; ++w) v[w] = s_wf[w][lane];
+    DF dm{v[0], 0.0f};
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) dm = df_add(dm, DF{v[w], 0.0f});
+    const uint32_t base = smem_addr(&xchg.jsd_from[rank][2 * lane]);
+    dsmem_st_f32(dsmem_map(base + 0, 0), dm.hi);
+    dsmem_st_f32(dsmem_map(base + 4, 0), dm.lo);
   }
   cluster_sync_w0(warp);  // #2: after this only CTA 0 touches shared memory, and only its own
   if (rank != 0 || warp != 0) return;

@@ -279,16 +279,28 @@ __device__ __forceinline__ void jsd_finalize_row(const JsdArgs& p, const int row
   float xd = xd_in;
   if (kMulti && MODE == kModeAsym && finite && d_ok && (lane == 1 || lane == 2))
     xd = G::at(p.x[lane == 1 ? NT - 1 : 1], row_base + size_t(d));
-  // Pass-B sums of the cluster's CTAs, in rank order (lane q holds CTA q's).
-  DF jn{0.0f, 0.0f}, jp{0.0f, 0.0f}, jq{0.0f, 0.0f};
-  if (lane < int(C)) {
-    jn = DF{jsd_from[lane][0], jsd_from[lane][1]};
-    jp = DF{jsd_from[lane][2], jsd_from[lane][3]};
-    jq = DF{jsd_from[lane][4], jsd_from[lane][5]};
+  // Pass-B sums of the cluster's CTAs: lane m < NS adds sum m over the CTAs in rank order (reads
+  // issued four CTAs at a time), then one batch of independent shuffles gives every lane all of them.
+  constexpr int NS = FUSE ? 6 : 3;
+  DF mine{0.0f, 0.0f};
+  if (lane < NS) {
+    for (uint32_t q0 = 0; q0 < C; q0 += 4) {
+      float h4[4], l4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const bool ok = q0 + u < C;
+        const float* f = jsd_from[ok ? q0 + u : 0];
+        h4[u] = ok ? f[2 * lane] : 0.0f;
+        l4[u] = ok ? f[2 * lane + 1] : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (q0 + u < C) mine = df_add(mine, DF{h4[u], l4[u]});
+      }
+    }
   }
-  jn = warp_sum_df(jn);
-  jp = warp_sum_df(jp);
-  jq = warp_sum_df(jq);
+  auto from_lane = [&](int m) { return DF{__shfl_sync(kAll, mine.hi, m), __shfl_sync(kAll, mine.lo, m)}; };
+  const DF jn = from_lane(0), jp = from_lane(1), jq = from_lane(2);
   float D = 0.0f;
   if (finite) {
     // Narrow terms are against sqrt(ea eb) 2^(MaL/2 + MbL/2 - hML); the row sums Sa, Sb against
@@ -305,15 +317,7 @@ __device__ __forceinline__ void jsd_finalize_row(const JsdArgs& p, const int row
   // Fused: J = JSD(a || t) from the second pair's sums, the same way.
   float J = 0.0f;
   if constexpr (FUSE) {
-    DF kn{0.0f, 0.0f}, kp{0.0f, 0.0f}, kq{0.0f, 0.0f};
-    if (lane < int(C)) {
-      kn = DF{jsd_from[lane][6], jsd_from[lane][7]};
-      kp = DF{jsd_from[lane][8], jsd_from[lane][9]};
-      kq = DF{jsd_from[lane][10], jsd_from[lane][11]};
-    }
-    kn = warp_sum_df(kn);
-    kp = warp_sum_df(kp);
-    kq = warp_sum_df(kq);
+    const DF kn = from_lane(3), kp = from_lane(4), kq = from_lane(5);
     if (finite) {
       const float ha = 0.5f * rc.ML[0], ht = 0.5f * rc.ML[2];
       const float bb = rc.hML2 - ha;
