@@ -338,56 +338,79 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
     }
   }
 
-  // CTA statistics: maximum; sums moved to the CTA reference; peaks.
+  // CTA statistics: maximum; sums moved to the CTA reference; peaks.  Each warp reduces its own
+  // (its sum against its own maximum), then lanes of warp 0 combine the warps' results, each reading
+  // its values of every warp (reads issued together) and adding them in registers in warp order.
+  // The serial sections of a row keep dependent shuffle and shared-memory round trips few: while
+  // other CTAs on the SM stream their loads, each such round trip waits behind those loads.
   {
     const float w = warp_max(pv[0]);
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      warp_argmax_pl(pv[k], pi[k], pz[k], pq[k]);
-      if (lane == 0) {
+    for (int k = 0; k < 2; ++k) warp_argmax_pl(pv[k], pi[k], pz[k], pq[k]);
+    const float s = acc.x + acc.y;
+    const float ws = warp_sum_f((s != 0.0f) ? s * exp2f(mL - ref_of(w)) : 0.0f);
+    const float wq = warp_sum_f(qacc.x + qacc.y);
+    if (lane == 0) {
+      s_w[warp][0] = ws;
+      s_w[warp][1] = wq;
+      s_w[warp][3] = w;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
         s_pv[warp][k] = pv[k];
         s_pi[warp][k] = pi[k];
         s_pz[warp][k] = pz[k];
         s_pq[warp][k] = pq[k];
       }
     }
-    if (lane == 0) s_w[warp][3] = w;
     __syncthreads();
-    float Mc = s_w[0][3];
+    if (warp == 0 && lane < 4) {
+      if (lane == 0) {  // maximum of z/T and the exp sum against it
+        float m[kWarps], sw[kWarps];
 #pragma unroll
-    for (int k = 1; k < kWarps; ++k) Mc = fmaxf(Mc, s_w[k][3]);
-    const float s = acc.x + acc.y;
-    const float moved = (s != 0.0f) ? s * exp2f(mL - ref_of(Mc)) : 0.0f;
-    const float ws = warp_sum_f(moved);
-    const float wq = warp_sum_f(qacc.x + qacc.y);
-    if (lane == 0) {
-      s_w[warp][0] = ws;
-      s_w[warp][1] = wq;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const DF se = warp_sum_df(DF{lane < kWarps ? s_w[lane][0] : 0.0f, 0.0f});
-      const DF sq = warp_sum_df(DF{lane < kWarps ? s_w[lane][1] : 0.0f, 0.0f});
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        float v = lane < kWarps ? s_pv[lane][k] : -INFINITY;
-        int i = lane < kWarps ? s_pi[lane][k] : INT_MAX;
-        float a = lane < kWarps ? s_pz[lane][k] : 0.0f;
-        float b = lane < kWarps ? s_pq[lane][k] : 0.0f;
-        warp_argmax_pl(v, i, a, b);
-        if (lane == 0) {
-          xchg.pk_v[k] = v;
-          xchg.pk_i[k] = i;
-          xchg.pk_z[k] = a;
-          xchg.pk_q[k] = b;
+        for (int k = 0; k < kWarps; ++k) {
+          m[k] = s_w[k][3];
+          sw[k] = s_w[k][0];
         }
-      }
-      if (lane == 0) {
+        float Mc = m[0];
+#pragma unroll
+        for (int k = 1; k < kWarps; ++k) Mc = fmaxf(Mc, m[k]);
+        const float Rc = ref_of(Mc);
+        DF d{0.0f, 0.0f};
+#pragma unroll
+        for (int k = 0; k < kWarps; ++k) {
+          if (sw[k] != 0.0f) d = df_add(d, DF{sw[k] * exp2f(ref_of(m[k]) - Rc), 0.0f});
+        }
         xchg.zmax = Mc;
-        xchg.se[0] = se.hi;
-        xchg.se[1] = se.lo;
-        xchg.sq[0] = sq.hi;
-        xchg.sq[1] = sq.lo;
+        xchg.se[0] = d.hi;
+        xchg.se[1] = d.lo;
+      } else if (lane == 1) {  // sum of q
+        float x[kWarps];
+#pragma unroll
+        for (int k = 0; k < kWarps; ++k) x[k] = s_w[k][1];
+        DF d{x[0], 0.0f};
+#pragma unroll
+        for (int k = 1; k < kWarps; ++k) d = df_add(d, DF{x[k], 0.0f});
+        xchg.sq[0] = d.hi;
+        xchg.sq[1] = d.lo;
+      } else {  // peak slot lane - 2
+        const int k = lane - 2;
+        float v = s_pv[0][k], a = s_pz[0][k], b = s_pq[0][k];
+        int i = s_pi[0][k];
+#pragma unroll
+        for (int w2 = 1; w2 < kWarps; ++w2) {
+          const float ov = s_pv[w2][k];
+          const int oi = s_pi[w2][k];
+          if (ov > v || (ov == v && oi < i)) {
+            v = ov;
+            i = oi;
+            a = s_pz[w2][k];
+            b = s_pq[w2][k];
+          }
+        }
+        xchg.pk_v[k] = v;
+        xchg.pk_i[k] = i;
+        xchg.pk_z[k] = a;
+        xchg.pk_q[k] = b;
       }
     }
   }
@@ -395,32 +418,80 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
 
   // ---------------------------------------------------------------- row statistics (warp 0)
   if (warp == 0) {
-    float mq = -INFINITY;
-    DF se{0.0f, 0.0f}, sq{0.0f, 0.0f};
-    float v[2] = {-INFINITY, -INFINITY}, a[2] = {0.0f, 0.0f}, b[2] = {0.0f, 0.0f};
-    int i[2] = {INT_MAX, INT_MAX};
-    if (lane < int(C)) {
-      const uint32_t q = uint32_t(lane);
-      mq = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.zmax), q));
-      se.hi = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.se[0]), q));
-      se.lo = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.se[1]), q));
-      sq.hi = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.sq[0]), q));
-      sq.lo = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.sq[1]), q));
+    // Lane 0: maximum of z/T and the exp sum; lane 1: sum of q; lanes 2, 3: peak slot lane - 2 --
+    // each over the cluster's CTAs, four CTAs' values read at a time (remote reads issued together)
+    // and combined in registers in rank order; one batch of shuffles brings them to lane 0.
+    const int ks = (lane == 3) ? 1 : 0;
+    const uint32_t o0 = (lane >= 2) ? uint32_t(offsetof(RapidXchg, pk_v)) + 4u * ks : uint32_t(offsetof(RapidXchg, zmax));
+    const uint32_t o1 = (lane == 0) ? uint32_t(offsetof(RapidXchg, se))
+                        : (lane == 1) ? uint32_t(offsetof(RapidXchg, sq)) : uint32_t(offsetof(RapidXchg, pk_z)) + 4u * ks;
+    const uint32_t o2 = (lane < 2) ? o1 + 4u : uint32_t(offsetof(RapidXchg, pk_q)) + 4u * ks;
+    const uint32_t o3 = uint32_t(offsetof(RapidXchg, pk_i)) + 4u * ks;
+    const uint32_t base = smem_addr(&xchg);
+    float mq = -INFINITY;  // lane 0: maximum so far; lanes 2, 3: peak value so far
+    DF sx{0.0f, 0.0f};     // lane 0: exp sum against ref_of(mq); lane 1: q sum
+    float pa_ = 0.0f, pb_ = 0.0f;
+    int pi_ = INT_MAX;
+    for (uint32_t q0 = 0; q0 < C; q0 += 4) {
+      float f0[4], f1[4], f2[4];
+      int f3[4];
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        v[k] = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.pk_v[k]), q));
-        i[k] = dsmem_ld_s32(dsmem_map(smem_addr(&xchg.pk_i[k]), q));
-        a[k] = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.pk_z[k]), q));
-        b[k] = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.pk_q[k]), q));
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t q = (q0 + u < C) ? q0 + u : 0u;
+        f0[u] = dsmem_ld_f32(dsmem_map(base + o0, q));
+        f1[u] = dsmem_ld_f32(dsmem_map(base + o1, q));
+        f2[u] = dsmem_ld_f32(dsmem_map(base + o2, q));
+        f3[u] = dsmem_ld_s32(dsmem_map(base + o3, q));
+      }
+      if (lane == 0) {
+        float Mn = mq;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (q0 + u < C) Mn = fmaxf(Mn, f0[u]);
+        const float Rn = ref_of(Mn);
+        if (sx.hi != 0.0f) {  // (more than four CTAs) move the running sum to the new reference
+          const float g = exp2f(ref_of(mq) - Rn);
+          sx = DF{sx.hi * g, sx.lo * g};
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (q0 + u < C && f1[u] != 0.0f) {
+            const float g = exp2f(ref_of(f0[u]) - Rn);
+            sx = df_add(sx, DF{f1[u] * g, f2[u] * g});
+          }
+        }
+        mq = Mn;
+      } else if (lane == 1) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (q0 + u < C) sx = df_add(sx, DF{f1[u], f2[u]});
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (q0 + u < C && (f0[u] > mq || (f0[u] == mq && f3[u] < pi_))) {
+            mq = f0[u];
+            pi_ = f3[u];
+            pa_ = f1[u];
+            pb_ = f2[u];
+          }
+        }
       }
     }
-    const float M = warp_max(mq);
-    const float ML = ref_of(M);
-    const float f = (se.hi != 0.0f) ? exp2f(ref_of(mq) - ML) : 0.0f;
-    const DF S = warp_sum_df(DF{se.hi * f, se.lo * f});
-    const DF Q = warp_sum_df(sq);
+    const unsigned kAll = 0xffffffffu;
+    const float M = mq;  // lane 0
+    const DF S = sx;     // lane 0
+    const DF Q{__shfl_sync(kAll, sx.hi, 1), __shfl_sync(kAll, sx.lo, 1)};
+    float v[2], a[2], b[2];
+    int i[2];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) warp_argmax_pl(v[k], i[k], a[k], b[k]);
+    for (int kk = 0; kk < 2; ++kk) {
+      v[kk] = __shfl_sync(kAll, mq, 2 + kk);
+      i[kk] = __shfl_sync(kAll, pi_, 2 + kk);
+      a[kk] = __shfl_sync(kAll, pa_, 2 + kk);
+      b[kk] = __shfl_sync(kAll, pb_, 2 + kk);
+    }
+    (void)v;
+    const float ML = ref_of(M);
     if (lane == 0) {
       const bool fin = isfinite(M) && isfinite(S.hi) && S.hi > 0.0f && isfinite(Q.hi);
       rs.M = M;
@@ -566,32 +637,55 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
     }
   }
   {
+    // As at the first exchange: each warp reduces against its own maximum, lanes 0 and 1 of warp 0
+    // combine the warps' results in registers.
     const float w = warp_max(L);
-    if (lane == 0) s_w[warp][3] = w;
-    __syncthreads();
-    float Mc = s_w[0][3];
-#pragma unroll
-    for (int k = 1; k < kWarps; ++k) Mc = fmaxf(Mc, s_w[k][3]);
     float wa = 0.0f, wp = 0.0f;
     if constexpr (AE) {
       const float s = aacc.x + aacc.y;
-      wa = warp_sum_f((s != 0.0f) ? s * exp2f(aL - ref_of(Mc)) : 0.0f);
+      wa = warp_sum_f((s != 0.0f) ? s * exp2f(aL - ref_of(w)) : 0.0f);
       wp = warp_sum_f(pall.x + pall.y);
     }
     if (lane == 0) {
       s_w[warp][0] = wa;
       s_w[warp][1] = wp;
+      s_w[warp][3] = w;
     }
     __syncthreads();
-    if (warp == 0) {
-      const DF sa = warp_sum_df(DF{lane < kWarps ? s_w[lane][0] : 0.0f, 0.0f});
-      const DF sp = warp_sum_df(DF{lane < kWarps ? s_w[lane][1] : 0.0f, 0.0f});
-      if (lane == 0) {
+    if (warp == 0 && lane < 2) {
+      if (lane == 0) {  // maximum of zhat/T and (AE) the exp sum against it
+        float m[kWarps], sw[kWarps];
+#pragma unroll
+        for (int k = 0; k < kWarps; ++k) {
+          m[k] = s_w[k][3];
+          sw[k] = s_w[k][0];
+        }
+        float Mc = m[0];
+#pragma unroll
+        for (int k = 1; k < kWarps; ++k) Mc = fmaxf(Mc, m[k]);
+        DF d{0.0f, 0.0f};
+        if constexpr (AE) {
+          const float Rc = ref_of(Mc);
+#pragma unroll
+          for (int k = 0; k < kWarps; ++k) {
+            if (sw[k] != 0.0f) d = df_add(d, DF{sw[k] * exp2f(ref_of(m[k]) - Rc), 0.0f});
+          }
+        }
         xchg.zhmax = Mc;
-        xchg.ae[0] = sa.hi;
-        xchg.ae[1] = sa.lo;
-        xchg.pa[0] = sp.hi;
-        xchg.pa[1] = sp.lo;
+        xchg.ae[0] = d.hi;
+        xchg.ae[1] = d.lo;
+      } else {  // (AE) sum of p
+        DF d{0.0f, 0.0f};
+        if constexpr (AE) {
+          float x[kWarps];
+#pragma unroll
+          for (int k = 0; k < kWarps; ++k) x[k] = s_w[k][1];
+          d = DF{x[0], 0.0f};
+#pragma unroll
+          for (int k = 1; k < kWarps; ++k) d = df_add(d, DF{x[k], 0.0f});
+        }
+        xchg.pa[0] = d.hi;
+        xchg.pa[1] = d.lo;
       }
     }
   }
@@ -599,28 +693,58 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
   cluster_sync_w0(warp);  // #2
 
   if (warp == 0) {
+    // Lane 0: maximum of zhat/T and (AE) the exp sum; lane 1: (AE) sum of p -- over the cluster's
+    // CTAs, four CTAs' values read at a time, combined in registers in rank order.
+    const uint32_t base = smem_addr(&xchg);
+    const uint32_t o0 = uint32_t(offsetof(RapidXchg, zhmax));
+    const uint32_t o1 = (lane == 0) ? uint32_t(offsetof(RapidXchg, ae)) : uint32_t(offsetof(RapidXchg, pa));
     float mq = -INFINITY;
-    DF sa{0.0f, 0.0f}, sp{0.0f, 0.0f};
-    if (lane < int(C)) {
-      const uint32_t q = uint32_t(lane);
-      mq = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.zhmax), q));
-      if constexpr (AE) {
-        sa.hi = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.ae[0]), q));
-        sa.lo = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.ae[1]), q));
-        sp.hi = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.pa[0]), q));
-        sp.lo = dsmem_ld_f32(dsmem_map(smem_addr(&xchg.pa[1]), q));
+    DF sx{0.0f, 0.0f};
+    for (uint32_t q0 = 0; q0 < C; q0 += 4) {
+      float f0[4], f1[4], f2[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t q = (q0 + u < C) ? q0 + u : 0u;
+        f0[u] = dsmem_ld_f32(dsmem_map(base + o0, q));
+        if constexpr (AE) {
+          f1[u] = dsmem_ld_f32(dsmem_map(base + o1, q));
+          f2[u] = dsmem_ld_f32(dsmem_map(base + o1 + 4u, q));
+        } else {
+          f1[u] = 0.0f;
+          f2[u] = 0.0f;
+        }
+      }
+      if (lane == 0) {
+        float Mn = mq;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (q0 + u < C) Mn = fmaxf(Mn, f0[u]);
+        if constexpr (AE) {
+          const float Rn = ref_of(Mn);
+          if (sx.hi != 0.0f) {
+            const float g = exp2f(ref_of(mq) - Rn);
+            sx = DF{sx.hi * g, sx.lo * g};
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (q0 + u < C && f1[u] != 0.0f) {
+              const float g = exp2f(ref_of(f0[u]) - Rn);
+              sx = df_add(sx, DF{f1[u] * g, f2[u] * g});
+            }
+          }
+        }
+        mq = Mn;
+      } else if (AE) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (q0 + u < C) sx = df_add(sx, DF{f1[u], f2[u]});
       }
     }
-    const float Mh = warp_max(mq);
-    if constexpr (AE) {
-      const float f = (sa.hi != 0.0f) ? exp2f(ref_of(mq) - ref_of(Mh)) : 0.0f;
-      sa = warp_sum_df(DF{sa.hi * f, sa.lo * f});
-      sp = warp_sum_df(sp);
-    }
+    const DF sp{__shfl_sync(0xffffffffu, sx.hi, 1), __shfl_sync(0xffffffffu, sx.lo, 1)};
     if (lane == 0) {
-      rs.zhmax = Mh;
-      rs.ae_hi = sa.hi;
-      rs.ae_lo = sa.lo;
+      rs.zhmax = mq;
+      rs.ae_hi = sx.hi;
+      rs.ae_lo = sx.lo;
       rs.pa_hi = sp.hi;
       rs.pa_lo = sp.lo;
     }
@@ -693,8 +817,13 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
     }
     __syncthreads();
     if (warp == 0) {
-      const DF dh = warp_sum_df(DF{lane < kWarps ? s_w[lane][0] : 0.0f, 0.0f});
-      const DF de = warp_sum_df(DF{lane < kWarps ? s_w[lane][1] : 0.0f, 0.0f});
+      // Lane k < kWarps holds warp k's sums; a butterfly over those lanes only (three steps).
+      DF dh{lane < kWarps ? s_w[lane][0] : 0.0f, 0.0f}, de{lane < kWarps ? s_w[lane][1] : 0.0f, 0.0f};
+#pragma unroll
+      for (int o = kWarps / 2; o > 0; o >>= 1) {
+        dh = df_add(dh, DF{__shfl_xor_sync(0xffffffffu, dh.hi, o), __shfl_xor_sync(0xffffffffu, dh.lo, o)});
+        de = df_add(de, DF{__shfl_xor_sync(0xffffffffu, de.hi, o), __shfl_xor_sync(0xffffffffu, de.lo, o)});
+      }
       if (lane == 0) {
         const uint32_t base = smem_addr(&xchg.head[rank][0]);
         dsmem_st_f32(dsmem_map(base + 0, 0), dh.hi);
@@ -708,13 +837,25 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
   if (rank != 0 || warp != 0) return;
 
   // ---------------------------------------------------------------- row finalisation (CTA 0, warp 0)
-  DF Hp{0.0f, 0.0f}, He{0.0f, 0.0f};
-  if (lane < int(C)) {
-    Hp = DF{xchg.head[lane][0], xchg.head[lane][1]};
-    He = DF{xchg.head[lane][2], xchg.head[lane][3]};
+  // Lane m < 2 adds head sum m over the cluster's CTAs in rank order (reads issued four CTAs at a
+  // time); lane 0 takes lane 1's by one shuffle.
+  DF hm{0.0f, 0.0f};
+  if (lane < 2) {
+    for (uint32_t q0 = 0; q0 < C; q0 += 4) {
+      float h4[4], l4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t q = (q0 + u < C) ? q0 + u : 0u;
+        h4[u] = xchg.head[q][2 * lane];
+        l4[u] = xchg.head[q][2 * lane + 1];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (q0 + u < C) hm = df_add(hm, DF{h4[u], l4[u]});
+    }
   }
-  Hp = warp_sum_df(Hp);
-  He = warp_sum_df(He);
+  const DF Hp = hm;
+  const DF He{__shfl_sync(0xffffffffu, hm.hi, 1), __shfl_sync(0xffffffffu, hm.lo, 1)};
   if (lane != 0) return;
   {
     float hp = Hp.hi + Hp.lo, he = He.hi + He.lo;
