@@ -462,8 +462,8 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
     float2 accn = make_float2(0.0f, 0.0f), accn2 = make_float2(0.0f, 0.0f);
     float an = 0.0f, ap = 0.0f, aq = 0.0f, an2 = 0.0f, ap2 = 0.0f, aq2 = 0.0f;
     // One vector of the pair (xa, xb) against row constants rb.
-    // sh: the short narrow form (|u| <= 3, fewer terms), for the AsymSpec pair, whose u stays small;
-    // the E2-SCI pair (draft, target) spreads wider and takes the |u| <= 4 form.
+    // sh: the short narrow form (|u| <= 3, two fewer terms), for the AsymSpec pair, whose u stays
+    // small; the E2-SCI pair (draft, target) spreads wider and takes the |u| <= 4 form.
     auto pair_terms = [&](const float2 (&xa)[NP], const float2 (&xb)[NP], const RowB& r, float2& acn, float& sn,
                           float& sp, float& sq, const bool sh) {
       const float kS0 = sh ? ASV_JSD_SHORT_S0 : ASV_JSD_EVEN_S0;
@@ -476,19 +476,13 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
         const float2 uu = fsub2(fsub2(xb[q2], xa[q2]), dl2);
         s2[q2] = fmul2(uu, uu);
       }
-      // Narrow form for the whole vector unless one entry is outside it (or NaN: -inf pairs).  The
-      // terms are non-negative, so a sum within the domain puts every entry in it (a NaN fails the
-      // test); only when the sum is outside are the entries checked one by one.
-      float2 ss = s2[0];
+      // Narrow form for the whole vector unless one entry is outside it (or NaN: -inf pairs): the
+      // largest u^2 by NaN-propagating maxima, which run on the ALU pipe -- this loop is bound by
+      // the fp32 pipe (about 13 fp32 operations per entry), so the test costs it nothing there.
+      float smax = fmax_nan(s2[0].x, s2[0].y);
 #pragma unroll
-      for (int q2 = 1; q2 < NP; ++q2) ss = fadd2(ss, s2[q2]);
-      bool narrow = (ss.x + ss.y) <= kS0;
-      if (!narrow) {
-        float smax = fmax_nan(s2[0].x, s2[0].y);
-#pragma unroll
-        for (int q2 = 1; q2 < NP; ++q2) smax = fmax_nan(smax, fmax_nan(s2[q2].x, s2[q2].y));
-        narrow = smax <= kS0;
-      }
+      for (int q2 = 1; q2 < NP; ++q2) smax = fmax_nan(smax, fmax_nan(s2[q2].x, s2[q2].y));
+      const bool narrow = smax <= kS0;
       if (narrow) {
 #pragma unroll
         for (int q2 = 0; q2 < NP; ++q2) {

@@ -17,9 +17,10 @@ Wide form (any u): with m = max(p, q), s = |u| and r = e^-s = min(p,q)/max(p,q),
 the entry's share is m * (A(r) - s*r) with A(r) = (1 + r) ln(2 / (1 + r)), and
 A(r) = (1 - r) * B(r) with B smooth on [0, 1] (B(0) = ln 2, B(1) = 1).
 
-A second, shorter narrow form (|u| <= U1 = 3, R of degree DEG1 = 7) serves pairs whose u stays
-small (the AsymSpec pair a, b): it is as accurate as the wide-domain one in fp32 and three
-multiply-adds shorter.
+A second, shorter narrow form (|u| <= U1 = 3, R of degree DEG1 = 6) serves pairs whose u stays
+small (the AsymSpec pair a, b).  The degrees are the lowest that keep both narrow forms within
+about 1.6e-7 relative in fp32, the size of ex2.approx's own error on the weights: the per-entry
+term is bound by the fp32 pipe, so every multiply-add counts.
 
 Both R and B are fitted here in 50-digit arithmetic by least squares in
 relative error on Chebyshev nodes; coefficients are rounded to fp32 one at a
@@ -36,9 +37,9 @@ import numpy as np
 
 mp.mp.dps = 50
 U0 = 4.0
-DEG = 10  # degree of R in s = u^2
+DEG = 8  # degree of R in s = u^2
 U1 = 3.0
-DEG1 = 7  # degree of the short form's R
+DEG1 = 6  # degree of the short form's R
 
 
 def f(u):
