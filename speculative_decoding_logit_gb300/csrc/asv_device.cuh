@@ -156,18 +156,6 @@ __device__ __forceinline__ int32_t dsmem_ld_s32(uint32_t a) {
   return v;
 }
 
-__device__ __forceinline__ uint32_t dsmem_ld_u32(uint32_t a) {
-  uint32_t v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ uint16_t dsmem_ld_u16(uint32_t a) {
-  uint16_t v;
-  asm volatile("ld.shared::cluster.u16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
-  return v;
-}
-
 // ------------------------------------------------------------------ special-function unit
 
 // 2^x and log2(x) on the special-function unit (approximate, flush-to-zero).
@@ -200,18 +188,6 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-__device__ __forceinline__ float warp_min(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
-__device__ __forceinline__ double warp_sum(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
 // (value, index): larger value wins; equal values -> lower index.
 __device__ __forceinline__ void argmax_merge(float& v, int& i, float ov, int oi) {
   if (ov > v || (ov == v && oi < i)) {
@@ -226,23 +202,6 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
     const float ov = __shfl_xor_sync(0xffffffffu, v, o);
     const int oi = __shfl_xor_sync(0xffffffffu, i, o);
     argmax_merge(v, i, ov, oi);
-  }
-}
-
-// (value, index): smaller value wins; equal values -> lower index.
-__device__ __forceinline__ void argmin_merge(float& v, int& i, float ov, int oi) {
-  if (ov < v || (ov == v && oi < i)) {
-    v = ov;
-    i = oi;
-  }
-}
-
-__device__ __forceinline__ void warp_argmin(float& v, int& i) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-    argmin_merge(v, i, ov, oi);
   }
 }
 
@@ -334,16 +293,6 @@ __device__ __forceinline__ DF df_add(DF a, DF b) {
   return DF{hi, e - (hi - s)};
 }
 
-__device__ __forceinline__ DF warp_sum_df(DF v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    DF w;
-    w.hi = __shfl_xor_sync(0xffffffffu, v.hi, o);
-    w.lo = __shfl_xor_sync(0xffffffffu, v.lo, o);
-    v = df_add(v, w);
-  }
-  return v;
-}
 
 __device__ __forceinline__ void dsmem_st_f32(uint32_t a, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");

@@ -32,7 +32,7 @@ struct __align__(16) JsdPart {
   int32_t argi[kMaxArg];  // their vocabulary indices
 };
 
-// Row constants, computed by one thread after the exchange and broadcast through shared memory.
+// Row constants, computed by warp 0 after the exchange and broadcast through shared memory.
 struct __align__(16) JsdRowConsts {
   float M[3];
   float ML[3];     // M * log2e, rounded
