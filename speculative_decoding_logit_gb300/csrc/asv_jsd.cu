@@ -10,23 +10,23 @@
 //     JSD(draft || target) against a threshold driven by an EWMA of the acceptance rate.
 //
 // Work decomposition.  One row (request r, position i) is V vocabulary entries of each input.  A
-// thread-block cluster of C CTAs owns one row; CTA q owns entries [q*n_slice, (q+1)*n_slice).  The
-// kernel streams; it stages nothing in shared memory:
-//   pass A  reads the slice of every input from HBM once (16-byte loads that bypass L1, one vector
-//           prefetched ahead) and keeps per thread a running maximum and a sum of exp(x - max)
-//           (rescaled on the rare occasions the maximum grows) for each input, plus the argmax of
-//           the verifier score;
+// thread-block cluster of C CTAs owns one row; CTA q owns entries [q*n_slice, (q+1)*n_slice):
+//   pass A  reads the slice of every input from HBM once into registers (16-byte loads that bypass
+//           L1, two vectors per trip) and keeps per thread a running maximum and a sum of
+//           exp(x - max) (rescaled on the rare occasions the maximum grows) for each input, plus the
+//           argmax of the verifier score;
 //   exchange the CTA's statistics go to every CTA of the cluster through distributed shared
 //           memory; one warp combines the C partials in rank order, so every CTA holds bit-identical
 //           row statistics (log-sum-exps, the lse difference used below, the argmax);
 //   pass B  re-reads the slice of the divergence pair (a and b; SCI: draft and target), which the
-//           L2 cache still holds from pass A (the resident CTAs' slices are a few tens of MB), and
-//           sums the per-entry Jensen-Shannon terms;
+//           L2 cache still holds from pass A (the resident CTAs' slices are a few tens of MB),
+//           through a per-thread ring of 16-byte cp.async copies in shared memory (aligned slices),
+//           and sums the per-entry Jensen-Shannon terms; this loop is bound by the fp32 pipe;
 //   finish  every CTA pushes its pass-B sums into CTA 0 and leaves; CTA 0 finalises the row (gate,
 //           outputs, a 16-byte row record) and takes a ticket on the request's counter.  The last of
 //           the K+1 rows to finish runs the left-to-right scan and resets the counter, so the whole
 //           step is one launch with no spin-waits.
-// Without shared-memory staging a CTA needs only registers, so several CTAs share an SM and hide
+// A CTA holds no slice in shared memory (the ring is 32 KB), so four CTAs share an SM and hide
 // each other's exchanges.  Arithmetic on entries is two-lane packed fp32 (fma/add/mul/sub .f32x2)
 // where it pairs up.  Sums that cross warps and CTAs are carried as compensated fp32 pairs: this
 // GPU's fp64 rate is a small fraction of its fp32 rate, so fp64 appears only in CTA 0's few
@@ -38,7 +38,9 @@
 // reference pass B uses, so the divergence sums and the row sums share one scale.  The constant
 // rounding error of ML is removed from the log-sum-exps.  The gate is decided in double in the log
 // domain.  The per-entry divergence term is evaluated from u = (xb - xa) - (lse_b - lse_a):
-//   narrow form (|u| <= 4): sqrt(p q) u^2 R(u^2), R an even-symmetric fitted polynomial;
+//   narrow form (|u| <= 4): sqrt(p q) u^2 R(u^2), R an even-symmetric fitted polynomial (a shorter
+//                           one on |u| <= 3 for the AsymSpec pair), taken by a whole vector when the
+//                           largest u^2 of its entries is inside the domain;
 //   wide form (any u):      max(p,q) (A(r) - |u| r), r = exp(-|u|), A(r) = (1 - r) B(r).
 // Both are sums of non-negative terms (no cancellation between large entropies), and identical rows
 // give exactly 0.  Loads carry L2 cache policies: the divergence pair is marked evict-last in pass A
