@@ -8,12 +8,15 @@ stream.  There is no CPU fallback: on a machine without the library or
 without a CUDA device the calls raise.
 
 Entry points (same names as the C ABI):
-  asymspec_verify  AsymSpec CDA gate + delta-fusion ("AsymSpec: Context-Asymmetric
-                   Speculative Decoding for Agentic LLMs", sec. 4.1-4.2)
-  rapid_verify     RAPID retrieval-augmented target verification ("RAPID: Long-Context
-                   Inference with Retrieval-Augmented Speculative Decoding", Key designs 2-4)
-  sci_verify       E2-SCI JSD test against an adaptive threshold ("E2-SCI: Elastic
-                   Edge-Cloud Speculative Decoding via Credit Inertia", Key design 3)
+  asymspec_verify        AsymSpec CDA gate + delta-fusion ("AsymSpec: Context-Asymmetric
+                         Speculative Decoding for Agentic LLMs", sec. 4.1-4.2)
+  asymspec_verify_sweep  the same for every (beta, gamma) of a grid from one read (sec. 5)
+  asymspec_sci_verify    AsymSpec and one E2-SCI window on the same tensors from one read
+  asymspec_verify_host   AsymSpec on host buffers (copies in and out on the call's stream)
+  rapid_verify           RAPID retrieval-augmented target verification ("RAPID: Long-Context
+                         Inference with Retrieval-Augmented Speculative Decoding", Key designs 2-4)
+  sci_verify             E2-SCI JSD test against an adaptive threshold ("E2-SCI: Elastic
+                         Edge-Cloud Speculative Decoding via Credit Inertia", Key design 3)
 """
 from __future__ import annotations
 
