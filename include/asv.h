@@ -123,6 +123,11 @@ asv_status asv_query_plan(int mode, int B, int K, int V, int dtype, int* cluster
  *   out_lse [B, K+1, 3] float, log-sum-exp of a, b, t (may be NULL);
  *   out_req_status [B] uint32 ASV_REQ_* bits.
  * B = 0 is a no-op that returns ASV_OK.
+ * Checks, in this order, each returning before anything is queued on the GPU: B, K, V
+ * (ASV_ERR_SHAPE), dtype (ASV_ERR_DTYPE); for B > 0: beta, gamma (ASV_ERR_PARAM), the alignment
+ * of every pointer given, NULL counting as aligned (ASV_ERR_ALIGN), the required pointers
+ * (ASV_ERR_NULL), then the workspace (ASV_ERR_WORKSPACE, ASV_ERR_ALIGN for a workspace not
+ * 256-byte aligned).
  */
 asv_status asymspec_verify(const void* a, const void* b, const void* t, int dtype, const int32_t* draft_ids, int B,
                            int K, int V, float beta, float gamma, int32_t* out_accept_len, int32_t* out_tokens,
@@ -199,8 +204,13 @@ asv_status asymspec_verify_host(const void* a_host, const void* b_host, const vo
  * The call allocates nothing (no cudaMalloc, no cudaFree, no allocating library routine).
  * - Batches whose workspace (asv_workspace_bytes) exceeds ASV_STATIC_SCRATCH_BYTES are rejected
  *   with ASV_ERR_WORKSPACE (at K = 8 that is a little over 7,000 requests).
- * - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
- *   that device current and caches it; make that first call before any stream capture.
+ * - Every call made outside stream capture looks up the array's device address
+ *   (cudaGetSymbolAddress) with the current device, so a device reset between calls (which reloads
+ *   the module and may move the array) is picked up.  A call made while `stream` is capturing uses
+ *   the address found by the last call outside capture on that device: make the first call on a
+ *   device, and the first call after any device reset, before capturing.
+ * - Every argument check of asymspec_verify, and the size limit, comes before the GPU or the array
+ *   is touched: a rejected call queues nothing.
  * - Every call shares the one array.  Each call clears the part that must start at zero (one
  *   cudaMemsetAsync on `stream`) before its kernel; calls that may overlap on the GPU (other
  *   streams, other host threads) race on the array and must not be issued.

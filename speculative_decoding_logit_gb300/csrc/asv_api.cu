@@ -129,6 +129,33 @@ int elem_size(int dt) { return dt == ASV_F32 ? 4 : 2; }
 
 }  // namespace
 
+namespace asv {
+
+// Argument checks of asymspec_verify, in the order they are applied: shapes and element type, then
+// (for B > 0) the scalar parameters, the alignment of every pointer given (NULL counts as
+// aligned), and last the required pointers.  A call that fails any of them touches neither the
+// GPU nor the workspace.
+asv_status check_asym_shape(int B, int K, int V, int dtype) {
+  if (B < 0 || K < 0 || V < 2) return ASV_ERR_SHAPE;
+  if ((long long)B * ((long long)K + 1) * asv::kMaxCluster > 0x7fffffffLL) return ASV_ERR_SHAPE;
+  if (!valid_dtype(dtype)) return ASV_ERR_DTYPE;
+  return ASV_OK;
+}
+
+asv_status check_asym_args(const void* a, const void* b, const void* t, int dtype, const int32_t* draft_ids, int K,
+                           float beta, float gamma, const int32_t* out_accept_len, const int32_t* out_tokens,
+                           const float* out_D, const float* out_lse, const uint32_t* out_req_status) {
+  if (!std::isfinite(beta) || !std::isfinite(gamma) || !(gamma > 0.0f)) return ASV_ERR_PARAM;
+  const size_t eb = size_t(elem_size(dtype));
+  if (!aligned(a, eb) || !aligned(b, eb) || !aligned(t, eb) || !aligned(draft_ids, 4) || !aligned(out_accept_len, 4) ||
+      !aligned(out_tokens, 4) || !aligned(out_req_status, 4) || !aligned(out_D, 4) || !aligned(out_lse, 4))
+    return ASV_ERR_ALIGN;
+  if (!a || !b || !t || (K > 0 && !draft_ids) || !out_accept_len || !out_tokens || !out_req_status) return ASV_ERR_NULL;
+  return ASV_OK;
+}
+
+}  // namespace asv
+
 extern "C" {
 
 const char* asv_status_string(asv_status s) {
@@ -254,17 +281,12 @@ asv_status asymspec_verify_ex(const void* a, const void* b, const void* t, int d
                               uint32_t* out_req_status, void* workspace, size_t ws_bytes, cudaStream_t stream) {
   const int dsrc = options ? options->delta_source : ASV_DELTA_A_MINUS_B;
   if (dsrc < ASV_DELTA_A_MINUS_B || dsrc > ASV_DELTA_T_MINUS_B) return ASV_ERR_PARAM;
-  if (B < 0 || K < 0 || V < 2) return ASV_ERR_SHAPE;
-  if ((long long)B * (K + 1) * asv::kMaxCluster > 0x7fffffffLL) return ASV_ERR_SHAPE;
-  if (!valid_dtype(dtype)) return ASV_ERR_DTYPE;
-  if (B == 0) return ASV_OK;
-  if (!a || !b || !t || (K > 0 && !draft_ids) || !out_accept_len || !out_tokens || !out_req_status) return ASV_ERR_NULL;
+  asv_status st = asv::check_asym_shape(B, K, V, dtype);
+  if (st != ASV_OK || B == 0) return st;
+  st = asv::check_asym_args(a, b, t, dtype, draft_ids, K, beta, gamma, out_accept_len, out_tokens, out_D, out_lse,
+                           out_req_status);
+  if (st != ASV_OK) return st;
   if (!workspace) return ASV_ERR_WORKSPACE;
-  const size_t eb = size_t(elem_size(dtype));
-  if (!aligned(a, eb) || !aligned(b, eb) || !aligned(t, eb) || !aligned(draft_ids, 4) || !aligned(out_accept_len, 4) ||
-      !aligned(out_tokens, 4) || !aligned(out_req_status, 4) || !aligned(out_D, 4) || !aligned(out_lse, 4))
-    return ASV_ERR_ALIGN;
-  if (!std::isfinite(beta) || !std::isfinite(gamma) || !(gamma > 0.0f)) return ASV_ERR_PARAM;
   asv::JsdArgs args;
   std::memset(&args, 0, sizeof(args));
   args.x[0] = a;

@@ -6,6 +6,8 @@
 
 #include <cuda_runtime.h>
 
+#include "asv.h"
+
 namespace asv {
 
 constexpr int kMaxCluster = 16;  // CTAs per row (16 needs the non-portable cluster attribute)
@@ -149,6 +151,14 @@ int rapid_smem_bytes(bool all_sums, int n_slice);                // dynamic shar
 int rapid_draw_smem_bytes(int n_slice, bool aligned);            // ... of the draw launch
 int rapid_threads();      // threads per CTA of the RAPID kernel
 int rapid_ctas_per_sm();  // CTAs of it that share an SM (its launch bounds)
+
+// Host-side argument checks shared by asymspec_verify and asymspec_verify_static (asv_api.cu):
+// check_asym_shape covers B, K, V and the element type; check_asym_args (for B > 0) the scalar
+// parameters, then the alignment of every pointer given, then the required pointers.
+asv_status check_asym_shape(int B, int K, int V, int dtype);
+asv_status check_asym_args(const void* a, const void* b, const void* t, int dtype, const int32_t* draft_ids, int K,
+                           float beta, float gamma, const int32_t* out_accept_len, const int32_t* out_tokens,
+                           const float* out_D, const float* out_lse, const uint32_t* out_req_status);
 
 // Occupancy query: clusters of `plan` that can be resident at once (0 = cannot launch).
 int jsd_max_active_clusters(int mode, int dtype, const LaunchPlan& plan);

@@ -131,9 +131,9 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
 
   // L2 policies: the verifier input is read once (evict first; fused: pass B reads it again); the
   // divergence pair is read again by pass B (evict last until then, evict first on that last read).
-  const uint64_t pol_last = policy_evict_first();
+  const uint64_t pol_evict_first = policy_evict_first();
   const uint64_t pol_keep = policy_evict_last();
-  const uint64_t pol_t = FUSE ? pol_keep : pol_last;
+  const uint64_t pol_t = FUSE ? pol_keep : pol_evict_first;
 
   // ---------------------------------------------------------------- pass A: maxima, exp sums, argmax
   RunMax<T> rmax[NT];
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
 #pragma unroll
       for (int m = 0; m < NPB; ++m)
         cp_async16(smem_addr(&s_ring[((j & (kRing - 1)) * NPB + m) * kJsdThreads + tid]),
-                   static_cast<const char*>(slice[m < 2 ? m : NT - 1]) + size_t(vi) * 16u, pol_last);
+                   static_cast<const char*>(slice[m < 2 ? m : NT - 1]) + size_t(vi) * 16u, pol_evict_first);
     }
     cp_async_commit();
   };
@@ -522,16 +522,16 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
       int vi = tid;
       uint4 ca, cb, ct, na, nb, nt;
       if (vi < nvec) {
-        ca = G::load(slice[0], vi * VEC, len, aligned, true, pol_last);
-        cb = G::load(slice[1], vi * VEC, len, aligned, true, pol_last);
-        if constexpr (FUSE) ct = G::load(slice[NT - 1], vi * VEC, len, aligned, true, pol_last);
+        ca = G::load(slice[0], vi * VEC, len, aligned, true, pol_evict_first);
+        cb = G::load(slice[1], vi * VEC, len, aligned, true, pol_evict_first);
+        if constexpr (FUSE) ct = G::load(slice[NT - 1], vi * VEC, len, aligned, true, pol_evict_first);
       }
       for (; vi < nvec; vi += kJsdThreads) {
         const int vn = vi + kJsdThreads;
         if (vn < nvec) {
-          na = G::load(slice[0], vn * VEC, len, aligned, true, pol_last);
-          nb = G::load(slice[1], vn * VEC, len, aligned, true, pol_last);
-          if constexpr (FUSE) nt = G::load(slice[NT - 1], vn * VEC, len, aligned, true, pol_last);
+          na = G::load(slice[0], vn * VEC, len, aligned, true, pol_evict_first);
+          nb = G::load(slice[1], vn * VEC, len, aligned, true, pol_evict_first);
+          if constexpr (FUSE) nt = G::load(slice[NT - 1], vn * VEC, len, aligned, true, pol_evict_first);
         }
         float2 xa[NP], xb[NP];
         G::pairs(ca, xa);

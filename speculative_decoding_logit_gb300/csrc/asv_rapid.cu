@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
   const float* zsl = p.z + row_base + v0;
   const float* qsl = p.q + row_base + v0;
   const uint64_t pol_keep = policy_evict_last();
-  const uint64_t pol_last = policy_evict_first();
+  const uint64_t pol_evict_first = policy_evict_first();
   const float invT = p.inv_T;
   const float etaT = p.eta * p.T;
   const float ln_tf = p.ln_tail_frac;
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
   {
     const float2 l2e2 = make_float2(kLog2e, kLog2e);
     // AE: pass B re-reads the whole slice (keep it in L2); else only a few vectors.
-    const uint64_t polA = AE ? pol_keep : pol_last;
+    const uint64_t polA = AE ? pol_keep : pol_evict_first;
     float gmax = -INFINITY;
     int it = 0;
     int vi = tid;
@@ -546,14 +546,14 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
     int vi = tid;
     float4 cz, cq, nz, nq;
     if (vi < nvec) {
-      cz = ld4(zsl, vi * VEC, len, ALIGNED, pol_last, -INFINITY);
-      cq = ld4(qsl, vi * VEC, len, ALIGNED, pol_last, 0.0f);
+      cz = ld4(zsl, vi * VEC, len, ALIGNED, pol_evict_first, -INFINITY);
+      cq = ld4(qsl, vi * VEC, len, ALIGNED, pol_evict_first, 0.0f);
     }
     for (; vi < nvec; vi += kRapidThreads) {
       const int vn = vi + kRapidThreads;
       if (vn < nvec) {
-        nz = ld4(zsl, vn * VEC, len, ALIGNED, pol_last, -INFINITY);
-        nq = ld4(qsl, vn * VEC, len, ALIGNED, pol_last, 0.0f);
+        nz = ld4(zsl, vn * VEC, len, ALIGNED, pol_evict_first, -INFINITY);
+        nq = ld4(qsl, vn * VEC, len, ALIGNED, pol_evict_first, 0.0f);
       }
       float2 p0, p1, h0, h1;
       pzhs2(make_float2(cz.x, cz.y), make_float2(cq.x, cq.y), invT2, nML2, inv2, etaT2, p0, h0);
@@ -793,8 +793,8 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
       } else {
         // Pass C: a thread ran out of candidate slots; test every entry of the slice.
         for (int vi = tid; vi < nvec; vi += kRapidThreads) {
-          const float4 z4 = ld4(zsl, vi * VEC, len, ALIGNED, pol_last, -INFINITY);
-          const float4 q4 = ld4(qsl, vi * VEC, len, ALIGNED, pol_last, 0.0f);
+          const float4 z4 = ld4(zsl, vi * VEC, len, ALIGNED, pol_evict_first, -INFINITY);
+          const float4 q4 = ld4(qsl, vi * VEC, len, ALIGNED, pol_evict_first, 0.0f);
           const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
           const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll

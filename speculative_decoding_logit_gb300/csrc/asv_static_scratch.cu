@@ -26,15 +26,22 @@ void* g_scratch_addr[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
 // Device address of g_static_scratch on the current device.  In host code the array's name is
-// only a host-side stand-in, so the address is looked up once per device (with that device
-// current) and cached.
-cudaError_t scratch_address(void** out) {
+// only a host-side stand-in, so the address is looked up with the device current.  A call made
+// outside stream capture looks it up again every time (a device reset reloads the module, and
+// the array may then sit at another address); a call made while `stream` is capturing uses the
+// address the last call outside capture found on this device (a lookup may load the module,
+// which capture does not allow), and looks it up only if there is none yet.
+cudaError_t scratch_address(cudaStream_t stream, void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  bool capturing = true;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) == cudaSuccess) capturing = cs != cudaStreamCaptureStatusNone;
+  else cudaGetLastError();
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  if (!capturing || !g_scratch_addr[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_static_scratch);
     if (e != cudaSuccess) return e;
@@ -50,12 +57,19 @@ extern "C" asv_status asymspec_verify_static(const void* a, const void* b, const
                                              const int32_t* draft_ids, int B, int K, int V, float beta, float gamma,
                                              int32_t* out_accept_len, int32_t* out_tokens, float* out_D,
                                              float* out_lse, uint32_t* out_req_status, cudaStream_t stream) {
-  if (B < 0 || K < 0 || V < 2) return ASV_ERR_SHAPE;
+  // Every check comes before the GPU or the shared array is touched: shapes (with the overflow
+  // guard on B * (K + 1)) first, so that the workspace size is computed only for a valid shape;
+  // then the size limit; then the checks asymspec_verify applies to its arguments.
+  asv_status st = asv::check_asym_shape(B, K, V, dtype);
+  if (st != ASV_OK) return st;
   const size_t need = asv_workspace_bytes(ASV_MODE_ASYMSPEC, B, K, V, dtype);
   if (need > size_t(ASV_STATIC_SCRATCH_BYTES)) return ASV_ERR_WORKSPACE;  // batch too large for the static scratch
   if (B == 0) return ASV_OK;
+  st = asv::check_asym_args(a, b, t, dtype, draft_ids, K, beta, gamma, out_accept_len, out_tokens, out_D, out_lse,
+                            out_req_status);
+  if (st != ASV_OK) return st;
   void* ws = nullptr;
-  cudaError_t e = scratch_address(&ws);
+  cudaError_t e = scratch_address(stream, &ws);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return ASV_ERR_CUDA;

@@ -44,28 +44,68 @@ def test_status_strings_and_workspace_sizes(lib):
 
 
 def test_host_validation_without_gpu(lib):
+    """Each case leaves every pointer NULL except the one it checks, so a regression in a check
+    ends at ASV_ERR_NULL on the host: no case can reach a launch."""
     f = lib.asymspec_verify
     vp = C.c_void_p
     f.argtypes = [vp, vp, vp, C.c_int, vp, C.c_int, C.c_int, C.c_int, C.c_float, C.c_float, vp, vp, vp, vp, vp, vp,
                   C.c_size_t, vp]
-    P = 1 << 20  # a non-null, 256-aligned stand-in address (never dereferenced: calls fail first)
+    host = (C.c_uint32 * 16)()   # a real (host) allocation: misaligned addresses are taken inside it
+    base = C.addressof(host)
+    assert base % 4 == 0
 
-    def call(B=2, K=2, V=64, dt=0, beta=1.0, gamma=0.5, a=P, ws=P, wsb=1 << 20, d=P):
-        return f(a, P, P, dt, d, B, K, V, beta, gamma, P, P, P, P, P, ws, wsb, None)
+    def call(B=2, K=2, V=64, dt=0, beta=1.0, gamma=0.5, a=None):
+        return f(a, None, None, dt, None, B, K, V, beta, gamma, None, None, None, None, None, None, 1 << 20, None)
 
     assert call(B=-1) == 2
     assert call(K=-1) == 2
     assert call(V=1) == 2
+    assert call(B=1 << 30, K=7) == 2           # B * (K + 1) beyond the launch grid
     assert call(dt=5) == 4
     assert call(B=0) == 0                      # empty batch is a no-op
-    assert call(a=None) == 1
-    assert call(d=None) == 1
-    assert call(ws=None) == 6
-    assert call(a=P + 2) == 3                  # fp32 input not 4-byte aligned
     assert call(gamma=0.0) == 5
     assert call(gamma=float("nan")) == 5
     assert call(beta=float("inf")) == 5
-    assert call(wsb=16) == 6                   # workspace too small
+    assert call(a=base + 2) == 3               # fp32 input not 4-byte aligned (checked before NULLs)
+    assert call(a=base + 2, dt=1) == 1         # 2-byte aligned is enough for bf16: then the NULLs
+    assert call() == 1                         # required pointers missing
+
+
+def _sized_workspace_bytes(lib):
+    return lib.asv_workspace_bytes(0, 2, 2, 64, 0)
+
+
+@pytest.mark.gpu
+def test_workspace_checks_with_real_buffers(lib):
+    """Workspace errors need every other argument valid: real device buffers of a B=2, K=2, V=64
+    fp32 batch, then a workspace that is missing, too small, misaligned, and finally sufficient."""
+    import torch
+    vp = C.c_void_p
+    f = lib.asymspec_verify
+    f.argtypes = [vp, vp, vp, C.c_int, vp, C.c_int, C.c_int, C.c_int, C.c_float, C.c_float, vp, vp, vp, vp, vp, vp,
+                  C.c_size_t, vp]
+    B, K, V = 2, 2, 64
+    g = torch.Generator().manual_seed(5)
+    a, b, t = (torch.randn(B, K + 1, V, generator=g).cuda() for _ in range(3))
+    d = torch.zeros(B, K, dtype=torch.int32, device="cuda")
+    acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    tok = torch.empty(B, K + 1, dtype=torch.int32, device="cuda")
+    D = torch.empty(B, K + 1, device="cuda")
+    st = torch.empty(B, dtype=torch.int32, device="cuda")
+    need = _sized_workspace_bytes(lib)
+    ws = torch.zeros(need + 512, dtype=torch.uint8, device="cuda")
+    sh = torch.cuda.current_stream().cuda_stream
+
+    def call(w, nbytes):
+        return f(a.data_ptr(), b.data_ptr(), t.data_ptr(), 0, d.data_ptr(), B, K, V, 1.0, 0.5, acc.data_ptr(),
+                 tok.data_ptr(), D.data_ptr(), None, st.data_ptr(), w, nbytes, sh)
+
+    assert call(None, need) == 6
+    assert call(ws.data_ptr(), 16) == 6
+    assert call(ws.data_ptr() + 16, need) == 3      # workspace not 256-byte aligned
+    assert call(ws.data_ptr(), need) == 0
+    torch.cuda.synchronize()
+    assert int(torch.count_nonzero(ws)) == 0
 
 
 def test_tuning_override_validation(lib):

@@ -76,12 +76,13 @@ def test_static_scratch_rejects_batches_beyond_its_size():
     B = 200000   # about 2 million rows: a workspace far beyond the static scratch
     need = lib.asv_workspace_bytes(0, B, K, V, 1)
     limit = _static_scratch_bytes()
-    # The call below passes placeholder addresses: it must be rejected before any launch, so the
-    # batch has to be far beyond the limit (checked here, not assumed).
-    assert need > 8 * limit, (need, limit)
+    # Every pointer is NULL: the size check must reject the batch first (ASV_ERR_WORKSPACE); if it
+    # ever let the batch through, the argument checks that follow it stop the call at ASV_ERR_NULL
+    # on the host.  Either way nothing reaches the GPU.
     f = lib.asymspec_verify_static
     vp = C.c_void_p
     f.argtypes = [vp, vp, vp, C.c_int, vp, C.c_int, C.c_int, C.c_int, C.c_float, C.c_float, vp, vp, vp, vp, vp, vp]
     f.restype = C.c_int
-    P = 1 << 20
-    assert f(P, P, P, 1, P, B, K, V, 1.0, 0.5, P, P, P, P, P, None) == 6   # ASV_ERR_WORKSPACE, nothing launched
+    assert f(None, None, None, 1, None, B, K, V, 1.0, 0.5, None, None, None, None, None, None) == 6
+    # Within the limit, the same all-NULL call ends at the argument checks, before any CUDA call.
+    assert f(None, None, None, 1, None, 4, K, V, 1.0, 0.5, None, None, None, None, None, None) == 1
