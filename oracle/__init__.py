@@ -31,7 +31,8 @@ FLAG_BAD_DRAFT = 2
 FLAG_NEAR_MARGIN = 4
 FLAG_NEAR_TAIL = 8
 FLAG_NEAR_RACE = 16
-FLAGS_UNGRADED = FLAG_NEAR_MARGIN | FLAG_NEAR_TAIL | FLAG_NEAR_RACE
+FLAG_NEAR_TIE = 32
+FLAGS_UNGRADED = FLAG_NEAR_MARGIN | FLAG_NEAR_TAIL | FLAG_NEAR_RACE | FLAG_NEAR_TIE
 
 
 def build(force: bool = False) -> str:
@@ -68,18 +69,18 @@ def _declare(L):
     L.oracle_lse.restype = C.c_double
     L.oracle_jsd.argtypes = [_vp, _vp, C.c_int, C.c_size_t, C.c_size_t, C.c_int]
     L.oracle_jsd.restype = C.c_double
-    L.oracle_fused_argmax.argtypes = [_vp, _vp, _vp, C.c_int, C.c_size_t, C.c_int, C.c_float]
-    L.oracle_fused_argmax.restype = C.c_int
-    L.oracle_fused_argmax_f64.argtypes = [_vp, _vp, _vp, C.c_int, C.c_size_t, C.c_int, C.c_double]
-    L.oracle_fused_argmax_f64.restype = C.c_int
+    L.oracle_fused_argmax_exact.argtypes = [_vp, _vp, _vp, C.c_int, C.c_size_t, C.c_int, C.c_double, C.c_int,
+                                            C.POINTER(C.c_int)]
+    L.oracle_fused_argmax_exact.restype = C.c_int
+    L.oracle_fused_argmax_fp32.argtypes = [_vp, _vp, _vp, C.c_int, C.c_size_t, C.c_int, C.c_float, C.c_int]
+    L.oracle_fused_argmax_fp32.restype = C.c_int
     L.oracle_asymspec_verify.argtypes = [_vp, _vp, _vp, C.c_int, _i32p, C.c_int, C.c_int, C.c_int, C.c_float,
-                                         C.c_float, _i32p, _i32p, _f64p, _f64p, _f64p, _i32p, _u32p]
+                                         C.c_float, _i32p, _i32p, _f64p, _f64p, _f64p, _i32p, _i32p, _u32p]
     L.oracle_asymspec_verify.restype = None
     L.oracle_asymspec_verify_src.argtypes = [_vp, _vp, _vp, C.c_int, _i32p, C.c_int, C.c_int, C.c_int, C.c_float,
-                                             C.c_float, C.c_int, _i32p, _i32p, _f64p, _f64p, _f64p, _i32p, _u32p]
+                                             C.c_float, C.c_int, _i32p, _i32p, _f64p, _f64p, _f64p, _i32p, _i32p,
+                                             _u32p]
     L.oracle_asymspec_verify_src.restype = None
-    L.oracle_fused_argmax_src.argtypes = [_vp, _vp, _vp, C.c_int, C.c_size_t, C.c_int, C.c_float, C.c_int]
-    L.oracle_fused_argmax_src.restype = C.c_int
     L.oracle_philox4x32_10.argtypes = [_u32p, _u32p, _u32p]
     L.oracle_philox4x32_10.restype = None
     L.oracle_uniform_from_word.argtypes = [C.c_uint32]
@@ -146,15 +147,26 @@ def jsd(x: np.ndarray, y: np.ndarray) -> float:
     return lib().oracle_jsd(x.ctypes.data, y.ctypes.data, _elem_dtype(x), 0, 0, x.size)
 
 
+def fused_argmax_near(a, b, t, beta: float, delta_source: int = 0):
+    """The delta-fusion token of one row, argmax_k (t_k + beta * delta_k) taken exactly (lowest
+    index on ties), and whether another entry lies within single-precision rounding of it."""
+    a, b, t = _c(a), _c(b), _c(t)
+    near = C.c_int(0)
+    k = lib().oracle_fused_argmax_exact(a.ctypes.data, b.ctypes.data, t.ctypes.data, _elem_dtype(a), 0, a.size,
+                                        float(np.float32(beta)), int(delta_source), C.byref(near))
+    return k, bool(near.value)
+
+
 def fused_argmax(a, b, t, beta: float) -> int:
-    a, b, t = _c(a), _c(b), _c(t)
-    return lib().oracle_fused_argmax(a.ctypes.data, b.ctypes.data, t.ctypes.data, _elem_dtype(a), 0, a.size, beta)
+    return fused_argmax_near(a, b, t, beta)[0]
 
 
-def fused_argmax_f64(a, b, t, beta: float) -> int:
+def fused_argmax_fp32(a, b, t, beta: float, delta_source: int = 0) -> int:
+    """What a single-precision evaluation of the same score picks (informational: the tests count
+    the rows where it differs from the exact argmax, each of which must be a near tie)."""
     a, b, t = _c(a), _c(b), _c(t)
-    return lib().oracle_fused_argmax_f64(a.ctypes.data, b.ctypes.data, t.ctypes.data, _elem_dtype(a), 0, a.size,
-                                         beta)
+    return lib().oracle_fused_argmax_fp32(a.ctypes.data, b.ctypes.data, t.ctypes.data, _elem_dtype(a), 0, a.size,
+                                          beta, int(delta_source))
 
 
 # ------------------------------------------------------------------ AsymSpec
@@ -166,8 +178,9 @@ class AsymSpecResult:
     D: np.ndarray            # [B, K+1] float64
     lse: np.ndarray          # [B, K+1, 3] float64 (a, b, t)
     margin: np.ndarray       # [B, K] float64
-    argmax: np.ndarray       # [B, K+1] int32
+    argmax: np.ndarray       # [B, K+1] int32 (exact delta-fusion argmax of every row)
     flags: np.ndarray        # [B] uint32
+    near: np.ndarray = None  # [B, K+1] bool: the row's argmax is a near tie
 
 
 DELTA_A_MINUS_B = 0
@@ -176,9 +189,7 @@ DELTA_T_MINUS_B = 2
 
 
 def fused_argmax_src(a, b, t, beta: float, delta_source: int) -> int:
-    a, b, t = _c(a), _c(b), _c(t)
-    return lib().oracle_fused_argmax_src(a.ctypes.data, b.ctypes.data, t.ctypes.data, _elem_dtype(a), 0, a.size,
-                                         beta, delta_source)
+    return fused_argmax_near(a, b, t, beta, delta_source)[0]
 
 
 def asymspec_verify(a, b, t, draft_ids, beta: float, gamma: float, delta_source: int = 0) -> AsymSpecResult:
@@ -189,11 +200,13 @@ def asymspec_verify(a, b, t, draft_ids, beta: float, gamma: float, delta_source:
     out = AsymSpecResult(np.zeros(B, np.int32), np.zeros((B, R), np.int32), np.zeros((B, R)),
                          np.zeros((B, R, 3)), np.zeros((B, max(K, 0))), np.zeros((B, R), np.int32),
                          np.zeros(B, np.uint32))
+    near = np.zeros((B, R), np.int32)
     lib().oracle_asymspec_verify_src(a.ctypes.data, b.ctypes.data, t.ctypes.data, _elem_dtype(a), _p(d, C.c_int32),
-                                 B, K, V, beta, gamma, delta_source, _p(out.accept_len, C.c_int32),
-                                 _p(out.tokens, C.c_int32),
-                                 _p(out.D, C.c_double), _p(out.lse, C.c_double), _p(out.margin, C.c_double),
-                                 _p(out.argmax, C.c_int32), _p(out.flags, C.c_uint32))
+                                     B, K, V, beta, gamma, delta_source, _p(out.accept_len, C.c_int32),
+                                     _p(out.tokens, C.c_int32),
+                                     _p(out.D, C.c_double), _p(out.lse, C.c_double), _p(out.margin, C.c_double),
+                                     _p(out.argmax, C.c_int32), _p(near, C.c_int32), _p(out.flags, C.c_uint32))
+    out.near = near.astype(bool)
     return out
 
 

@@ -25,8 +25,9 @@
  *   - The CDA accept test is the printed strict inequality, taken in the log domain.
  *   - The delta-fusion token is also emitted at the bonus row when all K drafts pass.
  *   - argmax ties go to the lowest index.  The delta-fusion score t + beta*(a - b)
- *     decides an integer, so it is formed in the kernel's precision (fp32: one
- *     rounded subtraction, then one fused multiply-add); everything else is double.
+ *     is taken exactly (double); a row whose winner another entry could displace
+ *     under the rounding of a single-precision evaluation of the same score is
+ *     marked as a near tie, counted by the parity tests instead of graded.
  *   - RAPID: probability-domain tail mask taken before protection; tail entries
  *     keep p exactly and the head is rescaled so the protected target sums to 1;
  *     accept iff u*q(d) < p'(d); residual max(p - p', p - q, 0) drawn by an
@@ -54,6 +55,7 @@
 #define OR_NEAR_MARGIN 4u
 #define OR_NEAR_TAIL 8u
 #define OR_NEAR_RACE 16u
+#define OR_NEAR_TIE 32u
 
 static float widen_f(const void* base, int dtype, size_t i) {
   if (dtype == OR_F32) return ((const float*)base)[i];
@@ -114,34 +116,86 @@ double oracle_jsd(const void* x, const void* y, int dtype, size_t offx, size_t o
   return D;
 }
 
-/* Lowest index attaining the maximum of the fp32 score
- * s_k = fmaf(beta, a_k - b_k, t_k).  An entry whose score is NaN or -inf (a token
- * the fused scores make impossible) is never chosen; if no entry qualifies the
- * result is 0.  [ASYM] sec. 4.1: d' = argmax(t + beta*delta), delta = a - b. */
-int oracle_fused_argmax(const void* a, const void* b, const void* t, int dtype, size_t off, int V,
-                        float beta) {
+/* The context-gain signal of the delta-fusion score ([ASYM] sec. 5, mechanism
+ * ablation): 0 -> delta = a - b (the method), 1 -> delta = a (raw enhanced
+ * logits), 2 -> delta = t - b (two-model difference). */
+static double delta_of(const void* a, const void* b, const void* t, int dtype, size_t i, int delta_source) {
+  if (delta_source == 1) return widen(a, dtype, i);
+  if (delta_source == 2) return widen(t, dtype, i) - widen(b, dtype, i);
+  return widen(a, dtype, i) - widen(b, dtype, i);
+}
+
+/* 1 when delta and the score t + beta * delta are single-precision numbers and the
+ * double evaluation of the score is exact (so every correctly rounded evaluation,
+ * in any precision down to single, gives the same value): delta is checked by a
+ * round trip through float; beta * delta is then exact in double (two 24-bit
+ * significands); the sum's rounding error comes from Knuth's TwoSum. */
+static int score_is_f32(double t, double beta, double d) {
+  if ((double)(float)d != d) return 0;
+  double p = beta * d;
+  double s = t + p;
+  double bp = s - t;
+  double err = (t - (s - bp)) + (p - bp);
+  return err == 0.0 && (double)(float)s == s;
+}
+
+/* The delta-fusion token, [ASYM] sec. 4.1: d' = argmax_k (t_k + beta * delta_k),
+ * taken exactly: the stored values widen to double without rounding, their
+ * difference and beta * delta are exact in double, and the sum carries a
+ * rounding of order 1e-16 relative at most.  Lowest index among equal scores;
+ * an entry whose score is NaN or -inf (a token the fused scores make impossible)
+ * is never chosen; if no entry qualifies the result is 0.
+ *
+ * *near (may be NULL) is set when the decision is within rounding distance of
+ * another entry k for a single-precision evaluation of the same score (delta
+ * rounded once, then one rounded fused multiply-add, each within 2^-24 relative):
+ *   0 < s_w - s_k <= 2^-22 * (|s_w| + |s_k| + |beta| * (|delta_w| + |delta_k|)),
+ * four times the bound on the two scores' rounding errors; or s_k == s_w with
+ * one of the two deltas or scores not a single-precision number (the rounding
+ * could then order them either way). */
+int oracle_fused_argmax_exact(const void* a, const void* b, const void* t, int dtype, size_t off, int V, double beta,
+                              int delta_source, int* near) {
   int best = -1;
-  float bv = -INFINITY;
+  double bv = -INFINITY;
   for (int k = 0; k < V; ++k) {
-    float ak = widen_f(a, dtype, off + (size_t)k);
-    float bk = widen_f(b, dtype, off + (size_t)k);
-    float tk = widen_f(t, dtype, off + (size_t)k);
-    float d = ak - bk;
-    float s = fmaf(beta, d, tk);
+    size_t i = off + (size_t)k;
+    double s = widen(t, dtype, i) + beta * delta_of(a, b, t, dtype, i, delta_source);
     if (s > bv) {
       bv = s;
       best = k;
     }
   }
-  return best < 0 ? 0 : best;
+  if (near) *near = 0;
+  if (best < 0) return 0;
+  if (near) {
+    size_t iw = off + (size_t)best;
+    double dw = delta_of(a, b, t, dtype, iw, delta_source);
+    int exact_w = score_is_f32(widen(t, dtype, iw), beta, dw);
+    for (int k = 0; k < V; ++k) {
+      if (k == best) continue;
+      size_t i = off + (size_t)k;
+      double dk = delta_of(a, b, t, dtype, i, delta_source);
+      double tk = widen(t, dtype, i);
+      double sk = tk + beta * dk;
+      if (!(sk > -INFINITY)) continue; /* NaN or -inf: never chosen */
+      double gap = bv - sk;
+      if (gap == 0.0) {
+        if (!(exact_w && score_is_f32(tk, beta, dk))) *near = 1;
+      } else if (gap <= ldexp(1.0, -22) * (fabs(bv) + fabs(sk) + fabs(beta) * (fabs(dw) + fabs(dk)))) {
+        *near = 1;
+      }
+    }
+  }
+  return best;
 }
 
-/* The same argmax with the context-gain signal chosen by `delta_source`
- * ([ASYM] sec. 5, mechanism ablation): 0 -> delta = a - b (the method), 1 -> delta = a
- * (raw enhanced logits), 2 -> delta = t - b (two-model difference).  The delta is one
- * rounded fp32 operation (none for source 1), then one fused multiply-add. */
-int oracle_fused_argmax_src(const void* a, const void* b, const void* t, int dtype, size_t off, int V, float beta,
-                            int delta_source) {
+/* What a single-precision evaluation of the same score picks: delta as one
+ * rounded fp32 operation (none for delta = a), then one fused multiply-add,
+ * lowest index among equal values, NaN/-inf never chosen (0 if none qualifies).
+ * The verification does not use it: the tests count the rows where it differs
+ * from the exact argmax (every such row must be a near tie). */
+int oracle_fused_argmax_fp32(const void* a, const void* b, const void* t, int dtype, size_t off, int V, float beta,
+                             int delta_source) {
   int best = -1;
   float bv = -INFINITY;
   for (int k = 0; k < V; ++k) {
@@ -158,29 +212,13 @@ int oracle_fused_argmax_src(const void* a, const void* b, const void* t, int dty
   return best < 0 ? 0 : best;
 }
 
-/* Same score in double, for the informational count of rows where fp32 and
- * fp64 scores disagree on the winner. */
-int oracle_fused_argmax_f64(const void* a, const void* b, const void* t, int dtype, size_t off, int V,
-                            double beta) {
-  int best = -1;
-  double bv = -INFINITY;
-  for (int k = 0; k < V; ++k) {
-    double s = widen(t, dtype, off + (size_t)k) +
-               beta * (widen(a, dtype, off + (size_t)k) - widen(b, dtype, off + (size_t)k));
-    if (s > bv) {
-      bv = s;
-      best = k;
-    }
-  }
-  return best < 0 ? 0 : best;
-}
-
 /*
  * AsymSpec verification over a batch [B, K+1, V].  [ASYM] sec. 4.1-4.2.
  *
  * Per row i of request r:
  *   lse of a, b, t;  D_i = JSD(softmax a_i || softmax b_i);
- *   c_i = argmax(t_i + beta*(a_i - b_i)) (fp32 score, lowest index);
+ *   c_i = argmax(t_i + beta*(a_i - b_i)) (exact score, lowest index; near_i marks a
+ *         winner within single-precision rounding of another entry);
  * per draft row i < K with d = draft_ids[r][i]:
  *   accept iff  softmax(t_i)[d] > gamma * exp(-D_i) * softmax(b_i)[d],
  *   i.e. margin_i = (t_d - lse_t) - ln gamma + D_i - (b_d - lse_b) > 0;
@@ -188,19 +226,22 @@ int oracle_fused_argmax_f64(const void* a, const void* b, const void* t, int dty
  *
  * Outputs (any may be NULL except accept_len/tokens):
  *   out_D [B,K+1], out_lse [B,K+1,3] (a,b,t), out_margin [B,K], out_argmax [B,K+1],
- *   out_flags [B].  A request with a non-finite row or an out-of-range draft id
- *   gets accept_len 0 and tokens all -1.
+ *   out_near [B,K+1] (near_i), out_flags [B].  A request with a non-finite row or an
+ *   out-of-range draft id gets accept_len 0 and tokens all -1.  A request whose emitted
+ *   position n has a near tie is flagged OR_NEAR_TIE.
  */
 void oracle_asymspec_verify_src(const void* a, const void* b, const void* t, int dtype,
                                 const int32_t* draft_ids, int B, int K, int V, float beta, float gamma,
                                 int delta_source, int32_t* out_accept_len, int32_t* out_tokens, double* out_D,
-                                double* out_lse, double* out_margin, int32_t* out_argmax, uint32_t* out_flags) {
+                                double* out_lse, double* out_margin, int32_t* out_argmax, int32_t* out_near,
+                                uint32_t* out_flags) {
   const double ln_gamma = log((double)gamma);
   for (int r = 0; r < B; ++r) {
     uint32_t flags = 0;
     int n = K;
     double* margin = (double*)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
     int32_t* cbest = (int32_t*)malloc(sizeof(int32_t) * (size_t)(K + 1));
+    int* cnear = (int*)malloc(sizeof(int) * (size_t)(K + 1));
     for (int i = 0; i < K; ++i) {
       int d = draft_ids[(size_t)r * K + i];
       if (d < 0 || d >= V) flags |= OR_BAD_DRAFT;
@@ -213,8 +254,9 @@ void oracle_asymspec_verify_src(const void* a, const void* b, const void* t, int
       double Lb = oracle_lse(b, dtype, off, V, 1.0);
       double Lt = oracle_lse(t, dtype, off, V, 1.0);
       double D = oracle_jsd(a, b, dtype, off, off, V);
-      int c = oracle_fused_argmax_src(a, b, t, dtype, off, V, beta, delta_source);
+      int c = oracle_fused_argmax_exact(a, b, t, dtype, off, V, (double)beta, delta_source, &cnear[i]);
       cbest[i] = c;
+      if (out_near) out_near[(size_t)r * (K + 1) + i] = cnear[i];
       size_t ri = (size_t)r * (K + 1) + i;
       if (out_D) out_D[ri] = D;
       if (out_lse) {
@@ -248,6 +290,7 @@ void oracle_asymspec_verify_src(const void* a, const void* b, const void* t, int
         }
       }
       out_accept_len[r] = n;
+      if (cnear[n]) flags |= OR_NEAR_TIE;
       for (int i = 0; i <= K; ++i) {
         int32_t tok = -1;
         if (i < n) tok = draft_ids[(size_t)r * K + i];
@@ -258,15 +301,16 @@ void oracle_asymspec_verify_src(const void* a, const void* b, const void* t, int
     if (out_flags) out_flags[r] = flags;
     free(margin);
     free(cbest);
+    free(cnear);
   }
 }
 
 void oracle_asymspec_verify(const void* a, const void* b, const void* t, int dtype, const int32_t* draft_ids, int B,
                             int K, int V, float beta, float gamma, int32_t* out_accept_len, int32_t* out_tokens,
                             double* out_D, double* out_lse, double* out_margin, int32_t* out_argmax,
-                            uint32_t* out_flags) {
+                            int32_t* out_near, uint32_t* out_flags) {
   oracle_asymspec_verify_src(a, b, t, dtype, draft_ids, B, K, V, beta, gamma, 0, out_accept_len, out_tokens, out_D,
-                             out_lse, out_margin, out_argmax, out_flags);
+                             out_lse, out_margin, out_argmax, out_near, out_flags);
 }
 
 /* ------------------------------------------------------------------ Philox */

@@ -99,16 +99,80 @@ def test_jsd_bounds_identity_and_disjoint():
     assert oracle.jsd(x, y) == pytest.approx(oracle.jsd(y, x), rel=1e-14)
 
 
+def _exact_score(a, b, t, beta, dtype, src=0):
+    """t + beta * delta in float64 from the exactly widened stored values (the definition)."""
+    af, bf, tf = (gen.widen(x, dtype).astype(np.float64) for x in (a, b, t))
+    d = {0: af - bf, 1: af, 2: tf - bf}[src]
+    return tf + np.float64(np.float32(beta)) * d
+
+
 @pytest.mark.parametrize("dtype", [gen.F32, gen.BF16])
 def test_fused_argmax_matches_numpy(dtype):
     rng = np.random.default_rng(5)
     for beta in (0.0, 1.0, 1.5, -0.75):
         for V in (1, 2, 9, 16, 4097):
             a, b, t = _rows(rng, 3, V, dtype)
-            af, bf, tf = (gen.widen(x, dtype) for x in (a, b, t))
-            d = (af - bf).astype(np.float32)                       # one rounding
-            s = (np.float64(np.float32(beta)) * d.astype(np.float64) + tf.astype(np.float64)).astype(np.float32)
-            assert oracle.fused_argmax(a, b, t, beta) == int(np.argmax(s))
+            assert oracle.fused_argmax(a, b, t, beta) == int(np.argmax(_exact_score(a, b, t, beta, dtype)))
+
+
+def test_fused_argmax_is_shift_invariant_and_ignores_equal_drafters():
+    """Adding a constant to t (exactly representable) or to both a and b leaves the winner; with
+    a == b the score is t itself (ASYM sec. 4.1: no context gain, no steering)."""
+    rng = np.random.default_rng(15)
+    for _ in range(20):
+        a, b, t = _rows(rng, 3, 777, gen.F32)
+        k = oracle.fused_argmax(a, b, t, 1.5)
+        assert oracle.fused_argmax(a, b, t + np.float32(8.0), 1.5) == k or oracle.fused_argmax_near(a, b, t, 1.5)[1]
+        assert oracle.fused_argmax(a, a, t, 2.0) == int(np.argmax(t))
+
+
+def test_fused_argmax_near_tie_under_single_precision():
+    """A row built so that the exact scores differ by 2^-30 while the single-precision evaluation
+    rounds both to the same value: the exact argmax is entry 1, the fp32 evaluation picks entry 0
+    (lowest index of equal values), and the oracle flags the row as a near tie."""
+    a = np.array([1 + 2 ** -23, 1 + 2 ** -23, -3.0], np.float32)
+    b = np.array([2 ** -30, 0.0, 0.0], np.float32)
+    t = np.zeros(3, np.float32)
+    assert float(a[0]) - float(b[0]) < float(a[1]) - float(b[1])          # exact order: entry 1 wins
+    assert np.float32(a[0] - b[0]) == np.float32(a[1] - b[1])             # fp32 difference: a tie
+    k, near = oracle.fused_argmax_near(a, b, t, 1.0)
+    assert (k, near) == (1, True)
+    assert oracle.fused_argmax_fp32(a, b, t, 1.0) == 0
+    # the same rows spread apart by more than the rounding bound: no flag
+    b2 = np.array([2 ** -10, 0.0, 0.0], np.float32)
+    assert oracle.fused_argmax_near(a, b2, t, 1.0) == (1, False)
+    # an exact tie of single-precision scores is decided by the index rule and not flagged
+    t3 = np.array([2.0, 2.0, 0.5], np.float32)
+    z = np.zeros(3, np.float32)
+    assert oracle.fused_argmax_near(z, z, t3, 1.0) == (0, False)
+    # an exact tie whose delta is not a single-precision number is flagged (rounding could reorder it)
+    a4 = np.array([1.0, 1.0 + 2 ** -23], np.float32)
+    b4 = np.array([2 ** -40, 2 ** -23 + 2 ** -40], np.float32)
+    t4 = np.zeros(2, np.float32)
+    s4 = _exact_score(a4, b4, t4, 1.0, gen.F32)
+    assert s4[0] == s4[1]
+    assert oracle.fused_argmax_near(a4, b4, t4, 1.0) == (0, True)
+
+
+@pytest.mark.parametrize("dtype", [gen.F32, gen.BF16])
+def test_single_precision_winners_differ_only_on_near_ties(dtype):
+    """Over many random rows (values spread so that near ties happen), every row where the
+    single-precision evaluation picks another entry than the exact argmax is flagged near."""
+    rng = np.random.default_rng(16 + dtype)
+    differ = 0
+    for _ in range(300):
+        V = int(rng.integers(2, 40))
+        a = gen.store(np.round(rng.standard_normal(V) * 8) / 8 + rng.standard_normal(V) * 1e-6, dtype)
+        b = gen.store(np.round(rng.standard_normal(V) * 8) / 8, dtype)
+        t = gen.store(np.round(rng.standard_normal(V) * 8) / 8, dtype)
+        beta = float(rng.choice([1.0, 1.5, 2.0, 0.3]))
+        k, near = oracle.fused_argmax_near(a, b, t, beta)
+        if oracle.fused_argmax_fp32(a, b, t, beta) != k:
+            differ += 1
+            assert near
+    # fp32 inputs: the 1e-6 perturbations survive storage and some rows do differ; bf16 storage
+    # rounds them away (every score is then a single-precision number and the two always agree)
+    assert differ >= 1 if dtype == gen.F32 else differ == 0
 
 
 def test_fused_argmax_ties_and_nan():
@@ -145,9 +209,7 @@ def _brute_request(a, b, t, drafts, beta, gamma, dtype):
         if not lhs > rhs:
             n = i
             break
-    af, bf, tf = (gen.widen(x[n], dtype) for x in (a, b, t))
-    s = (np.float64(np.float32(beta)) * (af - bf).astype(np.float32).astype(np.float64)
-         + tf.astype(np.float64)).astype(np.float32)
+    s = _exact_score(a[n], b[n], t[n], beta, dtype)
     tokens = [int(x) for x in drafts[:n]] + [int(np.argmax(s))] + [-1] * (K - n)
     return n, tokens, margins
 
@@ -169,7 +231,7 @@ def test_verify_brute_force_every_draft(dtype):
             drafts[0] = d0
             res = oracle.asymspec_verify(a[None], b[None], t[None], drafts[None], beta, gamma)
             n, tokens, margins = _brute_request(a, b, t, drafts, beta, gamma, dtype)
-            if res.flags[0] & oracle.FLAG_NEAR_MARGIN:
+            if res.flags[0] & (oracle.FLAG_NEAR_MARGIN | oracle.FLAG_NEAR_TIE):
                 flagged += 1
                 continue
             checked += 1
@@ -242,14 +304,12 @@ def test_gate_is_strict():
 @pytest.mark.parametrize("src", [0, 1, 2])
 def test_delta_source_ablation_argmax(src):
     """ASYM sec. 5 ablation: delta := a - b (method), a (raw), t - b (two-model difference);
-    checked against numpy argmax of the fp32 score."""
+    checked against numpy argmax of the exact score."""
     rng = np.random.default_rng(30 + src)
     for dtype in (gen.F32, gen.BF16):
         for beta in (0.0, 1.0, 2.0):
             a, b, t = _rows(rng, 3, 3001, dtype)
-            af, bf, tf = (gen.widen(x, dtype) for x in (a, b, t))
-            d = {0: (af - bf), 1: af, 2: (tf - bf)}[src].astype(np.float32)
-            s = (np.float64(np.float32(beta)) * d.astype(np.float64) + tf.astype(np.float64)).astype(np.float32)
+            s = _exact_score(a, b, t, beta, dtype, src)
             assert oracle.fused_argmax_src(a, b, t, beta, src) == int(np.argmax(s))
     # the default source is the method's a - b
     a, b, t = _rows(rng, 3, 500, gen.F32)
