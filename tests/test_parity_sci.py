@@ -69,18 +69,6 @@ def test_clamps_bind(asv):
     _compare(out, r_new, ref, gen.BF16)
 
 
-def test_five_windows_carry_state(asv):
-    """k = 5 windows with independently seeded tensors, credit state carried on the device."""
-    w = gen.WORKLOADS["sci_asymspec_b1024_k8_v151936_bf16"]
-    B = 32
-    r = np.full(B, w.params["r_hat0"])
-    for win in range(w.params["windows"]):
-        batch = gen.make_asymspec_batch(w.recipe, w.seed + win, B, w.K, w.V, w.dtype, processes=8)
-        out, r_gpu, ref = _window(asv, batch, r)
-        _compare(out, r_gpu, ref, w.dtype)
-        r = ref.r_hat
-
-
 def test_stabilised_windows(asv):
     """Six windows with hysteresis, a refresh interval of 2 and a fallback, state on the device."""
     B, K, V = 24, 4, 4096
