@@ -6,6 +6,14 @@ in HBM.  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+The K timed steps run back to back between two CUDA events on the launching stream; that region
+is repeated (each repetition exactly K steps, bracketed by a barrier and a synchronize) until the
+repetitions together last at least --min-region-s, so the clock sampler sees the kernel under
+load, and the line reports the median repetition.  The `secondary` key carries device-timed
+lines for the other workloads (the 1 x 3 x 32000 fp32 latency case, the 256 x 5 fp32 sweep, RAPID,
+and the 1024 x 9 bf16 batch in AsymSpec, fused AsymSpec + E2-SCI and E2-SCI modes), each timed
+the same way.
+
 N > 1 runs under torchrun, one rank per GPU; requests are independent, so every rank verifies
 its own batch (weak scaling, no collective on the data path).  `--impl reference` times the CPU
 oracle (the double-precision restatement of the pages) on the host cores instead.
@@ -55,10 +63,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def _profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary of the timed kernel, or None when the
-    kernel source has changed since that capture (the summary records a hash of the sources)."""
-    prof = os.path.join(ROOT, "profiles", f"jsd_family_{WORKLOAD}.md")
+def _profiled_traffic(workload: str = WORKLOAD, kernel: str = "jsd_family"):
+    """DRAM bytes per launch from the committed ncu summary of a kernel on a workload, or None when
+    there is none or the kernel source has changed since that capture (the summary records a hash
+    of the sources)."""
+    prof = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         text = open(prof).read()
         h = kernel_source_hash()
@@ -224,6 +233,43 @@ def run_reference(args):
     return 0
 
 
+def _timed_reps(step, steps, min_region_s, stream, dist=None):
+    """Run `steps` calls of `step(i)` back to back between two CUDA events on `stream`, bracketed by a
+    barrier and a synchronize; repeat until the repetitions together last at least `min_region_s`
+    (the count is fixed from one calibration repetition, the largest over ranks, so every rank runs
+    the same number).  Returns the per-repetition device times in ms."""
+    import torch
+
+    from speculative_decoding_logit_gb300.shard import max_over_ranks
+
+    def rep():
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        return e0.elapsed_time(e1)
+
+    first = rep()
+    n = max(1, int(np.ceil(min_region_s * 1e3 / max(first, 1e-3))))
+    n = int(max_over_ranks(n))
+    return [first] + [rep() for _ in range(n - 1)]
+
+
+def _gpu_id(dev):
+    import torch
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        return str(dev.index)
+
+
 def run_ours(args):
     import torch
 
@@ -274,31 +320,17 @@ def run_ours(args):
         step(i)
     torch.cuda.synchronize()
 
-    # The K launches run back to back between two events on the launching stream (no events between
-    # them, which would add their own gaps); the kernel's average launch duration is the timed
-    # region over K, gaps between launches included.
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    try:
-        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        gpu_id = str(dev.index)
-    clocks = ClockSampler(gpu_id)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
+    # Each repetition: the K launches back to back between two events on the launching stream (no
+    # events between them, which would add their own gaps); the kernel's average launch duration is
+    # that region over K, gaps between launches included.
+    clocks = ClockSampler(_gpu_id(dev))
     clocks.start()
     time.sleep(0.3)  # let the sampler start
-    e0.record(stream)
-    for i in range(args.steps):
-        step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
+    reps = _timed_reps(step, args.steps, args.min_region_s, stream, dist)
     clk = clocks.stop()
-    if dist:
-        dist.barrier()
-    elapsed_ms = e0.elapsed_time(e1)
-    launch_ms = elapsed_ms / args.steps
-    elapsed_ms = max_over_ranks(elapsed_ms)
+    rep_ms = float(np.median(reps))
+    elapsed_ms = max_over_ranks(rep_ms)
+    launch_ms = rep_ms / args.steps
     rows_total = R * args.steps * ws
     value = rows_total / (elapsed_ms / 1e3)
 
@@ -341,8 +373,17 @@ def run_ours(args):
     roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "peak_kind": peak_kind,
             "frac_of_8tbs": achieved / 8000.0, "kernel_ms": launch_ms,
-            "kernel_ms_from": "timed region / steps (back-to-back launches, CUDA events on the launching stream)",
+            "kernel_ms_from": "median repetition of K back-to-back launches / K (CUDA events on the launching "
+                              "stream)",
             "algorithmic_bytes_per_launch": in_bytes}
+    secondary = None
+    if ws == 1 and not args.no_secondary:
+        del sets, calls
+        torch.cuda.empty_cache()
+        secondary = {}
+        for name in SECONDARY:
+            secondary[name] = workload_line(name, args, dev, steps=None)
+            torch.cuda.empty_cache()
     cpu = cpu_par = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_oracle(batch)
@@ -355,37 +396,52 @@ def run_ours(args):
                 "config": {"workload": WORKLOAD, "B": w.B, "K": w.K, "V": w.V, "beta": BETA, "gamma": GAMMA,
                            "rows_per_step": R, "parallelism": f"replicas x{ws} (requests sharded, no collective)",
                            "l2": f"{N_SETS} rotating input sets of {in_bytes / 1e6:.0f} MB (> 129 MB L2)",
+                           "timed_reps": len(reps), "rep_ms_min_median_max": [min(reps), rep_ms, max(reps)],
                            "plan": plan},
                 "roofline": roof, "cpu_baseline": cpu, "cpu_baseline_all_cores": cpu_par, "e2e": e2e,
-                "gpu_launches": args.steps, "clocks": clk}
+                "gpu_launches": args.steps * len(reps), "clocks": clk, "secondary": secondary}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
     return 0
 
 
-def run_workload(args):
-    """Device-timed throughput of one of the other workloads (one launch per step, inputs resident
-    in HBM, timed with CUDA events on the launching stream; inputs larger than L2, or rotating
-    copies that together are).  Prints the same JSON line shape (no e2e or CPU leg)."""
+# The other workloads, timed in the same run (device-timed lines under the `secondary` key).
+SECONDARY = ("asymspec_b1_k2_v32000_f32", "asymspec_sweep_b256_k4_v151936_f32", "rapid_b32_g10_v128256_f32",
+             "asymspec_b1024_k8_v151936_bf16", "sci_asymspec_b1024_k8_v151936_bf16", "sci_b1024_k8_v151936_bf16")
+
+# Workload names that are modes of another workload's tensors: (source workload, mode).
+_MODES = {"asymspec_b1024_k8_v151936_bf16": ("sci_asymspec_b1024_k8_v151936_bf16", "asymspec"),
+          "sci_b1024_k8_v151936_bf16": ("sci_asymspec_b1024_k8_v151936_bf16", "sci"),
+          "sci_asymspec_b1024_k8_v151936_bf16": ("sci_asymspec_b1024_k8_v151936_bf16", "fused")}
+
+
+def workload_line(name, args, dev, steps=None):
+    """Device-timed throughput of one workload: launches back to back between two CUDA events on the
+    launching stream, repeated until the region lasts at least --min-region-s; inputs resident in
+    HBM and larger than L2 (or rotating copies that together are).  Returns a dict in the shape of
+    the headline line (no e2e or CPU leg)."""
+    import dataclasses
+
     import torch
 
     import speculative_decoding_logit_gb300 as asv
 
-    w = gen.WORKLOADS[args.workload]
+    src, mode = _MODES.get(name, (name, None))
+    w = gen.WORKLOADS[src]
+    if mode is None:
+        mode = {"asymspec": "asymspec", "rapid": "rapid", "sci": "fused"}[w.mode]
+        if name == "asymspec_sweep_b256_k4_v151936_f32":
+            mode = "sweep"
     if args.requests:
         # A smaller batch of the same workload (profiling captures must stay within a few GB).
-        import dataclasses
         w = dataclasses.replace(w, B=min(w.B, args.requests))
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
-    asv.build()
     todev = lambda x, dt: (torch.from_numpy(np.ascontiguousarray(x)).to(dev) if dt == gen.F32 else
                            torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev))
     R = w.B * (w.K + 1)
     extra = {}
-    per_step = 2 if w.mode == "rapid" else 1  # RAPID: verification launch + draw launch
-    if w.mode == "rapid":
+    per_step = 2 if mode == "rapid" else 1  # RAPID: verification launch + draw launch
+    if mode == "rapid":
         b = gen.make_rapid_batch(w.seed, w.B, w.K, w.V)
         sets = [(todev(b.z, gen.F32), todev(b.q, gen.F32)) for _ in range(3)]
         d = torch.from_numpy(b.drafts).to(dev)
@@ -406,20 +462,25 @@ def run_workload(args):
         a, b_, t = (todev(rep(x), w.dtype) for x in (batch.a, batch.b, batch.t))
         d = torch.from_numpy(rep(batch.drafts)).to(dev)
         s_el = 4 if w.dtype == gen.F32 else 2
-        step_bytes = 3 * R * w.V * s_el
+        n_in = 2 if mode == "sci" else 3
+        step_bytes = n_in * R * w.V * s_el
         nsets = max(1, min(4, int(np.ceil(4 * 129e6 / step_bytes))))
         sets = [(a, b_, t)] + [tuple(x.clone() for x in (a, b_, t)) for _ in range(nsets - 1)]
         dtype = "f32" if w.dtype == gen.F32 else "bf16"
         extra = {"requests_generated": gen_B, "tiled": tile, "sets": nsets}
-        if args.workload == "asymspec_sweep_b256_k4_v151936_f32":
+        if mode == "sweep":
             betas, gammas = [0.0, 1.0, 1.5, 2.0], [0.4, 0.5, 0.7, 1.0]
             call = lambda i: asv.asymspec_verify_sweep(*sets[i % nsets], d, betas, gammas)
-            kernel = "jsd_family_kernel (sweep: 4 betas x 4 gammas)"
+            kernel = "jsd_family_kernel (sweep: 4 betas x 4 gammas from one read)"
             extra["grid_points"] = 16
-        elif args.workload == "sci_asymspec_b1024_k8_v151936_bf16":
+        elif mode == "fused":
             r_hat = torch.full((w.B,), w.params["r_hat0"], dtype=torch.float64, device=dev)
             call = lambda i: asv.asymspec_sci_verify(*sets[i % nsets], d, 1.0, 0.5, r_hat)
-            kernel = "jsd_family_kernel (AsymSpec fused with E2-SCI)"
+            kernel = "jsd_family_kernel (AsymSpec fused with E2-SCI, one read of a, b, t)"
+        elif mode == "sci":
+            r_hat = torch.full((w.B,), w.params["r_hat0"], dtype=torch.float64, device=dev)
+            call = lambda i: asv.sci_verify(sets[i % nsets][0], sets[i % nsets][2], d, r_hat)
+            kernel = "jsd_family_kernel (E2-SCI: draft a, target t)"
         else:
             call = lambda i: asv.asymspec_verify(*sets[i % nsets], d, 1.0, 0.5)
             kernel = "jsd_family_kernel"
@@ -427,38 +488,44 @@ def run_workload(args):
         call(i)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream(dev)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    try:
-        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        gpu_id = "0"
-    clocks = ClockSampler(gpu_id)
+    # enough launches per repetition that a repetition is at least ~2 ms
+    t0 = time.perf_counter()
+    call(0)
     torch.cuda.synchronize()
+    est_ms = (time.perf_counter() - t0) * 1e3
+    n_steps = steps or max(5, int(np.ceil(2.0 / max(est_ms, 1e-3))))
+    clocks = ClockSampler(_gpu_id(dev))
     clocks.start()
     time.sleep(0.3)
-    e0.record(stream)
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        call(i)
-        ev[i][1].record(stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
+    reps = _timed_reps(call, n_steps, args.min_region_s, stream)
     clk = clocks.stop()
-    elapsed_ms = e0.elapsed_time(e1)
-    launch_ms = float(np.mean([x.elapsed_time(y) for x, y in ev]))
+    rep_ms = float(np.median(reps))
+    launch_ms = rep_ms / n_steps
     peaks, peak_kind = _peaks()
     achieved = step_bytes / (launch_ms / 1e3) / 1e9
-    line = {"metric": f"verified logit rows/s ({args.workload})", "value": R * args.steps / (elapsed_ms / 1e3),
-            "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": dtype, "data": "synthetic",
-            "config": dict({"workload": args.workload, "B": w.B, "K": w.K, "V": w.V, "rows_per_step": R,
-                            "kernel": kernel}, **extra),
+    kname = "rapid_kernel" if mode == "rapid" else "jsd_family"
+    return {"metric": f"verified logit rows/s ({name})", "value": R * n_steps / (rep_ms / 1e3),
+            "unit": "rows/s", "n_gpus": 1, "steps": n_steps, "ms_per_step": launch_ms, "higher_is_better": True,
+            "dtype": dtype, "data": "synthetic",
+            "config": dict({"workload": name, "B": w.B, "K": w.K, "V": w.V, "rows_per_step": R, "kernel": kernel,
+                            "timed_reps": len(reps), "rep_ms_min_median_max": [min(reps), rep_ms, max(reps)]},
+                           **extra),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_kind": peak_kind,
-                         "kernel_ms": launch_ms, "algorithmic_bytes_per_launch": step_bytes},
-            "gpu_launches": per_step * args.steps, "clocks": clk}
+                         "frac": achieved / peaks["hbm_gbs"], "frac_of_8tbs": achieved / 8000.0,
+                         "traffic": _profiled_traffic(name, kname), "peak_kind": peak_kind, "kernel_ms": launch_ms,
+                         "algorithmic_bytes_per_launch": step_bytes},
+            "gpu_launches": per_step * n_steps * len(reps), "clocks": clk}
+
+
+def run_workload(args):
+    """One workload's device-timed line alone (the `--workload` flag)."""
+    import torch
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    import speculative_decoding_logit_gb300 as asv
+    asv.build()
+    line = workload_line(args.workload, args, dev, steps=args.steps)
+    line["warmup"] = args.warmup
     print(json.dumps(line), flush=True)
     return 0
 
@@ -466,16 +533,19 @@ def run_workload(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--min-region-s", type=float, default=1.0,
+                    help="repeat the K-step timed region until the repetitions last this long in total")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch from an ncu capture of the current kernel (else null)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the other workloads' lines")
     ap.add_argument("--requests", type=int, default=0,
                     help="with --workload: verify only this many requests (small cases for ncu captures)")
-    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(gen.WORKLOADS),
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(set(gen.WORKLOADS) | set(_MODES)),
                     help="another workload (device-timed line only; the default is the headline workload)")
     args = ap.parse_args()
     if args.warmup < 3:
