@@ -28,10 +28,17 @@
  *    (ASV_REQ_* bits); a flagged request gets accept length 0 and tokens -1.
  *  - Output tokens per request: the accepted drafts, then one token chosen by the
  *    verifier at the first rejection (or at the bonus position), then -1 padding.
- *  - Rows are processed by thread-block clusters that stream them; rows whose
- *    base address is 16-byte aligned (V * element size a multiple of 16 and
- *    16-byte aligned base pointers) are read with 16-byte vector loads, others
- *    with element loads.
+ *  - Two kernels serve the AsymSpec / E2-SCI entry points.  Rows whose base
+ *    address is 16-byte aligned (V * element size a multiple of 16 and 16-byte
+ *    aligned base pointers), given a workspace of asv_workspace_bytes(...), go
+ *    to the staged kernel: one CTA per SM (a cooperative launch, so all of them
+ *    are resident at once), rows cut into units that bulk copies stage in shared
+ *    memory, every input byte read from HBM once, the CTAs of a row exchanging
+ *    partial sums through the workspace.  Other rows, the E2-SCI pre-hit, a
+ *    cluster-size override (asv_set_tuning) or a workspace only as large as the
+ *    cluster kernel needs select the cluster kernel: thread-block clusters that
+ *    stream their rows with 16-byte loads (element loads for unaligned rows).
+ *    Both give the same decisions and tokens.
  *  - `workspace` is device scratch of at least asv_workspace_bytes(...) bytes.
  *    It must be zero-filled before its first use (asv_workspace_init does that);
  *    every call leaves it zero-filled again.  Two calls that may run at the
@@ -75,7 +82,9 @@ typedef enum {
 /* Per-request status bits written by the kernels (never a trap). */
 #define ASV_REQ_NONFINITE 1u /* a row holds NaN or +inf, or is entirely -inf */
 #define ASV_REQ_BAD_DRAFT 2u /* a draft id lies outside [0, V) */
-#define ASV_REQ_TIMEOUT 4u   /* reserved: a bounded wait expired (no current kernel waits on data) */
+#define ASV_REQ_TIMEOUT 4u   /* a bounded wait of the staged kernel expired (its launch keeps every CTA
+                                resident, so this marks a fault, not a load condition): the request's
+                                outputs are unspecified and the workspace must be zero-filled again */
 
 /* Human-readable name of a status code (static string). */
 const char* asv_status_string(asv_status s);
@@ -97,9 +106,13 @@ asv_status asv_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t str
  */
 asv_status asv_set_tuning(int cluster_ctas, int threads_per_cta);
 
-/* The plan the next call with these shapes would use (cluster size, threads, dynamic
- * shared memory bytes, 1 if rows take 16-byte vector loads) and how many of its clusters
- * the device can hold at once (cudaOccupancyMaxActiveClusters).  Any output may be NULL. */
+/* The plan the next call with these shapes would use, and how many of its clusters the device
+ * can hold at once (cudaOccupancyMaxActiveClusters).  Any output may be NULL.
+ * - Cluster kernel: cluster size, threads, dynamic shared memory bytes, bulk_copy = 1 if rows take
+ *   16-byte vector loads (0 element loads), active clusters.
+ * - Staged kernel (AsymSpec, E2-SCI, the sweep and the fused mode on rows whose V * element size is
+ *   a multiple of 16, when no cluster-size override is set): units per row in cluster_ctas, its
+ *   threads, dynamic shared memory bytes, bulk_copy = 2, and its CTAs in max_active_clusters. */
 asv_status asv_query_plan(int mode, int B, int K, int V, int dtype, int* cluster_ctas, int* threads_per_cta,
                           int* smem_bytes, int* bulk_copy, int* max_active_clusters);
 

@@ -4,7 +4,9 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "asv.h"
 #include "asv_internal.h"
@@ -46,6 +48,29 @@ cudaError_t dev_info(DevInfo* out) {
 }
 
 inline size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
+
+// CTAs of the staged kernel that fit the device at once, per (device, kernel instantiation); the
+// first query of an instantiation on a device also raises its shared-memory limit.
+struct StagedKey {
+  int dev, mode, dtype, dsrc, variant;
+  bool operator<(const StagedKey& o) const {
+    return std::tie(dev, mode, dtype, dsrc, variant) < std::tie(o.dev, o.mode, o.dtype, o.dsrc, o.variant);
+  }
+};
+std::map<StagedKey, int> g_staged_grid;
+std::mutex g_staged_mu;
+
+cudaError_t staged_grid_cached(int mode, int dtype, const asv::JsdArgs& a, const asv::StagedPlan& plan, int* grid) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const StagedKey key{dev, mode, dtype, a.delta_source, a.variant};
+  std::lock_guard<std::mutex> lk(g_staged_mu);
+  auto it = g_staged_grid.find(key);
+  if (it == g_staged_grid.end()) it = g_staged_grid.emplace(key, asv::staged_grid(mode, dtype, a, plan)).first;
+  *grid = it->second;
+  return cudaSuccess;
+}
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -180,13 +205,46 @@ static size_t records_end(int mode, int B, int K) {
   return round_up(tickets_bytes(B) + size_t(B) * size_t(K + 1) * record_bytes(mode), 256);
 }
 
-size_t asv_workspace_bytes(int mode, int B, int K, int V, int dtype) {
-  (void)V;
-  (void)dtype;
+// Workspace of the cluster kernels (and of RAPID).
+static size_t cluster_workspace_bytes(int mode, int B, int K) {
   if (B < 0 || K < 0) return 0;
   if (mode == ASV_MODE_SCI) return records_end(mode, B, K) + size_t(B) * 4;
   if (mode == ASV_MODE_RAPID) return records_end(mode, B, K) + size_t(B) * sizeof(asv::RapidJob);
   return tickets_bytes(B) + size_t(B) * size_t(K + 1) * record_bytes(mode);
+}
+
+}  // extern "C"
+
+namespace asv {
+size_t asym_cluster_workspace_bytes(int B, int K) { return cluster_workspace_bytes(ASV_MODE_ASYMSPEC, B, K); }
+}  // namespace asv
+
+extern "C" {
+
+// The staged kernel's plan for a mode, or n_unit = 0 when it does not apply: rows must be whole
+// 16-byte vectors (V * element size a multiple of 16), at most kStagedMaxUnits units per row, and
+// the unit count must fit the launch's index arithmetic.
+constexpr int kStagedMaxUnits = 64;
+static asv::StagedPlan staged_plan_for(int mode, int B, int K, int V, int dtype) {
+  asv::StagedPlan pl{0, 0, 0};
+  if (mode == ASV_MODE_RAPID || !valid_dtype(dtype) || B < 1 || K < 0 || V < 2) return pl;
+  const int eb = elem_size(dtype);
+  if ((size_t(V) * size_t(eb)) % 16 != 0) return pl;
+  const int nt = mode == ASV_MODE_SCI ? 2 : 3;
+  asv::StagedPlan p = asv::staged_plan(V, eb, nt);
+  if (p.n_unit > kStagedMaxUnits) return pl;
+  if ((long long)B * ((long long)K + 1) * p.n_unit > 0x7fffffffLL) return pl;
+  return p;
+}
+
+// The staged kernel's workspace follows the cluster kernels', 256-byte aligned.
+static size_t staged_offset(int mode, int B, int K) { return round_up(cluster_workspace_bytes(mode, B, K), 256); }
+
+size_t asv_workspace_bytes(int mode, int B, int K, int V, int dtype) {
+  if (B < 0 || K < 0) return 0;
+  const asv::StagedPlan sp = staged_plan_for(mode, B, K, V, dtype);
+  if (sp.n_unit == 0) return cluster_workspace_bytes(mode, B, K);
+  return staged_offset(mode, B, K) + asv::staged_workspace_bytes((long long)B * (K + 1), sp.n_unit);
 }
 
 asv_status asv_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t stream) {
@@ -209,6 +267,26 @@ asv_status asv_query_plan(int mode, int B, int K, int V, int dtype, int* cluster
   if (mode == ASV_MODE_RAPID && dtype != ASV_F32) return ASV_ERR_DTYPE;
   const int eb = elem_size(dtype);
   const bool bulk = (size_t(V) * eb) % 16 == 0;
+  // The staged kernel (when a call with 16-byte aligned pointers and a full workspace would take it):
+  // units per row, its threads, dynamic shared memory, 2, and its CTAs (one per SM).
+  const asv::StagedPlan sp = staged_plan_for(mode, B, K, V, dtype);
+  if (sp.n_unit > 0 && g_tune_cluster.load() == 0) {
+    asv::JsdArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.variant = mode == ASV_MODE_SWEEP ? 1 : mode == ASV_MODE_ASYMSPEC_SCI ? 2 : 0;
+    const int kmode = mode == ASV_MODE_SCI ? asv::kModeSci : asv::kModeAsym;
+    int grid = 0;
+    cudaError_t e = staged_grid_cached(kmode, dtype, a, sp, &grid);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (grid >= sp.n_unit) {
+      if (cluster_ctas) *cluster_ctas = sp.n_unit;
+      if (threads_per_cta) *threads_per_cta = asv::staged_threads();
+      if (smem_bytes) *smem_bytes = sp.smem;
+      if (bulk_copy) *bulk_copy = 2;
+      if (max_active_clusters) *max_active_clusters = grid;
+      return ASV_OK;
+    }
+  }
   LaunchPlan pl;
   cudaError_t e = mode == ASV_MODE_RAPID
                       ? plan_rapid(V, (long long)B * (K + 1), bulk, false, &pl)
@@ -233,21 +311,47 @@ static asv_status run_jsd(int mode, asv::JsdArgs& a, int dtype, void* workspace,
   int amode = mode == asv::kModeAsym ? ASV_MODE_ASYMSPEC : ASV_MODE_SCI;
   if (a.variant == 1) amode = ASV_MODE_SWEEP;
   if (a.variant == 2) amode = ASV_MODE_ASYMSPEC_SCI;
-  if (ws_bytes < asv_workspace_bytes(amode, a.B, a.K, a.V, dtype)) return ASV_ERR_WORKSPACE;
+  if (ws_bytes < cluster_workspace_bytes(amode, a.B, a.K)) return ASV_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return ASV_ERR_ALIGN;
   const int eb = elem_size(dtype);
   const int NT = mode == asv::kModeAsym ? 3 : 2;
   bool bulk = (size_t(a.V) * eb) % 16 == 0;
   for (int j = 0; j < NT; ++j) bulk = bulk && aligned(a.x[j], 16);
+  a.tickets = reinterpret_cast<uint32_t*>(workspace);
+  a.records = reinterpret_cast<asv::RowRecord*>(static_cast<char*>(workspace) + tickets_bytes(a.B));
+  a.mrecords = reinterpret_cast<asv::MultiRecord*>(static_cast<char*>(workspace) + tickets_bytes(a.B));
+  // The staged kernel: aligned rows, no pre-hit, no cluster-size override, and a workspace that
+  // holds its exchange area (a smaller one, enough for the cluster kernel, selects that kernel).
+  const asv::StagedPlan sp = staged_plan_for(amode, a.B, a.K, a.V, dtype);
+  if (bulk && sp.n_unit > 0 && a.prehit_phase == 0 && g_tune_cluster.load() == 0 &&
+      ws_bytes >= asv_workspace_bytes(amode, a.B, a.K, a.V, dtype)) {
+    int grid = 0;
+    cudaError_t e = staged_grid_cached(mode, dtype, a, sp, &grid);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (grid >= sp.n_unit) {
+      const long long rows = (long long)a.B * (a.K + 1);
+      char* st = static_cast<char*>(workspace) + staged_offset(amode, a.B, a.K);
+      const size_t cnt = (size_t(rows) * 8 + 255) / 256 * 256;
+      a.n_slice = sp.n;
+      a.n_unit = sp.n_unit;
+      a.units = int(rows * sp.n_unit);
+      a.row_cnt = reinterpret_cast<uint32_t*>(st);
+      a.row_jcnt = a.row_cnt + rows;
+      a.abort_flag = reinterpret_cast<uint32_t*>(st + cnt);
+      a.part_a = st + cnt + 256;
+      a.part_b = reinterpret_cast<float*>(st + cnt + 256 + size_t(a.units) * 128);
+      a.bulk = 2;
+      e = asv::launch_jsd_staged(mode, dtype, a, sp, std::min(grid, a.units), stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+      return ASV_OK;
+    }
+  }
   LaunchPlan pl;
   cudaError_t e = plan_jsd(eb, a.V, (long long)a.B * (a.K + 1), bulk, &pl);
   if (e == cudaErrorInvalidValue) return ASV_ERR_SHAPE;
   if (e != cudaSuccess) return cuda_fail(e);
   a.n_slice = pl.n_slice;
   a.bulk = pl.bulk;
-  a.tickets = reinterpret_cast<uint32_t*>(workspace);
-  a.records = reinterpret_cast<asv::RowRecord*>(static_cast<char*>(workspace) + tickets_bytes(a.B));
-  a.mrecords = reinterpret_cast<asv::MultiRecord*>(static_cast<char*>(workspace) + tickets_bytes(a.B));
   if (mode == asv::kModeSci && a.prehit_phase != 0) {
     // E2-SCI pre-hit: phase 1 over row 0 of every request, phase 2 over rows 1..K of the requests
     // phase 1 kept, then the drop flags are cleared (the workspace is left zeroed).

@@ -119,6 +119,15 @@ struct JsdArgs {
   uint32_t* tickets;
   RowRecord* records;
   MultiRecord* mrecords;  // multi-outcome variants (the same workspace bytes as `records`)
+  // staged kernel: rows cut into `n_unit` units of n_slice entries, each staged in one CTA's shared
+  // memory; the CTAs of a row exchange partial statistics through the workspace
+  int n_unit;            // units per row
+  int units;             // rows * n_unit
+  uint32_t* row_cnt;     // [rows] pass-A partials published
+  uint32_t* row_jcnt;    // [rows] pass-B partials published
+  void* part_a;          // [units] 64-byte pass-A partials
+  float* part_b;         // [units] 16 floats: pass-B sums as (hi, lo) pairs
+  uint32_t* abort_flag;  // set by a CTA whose bounded wait expired
 };
 
 struct RapidArgs {
@@ -139,6 +148,25 @@ struct RapidArgs {
   RapidJob* jobs;
   int draw_ctas;  // CTAs per request of the draw launch
 };
+
+// Staged AsymSpec / E2-SCI kernel (asv_staged.cu): units per row and entries per unit for a row of
+// V entries of `elem_bytes` bytes over `nt` inputs (the unit buffers fill a fixed shared-memory
+// budget), dynamic shared memory of one CTA, threads per CTA, and the launch (cooperative: one CTA
+// per SM, all resident at once).
+struct StagedPlan {
+  int n_unit;    // units per row
+  int n;         // entries per unit (multiple of the 16-byte vector width)
+  int smem;      // dynamic shared memory bytes per CTA
+};
+StagedPlan staged_plan(int V, int elem_bytes, int nt);
+int staged_threads();
+size_t staged_workspace_bytes(long long rows, int n_unit);
+// Workspace bytes of the cluster AsymSpec kernel alone (tickets and row records); a call given
+// no more than this runs the cluster kernel.
+size_t asym_cluster_workspace_bytes(int B, int K);
+cudaError_t launch_jsd_staged(int mode, int dtype, const JsdArgs& args, const StagedPlan& plan, int grid,
+                              cudaStream_t s);
+int staged_grid(int mode, int dtype, const JsdArgs& args, const StagedPlan& plan);  // 0: cannot launch
 
 // Kernel launchers (return the cudaError_t of the launch).
 cudaError_t launch_jsd_family(int mode, int dtype, const JsdArgs& args, const LaunchPlan& plan, cudaStream_t s);

@@ -62,7 +62,10 @@ extern "C" asv_status asymspec_verify_static(const void* a, const void* b, const
   // then the size limit; then the checks asymspec_verify applies to its arguments.
   asv_status st = asv::check_asym_shape(B, K, V, dtype);
   if (st != ASV_OK) return st;
-  const size_t need = asv_workspace_bytes(ASV_MODE_ASYMSPEC, B, K, V, dtype);
+  // The scratch serves the cluster kernel (tickets and row records only): the call passes exactly
+  // that much, which keeps the staged kernel's exchange area, and the counters in it that would
+  // have to start at zero, out of the shared array.
+  const size_t need = asv::asym_cluster_workspace_bytes(B, K);
   if (need > size_t(ASV_STATIC_SCRATCH_BYTES)) return ASV_ERR_WORKSPACE;  // batch too large for the static scratch
   if (B == 0) return ASV_OK;
   st = asv::check_asym_args(a, b, t, dtype, draft_ids, K, beta, gamma, out_accept_len, out_tokens, out_D, out_lse,
@@ -80,5 +83,5 @@ extern "C" asv_status asymspec_verify_static(const void* a, const void* b, const
   e = cudaMemsetAsync(ws, 0, tickets, stream);
   if (e != cudaSuccess) return ASV_ERR_CUDA;
   return asymspec_verify(a, b, t, dtype, draft_ids, B, K, V, beta, gamma, out_accept_len, out_tokens, out_D, out_lse,
-                         out_req_status, ws, size_t(ASV_STATIC_SCRATCH_BYTES), stream);
+                         out_req_status, ws, need, stream);
 }

@@ -36,8 +36,15 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings_and_workspace_sizes(lib):
     for s in range(8):
         assert lib.asv_status_string(s).startswith(b"ASV_")
-    # tickets padded to 256 B + 16-byte row records (AsymSpec/SCI) or 32-byte (RAPID)
-    assert lib.asv_workspace_bytes(0, 64, 2, 151936, 1) == 256 + 64 * 3 * 16
+    # Rows that are not whole 16-byte vectors (V = 1001 bf16) take the cluster kernel: tickets padded
+    # to 256 B + 16-byte row records (AsymSpec/SCI) or 32-byte (RAPID).
+    assert lib.asv_workspace_bytes(0, 64, 2, 1001, 1) == 256 + 64 * 3 * 16
+    # Aligned rows add the staged kernel's exchange area after it: two counters per row (256-byte
+    # padded), the abort flag (256 B) and 128 + 64 bytes of partials per unit; V = 151936 bf16 over
+    # three inputs is 18 units of 8448 entries per row.
+    rows, units = 64 * 3, 64 * 3 * 18
+    assert lib.asv_workspace_bytes(0, 64, 2, 151936, 1) == 3328 + 1536 + 256 + units * 192
+    assert rows * 8 == 1536
     # RAPID: tickets, row records (to a 256-byte boundary), one draw job per request
     assert lib.asv_workspace_bytes(1, 32, 10, 128256, 0) == 256 + 32 * 11 * 32 + 32 * 64
     assert lib.asv_workspace_bytes(0, -1, 2, 10, 0) == 0
