@@ -28,17 +28,17 @@
  *    (ASV_REQ_* bits); a flagged request gets accept length 0 and tokens -1.
  *  - Output tokens per request: the accepted drafts, then one token chosen by the
  *    verifier at the first rejection (or at the bonus position), then -1 padding.
- *  - Two kernels serve the AsymSpec / E2-SCI entry points.  Rows whose base
+ *  - Two kernels serve the AsymSpec / E2-SCI entry points, with the same
+ *    decisions and tokens.  The cluster kernel (the default): thread-block
+ *    clusters that stream their rows with 16-byte loads (element loads for
+ *    unaligned rows).  The staged kernel (asv_set_kernel(ASV_KERNEL_STAGED)):
+ *    one CTA per SM (a cooperative launch, so all of them are resident at once),
+ *    rows cut into units that bulk copies stage in shared memory, the CTAs of a
+ *    row exchanging partial sums through the workspace; it takes rows whose base
  *    address is 16-byte aligned (V * element size a multiple of 16 and 16-byte
- *    aligned base pointers), given a workspace of asv_workspace_bytes(...), go
- *    to the staged kernel: one CTA per SM (a cooperative launch, so all of them
- *    are resident at once), rows cut into units that bulk copies stage in shared
- *    memory, every input byte read from HBM once, the CTAs of a row exchanging
- *    partial sums through the workspace.  Other rows, the E2-SCI pre-hit, a
- *    cluster-size override (asv_set_tuning) or a workspace only as large as the
- *    cluster kernel needs select the cluster kernel: thread-block clusters that
- *    stream their rows with 16-byte loads (element loads for unaligned rows).
- *    Both give the same decisions and tokens.
+ *    aligned base pointers) given a workspace of asv_workspace_bytes(...), and
+ *    leaves the E2-SCI pre-hit, cluster-size overrides (asv_set_tuning) and
+ *    workspaces only as large as the cluster kernel needs to the cluster kernel.
  *  - `workspace` is device scratch of at least asv_workspace_bytes(...) bytes.
  *    It must be zero-filled before its first use (asv_workspace_init does that);
  *    every call leaves it zero-filled again.  Two calls that may run at the
@@ -106,13 +106,22 @@ asv_status asv_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t str
  */
 asv_status asv_set_tuning(int cluster_ctas, int threads_per_cta);
 
+/* Kernel selection for the AsymSpec / E2-SCI entry points, for later calls from any thread:
+ * ASV_KERNEL_DEFAULT and ASV_KERNEL_CLUSTER select the cluster kernel, ASV_KERNEL_STAGED the
+ * staged kernel where it applies (see the conventions above).  Anything else is ASV_ERR_PARAM. */
+#define ASV_KERNEL_DEFAULT 0
+#define ASV_KERNEL_CLUSTER 1
+#define ASV_KERNEL_STAGED 2
+asv_status asv_set_kernel(int which);
+
 /* The plan the next call with these shapes would use, and how many of its clusters the device
  * can hold at once (cudaOccupancyMaxActiveClusters).  Any output may be NULL.
  * - Cluster kernel: cluster size, threads, dynamic shared memory bytes, bulk_copy = 1 if rows take
  *   16-byte vector loads (0 element loads), active clusters.
- * - Staged kernel (AsymSpec, E2-SCI, the sweep and the fused mode on rows whose V * element size is
- *   a multiple of 16, when no cluster-size override is set): units per row in cluster_ctas, its
- *   threads, dynamic shared memory bytes, bulk_copy = 2, and its CTAs in max_active_clusters. */
+ * - Staged kernel (when selected, for AsymSpec, E2-SCI, the sweep and the fused mode on rows whose
+ *   V * element size is a multiple of 16, with no cluster-size override): units per row in
+ *   cluster_ctas, its threads, dynamic shared memory bytes, bulk_copy = 2, and its CTAs in
+ *   max_active_clusters. */
 asv_status asv_query_plan(int mode, int B, int K, int V, int dtype, int* cluster_ctas, int* threads_per_cta,
                           int* smem_bytes, int* bulk_copy, int* max_active_clusters);
 

@@ -56,7 +56,11 @@ from ._binding import (  # noqa: F401
     sci_state_decode,
     sci_state_new,
     sci_verify,
+    set_kernel,
     set_tuning,
+    KERNEL_CLUSTER,
+    KERNEL_DEFAULT,
+    KERNEL_STAGED,
     workspace_bytes,
 )
 from .nvcc_build import build  # noqa: F401

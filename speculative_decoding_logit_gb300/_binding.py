@@ -91,6 +91,8 @@ def _declare(L):
     L.asv_workspace_init.restype = _i
     L.asv_set_tuning.argtypes = [_i, _i]
     L.asv_set_tuning.restype = _i
+    L.asv_set_kernel.argtypes = [_i]
+    L.asv_set_kernel.restype = _i
     L.asv_query_plan.argtypes = [_i, _i, _i, _i, _i] + [C.POINTER(_i)] * 5
     L.asv_query_plan.restype = _i
     L.asymspec_verify.argtypes = [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _f, _f, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
@@ -184,6 +186,17 @@ def workspace_bytes(mode: int, B: int, K: int, V: int, dtype: int) -> int:
 
 def set_tuning(cluster_ctas: int = 0, threads_per_cta: int = 0):
     _check(library().asv_set_tuning(cluster_ctas, threads_per_cta), "asv_set_tuning")
+
+
+KERNEL_DEFAULT = 0
+KERNEL_CLUSTER = 1
+KERNEL_STAGED = 2
+
+
+def set_kernel(which: int):
+    """Kernel for later AsymSpec / E2-SCI calls: KERNEL_DEFAULT / KERNEL_CLUSTER (the cluster
+    kernel) or KERNEL_STAGED (the staged kernel, where it applies)."""
+    _check(library().asv_set_kernel(int(which)), "asv_set_kernel")
 
 
 def query_plan(mode: int, B: int, K: int, V: int, dtype: int) -> dict:

@@ -19,6 +19,7 @@ namespace {
 
 thread_local int g_last_cuda_error = 0;
 std::atomic<int> g_tune_cluster{0};
+std::atomic<int> g_use_staged{0};  // asv_set_kernel: 1 selects the staged kernel where it applies
 
 asv_status cuda_fail(cudaError_t e) {
   g_last_cuda_error = int(e);
@@ -222,17 +223,17 @@ size_t asym_cluster_workspace_bytes(int B, int K) { return cluster_workspace_byt
 extern "C" {
 
 // The staged kernel's plan for a mode, or n_unit = 0 when it does not apply: rows must be whole
-// 16-byte vectors (V * element size a multiple of 16), at most kStagedMaxUnits units per row, and
-// the unit count must fit the launch's index arithmetic.
-constexpr int kStagedMaxUnits = 64;
+// 16-byte vectors (V * element size a multiple of 16), at most staged_max_units() units per row,
+// and the unit count must fit the launch's index arithmetic.
 static asv::StagedPlan staged_plan_for(int mode, int B, int K, int V, int dtype) {
-  asv::StagedPlan pl{0, 0, 0};
+  asv::StagedPlan pl{0, 0, 0, 0};
   if (mode == ASV_MODE_RAPID || !valid_dtype(dtype) || B < 1 || K < 0 || V < 2) return pl;
   const int eb = elem_size(dtype);
   if ((size_t(V) * size_t(eb)) % 16 != 0) return pl;
   const int nt = mode == ASV_MODE_SCI ? 2 : 3;
-  asv::StagedPlan p = asv::staged_plan(V, eb, nt);
-  if (p.n_unit > kStagedMaxUnits) return pl;
+  const int nb = mode == ASV_MODE_ASYMSPEC_SCI ? 3 : 2;
+  asv::StagedPlan p = asv::staged_plan(V, eb, nt, nb);
+  if (p.n_unit > asv::staged_max_units()) return pl;
   if ((long long)B * ((long long)K + 1) * p.n_unit > 0x7fffffffLL) return pl;
   return p;
 }
@@ -240,10 +241,12 @@ static asv::StagedPlan staged_plan_for(int mode, int B, int K, int V, int dtype)
 // The staged kernel's workspace follows the cluster kernels', 256-byte aligned.
 static size_t staged_offset(int mode, int B, int K) { return round_up(cluster_workspace_bytes(mode, B, K), 256); }
 
+// Sized for the kernel the current selection (asv_set_kernel) would use; a call given less than the
+// staged kernel's size runs the cluster kernel.
 size_t asv_workspace_bytes(int mode, int B, int K, int V, int dtype) {
   if (B < 0 || K < 0) return 0;
   const asv::StagedPlan sp = staged_plan_for(mode, B, K, V, dtype);
-  if (sp.n_unit == 0) return cluster_workspace_bytes(mode, B, K);
+  if (sp.n_unit == 0 || g_use_staged.load() != 1) return cluster_workspace_bytes(mode, B, K);
   return staged_offset(mode, B, K) + asv::staged_workspace_bytes((long long)B * (K + 1), sp.n_unit);
 }
 
@@ -260,6 +263,12 @@ asv_status asv_set_tuning(int cluster_ctas, int threads_per_cta) {
   return ASV_OK;
 }
 
+asv_status asv_set_kernel(int which) {
+  if (which < ASV_KERNEL_DEFAULT || which > ASV_KERNEL_STAGED) return ASV_ERR_PARAM;
+  g_use_staged.store(which == ASV_KERNEL_STAGED ? 1 : 0);
+  return ASV_OK;
+}
+
 asv_status asv_query_plan(int mode, int B, int K, int V, int dtype, int* cluster_ctas, int* threads_per_cta,
                           int* smem_bytes, int* bulk_copy, int* max_active_clusters) {
   if (B < 1 || K < 0 || V < 2) return ASV_ERR_SHAPE;
@@ -270,7 +279,7 @@ asv_status asv_query_plan(int mode, int B, int K, int V, int dtype, int* cluster
   // The staged kernel (when a call with 16-byte aligned pointers and a full workspace would take it):
   // units per row, its threads, dynamic shared memory, 2, and its CTAs (one per SM).
   const asv::StagedPlan sp = staged_plan_for(mode, B, K, V, dtype);
-  if (sp.n_unit > 0 && g_tune_cluster.load() == 0) {
+  if (sp.n_unit > 0 && g_tune_cluster.load() == 0 && g_use_staged.load() == 1) {
     asv::JsdArgs a;
     std::memset(&a, 0, sizeof(a));
     a.variant = mode == ASV_MODE_SWEEP ? 1 : mode == ASV_MODE_ASYMSPEC_SCI ? 2 : 0;
@@ -278,7 +287,7 @@ asv_status asv_query_plan(int mode, int B, int K, int V, int dtype, int* cluster
     int grid = 0;
     cudaError_t e = staged_grid_cached(kmode, dtype, a, sp, &grid);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (grid >= sp.n_unit) {
+    if (grid >= 2 * sp.n_unit) {
       if (cluster_ctas) *cluster_ctas = sp.n_unit;
       if (threads_per_cta) *threads_per_cta = asv::staged_threads();
       if (smem_bytes) *smem_bytes = sp.smem;
@@ -323,25 +332,26 @@ static asv_status run_jsd(int mode, asv::JsdArgs& a, int dtype, void* workspace,
   // The staged kernel: aligned rows, no pre-hit, no cluster-size override, and a workspace that
   // holds its exchange area (a smaller one, enough for the cluster kernel, selects that kernel).
   const asv::StagedPlan sp = staged_plan_for(amode, a.B, a.K, a.V, dtype);
-  if (bulk && sp.n_unit > 0 && a.prehit_phase == 0 && g_tune_cluster.load() == 0 &&
+  if (bulk && sp.n_unit > 0 && a.prehit_phase == 0 && g_tune_cluster.load() == 0 && g_use_staged.load() == 1 &&
       ws_bytes >= asv_workspace_bytes(amode, a.B, a.K, a.V, dtype)) {
     int grid = 0;
     cudaError_t e = staged_grid_cached(mode, dtype, a, sp, &grid);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (grid >= sp.n_unit) {
+    if (grid >= 2 * sp.n_unit) {
       const long long rows = (long long)a.B * (a.K + 1);
       char* st = static_cast<char*>(workspace) + staged_offset(amode, a.B, a.K);
       const size_t cnt = (size_t(rows) * 8 + 255) / 256 * 256;
       a.n_slice = sp.n;
       a.n_unit = sp.n_unit;
       a.units = int(rows * sp.n_unit);
+      a.chunk_units = asv::staged_chunk_for(sp, rows, grid);
       a.row_cnt = reinterpret_cast<uint32_t*>(st);
       a.row_jcnt = a.row_cnt + rows;
       a.abort_flag = reinterpret_cast<uint32_t*>(st + cnt);
       a.part_a = st + cnt + 256;
       a.part_b = reinterpret_cast<float*>(st + cnt + 256 + size_t(a.units) * 128);
       a.bulk = 2;
-      e = asv::launch_jsd_staged(mode, dtype, a, sp, std::min(grid, a.units), stream);
+      e = asv::launch_jsd_staged(mode, dtype, a, sp, std::min(grid, a.units / a.chunk_units), stream);
       if (e != cudaSuccess) return cuda_fail(e);
       return ASV_OK;
     }

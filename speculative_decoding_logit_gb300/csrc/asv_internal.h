@@ -123,6 +123,7 @@ struct JsdArgs {
   // memory; the CTAs of a row exchange partial statistics through the workspace
   int n_unit;            // units per row
   int units;             // rows * n_unit
+  int chunk_units;       // consecutive units of a row one CTA takes at a time (divides n_unit)
   uint32_t* row_cnt;     // [rows] pass-A partials published
   uint32_t* row_jcnt;    // [rows] pass-B partials published
   void* part_a;          // [units] 64-byte pass-A partials
@@ -150,15 +151,18 @@ struct RapidArgs {
 };
 
 // Staged AsymSpec / E2-SCI kernel (asv_staged.cu): units per row and entries per unit for a row of
-// V entries of `elem_bytes` bytes over `nt` inputs (the unit buffers fill a fixed shared-memory
-// budget), dynamic shared memory of one CTA, threads per CTA, and the launch (cooperative: one CTA
-// per SM, all resident at once).
+// V entries of `elem_bytes` bytes, `nt` inputs read by pass A and `nb` by pass B (the two rings of
+// unit buffers fill a fixed shared-memory budget), dynamic shared memory of one CTA, threads per
+// CTA, and the launch (cooperative: one CTA per SM, all resident at once).
 struct StagedPlan {
   int n_unit;    // units per row
   int n;         // entries per unit (multiple of the 16-byte vector width)
   int smem;      // dynamic shared memory bytes per CTA
+  int chunk;     // largest number of units per chunk
 };
-StagedPlan staged_plan(int V, int elem_bytes, int nt);
+int staged_chunk_for(const StagedPlan& pl, long long rows, int grid);
+StagedPlan staged_plan(int V, int elem_bytes, int nt, int nb);  // nb: inputs pass B reads
+int staged_max_units();
 int staged_threads();
 size_t staged_workspace_bytes(long long rows, int n_unit);
 // Workspace bytes of the cluster AsymSpec kernel alone (tickets and row records); a call given

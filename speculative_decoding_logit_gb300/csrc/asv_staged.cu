@@ -10,30 +10,36 @@
 //     (JSD(draft || target) against a threshold driven by an EWMA of the acceptance rate).
 //
 // Work decomposition.  A row (request r, position i) is V entries of each input; it is cut into
-// n_unit units of n entries (the last one shorter).  Unit u = row * n_unit + q.  CTA c of a grid of
-// G CTAs (one per SM, launched cooperatively, so all are resident at once) takes the units
-// c, c + G, c + 2G, ... in that order.  Its warps:
-//   producer   one lane copies each unit's slices of the inputs into one of kBuf shared-memory
-//              buffers (cp.async.bulk, completing on the buffer's `full` mbarrier) and refills a
-//              buffer when the compute warps release it (`empty`);
-//   compute    kW warps run pass A of unit s (running maxima, sums of exp against a lazily moved
-//              reference, the verifier argmax) and pass B of unit s - kLag (the per-entry
-//              Jensen-Shannon terms against the row constants), both from shared memory.  After each
-//              pass the warps' partials are combined in warp order and published to the workspace:
-//              pass A with a release increment of the row's counter, pass B with an acq_rel ticket
-//              on the row's second counter;
-//   stats      waits for the row of each unit to have all n_unit pass-A partials, combines them in
-//              unit order into the row constants (log-sum-exps, lse_b - lse_a, the argmax) and
-//              hands them to the compute warps (`rc_ready`);
-//   finaliser  takes the rows whose pass-B ticket this CTA drew last: D from the row's pass-B
-//              sums, the gate, the outputs and the request-level scan (the last row of a request
-//              scans its records), then clears the row's workspace entries.
-// A row's units are consecutive and n_unit <= G, so they fall in at most two consecutive steps of
-// the CTAs' unit sequences.  Pass B of step s waits for the pass-A partials of steps <= s + 1, and
-// every CTA publishes those before it waits for anything another CTA does, so every wait ends while
-// all CTAs are resident.  The waits are bounded all the same: a CTA whose wait expires marks the
-// request ASV_REQ_TIMEOUT, raises the workspace's abort flag (the other CTAs' polls then stop),
-// waits for its own copies in flight and leaves.
+// n_unit units of n entries (the last one shorter), and m consecutive units form a chunk (n_unit =
+// n_chunk * m).  Chunk ch = row * n_chunk + qc.  CTA c of a grid of G CTAs (one per SM, launched
+// cooperatively, so all are resident at once) takes the chunks c, c + G, c + 2G, ... in that order,
+// a unit at a time.  Its warps:
+//   producers    two warps (one lane each) issue cp.async.bulk copies into two rings of shared-memory
+//                buffers: the A ring receives each unit's slices of every input from HBM; the B
+//                ring, refilled as pass B frees it (kLag units behind), receives the divergence
+//                pair's slices again, which L2 still holds;
+//   compute      kW warps run pass A of unit s from the A ring (running maxima, sums of exp against
+//                a lazily moved reference, the verifier argmax) and pass B of unit s - kLag from the
+//                B ring (the per-entry Jensen-Shannon terms against the row constants), carrying
+//                per-thread state across the units of a chunk; at a chunk's last unit each warp
+//                reduces its state and leaves it in a shared-memory slot;
+//   publishers   one warp combines the compute warps' pass-A partials of a chunk in warp order and
+//                publishes them to the workspace with a release increment of the row's counter;
+//                another does the same for pass B;
+//   stats        kStatsN warps (chunk t of this CTA to warp t % kStatsN) wait for the row of a chunk
+//                to have all n_chunk pass-A partials, combine them in chunk order into the row
+//                constants (log-sum-exps, lse_b - lse_a, the argmax) and hand them to the compute
+//                warps;
+//   finaliser    for every row whose last chunk is this CTA's, waits for all n_chunk pass-B
+//                partials, then computes D, the gate, the outputs and the request-level scan (the
+//                last row of a request scans its records), and clears the row's workspace entries.
+// Every hand-over inside a CTA goes through an mbarrier pair (ready / free), so no warp waits for a
+// slower one except for data it needs.  A row's chunks are consecutive and n_chunk <= G / 2, so they
+// fall in at most two consecutive steps of the CTAs' chunk sequences; the row constants of step t
+// need the pass-A partials of steps <= t + 1, which a CTA publishes without waiting for anything
+// another CTA does, so every wait ends while all CTAs are resident.  The waits are bounded all the
+// same: a CTA whose wait expires marks the request ASV_REQ_TIMEOUT, raises the workspace's abort
+// flag (the other CTAs' polls then stop), waits for its own copies in flight and leaves.
 //
 // Numerics are those of the cluster kernel (asv_jsd.cu): inputs widened exactly to fp32, exp2 of
 // fma(x, log2e, -reference) on the special-function unit, compensated fp32 sums across warps and
@@ -45,22 +51,28 @@ namespace {
 
 constexpr int kW = 16;               // compute warps
 constexpr int kWT = kW * 32;         // compute threads
-constexpr int kProducerWarp = kW;    // the other roles' warps
-constexpr int kStatsWarp = kW + 1;
-constexpr int kFinalWarp = kW + 2;
-constexpr int kThreads = (kW + 3) * 32;
-constexpr int kBuf = 4;              // unit buffers
-constexpr int kLag = 2;              // pass B runs kLag units behind pass A
-constexpr int kSlots = 4;            // row-constant slots (>= kLag + 1, a power of 2)
-constexpr int kFq = 4;               // finalisation queue entries
-constexpr int kMaxUnits = 64;        // units per row the staging arrays hold
-constexpr int kBudget = 200 * 1024;  // dynamic shared memory for the unit buffers
+constexpr int kStatsN = 4;           // stats warps (unit s goes to stats warp s % kStatsN)
+constexpr int kProducerWarp = kW;    // the other roles' warps: A-ring producer,
+constexpr int kProducerBWarp = kW + 1;  // B-ring producer,
+constexpr int kPubAWarp = kW + 2;    // publishers,
+constexpr int kPubBWarp = kW + 3;
+constexpr int kStatsWarp0 = kW + 4;  // stats warps and the finaliser
+constexpr int kFinalWarp = kW + 4 + kStatsN;
+constexpr int kThreads = (kW + 5 + kStatsN) * 32;
+constexpr int kRingA = 3;            // A-ring buffers (every input of a unit, from HBM)
+constexpr int kRingB = 2;            // B-ring buffers (the divergence pair of a unit, from L2)
+constexpr int kChunk = 4;            // largest number of units per chunk
+constexpr int kLag = kChunk + 2;     // pass B runs kLag units behind pass A
+constexpr int kSlots = 4;            // chunk slots: partials and row constants (a power of 2)
+constexpr int kMaxUnits = 40;        // chunks per row the staging arrays hold
+constexpr int kBudget = 198 * 1024;  // dynamic shared memory for the two rings
 constexpr int kPartAStride = 32;     // words per pass-A partial in the workspace (128 bytes)
 constexpr int kPartBStride = 16;     // words per pass-B partial (64 bytes)
 constexpr unsigned long long kWaitNs = 1000000000ull;  // a wait is abandoned after 1 s
 
-static_assert(kSlots >= kLag + 1 && (kSlots & (kSlots - 1)) == 0, "row-constant slots");
-static_assert(kBuf >= kLag + 2, "the producer must never wait for a unit whose pass B waits on later units");
+static_assert((kSlots & (kSlots - 1)) == 0 && kSlots >= 2, "chunk slots");
+static_assert(kRingB >= 2, "the producer's B-ring wait must not depend on the compute warps' current unit");
+static_assert(kSlots % kStatsN == 0, "a stats warp reuses only its own row-constant slots");
 static_assert(sizeof(JsdPart) <= 4 * kPartAStride, "pass-A partial slot");
 
 // ------------------------------------------------------------------ mbarriers, bulk copies, time
@@ -95,16 +107,28 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test, but the thread may be suspended for up to `hint_ns` while the phase is incomplete
+// (it resumes when the phase completes), so a waiting warp takes no issue slots from the others.
+__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of parity `parity` to complete; false if `abort` is raised or a second passes.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort) {
   if (mbar_try(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (*abort) return false;
-      if (global_ns() - t0 > kWaitNs) return false;
-    }
+  for (;;) {
+    if (mbar_try_sleep(bar, parity, 20000u)) return true;
+    if (*abort) return false;
+    if (global_ns() - t0 > kWaitNs) return false;
   }
 }
 
@@ -122,10 +146,6 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-__device__ __forceinline__ void named_sync_compute() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kWT) : "memory");
-}
-
 __device__ __forceinline__ uint4 lds128(const void* p) { return *reinterpret_cast<const uint4*>(p); }
 
 __device__ __forceinline__ void st_cg_zero4(void* p) {
@@ -134,28 +154,21 @@ __device__ __forceinline__ void st_cg_zero4(void* p) {
 
 // ------------------------------------------------------------------ shared state
 
-struct FinJob {
-  int32_t row;
-  int32_t stop;
-  int32_t pad[2];
-  JsdRowConsts rc;
-};
-
 struct __align__(16) StagedShared {
-  uint64_t full[kBuf];
-  uint64_t empty[kBuf];
-  uint64_t rc_ready[kSlots];
-  uint64_t fq_full[kFq];
-  uint64_t fq_free[kFq];
+  uint64_t full_a[kRingA], empty_a[kRingA];
+  uint64_t full_b[kRingB], empty_b[kRingB];
+  uint64_t a_ready[kSlots], a_free[kSlots];    // compute -> pass-A publisher
+  uint64_t b_ready[kSlots], b_free[kSlots];    // compute -> pass-B publisher
+  uint64_t rc_ready[kSlots], rc_free[kSlots];  // stats -> compute
   JsdRowConsts rc[kSlots];
-  FinJob fq[kFq];
-  // per-warp partials of the last two units (pass A: maxima, sums, argmax slots; pass B: sums)
-  float wa_m[2][kW][3];
-  float wa_s[2][kW][3];
-  float wa_av[2][kW][kMaxArg];
-  int32_t wa_ai[2][kW][kMaxArg];
-  float wb[2][kW][6];
-  JsdPart from[kMaxUnits];          // stats warp: a row's pass-A partials
+  JsdRowConsts fin_rc;
+  // per-warp partials (pass A: maxima, sums, argmax slots; pass B: sums)
+  float wa_m[kSlots][kW][3];
+  float wa_s[kSlots][kW][3];
+  float wa_av[kSlots][kW][kMaxArg];
+  int32_t wa_ai[kSlots][kW][kMaxArg];
+  float wb[kSlots][kW][6];
+  JsdPart from[kStatsN + 1][kMaxUnits];  // a row's pass-A partials: the stats warps and the finaliser
   float jsd_from[kMaxUnits][12];    // finaliser: a row's pass-B sums
   volatile int abort;
 };
@@ -396,17 +409,74 @@ __device__ void mark_timeout(const JsdArgs& p, const int row, const int lane) {
 
 // ------------------------------------------------------------------ the kernel
 
+// Where unit s of this CTA lies: its chunk (the CTA's chunk counter t, the global chunk id), its
+// position j in the chunk, its row, unit index q in the row, first entry and length.
+struct UnitPos {
+  int t, j, ch, row, qc, q, v0, len;
+};
+
+__device__ __forceinline__ UnitPos unit_pos(int s, int G, int cta, int nch, int m, int n, int V) {
+  UnitPos r;
+  r.t = s / m;
+  r.j = s - r.t * m;
+  const long long ch = (long long)r.t * G + cta;
+  r.row = int(ch / nch);
+  r.qc = int(ch - (long long)r.row * nch);
+  r.ch = r.row * nch + r.qc;
+  r.q = r.qc * m + r.j;
+  r.v0 = r.q * n;
+  r.len = min(n, V - r.v0);
+  return r;
+}
+
+// A row's pass-A partials (one per chunk) from the workspace into `from` (lanes take chunks), then
+// the row constants into `rc` (whole warp).
+template <int MODE, int NA, bool FUSE>
+__device__ __forceinline__ void gather_row(const JsdArgs& p, int row, int nch, int lane, JsdPart* from,
+                                           JsdRowConsts& rc) {
+  for (int q = lane; q < nch; q += 32) {
+    const char* src = static_cast<const char*>(p.part_a) + (size_t(row) * nch + q) * (4 * kPartAStride);
+    float4* dst = reinterpret_cast<float4*>(&from[q]);
+#pragma unroll
+    for (int w4 = 0; w4 < int(sizeof(JsdPart) / 16); ++w4) dst[w4] = ld_cg_f4(src + 16 * w4);
+  }
+  __syncwarp();
+  combine_row<MODE, NA, FUSE>(from, uint32_t(nch), lane, rc);
+  __syncwarp();
+}
+
+// Every lane polls `*cnt` (acquire) until it reaches `target`; false if the workspace's abort flag
+// or this CTA's is raised, or a second passes.
+__device__ __forceinline__ bool poll_count(const uint32_t* cnt, uint32_t target, const JsdArgs& p,
+                                           const volatile int* abort) {
+  const unsigned long long t0 = global_ns();
+  uint32_t nap = 32;
+  for (uint32_t it = 0;; ++it) {
+    const uint32_t c = ld_acquire_gpu(cnt);
+    if (__all_sync(0xffffffffu, c >= target)) return true;
+    if ((it & 7u) == 7u) {
+      const bool stop = *abort || *reinterpret_cast<volatile uint32_t*>(p.abort_flag) != 0u ||
+                        global_ns() - t0 > kWaitNs;
+      if (__any_sync(0xffffffffu, stop)) return false;
+    }
+    __nanosleep(nap);  // back off (up to 1 us) while the other CTAs catch up
+    if (nap < 1024u) nap *= 2u;
+  }
+}
+
 template <typename T, int MODE, int DSRC, int NB, bool FUSE>
 __global__ void __launch_bounds__(kThreads, 1) jsd_staged_kernel(const JsdArgs p) {
   using G = GVec<T>;
   using PA = PassA<T, MODE, DSRC, NB, FUSE>;
   constexpr int NT = JsdTraits<MODE>::NT;
+  constexpr int NBI = FUSE ? 3 : 2;  // inputs pass B reads: the pair (fused: and the target)
   constexpr int VEC = G::kVec;
   constexpr int NP = G::kPairs;
   constexpr int NA = PA::NA;
   constexpr int NS = FUSE ? 6 : 3;   // pass-B sums
   constexpr bool kMulti = (NB > 1) || FUSE;
   static_assert(NA <= kMaxArg, "argmax slots");
+  (void)kMulti;
 
   extern __shared__ __align__(128) unsigned char s_buf[];
   __shared__ StagedShared sh;
@@ -416,22 +486,36 @@ __global__ void __launch_bounds__(kThreads, 1) jsd_staged_kernel(const JsdArgs p
   const int warp = tid >> 5;
   const int G_ = int(gridDim.x);
   const int cta = int(blockIdx.x);
-  const int C = p.n_unit;
+  const int m = p.chunk_units;
+  const int nch = p.n_unit / m;  // chunks per row
   const int n = p.n_slice;
   const int V = p.V;
-  const int my_units = cta < p.units ? (p.units - cta + G_ - 1) / G_ : 0;
+  const int chunks = p.units / m;
+  const int my_chunks = cta < chunks ? (chunks - cta + G_ - 1) / G_ : 0;
+  const int my_units = my_chunks * m;
   const size_t in_bytes = size_t(n) * G::kBytes;  // one input's slice in a buffer
-  auto buf_addr = [&](int b, int j) { return s_buf + (size_t(b) * NT + j) * in_bytes; };
+  unsigned char* ring_a = s_buf;
+  unsigned char* ring_b = s_buf + size_t(kRingA) * NT * in_bytes;
+  auto a_addr = [&](int i, int j) { return ring_a + (size_t(i) * NT + j) * in_bytes; };
+  auto b_addr = [&](int i, int j) { return ring_b + (size_t(i) * NBI + j) * in_bytes; };
+  auto bar = [](uint64_t& b) { return smem_addr(&b); };
 
   if (tid == 0) {
-    for (int b = 0; b < kBuf; ++b) {
-      mbar_init(smem_addr(&sh.full[b]), 1);
-      mbar_init(smem_addr(&sh.empty[b]), kW);
+    for (int i = 0; i < kRingA; ++i) {
+      mbar_init(bar(sh.full_a[i]), 1);
+      mbar_init(bar(sh.empty_a[i]), kW);
     }
-    for (int k = 0; k < kSlots; ++k) mbar_init(smem_addr(&sh.rc_ready[k]), 1);
-    for (int k = 0; k < kFq; ++k) {
-      mbar_init(smem_addr(&sh.fq_full[k]), 1);
-      mbar_init(smem_addr(&sh.fq_free[k]), 1);
+    for (int i = 0; i < kRingB; ++i) {
+      mbar_init(bar(sh.full_b[i]), 1);
+      mbar_init(bar(sh.empty_b[i]), kW);
+    }
+    for (int k = 0; k < kSlots; ++k) {
+      mbar_init(bar(sh.a_ready[k]), kW);
+      mbar_init(bar(sh.a_free[k]), 1);
+      mbar_init(bar(sh.b_ready[k]), kW);
+      mbar_init(bar(sh.b_free[k]), 1);
+      mbar_init(bar(sh.rc_ready[k]), 1);
+      mbar_init(bar(sh.rc_free[k]), kW);
     }
     sh.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -439,80 +523,128 @@ __global__ void __launch_bounds__(kThreads, 1) jsd_staged_kernel(const JsdArgs p
   }
   __syncthreads();
 
-  if (warp == kProducerWarp) {
-    // ---------------------------------------------------------------- producer
+  if (warp == kProducerWarp || warp == kProducerBWarp) {
+    // ---------------------------------------------------------------- producers
+    // A ring: unit y's slices of every input as soon as its buffer is free.  B ring (its own warp,
+    // so that its waits never hold up the A ring): the divergence pair of unit s2 -- pass B of a
+    // unit runs at compute step unit + kLag; the wait for a free B buffer is on pass B of unit
+    // s2 - kRingB, never on a unit the compute warps need before they can free it.
+    const bool ring_a_role = warp == kProducerWarp;
     if (lane == 0) {
+      const int nbuf = ring_a_role ? kRingA : kRingB;
+      const int nin = ring_a_role ? NT : NBI;
+      uint64_t* full = ring_a_role ? sh.full_a : sh.full_b;
+      uint64_t* empty = ring_a_role ? sh.empty_a : sh.empty_b;
       int issued = 0;
-      for (int s = 0; s < my_units; ++s) {
-        const int b = s % kBuf;
-        if (s >= kBuf && !mbar_wait(smem_addr(&sh.empty[b]), uint32_t((s / kBuf) - 1) & 1u, &sh.abort)) {
-          sh.abort = 1;
-          break;
+      for (int y = 0; y < my_units && !sh.abort; ++y) {
+        const int i = y % nbuf;
+        if (y >= nbuf && !mbar_wait(bar(empty[i]), uint32_t(y / nbuf - 1) & 1u, &sh.abort)) break;
+        const UnitPos up = unit_pos(y, G_, cta, nch, m, n, V);
+        const uint32_t bytes = uint32_t(up.len) * G::kBytes;
+        const size_t off = (size_t(up.row) * size_t(V) + size_t(up.v0)) * G::kBytes;
+        mbar_arrive_expect_tx(bar(full[i]), bytes * nin);
+        for (int j = 0; j < nin; ++j) {
+          const int src = ring_a_role ? j : (j < 2 ? j : NT - 1);
+          unsigned char* dst = ring_a_role ? a_addr(i, j) : b_addr(i, j);
+          bulk_copy(smem_addr(dst), static_cast<const char*>(p.x[src]) + off, bytes, bar(full[i]));
         }
-        if (sh.abort) break;
-        const long long u = (long long)s * G_ + cta;
-        const int row = int(u / C);
-        const int v0 = int(u - (long long)row * C) * n;
-        const int len = min(n, V - v0);
-        const uint32_t bytes = uint32_t(len) * G::kBytes;
-        mbar_arrive_expect_tx(smem_addr(&sh.full[b]), bytes * NT);
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          const char* src = static_cast<const char*>(p.x[j]) + (size_t(row) * size_t(V) + size_t(v0)) * G::kBytes;
-          bulk_copy(smem_addr(buf_addr(b, j)), src, bytes, smem_addr(&sh.full[b]));
-        }
-        issued = s + 1;
+        issued = y + 1;
       }
-      // Never leave with copies in flight into this CTA's shared memory: wait for the last copies
-      // of every buffer (earlier ones were consumed before their buffer was refilled).
-      for (int s = max(0, issued - kBuf); s < issued; ++s) {
-        const uint32_t bar = smem_addr(&sh.full[s % kBuf]);
-        const unsigned long long t0 = global_ns();
-        while (!mbar_try(bar, uint32_t(s / kBuf) & 1u) && global_ns() - t0 < kWaitNs) {
+      if (sh.abort) {
+        // Never leave with copies in flight into this CTA's shared memory: wait for the last copies
+        // of every buffer (earlier ones were consumed before their buffer was refilled).
+        for (int y = max(0, issued - nbuf); y < issued; ++y) {
+          const unsigned long long t0 = global_ns();
+          while (!mbar_try(bar(full[y % nbuf]), uint32_t(y / nbuf) & 1u) && global_ns() - t0 < kWaitNs) {
+          }
         }
       }
     }
     return;
   }
 
-  if (warp == kStatsWarp) {
-    // ---------------------------------------------------------------- stats
-    const JsdPart* part_a = static_cast<const JsdPart*>(p.part_a);
-    for (int s = 0; s < my_units; ++s) {
-      const long long u = (long long)s * G_ + cta;
-      const int row = int(u / C);
-      // every lane polls the row's counter with acquire semantics
-      bool ok = true;
-      const unsigned long long t0 = global_ns();
-      for (uint32_t it = 0;; ++it) {
-        const uint32_t c = ld_acquire_gpu(p.row_cnt + row);
-        if (__all_sync(0xffffffffu, c >= uint32_t(C))) break;
-        if ((it & 15u) == 15u) {
-          const bool stop = sh.abort || *reinterpret_cast<volatile uint32_t*>(p.abort_flag) != 0u ||
-                            global_ns() - t0 > kWaitNs;
-          if (__any_sync(0xffffffffu, stop)) {
-            ok = false;
-            break;
-          }
-        }
-        __nanosleep(64);
+  if (warp == kPubAWarp || warp == kPubBWarp) {
+    // ---------------------------------------------------------------- publishers (one chunk a step)
+    const bool is_a = warp == kPubAWarp;
+    for (int t = 0; t < my_chunks; ++t) {
+      const int k = t % kSlots;
+      if (!warp_wait(bar(is_a ? sh.a_ready[k] : sh.b_ready[k]), uint32_t(t / kSlots) & 1u, &sh.abort)) {
+        if (lane == 0) sh.abort = 1;
+        break;
       }
-      const int k = s % kSlots;
-      if (ok) {
-        for (int q = lane; q < C; q += 32) {
-          const char* src = reinterpret_cast<const char*>(part_a) + (size_t(row) * C + q) * (4 * kPartAStride);
-          float4* dst = reinterpret_cast<float4*>(&sh.from[q]);
+      const UnitPos up = unit_pos(t * m, G_, cta, nch, m, n, V);
+      const size_t ch = size_t(up.ch);
+      if (is_a) {
+        // lane j < NT: input j; lane NT + s: argmax slot s -- over the compute warps in order
+        JsdPart* dp = reinterpret_cast<JsdPart*>(static_cast<char*>(p.part_a) + ch * (4 * kPartAStride));
+        if (lane < NT) {
+          const int j = lane;
+          float mw[kW], sw[kW];
 #pragma unroll
-          for (int w4 = 0; w4 < int(sizeof(JsdPart) / 16); ++w4) dst[w4] = ld_cg_f4(src + 16 * w4);
+          for (int w = 0; w < kW; ++w) {
+            mw[w] = sh.wa_m[k][w][j];
+            sw[w] = sh.wa_s[k][w][j];
+          }
+          float Mc = mw[0];
+#pragma unroll
+          for (int w = 1; w < kW; ++w) Mc = fmaxf(Mc, mw[w]);
+          const float Rc = ref_of(Mc);
+          DF dsum{0.0f, 0.0f};
+#pragma unroll
+          for (int w = 0; w < kW; ++w)
+            if (sw[w] != 0.0f) dsum = df_add(dsum, DF{sw[w] * exp2f(ref_of(mw[w]) - Rc), 0.0f});
+          dp->mx[j] = Mc;
+          dp->sum_hi[j] = dsum.hi;
+          dp->sum_lo[j] = dsum.lo;
+        } else if (lane < NT + NA) {
+          const int sl = lane - NT;
+          float v = sh.wa_av[k][0][sl];
+          int i = sh.wa_ai[k][0][sl];
+#pragma unroll
+          for (int w = 1; w < kW; ++w) argmax_merge(v, i, sh.wa_av[k][w][sl], sh.wa_ai[k][w][sl]);
+          dp->argv[sl] = v;
+          dp->argi[sl] = i;
         }
         __syncwarp();
-        combine_row<MODE, NA, FUSE>(sh.from, uint32_t(C), lane, sh.rc[k]);
+        if (lane == 0) {
+          mbar_arrive(bar(sh.a_free[k]));
+          red_add_release_gpu(p.row_cnt + up.row, 1u);
+        }
       } else {
-        mark_timeout(p, row, lane);
+        float* dst = p.part_b + ch * kPartBStride;
+        if (lane < NS) {
+          DF dm{sh.wb[k][0][lane], 0.0f};
+#pragma unroll
+          for (int w = 1; w < kW; ++w) dm = df_add(dm, DF{sh.wb[k][w][lane], 0.0f});
+          dst[2 * lane] = dm.hi;
+          dst[2 * lane + 1] = dm.lo;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(sh.b_free[k]));
+          red_add_release_gpu(p.row_jcnt + up.row, 1u);
+        }
+      }
+    }
+    return;
+  }
+
+  if (warp >= kStatsWarp0 && warp < kStatsWarp0 + kStatsN) {
+    // ---------------------------------------------------------------- stats (chunks t with t % kStatsN == w)
+    const int sw = warp - kStatsWarp0;
+    for (int t = sw; t < my_chunks; t += kStatsN) {
+      const int k = t % kSlots;
+      const UnitPos up = unit_pos(t * m, G_, cta, nch, m, n, V);
+      bool ok = t < kSlots || warp_wait(bar(sh.rc_free[k]), uint32_t(t / kSlots - 1) & 1u, &sh.abort);
+      ok = ok && poll_count(p.row_cnt + up.row, uint32_t(nch), p, &sh.abort);
+      if (ok) {
+        gather_row<MODE, NA, FUSE>(p, up.row, nch, lane, sh.from[sw], sh.rc[k]);
+      } else {
+        mark_timeout(p, up.row, lane);
         if (lane == 0) sh.abort = 1;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&sh.rc_ready[k]));
+      if (lane == 0) mbar_arrive(bar(sh.rc_ready[k]));
       if (!ok) break;
     }
     return;
@@ -520,14 +652,19 @@ __global__ void __launch_bounds__(kThreads, 1) jsd_staged_kernel(const JsdArgs p
 
   if (warp == kFinalWarp) {
     // ---------------------------------------------------------------- finaliser
-    for (uint32_t jf = 0;; ++jf) {
-      const int slot = int(jf % kFq);
-      if (!warp_wait(smem_addr(&sh.fq_full[slot]), (jf / kFq) & 1u, &sh.abort)) break;
-      const FinJob& job = sh.fq[slot];
-      if (job.stop) break;
-      const int row = job.row;
-      for (int q = lane; q < C; q += 32) {
-        const float* src = p.part_b + (size_t(row) * C + q) * kPartBStride;
+    // The rows whose last chunk is this CTA's, in order.
+    for (int t = 0; t < my_chunks; ++t) {
+      const UnitPos up = unit_pos(t * m, G_, cta, nch, m, n, V);
+      if (up.qc != nch - 1) continue;
+      const int row = up.row;
+      if (!poll_count(p.row_jcnt + row, uint32_t(nch), p, &sh.abort)) {
+        mark_timeout(p, row, lane);
+        if (lane == 0) sh.abort = 1;
+        break;
+      }
+      gather_row<MODE, NA, FUSE>(p, row, nch, lane, sh.from[kStatsN], sh.fin_rc);
+      for (int q = lane; q < nch; q += 32) {
+        const float* src = p.part_b + (size_t(row) * nch + q) * kPartBStride;
 #pragma unroll
         for (int w4 = 0; w4 < 3; ++w4) {
           const float4 v = ld_cg_f4(src + 4 * w4);
@@ -545,19 +682,19 @@ __global__ void __launch_bounds__(kThreads, 1) jsd_staged_kernel(const JsdArgs p
       float xd = 0.0f;
       if (!kMulti && (lane == 1 || lane == 2) && pos < p.K) {
         d = p.draft_ids[size_t(req) * p.K + pos];
-        if (MODE == kModeAsym && job.rc.finite && d >= 0 && d < V)
+        if (MODE == kModeAsym && sh.fin_rc.finite && d >= 0 && d < V)
           xd = G::at(p.x[lane == 1 ? NT - 1 : 1], size_t(row) * size_t(V) + size_t(d));
       }
       __syncwarp();
-      jsd_finalize_row<T, MODE, NB, FUSE>(p, row, job.rc, sh.jsd_from, uint32_t(C), lane, d, xd);
+      jsd_finalize_row<T, MODE, NB, FUSE>(p, row, sh.fin_rc, sh.jsd_from, uint32_t(nch), lane, d, xd);
       __syncwarp();
-      // The row's workspace entries back to zero (every unit of the row has read its pass-A
-      // partials before its pass-B ticket, so nobody reads them any more).
-      for (int q = lane; q < C; q += 32) {
-        char* a = reinterpret_cast<char*>(p.part_a) + (size_t(row) * C + q) * (4 * kPartAStride);
+      // The row's workspace entries back to zero (every chunk of the row read its pass-A partials
+      // before its pass B, so nobody reads them any more).
+      for (int q = lane; q < nch; q += 32) {
+        char* a = static_cast<char*>(p.part_a) + (size_t(row) * nch + q) * (4 * kPartAStride);
 #pragma unroll
         for (int w4 = 0; w4 < int(sizeof(JsdPart) / 16); ++w4) st_cg_zero4(a + 16 * w4);
-        float* bsum = p.part_b + (size_t(row) * C + q) * kPartBStride;
+        float* bsum = p.part_b + (size_t(row) * nch + q) * kPartBStride;
 #pragma unroll
         for (int w4 = 0; w4 < 3; ++w4) st_cg_zero4(bsum + 4 * w4);
       }
@@ -566,7 +703,6 @@ __global__ void __launch_bounds__(kThreads, 1) jsd_staged_kernel(const JsdArgs p
         p.row_jcnt[row] = 0u;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&sh.fq_free[slot]));
     }
     return;
   }
@@ -576,163 +712,93 @@ __global__ void __launch_bounds__(kThreads, 1) jsd_staged_kernel(const JsdArgs p
 #pragma unroll
   for (int sl = 0; sl < NB; ++sl) beta2[sl] = make_float2(p.betas[sl], p.betas[sl]);
   constexpr bool kPairShort = MODE == kModeAsym;
-  uint32_t jq = 0;  // finalisation jobs queued (warp 0, lane 0)
-
-  // Queue a job for the finaliser (warp 0): the row and its constants, or the stop mark.
-  auto enqueue = [&](int row, bool stop, const JsdRowConsts* rc) {
-    const int slot = int(jq % kFq);
-    bool ok = true;
-    if (lane == 0 && jq >= uint32_t(kFq))
-      ok = mbar_wait(smem_addr(&sh.fq_free[slot]), ((jq / kFq) - 1) & 1u, &sh.abort);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (!ok) {
-      if (lane == 0) sh.abort = 1;
-      return false;
-    }
-    FinJob& job = sh.fq[slot];
-    if (rc) {
-      constexpr int kWords = int(sizeof(JsdRowConsts) / 4);
-      static_assert(kWords <= 32, "row constants");
-      if (lane < kWords) reinterpret_cast<uint32_t*>(&job.rc)[lane] = reinterpret_cast<const uint32_t*>(rc)[lane];
-    }
-    if (lane == 0) {
-      job.row = row;
-      job.stop = stop ? 1 : 0;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&sh.fq_full[slot]));
-    ++jq;
-    return true;
-  };
-
-  // Every compute warp runs the same sequence of named barriers, so a warp that gives up a wait
-  // (`dead`) keeps going through the loop without touching data until the end.
-  bool dead = false;
-  for (int s = 0; s < my_units + kLag; ++s) {
-    if (s < my_units) {
-      // ---------------------------------------------------------------- pass A of unit s
-      const int b = s % kBuf;
-      if (!dead && !warp_wait(smem_addr(&sh.full[b]), uint32_t(s / kBuf) & 1u, &sh.abort)) {
-        sh.abort = 1;
-        dead = true;
-      }
-      const long long u = (long long)s * G_ + cta;
-      const int row = int(u / C);
-      const int v0 = int(u - (long long)row * C) * n;
-      const int len = min(n, V - v0);
-      const int nvec = dead ? 0 : len / VEC;
-      PA st;
-      st.reset();
+  PA st;                   // pass-A state of the current chunk
+  RowB rb, rbt;            // pass-B row constants of the chunk pass B is in
+  bool finite_b = false;
+  float2 accn = make_float2(0.0f, 0.0f), accn2 = make_float2(0.0f, 0.0f);
+  float an = 0.0f, ap = 0.0f, aq = 0.0f, an2 = 0.0f, ap2 = 0.0f, aq2 = 0.0f;
+  for (int x = 0; x < my_units + kLag; ++x) {
+    if (x < my_units) {
+      // ---------------------------------------------------------------- pass A of unit x
+      const int i = x % kRingA;
+      const UnitPos up = unit_pos(x, G_, cta, nch, m, n, V);
+      if (up.j == 0) st.reset();
+      if (!warp_wait(bar(sh.full_a[i]), uint32_t(x / kRingA) & 1u, &sh.abort)) break;
+      const int nvec = up.len / VEC;
       const char* bin[NT];
 #pragma unroll
-      for (int j = 0; j < NT; ++j) bin[j] = reinterpret_cast<const char*>(buf_addr(b, j));
-      {
-        int vi = tid;
-        uint4 cur[NT], nxt[NT];
-        if (vi < nvec) {
+      for (int j = 0; j < NT; ++j) bin[j] = reinterpret_cast<const char*>(a_addr(i, j));
+      for (int vi = tid; vi < nvec; vi += kWT) {
+        uint4 cur[NT];
 #pragma unroll
-          for (int j = 0; j < NT; ++j) cur[j] = lds128(bin[j] + size_t(vi) * 16);
-        }
-        for (; vi < nvec; vi += kWT) {
-          const int vn = vi + kWT;
-          if (vn < nvec) {
-#pragma unroll
-            for (int j = 0; j < NT; ++j) nxt[j] = lds128(bin[j] + size_t(vn) * 16);
-          }
-          st.body(cur, v0 + vi * VEC, beta2);
-#pragma unroll
-          for (int j = 0; j < NT; ++j) cur[j] = nxt[j];
-        }
+        for (int j = 0; j < NT; ++j) cur[j] = lds128(bin[j] + size_t(vi) * 16);
+        st.body(cur, up.v0 + vi * VEC, beta2);
       }
-      // warp partials: maxima, argmax slots, sums against the warp maximum
-      const int ws = s & 1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(sh.empty_a[i]));
+      if (up.j == m - 1) {
+        // chunk done: warp partials (maxima, argmax slots, sums against the warp maximum)
+        const int k = up.t % kSlots;
+        float wm[NT], wsum[NT];
 #pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        const float wm = warp_max(st.rmax[j].value());
-        const float sm = st.acc[j].x + st.acc[j].y;
-        const float moved = (sm != 0.0f) ? sm * exp2f(st.mL[j] - ref_of(wm)) : 0.0f;
-        const float wsum = warp_sumf(moved);
+        for (int j = 0; j < NT; ++j) {
+          wm[j] = warp_max(st.rmax[j].value());
+          const float sm = st.acc[j].x + st.acc[j].y;
+          const float moved = (sm != 0.0f) ? sm * exp2f(st.mL[j] - ref_of(wm[j])) : 0.0f;
+          wsum[j] = warp_sumf(moved);
+        }
+#pragma unroll
+        for (int sl = 0; sl < NA; ++sl) warp_argmax(st.bv[sl], st.bi[sl]);
+        if (up.t >= kSlots && !warp_wait(bar(sh.a_free[k]), uint32_t(up.t / kSlots - 1) & 1u, &sh.abort)) break;
         if (lane == 0) {
-          sh.wa_m[ws][warp][j] = wm;
-          sh.wa_s[ws][warp][j] = wsum;
-        }
-      }
 #pragma unroll
-      for (int sl = 0; sl < NA; ++sl) {
-        warp_argmax(st.bv[sl], st.bi[sl]);
-        if (lane == 0) {
-          sh.wa_av[ws][warp][sl] = st.bv[sl];
-          sh.wa_ai[ws][warp][sl] = st.bi[sl];
-        }
-      }
-      named_sync_compute();
-      if (warp == 0 && __all_sync(0xffffffffu, !dead && sh.abort == 0)) {
-        // the unit's partial: lane j < NT input j, lane NT + s argmax slot s, over the warps in order
-        char* dst = reinterpret_cast<char*>(p.part_a) + size_t(u) * (4 * kPartAStride);
-        JsdPart* dp = reinterpret_cast<JsdPart*>(dst);
-        if (lane < NT) {
-          const int j = lane;
-          float Mc = sh.wa_m[ws][0][j];
-#pragma unroll
-          for (int w = 1; w < kW; ++w) Mc = fmaxf(Mc, sh.wa_m[ws][w][j]);
-          const float Rc = ref_of(Mc);
-          DF dsum{0.0f, 0.0f};
-#pragma unroll
-          for (int w = 0; w < kW; ++w) {
-            const float sw = sh.wa_s[ws][w][j];
-            if (sw != 0.0f) dsum = df_add(dsum, DF{sw * exp2f(ref_of(sh.wa_m[ws][w][j]) - Rc), 0.0f});
+          for (int j = 0; j < NT; ++j) {
+            sh.wa_m[k][warp][j] = wm[j];
+            sh.wa_s[k][warp][j] = wsum[j];
           }
-          dp->mx[j] = Mc;
-          dp->sum_hi[j] = dsum.hi;
-          dp->sum_lo[j] = dsum.lo;
-        } else if (lane < NT + NA) {
-          const int sl = lane - NT;
-          float v = sh.wa_av[ws][0][sl];
-          int i = sh.wa_ai[ws][0][sl];
 #pragma unroll
-          for (int w = 1; w < kW; ++w) argmax_merge(v, i, sh.wa_av[ws][w][sl], sh.wa_ai[ws][w][sl]);
-          dp->argv[sl] = v;
-          dp->argi[sl] = i;
+          for (int sl = 0; sl < NA; ++sl) {
+            sh.wa_av[k][warp][sl] = st.bv[sl];
+            sh.wa_ai[k][warp][sl] = st.bi[sl];
+          }
+          mbar_arrive(bar(sh.a_ready[k]));
         }
-        __syncwarp();
-        if (lane == 0) red_add_release_gpu(p.row_cnt + row, 1u);
       }
     }
-    if (s >= kLag) {
-      // ---------------------------------------------------------------- pass B of unit s - kLag
-      const int s2 = s - kLag;
-      const int b2 = s2 % kBuf;
-      const int k = s2 % kSlots;
-      if (!dead && (!warp_wait(smem_addr(&sh.rc_ready[k]), uint32_t(s2 / kSlots) & 1u, &sh.abort) ||
-                    __any_sync(0xffffffffu, sh.abort != 0))) {
-        sh.abort = 1;
-        dead = true;
+    const int s2 = x - kLag;
+    if (s2 >= 0) {
+      // ---------------------------------------------------------------- pass B of unit s2
+      const int i = s2 % kRingB;
+      const UnitPos up = unit_pos(s2, G_, cta, nch, m, n, V);
+      const int k = up.t % kSlots;
+      if (up.j == 0) {
+        // a new chunk: its row constants into registers, the accumulators to zero
+        if (!warp_wait(bar(sh.rc_ready[k]), uint32_t(up.t / kSlots) & 1u, &sh.abort)) break;
+        if (sh.abort) break;
+        const JsdRowConsts& rc = sh.rc[k];
+        finite_b = rc.finite != 0;
+        rb.dL = rc.dL;
+        rb.MaL = rc.ML[0];
+        rb.MbL = rc.ML[1];
+        rb.hML = rc.hML;
+        rbt = rb;
+        if constexpr (FUSE) {
+          rbt.dL = rc.dL2;
+          rbt.MbL = rc.ML[2];
+          rbt.hML = rc.hML2;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(sh.rc_free[k]));
+        accn = accn2 = make_float2(0.0f, 0.0f);
+        an = ap = aq = an2 = ap2 = aq2 = 0.0f;
       }
-      const long long u2 = (long long)s2 * G_ + cta;
-      const int row2 = int(u2 / C);
-      const int v02 = int(u2 - (long long)row2 * C) * n;
-      const int len2 = min(n, V - v02);
-      const int nvec2 = len2 / VEC;
-      const JsdRowConsts& rc = sh.rc[k];
-      const bool finite = !dead && rc.finite != 0;
-      RowB rb, rbt;
-      rb.dL = rc.dL;
-      rb.MaL = rc.ML[0];
-      rb.MbL = rc.ML[1];
-      rb.hML = rc.hML;
-      rbt = rb;
-      if constexpr (FUSE) {
-        rbt.dL = rc.dL2;
-        rbt.MbL = rc.ML[2];
-        rbt.hML = rc.hML2;
-      }
-      float2 accn = make_float2(0.0f, 0.0f), accn2 = make_float2(0.0f, 0.0f);
-      float an = 0.0f, ap = 0.0f, aq = 0.0f, an2 = 0.0f, ap2 = 0.0f, aq2 = 0.0f;
-      if (finite) {
-        const char* ba = reinterpret_cast<const char*>(buf_addr(b2, 0));
-        const char* bb = reinterpret_cast<const char*>(buf_addr(b2, 1));
-        const char* bt = reinterpret_cast<const char*>(buf_addr(b2, NT - 1));
-        for (int vi = tid; vi < nvec2; vi += kWT) {
+      if (!warp_wait(bar(sh.full_b[i]), uint32_t(s2 / kRingB) & 1u, &sh.abort)) break;
+      const int nvec = up.len / VEC;
+      if (finite_b) {
+        const char* ba = reinterpret_cast<const char*>(b_addr(i, 0));
+        const char* bb = reinterpret_cast<const char*>(b_addr(i, 1));
+        const char* bt = reinterpret_cast<const char*>(b_addr(i, NBI - 1));
+        for (int vi = tid; vi < nvec; vi += kWT) {
           float2 xa[NP], xb[NP];
           G::pairs(lds128(ba + size_t(vi) * 16), xa);
           G::pairs(lds128(bb + size_t(vi) * 16), xb);
@@ -744,51 +810,27 @@ __global__ void __launch_bounds__(kThreads, 1) jsd_staged_kernel(const JsdArgs p
           }
         }
       }
-      // the buffer is free once every lane of every compute warp has read it
       __syncwarp();
-      if (lane == 0 && !dead) mbar_arrive(smem_addr(&sh.empty[b2]));
-      const int wsb = s2 & 1;
-      {
-        const float wn = warp_sumf((accn.x + accn.y) + an);
-        const float wp = warp_sumf(ap);
-        const float wq = warp_sumf(aq);
-        if (lane == 0) {
-          sh.wb[wsb][warp][0] = wn;
-          sh.wb[wsb][warp][1] = wp;
-          sh.wb[wsb][warp][2] = wq;
-        }
+      if (lane == 0) mbar_arrive(bar(sh.empty_b[i]));
+      if (up.j == m - 1) {
+        float sums[6];
+        sums[0] = warp_sumf((accn.x + accn.y) + an);
+        sums[1] = warp_sumf(ap);
+        sums[2] = warp_sumf(aq);
         if constexpr (FUSE) {
-          const float wn2 = warp_sumf((accn2.x + accn2.y) + an2);
-          const float wp2 = warp_sumf(ap2);
-          const float wq2 = warp_sumf(aq2);
-          if (lane == 0) {
-            sh.wb[wsb][warp][3] = wn2;
-            sh.wb[wsb][warp][4] = wp2;
-            sh.wb[wsb][warp][5] = wq2;
-          }
+          sums[3] = warp_sumf((accn2.x + accn2.y) + an2);
+          sums[4] = warp_sumf(ap2);
+          sums[5] = warp_sumf(aq2);
         }
-      }
-      named_sync_compute();
-      if (warp == 0 && __all_sync(0xffffffffu, !dead && sh.abort == 0)) {
-        float* dst = p.part_b + size_t(u2) * kPartBStride;
-        if (lane < NS) {
-          DF dm{sh.wb[wsb][0][lane], 0.0f};
+        if (up.t >= kSlots && !warp_wait(bar(sh.b_free[k]), uint32_t(up.t / kSlots - 1) & 1u, &sh.abort)) break;
+        if (lane == 0) {
 #pragma unroll
-          for (int w = 1; w < kW; ++w) dm = df_add(dm, DF{sh.wb[wsb][w][lane], 0.0f});
-          dst[2 * lane] = dm.hi;
-          dst[2 * lane + 1] = dm.lo;
+          for (int mm = 0; mm < NS; ++mm) sh.wb[k][warp][mm] = sums[mm];
+          mbar_arrive(bar(sh.b_ready[k]));
         }
-        __syncwarp();
-        uint32_t ticket = 0;
-        if (lane == 0) ticket = atom_add_acq_rel_gpu(p.row_jcnt + row2, 1u);
-        ticket = __shfl_sync(0xffffffffu, ticket, 0);
-        // The unit that completes the row hands it to this CTA's finaliser.
-        if (ticket == uint32_t(C - 1) && !enqueue(row2, false, &rc)) dead = true;
       }
     }
   }
-  if (warp == 0) enqueue(0, true, nullptr);
-  (void)kMulti;
 }
 
 using StagedKernel = void (*)(const JsdArgs);
@@ -810,18 +852,35 @@ StagedKernel pick(int mode, int dtype, int dsrc, int variant) {
 
 }  // namespace
 
-StagedPlan staged_plan(int V, int elem_bytes, int nt) {
+StagedPlan staged_plan(int V, int elem_bytes, int nt, int nb) {
   const int vec = 16 / elem_bytes;
-  int n_max = kBudget / (kBuf * nt * elem_bytes);
+  int n_max = kBudget / ((kRingA * nt + kRingB * nb) * elem_bytes);
   n_max -= n_max % vec;
   StagedPlan pl;
   pl.n_unit = (V + n_max - 1) / n_max;
+  pl.chunk = pl.n_unit < kChunk ? pl.n_unit : kChunk;
   int n = (V + pl.n_unit - 1) / pl.n_unit;
   n = (n + vec - 1) / vec * vec;
   pl.n = n;
-  pl.smem = kBuf * nt * n * elem_bytes;
+  pl.smem = (kRingA * nt + kRingB * nb) * n * elem_bytes;
   return pl;
 }
+
+// Units per chunk for a batch of `rows` rows on `grid` CTAs: the largest m <= kChunk dividing the
+// row's units such that the busiest CTA does at most 5 % more units than the average (chunks are
+// the unit of work a CTA takes, so large chunks of few rows leave CTAs idle at the end).
+int staged_chunk_for(const StagedPlan& pl, long long rows, int grid) {
+  const double avg = double(rows) * pl.n_unit / grid;
+  for (int m = pl.chunk; m > 1; --m) {
+    if (pl.n_unit % m) continue;
+    const long long chunks = rows * (pl.n_unit / m);
+    const long long busiest = (chunks + grid - 1) / grid * m;
+    if (double(busiest) <= 1.05 * avg + 1e-9 || busiest <= m) return m;
+  }
+  return 1;
+}
+
+int staged_max_units() { return kMaxUnits; }
 
 int staged_threads() { return kThreads; }
 

@@ -39,12 +39,17 @@ def test_status_strings_and_workspace_sizes(lib):
     # Rows that are not whole 16-byte vectors (V = 1001 bf16) take the cluster kernel: tickets padded
     # to 256 B + 16-byte row records (AsymSpec/SCI) or 32-byte (RAPID).
     assert lib.asv_workspace_bytes(0, 64, 2, 1001, 1) == 256 + 64 * 3 * 16
-    # Aligned rows add the staged kernel's exchange area after it: two counters per row (256-byte
-    # padded), the abort flag (256 B) and 128 + 64 bytes of partials per unit; V = 151936 bf16 over
-    # three inputs is 18 units of 8448 entries per row.
-    rows, units = 64 * 3, 64 * 3 * 18
-    assert lib.asv_workspace_bytes(0, 64, 2, 151936, 1) == 3328 + 1536 + 256 + units * 192
-    assert rows * 8 == 1536
+    # With the staged kernel selected, aligned rows add its exchange area: two counters per row
+    # (256-byte padded), the abort flag (256 B) and 128 + 64 bytes of partials per unit; V = 151936
+    # bf16 (three inputs in pass A, two in pass B) is 20 units of 7600 entries per row.
+    assert lib.asv_workspace_bytes(0, 64, 2, 151936, 1) == 256 + 64 * 3 * 16   # cluster kernel (default)
+    rows, units = 64 * 3, 64 * 3 * 20
+    assert lib.asv_set_kernel(2) == 0
+    try:
+        assert lib.asv_workspace_bytes(0, 64, 2, 151936, 1) == 3328 + 1536 + 256 + units * 192
+        assert rows * 8 == 1536
+    finally:
+        lib.asv_set_kernel(0)
     # RAPID: tickets, row records (to a 256-byte boundary), one draw job per request
     assert lib.asv_workspace_bytes(1, 32, 10, 128256, 0) == 256 + 32 * 11 * 32 + 32 * 64
     assert lib.asv_workspace_bytes(0, -1, 2, 10, 0) == 0
@@ -113,6 +118,13 @@ def test_workspace_checks_with_real_buffers(lib):
     assert call(ws.data_ptr(), need) == 0
     torch.cuda.synchronize()
     assert int(torch.count_nonzero(ws)) == 0
+
+
+def test_kernel_selection_validation(lib):
+    assert lib.asv_set_kernel(3) == 5
+    assert lib.asv_set_kernel(-1) == 5
+    for k in (2, 1, 0):
+        assert lib.asv_set_kernel(k) == 0
 
 
 def test_tuning_override_validation(lib):

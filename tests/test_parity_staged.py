@@ -1,6 +1,6 @@
-"""GPU parity of the staged kernel (one CTA per SM, rows cut into units staged in shared memory,
-partials exchanged through the workspace) against the oracle and against the cluster kernel on
-the same inputs ("AsymSpec: Context-Asymmetric Speculative Decoding for Agentic LLMs", sec. 4.1-4.2
+"""GPU parity of the staged kernel (selected with set_kernel(KERNEL_STAGED): one CTA per SM, rows
+cut into units staged in shared memory, partials exchanged through the workspace) against the
+oracle and against the cluster kernel on the same inputs ("AsymSpec: Context-Asymmetric Speculative Decoding for Agentic LLMs", sec. 4.1-4.2
 and 5; "E2-SCI: Elastic Edge-Cloud Speculative Decoding via Credit Inertia", Key design 3).  The
 shapes cut rows into several units with a short last unit, and batches whose rows straddle two
 steps of the CTAs' unit sequences."""
@@ -19,7 +19,9 @@ pytestmark = pytest.mark.gpu
 def asv():
     import speculative_decoding_logit_gb300 as m
     m.build()
-    return m
+    m.set_kernel(m.KERNEL_STAGED)
+    yield m
+    m.set_kernel(m.KERNEL_DEFAULT)
 
 
 def _dev(batch):
@@ -28,16 +30,16 @@ def _dev(batch):
 
 
 class cluster_kernel:
-    """Selects the cluster kernel for the calls inside (a cluster-size override)."""
+    """Selects the cluster kernel for the calls inside."""
 
-    def __init__(self, asv, c=3):
-        self.asv, self.c = asv, c
+    def __init__(self, asv):
+        self.asv = asv
 
     def __enter__(self):
-        self.asv.set_tuning(self.c)
+        self.asv.set_kernel(self.asv.KERNEL_CLUSTER)
 
     def __exit__(self, *exc):
-        self.asv.set_tuning(0)
+        self.asv.set_kernel(self.asv.KERNEL_STAGED)
 
 
 @pytest.mark.parametrize("dtype,B,K,V", [(gen.BF16, 11, 2, 151936), (gen.F32, 7, 4, 151936), (gen.F32, 1, 2, 32000),
