@@ -206,6 +206,18 @@ static size_t records_end(int mode, int B, int K) {
   return round_up(tickets_bytes(B) + size_t(B) * size_t(K + 1) * record_bytes(mode), 256);
 }
 
+// A workspace region followed by the checked build's check log (256-byte aligned); the ordinary
+// build has no log and uses the region's exact size.
+static size_t with_log(size_t bytes) {
+  return asv::kCheckLogBytes ? round_up(bytes, 256) + asv::kCheckLogBytes : bytes;
+}
+
+// The check log of a call whose workspace region (without the log) is `region` bytes.
+static uint32_t* check_log_at(void* workspace, size_t region) {
+  if (!asv::kCheckLogBytes) return nullptr;
+  return reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + round_up(region, 256));
+}
+
 // Workspace of the cluster kernels (and of RAPID).
 static size_t cluster_workspace_bytes(int mode, int B, int K) {
   if (B < 0 || K < 0) return 0;
@@ -217,7 +229,7 @@ static size_t cluster_workspace_bytes(int mode, int B, int K) {
 }  // extern "C"
 
 namespace asv {
-size_t asym_cluster_workspace_bytes(int B, int K) { return cluster_workspace_bytes(ASV_MODE_ASYMSPEC, B, K); }
+size_t asym_cluster_workspace_bytes(int B, int K) { return with_log(cluster_workspace_bytes(ASV_MODE_ASYMSPEC, B, K)); }
 }  // namespace asv
 
 extern "C" {
@@ -246,8 +258,8 @@ static size_t staged_offset(int mode, int B, int K) { return round_up(cluster_wo
 size_t asv_workspace_bytes(int mode, int B, int K, int V, int dtype) {
   if (B < 0 || K < 0) return 0;
   const asv::StagedPlan sp = staged_plan_for(mode, B, K, V, dtype);
-  if (sp.n_unit == 0 || g_use_staged.load() != 1) return cluster_workspace_bytes(mode, B, K);
-  return staged_offset(mode, B, K) + asv::staged_workspace_bytes((long long)B * (K + 1), sp.n_unit);
+  if (sp.n_unit == 0 || g_use_staged.load() != 1) return with_log(cluster_workspace_bytes(mode, B, K));
+  return with_log(staged_offset(mode, B, K) + asv::staged_workspace_bytes((long long)B * (K + 1), sp.n_unit));
 }
 
 asv_status asv_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t stream) {
@@ -320,7 +332,7 @@ static asv_status run_jsd(int mode, asv::JsdArgs& a, int dtype, void* workspace,
   int amode = mode == asv::kModeAsym ? ASV_MODE_ASYMSPEC : ASV_MODE_SCI;
   if (a.variant == 1) amode = ASV_MODE_SWEEP;
   if (a.variant == 2) amode = ASV_MODE_ASYMSPEC_SCI;
-  if (ws_bytes < cluster_workspace_bytes(amode, a.B, a.K)) return ASV_ERR_WORKSPACE;
+  if (ws_bytes < with_log(cluster_workspace_bytes(amode, a.B, a.K))) return ASV_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return ASV_ERR_ALIGN;
   const int eb = elem_size(dtype);
   const int NT = mode == asv::kModeAsym ? 3 : 2;
@@ -329,6 +341,7 @@ static asv_status run_jsd(int mode, asv::JsdArgs& a, int dtype, void* workspace,
   a.tickets = reinterpret_cast<uint32_t*>(workspace);
   a.records = reinterpret_cast<asv::RowRecord*>(static_cast<char*>(workspace) + tickets_bytes(a.B));
   a.mrecords = reinterpret_cast<asv::MultiRecord*>(static_cast<char*>(workspace) + tickets_bytes(a.B));
+  a.check_log = check_log_at(workspace, cluster_workspace_bytes(amode, a.B, a.K));
   // The staged kernel: aligned rows, no pre-hit, no cluster-size override, and a workspace that
   // holds its exchange area (a smaller one, enough for the cluster kernel, selects that kernel).
   const asv::StagedPlan sp = staged_plan_for(amode, a.B, a.K, a.V, dtype);
@@ -351,6 +364,8 @@ static asv_status run_jsd(int mode, asv::JsdArgs& a, int dtype, void* workspace,
       a.part_a = st + cnt + 256;
       a.part_b = reinterpret_cast<float*>(st + cnt + 256 + size_t(a.units) * 128);
       a.bulk = 2;
+      a.check_log = check_log_at(workspace, staged_offset(amode, a.B, a.K) +
+                                                asv::staged_workspace_bytes(rows, sp.n_unit));
       e = asv::launch_jsd_staged(mode, dtype, a, sp, std::min(grid, a.units / a.chunk_units), stream);
       if (e != cudaSuccess) return cuda_fail(e);
       return ASV_OK;
@@ -722,6 +737,7 @@ asv_status rapid_verify_ex(const float* z, const float* q, const int32_t* draft_
       tail_frac < 0.0f || tail_frac >= 1.0f)
     return ASV_ERR_PARAM;
   if (ws_bytes < asv_workspace_bytes(ASV_MODE_RAPID, B, G, V, ASV_F32)) return ASV_ERR_WORKSPACE;
+  uint32_t* rapid_log = check_log_at(workspace, cluster_workspace_bytes(ASV_MODE_RAPID, B, G));
   bool bulk = (size_t(V) * 4) % 16 == 0 && aligned(z, 16) && aligned(q, 16);
   LaunchPlan pl;
   const float ln_tf = tail_frac > 0.0f ? std::log(tail_frac) : -INFINITY;
@@ -754,6 +770,7 @@ asv_status rapid_verify_ex(const float* z, const float* q, const int32_t* draft_
   a.records = reinterpret_cast<asv::RapidRecord*>(static_cast<char*>(workspace) + tickets_bytes(B));
   a.jobs = reinterpret_cast<asv::RapidJob*>(static_cast<char*>(workspace) + records_end(ASV_MODE_RAPID, B, G));
   a.draw_ctas = rapid_draw_ctas(V, B);
+  a.check_log = rapid_log;
   e = asv::launch_rapid(a, pl, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   return ASV_OK;

@@ -21,6 +21,23 @@ constexpr uint32_t kBitBadDraft = 2u;
 constexpr uint32_t kBitTimeout = 4u;
 constexpr uint32_t kBitAccept = 8u;
 
+// ------------------------------------------------------------------ checked build
+// Built with -DASV_CHECKED, the kernels test every global and shared-memory index they form
+// against the buffer it addresses.  A failed test is counted in the call's check log (two words at
+// the end of the workspace: the count and the source line of the first failure) and the access is
+// skipped -- nothing traps.  In the ordinary build the tests compile to nothing.
+#ifdef ASV_CHECKED
+__device__ __forceinline__ bool check_index(uint32_t* log, bool ok, int line) {
+  if (!ok && log != nullptr) {
+    if (atomicAdd(log, 1u) == 0u) atomicExch(log + 1, uint32_t(line));
+  }
+  return ok;
+}
+#define ASV_GUARD(args, cond) ::asv::check_index((args).check_log, bool(cond), __LINE__)
+#else
+#define ASV_GUARD(args, cond) true
+#endif
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

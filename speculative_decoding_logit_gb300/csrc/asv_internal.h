@@ -129,6 +129,7 @@ struct JsdArgs {
   void* part_a;          // [units] 64-byte pass-A partials
   float* part_b;         // [units] 16 floats: pass-B sums as (hi, lo) pairs
   uint32_t* abort_flag;  // set by a CTA whose bounded wait expired
+  uint32_t* check_log;   // checked build: [count of failed index tests, line of the first]
 };
 
 struct RapidArgs {
@@ -148,6 +149,7 @@ struct RapidArgs {
   RapidRecord* records;
   RapidJob* jobs;
   int draw_ctas;  // CTAs per request of the draw launch
+  uint32_t* check_log;  // checked build: [count of failed index tests, line of the first]
 };
 
 // Staged AsymSpec / E2-SCI kernel (asv_staged.cu): units per row and entries per unit for a row of
@@ -171,6 +173,13 @@ size_t asym_cluster_workspace_bytes(int B, int K);
 cudaError_t launch_jsd_staged(int mode, int dtype, const JsdArgs& args, const StagedPlan& plan, int grid,
                               cudaStream_t s);
 int staged_grid(int mode, int dtype, const JsdArgs& args, const StagedPlan& plan);  // 0: cannot launch
+
+// The checked build appends a 256-byte check log to every workspace (zero-filled like the rest).
+#ifdef ASV_CHECKED
+constexpr size_t kCheckLogBytes = 256;
+#else
+constexpr size_t kCheckLogBytes = 0;
+#endif
 
 // Kernel launchers (return the cudaError_t of the launch).
 cudaError_t launch_jsd_family(int mode, int dtype, const JsdArgs& args, const LaunchPlan& plan, cudaStream_t s);

@@ -112,7 +112,10 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
   const int pos = row - req * R1;
   const int V = p.V;
   const int v0 = int(rank) * p.n_slice;
-  const int len = max(0, min(V - v0, p.n_slice));
+  // (checked build: a row outside the batch, or a cluster larger than the exchange arrays, reads
+  // nothing; every CTA still takes part in the cluster barriers)
+  const bool row_ok = ASV_GUARD(p, row >= 0 && row < p.B * R1 && rank < uint32_t(kMaxCluster) && C <= uint32_t(kMaxCluster));
+  const int len = row_ok ? max(0, min(V - v0, p.n_slice)) : 0;
   const int nvec = (len + VEC - 1) / VEC;
   constexpr bool aligned = ALIGNED;
   const size_t row_base = size_t(row) * size_t(V);
@@ -127,7 +130,7 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
   // multi-outcome ones, short of registers, load them when they finalise).
   const bool fin_lane = !kMulti && rank == 0 && warp == 0 && (lane == 1 || lane == 2);
   int d_pre = -1;
-  if (fin_lane && pos < p.K) d_pre = __ldg(p.draft_ids + size_t(req) * p.K + pos);
+  if (fin_lane && pos < p.K && ASV_GUARD(p, row_ok && req < p.B)) d_pre = __ldg(p.draft_ids + size_t(req) * p.K + pos);
 
   // L2 policies: the verifier input is read once (evict first; fused: pass B reads it again); the
   // divergence pair is read again by pass B (evict last until then, evict first on that last read).
@@ -218,11 +221,17 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
         }
       }
     };
+    // One vector of input j (checked build: its entries must lie in the slice).
+    auto ldA = [&](int j, int v) {
+      return ASV_GUARD(p, v >= 0 && (!aligned || v * VEC + VEC <= len)) ? G::load(slice[j], v * VEC, len, aligned, true,
+                                                                            j == 2 ? pol_t : pol_keep)
+                                                                  : G::pad();
+    };
     uint4 cur[NT], nxt[NT];
     int vi = tid;
     if (vi < nvec) {
 #pragma unroll
-      for (int j = 0; j < NT; ++j) cur[j] = G::load(slice[j], vi * VEC, len, aligned, true, j == 2 ? pol_t : pol_keep);
+      for (int j = 0; j < NT; ++j) cur[j] = ldA(j, vi);
     }
     // (bf16 multi-outcome kernels, short of registers, keep one vector per trip.)
     if constexpr (ALIGNED && (!kMulti || std::is_same<T, float>::value)) {
@@ -231,15 +240,13 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
       for (; vi < nvec; vi += 2 * kJsdThreads) {
         if (vi + kJsdThreads < nvec) {
 #pragma unroll
-          for (int j = 0; j < NT; ++j)
-            nxt[j] = G::load(slice[j], (vi + kJsdThreads) * VEC, len, aligned, true, j == 2 ? pol_t : pol_keep);
+          for (int j = 0; j < NT; ++j) nxt[j] = ldA(j, vi + kJsdThreads);
         }
         a_body(cur, vi);
         if (vi + kJsdThreads >= nvec) break;
         if (vi + 2 * kJsdThreads < nvec) {
 #pragma unroll
-          for (int j = 0; j < NT; ++j)
-            cur[j] = G::load(slice[j], (vi + 2 * kJsdThreads) * VEC, len, aligned, true, j == 2 ? pol_t : pol_keep);
+          for (int j = 0; j < NT; ++j) cur[j] = ldA(j, vi + 2 * kJsdThreads);
         }
         a_body(nxt, vi + kJsdThreads);
       }
@@ -248,8 +255,7 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
       for (; vi < nvec; vi += kJsdThreads) {
         if (vi + kJsdThreads < nvec) {
 #pragma unroll
-          for (int j = 0; j < NT; ++j)
-            nxt[j] = G::load(slice[j], (vi + kJsdThreads) * VEC, len, aligned, true, j == 2 ? pol_t : pol_keep);
+          for (int j = 0; j < NT; ++j) nxt[j] = ldA(j, vi + kJsdThreads);
         }
         a_body(cur, vi);
 #pragma unroll
@@ -259,7 +265,7 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
   }
 
   float xd_pre = 0.0f;
-  if (MODE == kModeAsym && fin_lane && d_pre >= 0 && d_pre < V)
+  if (MODE == kModeAsym && fin_lane && d_pre >= 0 && d_pre < V && row_ok)
     xd_pre = G::at(p.x[lane == 1 ? NT - 1 : 1], row_base + size_t(d_pre));
 
   // Pass B of aligned slices streams the divergence pair (fused: and the verifier input) from L2
@@ -271,9 +277,12 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
     const int vi = tid + j * kJsdThreads;
     if (vi < nvec) {
 #pragma unroll
-      for (int m = 0; m < NPB; ++m)
-        cp_async16(smem_addr(&s_ring[((j & (kRing - 1)) * NPB + m) * kJsdThreads + tid]),
-                   static_cast<const char*>(slice[m < 2 ? m : NT - 1]) + size_t(vi) * 16u, pol_evict_first);
+      for (int m = 0; m < NPB; ++m) {
+        const int slot = ((j & (kRing - 1)) * NPB + m) * kJsdThreads + tid;
+        if (ASV_GUARD(p, slot < kRing * NPB * kJsdThreads && vi * VEC + VEC <= len))
+          cp_async16(smem_addr(&s_ring[slot]), static_cast<const char*>(slice[m < 2 ? m : NT - 1]) + size_t(vi) * 16u,
+                     pol_evict_first);
+      }
     }
     cp_async_commit();
   };
@@ -312,7 +321,7 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
   }
   __syncthreads();
   cluster_wait();
-  if (warp == 0 && lane < NT + NA) {
+  if (warp == 0 && lane < NT + NA && ASV_GUARD(p, rank < uint32_t(kMaxCluster) && C <= uint32_t(kMaxCluster))) {
     const uint32_t dst = smem_addr(&xchg.from[rank]);
     if (lane < NT) {
       const int j = lane;
@@ -506,6 +515,7 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
       for (int j = 0; tid + j * kJsdThreads < nvec; ++j) {
         cp_async_wait_group<kRing - 1>();  // the copies of vector j have landed
         const int slot = (j & (kRing - 1)) * NPB;
+        if (!ASV_GUARD(p, (slot + NPB - 1) * kJsdThreads + tid < kRing * NPB * kJsdThreads)) continue;
         float2 xa[NP], xb[NP];
         G::pairs(s_ring[(slot + 0) * kJsdThreads + tid], xa);
         G::pairs(s_ring[(slot + 1) * kJsdThreads + tid], xb);
@@ -521,7 +531,7 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
     } else if (finite) {
       int vi = tid;
       uint4 ca, cb, ct, na, nb, nt;
-      if (vi < nvec) {
+      if (vi < nvec && ASV_GUARD(p, vi >= 0)) {
         ca = G::load(slice[0], vi * VEC, len, aligned, true, pol_evict_first);
         cb = G::load(slice[1], vi * VEC, len, aligned, true, pol_evict_first);
         if constexpr (FUSE) ct = G::load(slice[NT - 1], vi * VEC, len, aligned, true, pol_evict_first);
@@ -569,7 +579,7 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
   }
   __syncthreads();
   constexpr int NS = FUSE ? 6 : 3;
-  if (warp == 0 && lane < NS) {
+  if (warp == 0 && lane < NS && ASV_GUARD(p, rank < uint32_t(kMaxCluster))) {
     // Lane m adds sum m of the CTA's warps in warp order (reads issued together) and pushes it into
     // CTA 0.
     float v[kWarps];
@@ -586,6 +596,7 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
   if (rank != 0 || warp != 0) return;
 
   // ---------------------------------------------------------------- row finalisation (CTA 0, warp 0)
+  if (!row_ok) return;
   jsd_finalize_row<T, MODE, NB, FUSE>(p, row, rc, xchg.jsd_from, C, lane, d_pre, xd_pre);
 }
 

@@ -272,6 +272,9 @@ __device__ __forceinline__ void jsd_finalize_row(const JsdArgs& p, const int row
   const unsigned kAll = 0xffffffffu;
   const int K = p.K;
   const bool finite = rc.finite != 0;
+  // (checked build: the row and its request inside the batch, the grid sizes inside their arrays)
+  if (!ASV_GUARD(p, row >= 0 && row < p.B * R1 && req < p.B && p.n_gamma <= kMaxGamma && p.n_beta <= kMaxArg))
+    return;
   // The draft token and its verifier / compressed-drafter logits: single-outcome callers pass them
   // in (loaded early by lanes 1 and 2); the multi-outcome kernels load them here.
   const int d = (pos < K) ? (kMulti ? p.draft_ids[size_t(req) * K + pos] : __shfl_sync(kAll, d_in, 1)) : -1;

@@ -194,10 +194,26 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
   const int pos = row - req * R1;
   const int V = p.V;
   const int v0 = int(rank) * p.n_slice;
-  const int len = max(0, min(V - v0, p.n_slice));
+  // (checked build: a row outside the batch, or a cluster larger than the exchange arrays, reads
+  // nothing; every CTA still takes part in the cluster barriers)
+  const bool row_ok = ASV_GUARD(p, row >= 0 && row < p.B * R1 && rank < uint32_t(kMaxCluster) && C <= uint32_t(kMaxCluster));
+  const int len = row_ok ? max(0, min(V - v0, p.n_slice)) : 0;
   const int nvec = (len + VEC - 1) / VEC;
   const size_t row_base = size_t(row) * size_t(V);
   const float* zsl = p.z + row_base + v0;
+#ifdef ASV_CHECKED
+  uint32_t dyn_smem = 0;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_smem));
+#endif
+  // One vector of the slice (checked build: its entries must lie in the slice).
+  auto LD4 = [&](const float* base, int k, uint64_t pol, float pad) {
+    return ASV_GUARD(p, k >= 0 && (!ALIGNED || k + VEC <= len)) ? ld4(base, k, len, ALIGNED, pol, pad)
+                                                            : make_float4(pad, pad, pad, pad);
+  };
+  auto LD4C = [&](const float* base, int k, float pad) {
+    return ASV_GUARD(p, k >= 0 && (!ALIGNED || k + VEC <= len)) ? ld4c(base, k, len, ALIGNED, pad)
+                                                            : make_float4(pad, pad, pad, pad);
+  };
   const float* qsl = p.q + row_base + v0;
   const uint64_t pol_keep = policy_evict_last();
   const uint64_t pol_evict_first = policy_evict_first();
@@ -211,7 +227,7 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
   // The draft token's z and q for the accept test in CTA 0 (loaded now, used at the end).
   int d = -1;
   float zd = 0.0f, qd = 0.0f;
-  if (rank == 0 && tid == 0 && pos < G) {
+  if (rank == 0 && tid == 0 && pos < G && row_ok) {
     d = p.draft_ids[size_t(req) * G + pos];
     if (d >= 0 && d < V) {
       zd = __ldg(p.z + row_base + d);
@@ -255,7 +271,10 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
         // One bound per kGroup consecutive vectors of this thread.
         gmax = fmaxf(gmax, vk);
         if ((it & (kGroup - 1)) == kGroup - 1 || vn >= nvec) {
-          s_umax[(it / kGroup) * kRapidThreads + tid] = gmax;
+#ifdef ASV_CHECKED
+          if (ASV_GUARD(p, uint32_t(((it / kGroup) * kRapidThreads + tid) * 4) < dyn_smem))
+#endif
+            s_umax[(it / kGroup) * kRapidThreads + tid] = gmax;
           ub_t = fmaxf(ub_t, gmax);
           gmax = -INFINITY;
         }
@@ -318,21 +337,21 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
     };
     float4 cz, cq, nz, nq;
     if (vi < nvec) {
-      cz = ld4(zsl, vi * VEC, len, ALIGNED, polA, -INFINITY);
-      cq = ld4(qsl, vi * VEC, len, ALIGNED, polA, 0.0f);
+      cz = LD4(zsl, vi * VEC, polA, -INFINITY);
+      cq = LD4(qsl, vi * VEC, polA, 0.0f);
     }
     // Two vectors per trip, the prefetch alternating between (cz, cq) and (nz, nq) (no register
     // copies); a prefetched vector is consumed only while it is in range.
     for (; vi < nvec; vi += 2 * kRapidThreads) {
       if (vi + kRapidThreads < nvec) {
-        nz = ld4(zsl, (vi + kRapidThreads) * VEC, len, ALIGNED, polA, -INFINITY);
-        nq = ld4(qsl, (vi + kRapidThreads) * VEC, len, ALIGNED, polA, 0.0f);
+        nz = LD4(zsl, (vi + kRapidThreads) * VEC, polA, -INFINITY);
+        nq = LD4(qsl, (vi + kRapidThreads) * VEC, polA, 0.0f);
       }
       a_body(cz, cq, vi);
       if (vi + kRapidThreads >= nvec) break;
       if (vi + 2 * kRapidThreads < nvec) {
-        cz = ld4(zsl, (vi + 2 * kRapidThreads) * VEC, len, ALIGNED, polA, -INFINITY);
-        cq = ld4(qsl, (vi + 2 * kRapidThreads) * VEC, len, ALIGNED, polA, 0.0f);
+        cz = LD4(zsl, (vi + 2 * kRapidThreads) * VEC, polA, -INFINITY);
+        cq = LD4(qsl, (vi + 2 * kRapidThreads) * VEC, polA, 0.0f);
       }
       a_body(nz, nq, vi + kRapidThreads);
     }
@@ -546,14 +565,14 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
     int vi = tid;
     float4 cz, cq, nz, nq;
     if (vi < nvec) {
-      cz = ld4(zsl, vi * VEC, len, ALIGNED, pol_evict_first, -INFINITY);
-      cq = ld4(qsl, vi * VEC, len, ALIGNED, pol_evict_first, 0.0f);
+      cz = LD4(zsl, vi * VEC, pol_evict_first, -INFINITY);
+      cq = LD4(qsl, vi * VEC, pol_evict_first, 0.0f);
     }
     for (; vi < nvec; vi += kRapidThreads) {
       const int vn = vi + kRapidThreads;
       if (vn < nvec) {
-        nz = ld4(zsl, vn * VEC, len, ALIGNED, pol_evict_first, -INFINITY);
-        nq = ld4(qsl, vn * VEC, len, ALIGNED, pol_evict_first, 0.0f);
+        nz = LD4(zsl, vn * VEC, pol_evict_first, -INFINITY);
+        nq = LD4(qsl, vn * VEC, pol_evict_first, 0.0f);
       }
       float2 p0, p1, h0, h1;
       pzhs2(make_float2(cz.x, cz.y), make_float2(cq.x, cq.y), invT2, nML2, inv2, etaT2, p0, h0);
@@ -625,8 +644,8 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
         for (int r = 0; r < kGroup; ++r) {
           const int vi = (g * kGroup + r) * kRapidThreads + tid;
           if (vi < nvec) {
-            const float4 z4 = ld4c(zsl, vi * VEC, len, ALIGNED, -INFINITY);
-            const float4 q4 = ld4c(qsl, vi * VEC, len, ALIGNED, 0.0f);
+            const float4 z4 = LD4C(zsl, vi * VEC, -INFINITY);
+            const float4 q4 = LD4C(qsl, vi * VEC, 0.0f);
             float2 p0, p1, h0, h1;
             pzhs2(make_float2(z4.x, z4.y), make_float2(q4.x, q4.y), invT2, nML2, inv2, etaT2, p0, h0);
             pzhs2(make_float2(z4.z, z4.w), make_float2(q4.z, q4.w), invT2, nML2, inv2, etaT2, p1, h1);
@@ -763,8 +782,8 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
           for (int r = 0; r < kGroup; ++r) {
             const int vi = (g * kGroup + r) * kRapidThreads + tid;
             if (vi >= nvec) break;
-            const float4 z4 = ld4c(zsl, vi * VEC, len, ALIGNED, -INFINITY);
-            const float4 q4 = ld4c(qsl, vi * VEC, len, ALIGNED, 0.0f);
+            const float4 z4 = LD4C(zsl, vi * VEC, -INFINITY);
+            const float4 q4 = LD4C(qsl, vi * VEC, 0.0f);
             const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
             const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
@@ -793,8 +812,8 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
       } else {
         // Pass C: a thread ran out of candidate slots; test every entry of the slice.
         for (int vi = tid; vi < nvec; vi += kRapidThreads) {
-          const float4 z4 = ld4(zsl, vi * VEC, len, ALIGNED, pol_evict_first, -INFINITY);
-          const float4 q4 = ld4(qsl, vi * VEC, len, ALIGNED, pol_evict_first, 0.0f);
+          const float4 z4 = LD4(zsl, vi * VEC, pol_evict_first, -INFINITY);
+          const float4 q4 = LD4(qsl, vi * VEC, pol_evict_first, 0.0f);
           const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
           const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
@@ -824,7 +843,7 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
         dh = df_add(dh, DF{__shfl_xor_sync(0xffffffffu, dh.hi, o), __shfl_xor_sync(0xffffffffu, dh.lo, o)});
         de = df_add(de, DF{__shfl_xor_sync(0xffffffffu, de.hi, o), __shfl_xor_sync(0xffffffffu, de.lo, o)});
       }
-      if (lane == 0) {
+      if (lane == 0 && ASV_GUARD(p, rank < uint32_t(kMaxCluster))) {
         const uint32_t base = smem_addr(&xchg.head[rank][0]);
         dsmem_st_f32(dsmem_map(base + 0, 0), dh.hi);
         dsmem_st_f32(dsmem_map(base + 4, 0), dh.lo);
@@ -845,7 +864,7 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
       float h4[4], l4[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const uint32_t q = (q0 + u < C) ? q0 + u : 0u;
+        const uint32_t q = (q0 + u < C && ASV_GUARD(p, q0 + u < uint32_t(kMaxCluster))) ? q0 + u : 0u;
         h4[u] = xchg.head[q][2 * lane];
         l4[u] = xchg.head[q][2 * lane + 1];
       }
@@ -890,6 +909,7 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
       if (u * qd < protd) bits |= kBitAccept;
     }
   }
+  if (!ASV_GUARD(p, row_ok && req < p.B)) return;
   RapidRecord rec;
   rec.zs_max = rs.M;
   rec.inv_sum = rc.inv_sum;
@@ -963,8 +983,10 @@ __global__ void __launch_bounds__(kDrawThreads) rapid_draw_kernel(const RapidArg
   const int parts = p.draw_ctas;
   const int req = blockIdx.x / parts;
   const int part = blockIdx.x - req * parts;
+  if (!ASV_GUARD(p, req < p.B && part < parts)) return;
   RapidJob* job = p.jobs + req;
   if (!job->active) return;  // uniform over the CTA
+  if (!ASV_GUARD(p, job->row >= 0 && job->row <= p.G)) return;
   const int G = p.G;
   const int R1 = G + 1;
   const int V = p.V;
@@ -994,7 +1016,11 @@ __global__ void __launch_bounds__(kDrawThreads) rapid_draw_kernel(const RapidArg
   if (al) {
     for (int it = 0; it < iters; ++it) {
       const int vi = it * kDrawThreads + tid;
-      if (vi < nvec) {
+#ifdef ASV_CHECKED
+      uint32_t dyn_smem = 0;
+      asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_smem));
+#endif
+      if (vi < nvec && ASV_GUARD(p, vi * VEC + VEC <= len && uint32_t(((2 * it + 1) * kDrawThreads + tid + 1) * 16) <= dyn_smem)) {
         cp_async16(smem_addr(&s_stage[(2 * it + 0) * kDrawThreads + tid]), zr + vi * VEC, pol);
         cp_async16(smem_addr(&s_stage[(2 * it + 1) * kDrawThreads + tid]), qr + vi * VEC, pol);
       }

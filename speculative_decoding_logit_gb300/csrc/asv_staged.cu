@@ -499,6 +499,14 @@ __global__ void __launch_bounds__(kThreads, 1) jsd_staged_kernel(const JsdArgs p
   auto a_addr = [&](int i, int j) { return ring_a + (size_t(i) * NT + j) * in_bytes; };
   auto b_addr = [&](int i, int j) { return ring_b + (size_t(i) * NBI + j) * in_bytes; };
   auto bar = [](uint64_t& b) { return smem_addr(&b); };
+#ifdef ASV_CHECKED
+  uint32_t dyn_smem = 0;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_smem));
+#else
+  const uint32_t dyn_smem = 0;
+#endif
+  (void)dyn_smem;
+  const int rows = p.B * (p.K + 1);
 
   if (tid == 0) {
     for (int i = 0; i < kRingA; ++i) {
@@ -542,6 +550,12 @@ __global__ void __launch_bounds__(kThreads, 1) jsd_staged_kernel(const JsdArgs p
         const UnitPos up = unit_pos(y, G_, cta, nch, m, n, V);
         const uint32_t bytes = uint32_t(up.len) * G::kBytes;
         const size_t off = (size_t(up.row) * size_t(V) + size_t(up.v0)) * G::kBytes;
+        // (checked build: the unit inside the batch and its row, the buffers inside shared memory;
+        // a unit that fails is not copied, and the waits for it run out -- the call then aborts)
+        if (!ASV_GUARD(p, up.row < rows && up.len > 0 && up.v0 + up.len <= V && nch <= kMaxUnits &&
+                              uint32_t(((ring_a_role ? a_addr(i, nin - 1) : b_addr(i, nin - 1)) - s_buf) + bytes) <=
+                                  dyn_smem))
+          break;
         mbar_arrive_expect_tx(bar(full[i]), bytes * nin);
         for (int j = 0; j < nin; ++j) {
           const int src = ring_a_role ? j : (j < 2 ? j : NT - 1);
@@ -574,6 +588,10 @@ __global__ void __launch_bounds__(kThreads, 1) jsd_staged_kernel(const JsdArgs p
       }
       const UnitPos up = unit_pos(t * m, G_, cta, nch, m, n, V);
       const size_t ch = size_t(up.ch);
+      if (!ASV_GUARD(p, up.row < rows && ch < size_t(p.units))) {
+        if (lane == 0) sh.abort = 1;
+        break;
+      }
       if (is_a) {
         // lane j < NT: input j; lane NT + s: argmax slot s -- over the compute warps in order
         JsdPart* dp = reinterpret_cast<JsdPart*>(static_cast<char*>(p.part_a) + ch * (4 * kPartAStride));
@@ -636,6 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1) jsd_staged_kernel(const JsdArgs p
       const int k = t % kSlots;
       const UnitPos up = unit_pos(t * m, G_, cta, nch, m, n, V);
       bool ok = t < kSlots || warp_wait(bar(sh.rc_free[k]), uint32_t(t / kSlots - 1) & 1u, &sh.abort);
+      ok = ok && ASV_GUARD(p, up.row < rows && nch <= kMaxUnits);
       ok = ok && poll_count(p.row_cnt + up.row, uint32_t(nch), p, &sh.abort);
       if (ok) {
         gather_row<MODE, NA, FUSE>(p, up.row, nch, lane, sh.from[sw], sh.rc[k]);
@@ -657,6 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1) jsd_staged_kernel(const JsdArgs p
       const UnitPos up = unit_pos(t * m, G_, cta, nch, m, n, V);
       if (up.qc != nch - 1) continue;
       const int row = up.row;
+      if (!ASV_GUARD(p, row < rows && nch <= kMaxUnits)) break;
       if (!poll_count(p.row_jcnt + row, uint32_t(nch), p, &sh.abort)) {
         mark_timeout(p, row, lane);
         if (lane == 0) sh.abort = 1;

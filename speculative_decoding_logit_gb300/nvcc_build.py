@@ -14,6 +14,9 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libasv.so")
+# The checked build: the same sources with -DASV_CHECKED (every kernel index tested against its
+# buffer, failures counted in the workspace's check log, the access skipped).
+LIB_CHECKED = os.path.join(BUILD, "libasv_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
@@ -31,20 +34,25 @@ def _deps():
             [os.path.join(INCLUDE, "asv.h"), os.path.abspath(__file__)])
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile csrc/*.cu and link _build/libasv.so; returns the library path."""
-    if not force and up_to_date():
-        return LIB
+def build_checked(force: bool = False, verbose: bool = False) -> str:
+    """Compile the checked library (_build/libasv_checked.so, -DASV_CHECKED)."""
+    return build(force=force, verbose=verbose, extra_flags=("-DASV_CHECKED",), lib=LIB_CHECKED)
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=(), lib: str = LIB) -> str:
+    """Compile csrc/*.cu and link `lib` (default _build/libasv.so); returns the library path."""
+    if not force and up_to_date(lib):
+        return lib
     os.makedirs(BUILD, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
-    tag = f"{os.getpid()}"
+    tag = f"{os.getpid()}{'c' if extra_flags else ''}"
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + f".{tag}.o")
@@ -58,16 +66,17 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".{tag}.tmp"
+    tmp = lib + f".{tag}.tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs, "-lcudart_static", "-ldl", "-lpthread", "-lrt"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     for o in objs:
         os.remove(o)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True))
+    print(build_checked(force="--force" in sys.argv, verbose=True))
