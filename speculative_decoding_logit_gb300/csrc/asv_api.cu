@@ -119,34 +119,51 @@ cudaError_t plan_jsd(int elem_bytes, int V, long long R, bool aligned, LaunchPla
   return cudaSuccess;
 }
 
-// Plan for the RAPID kernel (fp32 rows, four entries per 16-byte vector).  Without the all-entry
-// sums a CTA keeps a 2-byte bound per vector of its slice in shared memory: at least as many CTAs
-// per row as keep that within 48 KB, so four CTAs still share an SM.
+// Plan for the RAPID kernel (fp32 rows, four entries per 16-byte vector).  Aligned rows under the
+// default tail reading stream pass A through the shared-memory ring: the verification is then bound
+// by the bytes in flight while it streams, and every CTA pays its exchanges and sparse re-reads
+// once, so the fewest CTAs per row that keep at least 8 MB in flight over the batch (each CTA's ring
+// holds 32 KB), with the ring and the per-group bounds within 72 KB (three CTAs per SM).  Otherwise
+// (the dense pass B of the all-entry sums, or element loads) the wave-filling choice, with the
+// bounds within 52 KB (four CTAs per SM).
 cudaError_t plan_rapid(int V, long long R, bool aligned, bool all_sums, LaunchPlan* out) {
   DevInfo di;
   cudaError_t e = dev_info(&di);
   if (e != cudaSuccess) return e;
-  int C = wave_fill_cluster(V, R, asv::rapid_ctas_per_sm(), di.sms);
   auto n_slice = [&](int c) { return int(round_up(size_t(ceil_div(V, c)), 4)); };
-  if (g_tune_cluster.load() <= 0)
-    while (C < asv::kMaxCluster && asv::rapid_smem_bytes(all_sums, n_slice(C)) > 48 * 1024) ++C;
-  if (asv::rapid_smem_bytes(all_sums, n_slice(C)) > 200 * 1024) return cudaErrorInvalidValue;  // V too large
+  auto smem = [&](int c) { return asv::rapid_smem_bytes(all_sums, n_slice(c), aligned); };
+  const int c_max = std::max(1, std::min(asv::kMaxCluster, V / 1024));
+  int C = g_tune_cluster.load();
+  if (C <= 0) {
+    if (aligned && !all_sums) {
+      const long long per_row = std::max<long long>(1, R) * asv::rapid_ring_bytes();
+      C = int(std::min<long long>(c_max, std::max<long long>(1, ((8LL << 20) + per_row - 1) / per_row)));
+      while (C < asv::kMaxCluster && smem(C) > 72 * 1024) ++C;
+    } else {
+      C = wave_fill_cluster(V, R, asv::rapid_ctas_per_sm(), di.sms);
+      while (C < asv::kMaxCluster && smem(C) > 52 * 1024) ++C;
+    }
+  }
+  if (smem(C) > 200 * 1024) return cudaErrorInvalidValue;  // V too large
   out->cluster = C;
   out->threads = asv::rapid_threads();
   out->n_slice = n_slice(C);
-  out->smem = asv::rapid_smem_bytes(all_sums, out->n_slice);
+  out->smem = smem(C);
   out->bulk = aligned ? 1 : 0;
   return cudaSuccess;
 }
 
-// CTAs per request of the RAPID draw launch: at least one wave of resident CTAs over the batch's
-// requests, and slices of at most 6144 entries (the staged copy of a slice, 8 bytes per entry,
-// stays within 48 KB of shared memory), at least 1024 entries per CTA.
+// CTAs per request of the RAPID draw launch.  The draw reads the B stop rows once, so a second,
+// partial wave of CTAs would nearly double its time: while the batch fits one wave of resident
+// draw CTAs, as many CTAs per request as that wave holds (a CTA streams its slice through a ring of
+// six vectors per thread); larger batches take slices of at most one ring's worth (6144 entries)
+// over several waves.  At least 1024 entries per CTA.
 int rapid_draw_ctas(int V, int B) {
   DevInfo di;
   const int sms = dev_info(&di) == cudaSuccess ? di.sms : 1;
-  const long long wave = (1LL * asv::rapid_ctas_per_sm() * sms + B - 1) / std::max(B, 1);
-  const long long want = std::max<long long>(wave, (V + 6143) / 6144);
+  const long long slots = 1LL * asv::rapid_draw_ctas_per_sm() * sms;
+  long long want = slots / std::max(B, 1);
+  if (want < 1) want = (V + 6143) / 6144;
   return int(std::max(1LL, std::min<long long>(want, std::max(1, V / 1024))));
 }
 

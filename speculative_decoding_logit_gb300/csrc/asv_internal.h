@@ -188,8 +188,11 @@ cudaError_t launch_rapid(const RapidArgs& args, const LaunchPlan& plan, cudaStre
 int jsd_threads();      // threads per CTA of the AsymSpec / SCI kernel
 int jsd_ctas_per_sm();  // CTAs of it that share an SM (its launch bounds)
 bool rapid_needs_all_sums(int tail_mode, float ln_tail_frac);  // all-entry sums: dense pass B
-int rapid_smem_bytes(bool all_sums, int n_slice);                // dynamic shared memory per CTA
+int rapid_umax_bytes(bool all_sums, int n_slice);                 // the per-vector-group bounds of U
+int rapid_smem_bytes(bool all_sums, int n_slice, bool aligned);   // dynamic shared memory per CTA
+int rapid_ring_bytes();                                           // the pass-A ring of one CTA
 int rapid_draw_smem_bytes(int n_slice, bool aligned);            // ... of the draw launch
+int rapid_draw_ctas_per_sm();                                     // draw CTAs resident per SM
 int rapid_threads();      // threads per CTA of the RAPID kernel
 int rapid_ctas_per_sm();  // CTAs of it that share an SM (its launch bounds)
 

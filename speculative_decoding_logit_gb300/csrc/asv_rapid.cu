@@ -32,15 +32,19 @@
 // p-mass being (all p-mass) - (head p-mass).  CTA 0 of the row decides the draft's accept test
 // u*q(d) < protected(d) (u from Philox4x32-10) and files a row record; the last row of a request
 // to finish runs the scan, writes the outputs and leaves a draw job (the stop row and its
-// constants).  A second launch, one cluster per request, draws the emitted token at the stop
-// position with an exponential race over that row (re-read from global memory, normally still in
-// L2): argmin_k E_k / w_k, E_k = -ln u_k, with w the residual max(p - protected, p - q, 0) or, at
-// the bonus position, the protected target.  No CTA waits on another cluster, and no CTA of the
-// verification waits for its row's finalisation.
+// constants).  A second launch, a group of CTAs per request, draws the emitted token at the stop
+// position with an exponential race over that row (re-read from global memory): argmin_k E_k / w_k,
+// E_k = -ln u_k, with w the residual max(p - protected, p - q, 0) or, at the bonus position, the
+// protected target.  The draw is a programmatic dependent launch: every verification CTA signals
+// at its start that the draw may be scheduled, so the draw's CTAs take the SM slots the
+// verification's last CTAs leave free, and each waits (griddepcontrol.wait) for the whole
+// verification to complete, its writes visible, before it reads anything.  No CTA waits on another
+// cluster, and no CTA of the verification waits for its row's finalisation.
 //
 // Every quantity of an entry (p, zhat/T, the protected value) is formed by the same sequence of
 // correctly rounded operations wherever it is needed -- pass B (two lanes per instruction), pass C,
 // the accept test and the draw (one lane) -- so the head test gives the same answer everywhere.
+#include <algorithm>
 #include <climits>
 
 #include "asv_device.cuh"
@@ -52,7 +56,14 @@ constexpr int kRapidThreads = 256;    // threads per CTA (launch bounds)
 constexpr int kRapidCtasPerSm = 4;    // CTAs per SM the kernel is compiled for (launch bounds)
 constexpr float kRapidSlack = 64.0f;  // reference slack (log2 units), as in the AsymSpec kernel
 constexpr int kDrawThreads = 256;     // threads per CTA of the draw launch
+constexpr int kDrawStage = 6;         // slots of a draw thread's ring of vectors in shared memory
 constexpr int kGroup = 4;             // vectors of a thread per stored bound of U (a power of 2)
+// Pass A of aligned slices under the default tail reading streams through a per-thread ring of
+// kRingA vectors of z and of q in shared memory, filled by 16-byte cp.async copies: the copies in
+// flight hold no registers, so a thread keeps kRingA vectors per input on the way from HBM instead
+// of the two a register prefetch affords (the verification is bound by the bytes in flight).
+constexpr int kRingA = 4;  // a power of 2
+constexpr int kRingABytes = kRingA * 2 * kRapidThreads * 16;
 
 struct __align__(16) RapidXchg {
   // Exchange 1 (read by every CTA of the cluster).
@@ -177,11 +188,20 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
   __shared__ float s_w[kWarps][4];
   __shared__ float s_pv[kWarps][2], s_pz[kWarps][2], s_pq[kWarps][2];
   __shared__ int32_t s_pi[kWarps][2];
-  // !AE: for each thread and each group of kGroup of its vectors (vi = tid + j T, j = g kGroup ...
-  // g kGroup + kGroup - 1), the maximum of U = fl(fl(fma(eta T, q, z)) / T) over their entries;
+  __shared__ int32_t s_cnt[kWarps];  // kRing, pass B: candidate groups per warp (list offsets)
+  // Dynamic shared memory: the pass-A ring (kRing: [kRingA][z, q][kRapidThreads] 16-byte vectors),
+  // then, !AE, for each thread and each group of kGroup of its vectors (vi = tid + j T, j = g kGroup
+  // ... g kGroup + kGroup - 1), the maximum of U = fl(fl(fma(eta T, q, z)) / T) over their entries;
   // entry [g][tid].
-  extern __shared__ __align__(16) float s_umax[];
+  constexpr bool kRing = ALIGNED && !AE;
+  constexpr uint32_t kUmaxOff = kRing ? uint32_t(kRingABytes) : 0u;
+  extern __shared__ __align__(16) float4 s_dyn[];
+  float4* const s_ring = s_dyn;
+  float* const s_umax = reinterpret_cast<float*>(reinterpret_cast<char*>(s_dyn) + kUmaxOff);
 
+  // The draw launch may be scheduled once every CTA of this grid has started (it waits for this
+  // grid's completion before reading anything).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -272,7 +292,7 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
         gmax = fmaxf(gmax, vk);
         if ((it & (kGroup - 1)) == kGroup - 1 || vn >= nvec) {
 #ifdef ASV_CHECKED
-          if (ASV_GUARD(p, uint32_t(((it / kGroup) * kRapidThreads + tid) * 4) < dyn_smem))
+          if (ASV_GUARD(p, kUmaxOff + uint32_t(((it / kGroup) * kRapidThreads + tid) * 4) < dyn_smem))
 #endif
             s_umax[(it / kGroup) * kRapidThreads + tid] = gmax;
           ub_t = fmaxf(ub_t, gmax);
@@ -335,25 +355,53 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
       qacc = fadd2(qacc, make_float2(cq.x, cq.y));
       qacc = fadd2(qacc, make_float2(cq.z, cq.w));
     };
-    float4 cz, cq, nz, nq;
-    if (vi < nvec) {
-      cz = LD4(zsl, vi * VEC, polA, -INFINITY);
-      cq = LD4(qsl, vi * VEC, polA, 0.0f);
-    }
-    // Two vectors per trip, the prefetch alternating between (cz, cq) and (nz, nq) (no register
-    // copies); a prefetched vector is consumed only while it is in range.
-    for (; vi < nvec; vi += 2 * kRapidThreads) {
-      if (vi + kRapidThreads < nvec) {
-        nz = LD4(zsl, (vi + kRapidThreads) * VEC, polA, -INFINITY);
-        nq = LD4(qsl, (vi + kRapidThreads) * VEC, polA, 0.0f);
+    if constexpr (kRing) {
+      // Vector j of the thread (vi = tid + j T) goes to slot j mod kRingA; each thread reads only its
+      // own slots and refills a slot only after the arithmetic has consumed it.
+      auto ring_issue = [&](int j) {
+        const int v = tid + j * kRapidThreads;
+        if (v < nvec) {
+          const int slot = (j & (kRingA - 1)) * 2;
+          if (ASV_GUARD(p, v * VEC + VEC <= len &&
+                               uint32_t(((slot + 1) * kRapidThreads + tid + 1) * 16) <= dyn_smem)) {
+            cp_async16(smem_addr(&s_ring[(slot + 0) * kRapidThreads + tid]), zsl + v * VEC, pol_evict_first);
+            cp_async16(smem_addr(&s_ring[(slot + 1) * kRapidThreads + tid]), qsl + v * VEC, pol_evict_first);
+          }
+        }
+        cp_async_commit();
+      };
+#pragma unroll
+      for (int j = 0; j < kRingA; ++j) ring_issue(j);
+      for (int j = 0; vi < nvec; ++j, vi += kRapidThreads) {
+        cp_async_wait_group<kRingA - 1>();  // the copies of vector j have landed
+        const int slot = (j & (kRingA - 1)) * 2;
+        const float4 cz = s_ring[(slot + 0) * kRapidThreads + tid];
+        const float4 cq = s_ring[(slot + 1) * kRapidThreads + tid];
+        a_body(cz, cq, vi);
+        ring_issue(j + kRingA);
       }
-      a_body(cz, cq, vi);
-      if (vi + kRapidThreads >= nvec) break;
-      if (vi + 2 * kRapidThreads < nvec) {
-        cz = LD4(zsl, (vi + 2 * kRapidThreads) * VEC, polA, -INFINITY);
-        cq = LD4(qsl, (vi + 2 * kRapidThreads) * VEC, polA, 0.0f);
+      cp_async_wait_all();
+    } else {
+      float4 cz, cq, nz, nq;
+      if (vi < nvec) {
+        cz = LD4(zsl, vi * VEC, polA, -INFINITY);
+        cq = LD4(qsl, vi * VEC, polA, 0.0f);
       }
-      a_body(nz, nq, vi + kRapidThreads);
+      // Two vectors per trip, the prefetch alternating between (cz, cq) and (nz, nq) (no register
+      // copies); a prefetched vector is consumed only while it is in range.
+      for (; vi < nvec; vi += 2 * kRapidThreads) {
+        if (vi + kRapidThreads < nvec) {
+          nz = LD4(zsl, (vi + kRapidThreads) * VEC, polA, -INFINITY);
+          nq = LD4(qsl, (vi + kRapidThreads) * VEC, polA, 0.0f);
+        }
+        a_body(cz, cq, vi);
+        if (vi + kRapidThreads >= nvec) break;
+        if (vi + 2 * kRapidThreads < nvec) {
+          cz = LD4(zsl, (vi + 2 * kRapidThreads) * VEC, polA, -INFINITY);
+          cq = LD4(qsl, (vi + 2 * kRapidThreads) * VEC, polA, 0.0f);
+        }
+        a_body(nz, nq, vi + kRapidThreads);
+      }
     }
   }
 
@@ -634,7 +682,66 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
       cq = nq;
     }
   }
-  if (!AE && finite && ub_t >= L + ln_tf) {
+  // kRing: the vector groups whose bound reaches L0 + ln(tail_frac) are listed for the whole CTA
+  // (in the pass-A ring, free now; thread order, then group order: a deterministic list) and the
+  // CTA's threads share them out, so a slice whose candidates crowd into a few threads' groups
+  // costs a few memory round trips per thread rather than one per group on those threads.  The
+  // head sums walk the same list.  (A list that would not fit falls back to each thread's own
+  // groups.)
+  int n_list = -1;  // kRing: entries of the list (-1: not used)
+  if (kRing && finite) {
+    const float thrU = L + ln_tf;  // L = L0 here, the same in every thread
+    const int ng = (nvec - tid + kGroup * kRapidThreads - 1) / (kGroup * kRapidThreads);  // this thread's groups
+    int cnt = 0;
+    if (ub_t >= thrU)
+      for (int g = 0; g < ng; ++g) cnt += (s_umax[g * kRapidThreads + tid] >= thrU) ? 1 : 0;
+    int incl = cnt;  // inclusive scan over the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_cnt[warp] = incl;
+    __syncthreads();
+    int base = 0, total = 0;
+#pragma unroll
+    for (int w2 = 0; w2 < kWarps; ++w2) {
+      const int c = s_cnt[w2];
+      base += (w2 < warp) ? c : 0;
+      total += c;
+    }
+    constexpr int kListCap = kRingABytes / 4;
+    if (total <= kListCap) {
+      int32_t* const s_list = reinterpret_cast<int32_t*>(s_ring);
+      int off = base + incl - cnt;
+      if (cnt > 0)
+        for (int g = 0; g < ng; ++g)
+          if (s_umax[g * kRapidThreads + tid] >= thrU && ASV_GUARD(p, off < kListCap)) s_list[off++] = g * kRapidThreads + tid;
+      n_list = total;
+    }
+    __syncthreads();
+  }
+  if (n_list >= 0) {
+    const float2 nML2 = make_float2(-rc.ML, -rc.ML);
+    const float2 inv2 = make_float2(rc.inv_sum, rc.inv_sum);
+    const int32_t* const s_list = reinterpret_cast<const int32_t*>(s_ring);
+    for (int e = tid; e < n_list; e += kRapidThreads) {
+      const int u = s_list[e];
+      const int g = u / kRapidThreads, t = u - g * kRapidThreads;
+#pragma unroll
+      for (int r = 0; r < kGroup; ++r) {
+        const int vi = (g * kGroup + r) * kRapidThreads + t;
+        if (vi < nvec) {
+          const float4 z4 = LD4C(zsl, vi * VEC, -INFINITY);
+          const float4 q4 = LD4C(qsl, vi * VEC, 0.0f);
+          float2 p0, p1, h0, h1;
+          pzhs2(make_float2(z4.x, z4.y), make_float2(q4.x, q4.y), invT2, nML2, inv2, etaT2, p0, h0);
+          pzhs2(make_float2(z4.z, z4.w), make_float2(q4.z, q4.w), invT2, nML2, inv2, etaT2, p1, h1);
+          L = fmaxf(L, fmaxf(fmaxf(h0.x, h0.y), fmaxf(h1.x, h1.y)));
+        }
+      }
+    }
+  } else if (!AE && finite && ub_t >= L + ln_tf) {
     const float2 nML2 = make_float2(-rc.ML, -rc.ML);
     const float2 inv2 = make_float2(rc.inv_sum, rc.inv_sum);
     const float thrU = L + ln_tf;
@@ -775,26 +882,45 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
   // ---------------------------------------------------------------- head sums
   {
     float hp = 0.0f, he = 0.0f;
-    if (!AE && finite && ub_t >= rc.thr) {
+    // One vector of the slice into the head sums.
+    auto head_vec = [&](int vi) {
+      const float4 z4 = LD4C(zsl, vi * VEC, -INFINITY);
+      const float4 q4 = LD4C(qsl, vi * VEC, 0.0f);
+      const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
+      const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float pk, zh;
+        rapid_p_zhs(zz[e], qq[e], rc, pk, zh);
+        if (zh >= rc.thr) {
+          hp += pk;
+          he += head_exp(zh, rc.zhmax);
+        }
+      }
+    };
+    if (n_list >= 0) {
+      // The head lies in the listed groups whose bound reaches the boundary (re-read, normally
+      // from L1).
+      const int32_t* const s_list = reinterpret_cast<const int32_t*>(s_ring);
+      for (int e = tid; e < n_list; e += kRapidThreads) {
+        const int u = s_list[e];
+        if (s_umax[u] >= rc.thr) {
+          const int g = u / kRapidThreads, t = u - g * kRapidThreads;
+          for (int r = 0; r < kGroup; ++r) {
+            const int vi = (g * kGroup + r) * kRapidThreads + t;
+            if (vi >= nvec) break;
+            head_vec(vi);
+          }
+        }
+      }
+    } else if (!AE && finite && ub_t >= rc.thr) {
       // The head lies in the vectors whose bound reaches the boundary (re-read, normally from L1).
       for (int g = 0; g * kGroup * kRapidThreads + tid < nvec; ++g) {
         if (s_umax[g * kRapidThreads + tid] >= rc.thr) {
           for (int r = 0; r < kGroup; ++r) {
             const int vi = (g * kGroup + r) * kRapidThreads + tid;
             if (vi >= nvec) break;
-            const float4 z4 = LD4C(zsl, vi * VEC, -INFINITY);
-            const float4 q4 = LD4C(qsl, vi * VEC, 0.0f);
-            const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
-            const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float pk, zh;
-              rapid_p_zhs(zz[e], qq[e], rc, pk, zh);
-              if (zh >= rc.thr) {
-                hp += pk;
-                he += head_exp(zh, rc.zhmax);
-              }
-            }
+            head_vec(vi);
           }
         }
       }
@@ -977,6 +1103,9 @@ __global__ void __launch_bounds__(kDrawThreads) rapid_draw_kernel(const RapidArg
   constexpr float kMinOneMinusU = 0x1p-24f;
   __shared__ unsigned long long s_best[kWarps][2];
   __shared__ uint32_t s_last;
+  // Launched as a programmatic dependent of the verification: wait until it has completed and its
+  // writes (jobs, outputs) are visible.  (Without that launch attribute this returns at once.)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -1010,33 +1139,40 @@ __global__ void __launch_bounds__(kDrawThreads) rapid_draw_kernel(const RapidArg
   const bool al = p.bulk != 0;
   const uint64_t pol = policy_evict_first();
   const int iters = (nvec + kDrawThreads - 1) / kDrawThreads;  // uniform over the CTA
-  // Aligned rows: every vector of the thread is copied to shared memory at once (one round trip
-  // to memory instead of one per vector); each thread reads back only its own copies.
-  extern __shared__ float4 s_stage[];  // [iters][z, q][kDrawThreads]
-  if (al) {
-    for (int it = 0; it < iters; ++it) {
-      const int vi = it * kDrawThreads + tid;
+  // Aligned rows: a ring of kDrawStage vectors per thread in shared memory, filled by cp.async
+  // (vector `it` of the thread in slot it mod kDrawStage): the first kDrawStage are requested at
+  // once, and each slot is refilled with the vector kDrawStage further on as soon as the arithmetic
+  // has consumed it, so the copies overlap the arithmetic.  Each thread reads only its own slots.
+  extern __shared__ float4 s_stage[];  // [min(iters, kDrawStage)][z, q][kDrawThreads]
 #ifdef ASV_CHECKED
-      uint32_t dyn_smem = 0;
-      asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_smem));
+  uint32_t dyn_smem = 0;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_smem));
 #endif
-      if (vi < nvec && ASV_GUARD(p, vi * VEC + VEC <= len && uint32_t(((2 * it + 1) * kDrawThreads + tid + 1) * 16) <= dyn_smem)) {
-        cp_async16(smem_addr(&s_stage[(2 * it + 0) * kDrawThreads + tid]), zr + vi * VEC, pol);
-        cp_async16(smem_addr(&s_stage[(2 * it + 1) * kDrawThreads + tid]), qr + vi * VEC, pol);
+  auto stage = [&](int it) {
+    const int vi = it * kDrawThreads + tid;
+    if (al && it < iters && vi < nvec) {
+      const int sl = it % kDrawStage;
+      if (ASV_GUARD(p, vi * VEC + VEC <= len && uint32_t(((2 * sl + 1) * kDrawThreads + tid + 1) * 16) <= dyn_smem)) {
+        cp_async16(smem_addr(&s_stage[(2 * sl + 0) * kDrawThreads + tid]), zr + vi * VEC, pol);
+        cp_async16(smem_addr(&s_stage[(2 * sl + 1) * kDrawThreads + tid]), qr + vi * VEC, pol);
       }
     }
-    cp_async_wait_all();
-  }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int j = 0; j < kDrawStage; ++j) stage(j);
   float key[2] = {INFINITY, INFINITY};  // this thread's best keys and their indices
   int idx[2] = {INT_MAX, INT_MAX};
   float bound[2] = {INFINITY, INFINITY};  // the best keys its warp has seen (pruning bound)
   for (int it = 0; it < iters; ++it) {
+    cp_async_wait_group<kDrawStage - 1>();  // the copies of vector it have landed
     const int vi = it * kDrawThreads + tid;
+    const int sl = it % kDrawStage;
     if (vi < nvec) {
       const int kl = vi * VEC;
       const int kb = v0 + kl;
-      const float4 z4 = al ? s_stage[(2 * it + 0) * kDrawThreads + tid] : ld4(zr, kl, len, false, pol, -INFINITY);
-      const float4 q4 = al ? s_stage[(2 * it + 1) * kDrawThreads + tid] : ld4(qr, kl, len, false, pol, 0.0f);
+      const float4 z4 = al ? s_stage[(2 * sl + 0) * kDrawThreads + tid] : ld4(zr, kl, len, false, pol, -INFINITY);
+      const float4 q4 = al ? s_stage[(2 * sl + 1) * kDrawThreads + tid] : ld4(qr, kl, len, false, pol, 0.0f);
       const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
       const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
       float w[2][4];
@@ -1081,7 +1217,9 @@ __global__ void __launch_bounds__(kDrawThreads) rapid_draw_kernel(const RapidArg
 #pragma unroll
     for (int s = 0; s < 2; ++s)
       bound[s] = __uint_as_float(__reduce_min_sync(0xffffffffu, __float_as_uint(fminf(bound[s], key[s]))));
+    stage(it + kDrawStage);  // slot sl is consumed: refill it
   }
+  cp_async_wait_all();
   unsigned long long best[2];
 #pragma unroll
   for (int s = 0; s < 2; ++s)
@@ -1170,12 +1308,20 @@ bool rapid_needs_all_sums(int tail_mode, float ln_tail_frac) { return tail_mode 
 
 int rapid_draw_smem_bytes(int n_slice, bool aligned) {
   const int iters = (n_slice / 4 + kDrawThreads - 1) / kDrawThreads;
-  return aligned ? iters * 2 * kDrawThreads * 16 : 0;
+  return aligned ? std::min(iters, kDrawStage) * 2 * kDrawThreads * 16 : 0;
 }
 
-int rapid_smem_bytes(bool all_sums, int n_slice) {
+int rapid_draw_ctas_per_sm() { return 4; }  // 48 KB of staging each
+
+int rapid_umax_bytes(bool all_sums, int n_slice) {
   const int iters = (n_slice / 4 + kRapidThreads - 1) / kRapidThreads;
   return all_sums ? 0 : (iters + kGroup - 1) / kGroup * kRapidThreads * 4;
+}
+
+int rapid_ring_bytes() { return kRingABytes; }
+
+int rapid_smem_bytes(bool all_sums, int n_slice, bool aligned) {
+  return ((aligned && !all_sums) ? kRingABytes : 0) + rapid_umax_bytes(all_sums, n_slice);
 }
 
 // Two launches on the stream: the verification (every row), then the draws (draw_ctas CTAs per
@@ -1192,8 +1338,17 @@ cudaError_t launch_rapid(const RapidArgs& a, const LaunchPlan& plan, cudaStream_
   const int smem = rapid_draw_smem_bytes(b.n_slice, a.bulk != 0);
   e = cudaFuncSetAttribute(rapid_draw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  rapid_draw_kernel<<<unsigned(a.B) * unsigned(parts), kDrawThreads, size_t(smem), s>>>(b);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(a.B) * unsigned(parts), 1, 1);
+  cfg.blockDim = dim3(unsigned(kDrawThreads), 1, 1);
+  cfg.dynamicSmemBytes = size_t(smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, rapid_draw_kernel, b);
 }
 
 int rapid_max_active_clusters(const LaunchPlan& plan) {
