@@ -155,13 +155,14 @@ cudaError_t plan_rapid(int V, long long R, bool aligned, bool all_sums, LaunchPl
 
 // CTAs per request of the RAPID draw launch.  The draw reads the B stop rows once, so a second,
 // partial wave of CTAs would nearly double its time: while the batch fits one wave of resident
-// draw CTAs, as many CTAs per request as that wave holds (a CTA streams its slice through a ring of
-// six vectors per thread); larger batches take slices of at most one ring's worth (6144 entries)
-// over several waves.  At least 1024 entries per CTA.
+// draw CTAs, as many CTAs per request as 95 % of that wave holds (a CTA streams its slice through a
+// ring of six vectors per thread; measured, a few SMs hold one draw CTA fewer right after the
+// verification, whose last CTAs the draw's first ones overlap); larger batches take slices of at
+// most one ring's worth (6144 entries) over several waves.  At least 1024 entries per CTA.
 int rapid_draw_ctas(int V, int B) {
   DevInfo di;
   const int sms = dev_info(&di) == cudaSuccess ? di.sms : 1;
-  const long long slots = 1LL * asv::rapid_draw_ctas_per_sm() * sms;
+  const long long slots = 1LL * asv::rapid_draw_ctas_per_sm() * sms * 95 / 100;
   long long want = slots / std::max(B, 1);
   if (want < 1) want = (V + 6143) / 6144;
   return int(std::max(1LL, std::min<long long>(want, std::max(1, V / 1024))));

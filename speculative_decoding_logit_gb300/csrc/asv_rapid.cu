@@ -1164,19 +1164,30 @@ __global__ void __launch_bounds__(kDrawThreads) rapid_draw_kernel(const RapidArg
   float key[2] = {INFINITY, INFINITY};  // this thread's best keys and their indices
   int idx[2] = {INT_MAX, INT_MAX};
   float bound[2] = {INFINITY, INFINITY};  // the best keys its warp has seen (pruning bound)
+  // Keep the better of (k, i) and (key, idx): the smaller key, on equal keys the lower index.
+  auto offer = [&](int s, float k, int i) {
+    if (k < key[s] || (k == key[s] && i < idx[s])) {
+      key[s] = k;
+      idx[s] = i;
+    }
+  };
   for (int it = 0; it < iters; ++it) {
     cp_async_wait_group<kDrawStage - 1>();  // the copies of vector it have landed
     const int vi = it * kDrawThreads + tid;
     const int sl = it % kDrawStage;
+    const int kl = vi * VEC;
+    const int kb = v0 + kl;
+    // K (1 + 2^-20) for the pruning tests below, formed once per vector (w * that product rounds
+    // within the margin's allowance); a zero weight gives 0 or NaN there, and both tests fail on it.
+    float bm[2] = {bound[0] * kMargin, bound[1] * kMargin};
+    float w[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+    uint32_t rw[4] = {0u, 0u, 0u, 0u};
+    bool any = false;
     if (vi < nvec) {
-      const int kl = vi * VEC;
-      const int kb = v0 + kl;
       const float4 z4 = al ? s_stage[(2 * sl + 0) * kDrawThreads + tid] : ld4(zr, kl, len, false, pol, -INFINITY);
       const float4 q4 = al ? s_stage[(2 * sl + 1) * kDrawThreads + tid] : ld4(qr, kl, len, false, pol, 0.0f);
       const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
       const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
-      float w[2][4];
-      bool any = false;
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
         float pk, zhs, prot;
@@ -1185,31 +1196,59 @@ __global__ void __launch_bounds__(kDrawThreads) rapid_draw_kernel(const RapidArg
         w[0][e] = in ? ((n < G) ? fmaxf(fmaxf(pk - prot, pk - qq[e]), 0.0f) : prot) : 0.0f;
         w[1][e] = in ? pk : 0.0f;
 #pragma unroll
-        for (int s = 0; s < 2; ++s) any |= w[s][e] > 0.0f && !(kMinOneMinusU >= w[s][e] * bound[s] * kMargin);
+        for (int s = 0; s < 2; ++s) any |= w[s][e] * bm[s] > kMinOneMinusU;
       }
       if (any) {
         const Philox4 r4 =
             philox4x32_10(uint32_t(kb >> 2), uint32_t(n), uint32_t(req), stream + 4u * p.offset, p.seed_lo, p.seed_hi);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          const float u = uniform_from_word(r4.v[e]);
-          const float lo = 1.0f - u;  // exact
-          bool cand[2];
+        for (int e = 0; e < VEC; ++e) rw[e] = r4.v[e];
+      }
+    }
+    if (it == 0) {
+      // Before any key is known every entry would take the logarithm and the division: seed the
+      // warp's bounds with the keys of each thread's largest weight of its first vector (a key
+      // some entry reaches, so a valid bound), then test the rest against them.
+      float ks[2] = {INFINITY, INFINITY};
+      if (any) {
 #pragma unroll
-          for (int s = 0; s < 2; ++s) cand[s] = w[s][e] > 0.0f && !(lo >= w[s][e] * bound[s] * kMargin);
-          if (cand[0] || cand[1]) {
-            const float E = -logf(u);
+        for (int s = 0; s < 2; ++s) {
+          float wb = w[s][0];  // (selects over the unrolled entries: no indexed local array)
+          uint32_t rb = rw[0];
+          int eb = 0;
 #pragma unroll
-            for (int s = 0; s < 2; ++s) {
-              if (cand[s]) {
-                const float k = E / w[s][e];
-                if (k < key[s]) {  // entries arrive in increasing index: ties keep the earlier one
-                  key[s] = k;
-                  idx[s] = kb + e;
-                }
-              }
+          for (int e = 1; e < VEC; ++e) {
+            if (w[s][e] > wb) {
+              wb = w[s][e];
+              rb = rw[e];
+              eb = e;
             }
           }
+          if (wb > 0.0f) {
+            ks[s] = -logf(uniform_from_word(rb)) / wb;
+            offer(s, ks[s], kb + eb);
+          }
+        }
+      }
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        bound[s] = __uint_as_float(__reduce_min_sync(0xffffffffu, __float_as_uint(fminf(bound[s], ks[s]))));
+        bm[s] = bound[s] * kMargin;
+      }
+    }
+    if (any) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        const float u = uniform_from_word(rw[e]);
+        const float lo = 1.0f - u;  // exact
+        bool cand[2];
+#pragma unroll
+        for (int s = 0; s < 2; ++s) cand[s] = lo < w[s][e] * bm[s];
+        if (cand[0] || cand[1]) {
+          const float E = -logf(u);
+#pragma unroll
+          for (int s = 0; s < 2; ++s)
+            if (cand[s]) offer(s, E / w[s][e], kb + e);
         }
       }
     }
