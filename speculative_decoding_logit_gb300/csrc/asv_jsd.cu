@@ -272,10 +272,12 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
   // through a ring of kRing vectors per input per thread in shared memory, filled by 16-byte
   // cp.async copies (no registers held by copies in flight); each thread reads only its own slots
   // and refills a slot only after the arithmetic has consumed it.  The first kRing slots are filled
-  // now, so that their reads overlap the row's exchange.
+  // now, so that their reads overlap the row's exchange.  A thread takes its vectors in the reverse
+  // of pass A's order: those pass A read last are the likeliest to be still in L2.
+  const int jn = nvec > tid ? (nvec - tid + kJsdThreads - 1) / kJsdThreads : 0;  // this thread's vectors
   auto ring_issue = [&](int j) {
-    const int vi = tid + j * kJsdThreads;
-    if (vi < nvec) {
+    const int vi = tid + (jn - 1 - j) * kJsdThreads;
+    if (j < jn) {
 #pragma unroll
       for (int m = 0; m < NPB; ++m) {
         const int slot = ((j & (kRing - 1)) * NPB + m) * kJsdThreads + tid;
@@ -512,7 +514,7 @@ __global__ void __launch_bounds__(kJsdThreads, kJsdCtasPerSm) jsd_family_kernel(
     constexpr bool kPairShort = MODE == kModeAsym;
     if (finite && ALIGNED) {
       // (the ring's first kRing slots were filled before the exchange)
-      for (int j = 0; tid + j * kJsdThreads < nvec; ++j) {
+      for (int j = 0; j < jn; ++j) {
         cp_async_wait_group<kRing - 1>();  // the copies of vector j have landed
         const int slot = (j & (kRing - 1)) * NPB;
         if (!ASV_GUARD(p, (slot + NPB - 1) * kJsdThreads + tid < kRing * NPB * kJsdThreads)) continue;
