@@ -43,6 +43,9 @@ N_SETS = 4  # rotating input copies: 4 x 175 MB, larger than the 129 MB L2
 # The timed kernel's sources; its ncu summary under profiles/ records a hash of them (SHA-256 of the
 # files' bytes concatenated in this order, first 16 hex digits).
 KERNEL_SOURCES = ("asv_jsd.cu", "asv_jsd_common.cuh", "asv_device.cuh", "jsd_poly.inc", "asv_internal.h")
+# The sources each profiled kernel is built from (the hash a committed ncu summary records).
+KERNEL_SOURCES_OF = {"jsd_family": KERNEL_SOURCES,
+                     "rapid_kernel": ("asv_rapid.cu", "asv_device.cuh", "asv_internal.h")}
 
 
 def _peaks():
@@ -53,11 +56,11 @@ def _peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str = "jsd_family") -> str:
     import hashlib
     csrc = os.path.join(ROOT, "speculative_decoding_logit_gb300", "csrc")
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES_OF[kernel]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -70,8 +73,8 @@ def _profiled_traffic(workload: str = WORKLOAD, kernel: str = "jsd_family"):
     prof = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         text = open(prof).read()
-        h = kernel_source_hash()
-    except OSError:
+        h = kernel_source_hash(kernel)
+    except (OSError, KeyError):
         return None
     m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
     m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)

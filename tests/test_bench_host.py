@@ -27,6 +27,14 @@ def test_hash_covers_every_source_of_the_timed_kernel():
     assert len(bench.kernel_source_hash()) == 16
 
 
+def test_rapid_hash_covers_its_sources():
+    seen = set()
+    _local_includes("asv_rapid.cu", seen)
+    srcs = set(bench.KERNEL_SOURCES_OF["rapid_kernel"])
+    assert seen <= srcs, sorted(seen - srcs)
+    assert bench.kernel_source_hash("rapid_kernel") != bench.kernel_source_hash("jsd_family")
+
+
 def test_profile_records_hash_and_traffic():
     with open(os.path.join(bench.ROOT, "profiles", f"jsd_family_{bench.WORKLOAD}.md")) as f:
         text = f.read()
