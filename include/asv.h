@@ -265,6 +265,12 @@ asv_status asymspec_verify_static(const void* a, const void* b, const void* t, i
  * 0 = accept test (word 0), 1 = residual draw (word k), 2 = bonus draw (word k).
  * T > 0, eta >= 0, 0 <= tail_frac < 1, all finite.
  * Outputs: out_accept_len [B], out_tokens [B, G+1], out_req_status [B].
+ * Launches: two kernels on `stream`, the verification and then the draw; the draw
+ * is a programmatic dependent launch of the verification (it may be scheduled
+ * while the verification's last CTAs run and waits for the verification to
+ * complete before it reads anything), so work the caller enqueues on `stream`
+ * after this call runs after both, as in plain stream order; inside stream
+ * capture the pair becomes two graph nodes joined by a programmatic edge.
  */
 asv_status rapid_verify(const float* z, const float* q, const int32_t* draft_ids, int B, int G, int V, float T,
                         float eta, float tail_frac, uint64_t seed, uint32_t offset, int32_t* out_accept_len,
