@@ -110,7 +110,13 @@ cudaError_t plan_jsd(int elem_bytes, int V, long long R, bool aligned, LaunchPla
   cudaError_t e = dev_info(&di);
   if (e != cudaSuccess) return e;
   const int vec = 16 / elem_bytes;
-  const int C = wave_fill_cluster(V, R, asv::jsd_ctas_per_sm(), di.sms);
+  int C = wave_fill_cluster(V, R, asv::jsd_ctas_per_sm(), di.sms);
+  // fp32 rows carry half the arithmetic per byte of bf16 ones, so the pass-B re-reads that L2 misses
+  // weigh more: slices of at most 512 KB of the three inputs keep more of each CTA's pair in L2
+  // (measured on 1280 fp32 rows of V = 151936: 0.507 ms at C = 4 against 0.519 ms at C = 3; bf16
+  // batches measured best at the wave-filling choice).
+  if (elem_bytes == 4 && g_tune_cluster.load() <= 0)
+    while (C < asv::kMaxCluster && V / (C + 1) >= 1024 && 3LL * elem_bytes * ceil_div(V, C) > 512LL * 1024) ++C;
   out->cluster = C;
   out->threads = asv::jsd_threads();
   out->n_slice = int(round_up(size_t(ceil_div(V, C)), size_t(vec)));
