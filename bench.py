@@ -265,6 +265,55 @@ def _timed_reps(step, steps, min_region_s, stream, dist=None):
     return [first] + [rep() for _ in range(n - 1)]
 
 
+def _graph_of(step, steps, warm=2):
+    """The K-step loop captured once into a CUDA graph on a side stream (a few eager calls on that
+    stream first, so per-stream state such as the binding's workspace exists before the capture)."""
+    import torch
+
+    gs = torch.cuda.Stream()
+    gs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(gs):
+        for i in range(warm):
+            step(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=gs):
+        for i in range(steps):
+            step(i)
+    torch.cuda.synchronize()
+    g.replay()  # untimed
+    torch.cuda.synchronize()
+    return g
+
+
+def _timed_graph_reps(g, min_region_s, dist=None):
+    """Replays of a captured K-step graph between two CUDA events on the replaying stream, bracketed by
+    a barrier and a synchronize, repeated as _timed_reps does.  Returns per-replay device times (ms)."""
+    import torch
+
+    from speculative_decoding_logit_gb300.shard import max_over_ranks
+
+    stream = torch.cuda.current_stream()
+
+    def rep():
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        return e0.elapsed_time(e1)
+
+    first = rep()
+    n = max(1, int(np.ceil(min_region_s * 1e3 / max(first, 1e-3))))
+    n = int(max_over_ranks(n))
+    return [first] + [rep() for _ in range(n - 1)]
+
+
 def _gpu_id(dev):
     import torch
     try:
@@ -306,16 +355,24 @@ def run_ours(args):
                         device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    # Pre-marshalled argument lists: the timed loop is one ctypes call per step.
-    calls = []
-    for (a, b, t) in sets:
-        calls.append((a.data_ptr(), b.data_ptr(), t.data_ptr(), asv.ASV_BF16, d.data_ptr(), w.B, w.K, w.V,
-                      BETA, GAMMA, out.accept_len.data_ptr(), out.tokens.data_ptr(), out.D.data_ptr(),
-                      out.lse.data_ptr(), out.req_status.data_ptr(), wsbuf.data_ptr(), wsbuf.numel(), sh))
     fn = lib.asymspec_verify
+
+    # Pre-marshalled argument lists (the stream handle included): one ctypes call per step.
+    def marshalled(stream_handle):
+        return [(a.data_ptr(), b.data_ptr(), t.data_ptr(), asv.ASV_BF16, d.data_ptr(), w.B, w.K, w.V,
+                 BETA, GAMMA, out.accept_len.data_ptr(), out.tokens.data_ptr(), out.D.data_ptr(),
+                 out.lse.data_ptr(), out.req_status.data_ptr(), wsbuf.data_ptr(), wsbuf.numel(), stream_handle)
+                for (a, b, t) in sets]
+
+    calls = marshalled(sh)
 
     def step(i):
         st = fn(*calls[i % N_SETS])
+        if st != 0:
+            raise RuntimeError(f"asymspec_verify failed: {st}")
+
+    def step_on_current(i):
+        st = fn(*marshalled(torch.cuda.current_stream(dev).cuda_stream)[i % N_SETS])
         if st != 0:
             raise RuntimeError(f"asymspec_verify failed: {st}")
 
@@ -323,14 +380,18 @@ def run_ours(args):
         step(i)
     torch.cuda.synchronize()
 
-    # Each repetition: the K launches back to back between two events on the launching stream (no
-    # events between them, which would add their own gaps); the kernel's average launch duration is
-    # that region over K, gaps between launches included.
+    # The timed region: the K calls captured once into a CUDA graph (as a serving loop issues them),
+    # each repetition one replay between two events on the replaying stream; the kernel's average
+    # launch duration is that region over K, the gaps between the graph's kernels included.  The
+    # same K calls launched one by one from the host (eager) are timed too and reported beside it.
     clocks = ClockSampler(_gpu_id(dev))
     clocks.start()
     time.sleep(0.3)  # let the sampler start
-    reps = _timed_reps(step, args.steps, args.min_region_s, stream, dist)
+    graph = _graph_of(step_on_current, args.steps)
+    reps = _timed_graph_reps(graph, args.min_region_s, dist)
+    eager_reps = _timed_reps(step, args.steps, min(0.25, args.min_region_s), stream, dist)
     clk = clocks.stop()
+    del graph
     rep_ms = float(np.median(reps))
     elapsed_ms = max_over_ranks(rep_ms)
     launch_ms = rep_ms / args.steps
@@ -376,8 +437,8 @@ def run_ours(args):
     roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "peak_kind": peak_kind,
             "frac_of_8tbs": achieved / 8000.0, "kernel_ms": launch_ms,
-            "kernel_ms_from": "median repetition of K back-to-back launches / K (CUDA events on the launching "
-                              "stream)",
+            "kernel_ms_from": "median replay of the K calls captured in one CUDA graph / K (CUDA events on the "
+                              "replaying stream)",
             "algorithmic_bytes_per_launch": in_bytes}
     secondary = None
     if ws == 1 and not args.no_secondary:
@@ -400,6 +461,8 @@ def run_ours(args):
                            "rows_per_step": R, "parallelism": f"replicas x{ws} (requests sharded, no collective)",
                            "l2": f"{N_SETS} rotating input sets of {in_bytes / 1e6:.0f} MB (> 129 MB L2)",
                            "timed_reps": len(reps), "rep_ms_min_median_max": [min(reps), rep_ms, max(reps)],
+                           "launch": "the K calls captured once into a CUDA graph and replayed",
+                           "eager_ms_per_step": float(np.median(eager_reps)) / args.steps,
                            "plan": plan},
                 "roofline": roof, "cpu_baseline": cpu, "cpu_baseline_all_cores": cpu_par, "e2e": e2e,
                 "gpu_launches": args.steps * len(reps), "clocks": clk, "secondary": secondary}
@@ -500,8 +563,11 @@ def workload_line(name, args, dev, steps=None):
     clocks = ClockSampler(_gpu_id(dev))
     clocks.start()
     time.sleep(0.3)
-    reps = _timed_reps(call, n_steps, args.min_region_s, stream)
+    graph = _graph_of(call, n_steps)
+    reps = _timed_graph_reps(graph, args.min_region_s)
+    eager_reps = _timed_reps(call, n_steps, min(0.25, args.min_region_s), stream)
     clk = clocks.stop()
+    del graph
     rep_ms = float(np.median(reps))
     launch_ms = rep_ms / n_steps
     peaks, peak_kind = _peaks()
@@ -511,7 +577,9 @@ def workload_line(name, args, dev, steps=None):
             "unit": "rows/s", "n_gpus": 1, "steps": n_steps, "ms_per_step": launch_ms, "higher_is_better": True,
             "dtype": dtype, "data": "synthetic",
             "config": dict({"workload": name, "B": w.B, "K": w.K, "V": w.V, "rows_per_step": R, "kernel": kernel,
-                            "timed_reps": len(reps), "rep_ms_min_median_max": [min(reps), rep_ms, max(reps)]},
+                            "timed_reps": len(reps), "rep_ms_min_median_max": [min(reps), rep_ms, max(reps)],
+                            "launch": "the calls captured once into a CUDA graph and replayed",
+                            "eager_ms_per_step": float(np.median(eager_reps)) / n_steps},
                            **extra),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"], "frac_of_8tbs": achieved / 8000.0,
