@@ -193,7 +193,7 @@ def test_sci_sweep_fused_checked(clib, kernel, dtype, V):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("V", [2, 17, 1001, 4099])
+@pytest.mark.parametrize("V", [2, 17, 1001, 4099, 4096])
 def test_rapid_checked_every_cluster_size(clib, V):
     for G in (1, 3, 5):
         batch = gen.make_rapid_batch(300 + V + G, 3, G, V)

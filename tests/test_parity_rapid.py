@@ -58,6 +58,35 @@ def test_small_shapes(asv, V, G):
         assert g >= 14
 
 
+@pytest.mark.parametrize("B,G,V", [(1, 0, 4096), (3, 2, 4096), (37, 5, 4096), (16, 10, 8192), (64, 1, 32000)])
+def test_one_cta_per_row(asv, B, G, V):
+    """One CTA per row (the plan of the 32 x 11 x 128256 workload) on aligned rows under the default
+    tail reading, forced by the tuning override at smaller shapes, from a single request and no drafts
+    up: graded against the oracle; repeated calls give the same outputs and the workspace is left
+    zeroed."""
+    b = gen.make_rapid_batch(700 + B + G + V, B, G, V)
+    ws = torch.zeros(asv.workspace_bytes(asv.ASV_MODE_RAPID, B, G, V, asv.ASV_F32), dtype=torch.uint8,
+                     device="cuda")
+    z, q, d = (torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (b.z, b.q, b.drafts))
+    asv.set_tuning(1)
+    try:
+        for eta in (0.0, 10.0):
+            outs = []
+            for _ in range(2):
+                o = asv.rapid_verify(z, q, d, 1.0, eta, 0.1, 555, workspace=ws)
+                torch.cuda.synchronize()
+                outs.append(o)
+                assert not ws.any(), "the workspace is left zeroed"
+            ref = oracle.rapid_verify(b.z, b.q, b.drafts, 1.0, eta, 0.1, 555)
+            g, f = _compare(outs[0], ref)
+            assert g >= max(1, B - 2)
+            for x, y in zip((outs[0].accept_len, outs[0].tokens, outs[0].req_status),
+                            (outs[1].accept_len, outs[1].tokens, outs[1].req_status)):
+                assert torch.equal(x, y)
+    finally:
+        asv.set_tuning(0)
+
+
 def test_temperature_and_offset(asv):
     b = gen.make_rapid_batch(8, 24, 4, 3000)
     for T, off in ((0.7, 0), (1.5, 3), (1.0, 17)):
