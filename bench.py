@@ -595,7 +595,11 @@ def run_workload(args):
     dev = torch.device("cuda", 0)
     import speculative_decoding_logit_gb300 as asv
     asv.build()
+    if args.cluster:
+        asv.set_tuning(args.cluster)
     line = workload_line(args.workload, args, dev, steps=args.steps)
+    if args.cluster:
+        line["config"]["cluster_override"] = args.cluster
     line["warmup"] = args.warmup
     print(json.dumps(line), flush=True)
     return 0
@@ -616,6 +620,9 @@ def main():
     ap.add_argument("--no-secondary", action="store_true", help="skip the other workloads' lines")
     ap.add_argument("--requests", type=int, default=0,
                     help="with --workload: verify only this many requests (small cases for ncu captures)")
+    ap.add_argument("--cluster", type=int, default=0,
+                    help="with --workload: CTAs per row (the library's tuning override; profiling captures of a "
+                         "reduced batch in the full batch's plan)")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(set(gen.WORKLOADS) | set(_MODES)),
                     help="another workload (device-timed line only; the default is the headline workload)")
     args = ap.parse_args()
