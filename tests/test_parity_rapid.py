@@ -109,6 +109,16 @@ def test_rapid_b32_g10_v128256_full(asv):
     assert tot >= 4 * 30
 
 
+def test_draw_slices_longer_than_the_ring(asv):
+    """64 requests at V = 128256: the draw launch takes 9 CTAs per request, whose slices (3563 vectors)
+    stream through each thread's six-slot ring in 14 trips, refilling every slot."""
+    b = gen.make_rapid_batch(77, 64, 2, 128256)
+    out = _run(asv, b.z, b.q, b.drafts, 1.0, 10.0, 0.1, 2024)
+    ref = oracle.rapid_verify(b.z, b.q, b.drafts, 1.0, 10.0, 0.1, 2024)
+    g, f = _compare(out, ref)
+    assert g >= 60
+
+
 @pytest.mark.parametrize("eta", [40.0, 50.0])
 def test_upward_speculation_eta(asv, eta):
     """The page's upward-speculation setting (a larger drafter guiding a smaller target): eta 40, 50."""
