@@ -1092,15 +1092,13 @@ __global__ void __launch_bounds__(kRapidThreads, kRapidCtasPerSm) rapid_kernel(c
 // decides only if every residual weight is zero.  Pruning keeps the result exact: E_k > 1 - u_k
 // (1 - u_k exact, at least 2^-24), so an entry with (1 - u_k) >= w_k K (1 + 2^-20), K the best key
 // its warp has seen, has a key (as computed: logf, one division) above K and cannot win; the
-// logarithm and the division are skipped for it, and Philox for a vector where even 1 - u = 2^-24
-// cannot win.  A CTA's winners go into the job's slots with one 64-bit atomic max each (key bits
-// above the index, inverted, so the smaller key and then the lower index win); the last CTA of the
-// request writes the token and clears the job.
+// logarithm and the division are skipped for it.  A CTA's winners go into the job's slots with one
+// 64-bit atomic max each (key bits above the index, inverted, so the smaller key and then the lower
+// index win); the last CTA of the request writes the token and clears the job.
 __global__ void __launch_bounds__(kDrawThreads) rapid_draw_kernel(const RapidArgs p) {
   constexpr int VEC = 4;
   constexpr int kWarps = kDrawThreads / 32;
   constexpr float kMargin = 1.0f + 0x1p-20f;
-  constexpr float kMinOneMinusU = 0x1p-24f;
   __shared__ unsigned long long s_best[kWarps][2];
   __shared__ uint32_t s_last;
   // Launched as a programmatic dependent of the verification: wait until it has completed and its
@@ -1124,6 +1122,7 @@ __global__ void __launch_bounds__(kDrawThreads) rapid_draw_kernel(const RapidArg
   const int len = max(0, min(V - v0, p.n_slice));
   const int nvec = (len + VEC - 1) / VEC;
   const uint32_t stream = (n < G) ? 1u : 2u;
+  const bool resid = n < G;  // the residual race (else the bonus: the protected target)
   RowConsts dc;
   dc.invT = p.inv_T;
   dc.etaT = p.eta * p.T;
@@ -1182,28 +1181,31 @@ __global__ void __launch_bounds__(kDrawThreads) rapid_draw_kernel(const RapidArg
     float bm[2] = {bound[0] * kMargin, bound[1] * kMargin};
     float w[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
     uint32_t rw[4] = {0u, 0u, 0u, 0u};
-    bool any = false;
-    if (vi < nvec) {
+    // Every vector in range takes its Philox block: the p-weighted race keeps nearly every vector
+    // above the pruning threshold, so a test that could skip it would cost more than it saves.
+    const bool any = vi < nvec;
+    if (any) {
       const float4 z4 = al ? s_stage[(2 * sl + 0) * kDrawThreads + tid] : ld4(zr, kl, len, false, pol, -INFINITY);
       const float4 q4 = al ? s_stage[(2 * sl + 1) * kDrawThreads + tid] : ld4(qr, kl, len, false, pol, 0.0f);
       const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
       const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+      const bool full = kl + VEC <= len;  // (always, on aligned rows)
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
-        float pk, zhs, prot;
-        rapid_entry(zz[e], qq[e], dc, pk, zhs, prot);
-        const bool in = kl + e < len;
-        w[0][e] = in ? ((n < G) ? fmaxf(fmaxf(pk - prot, pk - qq[e]), 0.0f) : prot) : 0.0f;
+        // p, zhat/T and the protected target as rapid_entry forms them; the head term (an exp2) only
+        // for the few head entries.
+        float pk, zhs;
+        rapid_p_zhs(zz[e], qq[e], dc, pk, zhs);
+        float prot = __fmul_rn(pk, dc.tail_scale);
+        if (!(zhs < dc.thr)) prot = __fmul_rn(head_exp(zhs, dc.zhmax), dc.head_scale);
+        const bool in = full || kl + e < len;
+        w[0][e] = in ? (resid ? fmaxf(fmaxf(pk - prot, pk - qq[e]), 0.0f) : prot) : 0.0f;
         w[1][e] = in ? pk : 0.0f;
-#pragma unroll
-        for (int s = 0; s < 2; ++s) any |= w[s][e] * bm[s] > kMinOneMinusU;
       }
-      if (any) {
-        const Philox4 r4 =
-            philox4x32_10(uint32_t(kb >> 2), uint32_t(n), uint32_t(req), stream + 4u * p.offset, p.seed_lo, p.seed_hi);
+      const Philox4 r4 =
+          philox4x32_10(uint32_t(kb >> 2), uint32_t(n), uint32_t(req), stream + 4u * p.offset, p.seed_lo, p.seed_hi);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) rw[e] = r4.v[e];
-      }
+      for (int e = 0; e < VEC; ++e) rw[e] = r4.v[e];
     }
     if (it == 0) {
       // Before any key is known every entry would take the logarithm and the division: seed the
