@@ -91,3 +91,67 @@ def test_asymspec_replay_matches_direct_calls(asv):
         torch.cuda.synchronize()
         _same(got, (ref.accept_len, ref.tokens, ref.D, ref.lse, ref.req_status))
     assert not ws.any(), "the workspace is left zeroed"
+
+
+def _capture_returning(call):
+    """As _capture, returning the captured call's outputs too (allocated from the graph's pool)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        out = call()
+    torch.cuda.synchronize()
+    return g, out
+
+
+def test_sweep_replay_matches_direct_calls(asv):
+    B, K, V = 6, 4, 4096
+    b1 = gen.make_asymspec_batch("spiky", 41, B, K, V, gen.F32, identical_frac=0.3, processes=0)
+    b2 = gen.make_asymspec_batch("spiky", 42, B, K, V, gen.F32, identical_frac=0.3, processes=0)
+    a, b, t = (torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (b1.a, b1.b, b1.t))
+    d = torch.from_numpy(b1.drafts).cuda()
+    betas, gammas = [0.0, 1.0, 1.5, 2.0], [0.4, 0.5, 0.7, 1.0]
+    ws = torch.zeros(asv.workspace_bytes(asv.ASV_MODE_SWEEP, B, K, V, asv.ASV_F32), dtype=torch.uint8, device="cuda")
+    g, out = _capture_returning(lambda: asv.asymspec_verify_sweep(a, b, t, d, betas, gammas, workspace=ws))
+    for batch in (b1, b2):
+        for dst, src in ((a, batch.a), (b, batch.b), (t, batch.t)):
+            dst.copy_(torch.from_numpy(np.ascontiguousarray(src)))
+        d.copy_(torch.from_numpy(batch.drafts))
+        g.replay()
+        torch.cuda.synchronize()
+        got = tuple(x.clone() for x in (out.accept_len, out.tokens, out.D, out.lse, out.req_status))
+        ref = asv.asymspec_verify_sweep(a.clone(), b.clone(), t.clone(), d.clone(), betas, gammas)
+        torch.cuda.synchronize()
+        _same(got, (ref.accept_len, ref.tokens, ref.D, ref.lse, ref.req_status))
+    assert not ws.any(), "the workspace is left zeroed"
+
+
+def test_sci_replay_carries_the_credit_state(asv):
+    """Three E2-SCI windows replayed from one capture: r_hat, updated in place on the device by each
+    window, follows the same values as three direct calls."""
+    B, K, V = 8, 4, 4096
+    wins = [gen.make_asymspec_batch("spiky", 61 + w, B, K, V, gen.BF16, processes=0) for w in range(3)]
+    todev = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).cuda()
+    dr, tg = todev(wins[0].a), todev(wins[0].t)
+    d = torch.from_numpy(wins[0].drafts).cuda()
+    r = torch.full((B,), 0.6, dtype=torch.float64, device="cuda")
+    ws = torch.zeros(asv.workspace_bytes(asv.ASV_MODE_SCI, B, K, V, asv.ASV_BF16), dtype=torch.uint8, device="cuda")
+    g, out = _capture_returning(lambda: asv.sci_verify(dr, tg, d, r, workspace=ws))
+    r.fill_(0.6)  # (the warm-up call advanced it)
+    r_ref = torch.full((B,), 0.6, dtype=torch.float64, device="cuda")
+    for win in wins:
+        dr.copy_(todev(win.a))
+        tg.copy_(todev(win.t))
+        d.copy_(torch.from_numpy(win.drafts))
+        g.replay()
+        torch.cuda.synchronize()
+        got = tuple(x.clone() for x in (out.accept_len, out.tokens, out.jsd, out.T, out.req_status))
+        ref = asv.sci_verify(dr.clone(), tg.clone(), d.clone(), r_ref)
+        torch.cuda.synchronize()
+        _same(got, (ref.accept_len, ref.tokens, ref.jsd, ref.T, ref.req_status))
+        assert torch.equal(r, r_ref)
+    assert not ws.any(), "the workspace is left zeroed"
