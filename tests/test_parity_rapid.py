@@ -109,6 +109,32 @@ def test_rapid_b32_g10_v128256_full(asv):
     assert tot >= 4 * 30
 
 
+def test_candidate_list_overflow_falls_back(asv):
+    """Nearly flat target logits over V = 262144 with one CTA per row (the tuning override): every
+    vector group of a slice reaches the head bound, more groups (16384) than the shared-memory
+    candidate list holds (8192), so pass B and the head sums take each thread's own groups -- graded
+    against the oracle."""
+    rng = np.random.default_rng(4242)
+    B, G, V = 2, 1, 262144
+    z = rng.normal(0.0, 0.02, size=(B, G + 1, V)).astype(np.float32)
+    q = np.empty_like(z)
+    for r in range(B):
+        for i in range(G + 1):
+            x = z[r, i].astype(np.float64) + rng.normal(0.0, 0.05, size=V)
+            e = np.exp(x - x.max())
+            q[r, i] = (e / e.sum()).astype(np.float32)
+    qd = q[:, :G].astype(np.float64)
+    d = np.array([[rng.choice(V, p=qd[r, i] / qd[r, i].sum()) for i in range(G)] for r in range(B)], np.int32)
+    asv.set_tuning(1)
+    try:
+        out = _run(asv, z, q, d, 1.0, 10.0, 0.1, 99)
+    finally:
+        asv.set_tuning(0)
+    ref = oracle.rapid_verify(z, q, d, 1.0, 10.0, 0.1, 99)
+    g, f = _compare(out, ref)
+    assert g + f == B
+
+
 def test_draw_slices_longer_than_the_ring(asv):
     """64 requests at V = 128256: the draw launch takes 9 CTAs per request, whose slices (3563 vectors)
     stream through each thread's six-slot ring in 14 trips, refilling every slot."""
